@@ -1,0 +1,190 @@
+"""Seeded synthetic workloads for the Gemma 3 attention-block forward pass.
+
+This module only *draws numbers*: shapes, seeds and value distributions of the
+five synthetic workloads, and the random tensors that both the CUDA path and
+the fp64 oracle consume.  It holds none of the method's arithmetic (no norm,
+rotation, mask or softmax); the per-layer routing of the 6-layer stack is left
+to the callers (the C-ABI routing helper on the GPU side, the oracle's own
+routing on the checking side).
+
+Every tensor is generated on the CPU from a torch.Generator seeded per
+(tensor seed, row block), so a checker can regenerate any block of rows of a
+multi-GB activation without drawing the rest.  Values are sampled in fp32 and
+rounded to bf16 with round-to-nearest-even (torch's ``.to(torch.bfloat16)``).
+
+Distribution notation: "N(0, 1/D)" and "gamma ~ N(0, 0.1)" read the second
+argument as a variance (weight std D**-0.5, gamma std 0.1**0.5).
+"""
+from __future__ import annotations
+
+import math
+from concurrent.futures import ThreadPoolExecutor
+from dataclasses import dataclass, field
+
+import torch
+
+ROW_BLOCK = 1024          # rows of x per independently seeded block
+
+# Seeds of the individual input tensors (per layer: + 100 * layer).
+SEED_X, SEED_WQ, SEED_WKV, SEED_WO, SEED_GQ, SEED_GK, SEED_PAD = 1, 2, 3, 4, 5, 6, 7
+SEED_GPRE, SEED_GPOST = 8, 9
+
+
+@dataclass(frozen=True)
+class Workload:
+    """Shape and input recipe of one synthetic workload."""
+    name: str
+    B: int
+    T: int
+    D: int
+    H: int
+    H_kv: int
+    d_h: int
+    attn_type: str            # "local" | "global" | "stack" (routed per layer)
+    window: int               # local window W (0 for a global layer)
+    rope_base: float
+    rope_scale: float
+    query_scale: float
+    model_size: str           # Gemma 3 size the shape follows
+    pad: tuple = ("none",)    # ("none",) | ("pad_uniform", lo, hi) | ("valid_uniform", lo, hi)
+    num_layers: int = 1
+    description: str = field(default="", compare=False)
+
+    @property
+    def M(self) -> int:
+        return self.B * self.T
+
+    @property
+    def G(self) -> int:
+        return self.H // self.H_kv
+
+
+WORKLOADS = {
+    "tiny_local": Workload(
+        "tiny_local", B=1, T=1024, D=1152, H=4, H_kv=1, d_h=256, attn_type="local",
+        window=512, rope_base=1e4, rope_scale=1.0, query_scale=256 ** -0.5, model_size="1B",
+        description="tiny local MQA layer: B1 T1024 D1152 H4/1 d256 W512"),
+    "1b_global": Workload(
+        "1b_global", B=4, T=8192, D=1152, H=4, H_kv=1, d_h=256, attn_type="global",
+        window=0, rope_base=1e6, rope_scale=1.0, query_scale=256 ** -0.5, model_size="1B",
+        pad=("pad_uniform", 0, 1024),
+        description="1B-shaped global MQA layer: B4 T8192 D1152 H4/1 d256, pads U{0..1024}"),
+    "4b_local": Workload(
+        "4b_local", B=2, T=32768, D=2560, H=8, H_kv=4, d_h=256, attn_type="local",
+        window=1024, rope_base=1e4, rope_scale=1.0, query_scale=256 ** -0.5, model_size="4B",
+        description="4B-shaped local GQA layer: B2 T32768 D2560 H8/4 d256 W1024"),
+    "27b_global": Workload(
+        "27b_global", B=1, T=131072, D=5376, H=32, H_kv=16, d_h=128, attn_type="global",
+        window=0, rope_base=1e6, rope_scale=8.0, query_scale=168 ** -0.5, model_size="27B",
+        description="27B-shaped long-context global GQA layer: B1 T131072 D5376 H32/16 d128"),
+    "12b_stack": Workload(
+        "12b_stack", B=8, T=16384, D=3840, H=16, H_kv=8, d_h=256, attn_type="stack",
+        window=1024, rope_base=0.0, rope_scale=0.0, query_scale=256 ** -0.5, model_size="12B",
+        pad=("valid_uniform", 2048, 16384), num_layers=6,
+        description="12B-shaped 6-layer routed attention stack: B8 T16384 D3840 H16/8 d256"),
+}
+
+ORDER = ["tiny_local", "1b_global", "4b_local", "27b_global", "12b_stack"]
+
+
+def small(w: Workload, **kw) -> Workload:
+    """A copy of ``w`` with some fields replaced (for reduced-size test cases)."""
+    d = dict(w.__dict__)
+    d.update(kw)
+    return Workload(**d)
+
+
+# ----------------------------------------------------------------------------
+# random draws
+# ----------------------------------------------------------------------------
+def _gen(seed: int, block: int = 0) -> torch.Generator:
+    return torch.Generator().manual_seed((seed << 24) + block)
+
+
+def _normal_bf16(shape, std: float, seed: int, block: int = 0) -> torch.Tensor:
+    g = _gen(seed, block)
+    t = torch.randn(shape, generator=g, dtype=torch.float32)
+    if std != 1.0:
+        t.mul_(std)
+    return t.to(torch.bfloat16)
+
+
+def x_rows(w: Workload, b: int, t0: int, t1: int, seed: int = SEED_X) -> torch.Tensor:
+    """Rows [t0, t1) of batch row b of the activation x, bf16 [t1-t0, D]."""
+    out = []
+    blk0, blk1 = t0 // ROW_BLOCK, (t1 + ROW_BLOCK - 1) // ROW_BLOCK
+    for blk in range(blk0, blk1):
+        key = b * ((w.T + ROW_BLOCK - 1) // ROW_BLOCK) + blk
+        rows = min(ROW_BLOCK, w.T - blk * ROW_BLOCK)
+        full = _normal_bf16((rows, w.D), 1.0, seed, key)
+        lo = max(t0 - blk * ROW_BLOCK, 0)
+        hi = min(t1 - blk * ROW_BLOCK, rows)
+        out.append(full[lo:hi])
+    return torch.cat(out, 0)
+
+
+def x_full(w: Workload, seed: int = SEED_X, threads: int = 16) -> torch.Tensor:
+    """The whole activation x, bf16 [B, T, D] (blocks drawn in parallel)."""
+    x = torch.empty((w.B, w.T, w.D), dtype=torch.bfloat16)
+    nblk = (w.T + ROW_BLOCK - 1) // ROW_BLOCK
+
+    def fill(job):
+        b, blk = job
+        t0 = blk * ROW_BLOCK
+        t1 = min(t0 + ROW_BLOCK, w.T)
+        x[b, t0:t1] = x_rows(w, b, t0, t1, seed)
+
+    jobs = [(b, k) for b in range(w.B) for k in range(nblk)]
+    with ThreadPoolExecutor(max_workers=threads) as ex:
+        list(ex.map(fill, jobs))
+    return x
+
+
+def weights(w: Workload, layer: int = 0) -> dict:
+    """Projection weights and QK-norm scales of one layer (bf16, CPU).
+
+    Layouts (row-major): Wq [H*d_h, D] (row n = h*d_h + c), Wkv [2, H_kv*d_h, D]
+    ([0] = K, [1] = V), Wo [D, H*d_h], gamma_q / gamma_k [d_h].
+    """
+    off = 100 * layer
+    std_in = 1.0 / math.sqrt(w.D)
+    return {
+        "Wq": _normal_bf16((w.H * w.d_h, w.D), std_in, SEED_WQ + off),
+        "Wkv": _normal_bf16((2, w.H_kv * w.d_h, w.D), std_in, SEED_WKV + off),
+        "Wo": _normal_bf16((w.D, w.H * w.d_h), std_in, SEED_WO + off),
+        "gamma_q": _normal_bf16((w.d_h,), math.sqrt(0.1), SEED_GQ + off),
+        "gamma_k": _normal_bf16((w.d_h,), math.sqrt(0.1), SEED_GK + off),
+    }
+
+
+def block_norm_gammas(w: Workload, layer: int) -> dict:
+    """Pre- and post-attention RMSNorm scales [D] of one stack layer (bf16)."""
+    off = 100 * layer
+    return {
+        "gamma_pre": _normal_bf16((w.D,), math.sqrt(0.1), SEED_GPRE + off),
+        "gamma_post": _normal_bf16((w.D,), math.sqrt(0.1), SEED_GPOST + off),
+    }
+
+
+def pad_lens(w: Workload) -> torch.Tensor:
+    """Trailing pad count per batch row, int32 [B] (valid length = T - pad)."""
+    g = _gen(SEED_PAD)
+    kind = w.pad[0]
+    if kind == "none":
+        return torch.zeros(w.B, dtype=torch.int32)
+    lo, hi = w.pad[1], w.pad[2]
+    draw = torch.randint(lo, hi + 1, (w.B,), generator=g, dtype=torch.int64)
+    if kind == "pad_uniform":
+        return draw.to(torch.int32)
+    if kind == "valid_uniform":
+        return (w.T - draw).to(torch.int32)
+    raise ValueError(kind)
+
+
+def segment_pos(w: Workload) -> torch.Tensor:
+    """RoPE positions: 0..T-1 in every batch row, int32 [B, T]."""
+    return torch.arange(w.T, dtype=torch.int32).repeat(w.B, 1)
+
+
+def valid_tokens(w: Workload) -> int:
+    return int((w.T - pad_lens(w).to(torch.int64)).sum())
