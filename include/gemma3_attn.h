@@ -1,0 +1,201 @@
+/*
+ * gemma3_attn.h -- C ABI of libgemma3attn.so: the forward pass of the Gemma 3
+ * attention block on one NVIDIA GB300 (sm_103a).
+ *
+ * What it computes is defined by four pages, cited below by title and section:
+ *   [AB] "Gemma 3 Attention Block"        Overview; How it works (Projections,
+ *        QK-norm then RoPE then scale, Scores, Routing)
+ *   [FB] "Full Gemma 3 Block"             How it works (Block.__call__ equations)
+ *   [RT] "Global vs Local Layer Routing"  How it works; Watch-outs
+ *   [QK] "QK-Norm"                        How it works (RMSNorm equation); Watch-outs
+ *
+ * Conventions shared by every entry point
+ *   - All tensor pointers are DEVICE pointers, 16-byte aligned, row-major and
+ *     contiguous unless a leading dimension is given.  bf16 / f16 tensors are
+ *     passed as void* and hold IEEE binary16 / bfloat16 bit patterns.
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Every call is
+ *     asynchronous on that stream and never synchronises; read results after
+ *     synchronising the stream yourself.
+ *   - The caller owns every buffer.  The library never allocates device memory;
+ *     scratch space is the caller's `workspace` (see gemma3_attn_workspace_size).
+ *     Inputs are read only; only `out`/`y` and `workspace` are written.
+ *   - Every function returns a status (GEMMA3_OK = 0 or a negative error) and
+ *     validates all arguments before launching anything.  Kernels that lose a
+ *     synchronisation event stop after a bounded wait and record an error that
+ *     gemma3_attn_check_status() reports; they never hang or trap.
+ *   - Calls on different streams need distinct workspaces.
+ */
+#ifndef GEMMA3_ATTN_H_
+#define GEMMA3_ATTN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes. */
+enum {
+  GEMMA3_OK = 0,
+  GEMMA3_ERR_INVALID_ARG = -1, /* null pointer, bad shape or out-of-range value */
+  GEMMA3_ERR_MISALIGNED = -2,  /* pointer or row stride not 16-byte aligned */
+  GEMMA3_ERR_UNSUPPORTED = -3, /* d_h not in {128, 256}, G not in {1, 2, 4}, not sm_103 */
+  GEMMA3_ERR_CUDA = -4,        /* a CUDA runtime call or kernel launch failed */
+  GEMMA3_ERR_TIMEOUT = -5,     /* a kernel gave up on a bounded wait (device status word) */
+  GEMMA3_ERR_WORKSPACE = -6    /* workspace smaller than gemma3_*_workspace_size() */
+};
+
+/* Attention types of [RT] How it works (AttentionType enum). */
+enum { GEMMA3_LOCAL_SLIDING = 0, GEMMA3_GLOBAL = 1 };
+
+/* Element types for the stage entry points. */
+enum { GEMMA3_BF16 = 0, GEMMA3_F16 = 1, GEMMA3_F32 = 2 };
+
+/* Released sizes named by the pages ([AB] Overview, [RT] How it works). */
+enum { GEMMA3_270M = 0, GEMMA3_1B = 1, GEMMA3_4B = 2, GEMMA3_12B = 3, GEMMA3_27B = 4 };
+
+/* Layer shape: batch B, sequence T, model width D, H query heads, H_kv
+ * key/value heads (H % H_kv == 0, G = H / H_kv), head dim d_h. */
+typedef struct {
+  int B, T, D, H, H_kv, d_h;
+} gemma3_attn_dims;
+
+/* ------------------------------------------------------------------ routing */
+
+/* Attention type of layer `layer` (0-based) in a stack of `num_layers`:
+ * P[layer mod 6] with P = (L,L,L,L,L,G); a depth that is not a multiple of 6
+ * ends with the prefix P[:N % 6], so leftover layers are local ([RT] How it
+ * works, Watch-outs).  Returns GEMMA3_LOCAL_SLIDING or GEMMA3_GLOBAL, or
+ * GEMMA3_ERR_INVALID_ARG when layer is not in [0, num_layers). */
+int gemma3_layer_attn_type(int layer, int num_layers);
+
+/* Per-layer hyper-parameters that the type selects ([RT] How it works,
+ * Transformer.setup mapping; [AB] Overview): local layers RoPE base 1e4,
+ * scale 1, window 1024 (512 on 270M/1B); global layers base 1e6, scale 8 on
+ * 4B/12B/27B and 1 on 270M/1B, window 0 (= none).  Any output pointer may be
+ * NULL.  Returns the attention type or a negative status. */
+int gemma3_layer_config(int layer, int num_layers, int model_size, int* attn_type, int* window,
+                        double* rope_base, double* rope_scale);
+
+/* query_pre_attn_scalar ([AB] How it works, query scale): d_h^-1/2, or
+ * (D/H)^-1/2 on 27B.  Writes it to *alpha; returns a status. */
+int gemma3_query_scale(int model_size, int D, int H, int d_h, float* alpha);
+
+/* ------------------------------------------------------------ one attention layer */
+
+/* Bytes of workspace gemma3_attn_forward needs for `dims` (written to *bytes):
+ * Q/O rows [B*T, H*d_h] and K/V rows [B*T, 2*H_kv*d_h], 2 bytes per element. */
+int gemma3_attn_workspace_size(const gemma3_attn_dims* dims, size_t* bytes);
+
+/* Forward pass of one Gemma 3 attention layer ([AB] How it works, steps in
+ * order):
+ *   Q = x Wq^T, [K|V] = x Wkv^T                     (Projections; fp32 accumulate)
+ *   Q, K <- RMSNorm over d_h * (1 + gamma_q|gamma_k), eps 1e-6   ([QK])
+ *   Q, K <- RoPE(rope_base, rope_scale) at segment_pos; Q <- query_scale * Q
+ *   logits = Q K^T per head, kv head h / G; keep s <= t, s < T - pad_b and,
+ *   for GEMMA3_LOCAL_SLIDING, s > t - window; softmax over s; O = P V
+ *   out = O Wo^T                                    (attn_vec_einsum)
+ * Arguments:
+ *   x            [B, T, D] bf16
+ *   segment_pos  [B, T] int32 RoPE positions (0 <= pos < 2^24)
+ *   pad_lens     [B] int32 trailing pad count per batch row (0 <= pad_b <= T),
+ *                or NULL for none.  Rows t >= T - pad_b of `out` are written 0.
+ *   Wq           [H*d_h, D] bf16, row n = h*d_h + c
+ *   Wkv          [2, H_kv*d_h, D] bf16, [0] = K, [1] = V
+ *   Wo           [D, H*d_h] bf16
+ *   gamma_q/k    [d_h] bf16 each (separate scales, shared across heads)
+ *   attn_type    GEMMA3_LOCAL_SLIDING (window >= 1) or GEMMA3_GLOBAL (window ignored)
+ *   rope_base, rope_scale  > 0;  query_scale  the query scale alpha
+ *   out          [B, T, D] bf16
+ *   workspace    >= gemma3_attn_workspace_size() bytes, 256-byte aligned
+ * Limits: d_h in {128, 256}; G in {1, 2, 4}; D % 8 == 0; B*T < 2^31. */
+int gemma3_attn_forward(const gemma3_attn_dims* dims, const void* x, const int32_t* segment_pos,
+                        const int32_t* pad_lens, const void* Wq, const void* Wkv, const void* Wo,
+                        const void* gamma_q, const void* gamma_k, int attn_type, int window,
+                        double rope_base, double rope_scale, float query_scale, void* out,
+                        void* workspace, size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------- one block-attention layer */
+
+/* Workspace of gemma3_block_attn_forward: that of gemma3_attn_forward plus
+ * [B*T, D] bf16 (normed input) and [B*T, D] fp32 (attention output). */
+int gemma3_block_attn_workspace_size(const gemma3_attn_dims* dims, size_t* bytes);
+
+/* Attention half of a Gemma 3 block ([FB] How it works, first three lines):
+ *   a = Attn(RMSNorm_pre(x));  a <- RMSNorm_post(a);  y = x + a
+ * with D-axis RMSNorms, eps 1e-6, (1 + gamma).  x is [B, T, D] in x_dtype
+ * (GEMMA3_BF16 or GEMMA3_F32); y is [B, T, D] fp32 and may alias x when
+ * x_dtype is GEMMA3_F32.  gamma_pre / gamma_post are [D] bf16; the other
+ * arguments are those of gemma3_attn_forward.  Pad rows get a = 0, so y = x. */
+int gemma3_block_attn_forward(const gemma3_attn_dims* dims, const void* x, int x_dtype,
+                              float* y, const int32_t* segment_pos, const int32_t* pad_lens,
+                              const void* Wq, const void* Wkv, const void* Wo,
+                              const void* gamma_q, const void* gamma_k, const void* gamma_pre,
+                              const void* gamma_post, int attn_type, int window,
+                              double rope_base, double rope_scale, float query_scale,
+                              void* workspace, size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------- stage entry points */
+
+/* C[M, N] = A[M, K] * W[N, K]^T (the projection einsums of [AB] How it
+ * works).  A, W bf16 with row strides lda, ldw (elements); C in out_dtype
+ * (GEMMA3_BF16 | GEMMA3_F16 | GEMMA3_F32) with row stride ldc.  fp32
+ * accumulation on the tcgen05 tensor cores.  K % 8 == 0; strides in bytes
+ * must be multiples of 16.  max_ctas > 0 caps the persistent grid. */
+int gemma3_linear(const void* A, long lda, const void* W, long ldw, void* C, long ldc, int M,
+                  int N, int K, int out_dtype, int max_ctas, void* stream);
+
+/* In place on fp16 rows: for every token m and head, RMSNorm over d_h with
+ * (1 + gamma_q) (query heads of Q[m, h*d_h : (h+1)*d_h]) or (1 + gamma_k)
+ * (key heads of K[m, j*d_h : ...]), then RoPE at position pos[m] with
+ * (rope_base, rope_scale), then Q *= query_scale ([QK] How it works: norm,
+ * then RoPE, then query scale).  Q [M, ldq], K [M, ldk] fp16; gamma bf16 [d_h]. */
+int gemma3_qk_norm_rope(void* Q, long ldq, void* K, long ldk, const void* gamma_q,
+                        const void* gamma_k, const int32_t* pos, int M, int H, int H_kv,
+                        int d_h, double rope_base, double rope_scale, float query_scale,
+                        void* stream);
+
+/* Masked softmax attention ([AB] How it works, Scores): Q' [B, T, H, d_h]
+ * fp16 (query scale already applied); K', V rows of fp16 buffers with row
+ * stride ldkv elements, head j at column j*d_h ([B*T, ldkv]); O [B, T, H, d_h]
+ * bf16 (may alias Q').  Mask and padding as in gemma3_attn_forward
+ * (window <= 0 means global / causal only). */
+int gemma3_flash_attention(const void* Q, const void* K, const void* V, long ldkv, void* O,
+                           const int32_t* pad_lens, int B, int T, int H, int H_kv, int d_h,
+                           int window, void* stream);
+
+/* u[m, :] = x[m, :] / sqrt(mean(x[m, :]^2) + 1e-6) * (1 + gamma)  ([FB] block
+ * norms).  x [M, D] bf16 or fp32 (x_dtype), gamma [D] bf16, u [M, D] bf16. */
+int gemma3_rmsnorm(const void* x, int x_dtype, const void* gamma, void* u, int M, int D,
+                   void* stream);
+
+/* y = x + RMSNorm(a) * (1 + gamma)  ([FB] post-attention norm + residual).
+ * a [M, D] fp32, x [M, D] bf16|fp32, y [M, D] fp32 (may alias an fp32 x). */
+int gemma3_postnorm_residual(const float* a, const void* x, int x_dtype, const void* gamma,
+                             float* y, int M, int D, void* stream);
+
+/* ------------------------------------------------------------------ status */
+
+/* Synchronises `stream`, reads and clears the device status word of the
+ * current device.  Returns GEMMA3_OK, GEMMA3_ERR_TIMEOUT (a bounded wait in a
+ * kernel expired), or GEMMA3_ERR_CUDA (the stream reported an error). */
+int gemma3_attn_check_status(void* stream);
+
+/* Raw device status word of the last check (0 = none; 0x1000 + n = wait site n). */
+int gemma3_last_device_status(void);
+
+/* Human-readable text of a status code. */
+const char* gemma3_strerror(int status);
+
+/* Runs one kernel whose single wait nothing ever completes, with the given
+ * time limit in nanoseconds (1e6 .. 5e9), and returns what
+ * gemma3_attn_check_status() reports (GEMMA3_ERR_TIMEOUT when the bounded wait
+ * works).  Exercises the failure path without faulting the device. */
+int gemma3_selftest_wait_timeout(long long timeout_ns, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GEMMA3_ATTN_H_ */

@@ -145,6 +145,30 @@ def normalised_rotated_qk(x_rows, positions, Wq, Wkv, gamma_q, gamma_k, *,
     return Q, K
 
 
+def attend(Q, K, V, t_idx, s_idx, valid, attn_type, window):
+    """Masked softmax attention of one batch row ([AB] How it works, Scores).
+
+    Q [Tq, H, d_h] (query scale applied), K, V [S, H_kv, d_h] at key positions
+    s_idx, query positions t_idx.  Q is reshaped to [Tq, H_kv, G, d_h] and
+    contracted with K; blocked logits are K_MASK; softmax over s mixes V.
+    Returns [Tq, H, d_h]."""
+    Tq, H, d_h = Q.shape
+    H_kv = K.shape[1]
+    G = H // H_kv
+    Qg = Q.reshape(Tq, H_kv, G, d_h)
+    logits = torch.einsum("tkgc,skc->tkgs", Qg, K)        # [Tq, H_kv, G, S]
+
+    # Mask: causal + padding; local layers also multiply in the sliding mask
+    mask = causal_padding_mask(t_idx, s_idx, valid)
+    if attn_type == LOCAL_SLIDING:
+        mask = mask & create_sliding_mask(t_idx, s_idx, window)
+    logits = torch.where(mask[:, None, None, :], logits, torch.tensor(K_MASK, dtype=F64))
+
+    # Softmax over s, then mix V ([AB] Scores)
+    probs = torch.softmax(logits, dim=-1)
+    return torch.einsum("tkgs,skc->tkgc", probs, V).reshape(Tq, H, d_h)
+
+
 def attention_layer(x, segment_pos, pad_lens, Wq, Wkv, Wo, gamma_q, gamma_k, *,
                     H, H_kv, d_h, attn_type, window, rope_base, rope_scale,
                     query_scale, rows=None):
@@ -155,15 +179,14 @@ def attention_layer(x, segment_pos, pad_lens, Wq, Wkv, Wo, gamma_q, gamma_k, *,
     attn_type LOCAL_SLIDING | GLOBAL.
 
     ``rows`` (optional) is a list, per batch row, of query positions to compute;
-    only the keys those queries can see are projected.  Keys outside that range
-    are blocked for every requested query, and a blocked logit contributes
+    only the keys those queries can see are projected.  Every other key is
+    blocked for every requested query, and a blocked logit contributes
     exp(K_MASK - max) == 0.0 exactly in fp64, so the sampled outputs equal the
     corresponding rows of the full computation.
 
     Returns out [B,T,D] (rows=None) or a list, per batch row, of [len(rows[b]), D].
     """
     B, T, D = x.shape
-    G = H // H_kv
     if pad_lens is None:
         pad_lens = torch.zeros(B, dtype=torch.int64)
     outs = []
@@ -173,16 +196,20 @@ def attention_layer(x, segment_pos, pad_lens, Wq, Wkv, Wo, gamma_q, gamma_k, *,
         if t_req.numel() == 0:
             outs.append(torch.zeros(0, D, dtype=F64))
             continue
-        if attn_type == LOCAL_SLIDING:
-            s_lo = max(0, int(t_req.min()) - window + 1)
+        # Keys any requested query can see: s <= t (causal) and, on local
+        # layers, s > t - W; the union over the requested rows.
+        if rows is None:
+            s_idx = torch.arange(T)
         else:
-            s_lo = 0
-        s_hi = int(t_req.max())                            # keys s <= t (causal)
-        s_idx = torch.arange(s_lo, s_hi + 1)
+            seen = torch.zeros(T, dtype=torch.bool)
+            for t in t_req.tolist():
+                lo = max(0, t - window + 1) if attn_type == LOCAL_SLIDING else 0
+                seen[lo:t + 1] = True
+            s_idx = torch.nonzero(seen).flatten()
 
         # Projections ([AB] How it works, Projections)
         xq = x[b, t_req]                                   # [Tq, D]
-        xs = x[b, s_lo:s_hi + 1]                           # [S, D]
+        xs = x[b, s_idx]                                   # [S, D]
         Q = project(xq, Wq).reshape(-1, H, d_h)
         K = project(xs, Wkv[0]).reshape(-1, H_kv, d_h)
         V = project(xs, Wkv[1]).reshape(-1, H_kv, d_h)
@@ -194,26 +221,13 @@ def attention_layer(x, segment_pos, pad_lens, Wq, Wkv, Wo, gamma_q, gamma_k, *,
 
         # RoPE with the layer's base and scale ([AB] How it works)
         Q = rope(Q, segment_pos[b, t_req], rope_base, rope_scale)
-        K = rope(K, segment_pos[b, s_lo:s_hi + 1], rope_base, rope_scale)
+        K = rope(K, segment_pos[b, s_idx], rope_base, rope_scale)
 
         # Query scale after RoPE ([QK] How it works; [AB] query-scale cases)
         Q = Q * query_scale
 
-        # Scores: reshape Q to [Tq, H_kv, G, d_h], contract with K ([AB] Scores, GQA)
-        Qg = Q.reshape(-1, H_kv, G, d_h)
-        logits = torch.einsum("tkgc,skc->tkgs", Qg, K)    # [Tq, H_kv, G, S]
-
-        # Mask: causal + padding; local layers also multiply in the sliding mask
-        mask = causal_padding_mask(t_req, s_idx, valid)
-        if attn_type == LOCAL_SLIDING:
-            mask = mask & create_sliding_mask(t_req, s_idx, window)
-        logits = torch.where(mask[:, None, None, :], logits,
-                             torch.tensor(K_MASK, dtype=F64))
-
-        # Softmax over s, mix V, flatten heads, output projection ([AB] Scores)
-        probs = torch.softmax(logits, dim=-1)
-        enc = torch.einsum("tkgs,skc->tkgc", probs, V).reshape(-1, H * d_h)
-        out = project(enc, Wo)                             # [Tq, D]
+        enc = attend(Q, K, V, t_req, s_idx, valid, attn_type, window)
+        out = project(enc.reshape(-1, H * d_h), Wo)        # [Tq, D] (attn_vec_einsum)
 
         # Reading R3: rows past the valid length have no output
         out[t_req >= valid] = 0.0

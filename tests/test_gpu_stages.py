@@ -1,0 +1,150 @@
+"""GPU parity of each stage kernel against the fp64 oracle's definition of it.
+
+Stages: the tcgen05 projection GEMM, the fused QK-norm + RoPE + query-scale
+prologue, and the flash-attention kernel, each fed the same seeded inputs as
+the oracle, at sizes spanning several tiles and a ragged tail.
+"""
+import math
+
+import pytest
+import torch
+
+from oracle import gemma3_oracle as O
+from tests.helpers import QK_MAX_ABS, max_abs, rel_frob
+
+pytestmark = pytest.mark.gpu
+
+F64 = torch.float64
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from transformer_attention_gb300.build import build
+    build()
+    import transformer_attention_gb300 as G3
+    G3.lib()
+    torch.cuda.init()
+
+
+def _randn(shape, seed, std=1.0, dtype=torch.bfloat16):
+    g = torch.Generator().manual_seed(seed)
+    return (torch.randn(shape, generator=g) * std).to(dtype)
+
+
+# ---------------------------------------------------------------- projection GEMM
+@pytest.mark.parametrize("M,N,K", [(256, 512, 1152), (300, 1152, 4096), (1024, 2048, 2560),
+                                   (130, 200, 72), (128, 256, 64), (4096, 1536, 1024)])
+@pytest.mark.parametrize("out", ["bf16", "f16", "f32"])
+def test_linear_matches_fp64(M, N, K, out):
+    import transformer_attention_gb300 as G3
+    dt = {"bf16": torch.bfloat16, "f16": torch.float16, "f32": torch.float32}[out]
+    A = _randn((M, K), 1)
+    W = _randn((N, K), 2, K ** -0.5)
+    C = G3.linear(A.cuda(), W.cuda(), out_dtype=dt)
+    assert G3.gemma3_attn_check_status() == 0
+    ref = O.project(A, W)
+    tol = {"bf16": 4e-3, "f16": 1e-3, "f32": 1e-5}[out]
+    assert rel_frob(C.cpu(), ref) <= tol
+
+
+def test_linear_small_grid_many_tiles():
+    # a 3-CTA persistent grid walking 48 tiles exercises the accumulator ring
+    import transformer_attention_gb300 as G3
+    A = _randn((1024, 640), 3)
+    W = _randn((1536, 640), 4, 640 ** -0.5)
+    C = G3.linear(A.cuda(), W.cuda(), out_dtype=torch.float32, max_ctas=3)
+    assert G3.gemma3_attn_check_status() == 0
+    assert rel_frob(C.cpu(), O.project(A, W)) <= 1e-5
+
+
+# ---------------------------------------------------------------- QK-norm + RoPE prologue
+@pytest.mark.parametrize("d_h,H,H_kv,base,scale,alpha", [
+    (256, 4, 1, 1e4, 1.0, 256 ** -0.5),
+    (256, 8, 4, 1e6, 8.0, 256 ** -0.5),
+    (128, 32, 16, 1e6, 8.0, 168 ** -0.5),
+    (128, 4, 2, 1e4, 1.0, 128 ** -0.5),
+])
+def test_qk_norm_rope_matches_oracle(d_h, H, H_kv, base, scale, alpha):
+    import transformer_attention_gb300 as G3
+    M = 777
+    Qr = _randn((M, H * d_h), 10, 1.0, torch.float16)
+    KVr = _randn((M, 2 * H_kv * d_h), 11, 1.0, torch.float16)
+    gq = _randn((d_h,), 12, 0.1 ** 0.5)
+    gk = _randn((d_h,), 13, 0.1 ** 0.5)
+    g = torch.Generator().manual_seed(14)
+    pos = torch.cat([torch.arange(0, 300), torch.randint(0, 131072, (M - 302,), generator=g),
+                     torch.tensor([131071, 2 ** 20])]).to(torch.int32)
+    Qd, KVd = Qr.cuda(), KVr.cuda()
+    G3.gemma3_qk_norm_rope(Qd, H * d_h, KVd, 2 * H_kv * d_h, gq.cuda(), gk.cuda(), pos.cuda(),
+                           M, H, H_kv, d_h, base, scale, alpha)
+    assert G3.gemma3_attn_check_status() == 0
+    Qo, KVo = Qd.cpu(), KVd.cpu()
+    q_ref = O.rope(O.rms_norm(Qr.reshape(M, H, d_h), gq)[None], pos[None], base, scale)[0]
+    k_ref = O.rope(O.rms_norm(KVr[:, :H_kv * d_h].reshape(M, H_kv, d_h), gk)[None], pos[None],
+                   base, scale)[0]
+    q_got = Qo.reshape(M, H, d_h).to(F64) / alpha
+    k_got = KVo[:, :H_kv * d_h].reshape(M, H_kv, d_h)
+    assert max_abs(q_got, q_ref) <= QK_MAX_ABS
+    assert max_abs(k_got, k_ref) <= QK_MAX_ABS
+    # V columns are untouched ("QK-Norm": values are left unnormalised)
+    assert torch.equal(KVo[:, H_kv * d_h:], KVr[:, H_kv * d_h:])
+
+
+# ---------------------------------------------------------------- flash attention
+ATTN_CASES = [
+    # B, T, H, H_kv, d_h, window, pads
+    (2, 300, 4, 1, 256, 100, [0, 37]),
+    (1, 1024, 8, 4, 256, 0, [0]),
+    (2, 513, 4, 2, 128, 0, [0, 200]),
+    (1, 700, 2, 2, 128, 256, [0]),
+    (1, 640, 8, 2, 128, 0, [5]),
+    (1, 257, 2, 2, 256, 0, [0]),
+    (1, 1, 4, 1, 256, 0, [0]),
+    (3, 190, 4, 1, 256, 64, [0, 189, 190]),
+    (1, 1500, 4, 1, 256, 512, [0]),
+]
+
+
+@pytest.mark.parametrize("B,T,H,H_kv,d_h,window,pads", ATTN_CASES)
+def test_flash_attention_matches_oracle(B, T, H, H_kv, d_h, window, pads):
+    import transformer_attention_gb300 as G3
+    G = H // H_kv
+    alpha = d_h ** -0.5
+    # Q' carries the query scale; |q|, |k| ~ RMS-normalised heads with (1 + gamma)
+    Q = (_randn((B, T, H, d_h), 20, 1.3, torch.float32) * alpha).to(torch.float16)
+    KV = _randn((B, T, 2 * H_kv * d_h), 21, 1.3, torch.float16)
+    pad = torch.tensor(pads, dtype=torch.int32)
+    Qd, KVd = Q.cuda(), KV.cuda()
+    Od = torch.empty((B, T, H, d_h), dtype=torch.bfloat16, device="cuda")
+    Od.fill_(float("nan"))
+    G3.gemma3_flash_attention(Qd, KVd, KVd[..., H_kv * d_h:], 2 * H_kv * d_h, Od, pad.cuda(), B, T,
+                              H, H_kv, d_h, window)
+    assert G3.gemma3_attn_check_status() == 0
+    got = Od.cpu().to(F64)
+    kind = O.LOCAL_SLIDING if window > 0 else O.GLOBAL
+    for b in range(B):
+        valid = T - pads[b]
+        K = KV[b, :, :H_kv * d_h].reshape(T, H_kv, d_h).to(F64)
+        V = KV[b, :, H_kv * d_h:].reshape(T, H_kv, d_h).to(F64)
+        idx = torch.arange(T)
+        if valid > 0:
+            ref = O.attend(Q[b, :valid].to(F64), K, V, idx[:valid], idx, valid, kind, window)
+            assert rel_frob(got[b, :valid], ref) <= 5e-3, (b, rel_frob(got[b, :valid], ref))
+            assert max_abs(got[b, :valid], ref) <= 2e-2
+        assert torch.equal(got[b, valid:], torch.zeros_like(got[b, valid:]))
+    _ = G  # G in {1,2,4} is covered by the cases above
+
+
+def test_flash_attention_local_window_ge_T_equals_global():
+    import transformer_attention_gb300 as G3
+    B, T, H, H_kv, d_h = 1, 384, 4, 2, 256
+    Q = (_randn((B, T, H, d_h), 30, 1.0, torch.float32) / 16).to(torch.float16).cuda()
+    KV = _randn((B, T, 2 * H_kv * d_h), 31, 1.0, torch.float16).cuda()
+    outs = []
+    for window in (0, T, 5 * T):
+        Od = torch.empty((B, T, H, d_h), dtype=torch.bfloat16, device="cuda")
+        G3.gemma3_flash_attention(Q, KV, KV[..., H_kv * d_h:], 2 * H_kv * d_h, Od, None, B, T, H,
+                                  H_kv, d_h, window)
+        outs.append(Od.cpu())
+    assert G3.gemma3_attn_check_status() == 0
+    assert torch.equal(outs[0], outs[1]) and torch.equal(outs[0], outs[2])

@@ -1,0 +1,77 @@
+"""Gemma 3 attention-block forward pass on one GB300 (sm_103a).
+
+The compute lives in libgemma3attn.so (CUDA kernels behind the C ABI of
+include/gemma3_attn.h).  ``_lib`` binds that ABI under the same names;
+the helpers below only allocate outputs and workspaces with torch and call it.
+"""
+from __future__ import annotations
+
+from ._lib import (  # noqa: F401  (re-exported C-ABI names)
+    GEMMA3_BF16, GEMMA3_F16, GEMMA3_F32, GEMMA3_GLOBAL, GEMMA3_LOCAL_SLIDING, Gemma3Error,
+    gemma3_attn_check_status, gemma3_attn_forward, gemma3_attn_workspace_size,
+    gemma3_block_attn_forward, gemma3_block_attn_workspace_size, gemma3_flash_attention,
+    gemma3_last_device_status, gemma3_layer_attn_type, gemma3_layer_config, gemma3_linear,
+    gemma3_postnorm_residual, gemma3_qk_norm_rope, gemma3_query_scale, gemma3_rmsnorm,
+    gemma3_selftest_wait_timeout, lib)
+
+__all__ = ["attention_forward", "block_attention_forward", "linear", "lib"]
+
+
+def _empty_ws(nbytes: int, device):
+    import torch
+    return torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
+
+
+def attention_forward(x, segment_pos, pad_lens, Wq, Wkv, Wo, gamma_q, gamma_k, *, H, H_kv,
+                      attn_type, window, rope_base, rope_scale, query_scale, out=None,
+                      workspace=None, stream=None):
+    """One attention layer: x [B,T,D] bf16 (CUDA) -> out [B,T,D] bf16.
+
+    attn_type: GEMMA3_LOCAL_SLIDING or GEMMA3_GLOBAL.  pad_lens may be None.
+    """
+    import torch
+    B, T, D = x.shape
+    d_h = gamma_q.shape[0]
+    dims = (B, T, D, H, H_kv, d_h)
+    ws_bytes = gemma3_attn_workspace_size(*dims)
+    if workspace is None:
+        workspace = _empty_ws(ws_bytes, x.device)
+    if out is None:
+        out = torch.empty((B, T, D), dtype=torch.bfloat16, device=x.device)
+    gemma3_attn_forward(dims, x, segment_pos, pad_lens, Wq, Wkv, Wo, gamma_q, gamma_k, attn_type,
+                        window, rope_base, rope_scale, query_scale, out, workspace,
+                        workspace.numel(), stream)
+    return out
+
+
+def block_attention_forward(x, segment_pos, pad_lens, Wq, Wkv, Wo, gamma_q, gamma_k, gamma_pre,
+                            gamma_post, *, H, H_kv, attn_type, window, rope_base, rope_scale,
+                            query_scale, y=None, workspace=None, stream=None):
+    """y = x + RMSNorm_post(Attn(RMSNorm_pre(x))); x bf16 or fp32, y fp32 (may be x)."""
+    import torch
+    B, T, D = x.shape
+    d_h = gamma_q.shape[0]
+    dims = (B, T, D, H, H_kv, d_h)
+    ws_bytes = gemma3_block_attn_workspace_size(*dims)
+    if workspace is None:
+        workspace = _empty_ws(ws_bytes, x.device)
+    if y is None:
+        y = torch.empty((B, T, D), dtype=torch.float32, device=x.device)
+    x_dtype = GEMMA3_F32 if x.dtype == torch.float32 else GEMMA3_BF16
+    gemma3_block_attn_forward(dims, x, x_dtype, y, segment_pos, pad_lens, Wq, Wkv, Wo, gamma_q,
+                              gamma_k, gamma_pre, gamma_post, attn_type, window, rope_base,
+                              rope_scale, query_scale, workspace, workspace.numel(), stream)
+    return y
+
+
+def linear(A, W, out_dtype=None, max_ctas=0, stream=None):
+    """C = A @ W^T on the tcgen05 GEMM (A [M,K], W [N,K] bf16)."""
+    import torch
+    out_dtype = out_dtype or torch.bfloat16
+    code = {torch.bfloat16: GEMMA3_BF16, torch.float16: GEMMA3_F16, torch.float32: GEMMA3_F32}
+    M, K = A.shape
+    N = W.shape[0]
+    C = torch.empty((M, N), dtype=out_dtype, device=A.device)
+    gemma3_linear(A, A.stride(0), W, W.stride(0), C, C.stride(0), M, N, K, code[out_dtype],
+                  max_ctas, stream)
+    return C

@@ -1,0 +1,219 @@
+"""ctypes binding of libgemma3attn.so: same names as the C ABI in include/gemma3_attn.h.
+
+The functions here only marshal arguments (tensor -> device pointer, torch's
+current CUDA stream -> cudaStream_t) and turn a non-zero status into an
+exception.  All computation runs in the library's CUDA kernels; there is no
+fallback: if the library is missing or fails to load, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from .build import LIB
+
+c_int, c_long, c_double, c_float, c_size_t, c_void_p = (
+    ctypes.c_int, ctypes.c_long, ctypes.c_double, ctypes.c_float, ctypes.c_size_t, ctypes.c_void_p)
+
+GEMMA3_OK = 0
+GEMMA3_ERR_TIMEOUT = -5
+GEMMA3_LOCAL_SLIDING, GEMMA3_GLOBAL = 0, 1
+GEMMA3_BF16, GEMMA3_F16, GEMMA3_F32 = 0, 1, 2
+MODEL_SIZES = {"270M": 0, "1B": 1, "4B": 2, "12B": 3, "27B": 4}
+
+
+class gemma3_attn_dims(ctypes.Structure):
+    _fields_ = [("B", c_int), ("T", c_int), ("D", c_int), ("H", c_int), ("H_kv", c_int),
+                ("d_h", c_int)]
+
+
+# name -> (restype, argtypes); mirrors include/gemma3_attn.h
+SIGNATURES = {
+    "gemma3_layer_attn_type": (c_int, [c_int, c_int]),
+    "gemma3_layer_config": (c_int, [c_int, c_int, c_int, ctypes.POINTER(c_int),
+                                    ctypes.POINTER(c_int), ctypes.POINTER(c_double),
+                                    ctypes.POINTER(c_double)]),
+    "gemma3_query_scale": (c_int, [c_int, c_int, c_int, c_int, ctypes.POINTER(c_float)]),
+    "gemma3_attn_workspace_size": (c_int, [ctypes.POINTER(gemma3_attn_dims),
+                                           ctypes.POINTER(c_size_t)]),
+    "gemma3_attn_forward": (c_int, [ctypes.POINTER(gemma3_attn_dims), c_void_p, c_void_p, c_void_p,
+                                    c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int,
+                                    c_double, c_double, c_float, c_void_p, c_void_p, c_size_t,
+                                    c_void_p]),
+    "gemma3_block_attn_workspace_size": (c_int, [ctypes.POINTER(gemma3_attn_dims),
+                                                 ctypes.POINTER(c_size_t)]),
+    "gemma3_block_attn_forward": (c_int, [ctypes.POINTER(gemma3_attn_dims), c_void_p, c_int,
+                                          c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
+                                          c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int,
+                                          c_int, c_double, c_double, c_float, c_void_p, c_size_t,
+                                          c_void_p]),
+    "gemma3_linear": (c_int, [c_void_p, c_long, c_void_p, c_long, c_void_p, c_long, c_int, c_int,
+                              c_int, c_int, c_int, c_void_p]),
+    "gemma3_qk_norm_rope": (c_int, [c_void_p, c_long, c_void_p, c_long, c_void_p, c_void_p,
+                                    c_void_p, c_int, c_int, c_int, c_int, c_double, c_double,
+                                    c_float, c_void_p]),
+    "gemma3_flash_attention": (c_int, [c_void_p, c_void_p, c_void_p, c_long, c_void_p, c_void_p,
+                                       c_int, c_int, c_int, c_int, c_int, c_int, c_void_p]),
+    "gemma3_rmsnorm": (c_int, [c_void_p, c_int, c_void_p, c_void_p, c_int, c_int, c_void_p]),
+    "gemma3_postnorm_residual": (c_int, [c_void_p, c_void_p, c_int, c_void_p, c_void_p, c_int,
+                                         c_int, c_void_p]),
+    "gemma3_attn_check_status": (c_int, [c_void_p]),
+    "gemma3_last_device_status": (c_int, []),
+    "gemma3_strerror": (ctypes.c_char_p, [c_int]),
+    "gemma3_selftest_wait_timeout": (c_int, [ctypes.c_longlong, c_void_p]),
+}
+
+_lib = None
+
+
+class Gemma3Error(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__(f"{fn} failed: status {status} ({strerror(status)})")
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB):
+            raise RuntimeError(
+                f"{LIB} is missing: build it with transformer_attention_gb300.build.build() "
+                "(nvcc, sm_103a); there is no CPU fallback")
+        handle = ctypes.CDLL(LIB)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(handle, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = handle
+    return _lib
+
+
+def strerror(status: int) -> str:
+    return lib().gemma3_strerror(status).decode()
+
+
+def _check(fn: str, status: int) -> int:
+    if status < 0:
+        raise Gemma3Error(fn, status)
+    return status
+
+
+def _ptr(t) -> int | None:
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    if not t.is_cuda:
+        raise ValueError("tensor arguments must live on the GPU")
+    return t.data_ptr()
+
+
+def _stream(stream) -> int:
+    import torch
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _dims(B, T, D, H, H_kv, d_h):
+    return gemma3_attn_dims(B, T, D, H, H_kv, d_h)
+
+
+# ---------------------------------------------------------------- same-name wrappers
+def gemma3_layer_attn_type(layer: int, num_layers: int) -> int:
+    return _check("gemma3_layer_attn_type", lib().gemma3_layer_attn_type(layer, num_layers))
+
+
+def gemma3_layer_config(layer: int, num_layers: int, model_size: str):
+    t, w, base, scale = c_int(), c_int(), c_double(), c_double()
+    _check("gemma3_layer_config", lib().gemma3_layer_config(
+        layer, num_layers, MODEL_SIZES[model_size], ctypes.byref(t), ctypes.byref(w),
+        ctypes.byref(base), ctypes.byref(scale)))
+    return t.value, w.value, base.value, scale.value
+
+
+def gemma3_query_scale(model_size: str, D: int, H: int, d_h: int) -> float:
+    a = c_float()
+    _check("gemma3_query_scale",
+           lib().gemma3_query_scale(MODEL_SIZES[model_size], D, H, d_h, ctypes.byref(a)))
+    return a.value
+
+
+def gemma3_attn_workspace_size(B, T, D, H, H_kv, d_h) -> int:
+    n = c_size_t()
+    d = _dims(B, T, D, H, H_kv, d_h)
+    _check("gemma3_attn_workspace_size", lib().gemma3_attn_workspace_size(ctypes.byref(d),
+                                                                          ctypes.byref(n)))
+    return n.value
+
+
+def gemma3_block_attn_workspace_size(B, T, D, H, H_kv, d_h) -> int:
+    n = c_size_t()
+    d = _dims(B, T, D, H, H_kv, d_h)
+    _check("gemma3_block_attn_workspace_size",
+           lib().gemma3_block_attn_workspace_size(ctypes.byref(d), ctypes.byref(n)))
+    return n.value
+
+
+def gemma3_attn_forward(dims, x, segment_pos, pad_lens, Wq, Wkv, Wo, gamma_q, gamma_k,
+                        attn_type, window, rope_base, rope_scale, query_scale, out, workspace,
+                        workspace_bytes, stream=None):
+    d = _dims(*dims)
+    return _check("gemma3_attn_forward", lib().gemma3_attn_forward(
+        ctypes.byref(d), _ptr(x), _ptr(segment_pos), _ptr(pad_lens), _ptr(Wq), _ptr(Wkv),
+        _ptr(Wo), _ptr(gamma_q), _ptr(gamma_k), attn_type, window, rope_base, rope_scale,
+        query_scale, _ptr(out), _ptr(workspace), workspace_bytes, _stream(stream)))
+
+
+def gemma3_block_attn_forward(dims, x, x_dtype, y, segment_pos, pad_lens, Wq, Wkv, Wo, gamma_q,
+                              gamma_k, gamma_pre, gamma_post, attn_type, window, rope_base,
+                              rope_scale, query_scale, workspace, workspace_bytes, stream=None):
+    d = _dims(*dims)
+    return _check("gemma3_block_attn_forward", lib().gemma3_block_attn_forward(
+        ctypes.byref(d), _ptr(x), x_dtype, _ptr(y), _ptr(segment_pos), _ptr(pad_lens), _ptr(Wq),
+        _ptr(Wkv), _ptr(Wo), _ptr(gamma_q), _ptr(gamma_k), _ptr(gamma_pre), _ptr(gamma_post),
+        attn_type, window, rope_base, rope_scale, query_scale, _ptr(workspace), workspace_bytes,
+        _stream(stream)))
+
+
+def gemma3_linear(A, lda, W, ldw, C, ldc, M, N, K, out_dtype, max_ctas=0, stream=None):
+    return _check("gemma3_linear", lib().gemma3_linear(
+        _ptr(A), lda, _ptr(W), ldw, _ptr(C), ldc, M, N, K, out_dtype, max_ctas, _stream(stream)))
+
+
+def gemma3_qk_norm_rope(Q, ldq, K, ldk, gamma_q, gamma_k, pos, M, H, H_kv, d_h, rope_base,
+                        rope_scale, query_scale, stream=None):
+    return _check("gemma3_qk_norm_rope", lib().gemma3_qk_norm_rope(
+        _ptr(Q), ldq, _ptr(K), ldk, _ptr(gamma_q), _ptr(gamma_k), _ptr(pos), M, H, H_kv, d_h,
+        rope_base, rope_scale, query_scale, _stream(stream)))
+
+
+def gemma3_flash_attention(Q, K, V, ldkv, O, pad_lens, B, T, H, H_kv, d_h, window, stream=None):
+    return _check("gemma3_flash_attention", lib().gemma3_flash_attention(
+        _ptr(Q), _ptr(K), _ptr(V), ldkv, _ptr(O), _ptr(pad_lens), B, T, H, H_kv, d_h, window,
+        _stream(stream)))
+
+
+def gemma3_rmsnorm(x, x_dtype, gamma, u, M, D, stream=None):
+    return _check("gemma3_rmsnorm", lib().gemma3_rmsnorm(_ptr(x), x_dtype, _ptr(gamma), _ptr(u),
+                                                         M, D, _stream(stream)))
+
+
+def gemma3_postnorm_residual(a, x, x_dtype, gamma, y, M, D, stream=None):
+    return _check("gemma3_postnorm_residual", lib().gemma3_postnorm_residual(
+        _ptr(a), _ptr(x), x_dtype, _ptr(gamma), _ptr(y), M, D, _stream(stream)))
+
+
+def gemma3_attn_check_status(stream=None) -> int:
+    """Synchronises the stream and returns the library status (raises on error)."""
+    return _check("gemma3_attn_check_status", lib().gemma3_attn_check_status(_stream(stream)))
+
+
+def gemma3_last_device_status() -> int:
+    return lib().gemma3_last_device_status()
+
+
+def gemma3_selftest_wait_timeout(timeout_ns: int, stream=None) -> int:
+    """Returns the raw status (GEMMA3_ERR_TIMEOUT expected); never raises on it."""
+    return lib().gemma3_selftest_wait_timeout(timeout_ns, _stream(stream))

@@ -1,0 +1,414 @@
+// C ABI of libgemma3attn.so (declared in include/gemma3_attn.h): argument
+// validation, workspace carving, tensor-map creation and launch sequencing on
+// the caller's stream.  No entry point allocates device memory.
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include <cudaTypedefs.h>
+
+#include "../../include/gemma3_attn.h"
+#include "internal.h"
+#include "ptx.cuh"
+
+// Device status word (one per device that loads the library).
+__device__ int g3_device_status;
+
+namespace g3 {
+
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+thread_local int t_last_device_status = 0;
+
+int* status_ptr() {
+  // The symbol's device address, looked up on the current device each call
+  // (cheap; the runtime caches it per context).
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g3_device_status) != cudaSuccess) return nullptr;
+  return static_cast<int*>(p);
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
+
+int to_status(cudaError_t e) { return e == cudaSuccess ? GEMMA3_OK : GEMMA3_ERR_CUDA; }
+
+int check_device() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return GEMMA3_ERR_CUDA;
+  int major = 0, minor = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+    return GEMMA3_ERR_CUDA;
+  if (major != 10 || minor != 3) return GEMMA3_ERR_UNSUPPORTED;
+  return GEMMA3_OK;
+}
+
+int validate_dims(const gemma3_attn_dims* d) {
+  if (d == nullptr) return GEMMA3_ERR_INVALID_ARG;
+  if (d->B < 1 || d->T < 1 || d->D < 8 || d->H < 1 || d->H_kv < 1) return GEMMA3_ERR_INVALID_ARG;
+  if (d->H % d->H_kv != 0) return GEMMA3_ERR_INVALID_ARG;
+  if (d->D % 8 != 0) return GEMMA3_ERR_INVALID_ARG;
+  const int G = d->H / d->H_kv;
+  if (d->d_h != 128 && d->d_h != 256) return GEMMA3_ERR_UNSUPPORTED;
+  if (G != 1 && G != 2 && G != 4) return GEMMA3_ERR_UNSUPPORTED;
+  const long long M = static_cast<long long>(d->B) * d->T;
+  if (M >= (1LL << 31)) return GEMMA3_ERR_INVALID_ARG;
+  if (static_cast<long long>(d->H) * d->d_h > (1 << 20)) return GEMMA3_ERR_INVALID_ARG;
+  return GEMMA3_OK;
+}
+
+size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+struct AttnWs {
+  size_t q_bytes, kv_bytes, total;
+};
+
+AttnWs attn_ws(const gemma3_attn_dims* d) {
+  const size_t M = static_cast<size_t>(d->B) * d->T;
+  AttnWs w;
+  w.q_bytes = round_up(M * d->H * d->d_h * 2, 256);
+  w.kv_bytes = round_up(M * 2 * d->H_kv * d->d_h * 2, 256);
+  w.total = w.q_bytes + w.kv_bytes;
+  return w;
+}
+
+// The layer pipeline shared by the single-layer and block entry points.
+int attn_pipeline(const gemma3_attn_dims* d, const void* x, const int32_t* segment_pos,
+                  const int32_t* pad_lens, const void* Wq, const void* Wkv, const void* Wo,
+                  const void* gamma_q, const void* gamma_k, int attn_type, int window,
+                  double rope_base, double rope_scale, float query_scale, void* out,
+                  int out_dtype, uint8_t* ws, cudaStream_t s) {
+  int* st = status_ptr();
+  if (st == nullptr) return GEMMA3_ERR_CUDA;
+  const int M = d->B * d->T;
+  const int HD = d->H * d->d_h, KVD = d->H_kv * d->d_h;
+  const AttnWs w = attn_ws(d);
+  void* qbuf = ws;                // Q then Q' (fp16), then O (bf16), [M, H*d_h]
+  void* kvbuf = ws + w.q_bytes;   // [K'|V] fp16, [M, 2*H_kv*d_h]
+  cudaError_t e;
+  e = launch_linear(x, d->D, Wq, d->D, qbuf, HD, M, HD, d->D, kF16, s, st, 0);
+  if (e != cudaSuccess) return GEMMA3_ERR_CUDA;
+  e = launch_linear(x, d->D, Wkv, d->D, kvbuf, 2 * KVD, M, 2 * KVD, d->D, kF16, s, st, 0);
+  if (e != cudaSuccess) return GEMMA3_ERR_CUDA;
+  e = launch_qk_norm_rope(qbuf, HD, kvbuf, 2 * KVD, gamma_q, gamma_k, segment_pos, M, d->H,
+                          d->H_kv, d->d_h, rope_base, rope_scale, query_scale, s);
+  if (e != cudaSuccess) return GEMMA3_ERR_CUDA;
+  const int win = attn_type == GEMMA3_LOCAL_SLIDING ? window : 0;
+  e = launch_flash_attention(qbuf, kvbuf, static_cast<uint8_t*>(kvbuf) + KVD * 2, 2 * KVD, qbuf,
+                             pad_lens, d->B, d->T, d->H, d->H_kv, d->d_h, win, s, st);
+  if (e != cudaSuccess) return GEMMA3_ERR_CUDA;
+  e = launch_linear(qbuf, HD, Wo, HD, out, d->D, M, d->D, HD, out_dtype, s, st, 0);
+  return to_status(e);
+}
+
+int validate_layer_args(const gemma3_attn_dims* dims, const void* x, const int32_t* segment_pos,
+                        const void* Wq, const void* Wkv, const void* Wo, const void* gamma_q,
+                        const void* gamma_k, int attn_type, int window, double rope_base,
+                        double rope_scale, void* workspace) {
+  int rc = validate_dims(dims);
+  if (rc != GEMMA3_OK) return rc;
+  if (!x || !segment_pos || !Wq || !Wkv || !Wo || !gamma_q || !gamma_k || !workspace)
+    return GEMMA3_ERR_INVALID_ARG;
+  if (attn_type != GEMMA3_LOCAL_SLIDING && attn_type != GEMMA3_GLOBAL)
+    return GEMMA3_ERR_INVALID_ARG;
+  if (attn_type == GEMMA3_LOCAL_SLIDING && window < 1) return GEMMA3_ERR_INVALID_ARG;
+  if (!(rope_base > 0.0) || !(rope_scale > 0.0) || !std::isfinite(rope_base) ||
+      !std::isfinite(rope_scale))
+    return GEMMA3_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(Wq) || !aligned16(Wkv) || !aligned16(Wo) ||
+      !aligned16(gamma_q) || !aligned16(gamma_k) ||
+      (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return GEMMA3_ERR_MISALIGNED;
+  return check_device();
+}
+
+__global__ void wait_forever_kernel(long long timeout_ns, int* status) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    fence_barrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    // Nothing arrives on `bar`: the wait must end by its time limit.
+    const uint64_t t0 = globaltimer();
+    while (!mbar_try_wait(smem_u32(&bar), 0)) {
+      if (globaltimer() - t0 > static_cast<uint64_t>(timeout_ns)) {
+        record_error(status, kDevErrTimeoutBase + 99);
+        break;
+      }
+    }
+  }
+}
+
+}  // namespace
+
+bool encode_tiled(CUtensorMap* map, CUtensorMapDataType dt, int rank, const void* base,
+                  const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box) {
+  std::call_once(g_encode_once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void* fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  if (g_encode == nullptr) return false;
+  cuuint64_t gd[5];
+  cuuint64_t gs[4];
+  cuuint32_t bx[5], es[5];
+  for (int i = 0; i < rank; ++i) {
+    gd[i] = dims[i];
+    bx[i] = box[i];
+    es[i] = 1;
+    if (i + 1 < rank) gs[i] = strides_bytes[i];
+  }
+  const CUresult r = g_encode(map, dt, rank, const_cast<void*>(base), gd, gs, bx, es,
+                              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+int num_sms() {
+  int dev = 0, n = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  return n > 0 ? n : 1;
+}
+
+}  // namespace g3
+
+using namespace g3;
+
+extern "C" {
+
+int gemma3_layer_attn_type(int layer, int num_layers) {
+  if (num_layers < 1 || layer < 0 || layer >= num_layers) return GEMMA3_ERR_INVALID_ARG;
+  // Full tiles repeat P; the last N % 6 layers are the prefix P[:N % 6], whose
+  // index is again layer % 6 (and never reaches the global slot 5).
+  return (layer % 6 == 5) ? GEMMA3_GLOBAL : GEMMA3_LOCAL_SLIDING;
+}
+
+int gemma3_layer_config(int layer, int num_layers, int model_size, int* attn_type, int* window,
+                        double* rope_base, double* rope_scale) {
+  const int t = gemma3_layer_attn_type(layer, num_layers);
+  if (t < 0) return t;
+  if (model_size < GEMMA3_270M || model_size > GEMMA3_27B) return GEMMA3_ERR_INVALID_ARG;
+  const bool small = model_size == GEMMA3_270M || model_size == GEMMA3_1B;
+  if (attn_type) *attn_type = t;
+  if (t == GEMMA3_LOCAL_SLIDING) {
+    if (window) *window = small ? 512 : 1024;
+    if (rope_base) *rope_base = 1e4;
+    if (rope_scale) *rope_scale = 1.0;
+  } else {
+    if (window) *window = 0;
+    if (rope_base) *rope_base = 1e6;
+    if (rope_scale) *rope_scale = small ? 1.0 : 8.0;
+  }
+  return t;
+}
+
+int gemma3_query_scale(int model_size, int D, int H, int d_h, float* alpha) {
+  if (alpha == nullptr || D < 1 || H < 1 || d_h < 1) return GEMMA3_ERR_INVALID_ARG;
+  if (model_size < GEMMA3_270M || model_size > GEMMA3_27B) return GEMMA3_ERR_INVALID_ARG;
+  const double a = model_size == GEMMA3_27B ? 1.0 / std::sqrt(static_cast<double>(D) / H)
+                                            : 1.0 / std::sqrt(static_cast<double>(d_h));
+  *alpha = static_cast<float>(a);
+  return GEMMA3_OK;
+}
+
+int gemma3_attn_workspace_size(const gemma3_attn_dims* dims, size_t* bytes) {
+  const int rc = validate_dims(dims);
+  if (rc != GEMMA3_OK) return rc;
+  if (bytes == nullptr) return GEMMA3_ERR_INVALID_ARG;
+  *bytes = attn_ws(dims).total;
+  return GEMMA3_OK;
+}
+
+int gemma3_attn_forward(const gemma3_attn_dims* dims, const void* x, const int32_t* segment_pos,
+                        const int32_t* pad_lens, const void* Wq, const void* Wkv, const void* Wo,
+                        const void* gamma_q, const void* gamma_k, int attn_type, int window,
+                        double rope_base, double rope_scale, float query_scale, void* out,
+                        void* workspace, size_t workspace_bytes, void* stream) {
+  int rc = validate_layer_args(dims, x, segment_pos, Wq, Wkv, Wo, gamma_q, gamma_k, attn_type,
+                               window, rope_base, rope_scale, workspace);
+  if (rc != GEMMA3_OK) return rc;
+  if (out == nullptr) return GEMMA3_ERR_INVALID_ARG;
+  if (!aligned16(out)) return GEMMA3_ERR_MISALIGNED;
+  if (workspace_bytes < attn_ws(dims).total) return GEMMA3_ERR_WORKSPACE;
+  return attn_pipeline(dims, x, segment_pos, pad_lens, Wq, Wkv, Wo, gamma_q, gamma_k, attn_type,
+                       window, rope_base, rope_scale, query_scale, out, kBF16,
+                       static_cast<uint8_t*>(workspace), as_stream(stream));
+}
+
+int gemma3_block_attn_workspace_size(const gemma3_attn_dims* dims, size_t* bytes) {
+  const int rc = validate_dims(dims);
+  if (rc != GEMMA3_OK) return rc;
+  if (bytes == nullptr) return GEMMA3_ERR_INVALID_ARG;
+  const size_t M = static_cast<size_t>(dims->B) * dims->T;
+  *bytes = attn_ws(dims).total + round_up(M * dims->D * 2, 256) + round_up(M * dims->D * 4, 256);
+  return GEMMA3_OK;
+}
+
+int gemma3_block_attn_forward(const gemma3_attn_dims* dims, const void* x, int x_dtype,
+                              float* y, const int32_t* segment_pos, const int32_t* pad_lens,
+                              const void* Wq, const void* Wkv, const void* Wo,
+                              const void* gamma_q, const void* gamma_k, const void* gamma_pre,
+                              const void* gamma_post, int attn_type, int window,
+                              double rope_base, double rope_scale, float query_scale,
+                              void* workspace, size_t workspace_bytes, void* stream) {
+  int rc = validate_layer_args(dims, x, segment_pos, Wq, Wkv, Wo, gamma_q, gamma_k, attn_type,
+                               window, rope_base, rope_scale, workspace);
+  if (rc != GEMMA3_OK) return rc;
+  if (y == nullptr || gamma_pre == nullptr || gamma_post == nullptr) return GEMMA3_ERR_INVALID_ARG;
+  if (x_dtype != GEMMA3_BF16 && x_dtype != GEMMA3_F32) return GEMMA3_ERR_INVALID_ARG;
+  if (!aligned16(y) || !aligned16(gamma_pre) || !aligned16(gamma_post)) return GEMMA3_ERR_MISALIGNED;
+  size_t need = 0;
+  gemma3_block_attn_workspace_size(dims, &need);
+  if (workspace_bytes < need) return GEMMA3_ERR_WORKSPACE;
+  const int M = dims->B * dims->T;
+  const size_t a_ws = attn_ws(dims).total;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  void* u = ws + a_ws;                                                    // bf16 [M, D]
+  float* a = reinterpret_cast<float*>(ws + a_ws + round_up(static_cast<size_t>(M) * dims->D * 2, 256));
+  cudaStream_t s = as_stream(stream);
+  if (launch_rmsnorm_rows(x, x_dtype == GEMMA3_F32 ? kF32 : kBF16, gamma_pre, u, M, dims->D, s) !=
+      cudaSuccess)
+    return GEMMA3_ERR_CUDA;
+  rc = attn_pipeline(dims, u, segment_pos, pad_lens, Wq, Wkv, Wo, gamma_q, gamma_k, attn_type,
+                     window, rope_base, rope_scale, query_scale, a, kF32, ws, s);
+  if (rc != GEMMA3_OK) return rc;
+  return to_status(launch_postnorm_residual(a, x, x_dtype == GEMMA3_F32 ? kF32 : kBF16,
+                                            gamma_post, y, M, dims->D, s));
+}
+
+int gemma3_linear(const void* A, long lda, const void* W, long ldw, void* C, long ldc, int M,
+                  int N, int K, int out_dtype, int max_ctas, void* stream) {
+  if (!A || !W || !C || M < 0 || N < 0 || K < 1) return GEMMA3_ERR_INVALID_ARG;
+  if (out_dtype != GEMMA3_BF16 && out_dtype != GEMMA3_F16 && out_dtype != GEMMA3_F32)
+    return GEMMA3_ERR_INVALID_ARG;
+  if (lda < K || ldw < K || ldc < N) return GEMMA3_ERR_INVALID_ARG;
+  const int osz = out_dtype == GEMMA3_F32 ? 4 : 2;
+  if (!aligned16(A) || !aligned16(W) || !aligned16(C) || (lda * 2) % 16 || (ldw * 2) % 16 ||
+      (ldc * osz) % 16)
+    return GEMMA3_ERR_MISALIGNED;
+  int rc = check_device();
+  if (rc != GEMMA3_OK) return rc;
+  int* st = status_ptr();
+  if (st == nullptr) return GEMMA3_ERR_CUDA;
+  const int dt = out_dtype == GEMMA3_F32 ? kF32 : (out_dtype == GEMMA3_F16 ? kF16 : kBF16);
+  return to_status(launch_linear(A, lda, W, ldw, C, ldc, M, N, K, dt, as_stream(stream), st,
+                                 max_ctas));
+}
+
+int gemma3_qk_norm_rope(void* Q, long ldq, void* K, long ldk, const void* gamma_q,
+                        const void* gamma_k, const int32_t* pos, int M, int H, int H_kv,
+                        int d_h, double rope_base, double rope_scale, float query_scale,
+                        void* stream) {
+  if (!Q || !K || !gamma_q || !gamma_k || !pos || M < 0 || H < 1 || H_kv < 1)
+    return GEMMA3_ERR_INVALID_ARG;
+  if (d_h != 128 && d_h != 256) return GEMMA3_ERR_UNSUPPORTED;
+  if (ldq < static_cast<long>(H) * d_h || ldk < static_cast<long>(H_kv) * d_h)
+    return GEMMA3_ERR_INVALID_ARG;
+  if (!(rope_base > 0.0) || !(rope_scale > 0.0)) return GEMMA3_ERR_INVALID_ARG;
+  if (!aligned16(Q) || !aligned16(K) || (ldq * 2) % 16 || (ldk * 2) % 16 || !aligned16(gamma_q) ||
+      !aligned16(gamma_k))
+    return GEMMA3_ERR_MISALIGNED;
+  int rc = check_device();
+  if (rc != GEMMA3_OK) return rc;
+  return to_status(launch_qk_norm_rope(Q, ldq, K, ldk, gamma_q, gamma_k, pos, M, H, H_kv, d_h,
+                                       rope_base, rope_scale, query_scale, as_stream(stream)));
+}
+
+int gemma3_flash_attention(const void* Q, const void* K, const void* V, long ldkv, void* O,
+                           const int32_t* pad_lens, int B, int T, int H, int H_kv, int d_h,
+                           int window, void* stream) {
+  if (!Q || !K || !V || !O || B < 1 || T < 1 || H < 1 || H_kv < 1 || H % H_kv)
+    return GEMMA3_ERR_INVALID_ARG;
+  const int G = H / H_kv;
+  if ((d_h != 128 && d_h != 256) || (G != 1 && G != 2 && G != 4)) return GEMMA3_ERR_UNSUPPORTED;
+  if (ldkv < static_cast<long>(H_kv) * d_h) return GEMMA3_ERR_INVALID_ARG;
+  if (static_cast<long long>(B) * T >= (1LL << 31)) return GEMMA3_ERR_INVALID_ARG;
+  if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O) || (ldkv * 2) % 16)
+    return GEMMA3_ERR_MISALIGNED;
+  int rc = check_device();
+  if (rc != GEMMA3_OK) return rc;
+  int* st = status_ptr();
+  if (st == nullptr) return GEMMA3_ERR_CUDA;
+  return to_status(launch_flash_attention(Q, K, V, ldkv, O, pad_lens, B, T, H, H_kv, d_h,
+                                          window > 0 ? window : 0, as_stream(stream), st));
+}
+
+int gemma3_rmsnorm(const void* x, int x_dtype, const void* gamma, void* u, int M, int D,
+                   void* stream) {
+  if (!x || !gamma || !u || M < 0 || D < 4 || D % 4) return GEMMA3_ERR_INVALID_ARG;
+  if (x_dtype != GEMMA3_BF16 && x_dtype != GEMMA3_F32) return GEMMA3_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(gamma) || !aligned16(u)) return GEMMA3_ERR_MISALIGNED;
+  int rc = check_device();
+  if (rc != GEMMA3_OK) return rc;
+  return to_status(launch_rmsnorm_rows(x, x_dtype == GEMMA3_F32 ? kF32 : kBF16, gamma, u, M, D,
+                                       as_stream(stream)));
+}
+
+int gemma3_postnorm_residual(const float* a, const void* x, int x_dtype, const void* gamma,
+                             float* y, int M, int D, void* stream) {
+  if (!a || !x || !gamma || !y || M < 0 || D < 4 || D % 4) return GEMMA3_ERR_INVALID_ARG;
+  if (x_dtype != GEMMA3_BF16 && x_dtype != GEMMA3_F32) return GEMMA3_ERR_INVALID_ARG;
+  if (!aligned16(a) || !aligned16(x) || !aligned16(gamma) || !aligned16(y))
+    return GEMMA3_ERR_MISALIGNED;
+  int rc = check_device();
+  if (rc != GEMMA3_OK) return rc;
+  return to_status(launch_postnorm_residual(a, x, x_dtype == GEMMA3_F32 ? kF32 : kBF16, gamma, y,
+                                            M, D, as_stream(stream)));
+}
+
+int gemma3_attn_check_status(void* stream) {
+  cudaStream_t s = as_stream(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return GEMMA3_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g3_device_status, sizeof(int)) != cudaSuccess)
+    return GEMMA3_ERR_CUDA;
+  t_last_device_status = v;
+  if (v != 0) {
+    const int zero = 0;
+    if (cudaMemcpyToSymbol(g3_device_status, &zero, sizeof(int)) != cudaSuccess)
+      return GEMMA3_ERR_CUDA;
+    return GEMMA3_ERR_TIMEOUT;
+  }
+  return GEMMA3_OK;
+}
+
+int gemma3_last_device_status(void) { return t_last_device_status; }
+
+const char* gemma3_strerror(int status) {
+  switch (status) {
+    case GEMMA3_OK: return "ok";
+    case GEMMA3_ERR_INVALID_ARG: return "invalid argument";
+    case GEMMA3_ERR_MISALIGNED: return "pointer or stride not 16-byte aligned";
+    case GEMMA3_ERR_UNSUPPORTED: return "unsupported shape or device";
+    case GEMMA3_ERR_CUDA: return "CUDA error";
+    case GEMMA3_ERR_TIMEOUT: return "kernel gave up on a bounded wait";
+    case GEMMA3_ERR_WORKSPACE: return "workspace too small";
+    default: return "unknown status";
+  }
+}
+
+int gemma3_selftest_wait_timeout(long long timeout_ns, void* stream) {
+  if (timeout_ns < 1000000LL || timeout_ns > 5000000000LL) return GEMMA3_ERR_INVALID_ARG;
+  int rc = check_device();
+  if (rc != GEMMA3_OK) return rc;
+  int* st = status_ptr();
+  if (st == nullptr) return GEMMA3_ERR_CUDA;
+  cudaStream_t s = as_stream(stream);
+  wait_forever_kernel<<<1, 32, 0, s>>>(timeout_ns, st);
+  if (cudaGetLastError() != cudaSuccess) return GEMMA3_ERR_CUDA;
+  return gemma3_attn_check_status(stream);
+}
+
+}  // extern "C"

@@ -1,0 +1,420 @@
+// Flash-style attention forward on tcgen05 tensor cores.
+//
+// Computes, per query row t of batch row b and query head h (kv head
+// j = h / G, "Gemma 3 Attention Block", How it works: Scores and the GQA
+// reshape):
+//   logits[s] = sum_c Q'[b,t,h,c] K'[b,s,j,c]          (query scale already in Q')
+//   keep s iff s <= t, s < valid_b and (global or s > t - W)   (causal+padding
+//        mask times the sliding mask; blocked logits contribute exp(.) = 0)
+//   O[b,t,h,:] = softmax_s(logits) @ V[b,:,j,:]
+// with an fp32 online softmax.  Rows t >= valid_b are written as zeros.
+//
+// One CTA owns 128 query rows: TQ = 128/G consecutive tokens x the G query
+// heads that share kv head j, so every K/V tile loaded from memory feeds all G
+// heads of its group.  KV tiles of 128 keys outside the causal band / window
+// are never visited (local layers cost O(T*W)); only tiles that straddle the
+// band edge, the window edge or the valid length apply an element mask.
+//
+//   warp 0      TMA producer: Q once (4-D box over [B,T,H,d_h]), then K_i, V_i
+//   warp 1      TMEM allocation + single-thread MMA issue:
+//                 S_i = Q K_i^T   (SS, M=128 N=128, K=d_h)  -> TMEM S[i%2]
+//                 O  += P_i V_i   (TS: P_i read from TMEM,   M=128 N=d_h K=128)
+//   warps 4-7   softmax: one thread per query row (its TMEM lane); P_i is
+//               written back as fp16 over S[i%2]; O is rescaled in TMEM only
+//               when the running max grows by more than 2^8; final 1/l
+//               normalisation and bf16 store.
+// TMEM: S[0] cols 0-127, S[1] cols 128-255, O cols 256..256+d_h.
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace g3 {
+
+namespace {
+
+constexpr int THREADS = 256;
+constexpr int BM = 128;   // query rows per CTA
+constexpr int BN = 128;   // keys per KV tile
+constexpr uint32_t CHUNK = 128 * 128;  // one 128-row x 64-element (128 B) swizzled chunk
+constexpr uint32_t O_COL = 256;
+constexpr float LOG2E = 1.4426950408889634f;
+constexpr float RESCALE_THRESHOLD = 8.0f;  // log2 units
+
+enum : int {
+  kSiteQ = 11, kSiteKEmpty, kSiteVEmpty, kSiteKFull, kSiteODone, kSitePFull, kSiteVFull,
+  kSiteSFull, kSiteORescale, kSiteOFinal
+};
+
+template <int DH, int G>
+struct Cfg {
+  static constexpr int TQ = BM / G;
+  static constexpr int NCH = DH / 64;
+  static constexpr int KS = (DH == 256) ? 1 : 2;   // K ring depth
+  static constexpr int VS = KS;                     // V ring depth
+  static constexpr uint32_t Q_BYTES = BM * DH * 2;
+  static constexpr uint32_t KV_BYTES = BN * DH * 2;
+  static constexpr uint32_t SMEM = Q_BYTES + (KS + VS) * KV_BYTES + 1024;
+};
+
+template <int DH, int G>
+__global__ void __launch_bounds__(THREADS, 1)
+    attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                    const __grid_constant__ CUtensorMap tmV, __nv_bfloat16* __restrict__ O,
+                    const int32_t* __restrict__ pad_lens, int B, int T, int H, int H_kv,
+                    int window, int num_q_tiles, int* status) {
+  using C = Cfg<DH, G>;
+  // After a CTA of this or an earlier launch gave up, the rest do no work.
+  if (*reinterpret_cast<volatile int*>(status) != 0) return;
+  // Work item: heaviest query tiles first (longest-processing-time order for
+  // causal layers), all (b, j) of a query tile next to each other.
+  int idx = blockIdx.x;
+  const int j = idx % H_kv;
+  idx /= H_kv;
+  const int b = idx % B;
+  idx /= B;
+  const int qt = num_q_tiles - 1 - idx;
+  const int t0 = qt * C::TQ;
+  const int valid = T - (pad_lens != nullptr ? pad_lens[b] : 0);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (t0 >= valid) {
+    // The whole tile is padding: its output rows are zero.
+    const int rows = min(C::TQ, T - t0);
+    const int vecs = rows * G * (DH / 8);
+    for (int v = threadIdx.x; v < vecs; v += THREADS) {
+      const int e = v * 8;
+      const int c = e % DH, rg = e / DH;
+      const int g = rg % G, i = rg / G;
+      *reinterpret_cast<uint4*>(O + ((static_cast<size_t>(b) * T + t0 + i) * H + j * G + g) * DH +
+                                c) = make_uint4(0, 0, 0, 0);
+    }
+    return;
+  }
+  const int t_last = min(t0 + C::TQ, valid) - 1;
+  const int s_lo = window > 0 ? max(0, t0 - window + 1) : 0;
+  const int tile_lo = s_lo / BN;
+  const int n_tiles = t_last / BN - tile_lo + 1;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* sQ = smem;
+  uint8_t* sK = smem + C::Q_BYTES;                    // KS stages
+  uint8_t* sV = sK + C::KS * C::KV_BYTES;             // VS stages
+  __shared__ __align__(8) uint64_t q_full, k_full[C::KS], k_empty[C::KS], v_full[C::VS],
+      v_empty[C::VS], s_full[2], p_full[2], o_done, o_final, drain;
+  __shared__ uint32_t tmem_sh;
+  __shared__ int abort_flag;
+
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&q_full), 1);
+    for (int s = 0; s < C::KS; ++s) {
+      mbar_init(smem_u32(&k_full[s]), 1);
+      mbar_init(smem_u32(&k_empty[s]), 1);
+    }
+    for (int s = 0; s < C::VS; ++s) {
+      mbar_init(smem_u32(&v_full[s]), 1);
+      mbar_init(smem_u32(&v_empty[s]), 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(smem_u32(&s_full[s]), 1);
+      mbar_init(smem_u32(&p_full[s]), 4);
+    }
+    mbar_init(smem_u32(&o_done), 1);
+    mbar_init(smem_u32(&o_final), 1);
+    mbar_init(smem_u32(&drain), 1);
+    abort_flag = 0;
+    fence_barrier_init();
+    tma_prefetch_desc(&tmQ);
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&tmem_sh), 512);
+    tmem_relinquish();
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = tmem_sh;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- producer
+      const uint32_t qb = smem_u32(&q_full);
+      mbar_arrive_expect_tx(qb, C::Q_BYTES);
+      for (int ch = 0; ch < C::NCH; ++ch)
+        tma_load_4d(smem_u32(sQ + ch * CHUNK), &tmQ, qb, ch * 64, j * G, t0, b);
+      int kfill[C::KS] = {}, vfill[C::VS] = {};
+      for (int i = 0; i < n_tiles; ++i) {
+        const int s0 = (tile_lo + i) * BN;
+        const int ks = i % C::KS;
+        if (!mbar_wait(smem_u32(&k_empty[ks]), ((i / C::KS) & 1) ^ 1, &abort_flag, status,
+                       kSiteKEmpty))
+          break;
+        const uint32_t kb = smem_u32(&k_full[ks]);
+        mbar_arrive_expect_tx(kb, C::KV_BYTES);
+        for (int ch = 0; ch < C::NCH; ++ch)
+          tma_load_3d(smem_u32(sK + ks * C::KV_BYTES + ch * CHUNK), &tmK, kb, j * DH + ch * 64, s0,
+                      b);
+        ++kfill[ks];
+        const int vs = i % C::VS;
+        if (!mbar_wait(smem_u32(&v_empty[vs]), ((i / C::VS) & 1) ^ 1, &abort_flag, status,
+                       kSiteVEmpty))
+          break;
+        const uint32_t vb = smem_u32(&v_full[vs]);
+        mbar_arrive_expect_tx(vb, C::KV_BYTES);
+        for (int ch = 0; ch < C::NCH; ++ch)
+          tma_load_3d(smem_u32(sV + vs * C::KV_BYTES + ch * CHUNK), &tmV, vb, j * DH + ch * 64, s0,
+                      b);
+        ++vfill[vs];
+      }
+      mbar_wait_drain(qb, 0);
+      for (int s = 0; s < C::KS; ++s)
+        if (kfill[s] > 0) mbar_wait_drain(smem_u32(&k_full[s]), (kfill[s] - 1) & 1);
+      for (int s = 0; s < C::VS; ++s)
+        if (vfill[s] > 0) mbar_wait_drain(smem_u32(&v_full[s]), (vfill[s] - 1) & 1);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------- MMA issuer
+      constexpr uint32_t idesc_qk = idesc_f16(BM, BN, /*f16*/ 0, 0, 0);
+      constexpr uint32_t idesc_pv = idesc_f16(BM, DH, /*f16*/ 0, 0, /*B MN-major*/ 1);
+      const uint32_t q_addr = smem_u32(sQ);
+      auto issue_pv = [&](int jt) -> bool {
+        if (!mbar_wait(smem_u32(&p_full[jt & 1]), (jt >> 1) & 1, &abort_flag, status, kSitePFull))
+          return false;
+        const int vs = jt % C::VS;
+        if (!mbar_wait(smem_u32(&v_full[vs]), (jt / C::VS) & 1, &abort_flag, status, kSiteVFull))
+          return false;
+        tc_fence_after();
+        const uint32_t p_tmem = tbase + (jt & 1) * BN;
+        const uint32_t v_addr = smem_u32(sV + vs * C::KV_BYTES);
+#pragma unroll
+        for (int k = 0; k < BN / 16; ++k)
+          mma_ts(tbase + O_COL, p_tmem + k * 8, sdesc_sw128(v_addr + k * 2048, CHUNK, 1024),
+                 idesc_pv, (jt > 0 || k > 0) ? 1u : 0u);
+        mma_commit(smem_u32(&v_empty[vs]));
+        mma_commit(smem_u32(&o_done));
+        return true;
+      };
+      bool ok = mbar_wait(smem_u32(&q_full), 0, &abort_flag, status, kSiteQ);
+      for (int i = 0; ok && i < n_tiles; ++i) {
+        const int ks = i % C::KS;
+        if (!mbar_wait(smem_u32(&k_full[ks]), (i / C::KS) & 1, &abort_flag, status, kSiteKFull)) {
+          ok = false;
+          break;
+        }
+        // S[i%2] holds P_{i-2} until PV_{i-2} has read it.
+        if (i >= 2 &&
+            !mbar_wait(smem_u32(&o_done), (i - 2) & 1, &abort_flag, status, kSiteODone)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t s_tmem = tbase + (i & 1) * BN;
+        const uint32_t k_addr = smem_u32(sK + ks * C::KV_BYTES);
+#pragma unroll
+        for (int k = 0; k < DH / 16; ++k) {
+          const uint32_t off = (k >> 2) * CHUNK + (k & 3) * 32;
+          mma_ss(s_tmem, sdesc_sw128(q_addr + off, 16, 1024), sdesc_sw128(k_addr + off, 16, 1024),
+                 idesc_qk, k > 0 ? 1u : 0u);
+        }
+        mma_commit(smem_u32(&k_empty[ks]));
+        mma_commit(smem_u32(&s_full[i & 1]));
+        if (i >= 1 && !issue_pv(i - 1)) {
+          ok = false;
+          break;
+        }
+      }
+      // o_final: the whole O accumulation is complete (o_done alone cannot say
+      // so unambiguously, the final reader may be two phases behind it).
+      if (ok && issue_pv(n_tiles - 1)) mma_commit(smem_u32(&o_final));
+      mma_commit(smem_u32(&drain));
+      mbar_wait_drain(smem_u32(&drain), 0);
+    }
+  } else if (warp >= 4) {
+    // ---------------- softmax + epilogue (one thread per query row)
+    const int q = warp - 4;
+    const int r = q * 32 + lane;
+    const int i_tok = r / G, g = r % G;
+    const int t = t0 + i_tok;
+    const int h = j * G + g;
+    const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
+    float m_used = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int i = 0; i < n_tiles; ++i) {
+      const int sb = i & 1;
+      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&s_full[sb]), (i >> 1) & 1, &abort_flag,
+                                             status, kSiteSFull));
+      if (!ok) break;
+      tc_fence_after();
+      float s[BN];
+#pragma unroll
+      for (int c4 = 0; c4 < BN / 32; ++c4) {
+        uint32_t rr[32];
+        tmem_ld32(tbase + lane_off + sb * BN + c4 * 32, rr);
+        tmem_ld_wait();
+#pragma unroll
+        for (int e = 0; e < 32; ++e) s[c4 * 32 + e] = __uint_as_float(rr[e]);
+      }
+      const int s0 = (tile_lo + i) * BN;
+      const bool need_mask = (s0 + BN - 1 > t0) || (s0 + BN > valid) ||
+                             (window > 0 && s0 <= t_last - window);
+      if (need_mask) {
+#pragma unroll
+        for (int c = 0; c < BN; ++c) {
+          const int kv = s0 + c;
+          const bool keep = kv <= t && kv < valid && (window == 0 || kv > t - window);
+          if (!keep) s[c] = -INFINITY;
+        }
+      }
+      float mx = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < BN; ++c) mx = fmaxf(mx, s[c]);
+      mx *= LOG2E;
+      const bool grow = mx > m_used + RESCALE_THRESHOLD;
+      if (__any_sync(0xffffffffu, grow)) {
+        const float m_new = grow ? mx : m_used;
+        const float factor = (m_new == m_used) ? 1.f : exp2f(m_used - m_new);
+        if (i > 0) {
+          // O holds PV_0..PV_{i-1}; rescale it once PV_{i-1} has landed.
+          ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&o_done), (i - 1) & 1, &abort_flag,
+                                                 status, kSiteORescale));
+          if (!ok) break;
+          tc_fence_after();
+#pragma unroll 1
+          for (int c = 0; c < DH / 32; ++c) {
+            uint32_t rr[32];
+            const uint32_t ta = tbase + lane_off + O_COL + c * 32;
+            tmem_ld32(ta, rr);
+            tmem_ld_wait();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) rr[e] = __float_as_uint(__uint_as_float(rr[e]) * factor);
+            tmem_st32(ta, rr);
+          }
+          tmem_st_wait();
+        }
+        l *= factor;
+        m_used = m_new;
+      }
+      const float mref = (m_used == -INFINITY) ? 0.f : m_used;
+      float sum = 0.f;
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        uint32_t p[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const float p0 = exp2f(fmaf(s[half * 64 + 2 * e], LOG2E, -mref));
+          const float p1 = exp2f(fmaf(s[half * 64 + 2 * e + 1], LOG2E, -mref));
+          sum += p0 + p1;
+          p[e] = pack_half2(p0, p1);
+        }
+        tmem_st32(tbase + lane_off + sb * BN + half * 32, p);
+      }
+      l += sum;
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&p_full[sb]));
+    }
+    if (ok) {
+      ok = __all_sync(0xffffffffu,
+                      mbar_wait(smem_u32(&o_final), 0, &abort_flag, status, kSiteOFinal));
+    }
+    if (ok) {
+      tc_fence_after();
+      const bool row_valid = t < valid;
+      const float inv_l = row_valid ? 1.f / l : 0.f;
+      __nv_bfloat16* dst = O + ((static_cast<size_t>(b) * T + t) * H + h) * DH;
+#pragma unroll 1
+      for (int c = 0; c < DH / 32; ++c) {
+        uint32_t rr[32];
+        tmem_ld32(tbase + lane_off + O_COL + c * 32, rr);
+        tmem_ld_wait();
+        if (t < T) {
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            uint4 w;
+            if (row_valid) {
+              w.x = pack_bf162(__uint_as_float(rr[8 * v + 0]) * inv_l,
+                               __uint_as_float(rr[8 * v + 1]) * inv_l);
+              w.y = pack_bf162(__uint_as_float(rr[8 * v + 2]) * inv_l,
+                               __uint_as_float(rr[8 * v + 3]) * inv_l);
+              w.z = pack_bf162(__uint_as_float(rr[8 * v + 4]) * inv_l,
+                               __uint_as_float(rr[8 * v + 5]) * inv_l);
+              w.w = pack_bf162(__uint_as_float(rr[8 * v + 6]) * inv_l,
+                               __uint_as_float(rr[8 * v + 7]) * inv_l);
+            } else {
+              w = make_uint4(0, 0, 0, 0);
+            }
+            reinterpret_cast<uint4*>(dst + c * 32)[v] = w;
+          }
+        }
+      }
+    }
+  }
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tbase, 512);
+  }
+}
+
+template <int DH, int G>
+cudaError_t launch_cfg(const void* Q, const void* K, const void* V, long ldkv, void* O,
+                       const int32_t* pad_lens, int B, int T, int H, int H_kv, int window,
+                       cudaStream_t stream, int* status) {
+  using C = Cfg<DH, G>;
+  CUtensorMap tq, tk, tv;
+  // Q' [B, T, H, d_h]: box {64 of d_h, the G heads of one group, TQ tokens, 1}.
+  const uint64_t qdims[4] = {static_cast<uint64_t>(DH), static_cast<uint64_t>(H),
+                             static_cast<uint64_t>(T), static_cast<uint64_t>(B)};
+  const uint64_t qstr[3] = {static_cast<uint64_t>(DH) * 2, static_cast<uint64_t>(H) * DH * 2,
+                            static_cast<uint64_t>(T) * H * DH * 2};
+  const uint32_t qbox[4] = {64, static_cast<uint32_t>(G), static_cast<uint32_t>(C::TQ), 1};
+  // K', V: rows of a [B*T, ldkv] buffer; box {64 of d_h, 128 keys, 1}.
+  const uint64_t kdims[3] = {static_cast<uint64_t>(H_kv) * DH, static_cast<uint64_t>(T),
+                             static_cast<uint64_t>(B)};
+  const uint64_t kstr[2] = {static_cast<uint64_t>(ldkv) * 2, static_cast<uint64_t>(T) * ldkv * 2};
+  const uint32_t kbox[3] = {64, BN, 1};
+  if (!encode_tiled(&tq, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4, Q, qdims, qstr, qbox) ||
+      !encode_tiled(&tk, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, K, kdims, kstr, kbox) ||
+      !encode_tiled(&tv, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, V, kdims, kstr, kbox))
+    return cudaErrorInvalidValue;
+  auto kern = attn_fwd_kernel<DH, G>;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  const int num_q_tiles = (T + C::TQ - 1) / C::TQ;
+  const long grid = static_cast<long>(num_q_tiles) * B * H_kv;
+  if (grid > 0x7fffffffL) return cudaErrorInvalidValue;
+  kern<<<static_cast<unsigned>(grid), THREADS, C::SMEM, stream>>>(
+      tq, tk, tv, static_cast<__nv_bfloat16*>(O), pad_lens, B, T, H, H_kv, window, num_q_tiles,
+      status);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_flash_attention(const void* Q, const void* K, const void* V, long ldkv,
+                                   void* O, const int32_t* pad_lens, int B, int T, int H,
+                                   int H_kv, int d_h, int window, cudaStream_t stream,
+                                   int* status) {
+  if (B <= 0 || T <= 0) return cudaSuccess;
+  const int G = H / H_kv;
+#define G3_ATTN_CASE(DH_, G_)                                                                   \
+  if (d_h == DH_ && G == G_)                                                                    \
+    return launch_cfg<DH_, G_>(Q, K, V, ldkv, O, pad_lens, B, T, H, H_kv, window, stream, status);
+  G3_ATTN_CASE(256, 1)
+  G3_ATTN_CASE(256, 2)
+  G3_ATTN_CASE(256, 4)
+  G3_ATTN_CASE(128, 1)
+  G3_ATTN_CASE(128, 2)
+  G3_ATTN_CASE(128, 4)
+#undef G3_ATTN_CASE
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace g3

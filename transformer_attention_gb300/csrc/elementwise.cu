@@ -1,0 +1,262 @@
+// Memory-bound kernels of the attention block.
+//
+// qk_norm_rope: the fused prologue between the projections and attention
+//   ("QK-Norm", How it works; "Gemma 3 Attention Block", How it works:
+//   QK-norm, then RoPE, then scale).  For every token and every query / key
+//   head vector x in R^{d_h}:
+//     x <- x / sqrt(mean(x^2) + 1e-6) * (1 + gamma)     (gamma_q or gamma_k)
+//     x <- RoPE(x; pos, base, scale)                     (pairs (c, c + d_h/2),
+//          angle (pos / scale) * base^(-2c/d_h))
+//     Q only: x <- x * query_scale
+//   One warp per token, d_h/8 lanes per head vector, 8 fp16 elements (one
+//   16-byte load) per lane; the RMS is a shuffle reduction over those lanes
+//   and the RoPE partner element sits d_h/16 lanes away.  The rotation angle
+//   is formed as an fp32 double-float (exact two-product of pos and the split
+//   frequency) and reduced modulo 2*pi by Cody-Waite with a three-part 2*pi,
+//   so positions up to 2^24 keep ~1e-6 rad of angle error.  Rows are updated
+//   in place.
+//
+// rmsnorm_rows / postnorm_residual: the D-axis norms of the block sandwich
+//   ("Full Gemma 3 Block", How it works: a = Attn(RMSNorm_pre(x));
+//   a <- RMSNorm_post(a); h = x + a), one warp per row.
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace g3 {
+
+namespace {
+
+constexpr double kTwoPi = 6.283185307179586476925286766559;
+constexpr float kTwoPiHi = static_cast<float>(kTwoPi);
+constexpr float kTwoPiMid = static_cast<float>(kTwoPi - static_cast<double>(kTwoPiHi));
+constexpr float kInvTwoPi = static_cast<float>(1.0 / kTwoPi);
+constexpr float kEps = 1e-6f;
+
+template <int DH>
+__global__ void __launch_bounds__(256)
+    qk_norm_rope_kernel(__half* __restrict__ Q, long ldq, __half* __restrict__ K, long ldk,
+                        const __nv_bfloat16* __restrict__ gamma_q,
+                        const __nv_bfloat16* __restrict__ gamma_k, const int32_t* __restrict__ pos,
+                        int M, int H, int H_kv, double rope_base, double inv_scale,
+                        float query_scale) {
+  constexpr int LPV = DH / 8;      // lanes per head vector
+  constexpr int VPW = 32 / LPV;    // head vectors per warp step
+  constexpr int HALF = LPV / 2;    // lane distance of the RoPE partner
+  const int lane = threadIdx.x & 31;
+  const int sub = lane / LPV, ll = lane % LPV;
+  const bool second_half = ll >= HALF;
+  const int c0 = (ll % HALF) * 8;  // first rotation pair index of this lane
+
+  // Per-lane constants: split frequencies (inv_scale * base^(-2c/d_h) as
+  // hi + lo fp32), and (1 + gamma) for Q and K.
+  float f_hi[8], f_lo[8], gq[8], gk[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    const double f = inv_scale * pow(rope_base, -2.0 * (c0 + e) / DH);
+    f_hi[e] = static_cast<float>(f);
+    f_lo[e] = static_cast<float>(f - static_cast<double>(f_hi[e]));
+    gq[e] = 1.f + __bfloat162float(gamma_q[ll * 8 + e]);
+    gk[e] = 1.f + __bfloat162float(gamma_k[ll * 8 + e]);
+  }
+
+  const int warps_total = gridDim.x * (blockDim.x >> 5);
+  const int nvec = H + H_kv;
+  for (int m = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); m < M; m += warps_total) {
+    const float p = static_cast<float>(pos[m]);
+    float cs[8], sn[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const float a_hi = p * f_hi[e];
+      const float a_err = fmaf(p, f_hi[e], -a_hi);     // exact residual of the product
+      const float a_lo = fmaf(p, f_lo[e], a_err);
+      const float k = rintf(a_hi * kInvTwoPi);
+      float r = fmaf(-k, kTwoPiHi, a_hi);
+      r = fmaf(-k, kTwoPiMid, r);
+      r += a_lo;
+      sincosf(r, &sn[e], &cs[e]);
+    }
+    for (int base = 0; base < nvec; base += VPW) {
+      const int hv = base + sub;
+      const bool active = hv < nvec;
+      const bool is_q = hv < H;
+      __half* ptr = is_q ? Q + static_cast<long>(m) * ldq + hv * DH
+                         : K + static_cast<long>(m) * ldk + (hv - H) * DH;
+      ptr += ll * 8;
+      float x[8];
+      if (active) {
+        const uint4 raw = *reinterpret_cast<const uint4*>(ptr);
+        const __half2* h2 = reinterpret_cast<const __half2*>(&raw);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 f = __half22float2(h2[e]);
+          x[2 * e] = f.x;
+          x[2 * e + 1] = f.y;
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) x[e] = 0.f;
+      }
+      float ss = 0.f;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) ss = fmaf(x[e], x[e], ss);
+#pragma unroll
+      for (int off = HALF; off >= 1; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+      const float rs = rsqrtf(ss * (1.f / DH) + kEps);
+      float y[8], o[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) y[e] = x[e] * rs * (is_q ? gq[e] : gk[e]);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) o[e] = __shfl_xor_sync(0xffffffffu, y[e], HALF);
+      const float sc = is_q ? query_scale : 1.f;
+      uint4 w;
+      uint32_t* wp = reinterpret_cast<uint32_t*>(&w);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        float r0, r1;
+        if (!second_half) {  // y is x1 (first half), o is x2
+          r0 = y[2 * e] * cs[2 * e] - o[2 * e] * sn[2 * e];
+          r1 = y[2 * e + 1] * cs[2 * e + 1] - o[2 * e + 1] * sn[2 * e + 1];
+        } else {             // y is x2, o is x1
+          r0 = y[2 * e] * cs[2 * e] + o[2 * e] * sn[2 * e];
+          r1 = y[2 * e + 1] * cs[2 * e + 1] + o[2 * e + 1] * sn[2 * e + 1];
+        }
+        wp[e] = pack_half2(r0 * sc, r1 * sc);
+      }
+      if (active) *reinterpret_cast<uint4*>(ptr) = w;
+    }
+  }
+}
+
+template <typename T>
+__device__ __forceinline__ float4 load4(const T* p);
+template <> __device__ __forceinline__ float4 load4<float>(const float* p) {
+  return *reinterpret_cast<const float4*>(p);
+}
+template <> __device__ __forceinline__ float4 load4<__nv_bfloat16>(const __nv_bfloat16* p) {
+  const uint2 raw = *reinterpret_cast<const uint2*>(p);
+  const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.x));
+  const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.y));
+  return make_float4(a.x, a.y, b.x, b.y);
+}
+
+// u = RMSNorm(x) * (1 + gamma) -> bf16, one warp per row, D % 4 == 0.
+template <typename T>
+__global__ void __launch_bounds__(256)
+    rmsnorm_rows_kernel(const T* __restrict__ x, const __nv_bfloat16* __restrict__ gamma,
+                        __nv_bfloat16* __restrict__ u, int M, int D) {
+  const int lane = threadIdx.x & 31;
+  const int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (row >= M) return;
+  const T* xr = x + static_cast<long>(row) * D;
+  float ss = 0.f;
+  for (int c = lane * 4; c < D; c += 128) {
+    const float4 v = load4<T>(xr + c);
+    ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+  }
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+  const float rs = rsqrtf(ss / D + kEps);
+  __nv_bfloat16* ur = u + static_cast<long>(row) * D;
+  for (int c = lane * 4; c < D; c += 128) {
+    const float4 v = load4<T>(xr + c);
+    const float4 g = load4<__nv_bfloat16>(gamma + c);
+    uint2 w;
+    w.x = pack_bf162(v.x * rs * (1.f + g.x), v.y * rs * (1.f + g.y));
+    w.y = pack_bf162(v.z * rs * (1.f + g.z), v.w * rs * (1.f + g.w));
+    *reinterpret_cast<uint2*>(ur + c) = w;
+  }
+}
+
+// y = x + RMSNorm(a) * (1 + gamma), one warp per row; y may alias x (f32).
+template <typename T>
+__global__ void __launch_bounds__(256)
+    postnorm_residual_kernel(const float* __restrict__ a, const T* x,
+                             const __nv_bfloat16* __restrict__ gamma, float* y, int M, int D) {
+  const int lane = threadIdx.x & 31;
+  const int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (row >= M) return;
+  const float* ar = a + static_cast<long>(row) * D;
+  float ss = 0.f;
+  for (int c = lane * 4; c < D; c += 128) {
+    const float4 v = *reinterpret_cast<const float4*>(ar + c);
+    ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+  }
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+  const float rs = rsqrtf(ss / D + kEps);
+  const T* xr = x + static_cast<long>(row) * D;
+  float* yr = y + static_cast<long>(row) * D;
+  for (int c = lane * 4; c < D; c += 128) {
+    const float4 v = *reinterpret_cast<const float4*>(ar + c);
+    const float4 g = load4<__nv_bfloat16>(gamma + c);
+    const float4 xv = load4<T>(xr + c);
+    float4 o;
+    o.x = xv.x + v.x * rs * (1.f + g.x);
+    o.y = xv.y + v.y * rs * (1.f + g.y);
+    o.z = xv.z + v.z * rs * (1.f + g.z);
+    o.w = xv.w + v.w * rs * (1.f + g.w);
+    *reinterpret_cast<float4*>(yr + c) = o;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_qk_norm_rope(void* Q, long ldq, void* K, long ldk, const void* gamma_q,
+                                const void* gamma_k, const int32_t* pos, int M, int H, int H_kv,
+                                int d_h, double rope_base, double rope_scale, float query_scale,
+                                cudaStream_t stream) {
+  if (M <= 0) return cudaSuccess;
+  const int warps_per_block = 8;
+  long blocks = (M + warps_per_block - 1) / warps_per_block;
+  const long cap = static_cast<long>(num_sms()) * 16;
+  if (blocks > cap) blocks = cap;
+  const double inv_scale = 1.0 / rope_scale;
+  auto q = static_cast<__half*>(Q);
+  auto k = static_cast<__half*>(K);
+  auto gq = static_cast<const __nv_bfloat16*>(gamma_q);
+  auto gk = static_cast<const __nv_bfloat16*>(gamma_k);
+  if (d_h == 256)
+    qk_norm_rope_kernel<256><<<blocks, 256, 0, stream>>>(q, ldq, k, ldk, gq, gk, pos, M, H, H_kv,
+                                                         rope_base, inv_scale, query_scale);
+  else if (d_h == 128)
+    qk_norm_rope_kernel<128><<<blocks, 256, 0, stream>>>(q, ldq, k, ldk, gq, gk, pos, M, H, H_kv,
+                                                         rope_base, inv_scale, query_scale);
+  else
+    return cudaErrorInvalidValue;
+  return cudaGetLastError();
+}
+
+cudaError_t launch_rmsnorm_rows(const void* x, int x_dtype, const void* gamma, void* u, int M,
+                                int D, cudaStream_t stream) {
+  if (M <= 0) return cudaSuccess;
+  const int blocks = (M + 7) / 8;
+  auto g = static_cast<const __nv_bfloat16*>(gamma);
+  auto uo = static_cast<__nv_bfloat16*>(u);
+  if (x_dtype == kF32)
+    rmsnorm_rows_kernel<float><<<blocks, 256, 0, stream>>>(static_cast<const float*>(x), g, uo, M, D);
+  else if (x_dtype == kBF16)
+    rmsnorm_rows_kernel<__nv_bfloat16><<<blocks, 256, 0, stream>>>(
+        static_cast<const __nv_bfloat16*>(x), g, uo, M, D);
+  else
+    return cudaErrorInvalidValue;
+  return cudaGetLastError();
+}
+
+cudaError_t launch_postnorm_residual(const float* a, const void* x, int x_dtype,
+                                     const void* gamma, float* y, int M, int D,
+                                     cudaStream_t stream) {
+  if (M <= 0) return cudaSuccess;
+  const int blocks = (M + 7) / 8;
+  auto g = static_cast<const __nv_bfloat16*>(gamma);
+  if (x_dtype == kF32)
+    postnorm_residual_kernel<float><<<blocks, 256, 0, stream>>>(a, static_cast<const float*>(x), g,
+                                                                y, M, D);
+  else if (x_dtype == kBF16)
+    postnorm_residual_kernel<__nv_bfloat16><<<blocks, 256, 0, stream>>>(
+        a, static_cast<const __nv_bfloat16*>(x), g, y, M, D);
+  else
+    return cudaErrorInvalidValue;
+  return cudaGetLastError();
+}
+
+}  // namespace g3

@@ -1,0 +1,270 @@
+// Projection GEMM on the 5th-generation tensor cores (tcgen05).
+//
+// C[M,N] = A[M,K] * W[N,K]^T with bf16 operands and fp32 accumulation: the
+// Q / KV projections (x against Wq, Wkv) and the output projection (O against
+// Wo) of the attention layer ("Gemma 3 Attention Block", How it works:
+// Projections and the attn_vec_einsum).
+//
+// Design (one CTA per SM, persistent):
+//   warp 0      TMA producer: 128x64 A and 256x64 W tiles, 128-byte swizzle,
+//               into a 4-stage shared-memory ring (48 KB per stage).
+//   warp 1      allocates 512 TMEM columns and issues tcgen05.mma
+//               (M=128, N=256, K=16) from one thread; accumulators live in
+//               TMEM, double-buffered (2 x 256 columns) so the epilogue of one
+//               tile overlaps the main loop of the next.
+//   warps 4-7   epilogue: tcgen05.ld of the accumulator rows (one TMEM lane
+//               per thread), conversion to the output type, global stores.
+// Every mbarrier wait is bounded (see ptx.cuh).
+#include <type_traits>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace g3 {
+
+namespace {
+
+constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4, THREADS = 256;
+constexpr uint32_t A_BYTES = BM * BK * 2;   // 16 KB
+constexpr uint32_t B_BYTES = BN * BK * 2;   // 32 KB
+constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr uint32_t SMEM_BYTES = STAGES * STAGE_BYTES + 1024;
+constexpr uint32_t TMEM_COLS = 512;
+
+enum : int { kSiteEmpty = 1, kSiteFull = 2, kSiteAccEmpty = 3, kSiteAccFull = 4 };
+
+__device__ __forceinline__ void store_chunk(float* dst, const uint32_t (&r)[32], int ncols) {
+  if (ncols == 32) {
+#pragma unroll
+    for (int v = 0; v < 8; ++v)
+      reinterpret_cast<float4*>(dst)[v] =
+          make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
+                      __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
+  } else {
+    for (int c = 0; c < ncols; ++c) dst[c] = __uint_as_float(r[c]);
+  }
+}
+
+template <typename T>
+__device__ __forceinline__ uint32_t pack2(float a, float b);
+template <> __device__ __forceinline__ uint32_t pack2<__half>(float a, float b) {
+  return pack_half2(a, b);
+}
+template <> __device__ __forceinline__ uint32_t pack2<__nv_bfloat16>(float a, float b) {
+  return pack_bf162(a, b);
+}
+
+template <typename T>
+__device__ __forceinline__ void store_chunk16(T* dst, const uint32_t (&r)[32], int ncols) {
+  if (ncols == 32) {
+#pragma unroll
+    for (int v = 0; v < 4; ++v) {
+      uint4 w;
+      w.x = pack2<T>(__uint_as_float(r[8 * v + 0]), __uint_as_float(r[8 * v + 1]));
+      w.y = pack2<T>(__uint_as_float(r[8 * v + 2]), __uint_as_float(r[8 * v + 3]));
+      w.z = pack2<T>(__uint_as_float(r[8 * v + 4]), __uint_as_float(r[8 * v + 5]));
+      w.w = pack2<T>(__uint_as_float(r[8 * v + 6]), __uint_as_float(r[8 * v + 7]));
+      reinterpret_cast<uint4*>(dst)[v] = w;
+    }
+  } else {
+    for (int c = 0; c < ncols; ++c) {
+      float f = __uint_as_float(r[c]);
+      if constexpr (std::is_same<T, __half>::value) dst[c] = __float2half_rn(f);
+      else dst[c] = __float2bfloat16_rn(f);
+    }
+  }
+}
+
+template <typename OutT>
+__global__ void __launch_bounds__(THREADS, 1)
+    gemm_tn_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   OutT* __restrict__ C, long ldc, int M, int N, int K, int* status) {
+  // A kernel launched after an earlier one gave up does no work.
+  if (*reinterpret_cast<volatile int*>(status) != 0) return;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  __shared__ __align__(8) uint64_t full_bar[STAGES], empty_bar[STAGES];
+  __shared__ __align__(8) uint64_t accf_bar[2], acce_bar[2], drain_bar;
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ int abort_flag;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int m_tiles = (M + BM - 1) / BM, n_tiles = (N + BN - 1) / BN;
+  const int num_tiles = m_tiles * n_tiles;
+  const int num_kb = (K + BK - 1) / BK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(smem_u32(&full_bar[s]), 1);
+      mbar_init(smem_u32(&empty_bar[s]), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&accf_bar[b]), 1);
+      mbar_init(smem_u32(&acce_bar[b]), 4);
+    }
+    mbar_init(smem_u32(&drain_bar), 1);
+    abort_flag = 0;
+    fence_barrier_init();
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&tmem_base_sh), TMEM_COLS);
+    tmem_relinquish();
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = tmem_base_sh;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer
+      int stage = 0;
+      uint32_t phase = 0;
+      int fills[STAGES] = {};
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+        const int m0 = (tile / n_tiles) * BM, n0 = (tile % n_tiles) * BN;
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!mbar_wait(smem_u32(&empty_bar[stage]), phase ^ 1, &abort_flag, status, kSiteEmpty)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb = smem_u32(&full_bar[stage]);
+          uint8_t* sa = smem + stage * STAGE_BYTES;
+          mbar_arrive_expect_tx(fb, STAGE_BYTES);
+          tma_load_2d(smem_u32(sa), &tmA, fb, kb * BK, m0);
+          tma_load_2d(smem_u32(sa + A_BYTES), &tmB, fb, kb * BK, n0);
+          ++fills[stage];
+          if (++stage == STAGES) { stage = 0; phase ^= 1; }
+        }
+      }
+      // Let every copy this CTA issued land before shared memory is released.
+      for (int s = 0; s < STAGES; ++s)
+        if (fills[s] > 0) mbar_wait_drain(smem_u32(&full_bar[s]), (fills[s] - 1) & 1);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------- MMA issuer
+      const uint32_t idesc = idesc_f16(BM, BN, /*bf16*/ 1, 0, 0);
+      int stage = 0;
+      uint32_t phase = 0;
+      int abuf = 0;
+      uint32_t aphase = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+        if (!mbar_wait(smem_u32(&acce_bar[abuf]), aphase ^ 1, &abort_flag, status, kSiteAccEmpty))
+          break;
+        tc_fence_after();
+        const uint32_t d_tmem = tbase + abuf * BN;
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!mbar_wait(smem_u32(&full_bar[stage]), phase, &abort_flag, status, kSiteFull)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_addr = smem_u32(smem + stage * STAGE_BYTES);
+          const uint32_t b_addr = a_addr + A_BYTES;
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k) {
+            mma_ss(d_tmem, sdesc_sw128(a_addr + k * 32, 16, 1024),
+                   sdesc_sw128(b_addr + k * 32, 16, 1024), idesc, (kb | k) != 0);
+          }
+          mma_commit(smem_u32(&empty_bar[stage]));
+          if (++stage == STAGES) { stage = 0; phase ^= 1; }
+        }
+        if (!ok) break;
+        mma_commit(smem_u32(&accf_bar[abuf]));
+        abuf ^= 1;
+        if (abuf == 0) aphase ^= 1;
+      }
+      // Drain the tensor pipe before TMEM is released.
+      mma_commit(smem_u32(&drain_bar));
+      mbar_wait_drain(smem_u32(&drain_bar), 0);
+    }
+  } else if (warp >= 4) {
+    // ---------------- epilogue: TMEM -> registers -> global
+    const int q = warp - 4;
+    const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
+    int abuf = 0;
+    uint32_t aphase = 0;
+    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+      const int m0 = (tile / n_tiles) * BM, n0 = (tile % n_tiles) * BN;
+      bool ok = mbar_wait(smem_u32(&accf_bar[abuf]), aphase, &abort_flag, status, kSiteAccFull);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after();
+      const int row = m0 + q * 32 + lane;
+      for (int c = 0; c < BN / 32; ++c) {
+        const int col0 = n0 + c * 32;
+        if (col0 >= N) break;
+        uint32_t r[32];
+        tmem_ld32(tbase + lane_off + abuf * BN + c * 32, r);
+        tmem_ld_wait();
+        if (row < M) {
+          const int ncols = min(32, N - col0);
+          OutT* dst = C + static_cast<long>(row) * ldc + col0;
+          if constexpr (std::is_same<OutT, float>::value) store_chunk(dst, r, ncols);
+          else store_chunk16<OutT>(dst, r, ncols);
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&acce_bar[abuf]));
+      abuf ^= 1;
+      if (abuf == 0) aphase ^= 1;
+    }
+  }
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tbase, TMEM_COLS);
+  }
+}
+
+template <typename OutT>
+cudaError_t launch_typed(const CUtensorMap& ta, const CUtensorMap& tb, void* C, long ldc, int M,
+                         int N, int K, cudaStream_t stream, int* status, int max_ctas) {
+  auto kern = gemm_tn_kernel<OutT>;
+  static bool attr_set = false;  // benign race: setting the same attribute twice is harmless
+  if (!attr_set) {
+    cudaError_t e =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  const int tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
+  int grid = num_sms();
+  if (max_ctas > 0 && max_ctas < grid) grid = max_ctas;
+  if (tiles < grid) grid = tiles;
+  kern<<<grid, THREADS, SMEM_BYTES, stream>>>(ta, tb, static_cast<OutT*>(C), ldc, M, N, K, status);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_linear(const void* A, long lda, const void* W, long ldw, void* C, long ldc,
+                          int M, int N, int K, int out_dtype, cudaStream_t stream, int* status,
+                          int max_ctas) {
+  if (M <= 0 || N <= 0 || K <= 0) return cudaSuccess;
+  CUtensorMap ta, tb;
+  const uint64_t adims[2] = {static_cast<uint64_t>(K), static_cast<uint64_t>(M)};
+  const uint64_t astr[1] = {static_cast<uint64_t>(lda) * 2};
+  const uint32_t abox[2] = {BK, BM};
+  const uint64_t bdims[2] = {static_cast<uint64_t>(K), static_cast<uint64_t>(N)};
+  const uint64_t bstr[1] = {static_cast<uint64_t>(ldw) * 2};
+  const uint32_t bbox[2] = {BK, BN};
+  if (!encode_tiled(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, A, adims, astr, abox) ||
+      !encode_tiled(&tb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, W, bdims, bstr, bbox))
+    return cudaErrorInvalidValue;
+  switch (out_dtype) {
+    case kF32: return launch_typed<float>(ta, tb, C, ldc, M, N, K, stream, status, max_ctas);
+    case kF16: return launch_typed<__half>(ta, tb, C, ldc, M, N, K, stream, status, max_ctas);
+    case kBF16:
+      return launch_typed<__nv_bfloat16>(ta, tb, C, ldc, M, N, K, stream, status, max_ctas);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace g3

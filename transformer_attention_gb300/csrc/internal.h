@@ -1,0 +1,49 @@
+// Internal launchers shared by the translation units of libgemma3attn.so.
+// Nothing here is part of the C ABI (see include/gemma3_attn.h).
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace g3 {
+
+enum DType : int { kBF16 = 0, kF16 = 1, kF32 = 2 };
+
+// cuTensorMapEncodeTiled, fetched from the driver at first use (the library
+// does not link libcuda, so it loads on machines without a driver).
+bool encode_tiled(CUtensorMap* map, CUtensorMapDataType dt, int rank, const void* base,
+                  const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box);
+
+int num_sms();
+
+// C[M,N] = A[M,K] * W[N,K]^T, bf16 operands, fp32 accumulation, C in out_dtype.
+cudaError_t launch_linear(const void* A, long lda, const void* W, long ldw, void* C, long ldc,
+                          int M, int N, int K, int out_dtype, cudaStream_t stream, int* status,
+                          int max_ctas);
+
+// In place on fp16 rows: Q[m, h*d_h:(h+1)*d_h] and K[m, j*d_h:(j+1)*d_h] get
+// last-axis RMSNorm, (1 + gamma), RoPE; Q also the query scale.
+cudaError_t launch_qk_norm_rope(void* Q, long ldq, void* K, long ldk, const void* gamma_q,
+                                const void* gamma_k, const int32_t* pos, int M, int H, int H_kv,
+                                int d_h, double rope_base, double rope_scale, float query_scale,
+                                cudaStream_t stream);
+
+// Flash attention forward over Q' [B,T,H,d_h] fp16 and K'/V rows of an fp16
+// buffer with row stride ldkv (K' at column j*d_h, V at column v_off + j*d_h).
+// Writes O [B,T,H,d_h] bf16 (may alias Q'); rows past the valid length are 0.
+cudaError_t launch_flash_attention(const void* Q, const void* K, const void* V, long ldkv,
+                                   void* O, const int32_t* pad_lens, int B, int T, int H,
+                                   int H_kv, int d_h, int window, cudaStream_t stream,
+                                   int* status);
+
+// u[m,:] = RMSNorm(x[m,:]) * (1 + gamma) over D, x in x_dtype (bf16|f32), u bf16.
+cudaError_t launch_rmsnorm_rows(const void* x, int x_dtype, const void* gamma, void* u, int M,
+                                int D, cudaStream_t stream);
+
+// y[m,:] = x[m,:] + RMSNorm(a[m,:]) * (1 + gamma); a f32, x bf16|f32, y f32.
+cudaError_t launch_postnorm_residual(const float* a, const void* x, int x_dtype,
+                                     const void* gamma, float* y, int M, int D,
+                                     cudaStream_t stream);
+
+}  // namespace g3
