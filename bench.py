@@ -1,0 +1,543 @@
+"""Benchmark of the Gemma 3 attention-block forward pass on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+One step is one pass of the whole hot path over one batch of synthetic input:
+the Q and KV projections, the QK-norm + RoPE + query-scale prologue, flash
+attention and the output projection (for the 6-layer stack, all six routed
+block-attention layers including their pre/post norms).  Inputs are resident
+in HBM when the timed region starts; L2 is flushed (a 256 MiB write) before
+every timed step, outside the step's CUDA events.  Prints one JSON line.
+
+Under torchrun (N > 1) every rank runs its own replica of the workload on its
+own GPU (data-parallel replicas, no collective on the data path); rank 0
+prints the line, with value = all ranks' tokens / the slowest rank's time.
+
+--impl reference times the fp64 CPU oracle instead (the reference arm), on a
+bounded sample of the same workload per step, on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from transformer_attention_gb300 import metrics  # noqa: E402
+from transformer_attention_gb300 import workloads as WL  # noqa: E402
+
+METRIC = "attention-layer tokens/s; attn TFLOP/s as % of GB300 dense BF16 peak"
+DEFAULT_WORKLOAD = "1b_global"
+MODEL_CODE = {"270M": 0, "1B": 1, "4B": 2, "12B": 3, "27B": 4}
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ---------------------------------------------------------------------------- helpers
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def reduce_max(value: float, world: int, device=None) -> float:
+    """Max over ranks (identity for one process)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_value(tokens_per_rank: float, seconds_per_rank: float, world: int,
+                    device=None) -> tuple:
+    """(value, max seconds): all ranks' tokens over the slowest rank's time."""
+    t = reduce_max(seconds_per_rank, world, device)
+    return tokens_per_rank * world / t, t
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def source_hash(path: str) -> str:
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def traffic_for(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, or None when the
+    kernel's source changed since the counters were taken."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        table = json.load(f)
+    e = table.get(kernel, {}).get(workload)
+    if not e:
+        return None
+    src = os.path.join(ROOT, "transformer_attention_gb300", "csrc", e["source"])
+    if not os.path.exists(src) or source_hash(src) != e["source_sha256_16"]:
+        return None
+    return e["dram_bytes_per_launch"]
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples taken while the timed region runs."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: str | None):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                   "-lms", "100"]
+            if self.gpu_index is not None:
+                cmd += ["-i", self.gpu_index]
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(cmd, stdout=self.out, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.out.close()
+
+    def summary(self):
+        if self.proc is None or self.path is None:
+            return {"error": "nvidia-smi unavailable"}
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"error": "no samples"}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v == "Active"})
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+# ---------------------------------------------------------------------------- GPU arm
+class LayerBuffers:
+    """Device inputs and the stage buffers of one attention layer."""
+
+    def __init__(self, w, layer, x_dev, torch, G3, stack=False):
+        self.w = w
+        p = WL.weights(w, layer)
+        self.p = {k: v.cuda() for k, v in p.items()}
+        if stack:
+            self.p.update({k: v.cuda() for k, v in WL.block_norm_gammas(w, layer).items()})
+            t, win, base, scale = G3.gemma3_layer_config(layer, w.num_layers, w.model_size)
+            self.attn_type, self.window, self.rope_base, self.rope_scale = t, win, base, scale
+        else:
+            self.attn_type = G3.GEMMA3_LOCAL_SLIDING if w.attn_type == "local" else G3.GEMMA3_GLOBAL
+            self.window, self.rope_base, self.rope_scale = w.window, w.rope_base, w.rope_scale
+
+
+def run_gpu(args, world, rank, local):
+    import torch
+
+    import __graft_entry__
+    __graft_entry__.build()
+    import transformer_attention_gb300 as G3
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    w = WL.WORKLOADS[args.workload]
+    stack = w.attn_type == "stack"
+    M, D, H, H_kv, d_h = w.M, w.D, w.H, w.H_kv, w.d_h
+    HD, KVD = H * d_h, H_kv * d_h
+    pads = WL.pad_lens(w)
+    valids = [w.T - int(p) for p in pads]
+    tokens = float(sum(valids))
+
+    x_cpu = WL.x_full(w)
+    x = x_cpu.to(dev)
+    pos = WL.segment_pos(w).to(dev)
+    pad = pads.to(dev)
+    layers = [LayerBuffers(w, l, x, torch, G3, stack) for l in range(w.num_layers)]
+    alpha = w.query_scale
+    qbuf = torch.empty((M, HD), dtype=torch.float16, device=dev)
+    kvbuf = torch.empty((M, 2 * KVD), dtype=torch.float16, device=dev)
+    out = torch.empty((M, D), dtype=torch.float32 if stack else torch.bfloat16, device=dev)
+    if stack:
+        resid = torch.empty((M, D), dtype=torch.float32, device=dev)
+        u = torch.empty((M, D), dtype=torch.bfloat16, device=dev)
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    # per-kernel work of one step
+    work = {"linear": 0.0, "attention": 0.0, "qk_norm_rope": 0.0, "rmsnorm": 0.0,
+            "postnorm": 0.0}
+    for L in layers:
+        work["linear"] += sum(metrics.layer_gemm_flops(M, D, H, H_kv, d_h).values())
+        work["attention"] += metrics.attention_flops(valids, H, d_h, L.window if
+                                                     L.attn_type == G3.GEMMA3_LOCAL_SLIDING else 0)
+        work["qk_norm_rope"] += metrics.prologue_bytes(M, H, H_kv, d_h)
+        if stack:
+            work["rmsnorm"] += metrics.rmsnorm_bytes(M, D, 4)
+            work["postnorm"] += metrics.postnorm_bytes(M, D, 4)
+    launches = {"linear": 3 * w.num_layers, "attention": w.num_layers,
+                "qk_norm_rope": w.num_layers, "rmsnorm": w.num_layers if stack else 0,
+                "postnorm": w.num_layers if stack else 0}
+
+    def step(ev=None):
+        """One pass of the hot path as stage calls (the same kernels, buffers
+        and launch shapes as gemma3_attn_forward / gemma3_block_attn_forward).
+        ev: optional dict kernel -> list of (start, end) events to fill."""
+        def mark(name):
+            if ev is None:
+                return None
+            e0 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            return e0
+
+        def done(name, e0):
+            if ev is None:
+                return
+            e1 = torch.cuda.Event(enable_timing=True)
+            e1.record(stream)
+            ev.setdefault(name, []).append((e0, e1))
+
+        for li, L in enumerate(layers):
+            a_in = x.reshape(M, D)
+            # the stack's residual stream: bf16 x into layer 0, fp32 afterwards
+            r_in, r_t = (x, G3.GEMMA3_BF16) if li == 0 else (resid, G3.GEMMA3_F32)
+            if stack:
+                e = mark("rmsnorm")
+                G3.gemma3_rmsnorm(r_in, r_t, L.p["gamma_pre"], u, M, D)
+                done("rmsnorm", e)
+                a_in = u
+            e = mark("linear")
+            G3.gemma3_linear(a_in, D, L.p["Wq"], D, qbuf, HD, M, HD, D, G3.GEMMA3_F16)
+            G3.gemma3_linear(a_in, D, L.p["Wkv"], D, kvbuf, 2 * KVD, M, 2 * KVD, D, G3.GEMMA3_F16)
+            done("linear", e)
+            e = mark("qk_norm_rope")
+            G3.gemma3_qk_norm_rope(qbuf, HD, kvbuf, 2 * KVD, L.p["gamma_q"], L.p["gamma_k"], pos,
+                                   M, H, H_kv, d_h, L.rope_base, L.rope_scale, alpha)
+            done("qk_norm_rope", e)
+            e = mark("attention")
+            win = L.window if L.attn_type == G3.GEMMA3_LOCAL_SLIDING else 0
+            G3.gemma3_flash_attention(qbuf, kvbuf, kvbuf[:, KVD:], 2 * KVD, qbuf, pad, w.B, w.T,
+                                      H, H_kv, d_h, win)
+            done("attention", e)
+            e = mark("linear")
+            G3.gemma3_linear(qbuf, HD, L.p["Wo"], HD, out, D, M, D, HD,
+                             G3.GEMMA3_F32 if stack else G3.GEMMA3_BF16)
+            done("linear", e)
+            if stack:
+                e = mark("postnorm")
+                G3.gemma3_postnorm_residual(out, r_in, r_t, L.p["gamma_post"], resid, M, D)
+                done("postnorm", e)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    assert G3.gemma3_attn_check_status() == 0
+
+    gpu_index = None
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    if vis:
+        gpu_index = vis.split(",")[local]
+    events = {}
+    step_ev = []
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(gpu_index) as clocks:
+        wall0 = time.perf_counter()
+        for _ in range(args.steps):
+            flush.zero_()
+            s0 = torch.cuda.Event(enable_timing=True)
+            s1 = torch.cuda.Event(enable_timing=True)
+            s0.record(stream)
+            step(events)
+            s1.record(stream)
+            step_ev.append((s0, s1))
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - wall0
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    st = G3.gemma3_attn_check_status()
+    assert st == 0, st
+    step_ms = [a.elapsed_time(b) for a, b in step_ev]
+    dev_seconds = sum(step_ms) / 1e3
+    value, max_seconds = whole_job_value(tokens, dev_seconds, world, dev)
+    kern_ms = {k: sum(a.elapsed_time(b) for a, b in v) for k, v in events.items()}
+
+    # ---- end to end through the public C ABI with host buffers
+    e2e = run_e2e(args, w, layers, x_cpu, pads, torch, G3, dev, stack, world)
+
+    # ---- roofline of the dominant kernel (largest share of device time)
+    peaks, peak_src = load_peaks()
+    dom = max((k for k in ("attention", "linear", "qk_norm_rope") if k in kern_ms),
+              key=lambda k: kern_ms[k])
+    n_launch = launches[dom] * args.steps
+    avg_s = kern_ms[dom] / 1e3 / n_launch
+    per_launch_work = work[dom] / launches[dom]
+    if dom in ("attention", "linear"):
+        peak = peaks["bf16_tflops_sustained"]
+        achieved = per_launch_work / avg_s / 1e12
+        roof = {"bound": "tensor", "unit": "TFLOP/s", "peak_kind": f"bf16 sustained ({peak_src})",
+                "frac_of_burst": achieved / peaks["bf16_tflops"]}
+    else:
+        peak = peaks["hbm_gbs"]
+        achieved = per_launch_work / avg_s / 1e9
+        roof = {"bound": "hbm", "unit": "GB/s", "peak_kind": f"hbm copy ({peak_src})"}
+    roof.update({"kernel": dom, "achieved": achieved, "peak": peak, "frac": achieved / peak,
+                 "traffic": traffic_for(dom, w.name)})
+
+    # ---- per-kernel breakdown (device time over the timed region)
+    total_ms = sum(step_ms)
+    breakdown = {}
+    for k, ms in kern_ms.items():
+        b = {"ms_per_step": ms / args.steps, "share": ms / total_ms}
+        if k in ("attention", "linear"):
+            b["tflops"] = work[k] * args.steps / (ms / 1e3) / 1e12
+        elif k in work and work[k]:
+            b["gbs"] = work[k] * args.steps / (ms / 1e3) / 1e9
+        breakdown[k] = b
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": max_seconds * 1e3 / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) activations, N(0,1/D) weights, gamma N(0,0.1))",
+        "config": {"workload": w.name, "B": w.B, "T": w.T, "D": D, "H": H, "H_kv": H_kv,
+                   "d_h": d_h, "attn": w.attn_type, "window": w.window,
+                   "layers": w.num_layers, "valid_tokens": int(tokens),
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": "flushed before every timed step (256 MiB write, outside step events)",
+                   "operands": "bf16 projections, f16 attention operands, f32 accumulation"},
+        "attn_tflops": work["attention"] * args.steps / (kern_ms["attention"] / 1e3) / 1e12,
+        "attn_frac_of_bf16_peak": (work["attention"] * args.steps / (kern_ms["attention"] / 1e3)
+                                   / 1e12) / peaks["bf16_tflops"],
+        "roofline": roof, "kernels": breakdown,
+        "gpu_launches": int(sum(launches.values()) * args.steps),
+        "wall_s_timed_region": wall, "e2e": e2e, "clocks": clocks.summary(),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, budget_s=args.cpu_budget)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def run_e2e(args, w, layers, x_cpu, pads, torch, G3, dev, stack, world):
+    """Same metric through the public C ABI (gemma3_attn_forward /
+    gemma3_block_attn_forward), timing host->device copies of the step's
+    activations from pinned memory and the device->host read of its result."""
+    M, D = w.M, w.D
+    x_host = x_cpu.pin_memory()
+    pos_host = WL.segment_pos(w).pin_memory()
+    pad_host = pads.pin_memory()
+    x_d = torch.empty_like(x_host, device=dev)
+    pos_d = torch.empty_like(pos_host, device=dev)
+    pad_d = torch.empty_like(pad_host, device=dev)
+    out_host = torch.empty((w.B, w.T, D), dtype=torch.float32 if stack else torch.bfloat16,
+                           pin_memory=True)
+    dims = (w.B, w.T, D, w.H, w.H_kv, w.d_h)
+    if stack:
+        ws_bytes = G3.gemma3_block_attn_workspace_size(*dims)
+        y = torch.empty((w.B, w.T, D), dtype=torch.float32, device=dev)
+    else:
+        ws_bytes = G3.gemma3_attn_workspace_size(*dims)
+        y = torch.empty((w.B, w.T, D), dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+
+    def one():
+        x_d.copy_(x_host, non_blocking=True)
+        pos_d.copy_(pos_host, non_blocking=True)
+        pad_d.copy_(pad_host, non_blocking=True)
+        if stack:
+            src, src_t = x_d, G3.GEMMA3_BF16
+            for L in layers:
+                G3.gemma3_block_attn_forward(
+                    dims, src, src_t, y, pos_d, pad_d, L.p["Wq"], L.p["Wkv"], L.p["Wo"],
+                    L.p["gamma_q"], L.p["gamma_k"], L.p["gamma_pre"], L.p["gamma_post"],
+                    L.attn_type, L.window, L.rope_base, L.rope_scale, w.query_scale, ws,
+                    ws_bytes)
+                src, src_t = y, G3.GEMMA3_F32
+        else:
+            L = layers[0]
+            G3.gemma3_attn_forward(dims, x_d, pos_d, pad_d, L.p["Wq"], L.p["Wkv"], L.p["Wo"],
+                                   L.p["gamma_q"], L.p["gamma_k"], L.attn_type, L.window,
+                                   L.rope_base, L.rope_scale, w.query_scale, y, ws, ws_bytes)
+        out_host.copy_(y, non_blocking=True)
+
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(max(1, args.warmup)):
+        flush.zero_()
+        one()
+    torch.cuda.synchronize()
+    assert G3.gemma3_attn_check_status() == 0
+    total = 0.0
+    for _ in range(args.steps):
+        flush.zero_()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        one()
+        b.record(stream)
+        b.synchronize()
+        total += a.elapsed_time(b) / 1e3
+    valid = float(sum(w.T - int(p) for p in pads))
+    value, _ = whole_job_value(valid * args.steps, total, world, dev)
+    h2d = x_host.numel() * x_host.element_size() + pos_host.numel() * 4 + pad_host.numel() * 4
+    d2h = out_host.numel() * out_host.element_size()
+    return {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h,
+            "api": "gemma3_block_attn_forward" if stack else "gemma3_attn_forward"}
+
+
+# ---------------------------------------------------------------------------- oracle (CPU)
+_ORACLE_WEIGHTS = {}
+
+
+def _oracle_weights(w):
+    if w.name not in _ORACLE_WEIGHTS:
+        if w.attn_type == "stack":
+            _ORACLE_WEIGHTS[w.name] = [dict(WL.weights(w, l), **WL.block_norm_gammas(w, l))
+                                       for l in range(w.num_layers)]
+        else:
+            _ORACLE_WEIGHTS[w.name] = WL.weights(w)
+    return _ORACLE_WEIGHTS[w.name]
+
+
+def oracle_sample(w, n_tokens: int):
+    """The fp64 oracle over the first n_tokens of batch row 0 (a causal prefix,
+    so these rows equal the full workload's first rows).  Returns seconds;
+    input generation is outside the timing."""
+    import torch
+
+    from oracle import gemma3_oracle as O
+    ws = WL.small(w, B=1, T=n_tokens, pad=("none",))
+    x = WL.x_rows(w, 0, 0, n_tokens)[None]
+    pos = WL.segment_pos(ws)
+    p = _oracle_weights(w)
+    t0 = time.perf_counter()
+    if w.attn_type == "stack":
+        O.attention_stack(x, p, model_size=w.model_size, H=w.H, H_kv=w.H_kv, d_h=w.d_h,
+                          segment_pos=pos, pad_lens=torch.zeros(1, dtype=torch.int64))
+    else:
+        O.attention_layer(x, pos, None, p["Wq"], p["Wkv"], p["Wo"], p["gamma_q"], p["gamma_k"],
+                          H=w.H, H_kv=w.H_kv, d_h=w.d_h,
+                          attn_type=O.LOCAL_SLIDING if w.attn_type == "local" else O.GLOBAL,
+                          window=w.window, rope_base=w.rope_base, rope_scale=w.rope_scale,
+                          query_scale=w.query_scale)
+    return time.perf_counter() - t0
+
+
+def sample_tokens(w, budget_s: float) -> int:
+    """Prefix length whose oracle run takes roughly budget_s (probed at 256)."""
+    probe = min(256, w.T)
+    t = oracle_sample(w, probe)
+    n = probe
+    while n < w.T and t * (2 * n / probe) <= budget_s:
+        n *= 2
+    return min(n, w.T, 4096)
+
+
+def cpu_baseline(w, budget_s: float = 15.0):
+    import torch
+    n = sample_tokens(w, budget_s)
+    secs = oracle_sample(w, n)
+    return {"value": n / secs, "unit": "tokens/s", "cores": torch.get_num_threads(),
+            "kind": "oracle",
+            "sample": f"fp64 oracle on the first {n} tokens of batch row 0 of {w.name} "
+                      f"(causal prefix; {w.num_layers} layer(s)), {secs:.2f} s"}
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    import torch
+    w = WL.WORKLOADS[args.workload]
+    n = sample_tokens(w, 4.0)
+    for _ in range(args.warmup):
+        oracle_sample(w, n)
+    times = [oracle_sample(w, n) for _ in range(args.steps)]
+    secs = sum(times)
+    value = n * args.steps / secs
+    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs * 1e3 / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "impl": "reference",
+            "config": {"workload": w.name, "B": w.B, "T": w.T, "D": w.D, "H": w.H,
+                       "H_kv": w.H_kv, "d_h": w.d_h, "attn": w.attn_type},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": torch.get_num_threads(),
+                             "kind": "oracle",
+                             "sample": f"first {n} tokens of batch row 0 per step"},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WL.WORKLOADS))
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world, rank, local = dist_env()
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+        return
+    run_gpu(args, world, rank, local)
+
+
+if __name__ == "__main__":
+    main()
