@@ -17,7 +17,8 @@
  *     asynchronous on that stream and never synchronises; read results after
  *     synchronising the stream yourself.
  *   - The caller owns every buffer.  The library never allocates device memory;
- *     scratch space is the caller's `workspace` (see gemma3_attn_workspace_size).
+ *     scratch space is the caller's `workspace` (see gemma3_attn_workspace_size),
+ *     or, for gemma3_attn_forward_noalloc only, a fixed array inside the library.
  *     Inputs are read only; only `out`/`y` and `workspace` are written.
  *   - Every function returns a status (GEMMA3_OK = 0 or a negative error) and
  *     validates all arguments before launching anything.  Kernels that lose a
@@ -115,6 +116,37 @@ int gemma3_attn_forward(const gemma3_attn_dims* dims, const void* x, const int32
                         const void* gamma_q, const void* gamma_k, int attn_type, int window,
                         double rope_base, double rope_scale, float query_scale, void* out,
                         void* workspace, size_t workspace_bytes, void* stream);
+
+/* ---------------------------------------------- one attention layer, no allocation */
+
+/* The pages have no counterpart to this entry point; it exists for callers
+ * that cannot give the library a workspace, e.g. code that may not call
+ * cudaMalloc (a latency-critical loop, a process whose device memory is owned
+ * by another framework's pool, an interface that only carries input and
+ * output buffers).
+ *
+ * Same computation, arguments and output as gemma3_attn_forward, but the
+ * intermediate rows live in a fixed scratch array inside the library
+ * (gemma3_attn_noalloc_max_scratch() bytes = 16 MiB per device, reserved on
+ * every GPU that loads the library until the process exits).  The call makes
+ * no device allocation of any kind.
+ *   - Problems whose workspace (gemma3_attn_workspace_size) exceeds the
+ *     scratch size are refused with GEMMA3_ERR_WORKSPACE before any launch.
+ *   - The first call on each device looks up the scratch array's device
+ *     address (cudaGetSymbolAddress, no allocation); make that first call
+ *     before capturing a stream on that device.
+ *   - All calls share the one array and nothing in it needs clearing between
+ *     calls; calls whose kernels overlap on the GPU (different streams, or
+ *     unordered host threads) race on it: serialise them. */
+int gemma3_attn_forward_noalloc(const gemma3_attn_dims* dims, const void* x,
+                                const int32_t* segment_pos, const int32_t* pad_lens,
+                                const void* Wq, const void* Wkv, const void* Wo,
+                                const void* gamma_q, const void* gamma_k, int attn_type,
+                                int window, double rope_base, double rope_scale,
+                                float query_scale, void* out, void* stream);
+
+/* Size in bytes of the scratch array gemma3_attn_forward_noalloc uses. */
+size_t gemma3_attn_noalloc_max_scratch(void);
 
 /* ------------------------------------------------------- one block-attention layer */
 

@@ -40,6 +40,11 @@ SIGNATURES = {
                                     c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int,
                                     c_double, c_double, c_float, c_void_p, c_void_p, c_size_t,
                                     c_void_p]),
+    "gemma3_attn_forward_noalloc": (c_int, [ctypes.POINTER(gemma3_attn_dims), c_void_p, c_void_p,
+                                            c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
+                                            c_void_p, c_int, c_int, c_double, c_double, c_float,
+                                            c_void_p, c_void_p]),
+    "gemma3_attn_noalloc_max_scratch": (c_size_t, []),
     "gemma3_block_attn_workspace_size": (c_int, [ctypes.POINTER(gemma3_attn_dims),
                                                  ctypes.POINTER(c_size_t)]),
     "gemma3_block_attn_forward": (c_int, [ctypes.POINTER(gemma3_attn_dims), c_void_p, c_int,
@@ -164,6 +169,22 @@ def gemma3_attn_forward(dims, x, segment_pos, pad_lens, Wq, Wkv, Wo, gamma_q, ga
         ctypes.byref(d), _ptr(x), _ptr(segment_pos), _ptr(pad_lens), _ptr(Wq), _ptr(Wkv),
         _ptr(Wo), _ptr(gamma_q), _ptr(gamma_k), attn_type, window, rope_base, rope_scale,
         query_scale, _ptr(out), _ptr(workspace), workspace_bytes, _stream(stream)))
+
+
+def gemma3_attn_forward_noalloc(dims, x, segment_pos, pad_lens, Wq, Wkv, Wo, gamma_q, gamma_k,
+                                attn_type, window, rope_base, rope_scale, query_scale, out,
+                                stream=None):
+    """gemma3_attn_forward without a workspace: for callers that cannot
+    allocate device memory; uses the library's fixed per-device scratch."""
+    d = _dims(*dims)
+    return _check("gemma3_attn_forward_noalloc", lib().gemma3_attn_forward_noalloc(
+        ctypes.byref(d), _ptr(x), _ptr(segment_pos), _ptr(pad_lens), _ptr(Wq), _ptr(Wkv),
+        _ptr(Wo), _ptr(gamma_q), _ptr(gamma_k), attn_type, window, rope_base, rope_scale,
+        query_scale, _ptr(out), _stream(stream)))
+
+
+def gemma3_attn_noalloc_max_scratch() -> int:
+    return lib().gemma3_attn_noalloc_max_scratch()
 
 
 def gemma3_block_attn_forward(dims, x, x_dtype, y, segment_pos, pad_lens, Wq, Wkv, Wo, gamma_q,

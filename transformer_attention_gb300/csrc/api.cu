@@ -412,3 +412,73 @@ int gemma3_selftest_wait_timeout(long long timeout_ns, void* stream) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Forward pass without any device allocation.
+//
+// Some callers cannot hand the library a workspace: code that runs where
+// cudaMalloc is not allowed or not wanted (inside a real-time loop that must
+// never hit the allocator, in a host process whose memory is owned by another
+// framework's pool, or behind an interface that only passes input and output
+// buffers).  For them the layer's intermediate Q/K/V/O rows live in one
+// fixed array of device memory that belongs to the library itself.
+//
+// The array is a file-scope __device__ variable: the CUDA runtime reserves it
+// on every GPU that loads this library, for as long as the process runs.  Its
+// name is only a host-side stand-in in host code, so the device address is
+// looked up once per device with cudaGetSymbolAddress and passed to the
+// kernels.  Every call shares this one array: two calls whose kernels overlap
+// on the GPU (different streams, or different host threads without ordering)
+// race on it and produce garbage.  The kernels overwrite every scratch byte
+// they read, so nothing has to be cleared between calls.
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;  // 16 MiB per device
+static __device__ __align__(256) unsigned char g3_noalloc_scratch[kNoAllocScratchBytes];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[kMaxDevices] = {};
+
+// Device address of the scratch array on the current device (first call on a
+// device looks it up; later calls read the cache).  nullptr on failure.
+void* noalloc_scratch() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (g_noalloc_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g3_noalloc_scratch) != cudaSuccess) return nullptr;
+    g_noalloc_ptr[dev] = p;
+  }
+  return g_noalloc_ptr[dev];
+}
+
+}  // namespace
+
+extern "C" size_t gemma3_attn_noalloc_max_scratch(void) { return kNoAllocScratchBytes; }
+
+extern "C" int gemma3_attn_forward_noalloc(const gemma3_attn_dims* dims, const void* x,
+                                           const int32_t* segment_pos, const int32_t* pad_lens,
+                                           const void* Wq, const void* Wkv, const void* Wo,
+                                           const void* gamma_q, const void* gamma_k,
+                                           int attn_type, int window, double rope_base,
+                                           double rope_scale, float query_scale, void* out,
+                                           void* stream) {
+  const int rc = validate_dims(dims);
+  if (rc != GEMMA3_OK) return rc;
+  if (out == nullptr) return GEMMA3_ERR_INVALID_ARG;
+  if (!aligned16(out)) return GEMMA3_ERR_MISALIGNED;
+  if (attn_ws(dims).total > kNoAllocScratchBytes) return GEMMA3_ERR_WORKSPACE;
+  // Same validation as the workspace entry point (a non-null stand-in for the
+  // workspace pointer: the scratch address is checked separately below).
+  const int vr = validate_layer_args(dims, x, segment_pos, Wq, Wkv, Wo, gamma_q, gamma_k,
+                                     attn_type, window, rope_base, rope_scale,
+                                     reinterpret_cast<void*>(uintptr_t(256)));
+  if (vr != GEMMA3_OK) return vr;
+  void* scratch = noalloc_scratch();
+  if (scratch == nullptr) return GEMMA3_ERR_CUDA;
+  return attn_pipeline(dims, x, segment_pos, pad_lens, Wq, Wkv, Wo, gamma_q, gamma_k, attn_type,
+                       window, rope_base, rope_scale, query_scale, out, kBF16,
+                       static_cast<uint8_t*>(scratch), as_stream(stream));
+}
