@@ -305,7 +305,7 @@ def run_gpu(args, world, rank, local):
     assert st == 0, st
     step_ms = [a.elapsed_time(b) for a, b in step_ev]
     dev_seconds = sum(step_ms) / 1e3
-    value, max_seconds = whole_job_value(tokens, dev_seconds, world, dev)
+    value, max_seconds = whole_job_value(tokens * args.steps, dev_seconds, world, dev)
     kern_ms = {k: sum(a.elapsed_time(b) for a, b in v) for k, v in events.items()}
 
     # ---- end to end through the public C ABI with host buffers
@@ -527,12 +527,18 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WL.WORKLOADS))
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--seq-len", type=int, default=None,
+                    help="override T (smaller cases for profiler captures)")
+    ap.add_argument("--batch", type=int, default=None, help="override B")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     world, rank, local = dist_env()
+    over = {k: v for k, v in (("T", args.seq_len), ("B", args.batch)) if v}
+    if over:
+        WL.WORKLOADS[args.workload] = WL.small(WL.WORKLOADS[args.workload], **over)
     if args.impl == "reference":
         run_reference(args, world, rank)
         return

@@ -12,13 +12,16 @@
 //   16-byte load) per lane; the RMS is a shuffle reduction over those lanes
 //   and the RoPE partner element sits d_h/16 lanes away.  The rotation angle
 //   is formed as an fp32 double-float (exact two-product of pos and the split
-//   frequency) and reduced modulo 2*pi by Cody-Waite with a three-part 2*pi,
-//   so positions up to 2^24 keep ~1e-6 rad of angle error.  Rows are updated
-//   in place.
+//   frequency, split hi + lo on the host in double precision) and reduced
+//   modulo 2*pi by Cody-Waite with a two-part 2*pi, so positions up to 2^24
+//   keep ~1e-6 rad of angle error without any fp64 work on the device.  Rows
+//   are updated in place.
 //
 // rmsnorm_rows / postnorm_residual: the D-axis norms of the block sandwich
 //   ("Full Gemma 3 Block", How it works: a = Attn(RMSNorm_pre(x));
 //   a <- RMSNorm_post(a); h = x + a), one warp per row.
+#include <cmath>
+
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -32,12 +35,20 @@ constexpr float kTwoPiMid = static_cast<float>(kTwoPi - static_cast<double>(kTwo
 constexpr float kInvTwoPi = static_cast<float>(1.0 / kTwoPi);
 constexpr float kEps = 1e-6f;
 
+// RoPE frequencies inv_scale * base^(-2c/d_h), c < d_h/2, each split into an
+// fp32 (hi, lo) pair on the host in double precision.
+struct RopeFreqs {
+  float2 f[128];
+};
+
+constexpr int kVecUnroll = 4;  // head vectors in flight per lane
+
 template <int DH>
 __global__ void __launch_bounds__(256)
     qk_norm_rope_kernel(__half* __restrict__ Q, long ldq, __half* __restrict__ K, long ldk,
                         const __nv_bfloat16* __restrict__ gamma_q,
                         const __nv_bfloat16* __restrict__ gamma_k, const int32_t* __restrict__ pos,
-                        int M, int H, int H_kv, double rope_base, double inv_scale,
+                        int M, int H, int H_kv, const __grid_constant__ RopeFreqs freqs,
                         float query_scale) {
   constexpr int LPV = DH / 8;      // lanes per head vector
   constexpr int VPW = 32 / LPV;    // head vectors per warp step
@@ -47,14 +58,12 @@ __global__ void __launch_bounds__(256)
   const bool second_half = ll >= HALF;
   const int c0 = (ll % HALF) * 8;  // first rotation pair index of this lane
 
-  // Per-lane constants: split frequencies (inv_scale * base^(-2c/d_h) as
-  // hi + lo fp32), and (1 + gamma) for Q and K.
   float f_hi[8], f_lo[8], gq[8], gk[8];
 #pragma unroll
   for (int e = 0; e < 8; ++e) {
-    const double f = inv_scale * pow(rope_base, -2.0 * (c0 + e) / DH);
-    f_hi[e] = static_cast<float>(f);
-    f_lo[e] = static_cast<float>(f - static_cast<double>(f_hi[e]));
+    const float2 f = freqs.f[c0 + e];
+    f_hi[e] = f.x;
+    f_lo[e] = f.y;
     gq[e] = 1.f + __bfloat162float(gamma_q[ll * 8 + e]);
     gk[e] = 1.f + __bfloat162float(gamma_k[ll * 8 + e]);
   }
@@ -75,54 +84,58 @@ __global__ void __launch_bounds__(256)
       r += a_lo;
       sincosf(r, &sn[e], &cs[e]);
     }
-    for (int base = 0; base < nvec; base += VPW) {
-      const int hv = base + sub;
-      const bool active = hv < nvec;
-      const bool is_q = hv < H;
-      __half* ptr = is_q ? Q + static_cast<long>(m) * ldq + hv * DH
-                         : K + static_cast<long>(m) * ldk + (hv - H) * DH;
-      ptr += ll * 8;
-      float x[8];
-      if (active) {
-        const uint4 raw = *reinterpret_cast<const uint4*>(ptr);
-        const __half2* h2 = reinterpret_cast<const __half2*>(&raw);
+    for (int base = 0; base < nvec; base += VPW * kVecUnroll) {
+      uint4 raw[kVecUnroll];
+      __half* ptr[kVecUnroll];
+      bool active[kVecUnroll], is_q[kVecUnroll];
+#pragma unroll
+      for (int u = 0; u < kVecUnroll; ++u) {
+        const int hv = base + u * VPW + sub;
+        active[u] = hv < nvec;
+        is_q[u] = hv < H;
+        ptr[u] = (is_q[u] ? Q + static_cast<long>(m) * ldq + hv * DH
+                          : K + static_cast<long>(m) * ldk + (hv - H) * DH) + ll * 8;
+        raw[u] = active[u] ? *reinterpret_cast<const uint4*>(ptr[u]) : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int u = 0; u < kVecUnroll; ++u) {
+        if (base + u * VPW >= nvec) break;   // warp-uniform
+        float x[8];
+        const __half2* h2 = reinterpret_cast<const __half2*>(&raw[u]);
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const float2 f = __half22float2(h2[e]);
           x[2 * e] = f.x;
           x[2 * e + 1] = f.y;
         }
-      } else {
+        float ss = 0.f;
 #pragma unroll
-        for (int e = 0; e < 8; ++e) x[e] = 0.f;
-      }
-      float ss = 0.f;
+        for (int e = 0; e < 8; ++e) ss = fmaf(x[e], x[e], ss);
 #pragma unroll
-      for (int e = 0; e < 8; ++e) ss = fmaf(x[e], x[e], ss);
+        for (int off = HALF; off >= 1; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+        const float rs = rsqrtf(ss * (1.f / DH) + kEps);
+        float y[8], o[8];
 #pragma unroll
-      for (int off = HALF; off >= 1; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
-      const float rs = rsqrtf(ss * (1.f / DH) + kEps);
-      float y[8], o[8];
+        for (int e = 0; e < 8; ++e) y[e] = x[e] * rs * (is_q[u] ? gq[e] : gk[e]);
 #pragma unroll
-      for (int e = 0; e < 8; ++e) y[e] = x[e] * rs * (is_q ? gq[e] : gk[e]);
+        for (int e = 0; e < 8; ++e) o[e] = __shfl_xor_sync(0xffffffffu, y[e], HALF);
+        const float sc = is_q[u] ? query_scale : 1.f;
+        uint4 w;
+        uint32_t* wp = reinterpret_cast<uint32_t*>(&w);
 #pragma unroll
-      for (int e = 0; e < 8; ++e) o[e] = __shfl_xor_sync(0xffffffffu, y[e], HALF);
-      const float sc = is_q ? query_scale : 1.f;
-      uint4 w;
-      uint32_t* wp = reinterpret_cast<uint32_t*>(&w);
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        float r0, r1;
-        if (!second_half) {  // y is x1 (first half), o is x2
-          r0 = y[2 * e] * cs[2 * e] - o[2 * e] * sn[2 * e];
-          r1 = y[2 * e + 1] * cs[2 * e + 1] - o[2 * e + 1] * sn[2 * e + 1];
-        } else {             // y is x2, o is x1
-          r0 = y[2 * e] * cs[2 * e] + o[2 * e] * sn[2 * e];
-          r1 = y[2 * e + 1] * cs[2 * e + 1] + o[2 * e + 1] * sn[2 * e + 1];
+        for (int e = 0; e < 4; ++e) {
+          float r0, r1;
+          if (!second_half) {  // y is x1 (first half), o is x2
+            r0 = y[2 * e] * cs[2 * e] - o[2 * e] * sn[2 * e];
+            r1 = y[2 * e + 1] * cs[2 * e + 1] - o[2 * e + 1] * sn[2 * e + 1];
+          } else {             // y is x2, o is x1
+            r0 = y[2 * e] * cs[2 * e] + o[2 * e] * sn[2 * e];
+            r1 = y[2 * e + 1] * cs[2 * e + 1] + o[2 * e + 1] * sn[2 * e + 1];
+          }
+          wp[e] = pack_half2(r0 * sc, r1 * sc);
         }
-        wp[e] = pack_half2(r0 * sc, r1 * sc);
+        if (active[u]) *reinterpret_cast<uint4*>(ptr[u]) = w;
       }
-      if (active) *reinterpret_cast<uint4*>(ptr) = w;
     }
   }
 }
@@ -210,17 +223,22 @@ cudaError_t launch_qk_norm_rope(void* Q, long ldq, void* K, long ldk, const void
   long blocks = (M + warps_per_block - 1) / warps_per_block;
   const long cap = static_cast<long>(num_sms()) * 16;
   if (blocks > cap) blocks = cap;
-  const double inv_scale = 1.0 / rope_scale;
+  RopeFreqs freqs;
+  for (int c = 0; c < d_h / 2; ++c) {
+    const double f = std::pow(rope_base, -2.0 * c / d_h) / rope_scale;
+    freqs.f[c].x = static_cast<float>(f);
+    freqs.f[c].y = static_cast<float>(f - static_cast<double>(freqs.f[c].x));
+  }
   auto q = static_cast<__half*>(Q);
   auto k = static_cast<__half*>(K);
   auto gq = static_cast<const __nv_bfloat16*>(gamma_q);
   auto gk = static_cast<const __nv_bfloat16*>(gamma_k);
   if (d_h == 256)
     qk_norm_rope_kernel<256><<<blocks, 256, 0, stream>>>(q, ldq, k, ldk, gq, gk, pos, M, H, H_kv,
-                                                         rope_base, inv_scale, query_scale);
+                                                         freqs, query_scale);
   else if (d_h == 128)
     qk_norm_rope_kernel<128><<<blocks, 256, 0, stream>>>(q, ldq, k, ldk, gq, gk, pos, M, H, H_kv,
-                                                         rope_base, inv_scale, query_scale);
+                                                         freqs, query_scale);
   else
     return cudaErrorInvalidValue;
   return cudaGetLastError();
