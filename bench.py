@@ -202,8 +202,12 @@ def run_gpu(args, world, rank, local):
     kvbuf = torch.empty((M, 2 * KVD), dtype=torch.float16, device=dev)
     out = torch.empty((M, D), dtype=torch.float32 if stack else torch.bfloat16, device=dev)
     if stack:
+        # the block path keeps its activations in fp16 with fp16 weight copies
         resid = torch.empty((M, D), dtype=torch.float32, device=dev)
-        u = torch.empty((M, D), dtype=torch.bfloat16, device=dev)
+        u = torch.empty((M, D), dtype=torch.float16, device=dev)
+        wq16 = torch.empty((HD, D), dtype=torch.float16, device=dev)
+        wkv16 = torch.empty((2 * KVD, D), dtype=torch.float16, device=dev)
+        wo16 = torch.empty((D, HD), dtype=torch.float16, device=dev)
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
@@ -218,9 +222,10 @@ def run_gpu(args, world, rank, local):
         if stack:
             work["rmsnorm"] += metrics.rmsnorm_bytes(M, D, 4)
             work["postnorm"] += metrics.postnorm_bytes(M, D, 4)
+            work["cast"] = work.get("cast", 0.0) + (2 * HD * D + 2 * KVD * D) * 4.0
     launches = {"linear": 3 * w.num_layers, "attention": w.num_layers,
                 "qk_norm_rope": w.num_layers, "rmsnorm": w.num_layers if stack else 0,
-                "postnorm": w.num_layers if stack else 0}
+                "postnorm": w.num_layers if stack else 0, "cast": 3 * w.num_layers if stack else 0}
 
     def step(ev=None):
         """One pass of the hot path as stage calls (the same kernels, buffers
@@ -241,17 +246,23 @@ def run_gpu(args, world, rank, local):
             ev.setdefault(name, []).append((e0, e1))
 
         for li, L in enumerate(layers):
-            a_in = x.reshape(M, D)
+            a_in, act = x.reshape(M, D), G3.GEMMA3_BF16
+            wq, wkv, wo = L.p["Wq"], L.p["Wkv"], L.p["Wo"]
             # the stack's residual stream: bf16 x into layer 0, fp32 afterwards
             r_in, r_t = (x, G3.GEMMA3_BF16) if li == 0 else (resid, G3.GEMMA3_F32)
             if stack:
                 e = mark("rmsnorm")
-                G3.gemma3_rmsnorm(r_in, r_t, L.p["gamma_pre"], u, M, D)
+                G3.gemma3_rmsnorm(r_in, r_t, L.p["gamma_pre"], u, G3.GEMMA3_F16, M, D)
                 done("rmsnorm", e)
-                a_in = u
+                e = mark("cast")
+                G3.gemma3_cast_bf16_f16(wq, wq16, HD * D)
+                G3.gemma3_cast_bf16_f16(wkv, wkv16, 2 * KVD * D)
+                G3.gemma3_cast_bf16_f16(wo, wo16, D * HD)
+                done("cast", e)
+                a_in, act, wq, wkv, wo = u, G3.GEMMA3_F16, wq16, wkv16, wo16
             e = mark("linear")
-            G3.gemma3_linear(a_in, D, L.p["Wq"], D, qbuf, HD, M, HD, D, G3.GEMMA3_F16)
-            G3.gemma3_linear(a_in, D, L.p["Wkv"], D, kvbuf, 2 * KVD, M, 2 * KVD, D, G3.GEMMA3_F16)
+            G3.gemma3_linear(a_in, D, wq, D, qbuf, HD, M, HD, D, act, G3.GEMMA3_F16)
+            G3.gemma3_linear(a_in, D, wkv, D, kvbuf, 2 * KVD, M, 2 * KVD, D, act, G3.GEMMA3_F16)
             done("linear", e)
             e = mark("qk_norm_rope")
             G3.gemma3_qk_norm_rope(qbuf, HD, kvbuf, 2 * KVD, L.p["gamma_q"], L.p["gamma_k"], pos,
@@ -259,11 +270,11 @@ def run_gpu(args, world, rank, local):
             done("qk_norm_rope", e)
             e = mark("attention")
             win = L.window if L.attn_type == G3.GEMMA3_LOCAL_SLIDING else 0
-            G3.gemma3_flash_attention(qbuf, kvbuf, kvbuf[:, KVD:], 2 * KVD, qbuf, pad, w.B, w.T,
-                                      H, H_kv, d_h, win)
+            G3.gemma3_flash_attention(qbuf, kvbuf, kvbuf[:, KVD:], 2 * KVD, qbuf, act, pad, w.B,
+                                      w.T, H, H_kv, d_h, win)
             done("attention", e)
             e = mark("linear")
-            G3.gemma3_linear(qbuf, HD, L.p["Wo"], HD, out, D, M, D, HD,
+            G3.gemma3_linear(qbuf, HD, wo, HD, out, D, M, D, HD, act,
                              G3.GEMMA3_F32 if stack else G3.GEMMA3_BF16)
             done("linear", e)
             if stack:

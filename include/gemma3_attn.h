@@ -150,8 +150,9 @@ size_t gemma3_attn_noalloc_max_scratch(void);
 
 /* ------------------------------------------------------- one block-attention layer */
 
-/* Workspace of gemma3_block_attn_forward: that of gemma3_attn_forward plus
- * [B*T, D] bf16 (normed input) and [B*T, D] fp32 (attention output). */
+/* Workspace of gemma3_block_attn_forward: that of gemma3_attn_forward, fp16
+ * copies of Wq, Wkv and Wo, [B*T, D] fp16 (normed input) and [B*T, D] fp32
+ * (attention output). */
 int gemma3_block_attn_workspace_size(const gemma3_attn_dims* dims, size_t* bytes);
 
 /* Attention half of a Gemma 3 block ([FB] How it works, first three lines):
@@ -159,7 +160,11 @@ int gemma3_block_attn_workspace_size(const gemma3_attn_dims* dims, size_t* bytes
  * with D-axis RMSNorms, eps 1e-6, (1 + gamma).  x is [B, T, D] in x_dtype
  * (GEMMA3_BF16 or GEMMA3_F32); y is [B, T, D] fp32 and may alias x when
  * x_dtype is GEMMA3_F32.  gamma_pre / gamma_post are [D] bf16; the other
- * arguments are those of gemma3_attn_forward.  Pad rows get a = 0, so y = x. */
+ * arguments are those of gemma3_attn_forward.  Pad rows get a = 0, so y = x.
+ * Precision: the normed input and the attention output are kept in fp16
+ * (the bf16 weights are cast to fp16 copies in the workspace), since in a
+ * stack of layers bf16 rounding of those activations accumulates past the
+ * tolerance of the block output; the residual stream stays fp32. */
 int gemma3_block_attn_forward(const gemma3_attn_dims* dims, const void* x, int x_dtype,
                               float* y, const int32_t* segment_pos, const int32_t* pad_lens,
                               const void* Wq, const void* Wkv, const void* Wo,
@@ -171,12 +176,17 @@ int gemma3_block_attn_forward(const gemma3_attn_dims* dims, const void* x, int x
 /* ------------------------------------------------------------- stage entry points */
 
 /* C[M, N] = A[M, K] * W[N, K]^T (the projection einsums of [AB] How it
- * works).  A, W bf16 with row strides lda, ldw (elements); C in out_dtype
- * (GEMMA3_BF16 | GEMMA3_F16 | GEMMA3_F32) with row stride ldc.  fp32
- * accumulation on the tcgen05 tensor cores.  K % 8 == 0; strides in bytes
- * must be multiples of 16.  max_ctas > 0 caps the persistent grid. */
+ * works).  A, W in in_dtype (GEMMA3_BF16 | GEMMA3_F16) with row strides lda,
+ * ldw (elements); C in out_dtype (GEMMA3_BF16 | GEMMA3_F16 | GEMMA3_F32) with
+ * row stride ldc.  fp32 accumulation on the tcgen05 tensor cores.  K % 8 == 0;
+ * strides in bytes must be multiples of 16.  max_ctas > 0 caps the
+ * persistent grid. */
 int gemma3_linear(const void* A, long lda, const void* W, long ldw, void* C, long ldc, int M,
-                  int N, int K, int out_dtype, int max_ctas, void* stream);
+                  int N, int K, int in_dtype, int out_dtype, int max_ctas, void* stream);
+
+/* dst[i] = src[i] for i < n, bf16 -> fp16 with round-to-nearest-even
+ * (n % 8 == 0; both 16-byte aligned). */
+int gemma3_cast_bf16_f16(const void* src, void* dst, size_t n, void* stream);
 
 /* In place on fp16 rows: for every token m and head, RMSNorm over d_h with
  * (1 + gamma_q) (query heads of Q[m, h*d_h : (h+1)*d_h]) or (1 + gamma_k)
@@ -191,16 +201,17 @@ int gemma3_qk_norm_rope(void* Q, long ldq, void* K, long ldk, const void* gamma_
 /* Masked softmax attention ([AB] How it works, Scores): Q' [B, T, H, d_h]
  * fp16 (query scale already applied); K', V rows of fp16 buffers with row
  * stride ldkv elements, head j at column j*d_h ([B*T, ldkv]); O [B, T, H, d_h]
- * bf16 (may alias Q').  Mask and padding as in gemma3_attn_forward
- * (window <= 0 means global / causal only). */
+ * in o_dtype (GEMMA3_BF16 | GEMMA3_F16; may alias Q').  Mask and padding as in
+ * gemma3_attn_forward (window <= 0 means global / causal only). */
 int gemma3_flash_attention(const void* Q, const void* K, const void* V, long ldkv, void* O,
-                           const int32_t* pad_lens, int B, int T, int H, int H_kv, int d_h,
-                           int window, void* stream);
+                           int o_dtype, const int32_t* pad_lens, int B, int T, int H, int H_kv,
+                           int d_h, int window, void* stream);
 
 /* u[m, :] = x[m, :] / sqrt(mean(x[m, :]^2) + 1e-6) * (1 + gamma)  ([FB] block
- * norms).  x [M, D] bf16 or fp32 (x_dtype), gamma [D] bf16, u [M, D] bf16. */
-int gemma3_rmsnorm(const void* x, int x_dtype, const void* gamma, void* u, int M, int D,
-                   void* stream);
+ * norms).  x [M, D] bf16 or fp32 (x_dtype), gamma [D] bf16, u [M, D] in
+ * u_dtype (GEMMA3_BF16 | GEMMA3_F16). */
+int gemma3_rmsnorm(const void* x, int x_dtype, const void* gamma, void* u, int u_dtype, int M,
+                   int D, void* stream);
 
 /* y = x + RMSNorm(a) * (1 + gamma)  ([FB] post-attention norm + residual).
  * a [M, D] fp32, x [M, D] bf16|fp32, y [M, D] fp32 (may alias an fp32 x). */

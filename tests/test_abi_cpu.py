@@ -115,5 +115,6 @@ def test_forward_rejects_bad_type_and_window(lib):
 
 
 def test_linear_rejects_misaligned(lib):
-    assert lib.gemma3_linear(4096 + 2, 64, 4096, 64, 4096, 64, 16, 16, 64, 0, 0, None) == -2
-    assert lib.gemma3_linear(4096, 60, 4096, 64, 4096, 64, 16, 16, 64, 0, 0, None) == -1
+    assert lib.gemma3_linear(4096 + 2, 64, 4096, 64, 4096, 64, 16, 16, 64, 0, 0, 0, None) == -2
+    assert lib.gemma3_linear(4096, 60, 4096, 64, 4096, 64, 16, 16, 64, 0, 0, 0, None) == -1
+    assert lib.gemma3_linear(4096, 64, 4096, 64, 4096, 64, 16, 16, 64, 2, 0, 0, None) == -1

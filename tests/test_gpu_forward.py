@@ -80,8 +80,10 @@ def test_normalised_rotated_qk_of_the_forward_stages():
         xq = dev["x"].reshape(M, w.D)
         Q = torch.empty((M, HD), dtype=torch.float16, device="cuda")
         KV = torch.empty((M, 2 * KVD), dtype=torch.float16, device="cuda")
-        G3.gemma3_linear(xq, w.D, dev["Wq"], w.D, Q, HD, M, HD, w.D, G3.GEMMA3_F16)
-        G3.gemma3_linear(xq, w.D, dev["Wkv"], w.D, KV, 2 * KVD, M, 2 * KVD, w.D, G3.GEMMA3_F16)
+        G3.gemma3_linear(xq, w.D, dev["Wq"], w.D, Q, HD, M, HD, w.D, G3.GEMMA3_BF16,
+                         G3.GEMMA3_F16)
+        G3.gemma3_linear(xq, w.D, dev["Wkv"], w.D, KV, 2 * KVD, M, 2 * KVD, w.D, G3.GEMMA3_BF16,
+                         G3.GEMMA3_F16)
         G3.gemma3_qk_norm_rope(Q, HD, KV, 2 * KVD, dev["gamma_q"], dev["gamma_k"],
                                dev["segment_pos"], M, w.H, w.H_kv, w.d_h, w.rope_base,
                                w.rope_scale, w.query_scale)

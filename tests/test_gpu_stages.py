@@ -35,16 +35,27 @@ def _randn(shape, seed, std=1.0, dtype=torch.bfloat16):
 @pytest.mark.parametrize("M,N,K", [(256, 512, 1152), (300, 1152, 4096), (1024, 2048, 2560),
                                    (130, 200, 72), (128, 256, 64), (4096, 1536, 1024)])
 @pytest.mark.parametrize("out", ["bf16", "f16", "f32"])
-def test_linear_matches_fp64(M, N, K, out):
+@pytest.mark.parametrize("inp", ["bf16", "f16"])
+def test_linear_matches_fp64(M, N, K, out, inp):
     import transformer_attention_gb300 as G3
     dt = {"bf16": torch.bfloat16, "f16": torch.float16, "f32": torch.float32}[out]
-    A = _randn((M, K), 1)
-    W = _randn((N, K), 2, K ** -0.5)
+    it = {"bf16": torch.bfloat16, "f16": torch.float16}[inp]
+    A = _randn((M, K), 1, 1.0, it)
+    W = _randn((N, K), 2, K ** -0.5, it)
     C = G3.linear(A.cuda(), W.cuda(), out_dtype=dt)
     assert G3.gemma3_attn_check_status() == 0
     ref = O.project(A, W)
     tol = {"bf16": 4e-3, "f16": 1e-3, "f32": 1e-5}[out]
     assert rel_frob(C.cpu(), ref) <= tol
+
+
+def test_cast_bf16_f16_is_exact_rounding():
+    import transformer_attention_gb300 as G3
+    src = _randn((4096,), 5, 3.0)
+    dst = torch.empty(4096, dtype=torch.float16, device="cuda")
+    G3.gemma3_cast_bf16_f16(src.cuda(), dst, 4096)
+    assert G3.gemma3_attn_check_status() == 0
+    assert torch.equal(dst.cpu(), src.float().to(torch.float16))
 
 
 def test_linear_small_grid_many_tiles():
@@ -106,7 +117,8 @@ ATTN_CASES = [
 
 
 @pytest.mark.parametrize("B,T,H,H_kv,d_h,window,pads", ATTN_CASES)
-def test_flash_attention_matches_oracle(B, T, H, H_kv, d_h, window, pads):
+@pytest.mark.parametrize("o_f16", [False, True])
+def test_flash_attention_matches_oracle(B, T, H, H_kv, d_h, window, pads, o_f16):
     import transformer_attention_gb300 as G3
     G = H // H_kv
     alpha = d_h ** -0.5
@@ -115,9 +127,11 @@ def test_flash_attention_matches_oracle(B, T, H, H_kv, d_h, window, pads):
     KV = _randn((B, T, 2 * H_kv * d_h), 21, 1.3, torch.float16)
     pad = torch.tensor(pads, dtype=torch.int32)
     Qd, KVd = Q.cuda(), KV.cuda()
-    Od = torch.empty((B, T, H, d_h), dtype=torch.bfloat16, device="cuda")
+    Od = torch.empty((B, T, H, d_h), dtype=torch.float16 if o_f16 else torch.bfloat16,
+                     device="cuda")
     Od.fill_(float("nan"))
-    G3.gemma3_flash_attention(Qd, KVd, KVd[..., H_kv * d_h:], 2 * H_kv * d_h, Od, pad.cuda(), B, T,
+    G3.gemma3_flash_attention(Qd, KVd, KVd[..., H_kv * d_h:], 2 * H_kv * d_h, Od,
+                              G3.GEMMA3_F16 if o_f16 else G3.GEMMA3_BF16, pad.cuda(), B, T,
                               H, H_kv, d_h, window)
     assert G3.gemma3_attn_check_status() == 0
     got = Od.cpu().to(F64)
@@ -143,8 +157,8 @@ def test_flash_attention_local_window_ge_T_equals_global():
     outs = []
     for window in (0, T, 5 * T):
         Od = torch.empty((B, T, H, d_h), dtype=torch.bfloat16, device="cuda")
-        G3.gemma3_flash_attention(Q, KV, KV[..., H_kv * d_h:], 2 * H_kv * d_h, Od, None, B, T, H,
-                                  H_kv, d_h, window)
+        G3.gemma3_flash_attention(Q, KV, KV[..., H_kv * d_h:], 2 * H_kv * d_h, Od, G3.GEMMA3_BF16,
+                                  None, B, T, H, H_kv, d_h, window)
         outs.append(Od.cpu())
     assert G3.gemma3_attn_check_status() == 0
     assert torch.equal(outs[0], outs[1]) and torch.equal(outs[0], outs[2])

@@ -31,6 +31,6 @@ def test_invalid_arguments_refused_on_gpu():
     import transformer_attention_gb300 as G3
     x = torch.zeros(1, 64, 1152, dtype=torch.bfloat16, device="cuda")
     with pytest.raises(G3.Gemma3Error):
-        G3.gemma3_flash_attention(x, x, x, 256, x, None, 1, 64, 8, 1, 256, 0)   # G = 8
+        G3.gemma3_flash_attention(x, x, x, 256, x, 0, None, 1, 64, 8, 1, 256, 0)   # G = 8
     with pytest.raises(G3.Gemma3Error):
-        G3.gemma3_linear(x, 1152, x, 1152, x, 1152, 64, 64, 1152, 9)            # bad dtype
+        G3.gemma3_linear(x, 1152, x, 1152, x, 1152, 64, 64, 1152, 0, 9)            # bad dtype

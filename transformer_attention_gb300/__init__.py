@@ -9,7 +9,8 @@ from __future__ import annotations
 from ._lib import (  # noqa: F401  (re-exported C-ABI names)
     GEMMA3_BF16, GEMMA3_F16, GEMMA3_F32, GEMMA3_GLOBAL, GEMMA3_LOCAL_SLIDING, Gemma3Error,
     gemma3_attn_check_status, gemma3_attn_forward, gemma3_attn_workspace_size,
-    gemma3_block_attn_forward, gemma3_block_attn_workspace_size, gemma3_flash_attention,
+    gemma3_block_attn_forward, gemma3_block_attn_workspace_size, gemma3_cast_bf16_f16,
+    gemma3_flash_attention,
     gemma3_last_device_status, gemma3_layer_attn_type, gemma3_layer_config, gemma3_linear,
     gemma3_postnorm_residual, gemma3_qk_norm_rope, gemma3_query_scale, gemma3_rmsnorm,
     gemma3_selftest_wait_timeout, lib)
@@ -65,13 +66,15 @@ def block_attention_forward(x, segment_pos, pad_lens, Wq, Wkv, Wo, gamma_q, gamm
 
 
 def linear(A, W, out_dtype=None, max_ctas=0, stream=None):
-    """C = A @ W^T on the tcgen05 GEMM (A [M,K], W [N,K] bf16)."""
+    """C = A @ W^T on the tcgen05 GEMM (A [M,K], W [N,K], both bf16 or both f16)."""
     import torch
     out_dtype = out_dtype or torch.bfloat16
     code = {torch.bfloat16: GEMMA3_BF16, torch.float16: GEMMA3_F16, torch.float32: GEMMA3_F32}
+    if A.dtype != W.dtype or A.dtype not in (torch.bfloat16, torch.float16):
+        raise ValueError("A and W must both be bf16 or both f16")
     M, K = A.shape
     N = W.shape[0]
     C = torch.empty((M, N), dtype=out_dtype, device=A.device)
-    gemma3_linear(A, A.stride(0), W, W.stride(0), C, C.stride(0), M, N, K, code[out_dtype],
-                  max_ctas, stream)
+    gemma3_linear(A, A.stride(0), W, W.stride(0), C, C.stride(0), M, N, K, code[A.dtype],
+                  code[out_dtype], max_ctas, stream)
     return C

@@ -53,13 +53,16 @@ SIGNATURES = {
                                           c_int, c_double, c_double, c_float, c_void_p, c_size_t,
                                           c_void_p]),
     "gemma3_linear": (c_int, [c_void_p, c_long, c_void_p, c_long, c_void_p, c_long, c_int, c_int,
-                              c_int, c_int, c_int, c_void_p]),
+                              c_int, c_int, c_int, c_int, c_void_p]),
+    "gemma3_cast_bf16_f16": (c_int, [c_void_p, c_void_p, c_size_t, c_void_p]),
     "gemma3_qk_norm_rope": (c_int, [c_void_p, c_long, c_void_p, c_long, c_void_p, c_void_p,
                                     c_void_p, c_int, c_int, c_int, c_int, c_double, c_double,
                                     c_float, c_void_p]),
-    "gemma3_flash_attention": (c_int, [c_void_p, c_void_p, c_void_p, c_long, c_void_p, c_void_p,
-                                       c_int, c_int, c_int, c_int, c_int, c_int, c_void_p]),
-    "gemma3_rmsnorm": (c_int, [c_void_p, c_int, c_void_p, c_void_p, c_int, c_int, c_void_p]),
+    "gemma3_flash_attention": (c_int, [c_void_p, c_void_p, c_void_p, c_long, c_void_p, c_int,
+                                       c_void_p, c_int, c_int, c_int, c_int, c_int, c_int,
+                                       c_void_p]),
+    "gemma3_rmsnorm": (c_int, [c_void_p, c_int, c_void_p, c_void_p, c_int, c_int, c_int,
+                               c_void_p]),
     "gemma3_postnorm_residual": (c_int, [c_void_p, c_void_p, c_int, c_void_p, c_void_p, c_int,
                                          c_int, c_void_p]),
     "gemma3_attn_check_status": (c_int, [c_void_p]),
@@ -198,9 +201,16 @@ def gemma3_block_attn_forward(dims, x, x_dtype, y, segment_pos, pad_lens, Wq, Wk
         _stream(stream)))
 
 
-def gemma3_linear(A, lda, W, ldw, C, ldc, M, N, K, out_dtype, max_ctas=0, stream=None):
+def gemma3_linear(A, lda, W, ldw, C, ldc, M, N, K, in_dtype, out_dtype, max_ctas=0,
+                  stream=None):
     return _check("gemma3_linear", lib().gemma3_linear(
-        _ptr(A), lda, _ptr(W), ldw, _ptr(C), ldc, M, N, K, out_dtype, max_ctas, _stream(stream)))
+        _ptr(A), lda, _ptr(W), ldw, _ptr(C), ldc, M, N, K, in_dtype, out_dtype, max_ctas,
+        _stream(stream)))
+
+
+def gemma3_cast_bf16_f16(src, dst, n, stream=None):
+    return _check("gemma3_cast_bf16_f16", lib().gemma3_cast_bf16_f16(_ptr(src), _ptr(dst), n,
+                                                                      _stream(stream)))
 
 
 def gemma3_qk_norm_rope(Q, ldq, K, ldk, gamma_q, gamma_k, pos, M, H, H_kv, d_h, rope_base,
@@ -210,15 +220,16 @@ def gemma3_qk_norm_rope(Q, ldq, K, ldk, gamma_q, gamma_k, pos, M, H, H_kv, d_h, 
         rope_base, rope_scale, query_scale, _stream(stream)))
 
 
-def gemma3_flash_attention(Q, K, V, ldkv, O, pad_lens, B, T, H, H_kv, d_h, window, stream=None):
+def gemma3_flash_attention(Q, K, V, ldkv, O, o_dtype, pad_lens, B, T, H, H_kv, d_h, window,
+                           stream=None):
     return _check("gemma3_flash_attention", lib().gemma3_flash_attention(
-        _ptr(Q), _ptr(K), _ptr(V), ldkv, _ptr(O), _ptr(pad_lens), B, T, H, H_kv, d_h, window,
-        _stream(stream)))
+        _ptr(Q), _ptr(K), _ptr(V), ldkv, _ptr(O), o_dtype, _ptr(pad_lens), B, T, H, H_kv, d_h,
+        window, _stream(stream)))
 
 
-def gemma3_rmsnorm(x, x_dtype, gamma, u, M, D, stream=None):
+def gemma3_rmsnorm(x, x_dtype, gamma, u, u_dtype, M, D, stream=None):
     return _check("gemma3_rmsnorm", lib().gemma3_rmsnorm(_ptr(x), x_dtype, _ptr(gamma), _ptr(u),
-                                                         M, D, _stream(stream)))
+                                                         u_dtype, M, D, _stream(stream)))
 
 
 def gemma3_postnorm_residual(a, x, x_dtype, gamma, y, M, D, stream=None):

@@ -65,44 +65,69 @@ int validate_dims(const gemma3_attn_dims* d) {
 size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 struct AttnWs {
-  size_t q_bytes, kv_bytes, total;
+  size_t q_bytes, kv_bytes, w_bytes, total;
 };
 
-AttnWs attn_ws(const gemma3_attn_dims* d) {
+// Workspace of the layer pipeline: Q/O rows, K/V rows and, when the
+// activations are fp16, fp16 copies of Wq, Wkv and Wo.
+AttnWs attn_ws(const gemma3_attn_dims* d, bool f16_weights = false) {
   const size_t M = static_cast<size_t>(d->B) * d->T;
   AttnWs w;
   w.q_bytes = round_up(M * d->H * d->d_h * 2, 256);
   w.kv_bytes = round_up(M * 2 * d->H_kv * d->d_h * 2, 256);
-  w.total = w.q_bytes + w.kv_bytes;
+  const size_t HD = static_cast<size_t>(d->H) * d->d_h, KVD = static_cast<size_t>(d->H_kv) * d->d_h;
+  w.w_bytes = f16_weights ? round_up(HD * d->D * 2, 256) + round_up(2 * KVD * d->D * 2, 256) +
+                                round_up(HD * d->D * 2, 256)
+                          : 0;
+  w.total = w.q_bytes + w.kv_bytes + w.w_bytes;
   return w;
 }
 
 // The layer pipeline shared by the single-layer and block entry points.
-int attn_pipeline(const gemma3_attn_dims* d, const void* x, const int32_t* segment_pos,
-                  const int32_t* pad_lens, const void* Wq, const void* Wkv, const void* Wo,
-                  const void* gamma_q, const void* gamma_k, int attn_type, int window,
-                  double rope_base, double rope_scale, float query_scale, void* out,
-                  int out_dtype, uint8_t* ws, cudaStream_t s) {
+// act_dtype kBF16: x and the weights are used as given (bf16) and O is bf16.
+// act_dtype kF16: x is fp16, the weights are first cast to fp16 copies in the
+// workspace, and O is fp16 (about 8x finer rounding of the activations, used
+// where layers are stacked and rounding errors accumulate).
+int attn_pipeline(const gemma3_attn_dims* d, const void* x, int act_dtype,
+                  const int32_t* segment_pos, const int32_t* pad_lens, const void* Wq,
+                  const void* Wkv, const void* Wo, const void* gamma_q, const void* gamma_k,
+                  int attn_type, int window, double rope_base, double rope_scale,
+                  float query_scale, void* out, int out_dtype, uint8_t* ws, cudaStream_t s) {
   int* st = status_ptr();
   if (st == nullptr) return GEMMA3_ERR_CUDA;
   const int M = d->B * d->T;
   const int HD = d->H * d->d_h, KVD = d->H_kv * d->d_h;
-  const AttnWs w = attn_ws(d);
-  void* qbuf = ws;                // Q then Q' (fp16), then O (bf16), [M, H*d_h]
+  const bool f16 = act_dtype == kF16;
+  const AttnWs w = attn_ws(d, f16);
+  void* qbuf = ws;                // Q then Q' (fp16), then O, [M, H*d_h]
   void* kvbuf = ws + w.q_bytes;   // [K'|V] fp16, [M, 2*H_kv*d_h]
   cudaError_t e;
-  e = launch_linear(x, d->D, Wq, d->D, qbuf, HD, M, HD, d->D, kF16, s, st, 0);
+  if (f16) {
+    uint8_t* wb = ws + w.q_bytes + w.kv_bytes;
+    void* wq = wb;
+    void* wkv = wb + round_up(static_cast<size_t>(HD) * d->D * 2, 256);
+    void* wo = static_cast<uint8_t*>(wkv) + round_up(static_cast<size_t>(2) * KVD * d->D * 2, 256);
+    if (launch_cast_bf16_f16(Wq, wq, static_cast<size_t>(HD) * d->D, s) != cudaSuccess ||
+        launch_cast_bf16_f16(Wkv, wkv, static_cast<size_t>(2) * KVD * d->D, s) != cudaSuccess ||
+        launch_cast_bf16_f16(Wo, wo, static_cast<size_t>(HD) * d->D, s) != cudaSuccess)
+      return GEMMA3_ERR_CUDA;
+    Wq = wq;
+    Wkv = wkv;
+    Wo = wo;
+  }
+  e = launch_linear(x, d->D, Wq, d->D, qbuf, HD, M, HD, d->D, act_dtype, kF16, s, st, 0);
   if (e != cudaSuccess) return GEMMA3_ERR_CUDA;
-  e = launch_linear(x, d->D, Wkv, d->D, kvbuf, 2 * KVD, M, 2 * KVD, d->D, kF16, s, st, 0);
+  e = launch_linear(x, d->D, Wkv, d->D, kvbuf, 2 * KVD, M, 2 * KVD, d->D, act_dtype, kF16, s, st,
+                    0);
   if (e != cudaSuccess) return GEMMA3_ERR_CUDA;
   e = launch_qk_norm_rope(qbuf, HD, kvbuf, 2 * KVD, gamma_q, gamma_k, segment_pos, M, d->H,
                           d->H_kv, d->d_h, rope_base, rope_scale, query_scale, s);
   if (e != cudaSuccess) return GEMMA3_ERR_CUDA;
   const int win = attn_type == GEMMA3_LOCAL_SLIDING ? window : 0;
   e = launch_flash_attention(qbuf, kvbuf, static_cast<uint8_t*>(kvbuf) + KVD * 2, 2 * KVD, qbuf,
-                             pad_lens, d->B, d->T, d->H, d->H_kv, d->d_h, win, s, st);
+                             act_dtype, pad_lens, d->B, d->T, d->H, d->H_kv, d->d_h, win, s, st);
   if (e != cudaSuccess) return GEMMA3_ERR_CUDA;
-  e = launch_linear(qbuf, HD, Wo, HD, out, d->D, M, d->D, HD, out_dtype, s, st, 0);
+  e = launch_linear(qbuf, HD, Wo, HD, out, d->D, M, d->D, HD, act_dtype, out_dtype, s, st, 0);
   return to_status(e);
 }
 
@@ -242,8 +267,8 @@ int gemma3_attn_forward(const gemma3_attn_dims* dims, const void* x, const int32
   if (out == nullptr) return GEMMA3_ERR_INVALID_ARG;
   if (!aligned16(out)) return GEMMA3_ERR_MISALIGNED;
   if (workspace_bytes < attn_ws(dims).total) return GEMMA3_ERR_WORKSPACE;
-  return attn_pipeline(dims, x, segment_pos, pad_lens, Wq, Wkv, Wo, gamma_q, gamma_k, attn_type,
-                       window, rope_base, rope_scale, query_scale, out, kBF16,
+  return attn_pipeline(dims, x, kBF16, segment_pos, pad_lens, Wq, Wkv, Wo, gamma_q, gamma_k,
+                       attn_type, window, rope_base, rope_scale, query_scale, out, kBF16,
                        static_cast<uint8_t*>(workspace), as_stream(stream));
 }
 
@@ -252,7 +277,8 @@ int gemma3_block_attn_workspace_size(const gemma3_attn_dims* dims, size_t* bytes
   if (rc != GEMMA3_OK) return rc;
   if (bytes == nullptr) return GEMMA3_ERR_INVALID_ARG;
   const size_t M = static_cast<size_t>(dims->B) * dims->T;
-  *bytes = attn_ws(dims).total + round_up(M * dims->D * 2, 256) + round_up(M * dims->D * 4, 256);
+  *bytes = attn_ws(dims, true).total + round_up(M * dims->D * 2, 256) +
+           round_up(M * dims->D * 4, 256);
   return GEMMA3_OK;
 }
 
@@ -273,24 +299,24 @@ int gemma3_block_attn_forward(const gemma3_attn_dims* dims, const void* x, int x
   gemma3_block_attn_workspace_size(dims, &need);
   if (workspace_bytes < need) return GEMMA3_ERR_WORKSPACE;
   const int M = dims->B * dims->T;
-  const size_t a_ws = attn_ws(dims).total;
+  const size_t a_ws = attn_ws(dims, true).total;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  void* u = ws + a_ws;                                                    // bf16 [M, D]
+  void* u = ws + a_ws;                                                    // fp16 [M, D]
   float* a = reinterpret_cast<float*>(ws + a_ws + round_up(static_cast<size_t>(M) * dims->D * 2, 256));
   cudaStream_t s = as_stream(stream);
-  if (launch_rmsnorm_rows(x, x_dtype == GEMMA3_F32 ? kF32 : kBF16, gamma_pre, u, M, dims->D, s) !=
-      cudaSuccess)
+  const int xt = x_dtype == GEMMA3_F32 ? kF32 : kBF16;
+  if (launch_rmsnorm_rows(x, xt, gamma_pre, u, kF16, M, dims->D, s) != cudaSuccess)
     return GEMMA3_ERR_CUDA;
-  rc = attn_pipeline(dims, u, segment_pos, pad_lens, Wq, Wkv, Wo, gamma_q, gamma_k, attn_type,
-                     window, rope_base, rope_scale, query_scale, a, kF32, ws, s);
+  rc = attn_pipeline(dims, u, kF16, segment_pos, pad_lens, Wq, Wkv, Wo, gamma_q, gamma_k,
+                     attn_type, window, rope_base, rope_scale, query_scale, a, kF32, ws, s);
   if (rc != GEMMA3_OK) return rc;
-  return to_status(launch_postnorm_residual(a, x, x_dtype == GEMMA3_F32 ? kF32 : kBF16,
-                                            gamma_post, y, M, dims->D, s));
+  return to_status(launch_postnorm_residual(a, x, xt, gamma_post, y, M, dims->D, s));
 }
 
 int gemma3_linear(const void* A, long lda, const void* W, long ldw, void* C, long ldc, int M,
-                  int N, int K, int out_dtype, int max_ctas, void* stream) {
+                  int N, int K, int in_dtype, int out_dtype, int max_ctas, void* stream) {
   if (!A || !W || !C || M < 0 || N < 0 || K < 1) return GEMMA3_ERR_INVALID_ARG;
+  if (in_dtype != GEMMA3_BF16 && in_dtype != GEMMA3_F16) return GEMMA3_ERR_INVALID_ARG;
   if (out_dtype != GEMMA3_BF16 && out_dtype != GEMMA3_F16 && out_dtype != GEMMA3_F32)
     return GEMMA3_ERR_INVALID_ARG;
   if (lda < K || ldw < K || ldc < N) return GEMMA3_ERR_INVALID_ARG;
@@ -302,9 +328,19 @@ int gemma3_linear(const void* A, long lda, const void* W, long ldw, void* C, lon
   if (rc != GEMMA3_OK) return rc;
   int* st = status_ptr();
   if (st == nullptr) return GEMMA3_ERR_CUDA;
+  const int it = in_dtype == GEMMA3_F16 ? kF16 : kBF16;
   const int dt = out_dtype == GEMMA3_F32 ? kF32 : (out_dtype == GEMMA3_F16 ? kF16 : kBF16);
-  return to_status(launch_linear(A, lda, W, ldw, C, ldc, M, N, K, dt, as_stream(stream), st,
+  return to_status(launch_linear(A, lda, W, ldw, C, ldc, M, N, K, it, dt, as_stream(stream), st,
                                  max_ctas));
+}
+
+int gemma3_cast_bf16_f16(const void* src, void* dst, size_t n, void* stream) {
+  if (!src || !dst) return GEMMA3_ERR_INVALID_ARG;
+  if (n % 8 != 0) return GEMMA3_ERR_INVALID_ARG;
+  if (!aligned16(src) || !aligned16(dst)) return GEMMA3_ERR_MISALIGNED;
+  int rc = check_device();
+  if (rc != GEMMA3_OK) return rc;
+  return to_status(launch_cast_bf16_f16(src, dst, n, as_stream(stream)));
 }
 
 int gemma3_qk_norm_rope(void* Q, long ldq, void* K, long ldk, const void* gamma_q,
@@ -327,10 +363,11 @@ int gemma3_qk_norm_rope(void* Q, long ldq, void* K, long ldk, const void* gamma_
 }
 
 int gemma3_flash_attention(const void* Q, const void* K, const void* V, long ldkv, void* O,
-                           const int32_t* pad_lens, int B, int T, int H, int H_kv, int d_h,
-                           int window, void* stream) {
+                           int o_dtype, const int32_t* pad_lens, int B, int T, int H, int H_kv,
+                           int d_h, int window, void* stream) {
   if (!Q || !K || !V || !O || B < 1 || T < 1 || H < 1 || H_kv < 1 || H % H_kv)
     return GEMMA3_ERR_INVALID_ARG;
+  if (o_dtype != GEMMA3_BF16 && o_dtype != GEMMA3_F16) return GEMMA3_ERR_INVALID_ARG;
   const int G = H / H_kv;
   if ((d_h != 128 && d_h != 256) || (G != 1 && G != 2 && G != 4)) return GEMMA3_ERR_UNSUPPORTED;
   if (ldkv < static_cast<long>(H_kv) * d_h) return GEMMA3_ERR_INVALID_ARG;
@@ -341,18 +378,21 @@ int gemma3_flash_attention(const void* Q, const void* K, const void* V, long ldk
   if (rc != GEMMA3_OK) return rc;
   int* st = status_ptr();
   if (st == nullptr) return GEMMA3_ERR_CUDA;
-  return to_status(launch_flash_attention(Q, K, V, ldkv, O, pad_lens, B, T, H, H_kv, d_h,
-                                          window > 0 ? window : 0, as_stream(stream), st));
+  return to_status(launch_flash_attention(Q, K, V, ldkv, O, o_dtype == GEMMA3_F16 ? kF16 : kBF16,
+                                          pad_lens, B, T, H, H_kv, d_h, window > 0 ? window : 0,
+                                          as_stream(stream), st));
 }
 
-int gemma3_rmsnorm(const void* x, int x_dtype, const void* gamma, void* u, int M, int D,
-                   void* stream) {
+int gemma3_rmsnorm(const void* x, int x_dtype, const void* gamma, void* u, int u_dtype, int M,
+                   int D, void* stream) {
   if (!x || !gamma || !u || M < 0 || D < 4 || D % 4) return GEMMA3_ERR_INVALID_ARG;
   if (x_dtype != GEMMA3_BF16 && x_dtype != GEMMA3_F32) return GEMMA3_ERR_INVALID_ARG;
+  if (u_dtype != GEMMA3_BF16 && u_dtype != GEMMA3_F16) return GEMMA3_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(gamma) || !aligned16(u)) return GEMMA3_ERR_MISALIGNED;
   int rc = check_device();
   if (rc != GEMMA3_OK) return rc;
-  return to_status(launch_rmsnorm_rows(x, x_dtype == GEMMA3_F32 ? kF32 : kBF16, gamma, u, M, D,
+  return to_status(launch_rmsnorm_rows(x, x_dtype == GEMMA3_F32 ? kF32 : kBF16, gamma, u,
+                                       u_dtype == GEMMA3_F16 ? kF16 : kBF16, M, D,
                                        as_stream(stream)));
 }
 
@@ -478,7 +518,7 @@ extern "C" int gemma3_attn_forward_noalloc(const gemma3_attn_dims* dims, const v
   if (vr != GEMMA3_OK) return vr;
   void* scratch = noalloc_scratch();
   if (scratch == nullptr) return GEMMA3_ERR_CUDA;
-  return attn_pipeline(dims, x, segment_pos, pad_lens, Wq, Wkv, Wo, gamma_q, gamma_k, attn_type,
-                       window, rope_base, rope_scale, query_scale, out, kBF16,
+  return attn_pipeline(dims, x, kBF16, segment_pos, pad_lens, Wq, Wkv, Wo, gamma_q, gamma_k,
+                       attn_type, window, rope_base, rope_scale, query_scale, out, kBF16,
                        static_cast<uint8_t*>(scratch), as_stream(stream));
 }

@@ -7,23 +7,33 @@
 //   keep s iff s <= t, s < valid_b and (global or s > t - W)   (causal+padding
 //        mask times the sliding mask; blocked logits contribute exp(.) = 0)
 //   O[b,t,h,:] = softmax_s(logits) @ V[b,:,j,:]
-// with an fp32 online softmax.  Rows t >= valid_b are written as zeros.
+// with an fp32 online softmax; O is stored as bf16 or fp16.  Rows
+// t >= valid_b are written as zeros.
 //
 // One CTA owns 128 query rows: TQ = 128/G consecutive tokens x the G query
 // heads that share kv head j, so every K/V tile loaded from memory feeds all G
 // heads of its group.  KV tiles of 128 keys outside the causal band / window
 // are never visited (local layers cost O(T*W)); only tiles that straddle the
 // band edge, the window edge or the valid length apply an element mask.
+// CTAs are ordered kv-head-major with the heaviest query tiles first, so the
+// CTAs in flight stream the same K/V tiles of one head through L2 together.
 //
-//   warp 0      TMA producer: Q once (4-D box over [B,T,H,d_h]), then K_i, V_i
+// Warp roles (12 warps):
+//   warp 0      TMA producer of Q (once, 4-D box over [B,T,H,d_h]) and K_i
+//   warp 2      TMA producer of V_i
 //   warp 1      TMEM allocation + single-thread MMA issue:
-//                 S_i = Q K_i^T   (SS, M=128 N=128, K=d_h)  -> TMEM S[i%2]
-//                 O  += P_i V_i   (TS: P_i read from TMEM,   M=128 N=d_h K=128)
-//   warps 4-7   softmax: one thread per query row (its TMEM lane); P_i is
-//               written back as fp16 over S[i%2]; O is rescaled in TMEM only
-//               when the running max grows by more than 2^8; final 1/l
-//               normalisation and bf16 store.
-// TMEM: S[0] cols 0-127, S[1] cols 128-255, O cols 256..256+d_h.
+//                 S  = Q K_i^T   (SS, M=128 N=128, K=d_h)      -> TMEM S
+//                 O += P_i V_i   (TS: P_i read from TMEM,      M=128 N=d_h K=128)
+//   warps 4-11  softmax, two warpgroups: row r of S lives in TMEM lane r; the
+//               warpgroup wg in {0,1} handles columns [64 wg, 64 wg + 64) of
+//               every row, exchanging the row max with its partner thread
+//               through shared memory (a bounded mbarrier handshake).
+// TMEM columns: S 0-127 | P[0] 128-191 | P[1] 192-255 | O 256..256+d_h.
+// S is single-buffered: the softmax releases it (s_free) as soon as it has
+// loaded the row into registers, so S_{i+1} overlaps the exponentials of
+// tile i; P is double-buffered so PV_{i-1} and the softmax of tile i never
+// touch the same columns.  O is rescaled in TMEM only when a row max grows by
+// more than 2^8, each warpgroup rescaling its half of the columns.
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -31,47 +41,56 @@ namespace g3 {
 
 namespace {
 
-constexpr int THREADS = 256;
+constexpr int NUM_WARPS = 12;
+constexpr int THREADS = NUM_WARPS * 32;
 constexpr int BM = 128;   // query rows per CTA
 constexpr int BN = 128;   // keys per KV tile
+constexpr int SM_WARPS = 8;  // softmax warps
 constexpr uint32_t CHUNK = 128 * 128;  // one 128-row x 64-element (128 B) swizzled chunk
-constexpr uint32_t O_COL = 256;
+constexpr uint32_t S_COL = 0, P_COL = 128, O_COL = 256;
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr float RESCALE_THRESHOLD = 8.0f;  // log2 units
 
 enum : int {
-  kSiteQ = 11, kSiteKEmpty, kSiteVEmpty, kSiteKFull, kSiteODone, kSitePFull, kSiteVFull,
-  kSiteSFull, kSiteORescale, kSiteOFinal
+  kSiteQ = 11, kSiteKEmpty, kSiteVEmpty, kSiteKFull, kSiteSFree, kSitePFull, kSiteVFull,
+  kSiteSFull, kSiteORescale, kSitePFree, kSiteOFinal, kSiteRed
 };
 
 template <int DH, int G>
 struct Cfg {
   static constexpr int TQ = BM / G;
   static constexpr int NCH = DH / 64;
-  static constexpr int KS = (DH == 256) ? 1 : 2;   // K ring depth
-  static constexpr int VS = KS;                     // V ring depth
+  // Ring depths within the 227 KB of shared memory (Q + K ring + V ring).
+  static constexpr int KS = (DH == 256) ? 1 : 3;   // K ring depth
+  static constexpr int VS = (DH == 256) ? 1 : 2;   // V ring depth
   static constexpr uint32_t Q_BYTES = BM * DH * 2;
   static constexpr uint32_t KV_BYTES = BN * DH * 2;
   static constexpr uint32_t SMEM = Q_BYTES + (KS + VS) * KV_BYTES + 1024;
+  static_assert(SMEM + 2304 <= 232448, "shared memory budget");
 };
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
 
 template <int DH, int G>
 __global__ void __launch_bounds__(THREADS, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                    const __grid_constant__ CUtensorMap tmV, __nv_bfloat16* __restrict__ O,
+                    const __grid_constant__ CUtensorMap tmV, uint16_t* __restrict__ O, int o_f16,
                     const int32_t* __restrict__ pad_lens, int B, int T, int H, int H_kv,
                     int window, int num_q_tiles, int* status) {
   using C = Cfg<DH, G>;
   // After a CTA of this or an earlier launch gave up, the rest do no work.
   if (*reinterpret_cast<volatile int*>(status) != 0) return;
-  // Work item: heaviest query tiles first (longest-processing-time order for
-  // causal layers), all (b, j) of a query tile next to each other.
+  // Work item: kv-head-major, heaviest query tile first within each (b, j).
   int idx = blockIdx.x;
+  const int qi = idx % num_q_tiles;
+  idx /= num_q_tiles;
   const int j = idx % H_kv;
-  idx /= H_kv;
-  const int b = idx % B;
-  idx /= B;
-  const int qt = num_q_tiles - 1 - idx;
+  const int b = idx / H_kv;
+  const int qt = num_q_tiles - 1 - qi;
   const int t0 = qt * C::TQ;
   const int valid = T - (pad_lens != nullptr ? pad_lens[b] : 0);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -79,7 +98,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   if (t0 >= valid) {
     // The whole tile is padding: its output rows are zero.
     const int rows = min(C::TQ, T - t0);
-    const int vecs = rows * G * (DH / 8);
+    const int vecs = rows * G * (DH / 8);   // zero bits are 0 in bf16 and f16 alike
     for (int v = threadIdx.x; v < vecs; v += THREADS) {
       const int e = v * 8;
       const int c = e % DH, rg = e / DH;
@@ -101,7 +120,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint8_t* sK = smem + C::Q_BYTES;                    // KS stages
   uint8_t* sV = sK + C::KS * C::KV_BYTES;             // VS stages
   __shared__ __align__(8) uint64_t q_full, k_full[C::KS], k_empty[C::KS], v_full[C::VS],
-      v_empty[C::VS], s_full[2], p_full[2], o_done, o_final, drain;
+      v_empty[C::VS], s_full, s_free, p_full[2], pv_done[2], o_final, drain, red_bar[4];
+  __shared__ float red[2][2][BM];   // [iteration parity][warpgroup][row]
   __shared__ uint32_t tmem_sh;
   __shared__ int abort_flag;
 
@@ -115,11 +135,13 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_init(smem_u32(&v_full[s]), 1);
       mbar_init(smem_u32(&v_empty[s]), 1);
     }
+    mbar_init(smem_u32(&s_full), 1);
+    mbar_init(smem_u32(&s_free), SM_WARPS);
     for (int s = 0; s < 2; ++s) {
-      mbar_init(smem_u32(&s_full[s]), 1);
-      mbar_init(smem_u32(&p_full[s]), 4);
+      mbar_init(smem_u32(&p_full[s]), SM_WARPS);
+      mbar_init(smem_u32(&pv_done[s]), 1);
     }
-    mbar_init(smem_u32(&o_done), 1);
+    for (int s = 0; s < 4; ++s) mbar_init(smem_u32(&red_bar[s]), 2);
     mbar_init(smem_u32(&o_final), 1);
     mbar_init(smem_u32(&drain), 1);
     abort_flag = 0;
@@ -138,40 +160,46 @@ __global__ void __launch_bounds__(THREADS, 1)
 
   if (warp == 0) {
     if (lane == 0) {
-      // ---------------- producer
+      // ---------------- producer: Q once, then the K ring
       const uint32_t qb = smem_u32(&q_full);
       mbar_arrive_expect_tx(qb, C::Q_BYTES);
       for (int ch = 0; ch < C::NCH; ++ch)
         tma_load_4d(smem_u32(sQ + ch * CHUNK), &tmQ, qb, ch * 64, j * G, t0, b);
-      int kfill[C::KS] = {}, vfill[C::VS] = {};
+      int fills[C::KS] = {};
       for (int i = 0; i < n_tiles; ++i) {
-        const int s0 = (tile_lo + i) * BN;
-        const int ks = i % C::KS;
-        if (!mbar_wait(smem_u32(&k_empty[ks]), ((i / C::KS) & 1) ^ 1, &abort_flag, status,
+        const int st = i % C::KS;
+        if (!mbar_wait(smem_u32(&k_empty[st]), ((i / C::KS) & 1) ^ 1, &abort_flag, status,
                        kSiteKEmpty))
           break;
-        const uint32_t kb = smem_u32(&k_full[ks]);
-        mbar_arrive_expect_tx(kb, C::KV_BYTES);
+        const uint32_t fb = smem_u32(&k_full[st]);
+        mbar_arrive_expect_tx(fb, C::KV_BYTES);
         for (int ch = 0; ch < C::NCH; ++ch)
-          tma_load_3d(smem_u32(sK + ks * C::KV_BYTES + ch * CHUNK), &tmK, kb, j * DH + ch * 64, s0,
-                      b);
-        ++kfill[ks];
-        const int vs = i % C::VS;
-        if (!mbar_wait(smem_u32(&v_empty[vs]), ((i / C::VS) & 1) ^ 1, &abort_flag, status,
-                       kSiteVEmpty))
-          break;
-        const uint32_t vb = smem_u32(&v_full[vs]);
-        mbar_arrive_expect_tx(vb, C::KV_BYTES);
-        for (int ch = 0; ch < C::NCH; ++ch)
-          tma_load_3d(smem_u32(sV + vs * C::KV_BYTES + ch * CHUNK), &tmV, vb, j * DH + ch * 64, s0,
-                      b);
-        ++vfill[vs];
+          tma_load_3d(smem_u32(sK + st * C::KV_BYTES + ch * CHUNK), &tmK, fb, j * DH + ch * 64,
+                      (tile_lo + i) * BN, b);
+        ++fills[st];
       }
       mbar_wait_drain(qb, 0);
       for (int s = 0; s < C::KS; ++s)
-        if (kfill[s] > 0) mbar_wait_drain(smem_u32(&k_full[s]), (kfill[s] - 1) & 1);
+        if (fills[s] > 0) mbar_wait_drain(smem_u32(&k_full[s]), (fills[s] - 1) & 1);
+    }
+  } else if (warp == 2) {
+    if (lane == 0) {
+      // ---------------- producer: the V ring
+      int fills[C::VS] = {};
+      for (int i = 0; i < n_tiles; ++i) {
+        const int st = i % C::VS;
+        if (!mbar_wait(smem_u32(&v_empty[st]), ((i / C::VS) & 1) ^ 1, &abort_flag, status,
+                       kSiteVEmpty))
+          break;
+        const uint32_t fb = smem_u32(&v_full[st]);
+        mbar_arrive_expect_tx(fb, C::KV_BYTES);
+        for (int ch = 0; ch < C::NCH; ++ch)
+          tma_load_3d(smem_u32(sV + st * C::KV_BYTES + ch * CHUNK), &tmV, fb, j * DH + ch * 64,
+                      (tile_lo + i) * BN, b);
+        ++fills[st];
+      }
       for (int s = 0; s < C::VS; ++s)
-        if (vfill[s] > 0) mbar_wait_drain(smem_u32(&v_full[s]), (vfill[s] - 1) & 1);
+        if (fills[s] > 0) mbar_wait_drain(smem_u32(&v_full[s]), (fills[s] - 1) & 1);
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -182,109 +210,126 @@ __global__ void __launch_bounds__(THREADS, 1)
       auto issue_pv = [&](int jt) -> bool {
         if (!mbar_wait(smem_u32(&p_full[jt & 1]), (jt >> 1) & 1, &abort_flag, status, kSitePFull))
           return false;
-        const int vs = jt % C::VS;
-        if (!mbar_wait(smem_u32(&v_full[vs]), (jt / C::VS) & 1, &abort_flag, status, kSiteVFull))
+        const int st = jt % C::VS;
+        if (!mbar_wait(smem_u32(&v_full[st]), (jt / C::VS) & 1, &abort_flag, status, kSiteVFull))
           return false;
         tc_fence_after();
-        const uint32_t p_tmem = tbase + (jt & 1) * BN;
-        const uint32_t v_addr = smem_u32(sV + vs * C::KV_BYTES);
+        const uint32_t p_tmem = tbase + P_COL + (jt & 1) * 64;
+        const uint32_t v_addr = smem_u32(sV + st * C::KV_BYTES);
 #pragma unroll
         for (int k = 0; k < BN / 16; ++k)
           mma_ts(tbase + O_COL, p_tmem + k * 8, sdesc_sw128(v_addr + k * 2048, CHUNK, 1024),
                  idesc_pv, (jt > 0 || k > 0) ? 1u : 0u);
-        mma_commit(smem_u32(&v_empty[vs]));
-        mma_commit(smem_u32(&o_done));
+        mma_commit(smem_u32(&v_empty[st]));
+        mma_commit(smem_u32(&pv_done[jt & 1]));
         return true;
       };
       bool ok = mbar_wait(smem_u32(&q_full), 0, &abort_flag, status, kSiteQ);
       for (int i = 0; ok && i < n_tiles; ++i) {
-        const int ks = i % C::KS;
-        if (!mbar_wait(smem_u32(&k_full[ks]), (i / C::KS) & 1, &abort_flag, status, kSiteKFull)) {
+        const int st = i % C::KS;
+        if (!mbar_wait(smem_u32(&k_full[st]), (i / C::KS) & 1, &abort_flag, status, kSiteKFull)) {
           ok = false;
           break;
         }
-        // S[i%2] holds P_{i-2} until PV_{i-2} has read it.
-        if (i >= 2 &&
-            !mbar_wait(smem_u32(&o_done), (i - 2) & 1, &abort_flag, status, kSiteODone)) {
+        // S is single-buffered: the softmax must have read S_{i-1}.
+        if (i >= 1 &&
+            !mbar_wait(smem_u32(&s_free), (i - 1) & 1, &abort_flag, status, kSiteSFree)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint32_t s_tmem = tbase + (i & 1) * BN;
-        const uint32_t k_addr = smem_u32(sK + ks * C::KV_BYTES);
+        const uint32_t k_addr = smem_u32(sK + st * C::KV_BYTES);
 #pragma unroll
         for (int k = 0; k < DH / 16; ++k) {
           const uint32_t off = (k >> 2) * CHUNK + (k & 3) * 32;
-          mma_ss(s_tmem, sdesc_sw128(q_addr + off, 16, 1024), sdesc_sw128(k_addr + off, 16, 1024),
-                 idesc_qk, k > 0 ? 1u : 0u);
+          mma_ss(tbase + S_COL, sdesc_sw128(q_addr + off, 16, 1024),
+                 sdesc_sw128(k_addr + off, 16, 1024), idesc_qk, k > 0 ? 1u : 0u);
         }
-        mma_commit(smem_u32(&k_empty[ks]));
-        mma_commit(smem_u32(&s_full[i & 1]));
+        mma_commit(smem_u32(&k_empty[st]));
+        mma_commit(smem_u32(&s_full));
         if (i >= 1 && !issue_pv(i - 1)) {
           ok = false;
           break;
         }
       }
-      // o_final: the whole O accumulation is complete (o_done alone cannot say
-      // so unambiguously, the final reader may be two phases behind it).
+      // o_final: the whole O accumulation is complete.
       if (ok && issue_pv(n_tiles - 1)) mma_commit(smem_u32(&o_final));
       mma_commit(smem_u32(&drain));
       mbar_wait_drain(smem_u32(&drain), 0);
     }
   } else if (warp >= 4) {
-    // ---------------- softmax + epilogue (one thread per query row)
-    const int q = warp - 4;
-    const int r = q * 32 + lane;
+    // ---------------- softmax + epilogue
+    const int wg = (warp - 4) >> 2;        // column half of every row
+    const int q = warp & 3;                // TMEM lane quarter (= warp % 4)
+    const int r = q * 32 + lane;           // query row of this thread
     const int i_tok = r / G, g = r % G;
     const int t = t0 + i_tok;
     const int h = j * G + g;
     const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
+    const int c_base = wg * (BN / 2);
+    const int kv_lo = window > 0 ? t - window + 1 : 0;   // keys kv_lo..kv_hi are kept
+    const int kv_hi = min(t, valid - 1);
+    const uint32_t rbar = smem_u32(&red_bar[q]);
     float m_used = -INFINITY, l = 0.f;
     bool ok = true;
-    for (int i = 0; i < n_tiles; ++i) {
-      const int sb = i & 1;
-      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&s_full[sb]), (i >> 1) & 1, &abort_flag,
-                                             status, kSiteSFull));
+    int i = 0;
+    for (; i < n_tiles; ++i) {
+      ok = __all_sync(0xffffffffu,
+                      mbar_wait(smem_u32(&s_full), i & 1, &abort_flag, status, kSiteSFull));
       if (!ok) break;
       tc_fence_after();
-      float s[BN];
-#pragma unroll
-      for (int c4 = 0; c4 < BN / 32; ++c4) {
+      float s[BN / 2];
+      {
         uint32_t rr[32];
-        tmem_ld32(tbase + lane_off + sb * BN + c4 * 32, rr);
+        tmem_ld32(tbase + lane_off + S_COL + c_base, rr);
         tmem_ld_wait();
 #pragma unroll
-        for (int e = 0; e < 32; ++e) s[c4 * 32 + e] = __uint_as_float(rr[e]);
+        for (int e = 0; e < 32; ++e) s[e] = __uint_as_float(rr[e]);
+        tmem_ld32(tbase + lane_off + S_COL + c_base + 32, rr);
+        tmem_ld_wait();
+#pragma unroll
+        for (int e = 0; e < 32; ++e) s[32 + e] = __uint_as_float(rr[e]);
       }
-      const int s0 = (tile_lo + i) * BN;
-      const bool need_mask = (s0 + BN - 1 > t0) || (s0 + BN > valid) ||
-                             (window > 0 && s0 <= t_last - window);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&s_free));
+
+      const int s_tile = (tile_lo + i) * BN;
+      const bool need_mask = (s_tile + BN - 1 > t0) || (s_tile + BN > valid) ||
+                             (window > 0 && s_tile <= t_last - window);
       if (need_mask) {
+        const int c_lo = kv_lo - (s_tile + c_base), c_hi = kv_hi - (s_tile + c_base);
 #pragma unroll
-        for (int c = 0; c < BN; ++c) {
-          const int kv = s0 + c;
-          const bool keep = kv <= t && kv < valid && (window == 0 || kv > t - window);
-          if (!keep) s[c] = -INFINITY;
-        }
+        for (int c = 0; c < BN / 2; ++c)
+          if (c < c_lo || c > c_hi) s[c] = -INFINITY;
       }
-      float mx = -INFINITY;
+      float mx = s[0];
 #pragma unroll
-      for (int c = 0; c < BN; ++c) mx = fmaxf(mx, s[c]);
-      mx *= LOG2E;
+      for (int c = 1; c < BN / 2; ++c) mx = fmaxf(mx, s[c]);
+      // Row max over both column halves: exchange with the partner thread.
+      red[i & 1][wg][r] = mx;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(rbar);
+      ok = __all_sync(0xffffffffu, mbar_wait(rbar, i & 1, &abort_flag, status, kSiteRed));
+      if (!ok) break;
+      mx = fmaxf(mx, red[i & 1][wg ^ 1][r]) * LOG2E;
+
       const bool grow = mx > m_used + RESCALE_THRESHOLD;
       if (__any_sync(0xffffffffu, grow)) {
         const float m_new = grow ? mx : m_used;
-        const float factor = (m_new == m_used) ? 1.f : exp2f(m_used - m_new);
+        const float factor = (m_new == m_used) ? 1.f : ex2(m_used - m_new);
         if (i > 0) {
-          // O holds PV_0..PV_{i-1}; rescale it once PV_{i-1} has landed.
-          ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&o_done), (i - 1) & 1, &abort_flag,
-                                                 status, kSiteORescale));
+          // O holds PV_0..PV_{i-1}: rescale this half of its columns once
+          // PV_{i-1} has landed.
+          ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&pv_done[(i - 1) & 1]),
+                                                 ((i - 1) >> 1) & 1, &abort_flag, status,
+                                                 kSiteORescale));
           if (!ok) break;
           tc_fence_after();
 #pragma unroll 1
-          for (int c = 0; c < DH / 32; ++c) {
+          for (int c = 0; c < DH / 64; ++c) {
             uint32_t rr[32];
-            const uint32_t ta = tbase + lane_off + O_COL + c * 32;
+            const uint32_t ta = tbase + lane_off + O_COL + wg * (DH / 2) + c * 32;
             tmem_ld32(ta, rr);
             tmem_ld_wait();
 #pragma unroll
@@ -298,51 +343,61 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
       const float mref = (m_used == -INFINITY) ? 0.f : m_used;
       float sum = 0.f;
+      uint32_t p[32];
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint32_t p[32];
-#pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const float p0 = exp2f(fmaf(s[half * 64 + 2 * e], LOG2E, -mref));
-          const float p1 = exp2f(fmaf(s[half * 64 + 2 * e + 1], LOG2E, -mref));
-          sum += p0 + p1;
-          p[e] = pack_half2(p0, p1);
-        }
-        tmem_st32(tbase + lane_off + sb * BN + half * 32, p);
+      for (int e = 0; e < 32; ++e) {
+        const float p0 = ex2(fmaf(s[2 * e], LOG2E, -mref));
+        const float p1 = ex2(fmaf(s[2 * e + 1], LOG2E, -mref));
+        sum += p0 + p1;
+        p[e] = pack_half2(p0, p1);
       }
       l += sum;
+      if (i >= 2) {
+        // P buffer i%2 is free once PV_{i-2} has read it.
+        ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&pv_done[i & 1]), ((i - 2) >> 1) & 1,
+                                               &abort_flag, status, kSitePFree));
+        if (!ok) break;
+      }
+      tmem_st32(tbase + lane_off + P_COL + (i & 1) * 64 + wg * 32, p);
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&p_full[sb]));
+      if (lane == 0) mbar_arrive(smem_u32(&p_full[i & 1]));
     }
     if (ok) {
       ok = __all_sync(0xffffffffu,
                       mbar_wait(smem_u32(&o_final), 0, &abort_flag, status, kSiteOFinal));
     }
     if (ok) {
+      // Row sum over both halves (one more handshake phase), then 1/l and store.
+      red[i & 1][wg][r] = l;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(rbar);
+      ok = __all_sync(0xffffffffu, mbar_wait(rbar, i & 1, &abort_flag, status, kSiteRed));
+    }
+    if (ok) {
       tc_fence_after();
+      const float l_tot = l + red[i & 1][wg ^ 1][r];
       const bool row_valid = t < valid;
-      const float inv_l = row_valid ? 1.f / l : 0.f;
-      __nv_bfloat16* dst = O + ((static_cast<size_t>(b) * T + t) * H + h) * DH;
+      const float inv_l = row_valid ? 1.f / l_tot : 0.f;
+      uint16_t* dst = O + ((static_cast<size_t>(b) * T + t) * H + h) * DH + wg * (DH / 2);
 #pragma unroll 1
-      for (int c = 0; c < DH / 32; ++c) {
+      for (int c = 0; c < DH / 64; ++c) {
         uint32_t rr[32];
-        tmem_ld32(tbase + lane_off + O_COL + c * 32, rr);
+        tmem_ld32(tbase + lane_off + O_COL + wg * (DH / 2) + c * 32, rr);
         tmem_ld_wait();
         if (t < T) {
 #pragma unroll
           for (int v = 0; v < 4; ++v) {
             uint4 w;
             if (row_valid) {
-              w.x = pack_bf162(__uint_as_float(rr[8 * v + 0]) * inv_l,
-                               __uint_as_float(rr[8 * v + 1]) * inv_l);
-              w.y = pack_bf162(__uint_as_float(rr[8 * v + 2]) * inv_l,
-                               __uint_as_float(rr[8 * v + 3]) * inv_l);
-              w.z = pack_bf162(__uint_as_float(rr[8 * v + 4]) * inv_l,
-                               __uint_as_float(rr[8 * v + 5]) * inv_l);
-              w.w = pack_bf162(__uint_as_float(rr[8 * v + 6]) * inv_l,
-                               __uint_as_float(rr[8 * v + 7]) * inv_l);
+              uint32_t* wp = reinterpret_cast<uint32_t*>(&w);
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const float lo = __uint_as_float(rr[8 * v + 2 * e]) * inv_l;
+                const float hi = __uint_as_float(rr[8 * v + 2 * e + 1]) * inv_l;
+                wp[e] = o_f16 ? pack_half2(lo, hi) : pack_bf162(lo, hi);
+              }
             } else {
               w = make_uint4(0, 0, 0, 0);
             }
@@ -361,8 +416,8 @@ __global__ void __launch_bounds__(THREADS, 1)
 
 template <int DH, int G>
 cudaError_t launch_cfg(const void* Q, const void* K, const void* V, long ldkv, void* O,
-                       const int32_t* pad_lens, int B, int T, int H, int H_kv, int window,
-                       cudaStream_t stream, int* status) {
+                       int o_dtype, const int32_t* pad_lens, int B, int T, int H, int H_kv,
+                       int window, cudaStream_t stream, int* status) {
   using C = Cfg<DH, G>;
   CUtensorMap tq, tk, tv;
   // Q' [B, T, H, d_h]: box {64 of d_h, the G heads of one group, TQ tokens, 1}.
@@ -391,22 +446,24 @@ cudaError_t launch_cfg(const void* Q, const void* K, const void* V, long ldkv, v
   const long grid = static_cast<long>(num_q_tiles) * B * H_kv;
   if (grid > 0x7fffffffL) return cudaErrorInvalidValue;
   kern<<<static_cast<unsigned>(grid), THREADS, C::SMEM, stream>>>(
-      tq, tk, tv, static_cast<__nv_bfloat16*>(O), pad_lens, B, T, H, H_kv, window, num_q_tiles,
-      status);
+      tq, tk, tv, static_cast<uint16_t*>(O), o_dtype == kF16 ? 1 : 0, pad_lens, B, T, H, H_kv,
+      window, num_q_tiles, status);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_flash_attention(const void* Q, const void* K, const void* V, long ldkv,
-                                   void* O, const int32_t* pad_lens, int B, int T, int H,
-                                   int H_kv, int d_h, int window, cudaStream_t stream,
+                                   void* O, int o_dtype, const int32_t* pad_lens, int B, int T,
+                                   int H, int H_kv, int d_h, int window, cudaStream_t stream,
                                    int* status) {
   if (B <= 0 || T <= 0) return cudaSuccess;
+  if (o_dtype != kBF16 && o_dtype != kF16) return cudaErrorInvalidValue;
   const int G = H / H_kv;
 #define G3_ATTN_CASE(DH_, G_)                                                                   \
   if (d_h == DH_ && G == G_)                                                                    \
-    return launch_cfg<DH_, G_>(Q, K, V, ldkv, O, pad_lens, B, T, H, H_kv, window, stream, status);
+    return launch_cfg<DH_, G_>(Q, K, V, ldkv, O, o_dtype, pad_lens, B, T, H, H_kv, window, stream, \
+                               status);
   G3_ATTN_CASE(256, 1)
   G3_ATTN_CASE(256, 2)
   G3_ATTN_CASE(256, 4)

@@ -152,11 +152,11 @@ template <> __device__ __forceinline__ float4 load4<__nv_bfloat16>(const __nv_bf
   return make_float4(a.x, a.y, b.x, b.y);
 }
 
-// u = RMSNorm(x) * (1 + gamma) -> bf16, one warp per row, D % 4 == 0.
-template <typename T>
+// u = RMSNorm(x) * (1 + gamma) -> bf16 or fp16, one warp per row, D % 4 == 0.
+template <typename T, bool OUT_F16>
 __global__ void __launch_bounds__(256)
     rmsnorm_rows_kernel(const T* __restrict__ x, const __nv_bfloat16* __restrict__ gamma,
-                        __nv_bfloat16* __restrict__ u, int M, int D) {
+                        uint16_t* __restrict__ u, int M, int D) {
   const int lane = threadIdx.x & 31;
   const int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (row >= M) return;
@@ -169,14 +169,38 @@ __global__ void __launch_bounds__(256)
 #pragma unroll
   for (int off = 16; off >= 1; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
   const float rs = rsqrtf(ss / D + kEps);
-  __nv_bfloat16* ur = u + static_cast<long>(row) * D;
+  uint16_t* ur = u + static_cast<long>(row) * D;
   for (int c = lane * 4; c < D; c += 128) {
     const float4 v = load4<T>(xr + c);
     const float4 g = load4<__nv_bfloat16>(gamma + c);
+    const float a0 = v.x * rs * (1.f + g.x), a1 = v.y * rs * (1.f + g.y);
+    const float a2 = v.z * rs * (1.f + g.z), a3 = v.w * rs * (1.f + g.w);
     uint2 w;
-    w.x = pack_bf162(v.x * rs * (1.f + g.x), v.y * rs * (1.f + g.y));
-    w.y = pack_bf162(v.z * rs * (1.f + g.z), v.w * rs * (1.f + g.w));
+    if (OUT_F16) {
+      w.x = pack_half2(a0, a1);
+      w.y = pack_half2(a2, a3);
+    } else {
+      w.x = pack_bf162(a0, a1);
+      w.y = pack_bf162(a2, a3);
+    }
     *reinterpret_cast<uint2*>(ur + c) = w;
+  }
+}
+
+// bf16 -> fp16, 8 elements per thread per step (n % 8 == 0, 16-byte aligned).
+__global__ void __launch_bounds__(256)
+    cast_bf16_f16_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst, size_t n8) {
+  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n8;
+       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    const uint4 v = src[i];
+    const uint32_t in[4] = {v.x, v.y, v.z, v.w};
+    uint32_t out[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&in[e]));
+      out[e] = pack_half2(f.x, f.y);
+    }
+    dst[i] = make_uint4(out[0], out[1], out[2], out[3]);
   }
 }
 
@@ -244,19 +268,37 @@ cudaError_t launch_qk_norm_rope(void* Q, long ldq, void* K, long ldk, const void
   return cudaGetLastError();
 }
 
-cudaError_t launch_rmsnorm_rows(const void* x, int x_dtype, const void* gamma, void* u, int M,
-                                int D, cudaStream_t stream) {
+cudaError_t launch_rmsnorm_rows(const void* x, int x_dtype, const void* gamma, void* u,
+                                int u_dtype, int M, int D, cudaStream_t stream) {
   if (M <= 0) return cudaSuccess;
   const int blocks = (M + 7) / 8;
   auto g = static_cast<const __nv_bfloat16*>(gamma);
-  auto uo = static_cast<__nv_bfloat16*>(u);
-  if (x_dtype == kF32)
-    rmsnorm_rows_kernel<float><<<blocks, 256, 0, stream>>>(static_cast<const float*>(x), g, uo, M, D);
-  else if (x_dtype == kBF16)
-    rmsnorm_rows_kernel<__nv_bfloat16><<<blocks, 256, 0, stream>>>(
-        static_cast<const __nv_bfloat16*>(x), g, uo, M, D);
-  else
+  auto uo = static_cast<uint16_t*>(u);
+  if (u_dtype != kBF16 && u_dtype != kF16) return cudaErrorInvalidValue;
+  const bool f16 = u_dtype == kF16;
+  if (x_dtype == kF32) {
+    auto xp = static_cast<const float*>(x);
+    if (f16) rmsnorm_rows_kernel<float, true><<<blocks, 256, 0, stream>>>(xp, g, uo, M, D);
+    else rmsnorm_rows_kernel<float, false><<<blocks, 256, 0, stream>>>(xp, g, uo, M, D);
+  } else if (x_dtype == kBF16) {
+    auto xp = static_cast<const __nv_bfloat16*>(x);
+    if (f16) rmsnorm_rows_kernel<__nv_bfloat16, true><<<blocks, 256, 0, stream>>>(xp, g, uo, M, D);
+    else rmsnorm_rows_kernel<__nv_bfloat16, false><<<blocks, 256, 0, stream>>>(xp, g, uo, M, D);
+  } else {
     return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_cast_bf16_f16(const void* src, void* dst, size_t n, cudaStream_t stream) {
+  if (n == 0) return cudaSuccess;
+  if (n % 8 != 0) return cudaErrorInvalidValue;
+  const size_t n8 = n / 8;
+  long blocks = static_cast<long>((n8 + 255) / 256);
+  const long cap = static_cast<long>(num_sms()) * 8;
+  if (blocks > cap) blocks = cap;
+  cast_bf16_f16_kernel<<<blocks, 256, 0, stream>>>(static_cast<const uint4*>(src),
+                                                   static_cast<uint4*>(dst), n8);
   return cudaGetLastError();
 }
 

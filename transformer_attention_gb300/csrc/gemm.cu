@@ -1,9 +1,9 @@
 // Projection GEMM on the 5th-generation tensor cores (tcgen05).
 //
-// C[M,N] = A[M,K] * W[N,K]^T with bf16 operands and fp32 accumulation: the
-// Q / KV projections (x against Wq, Wkv) and the output projection (O against
-// Wo) of the attention layer ("Gemma 3 Attention Block", How it works:
-// Projections and the attn_vec_einsum).
+// C[M,N] = A[M,K] * W[N,K]^T with bf16 (or fp16) operands and fp32
+// accumulation: the Q / KV projections (x against Wq, Wkv) and the output
+// projection (O against Wo) of the attention layer ("Gemma 3 Attention
+// Block", How it works: Projections and the attn_vec_einsum).
 //
 // Design (one CTA per SM, persistent):
 //   warp 0      TMA producer: 128x64 A and 256x64 W tiles, 128-byte swizzle,
@@ -75,7 +75,7 @@ __device__ __forceinline__ void store_chunk16(T* dst, const uint32_t (&r)[32], i
   }
 }
 
-template <typename OutT>
+template <int AB_BF16, typename OutT>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_tn_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    OutT* __restrict__ C, long ldc, int M, int N, int K, int* status) {
@@ -147,7 +147,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   } else if (warp == 1) {
     if (lane == 0) {
       // ---------------- MMA issuer
-      const uint32_t idesc = idesc_f16(BM, BN, /*bf16*/ 1, 0, 0);
+      const uint32_t idesc = idesc_f16(BM, BN, AB_BF16, 0, 0);
       int stage = 0;
       uint32_t phase = 0;
       int abuf = 0;
@@ -223,10 +223,10 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
 }
 
-template <typename OutT>
+template <int AB_BF16, typename OutT>
 cudaError_t launch_typed(const CUtensorMap& ta, const CUtensorMap& tb, void* C, long ldc, int M,
                          int N, int K, cudaStream_t stream, int* status, int max_ctas) {
-  auto kern = gemm_tn_kernel<OutT>;
+  auto kern = gemm_tn_kernel<AB_BF16, OutT>;
   static bool attr_set = false;  // benign race: setting the same attribute twice is harmless
   if (!attr_set) {
     cudaError_t e =
@@ -245,9 +245,12 @@ cudaError_t launch_typed(const CUtensorMap& ta, const CUtensorMap& tb, void* C, 
 }  // namespace
 
 cudaError_t launch_linear(const void* A, long lda, const void* W, long ldw, void* C, long ldc,
-                          int M, int N, int K, int out_dtype, cudaStream_t stream, int* status,
-                          int max_ctas) {
+                          int M, int N, int K, int in_dtype, int out_dtype, cudaStream_t stream,
+                          int* status, int max_ctas) {
   if (M <= 0 || N <= 0 || K <= 0) return cudaSuccess;
+  if (in_dtype != kBF16 && in_dtype != kF16) return cudaErrorInvalidValue;
+  const CUtensorMapDataType tdt =
+      in_dtype == kBF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   CUtensorMap ta, tb;
   const uint64_t adims[2] = {static_cast<uint64_t>(K), static_cast<uint64_t>(M)};
   const uint64_t astr[1] = {static_cast<uint64_t>(lda) * 2};
@@ -255,16 +258,22 @@ cudaError_t launch_linear(const void* A, long lda, const void* W, long ldw, void
   const uint64_t bdims[2] = {static_cast<uint64_t>(K), static_cast<uint64_t>(N)};
   const uint64_t bstr[1] = {static_cast<uint64_t>(ldw) * 2};
   const uint32_t bbox[2] = {BK, BN};
-  if (!encode_tiled(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, A, adims, astr, abox) ||
-      !encode_tiled(&tb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, W, bdims, bstr, bbox))
+  if (!encode_tiled(&ta, tdt, 2, A, adims, astr, abox) ||
+      !encode_tiled(&tb, tdt, 2, W, bdims, bstr, bbox))
     return cudaErrorInvalidValue;
-  switch (out_dtype) {
-    case kF32: return launch_typed<float>(ta, tb, C, ldc, M, N, K, stream, status, max_ctas);
-    case kF16: return launch_typed<__half>(ta, tb, C, ldc, M, N, K, stream, status, max_ctas);
-    case kBF16:
-      return launch_typed<__nv_bfloat16>(ta, tb, C, ldc, M, N, K, stream, status, max_ctas);
-    default: return cudaErrorInvalidValue;
+#define G3_GEMM_OUT(AB)                                                                         \
+  switch (out_dtype) {                                                                          \
+    case kF32: return launch_typed<AB, float>(ta, tb, C, ldc, M, N, K, stream, status, max_ctas); \
+    case kF16: return launch_typed<AB, __half>(ta, tb, C, ldc, M, N, K, stream, status, max_ctas); \
+    case kBF16:                                                                                 \
+      return launch_typed<AB, __nv_bfloat16>(ta, tb, C, ldc, M, N, K, stream, status, max_ctas); \
+    default: return cudaErrorInvalidValue;                                                      \
   }
+  if (in_dtype == kBF16) {
+    G3_GEMM_OUT(1)
+  }
+  G3_GEMM_OUT(0)
+#undef G3_GEMM_OUT
 }
 
 }  // namespace g3

@@ -17,10 +17,11 @@ bool encode_tiled(CUtensorMap* map, CUtensorMapDataType dt, int rank, const void
 
 int num_sms();
 
-// C[M,N] = A[M,K] * W[N,K]^T, bf16 operands, fp32 accumulation, C in out_dtype.
+// C[M,N] = A[M,K] * W[N,K]^T, operands in in_dtype (bf16|f16), fp32
+// accumulation, C in out_dtype.
 cudaError_t launch_linear(const void* A, long lda, const void* W, long ldw, void* C, long ldc,
-                          int M, int N, int K, int out_dtype, cudaStream_t stream, int* status,
-                          int max_ctas);
+                          int M, int N, int K, int in_dtype, int out_dtype, cudaStream_t stream,
+                          int* status, int max_ctas);
 
 // In place on fp16 rows: Q[m, h*d_h:(h+1)*d_h] and K[m, j*d_h:(j+1)*d_h] get
 // last-axis RMSNorm, (1 + gamma), RoPE; Q also the query scale.
@@ -31,15 +32,20 @@ cudaError_t launch_qk_norm_rope(void* Q, long ldq, void* K, long ldk, const void
 
 // Flash attention forward over Q' [B,T,H,d_h] fp16 and K'/V rows of an fp16
 // buffer with row stride ldkv (K' at column j*d_h, V at column v_off + j*d_h).
-// Writes O [B,T,H,d_h] bf16 (may alias Q'); rows past the valid length are 0.
+// Writes O [B,T,H,d_h] in o_dtype (bf16|f16; may alias Q'); rows past the
+// valid length are 0.
 cudaError_t launch_flash_attention(const void* Q, const void* K, const void* V, long ldkv,
-                                   void* O, const int32_t* pad_lens, int B, int T, int H,
-                                   int H_kv, int d_h, int window, cudaStream_t stream,
+                                   void* O, int o_dtype, const int32_t* pad_lens, int B, int T,
+                                   int H, int H_kv, int d_h, int window, cudaStream_t stream,
                                    int* status);
 
-// u[m,:] = RMSNorm(x[m,:]) * (1 + gamma) over D, x in x_dtype (bf16|f32), u bf16.
-cudaError_t launch_rmsnorm_rows(const void* x, int x_dtype, const void* gamma, void* u, int M,
-                                int D, cudaStream_t stream);
+// u[m,:] = RMSNorm(x[m,:]) * (1 + gamma) over D, x in x_dtype (bf16|f32), u in
+// u_dtype (bf16|f16).
+cudaError_t launch_rmsnorm_rows(const void* x, int x_dtype, const void* gamma, void* u,
+                                int u_dtype, int M, int D, cudaStream_t stream);
+
+// dst[i] = src[i] converted bf16 -> f16 (round to nearest even), n elements.
+cudaError_t launch_cast_bf16_f16(const void* src, void* dst, size_t n, cudaStream_t stream);
 
 // y[m,:] = x[m,:] + RMSNorm(a[m,:]) * (1 + gamma); a f32, x bf16|f32, y f32.
 cudaError_t launch_postnorm_residual(const float* a, const void* x, int x_dtype,
