@@ -262,8 +262,10 @@ def run_gpu(args, world, rank, local):
                 a_in, act, wq, wkv, wo = u, G3.GEMMA3_F16, wq16, wkv16, wo16
             e = mark("linear")
             G3.gemma3_linear(a_in, D, wq, D, qbuf, HD, M, HD, D, act, G3.GEMMA3_F16)
+            done("proj_q", e)
+            e = mark("linear")
             G3.gemma3_linear(a_in, D, wkv, D, kvbuf, 2 * KVD, M, 2 * KVD, D, act, G3.GEMMA3_F16)
-            done("linear", e)
+            done("proj_kv", e)
             e = mark("qk_norm_rope")
             G3.gemma3_qk_norm_rope(qbuf, HD, kvbuf, 2 * KVD, L.p["gamma_q"], L.p["gamma_k"], pos,
                                    M, H, H_kv, d_h, L.rope_base, L.rope_scale, alpha)
@@ -276,7 +278,7 @@ def run_gpu(args, world, rank, local):
             e = mark("linear")
             G3.gemma3_linear(qbuf, HD, wo, HD, out, D, M, D, HD, act,
                              G3.GEMMA3_F32 if stack else G3.GEMMA3_BF16)
-            done("linear", e)
+            done("proj_o", e)
             if stack:
                 e = mark("postnorm")
                 G3.gemma3_postnorm_residual(out, r_in, r_t, L.p["gamma_post"], resid, M, D)
@@ -318,6 +320,9 @@ def run_gpu(args, world, rank, local):
     dev_seconds = sum(step_ms) / 1e3
     value, max_seconds = whole_job_value(tokens * args.steps, dev_seconds, world, dev)
     kern_ms = {k: sum(a.elapsed_time(b) for a, b in v) for k, v in events.items()}
+    kern_ms["linear"] = sum(kern_ms.pop(k, 0.0) for k in ("proj_q", "proj_kv", "proj_o"))
+    proj_ms = {k: sum(a.elapsed_time(b) for a, b in events[k]) / args.steps
+               for k in ("proj_q", "proj_kv", "proj_o")}
 
     # ---- end to end through the public C ABI with host buffers
     e2e = run_e2e(args, w, layers, x_cpu, pads, torch, G3, dev, stack, world)
@@ -351,6 +356,10 @@ def run_gpu(args, world, rank, local):
         elif k in work and work[k]:
             b["gbs"] = work[k] * args.steps / (ms / 1e3) / 1e9
         breakdown[k] = b
+    gf = metrics.layer_gemm_flops(M, D, H, H_kv, d_h)
+    for k, name in (("proj_q", "q_proj"), ("proj_kv", "kv_proj"), ("proj_o", "o_proj")):
+        breakdown[k] = {"ms_per_step": proj_ms[k],
+                        "tflops": gf[name] * w.num_layers / (proj_ms[k] / 1e3) / 1e12}
 
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,

@@ -15,8 +15,10 @@
 // heads of its group.  KV tiles of 128 keys outside the causal band / window
 // are never visited (local layers cost O(T*W)); only tiles that straddle the
 // band edge, the window edge or the valid length apply an element mask.
-// CTAs are ordered kv-head-major with the heaviest query tiles first, so the
-// CTAs in flight stream the same K/V tiles of one head through L2 together.
+// Work items are ordered in groups of (b, kv-head) pairs whose K/V fit in L2,
+// heaviest query tiles first within a group, and the persistent CTAs (one per
+// SM) take them in boustrophedon rounds, so the items in flight stream the
+// same K/V tiles through L2 together and causal costs even out.
 //
 // Warp roles (12 warps):
 //   warp 0      TMA producer of Q (once, 4-D box over [B,T,H,d_h]) and K_i
@@ -75,43 +77,62 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+// One work item: a query tile of TQ tokens x G heads of kv head j in batch row b.
+struct Item {
+  int b, j, t0, valid, t_last, tile_lo, n_tiles;
+  bool pad;   // every row past the valid length: the item only writes zeros
+};
+
+// Work items are ordered by groups of `gsz` (b, j) pairs whose K/V fit in L2
+// together; within a group the heaviest query tiles come first (longest
+// processing time first for causal layers), the group's (b, j) pairs
+// varying fastest.  Position p of that order -> item.
+template <int TQ>
+__device__ __forceinline__ Item decode_item(int p, int num_q_tiles, int gsz, int B, int H_kv,
+                                            int T, int window, const int32_t* pad_lens) {
+  Item it;
+  const int BH = B * H_kv;
+  const int group = p / (gsz * num_q_tiles);
+  const int base = group * gsz;
+  const int gs = min(gsz, BH - base);
+  const int within = p - group * gsz * num_q_tiles;
+  const int qi = within / gs;
+  const int bj = base + within % gs;
+  it.b = bj / H_kv;
+  it.j = bj % H_kv;
+  it.t0 = (num_q_tiles - 1 - qi) * TQ;
+  it.valid = T - (pad_lens != nullptr ? pad_lens[it.b] : 0);
+  it.pad = it.t0 >= it.valid;
+  it.t_last = min(it.t0 + TQ, it.valid) - 1;
+  const int s_lo = window > 0 ? max(0, it.t0 - window + 1) : 0;
+  it.tile_lo = s_lo / BN;
+  it.n_tiles = it.pad ? 0 : it.t_last / BN - it.tile_lo + 1;
+  return it;
+}
+
+// Static boustrophedon assignment: in round r the CTAs take the next
+// gridDim.x positions, in reverse order on odd rounds, so heavy-first
+// costs even out across CTAs.  Positions grow with r.
+__device__ __forceinline__ int item_position(int r) {
+  return r * static_cast<int>(gridDim.x) +
+         ((r & 1) ? static_cast<int>(gridDim.x) - 1 - static_cast<int>(blockIdx.x)
+                  : static_cast<int>(blockIdx.x));
+}
+
+// Persistent: one CTA per SM walks the positions item_position(0, 1, ...).
+// All pipeline phases count tiles (g) and items globally, so the K/V rings
+// run ahead into the next item and the next item's Q is fetched as soon as
+// the current item's last S MMA has consumed the Q buffer.
 template <int DH, int G>
 __global__ void __launch_bounds__(THREADS, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, uint16_t* __restrict__ O, int o_f16,
                     const int32_t* __restrict__ pad_lens, int B, int T, int H, int H_kv,
-                    int window, int num_q_tiles, int* status) {
+                    int window, int num_q_tiles, int gsz, int num_items, int* status) {
   using C = Cfg<DH, G>;
   // After a CTA of this or an earlier launch gave up, the rest do no work.
   if (*reinterpret_cast<volatile int*>(status) != 0) return;
-  // Work item: kv-head-major, heaviest query tile first within each (b, j).
-  int idx = blockIdx.x;
-  const int qi = idx % num_q_tiles;
-  idx /= num_q_tiles;
-  const int j = idx % H_kv;
-  const int b = idx / H_kv;
-  const int qt = num_q_tiles - 1 - qi;
-  const int t0 = qt * C::TQ;
-  const int valid = T - (pad_lens != nullptr ? pad_lens[b] : 0);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
-  if (t0 >= valid) {
-    // The whole tile is padding: its output rows are zero.
-    const int rows = min(C::TQ, T - t0);
-    const int vecs = rows * G * (DH / 8);   // zero bits are 0 in bf16 and f16 alike
-    for (int v = threadIdx.x; v < vecs; v += THREADS) {
-      const int e = v * 8;
-      const int c = e % DH, rg = e / DH;
-      const int g = rg % G, i = rg / G;
-      *reinterpret_cast<uint4*>(O + ((static_cast<size_t>(b) * T + t0 + i) * H + j * G + g) * DH +
-                                c) = make_uint4(0, 0, 0, 0);
-    }
-    return;
-  }
-  const int t_last = min(t0 + C::TQ, valid) - 1;
-  const int s_lo = window > 0 ? max(0, t0 - window + 1) : 0;
-  const int tile_lo = s_lo / BN;
-  const int n_tiles = t_last / BN - tile_lo + 1;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -119,14 +140,16 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint8_t* sQ = smem;
   uint8_t* sK = smem + C::Q_BYTES;                    // KS stages
   uint8_t* sV = sK + C::KS * C::KV_BYTES;             // VS stages
-  __shared__ __align__(8) uint64_t q_full, k_full[C::KS], k_empty[C::KS], v_full[C::VS],
-      v_empty[C::VS], s_full, s_free, p_full[2], pv_done[2], o_final, drain, red_bar[4];
-  __shared__ float red[2][2][BM];   // [iteration parity][warpgroup][row]
+  __shared__ __align__(8) uint64_t q_full, q_empty, k_full[C::KS], k_empty[C::KS],
+      v_full[C::VS], v_empty[C::VS], s_full, s_free, p_full[2], pv_done[2], o_final, o_free,
+      drain, red_bar[4];
+  __shared__ float red[2][2][BM];   // [handshake parity][warpgroup][row]
   __shared__ uint32_t tmem_sh;
   __shared__ int abort_flag;
 
   if (threadIdx.x == 0) {
     mbar_init(smem_u32(&q_full), 1);
+    mbar_init(smem_u32(&q_empty), 1);
     for (int s = 0; s < C::KS; ++s) {
       mbar_init(smem_u32(&k_full[s]), 1);
       mbar_init(smem_u32(&k_empty[s]), 1);
@@ -143,6 +166,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     for (int s = 0; s < 4; ++s) mbar_init(smem_u32(&red_bar[s]), 2);
     mbar_init(smem_u32(&o_final), 1);
+    mbar_init(smem_u32(&o_free), SM_WARPS);
     mbar_init(smem_u32(&drain), 1);
     abort_flag = 0;
     fence_barrier_init();
@@ -160,43 +184,61 @@ __global__ void __launch_bounds__(THREADS, 1)
 
   if (warp == 0) {
     if (lane == 0) {
-      // ---------------- producer: Q once, then the K ring
-      const uint32_t qb = smem_u32(&q_full);
-      mbar_arrive_expect_tx(qb, C::Q_BYTES);
-      for (int ch = 0; ch < C::NCH; ++ch)
-        tma_load_4d(smem_u32(sQ + ch * CHUNK), &tmQ, qb, ch * 64, j * G, t0, b);
+      // ---------------- producer: Q of each item, then its K tiles
       int fills[C::KS] = {};
-      for (int i = 0; i < n_tiles; ++i) {
-        const int st = i % C::KS;
-        if (!mbar_wait(smem_u32(&k_empty[st]), ((i / C::KS) & 1) ^ 1, &abort_flag, status,
-                       kSiteKEmpty))
-          break;
-        const uint32_t fb = smem_u32(&k_full[st]);
-        mbar_arrive_expect_tx(fb, C::KV_BYTES);
+      int f = 0, nq = 0;
+      bool ok = true;
+      for (int rr = 0, pos; ok && (pos = item_position(rr)) < num_items; ++rr) {
+        const Item it = decode_item<C::TQ>(pos, num_q_tiles, gsz, B, H_kv, T, window, pad_lens);
+        if (it.pad) continue;
+        // The Q buffer is free once the previous item's last S MMA is done.
+        if (!mbar_wait(smem_u32(&q_empty), (nq & 1) ^ 1, &abort_flag, status, kSiteQ)) break;
+        const uint32_t qb = smem_u32(&q_full);
+        mbar_arrive_expect_tx(qb, C::Q_BYTES);
         for (int ch = 0; ch < C::NCH; ++ch)
-          tma_load_3d(smem_u32(sK + st * C::KV_BYTES + ch * CHUNK), &tmK, fb, j * DH + ch * 64,
-                      (tile_lo + i) * BN, b);
-        ++fills[st];
+          tma_load_4d(smem_u32(sQ + ch * CHUNK), &tmQ, qb, ch * 64, it.j * G, it.t0, it.b);
+        ++nq;
+        for (int i = 0; i < it.n_tiles; ++i, ++f) {
+          const int st = f % C::KS;
+          if (!mbar_wait(smem_u32(&k_empty[st]), ((f / C::KS) & 1) ^ 1, &abort_flag, status,
+                         kSiteKEmpty)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb = smem_u32(&k_full[st]);
+          mbar_arrive_expect_tx(fb, C::KV_BYTES);
+          for (int ch = 0; ch < C::NCH; ++ch)
+            tma_load_3d(smem_u32(sK + st * C::KV_BYTES + ch * CHUNK), &tmK, fb,
+                        it.j * DH + ch * 64, (it.tile_lo + i) * BN, it.b);
+          ++fills[st];
+        }
       }
-      mbar_wait_drain(qb, 0);
+      if (nq > 0) mbar_wait_drain(smem_u32(&q_full), (nq - 1) & 1);
       for (int s = 0; s < C::KS; ++s)
         if (fills[s] > 0) mbar_wait_drain(smem_u32(&k_full[s]), (fills[s] - 1) & 1);
     }
   } else if (warp == 2) {
     if (lane == 0) {
-      // ---------------- producer: the V ring
+      // ---------------- producer: V tiles of each item
       int fills[C::VS] = {};
-      for (int i = 0; i < n_tiles; ++i) {
-        const int st = i % C::VS;
-        if (!mbar_wait(smem_u32(&v_empty[st]), ((i / C::VS) & 1) ^ 1, &abort_flag, status,
-                       kSiteVEmpty))
-          break;
-        const uint32_t fb = smem_u32(&v_full[st]);
-        mbar_arrive_expect_tx(fb, C::KV_BYTES);
-        for (int ch = 0; ch < C::NCH; ++ch)
-          tma_load_3d(smem_u32(sV + st * C::KV_BYTES + ch * CHUNK), &tmV, fb, j * DH + ch * 64,
-                      (tile_lo + i) * BN, b);
-        ++fills[st];
+      int f = 0;
+      bool ok = true;
+      for (int rr = 0, pos; ok && (pos = item_position(rr)) < num_items; ++rr) {
+        const Item it = decode_item<C::TQ>(pos, num_q_tiles, gsz, B, H_kv, T, window, pad_lens);
+        for (int i = 0; i < it.n_tiles; ++i, ++f) {
+          const int st = f % C::VS;
+          if (!mbar_wait(smem_u32(&v_empty[st]), ((f / C::VS) & 1) ^ 1, &abort_flag, status,
+                         kSiteVEmpty)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb = smem_u32(&v_full[st]);
+          mbar_arrive_expect_tx(fb, C::KV_BYTES);
+          for (int ch = 0; ch < C::NCH; ++ch)
+            tma_load_3d(smem_u32(sV + st * C::KV_BYTES + ch * CHUNK), &tmV, fb,
+                        it.j * DH + ch * 64, (it.tile_lo + i) * BN, it.b);
+          ++fills[st];
+        }
       }
       for (int s = 0; s < C::VS; ++s)
         if (fills[s] > 0) mbar_wait_drain(smem_u32(&v_full[s]), (fills[s] - 1) & 1);
@@ -207,53 +249,70 @@ __global__ void __launch_bounds__(THREADS, 1)
       constexpr uint32_t idesc_qk = idesc_f16(BM, BN, /*f16*/ 0, 0, 0);
       constexpr uint32_t idesc_pv = idesc_f16(BM, DH, /*f16*/ 0, 0, /*B MN-major*/ 1);
       const uint32_t q_addr = smem_u32(sQ);
-      auto issue_pv = [&](int jt) -> bool {
-        if (!mbar_wait(smem_u32(&p_full[jt & 1]), (jt >> 1) & 1, &abort_flag, status, kSitePFull))
+      int nitem = 0;   // items processed so far
+      // PV of global tile gt, local tile lt of the current item.
+      auto issue_pv = [&](int gt, int lt) -> bool {
+        // The first PV of an item overwrites O: the previous item's epilogue
+        // must have read it.
+        if (lt == 0 && nitem >= 1 &&
+            !mbar_wait(smem_u32(&o_free), (nitem - 1) & 1, &abort_flag, status, kSiteOFinal))
           return false;
-        const int st = jt % C::VS;
-        if (!mbar_wait(smem_u32(&v_full[st]), (jt / C::VS) & 1, &abort_flag, status, kSiteVFull))
+        if (!mbar_wait(smem_u32(&p_full[gt & 1]), (gt >> 1) & 1, &abort_flag, status, kSitePFull))
+          return false;
+        const int st = gt % C::VS;
+        if (!mbar_wait(smem_u32(&v_full[st]), (gt / C::VS) & 1, &abort_flag, status, kSiteVFull))
           return false;
         tc_fence_after();
-        const uint32_t p_tmem = tbase + P_COL + (jt & 1) * 64;
+        const uint32_t p_tmem = tbase + P_COL + (gt & 1) * 64;
         const uint32_t v_addr = smem_u32(sV + st * C::KV_BYTES);
 #pragma unroll
         for (int k = 0; k < BN / 16; ++k)
           mma_ts(tbase + O_COL, p_tmem + k * 8, sdesc_sw128(v_addr + k * 2048, CHUNK, 1024),
-                 idesc_pv, (jt > 0 || k > 0) ? 1u : 0u);
+                 idesc_pv, (lt > 0 || k > 0) ? 1u : 0u);
         mma_commit(smem_u32(&v_empty[st]));
-        mma_commit(smem_u32(&pv_done[jt & 1]));
+        mma_commit(smem_u32(&pv_done[gt & 1]));
         return true;
       };
-      bool ok = mbar_wait(smem_u32(&q_full), 0, &abort_flag, status, kSiteQ);
-      for (int i = 0; ok && i < n_tiles; ++i) {
-        const int st = i % C::KS;
-        if (!mbar_wait(smem_u32(&k_full[st]), (i / C::KS) & 1, &abort_flag, status, kSiteKFull)) {
-          ok = false;
-          break;
-        }
-        // S is single-buffered: the softmax must have read S_{i-1}.
-        if (i >= 1 &&
-            !mbar_wait(smem_u32(&s_free), (i - 1) & 1, &abort_flag, status, kSiteSFree)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t k_addr = smem_u32(sK + st * C::KV_BYTES);
+      bool ok = true;
+      int g = 0;
+      for (int rr = 0, pos; ok && (pos = item_position(rr)) < num_items; ++rr) {
+        const Item it = decode_item<C::TQ>(pos, num_q_tiles, gsz, B, H_kv, T, window, pad_lens);
+        if (it.pad) continue;
+        if (!mbar_wait(smem_u32(&q_full), nitem & 1, &abort_flag, status, kSiteQ)) break;
+        for (int i = 0; i < it.n_tiles; ++i, ++g) {
+          const int st = g % C::KS;
+          if (!mbar_wait(smem_u32(&k_full[st]), (g / C::KS) & 1, &abort_flag, status,
+                         kSiteKFull)) {
+            ok = false;
+            break;
+          }
+          // S is single-buffered: the softmax must have read the previous S.
+          if (g >= 1 &&
+              !mbar_wait(smem_u32(&s_free), (g - 1) & 1, &abort_flag, status, kSiteSFree)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t k_addr = smem_u32(sK + st * C::KV_BYTES);
 #pragma unroll
-        for (int k = 0; k < DH / 16; ++k) {
-          const uint32_t off = (k >> 2) * CHUNK + (k & 3) * 32;
-          mma_ss(tbase + S_COL, sdesc_sw128(q_addr + off, 16, 1024),
-                 sdesc_sw128(k_addr + off, 16, 1024), idesc_qk, k > 0 ? 1u : 0u);
+          for (int k = 0; k < DH / 16; ++k) {
+            const uint32_t off = (k >> 2) * CHUNK + (k & 3) * 32;
+            mma_ss(tbase + S_COL, sdesc_sw128(q_addr + off, 16, 1024),
+                   sdesc_sw128(k_addr + off, 16, 1024), idesc_qk, k > 0 ? 1u : 0u);
+          }
+          mma_commit(smem_u32(&k_empty[st]));
+          mma_commit(smem_u32(&s_full));
+          if (i == it.n_tiles - 1) mma_commit(smem_u32(&q_empty));
+          if (i >= 1 && !issue_pv(g - 1, i - 1)) {
+            ok = false;
+            break;
+          }
         }
-        mma_commit(smem_u32(&k_empty[st]));
-        mma_commit(smem_u32(&s_full));
-        if (i >= 1 && !issue_pv(i - 1)) {
-          ok = false;
-          break;
-        }
+        // o_final: this item's O accumulation is complete.
+        if (!ok || !issue_pv(g - 1, it.n_tiles - 1)) break;
+        mma_commit(smem_u32(&o_final));
+        ++nitem;
       }
-      // o_final: the whole O accumulation is complete.
-      if (ok && issue_pv(n_tiles - 1)) mma_commit(smem_u32(&o_final));
       mma_commit(smem_u32(&drain));
       mbar_wait_drain(smem_u32(&drain), 0);
     }
@@ -262,130 +321,154 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int wg = (warp - 4) >> 2;        // column half of every row
     const int q = warp & 3;                // TMEM lane quarter (= warp % 4)
     const int r = q * 32 + lane;           // query row of this thread
-    const int i_tok = r / G, g = r % G;
-    const int t = t0 + i_tok;
-    const int h = j * G + g;
+    const int i_tok = r / G, gh = r % G;
     const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
     const int c_base = wg * (BN / 2);
-    const int kv_lo = window > 0 ? t - window + 1 : 0;   // keys kv_lo..kv_hi are kept
-    const int kv_hi = min(t, valid - 1);
     const uint32_t rbar = smem_u32(&red_bar[q]);
-    float m_used = -INFINITY, l = 0.f;
+    int g = 0, nitem = 0, hs = 0;   // global tile, items, handshakes
     bool ok = true;
-    int i = 0;
-    for (; i < n_tiles; ++i) {
-      ok = __all_sync(0xffffffffu,
-                      mbar_wait(smem_u32(&s_full), i & 1, &abort_flag, status, kSiteSFull));
-      if (!ok) break;
-      tc_fence_after();
-      float s[BN / 2];
-      {
-        uint32_t rr[32];
-        tmem_ld32(tbase + lane_off + S_COL + c_base, rr);
-        tmem_ld_wait();
-#pragma unroll
-        for (int e = 0; e < 32; ++e) s[e] = __uint_as_float(rr[e]);
-        tmem_ld32(tbase + lane_off + S_COL + c_base + 32, rr);
-        tmem_ld_wait();
-#pragma unroll
-        for (int e = 0; e < 32; ++e) s[32 + e] = __uint_as_float(rr[e]);
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&s_free));
-
-      const int s_tile = (tile_lo + i) * BN;
-      const bool need_mask = (s_tile + BN - 1 > t0) || (s_tile + BN > valid) ||
-                             (window > 0 && s_tile <= t_last - window);
-      if (need_mask) {
-        const int c_lo = kv_lo - (s_tile + c_base), c_hi = kv_hi - (s_tile + c_base);
-#pragma unroll
-        for (int c = 0; c < BN / 2; ++c)
-          if (c < c_lo || c > c_hi) s[c] = -INFINITY;
-      }
-      float mx = s[0];
-#pragma unroll
-      for (int c = 1; c < BN / 2; ++c) mx = fmaxf(mx, s[c]);
-      // Row max over both column halves: exchange with the partner thread.
-      red[i & 1][wg][r] = mx;
-      __syncwarp();
-      if (lane == 0) mbar_arrive(rbar);
-      ok = __all_sync(0xffffffffu, mbar_wait(rbar, i & 1, &abort_flag, status, kSiteRed));
-      if (!ok) break;
-      mx = fmaxf(mx, red[i & 1][wg ^ 1][r]) * LOG2E;
-
-      const bool grow = mx > m_used + RESCALE_THRESHOLD;
-      if (__any_sync(0xffffffffu, grow)) {
-        const float m_new = grow ? mx : m_used;
-        const float factor = (m_new == m_used) ? 1.f : ex2(m_used - m_new);
-        if (i > 0) {
-          // O holds PV_0..PV_{i-1}: rescale this half of its columns once
-          // PV_{i-1} has landed.
-          ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&pv_done[(i - 1) & 1]),
-                                                 ((i - 1) >> 1) & 1, &abort_flag, status,
-                                                 kSiteORescale));
-          if (!ok) break;
-          tc_fence_after();
-#pragma unroll 1
-          for (int c = 0; c < DH / 64; ++c) {
-            uint32_t rr[32];
-            const uint32_t ta = tbase + lane_off + O_COL + wg * (DH / 2) + c * 32;
-            tmem_ld32(ta, rr);
-            tmem_ld_wait();
-#pragma unroll
-            for (int e = 0; e < 32; ++e) rr[e] = __float_as_uint(__uint_as_float(rr[e]) * factor);
-            tmem_st32(ta, rr);
-          }
-          tmem_st_wait();
+    for (int rr = 0, pos; ok && (pos = item_position(rr)) < num_items; ++rr) {
+      const Item it = decode_item<C::TQ>(pos, num_q_tiles, gsz, B, H_kv, T, window, pad_lens);
+      if (it.pad) {
+        // The whole tile is padding: its output rows are zero (bits 0 in bf16 and f16).
+        const int rows = min(C::TQ, T - it.t0);
+        const int vecs = rows * G * (DH / 8);
+        for (int v = threadIdx.x - 128; v < vecs; v += SM_WARPS * 32) {
+          const int e = v * 8;
+          const int c = e % DH, rg = e / DH;
+          const int gg = rg % G, ii = rg / G;
+          *reinterpret_cast<uint4*>(
+              O + ((static_cast<size_t>(it.b) * T + it.t0 + ii) * H + it.j * G + gg) * DH + c) =
+              make_uint4(0, 0, 0, 0);
         }
-        l *= factor;
-        m_used = m_new;
+        continue;
       }
-      const float mref = (m_used == -INFINITY) ? 0.f : m_used;
-      float sum = 0.f;
-      uint32_t p[32];
-#pragma unroll
-      for (int e = 0; e < 32; ++e) {
-        const float p0 = ex2(fmaf(s[2 * e], LOG2E, -mref));
-        const float p1 = ex2(fmaf(s[2 * e + 1], LOG2E, -mref));
-        sum += p0 + p1;
-        p[e] = pack_half2(p0, p1);
-      }
-      l += sum;
-      if (i >= 2) {
-        // P buffer i%2 is free once PV_{i-2} has read it.
-        ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&pv_done[i & 1]), ((i - 2) >> 1) & 1,
-                                               &abort_flag, status, kSitePFree));
+      const int t = it.t0 + i_tok;
+      const int h = it.j * G + gh;
+      const int kv_lo = window > 0 ? t - window + 1 : 0;   // keys kv_lo..kv_hi are kept
+      const int kv_hi = min(t, it.valid - 1);
+      float m_used = -INFINITY, l = 0.f;
+      for (int i = 0; i < it.n_tiles; ++i, ++g) {
+        ok = __all_sync(0xffffffffu,
+                        mbar_wait(smem_u32(&s_full), g & 1, &abort_flag, status, kSiteSFull));
         if (!ok) break;
+        tc_fence_after();
+        float s[BN / 2];
+        {
+          uint32_t ra[32], rb[32];
+          tmem_ld32(tbase + lane_off + S_COL + c_base, ra);
+          tmem_ld32(tbase + lane_off + S_COL + c_base + 32, rb);
+          tmem_ld_wait(ra);
+          tmem_ld_wait(rb);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            s[e] = __uint_as_float(ra[e]);
+            s[32 + e] = __uint_as_float(rb[e]);
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&s_free));
+
+        const int s_tile = (it.tile_lo + i) * BN;
+        const bool need_mask = (s_tile + BN - 1 > it.t0) || (s_tile + BN > it.valid) ||
+                               (window > 0 && s_tile <= it.t_last - window);
+        if (need_mask) {
+          const int c_lo = kv_lo - (s_tile + c_base), c_hi = kv_hi - (s_tile + c_base);
+#pragma unroll
+          for (int c = 0; c < BN / 2; ++c)
+            if (c < c_lo || c > c_hi) s[c] = -INFINITY;
+        }
+        // Row max with eight independent partial maxima (short dependency chains).
+        float m8[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) m8[k] = s[k];
+#pragma unroll
+        for (int c = 8; c < BN / 2; ++c) m8[c & 7] = fmaxf(m8[c & 7], s[c]);
+        float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                         fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+        // Row max over both column halves: exchange with the partner thread.
+        red[hs & 1][wg][r] = mx;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(rbar);
+        ok = __all_sync(0xffffffffu, mbar_wait(rbar, hs & 1, &abort_flag, status, kSiteRed));
+        if (!ok) break;
+        mx = fmaxf(mx, red[hs & 1][wg ^ 1][r]) * LOG2E;
+        ++hs;
+
+        const bool grow = mx > m_used + RESCALE_THRESHOLD;
+        if (__any_sync(0xffffffffu, grow)) {
+          const float m_new = grow ? mx : m_used;
+          const float factor = (m_new == m_used) ? 1.f : ex2(m_used - m_new);
+          if (i > 0) {
+            // O holds this item's PV so far: rescale this half of its
+            // columns once the previous PV has landed.
+            ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&pv_done[(g - 1) & 1]),
+                                                   ((g - 1) >> 1) & 1, &abort_flag, status,
+                                                   kSiteORescale));
+            if (!ok) break;
+            tc_fence_after();
+#pragma unroll 1
+            for (int c = 0; c < DH / 64; ++c) {
+              uint32_t rr[32];
+              const uint32_t ta = tbase + lane_off + O_COL + wg * (DH / 2) + c * 32;
+              tmem_ld32(ta, rr);
+              tmem_ld_wait(rr);
+#pragma unroll
+              for (int e = 0; e < 32; ++e)
+                rr[e] = __float_as_uint(__uint_as_float(rr[e]) * factor);
+              tmem_st32(ta, rr);
+            }
+            tmem_st_wait();
+          }
+          l *= factor;
+          m_used = m_new;
+        }
+        const float mref = (m_used == -INFINITY) ? 0.f : m_used;
+        float sum4[4] = {0.f, 0.f, 0.f, 0.f};
+        uint32_t p[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const float p0 = ex2(fmaf(s[2 * e], LOG2E, -mref));
+          const float p1 = ex2(fmaf(s[2 * e + 1], LOG2E, -mref));
+          sum4[e & 3] += p0 + p1;
+          p[e] = pack_half2(p0, p1);
+        }
+        l += (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
+        if (g >= 2) {
+          // P buffer g%2 is free once the PV two tiles back has read it.
+          ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&pv_done[g & 1]), ((g - 2) >> 1) & 1,
+                                                 &abort_flag, status, kSitePFree));
+          if (!ok) break;
+        }
+        tmem_st32(tbase + lane_off + P_COL + (g & 1) * 64 + wg * 32, p);
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&p_full[g & 1]));
       }
-      tmem_st32(tbase + lane_off + P_COL + (i & 1) * 64 + wg * 32, p);
-      tmem_st_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&p_full[i & 1]));
-    }
-    if (ok) {
+      if (!ok) break;
       ok = __all_sync(0xffffffffu,
-                      mbar_wait(smem_u32(&o_final), 0, &abort_flag, status, kSiteOFinal));
-    }
-    if (ok) {
-      // Row sum over both halves (one more handshake phase), then 1/l and store.
-      red[i & 1][wg][r] = l;
+                      mbar_wait(smem_u32(&o_final), nitem & 1, &abort_flag, status, kSiteOFinal));
+      if (!ok) break;
+      // Row sum over both halves (one more handshake), then 1/l and store.
+      red[hs & 1][wg][r] = l;
       __syncwarp();
       if (lane == 0) mbar_arrive(rbar);
-      ok = __all_sync(0xffffffffu, mbar_wait(rbar, i & 1, &abort_flag, status, kSiteRed));
-    }
-    if (ok) {
+      ok = __all_sync(0xffffffffu, mbar_wait(rbar, hs & 1, &abort_flag, status, kSiteRed));
+      if (!ok) break;
+      const float l_tot = l + red[hs & 1][wg ^ 1][r];
+      ++hs;
       tc_fence_after();
-      const float l_tot = l + red[i & 1][wg ^ 1][r];
-      const bool row_valid = t < valid;
+      const bool row_valid = t < it.valid;
       const float inv_l = row_valid ? 1.f / l_tot : 0.f;
-      uint16_t* dst = O + ((static_cast<size_t>(b) * T + t) * H + h) * DH + wg * (DH / 2);
+      uint16_t* dst =
+          O + ((static_cast<size_t>(it.b) * T + t) * H + h) * DH + wg * (DH / 2);
 #pragma unroll 1
       for (int c = 0; c < DH / 64; ++c) {
         uint32_t rr[32];
         tmem_ld32(tbase + lane_off + O_COL + wg * (DH / 2) + c * 32, rr);
-        tmem_ld_wait();
+        tmem_ld_wait(rr);
         if (t < T) {
 #pragma unroll
           for (int v = 0; v < 4; ++v) {
@@ -405,6 +488,11 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
         }
       }
+      // O may now be overwritten by the next item's first PV.
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&o_free));
+      ++nitem;
     }
   }
   __syncthreads();
@@ -443,11 +531,19 @@ cudaError_t launch_cfg(const void* Q, const void* K, const void* V, long ldkv, v
     attr_set = true;
   }
   const int num_q_tiles = (T + C::TQ - 1) / C::TQ;
-  const long grid = static_cast<long>(num_q_tiles) * B * H_kv;
-  if (grid > 0x7fffffffL) return cudaErrorInvalidValue;
-  kern<<<static_cast<unsigned>(grid), THREADS, C::SMEM, stream>>>(
-      tq, tk, tv, static_cast<uint16_t*>(O), o_dtype == kF16 ? 1 : 0, pad_lens, B, T, H, H_kv,
-      window, num_q_tiles, status);
+  const long items = static_cast<long>(num_q_tiles) * B * H_kv;
+  if (items > 0x7fffffffL) return cudaErrorInvalidValue;
+  const int grid = static_cast<int>(items < num_sms() ? items : num_sms());
+  // (b, j) pairs per ordering group: as many as keep their K/V (T x d_h x 2
+  // tensors x 2 B) within ~48 MB of L2; local layers touch only a window of
+  // K/V per item, so they use a single group (pure heavy-first order).
+  const double kv_bytes = static_cast<double>(T) * DH * 2.0 * 2.0;
+  int gsz = window > 0 ? B * H_kv : static_cast<int>(48.0 * 1024 * 1024 / kv_bytes);
+  gsz = gsz < 1 ? 1 : (gsz > B * H_kv ? B * H_kv : gsz);
+  kern<<<grid, THREADS, C::SMEM, stream>>>(tq, tk, tv, static_cast<uint16_t*>(O),
+                                           o_dtype == kF16 ? 1 : 0, pad_lens, B, T, H, H_kv,
+                                           window, num_q_tiles, gsz, static_cast<int>(items),
+                                           status);
   return cudaGetLastError();
 }
 

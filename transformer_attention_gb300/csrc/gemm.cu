@@ -201,7 +201,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (col0 >= N) break;
         uint32_t r[32];
         tmem_ld32(tbase + lane_off + abuf * BN + c * 32, r);
-        tmem_ld_wait();
+        tmem_ld_wait(r);
         if (row < M) {
           const int ncols = min(32, N - col0);
           OutT* dst = C + static_cast<long>(row) * ldc + col0;
