@@ -30,10 +30,10 @@
 //               warpgroup wg in {0,1} handles columns [64 wg, 64 wg + 64) of
 //               every row, exchanging the row max with its partner thread
 //               through shared memory (a bounded mbarrier handshake).
-// TMEM columns: S 0-127 | P[0] 128-191 | P[1] 192-255 | O 256..256+d_h.
-// S is single-buffered: the softmax releases it (s_free) as soon as it has
-// loaded the row into registers, so S_{i+1} overlaps the exponentials of
-// tile i; P is double-buffered so PV_{i-1} and the softmax of tile i never
+// TMEM columns: S 0-127 | P[0] 128-191 | P[1] 192-255 | O 256..256+d_h, and
+// for d_h = 128 a second S buffer at 384-511.  The softmax releases an S
+// buffer (s_free) as soon as it has loaded its rows into registers, so the
+// next S overlaps the exponentials of this tile; P is double-buffered so PV_{i-1} and the softmax of tile i never
 // touch the same columns.  O is rescaled in TMEM only when a row max grows by
 // more than 2^8, each warpgroup rescaling its half of the columns.
 #include "internal.h"
@@ -49,7 +49,7 @@ constexpr int BM = 128;   // query rows per CTA
 constexpr int BN = 128;   // keys per KV tile
 constexpr int SM_WARPS = 8;  // softmax warps
 constexpr uint32_t CHUNK = 128 * 128;  // one 128-row x 64-element (128 B) swizzled chunk
-constexpr uint32_t S_COL = 0, P_COL = 128, O_COL = 256;
+constexpr uint32_t P_COL = 128, O_COL = 256;
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr float RESCALE_THRESHOLD = 8.0f;  // log2 units
 
@@ -69,7 +69,17 @@ struct Cfg {
   static constexpr uint32_t KV_BYTES = BN * DH * 2;
   static constexpr uint32_t SMEM = Q_BYTES + (KS + VS) * KV_BYTES + 1024;
   static_assert(SMEM + 2304 <= 232448, "shared memory budget");
+  // S buffers in TMEM: one at columns 0-127; with d_h = 128 the columns
+  // 384-511 left over by O hold a second one.
+  static constexpr int NS = (DH == 128) ? 2 : 1;
+  static __device__ __forceinline__ uint32_t s_col(int buf) { return buf == 0 ? 0u : 384u; }
 };
+
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
 
 __device__ __forceinline__ float ex2(float x) {
   float y;
@@ -141,8 +151,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint8_t* sK = smem + C::Q_BYTES;                    // KS stages
   uint8_t* sV = sK + C::KS * C::KV_BYTES;             // VS stages
   __shared__ __align__(8) uint64_t q_full, q_empty, k_full[C::KS], k_empty[C::KS],
-      v_full[C::VS], v_empty[C::VS], s_full, s_free, p_full[2], pv_done[2], o_final, o_free,
-      drain, red_bar[4];
+      v_full[C::VS], v_empty[C::VS], s_full[C::NS], s_free[C::NS], p_full[2], pv_done[2],
+      o_final, o_free, drain, red_bar[4];
   __shared__ float red[2][2][BM];   // [handshake parity][warpgroup][row]
   __shared__ uint32_t tmem_sh;
   __shared__ int abort_flag;
@@ -158,8 +168,10 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_init(smem_u32(&v_full[s]), 1);
       mbar_init(smem_u32(&v_empty[s]), 1);
     }
-    mbar_init(smem_u32(&s_full), 1);
-    mbar_init(smem_u32(&s_free), SM_WARPS);
+    for (int s = 0; s < C::NS; ++s) {
+      mbar_init(smem_u32(&s_full[s]), 1);
+      mbar_init(smem_u32(&s_free[s]), SM_WARPS);
+    }
     for (int s = 0; s < 2; ++s) {
       mbar_init(smem_u32(&p_full[s]), SM_WARPS);
       mbar_init(smem_u32(&pv_done[s]), 1);
@@ -286,9 +298,10 @@ __global__ void __launch_bounds__(THREADS, 1)
             ok = false;
             break;
           }
-          // S is single-buffered: the softmax must have read the previous S.
-          if (g >= 1 &&
-              !mbar_wait(smem_u32(&s_free), (g - 1) & 1, &abort_flag, status, kSiteSFree)) {
+          // S buffer g % NS: the softmax must have read the S it held before.
+          const int sb = g % C::NS;
+          if (g >= C::NS && !mbar_wait(smem_u32(&s_free[sb]), ((g / C::NS) - 1) & 1, &abort_flag,
+                                       status, kSiteSFree)) {
             ok = false;
             break;
           }
@@ -297,11 +310,11 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
           for (int k = 0; k < DH / 16; ++k) {
             const uint32_t off = (k >> 2) * CHUNK + (k & 3) * 32;
-            mma_ss(tbase + S_COL, sdesc_sw128(q_addr + off, 16, 1024),
+            mma_ss(tbase + C::s_col(sb), sdesc_sw128(q_addr + off, 16, 1024),
                    sdesc_sw128(k_addr + off, 16, 1024), idesc_qk, k > 0 ? 1u : 0u);
           }
           mma_commit(smem_u32(&k_empty[st]));
-          mma_commit(smem_u32(&s_full));
+          mma_commit(smem_u32(&s_full[sb]));
           if (i == it.n_tiles - 1) mma_commit(smem_u32(&q_empty));
           if (i >= 1 && !issue_pv(g - 1, i - 1)) {
             ok = false;
@@ -349,15 +362,16 @@ __global__ void __launch_bounds__(THREADS, 1)
       const int kv_hi = min(t, it.valid - 1);
       float m_used = -INFINITY, l = 0.f;
       for (int i = 0; i < it.n_tiles; ++i, ++g) {
-        ok = __all_sync(0xffffffffu,
-                        mbar_wait(smem_u32(&s_full), g & 1, &abort_flag, status, kSiteSFull));
+        const int sb = g % C::NS;
+        ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&s_full[sb]), (g / C::NS) & 1,
+                                               &abort_flag, status, kSiteSFull));
         if (!ok) break;
         tc_fence_after();
         float s[BN / 2];
         {
           uint32_t ra[32], rb[32];
-          tmem_ld32(tbase + lane_off + S_COL + c_base, ra);
-          tmem_ld32(tbase + lane_off + S_COL + c_base + 32, rb);
+          tmem_ld32(tbase + lane_off + C::s_col(sb) + c_base, ra);
+          tmem_ld32(tbase + lane_off + C::s_col(sb) + c_base + 32, rb);
           tmem_ld_wait(ra);
           tmem_ld_wait(rb);
 #pragma unroll
@@ -368,7 +382,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&s_free));
+        if (lane == 0) mbar_arrive(smem_u32(&s_free[sb]));
 
         const int s_tile = (it.tile_lo + i) * BN;
         const bool need_mask = (s_tile + BN - 1 > it.t0) || (s_tile + BN > it.valid) ||
@@ -379,14 +393,15 @@ __global__ void __launch_bounds__(THREADS, 1)
           for (int c = 0; c < BN / 2; ++c)
             if (c < c_lo || c > c_hi) s[c] = -INFINITY;
         }
-        // Row max with eight independent partial maxima (short dependency chains).
+        // Row max: eight independent partial maxima fed two values per
+        // three-input max (short dependency chains, half the instructions).
         float m8[8];
 #pragma unroll
         for (int k = 0; k < 8; ++k) m8[k] = s[k];
 #pragma unroll
-        for (int c = 8; c < BN / 2; ++c) m8[c & 7] = fmaxf(m8[c & 7], s[c]);
-        float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                         fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+        for (int c = 8; c < BN / 2; c += 2) m8[(c >> 1) & 7] = fmax3(m8[(c >> 1) & 7], s[c], s[c + 1]);
+        float mx = fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]),
+                         fmaxf(m8[6], m8[7]));
         // Row max over both column halves: exchange with the partner thread.
         red[hs & 1][wg][r] = mx;
         __syncwarp();
@@ -425,16 +440,22 @@ __global__ void __launch_bounds__(THREADS, 1)
           m_used = m_new;
         }
         const float mref = (m_used == -INFINITY) ? 0.f : m_used;
-        float sum4[4] = {0.f, 0.f, 0.f, 0.f};
+        // Exponentials in pairs: one packed fp32x2 FMA forms s*log2(e) - m
+        // for two columns, one packed add accumulates the row sum.
+        const float2 l2e = make_float2(LOG2E, LOG2E), negm = make_float2(-mref, -mref);
+        float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                         make_float2(0.f, 0.f)};
         uint32_t p[32];
 #pragma unroll
         for (int e = 0; e < 32; ++e) {
-          const float p0 = ex2(fmaf(s[2 * e], LOG2E, -mref));
-          const float p1 = ex2(fmaf(s[2 * e + 1], LOG2E, -mref));
-          sum4[e & 3] += p0 + p1;
-          p[e] = pack_half2(p0, p1);
+          const float2 xx = __ffma2_rn(make_float2(s[2 * e], s[2 * e + 1]), l2e, negm);
+          const float2 pp = make_float2(ex2(xx.x), ex2(xx.y));
+          acc[e & 3] = __fadd2_rn(acc[e & 3], pp);
+          p[e] = pack_half2(pp.x, pp.y);
         }
-        l += (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
+        const float2 a01 = __fadd2_rn(acc[0], acc[1]), a23 = __fadd2_rn(acc[2], acc[3]);
+        const float2 a = __fadd2_rn(a01, a23);
+        l += a.x + a.y;
         if (g >= 2) {
           // P buffer g%2 is free once the PV two tiles back has read it.
           ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&pv_done[g & 1]), ((g - 2) >> 1) & 1,

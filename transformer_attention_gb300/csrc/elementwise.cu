@@ -14,7 +14,8 @@
 //   is formed as an fp32 double-float (exact two-product of pos and the split
 //   frequency, split hi + lo on the host in double precision) and reduced
 //   modulo 2*pi by Cody-Waite with a two-part 2*pi, so positions up to 2^24
-//   keep ~1e-6 rad of angle error without any fp64 work on the device.  Rows
+//   keep ~1e-6 rad of angle error without any fp64 work on the device; sin
+//   and cos of the reduced angle come from the hardware approximation.  Rows
 //   are updated in place.
 //
 // rmsnorm_rows / postnorm_residual: the D-axis norms of the block sandwich
@@ -41,10 +42,10 @@ struct RopeFreqs {
   float2 f[128];
 };
 
-constexpr int kVecUnroll = 4;  // head vectors in flight per lane
+constexpr int kVecUnroll = 8;  // head vectors in flight per lane
 
 template <int DH>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(256, 2)
     qk_norm_rope_kernel(__half* __restrict__ Q, long ldq, __half* __restrict__ K, long ldk,
                         const __nv_bfloat16* __restrict__ gamma_q,
                         const __nv_bfloat16* __restrict__ gamma_k, const int32_t* __restrict__ pos,
@@ -58,48 +59,55 @@ __global__ void __launch_bounds__(256)
   const bool second_half = ll >= HALF;
   const int c0 = (ll % HALF) * 8;  // first rotation pair index of this lane
 
-  float f_hi[8], f_lo[8], gq[8], gk[8];
-#pragma unroll
-  for (int e = 0; e < 8; ++e) {
-    const float2 f = freqs.f[c0 + e];
-    f_hi[e] = f.x;
-    f_lo[e] = f.y;
-    gq[e] = 1.f + __bfloat162float(gamma_q[ll * 8 + e]);
-    gk[e] = 1.f + __bfloat162float(gamma_k[ll * 8 + e]);
-  }
+  // (1 + gamma) of this lane's 8 channels, kept packed (bf16x8) to save registers.
+  const uint4 gq_raw = *reinterpret_cast<const uint4*>(gamma_q + ll * 8);
+  const uint4 gk_raw = *reinterpret_cast<const uint4*>(gamma_k + ll * 8);
 
   const int warps_total = gridDim.x * (blockDim.x >> 5);
   const int nvec = H + H_kv;
   for (int m = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); m < M; m += warps_total) {
+    // Issue this token's head-vector loads first, then the angle math.
+    uint4 raw[kVecUnroll];
+    const int first = sub;
+#pragma unroll
+    for (int u = 0; u < kVecUnroll; ++u) {
+      const int hv = first + u * VPW;
+      const __half* src = hv < H ? Q + static_cast<long>(m) * ldq + hv * DH
+                                 : K + static_cast<long>(m) * ldk + (hv - H) * DH;
+      raw[u] = hv < nvec ? *reinterpret_cast<const uint4*>(src + ll * 8) : make_uint4(0, 0, 0, 0);
+    }
     const float p = static_cast<float>(pos[m]);
     float cs[8], sn[8];
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
-      const float a_hi = p * f_hi[e];
-      const float a_err = fmaf(p, f_hi[e], -a_hi);     // exact residual of the product
-      const float a_lo = fmaf(p, f_lo[e], a_err);
+      const float2 f = freqs.f[c0 + e];
+      const float a_hi = p * f.x;
+      const float a_err = fmaf(p, f.x, -a_hi);     // exact residual of the product
+      const float a_lo = fmaf(p, f.y, a_err);
       const float k = rintf(a_hi * kInvTwoPi);
       float r = fmaf(-k, kTwoPiHi, a_hi);
       r = fmaf(-k, kTwoPiMid, r);
       r += a_lo;
-      sincosf(r, &sn[e], &cs[e]);
+      // r is already reduced to about [-pi, pi], where the hardware
+      // approximation's absolute error (~2^-21) is far below fp16 rounding.
+      __sincosf(r, &sn[e], &cs[e]);
     }
     for (int base = 0; base < nvec; base += VPW * kVecUnroll) {
-      uint4 raw[kVecUnroll];
-      __half* ptr[kVecUnroll];
-      bool active[kVecUnroll], is_q[kVecUnroll];
+      if (base > 0) {
 #pragma unroll
-      for (int u = 0; u < kVecUnroll; ++u) {
-        const int hv = base + u * VPW + sub;
-        active[u] = hv < nvec;
-        is_q[u] = hv < H;
-        ptr[u] = (is_q[u] ? Q + static_cast<long>(m) * ldq + hv * DH
-                          : K + static_cast<long>(m) * ldk + (hv - H) * DH) + ll * 8;
-        raw[u] = active[u] ? *reinterpret_cast<const uint4*>(ptr[u]) : make_uint4(0, 0, 0, 0);
+        for (int u = 0; u < kVecUnroll; ++u) {
+          const int hv = base + first + u * VPW;
+          const __half* src = hv < H ? Q + static_cast<long>(m) * ldq + hv * DH
+                                     : K + static_cast<long>(m) * ldk + (hv - H) * DH;
+          raw[u] =
+              hv < nvec ? *reinterpret_cast<const uint4*>(src + ll * 8) : make_uint4(0, 0, 0, 0);
+        }
       }
 #pragma unroll
       for (int u = 0; u < kVecUnroll; ++u) {
         if (base + u * VPW >= nvec) break;   // warp-uniform
+        const int hv = base + first + u * VPW;
+        const bool is_q = hv < H;
         float x[8];
         const __half2* h2 = reinterpret_cast<const __half2*>(&raw[u]);
 #pragma unroll
@@ -114,12 +122,18 @@ __global__ void __launch_bounds__(256)
 #pragma unroll
         for (int off = HALF; off >= 1; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
         const float rs = rsqrtf(ss * (1.f / DH) + kEps);
+        const uint4 graw = is_q ? gq_raw : gk_raw;
+        const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&graw);
         float y[8], o[8];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) y[e] = x[e] * rs * (is_q[u] ? gq[e] : gk[e]);
+        for (int e = 0; e < 4; ++e) {
+          const float2 gf = __bfloat1622float2(g2[e]);
+          y[2 * e] = x[2 * e] * rs * (1.f + gf.x);
+          y[2 * e + 1] = x[2 * e + 1] * rs * (1.f + gf.y);
+        }
 #pragma unroll
         for (int e = 0; e < 8; ++e) o[e] = __shfl_xor_sync(0xffffffffu, y[e], HALF);
-        const float sc = is_q[u] ? query_scale : 1.f;
+        const float sc = is_q ? query_scale : 1.f;
         uint4 w;
         uint32_t* wp = reinterpret_cast<uint32_t*>(&w);
 #pragma unroll
@@ -134,7 +148,11 @@ __global__ void __launch_bounds__(256)
           }
           wp[e] = pack_half2(r0 * sc, r1 * sc);
         }
-        if (active[u]) *reinterpret_cast<uint4*>(ptr[u]) = w;
+        if (hv < nvec) {
+          __half* dst = is_q ? Q + static_cast<long>(m) * ldq + hv * DH
+                             : K + static_cast<long>(m) * ldk + (hv - H) * DH;
+          *reinterpret_cast<uint4*>(dst + ll * 8) = w;
+        }
       }
     }
   }
@@ -245,7 +263,7 @@ cudaError_t launch_qk_norm_rope(void* Q, long ldq, void* K, long ldk, const void
   if (M <= 0) return cudaSuccess;
   const int warps_per_block = 8;
   long blocks = (M + warps_per_block - 1) / warps_per_block;
-  const long cap = static_cast<long>(num_sms()) * 16;
+  const long cap = static_cast<long>(num_sms()) * 4;
   if (blocks > cap) blocks = cap;
   RopeFreqs freqs;
   for (int c = 0; c < d_h / 2; ++c) {
