@@ -33,8 +33,10 @@
 // TMEM columns: S 0-127 | P[0] 128-191 | P[1] 192-255 | O 256..256+d_h, and
 // for d_h = 128 a second S buffer at 384-511.  The softmax releases an S
 // buffer (s_free) as soon as it has loaded its rows into registers, so the
-// next S overlaps the exponentials of this tile; P is double-buffered so PV_{i-1} and the softmax of tile i never
-// touch the same columns.  O is rescaled in TMEM only when a row max grows by
+// next S overlaps the exponentials of this tile; P is double-buffered so
+// PV_{i-1} and the softmax of tile i never touch the same columns.  On
+// tiles without masked elements the row max comes from the TMEM load's own
+// max reduction (tcgen05.ld.red).  O is rescaled in TMEM only when a row max grows by
 // more than 2^8, each warpgroup rescaling its half of the columns.
 #include "internal.h"
 #include "ptx.cuh"
@@ -368,12 +370,15 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (!ok) break;
         tc_fence_after();
         float s[BN / 2];
+        float mxa, mxb;   // maxima of the two loaded 32-column groups (before masking)
         {
           uint32_t ra[32], rb[32];
-          tmem_ld32(tbase + lane_off + C::s_col(sb) + c_base, ra);
-          tmem_ld32(tbase + lane_off + C::s_col(sb) + c_base + 32, rb);
+          tmem_ld32_max(tbase + lane_off + C::s_col(sb) + c_base, ra, mxa);
+          tmem_ld32_max(tbase + lane_off + C::s_col(sb) + c_base + 32, rb, mxb);
           tmem_ld_wait(ra);
           tmem_ld_wait(rb);
+          tmem_ld_wait(mxa);
+          tmem_ld_wait(mxb);
 #pragma unroll
           for (int e = 0; e < 32; ++e) {
             s[e] = __uint_as_float(ra[e]);
@@ -387,21 +392,22 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int s_tile = (it.tile_lo + i) * BN;
         const bool need_mask = (s_tile + BN - 1 > it.t0) || (s_tile + BN > it.valid) ||
                                (window > 0 && s_tile <= it.t_last - window);
+        float mx = fmaxf(mxa, mxb);   // the loads' own reduction (unmasked tiles)
         if (need_mask) {
           const int c_lo = kv_lo - (s_tile + c_base), c_hi = kv_hi - (s_tile + c_base);
 #pragma unroll
           for (int c = 0; c < BN / 2; ++c)
             if (c < c_lo || c > c_hi) s[c] = -INFINITY;
+          // Row max after masking: eight independent partial maxima fed two
+          // values per three-input max.
+          float m8[8];
+#pragma unroll
+          for (int k = 0; k < 8; ++k) m8[k] = s[k];
+#pragma unroll
+          for (int c = 8; c < BN / 2; c += 2)
+            m8[(c >> 1) & 7] = fmax3(m8[(c >> 1) & 7], s[c], s[c + 1]);
+          mx = fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
         }
-        // Row max: eight independent partial maxima fed two values per
-        // three-input max (short dependency chains, half the instructions).
-        float m8[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) m8[k] = s[k];
-#pragma unroll
-        for (int c = 8; c < BN / 2; c += 2) m8[(c >> 1) & 7] = fmax3(m8[(c >> 1) & 7], s[c], s[c + 1]);
-        float mx = fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]),
-                         fmaxf(m8[6], m8[7]));
         // Row max over both column halves: exchange with the partner thread.
         red[hs & 1][wg][r] = mx;
         __syncwarp();
