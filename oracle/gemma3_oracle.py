@@ -268,3 +268,49 @@ def attention_stack(x, layers, *, model_size, H, H_kv, d_h, segment_pos, pad_len
             attn_type=types[l], window=window, rope_base=base, rope_scale=scale,
             query_scale=query_pre_attn_scalar(model_size, D, H, d_h))
     return h
+
+
+# ----------------------------------------------------------------------------
+# the feed-forward half of the block
+# ----------------------------------------------------------------------------
+def ffn_hidden_dim(model_size: str, D: int) -> int:
+    """[FB] How it works (MLP): hidden widths 2048 on 270M, 6D on 1B, and 4D on
+    4B/12B/27B (hidden_dim = embed_dim * 8 // 2)."""
+    if model_size == "270M":
+        return 2048
+    if model_size == "1B":
+        return 6 * D
+    return D * 8 // 2
+
+
+def gelu_tanh(x: torch.Tensor) -> torch.Tensor:
+    """[FB] How it works (MLP): the Flax default GELU, its tanh approximation:
+    0.5 x (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3)))."""
+    x = x.to(F64)
+    return 0.5 * x * (1.0 + torch.tanh(math.sqrt(2.0 / math.pi) * (x + 0.044715 * x ** 3)))
+
+
+def feed_forward(u: torch.Tensor, W_gating: torch.Tensor, W_down: torch.Tensor) -> torch.Tensor:
+    """[FB] How it works (MLP): the gating einsum '...F,NHF->...NH' with the
+    weight stored as (2, D_ff, D) gives [..., 2, D_ff]; slice 0 is uW_g and
+    slice 1 is uW_u; FFN(u) = (GELU(uW_g) * (uW_u)) W_d with W_d of shape
+    (D_ff, D)."""
+    gate_up = torch.einsum("...f,nhf->...nh", u.to(F64), W_gating.to(F64))
+    z = gelu_tanh(gate_up[..., 0, :]) * gate_up[..., 1, :]
+    return torch.matmul(z, W_down.to(F64))
+
+
+def block_ffn(h, gamma_pre_ffn, gamma_post_ffn, W_gating, W_down):
+    """[FB] How it works, last three lines of Block.__call__:
+    m = FFN(RMSNorm_pre-ffn(h)); m <- RMSNorm_post-ffn(m); y = h + m.
+    Rows are independent (pad rows too: the pages define no mask here)."""
+    m = feed_forward(rms_norm(h, gamma_pre_ffn), W_gating, W_down)
+    return h.to(F64) + rms_norm(m, gamma_post_ffn)
+
+
+def full_block(x, gamma_pre_attn, gamma_post_attn, gamma_pre_ffn, gamma_post_ffn, W_gating,
+               W_down, **layer_kwargs):
+    """[FB] How it works, Block.__call__: the attention sandwich, then the
+    feed-forward sandwich, on the residual stream (fp64)."""
+    h = block_attention(x, gamma_pre_attn, gamma_post_attn, **layer_kwargs)
+    return block_ffn(h, gamma_pre_ffn, gamma_post_ffn, W_gating, W_down)

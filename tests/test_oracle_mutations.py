@@ -161,3 +161,41 @@ def test_padding_ignored_is_caught(monkeypatch):
 
     monkeypatch.setattr(O, "attention_layer", no_zero)
     assert _fails(P.test_bruteforce_matches, False, 0, 9, 4, 1)
+
+
+# ---------------------------------------------------------------- feed-forward half
+from tests import test_oracle_ffn_pins as PF  # noqa: E402
+
+
+def test_gate_and_up_swapped_is_caught(monkeypatch):
+    real = O.feed_forward
+    monkeypatch.setattr(O, "feed_forward", lambda u, W, Wd: real(u, W.flip(0), Wd))
+    assert _fails(PF.test_feed_forward_scalar_brute_force)
+
+
+def test_exact_erf_gelu_is_caught(monkeypatch):
+    # The page names the approximate tanh form, not the erf form.
+    monkeypatch.setattr(O, "gelu_tanh",
+                        lambda x: x.to(F64) * 0.5 * (1 + torch.special.erf(x.to(F64) / 2 ** 0.5)))
+    assert _fails(PF.test_gelu_tanh_odd_part_is_identity) or _fails(
+        PF.test_feed_forward_scalar_brute_force)
+    assert _fails(PF.test_gelu_tanh_is_close_to_exact_gelu)
+
+
+def test_gelu_on_up_slice_is_caught(monkeypatch):
+    def wrong(u, W, Wd):
+        gu = torch.einsum("...f,nhf->...nh", u.to(F64), W.to(F64))
+        return torch.matmul(gu[..., 0, :] * O.gelu_tanh(gu[..., 1, :]), Wd.to(F64))
+    monkeypatch.setattr(O, "feed_forward", wrong)
+    assert _fails(PF.test_feed_forward_scalar_brute_force)
+
+
+def test_missing_post_ffn_norm_is_caught(monkeypatch):
+    monkeypatch.setattr(O, "block_ffn", lambda h, g1, g2, W, Wd: h.to(F64) + O.feed_forward(
+        O.rms_norm(h, g1), W, Wd))
+    assert _fails(PF.test_block_ffn_structural_zeros)
+
+
+def test_hidden_width_8d_is_caught(monkeypatch):
+    monkeypatch.setattr(O, "ffn_hidden_dim", lambda size, D: 8 * D)
+    assert _fails(PF.test_hidden_dims_match_page)
