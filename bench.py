@@ -5,7 +5,8 @@
 One step is one pass of the whole hot path over one batch of synthetic input:
 the Q and KV projections, the QK-norm + RoPE + query-scale prologue, flash
 attention and the output projection (for the 6-layer stack, all six routed
-block-attention layers including their pre/post norms).  Inputs are resident
+block-attention layers including their pre/post norms; for the full-block
+workload, the attention sandwich and the GeGLU feed-forward sandwich).  Inputs are resident
 in HBM when the timed region starts; L2 is flushed (a 256 MiB write) before
 every timed step, outside the step's CUDA events.  Prints one JSON line.
 
@@ -159,12 +160,15 @@ class ClockSampler:
 class LayerBuffers:
     """Device inputs and the stage buffers of one attention layer."""
 
-    def __init__(self, w, layer, x_dev, torch, G3, stack=False):
+    def __init__(self, w, layer, x_dev, torch, G3, block=False):
         self.w = w
         p = WL.weights(w, layer)
         self.p = {k: v.cuda() for k, v in p.items()}
-        if stack:
+        if block:
             self.p.update({k: v.cuda() for k, v in WL.block_norm_gammas(w, layer).items()})
+        if w.d_ff > 0:
+            self.p.update({k: v.cuda() for k, v in WL.ffn_weights(w, layer).items()})
+        if w.attn_type == "stack":
             t, win, base, scale = G3.gemma3_layer_config(layer, w.num_layers, w.model_size)
             self.attn_type, self.window, self.rope_base, self.rope_scale = t, win, base, scale
         else:
@@ -185,7 +189,10 @@ def run_gpu(args, world, rank, local):
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
     w = WL.WORKLOADS[args.workload]
-    stack = w.attn_type == "stack"
+    # block path: the routed stack and the full block run the block sandwich
+    # (fp16 activations, fp32 residual stream); the full block adds the FFN.
+    stack = w.attn_type == "stack" or w.d_ff > 0
+    ffn = w.d_ff > 0
     M, D, H, H_kv, d_h = w.M, w.D, w.H, w.H_kv, w.d_h
     HD, KVD = H * d_h, H_kv * d_h
     pads = WL.pad_lens(w)
@@ -208,6 +215,10 @@ def run_gpu(args, world, rank, local):
         wq16 = torch.empty((HD, D), dtype=torch.float16, device=dev)
         wkv16 = torch.empty((2 * KVD, D), dtype=torch.float16, device=dev)
         wo16 = torch.empty((D, HD), dtype=torch.float16, device=dev)
+    if ffn:
+        z = torch.empty((M, w.d_ff), dtype=torch.float16, device=dev)
+        wgu16 = torch.empty((2 * w.d_ff, D), dtype=torch.float16, device=dev)
+        wd16 = torch.empty((D, w.d_ff), dtype=torch.float16, device=dev)
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
@@ -223,9 +234,16 @@ def run_gpu(args, world, rank, local):
             work["rmsnorm"] += metrics.rmsnorm_bytes(M, D, 4)
             work["postnorm"] += metrics.postnorm_bytes(M, D, 4)
             work["cast"] = work.get("cast", 0.0) + (2 * HD * D + 2 * KVD * D) * 4.0
-    launches = {"linear": 3 * w.num_layers, "attention": w.num_layers,
-                "qk_norm_rope": w.num_layers, "rmsnorm": w.num_layers if stack else 0,
-                "postnorm": w.num_layers if stack else 0, "cast": 3 * w.num_layers if stack else 0}
+        if ffn:
+            work["linear"] += 2.0 * M * (2 * w.d_ff) * D + 2.0 * M * D * w.d_ff
+            work["rmsnorm"] += metrics.rmsnorm_bytes(M, D, 4)
+            work["postnorm"] += metrics.postnorm_bytes(M, D, 4)
+            work["cast"] += 3 * w.d_ff * D * 4.0
+    nl = w.num_layers
+    launches = {"linear": (5 if ffn else 3) * nl, "attention": nl, "qk_norm_rope": nl,
+                "rmsnorm": (2 if ffn else 1) * nl if stack else 0,
+                "postnorm": (2 if ffn else 1) * nl if stack else 0,
+                "cast": (5 if ffn else 3) * nl if stack else 0}
 
     def step(ev=None):
         """One pass of the hot path as stage calls (the same kernels, buffers
@@ -283,6 +301,27 @@ def run_gpu(args, world, rank, local):
                 e = mark("postnorm")
                 G3.gemma3_postnorm_residual(out, r_in, r_t, L.p["gamma_post"], resid, M, D)
                 done("postnorm", e)
+            if ffn:
+                # the feed-forward sandwich, in place on the fp32 residual stream
+                e = mark("rmsnorm")
+                G3.gemma3_rmsnorm(resid, G3.GEMMA3_F32, L.p["gamma_pre_ffn"], u, G3.GEMMA3_F16,
+                                  M, D)
+                done("rmsnorm", e)
+                e = mark("cast")
+                G3.gemma3_cast_bf16_f16(L.p["W_gating"], wgu16, 2 * w.d_ff * D)
+                G3.gemma3_cast_bf16_f16(L.p["W_down"], wd16, D * w.d_ff)
+                done("cast", e)
+                e = mark("linear")
+                G3.gemma3_geglu(u, D, wgu16, D, z, w.d_ff, M, w.d_ff, D, G3.GEMMA3_F16)
+                done("ffn_geglu", e)
+                e = mark("linear")
+                G3.gemma3_linear(z, w.d_ff, wd16, w.d_ff, out, D, M, D, w.d_ff, G3.GEMMA3_F16,
+                                 G3.GEMMA3_F32)
+                done("ffn_down", e)
+                e = mark("postnorm")
+                G3.gemma3_postnorm_residual(out, resid, G3.GEMMA3_F32, L.p["gamma_post_ffn"],
+                                            resid, M, D)
+                done("postnorm", e)
 
     for _ in range(args.warmup):
         flush.zero_()
@@ -320,9 +359,9 @@ def run_gpu(args, world, rank, local):
     dev_seconds = sum(step_ms) / 1e3
     value, max_seconds = whole_job_value(tokens * args.steps, dev_seconds, world, dev)
     kern_ms = {k: sum(a.elapsed_time(b) for a, b in v) for k, v in events.items()}
-    kern_ms["linear"] = sum(kern_ms.pop(k, 0.0) for k in ("proj_q", "proj_kv", "proj_o"))
-    proj_ms = {k: sum(a.elapsed_time(b) for a, b in events[k]) / args.steps
-               for k in ("proj_q", "proj_kv", "proj_o")}
+    gemm_names = ("proj_q", "proj_kv", "proj_o") + (("ffn_geglu", "ffn_down") if ffn else ())
+    proj_ms = {k: sum(a.elapsed_time(b) for a, b in events[k]) / args.steps for k in gemm_names}
+    kern_ms["linear"] = sum(kern_ms.pop(k, 0.0) for k in gemm_names)
 
     # ---- end to end through the public C ABI with host buffers
     e2e = run_e2e(args, w, layers, x_cpu, pads, torch, G3, dev, stack, world)
@@ -357,9 +396,14 @@ def run_gpu(args, world, rank, local):
             b["gbs"] = work[k] * args.steps / (ms / 1e3) / 1e9
         breakdown[k] = b
     gf = metrics.layer_gemm_flops(M, D, H, H_kv, d_h)
-    for k, name in (("proj_q", "q_proj"), ("proj_kv", "kv_proj"), ("proj_o", "o_proj")):
-        breakdown[k] = {"ms_per_step": proj_ms[k],
-                        "tflops": gf[name] * w.num_layers / (proj_ms[k] / 1e3) / 1e12}
+    if ffn:
+        gf["ffn_geglu"] = 2.0 * M * (2 * w.d_ff) * D
+        gf["ffn_down"] = 2.0 * M * D * w.d_ff
+    for k, name in (("proj_q", "q_proj"), ("proj_kv", "kv_proj"), ("proj_o", "o_proj"),
+                    ("ffn_geglu", "ffn_geglu"), ("ffn_down", "ffn_down")):
+        if k in proj_ms:
+            breakdown[k] = {"ms_per_step": proj_ms[k],
+                            "tflops": gf[name] * w.num_layers / (proj_ms[k] / 1e3) / 1e12}
 
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
@@ -369,7 +413,7 @@ def run_gpu(args, world, rank, local):
         "data": "synthetic (seeded N(0,1) activations, N(0,1/D) weights, gamma N(0,0.1))",
         "config": {"workload": w.name, "B": w.B, "T": w.T, "D": D, "H": H, "H_kv": H_kv,
                    "d_h": d_h, "attn": w.attn_type, "window": w.window,
-                   "layers": w.num_layers, "valid_tokens": int(tokens),
+                   "layers": w.num_layers, "d_ff": w.d_ff or None, "valid_tokens": int(tokens),
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "l2": "flushed before every timed step (256 MiB write, outside step events)",
                    "operands": "bf16 projections, f16 attention operands, f32 accumulation"},
@@ -403,7 +447,10 @@ def run_e2e(args, w, layers, x_cpu, pads, torch, G3, dev, stack, world):
     out_host = torch.empty((w.B, w.T, D), dtype=torch.float32 if stack else torch.bfloat16,
                            pin_memory=True)
     dims = (w.B, w.T, D, w.H, w.H_kv, w.d_h)
-    if stack:
+    if w.d_ff > 0:
+        ws_bytes = G3.gemma3_block_workspace_size(dims, w.d_ff)
+        y = torch.empty((w.B, w.T, D), dtype=torch.float32, device=dev)
+    elif stack:
         ws_bytes = G3.gemma3_block_attn_workspace_size(*dims)
         y = torch.empty((w.B, w.T, D), dtype=torch.float32, device=dev)
     else:
@@ -416,7 +463,17 @@ def run_e2e(args, w, layers, x_cpu, pads, torch, G3, dev, stack, world):
         x_d.copy_(x_host, non_blocking=True)
         pos_d.copy_(pos_host, non_blocking=True)
         pad_d.copy_(pad_host, non_blocking=True)
-        if stack:
+        if w.d_ff > 0:
+            src, src_t = x_d, G3.GEMMA3_BF16
+            for L in layers:
+                G3.gemma3_block_forward(
+                    dims, w.d_ff, src, src_t, y, pos_d, pad_d, L.p["Wq"], L.p["Wkv"], L.p["Wo"],
+                    L.p["gamma_q"], L.p["gamma_k"], L.p["gamma_pre"], L.p["gamma_post"],
+                    L.p["gamma_pre_ffn"], L.p["gamma_post_ffn"], L.p["W_gating"],
+                    L.p["W_down"], L.attn_type, L.window, L.rope_base, L.rope_scale,
+                    w.query_scale, ws, ws_bytes)
+                src, src_t = y, G3.GEMMA3_F32
+        elif stack:
             src, src_t = x_d, G3.GEMMA3_BF16
             for L in layers:
                 G3.gemma3_block_attn_forward(
@@ -454,7 +511,8 @@ def run_e2e(args, w, layers, x_cpu, pads, torch, G3, dev, stack, world):
     d2h = out_host.numel() * out_host.element_size()
     return {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h,
-            "api": "gemma3_block_attn_forward" if stack else "gemma3_attn_forward"}
+            "api": ("gemma3_block_forward" if w.d_ff > 0 else
+                    "gemma3_block_attn_forward" if stack else "gemma3_attn_forward")}
 
 
 # ---------------------------------------------------------------------------- oracle (CPU)
@@ -466,6 +524,9 @@ def _oracle_weights(w):
         if w.attn_type == "stack":
             _ORACLE_WEIGHTS[w.name] = [dict(WL.weights(w, l), **WL.block_norm_gammas(w, l))
                                        for l in range(w.num_layers)]
+        elif w.d_ff > 0:
+            _ORACLE_WEIGHTS[w.name] = dict(WL.weights(w), **WL.block_norm_gammas(w, 0),
+                                           **WL.ffn_weights(w))
         else:
             _ORACLE_WEIGHTS[w.name] = WL.weights(w)
     return _ORACLE_WEIGHTS[w.name]
@@ -486,6 +547,14 @@ def oracle_sample(w, n_tokens: int):
     if w.attn_type == "stack":
         O.attention_stack(x, p, model_size=w.model_size, H=w.H, H_kv=w.H_kv, d_h=w.d_h,
                           segment_pos=pos, pad_lens=torch.zeros(1, dtype=torch.int64))
+    elif w.d_ff > 0:
+        O.full_block(x, p["gamma_pre"], p["gamma_post"], p["gamma_pre_ffn"], p["gamma_post_ffn"],
+                     p["W_gating"], p["W_down"].transpose(0, 1), segment_pos=pos, pad_lens=None,
+                     Wq=p["Wq"], Wkv=p["Wkv"], Wo=p["Wo"], gamma_q=p["gamma_q"],
+                     gamma_k=p["gamma_k"], H=w.H, H_kv=w.H_kv, d_h=w.d_h,
+                     attn_type=O.LOCAL_SLIDING if w.attn_type == "local" else O.GLOBAL,
+                     window=w.window, rope_base=w.rope_base, rope_scale=w.rope_scale,
+                     query_scale=w.query_scale)
     else:
         O.attention_layer(x, pos, None, p["Wq"], p["Wkv"], p["Wo"], p["gamma_q"], p["gamma_k"],
                           H=w.H, H_kv=w.H_kv, d_h=w.d_h,

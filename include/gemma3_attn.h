@@ -173,6 +173,50 @@ int gemma3_block_attn_forward(const gemma3_attn_dims* dims, const void* x, int x
                               double rope_base, double rope_scale, float query_scale,
                               void* workspace, size_t workspace_bytes, void* stream);
 
+/* ----------------------------------------------------- feed-forward half, full block */
+
+/* Workspace of gemma3_block_ffn_forward for M = B*T rows: [M, D] fp16 normed
+ * input, [M, D_ff] fp16 gated activations, [M, D] fp32 FFN output and fp16
+ * copies of the two weights. */
+int gemma3_block_ffn_workspace_size(int M, int D, int D_ff, size_t* bytes);
+
+/* Feed-forward half of a Gemma 3 block ([FB] How it works, last three lines
+ * of Block.__call__ and the MLP paragraph):
+ *   m = FFN(RMSNorm_pre-ffn(h));  m <- RMSNorm_post-ffn(m);  y = h + m
+ *   FFN(u) = (GELU(u Wg^T) * (u Wu^T)) Wd^T, GELU in its tanh form.
+ * Arguments:
+ *   h, y         [M, D] fp32 (y may alias h); D % 8 == 0, D_ff % 8 == 0
+ *   gamma_*_ffn  [D] bf16, (1 + gamma) RMSNorms with eps 1e-6
+ *   W_gating     [2, D_ff, D] bf16, the page's transposed gating weight:
+ *                [0] = W_g (gate, takes the GELU), [1] = W_u (up)
+ *   W_down       [D, D_ff] bf16: the page's (D_ff, D) linear stored
+ *                transposed (K-major, like every weight of this library)
+ * The normed input and the gated activations are fp16 (the weights are cast
+ * to fp16 copies in the workspace), as in gemma3_block_attn_forward.  Rows
+ * are independent; pad rows are computed like any other. */
+int gemma3_block_ffn_forward(int M, int D, int D_ff, const float* h, float* y,
+                             const void* gamma_pre_ffn, const void* gamma_post_ffn,
+                             const void* W_gating, const void* W_down, void* workspace,
+                             size_t workspace_bytes, void* stream);
+
+/* Workspace of gemma3_block_forward: the larger of its two halves'. */
+int gemma3_block_workspace_size(const gemma3_attn_dims* dims, int D_ff, size_t* bytes);
+
+/* The whole Gemma 3 block ([FB] How it works, Block.__call__): the
+ * block-attention sandwich of gemma3_block_attn_forward, then the
+ * feed-forward sandwich of gemma3_block_ffn_forward.  x [B, T, D] bf16 or
+ * fp32 (x_dtype), y [B, T, D] fp32 (may alias an fp32 x); the other
+ * arguments are those two calls'. */
+int gemma3_block_forward(const gemma3_attn_dims* dims, int D_ff, const void* x, int x_dtype,
+                         float* y, const int32_t* segment_pos, const int32_t* pad_lens,
+                         const void* Wq, const void* Wkv, const void* Wo, const void* gamma_q,
+                         const void* gamma_k, const void* gamma_pre_attn,
+                         const void* gamma_post_attn, const void* gamma_pre_ffn,
+                         const void* gamma_post_ffn, const void* W_gating, const void* W_down,
+                         int attn_type, int window, double rope_base, double rope_scale,
+                         float query_scale, void* workspace, size_t workspace_bytes,
+                         void* stream);
+
 /* ------------------------------------------------------------- stage entry points */
 
 /* C[M, N] = A[M, K] * W[N, K]^T (the projection einsums of [AB] How it
@@ -183,6 +227,13 @@ int gemma3_block_attn_forward(const gemma3_attn_dims* dims, const void* x, int x
  * persistent grid. */
 int gemma3_linear(const void* A, long lda, const void* W, long ldw, void* C, long ldc, int M,
                   int N, int K, int in_dtype, int out_dtype, int max_ctas, void* stream);
+
+/* Z[M, D_ff] fp16 = GELU_tanh(A Wg^T) * (A Wu^T), the gating projection of
+ * the feed-forward with the GeGLU applied in the GEMM epilogue ([FB] How it
+ * works, MLP).  A [M, K] and W_gating [2*D_ff, K] (the (2, D_ff, K) weight
+ * viewed as rows: gate rows first) in in_dtype (GEMMA3_BF16 | GEMMA3_F16). */
+int gemma3_geglu(const void* A, long lda, const void* W_gating, long ldw, void* Z, long ldz,
+                 int M, int D_ff, int K, int in_dtype, void* stream);
 
 /* dst[i] = src[i] for i < n, bf16 -> fp16 with round-to-nearest-even
  * (n % 8 == 0; both 16-byte aligned). */

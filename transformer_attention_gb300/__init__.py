@@ -9,13 +9,15 @@ from __future__ import annotations
 from ._lib import (  # noqa: F401  (re-exported C-ABI names)
     GEMMA3_BF16, GEMMA3_F16, GEMMA3_F32, GEMMA3_GLOBAL, GEMMA3_LOCAL_SLIDING, Gemma3Error,
     gemma3_attn_check_status, gemma3_attn_forward, gemma3_attn_workspace_size,
-    gemma3_block_attn_forward, gemma3_block_attn_workspace_size, gemma3_cast_bf16_f16,
+    gemma3_block_attn_forward, gemma3_block_attn_workspace_size, gemma3_block_ffn_forward,
+    gemma3_block_ffn_workspace_size, gemma3_block_forward, gemma3_block_workspace_size,
+    gemma3_cast_bf16_f16, gemma3_geglu,
     gemma3_flash_attention,
     gemma3_last_device_status, gemma3_layer_attn_type, gemma3_layer_config, gemma3_linear,
     gemma3_postnorm_residual, gemma3_qk_norm_rope, gemma3_query_scale, gemma3_rmsnorm,
     gemma3_selftest_wait_timeout, lib)
 
-__all__ = ["attention_forward", "block_attention_forward", "linear", "lib"]
+__all__ = ["attention_forward", "block_attention_forward", "block_forward", "linear", "lib"]
 
 
 def _empty_ws(nbytes: int, device):
@@ -62,6 +64,30 @@ def block_attention_forward(x, segment_pos, pad_lens, Wq, Wkv, Wo, gamma_q, gamm
     gemma3_block_attn_forward(dims, x, x_dtype, y, segment_pos, pad_lens, Wq, Wkv, Wo, gamma_q,
                               gamma_k, gamma_pre, gamma_post, attn_type, window, rope_base,
                               rope_scale, query_scale, workspace, workspace.numel(), stream)
+    return y
+
+
+def block_forward(x, segment_pos, pad_lens, Wq, Wkv, Wo, gamma_q, gamma_k, gamma_pre_attn,
+                  gamma_post_attn, gamma_pre_ffn, gamma_post_ffn, W_gating, W_down, *, H, H_kv,
+                  attn_type, window, rope_base, rope_scale, query_scale, y=None,
+                  workspace=None, stream=None):
+    """The whole block: y = h + FFN sandwich(h), h = x + attention sandwich(x).
+    x bf16 or fp32 [B,T,D]; y fp32 (may be x); W_gating [2,D_ff,D], W_down [D,D_ff]."""
+    import torch
+    B, T, D = x.shape
+    d_h = gamma_q.shape[0]
+    D_ff = W_gating.shape[1]
+    dims = (B, T, D, H, H_kv, d_h)
+    ws_bytes = gemma3_block_workspace_size(dims, D_ff)
+    if workspace is None:
+        workspace = _empty_ws(ws_bytes, x.device)
+    if y is None:
+        y = torch.empty((B, T, D), dtype=torch.float32, device=x.device)
+    x_dtype = GEMMA3_F32 if x.dtype == torch.float32 else GEMMA3_BF16
+    gemma3_block_forward(dims, D_ff, x, x_dtype, y, segment_pos, pad_lens, Wq, Wkv, Wo, gamma_q,
+                         gamma_k, gamma_pre_attn, gamma_post_attn, gamma_pre_ffn, gamma_post_ffn,
+                         W_gating, W_down, attn_type, window, rope_base, rope_scale, query_scale,
+                         workspace, workspace.numel(), stream)
     return y
 
 

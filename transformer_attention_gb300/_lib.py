@@ -52,6 +52,19 @@ SIGNATURES = {
                                           c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int,
                                           c_int, c_double, c_double, c_float, c_void_p, c_size_t,
                                           c_void_p]),
+    "gemma3_block_ffn_workspace_size": (c_int, [c_int, c_int, c_int, ctypes.POINTER(c_size_t)]),
+    "gemma3_block_ffn_forward": (c_int, [c_int, c_int, c_int, c_void_p, c_void_p, c_void_p,
+                                         c_void_p, c_void_p, c_void_p, c_void_p, c_size_t,
+                                         c_void_p]),
+    "gemma3_block_workspace_size": (c_int, [ctypes.POINTER(gemma3_attn_dims), c_int,
+                                            ctypes.POINTER(c_size_t)]),
+    "gemma3_block_forward": (c_int, [ctypes.POINTER(gemma3_attn_dims), c_int, c_void_p, c_int,
+                                     c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
+                                     c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
+                                     c_void_p, c_void_p, c_int, c_int, c_double, c_double,
+                                     c_float, c_void_p, c_size_t, c_void_p]),
+    "gemma3_geglu": (c_int, [c_void_p, c_long, c_void_p, c_long, c_void_p, c_long, c_int, c_int,
+                             c_int, c_int, c_void_p]),
     "gemma3_linear": (c_int, [c_void_p, c_long, c_void_p, c_long, c_void_p, c_long, c_int, c_int,
                               c_int, c_int, c_int, c_int, c_void_p]),
     "gemma3_cast_bf16_f16": (c_int, [c_void_p, c_void_p, c_size_t, c_void_p]),
@@ -199,6 +212,46 @@ def gemma3_block_attn_forward(dims, x, x_dtype, y, segment_pos, pad_lens, Wq, Wk
         _ptr(Wkv), _ptr(Wo), _ptr(gamma_q), _ptr(gamma_k), _ptr(gamma_pre), _ptr(gamma_post),
         attn_type, window, rope_base, rope_scale, query_scale, _ptr(workspace), workspace_bytes,
         _stream(stream)))
+
+
+def gemma3_block_ffn_workspace_size(M, D, D_ff) -> int:
+    n = c_size_t()
+    _check("gemma3_block_ffn_workspace_size",
+           lib().gemma3_block_ffn_workspace_size(M, D, D_ff, ctypes.byref(n)))
+    return n.value
+
+
+def gemma3_block_ffn_forward(M, D, D_ff, h, y, gamma_pre_ffn, gamma_post_ffn, W_gating, W_down,
+                             workspace, workspace_bytes, stream=None):
+    return _check("gemma3_block_ffn_forward", lib().gemma3_block_ffn_forward(
+        M, D, D_ff, _ptr(h), _ptr(y), _ptr(gamma_pre_ffn), _ptr(gamma_post_ffn), _ptr(W_gating),
+        _ptr(W_down), _ptr(workspace), workspace_bytes, _stream(stream)))
+
+
+def gemma3_block_workspace_size(dims, D_ff) -> int:
+    n = c_size_t()
+    d = _dims(*dims)
+    _check("gemma3_block_workspace_size",
+           lib().gemma3_block_workspace_size(ctypes.byref(d), D_ff, ctypes.byref(n)))
+    return n.value
+
+
+def gemma3_block_forward(dims, D_ff, x, x_dtype, y, segment_pos, pad_lens, Wq, Wkv, Wo, gamma_q,
+                         gamma_k, gamma_pre_attn, gamma_post_attn, gamma_pre_ffn, gamma_post_ffn,
+                         W_gating, W_down, attn_type, window, rope_base, rope_scale, query_scale,
+                         workspace, workspace_bytes, stream=None):
+    d = _dims(*dims)
+    return _check("gemma3_block_forward", lib().gemma3_block_forward(
+        ctypes.byref(d), D_ff, _ptr(x), x_dtype, _ptr(y), _ptr(segment_pos), _ptr(pad_lens),
+        _ptr(Wq), _ptr(Wkv), _ptr(Wo), _ptr(gamma_q), _ptr(gamma_k), _ptr(gamma_pre_attn),
+        _ptr(gamma_post_attn), _ptr(gamma_pre_ffn), _ptr(gamma_post_ffn), _ptr(W_gating),
+        _ptr(W_down), attn_type, window, rope_base, rope_scale, query_scale, _ptr(workspace),
+        workspace_bytes, _stream(stream)))
+
+
+def gemma3_geglu(A, lda, W_gating, ldw, Z, ldz, M, D_ff, K, in_dtype, stream=None):
+    return _check("gemma3_geglu", lib().gemma3_geglu(
+        _ptr(A), lda, _ptr(W_gating), ldw, _ptr(Z), ldz, M, D_ff, K, in_dtype, _stream(stream)))
 
 
 def gemma3_linear(A, lda, W, ldw, C, ldc, M, N, K, in_dtype, out_dtype, max_ctas=0,

@@ -313,6 +313,138 @@ int gemma3_block_attn_forward(const gemma3_attn_dims* dims, const void* x, int x
   return to_status(launch_postnorm_residual(a, x, xt, gamma_post, y, M, dims->D, s));
 }
 
+// ------------------------------------------------------------ feed-forward half
+
+namespace {
+
+struct FfnWs {
+  size_t u, z, m, wgu, wd, total;
+};
+
+FfnWs ffn_ws(int M, int D, int D_ff) {
+  FfnWs w;
+  w.u = round_up(static_cast<size_t>(M) * D * 2, 256);
+  w.z = round_up(static_cast<size_t>(M) * D_ff * 2, 256);
+  w.m = round_up(static_cast<size_t>(M) * D * 4, 256);
+  w.wgu = round_up(static_cast<size_t>(2) * D_ff * D * 2, 256);
+  w.wd = round_up(static_cast<size_t>(D) * D_ff * 2, 256);
+  w.total = w.u + w.z + w.m + w.wgu + w.wd;
+  return w;
+}
+
+int validate_ffn(int M, int D, int D_ff) {
+  if (M < 1 || D < 8 || D_ff < 8 || D % 8 || D_ff % 8) return GEMMA3_ERR_INVALID_ARG;
+  if (static_cast<long long>(M) * D_ff >= (1LL << 40)) return GEMMA3_ERR_INVALID_ARG;
+  return GEMMA3_OK;
+}
+
+// y = h + RMSNorm_post(FFN(RMSNorm_pre(h))) on fp16 activations (see the
+// block path's precision note) with fp32 h / y.
+int ffn_pipeline(int M, int D, int D_ff, const void* h, int h_dtype, float* y,
+                 const void* gamma_pre, const void* gamma_post, const void* W_gating,
+                 const void* W_down, uint8_t* ws, cudaStream_t s) {
+  int* st = status_ptr();
+  if (st == nullptr) return GEMMA3_ERR_CUDA;
+  const FfnWs w = ffn_ws(M, D, D_ff);
+  uint8_t* u = ws;
+  uint8_t* z = u + w.u;
+  float* m = reinterpret_cast<float*>(z + w.z);
+  uint8_t* wgu = z + w.z + w.m;
+  uint8_t* wd = wgu + w.wgu;
+  if (launch_rmsnorm_rows(h, h_dtype, gamma_pre, u, kF16, M, D, s) != cudaSuccess ||
+      launch_cast_bf16_f16(W_gating, wgu, static_cast<size_t>(2) * D_ff * D, s) != cudaSuccess ||
+      launch_cast_bf16_f16(W_down, wd, static_cast<size_t>(D) * D_ff, s) != cudaSuccess ||
+      launch_geglu(u, D, wgu, D, z, D_ff, M, D_ff, D, kF16, s, st) != cudaSuccess ||
+      launch_linear(z, D_ff, wd, D_ff, m, D, M, D, D_ff, kF16, kF32, s, st, 0) != cudaSuccess)
+    return GEMMA3_ERR_CUDA;
+  return to_status(launch_postnorm_residual(m, h, h_dtype, gamma_post, y, M, D, s));
+}
+
+}  // namespace
+
+int gemma3_block_ffn_workspace_size(int M, int D, int D_ff, size_t* bytes) {
+  const int rc = validate_ffn(M, D, D_ff);
+  if (rc != GEMMA3_OK) return rc;
+  if (bytes == nullptr) return GEMMA3_ERR_INVALID_ARG;
+  *bytes = ffn_ws(M, D, D_ff).total;
+  return GEMMA3_OK;
+}
+
+int gemma3_block_ffn_forward(int M, int D, int D_ff, const float* h, float* y,
+                             const void* gamma_pre_ffn, const void* gamma_post_ffn,
+                             const void* W_gating, const void* W_down, void* workspace,
+                             size_t workspace_bytes, void* stream) {
+  int rc = validate_ffn(M, D, D_ff);
+  if (rc != GEMMA3_OK) return rc;
+  if (!h || !y || !gamma_pre_ffn || !gamma_post_ffn || !W_gating || !W_down || !workspace)
+    return GEMMA3_ERR_INVALID_ARG;
+  if (!aligned16(h) || !aligned16(y) || !aligned16(gamma_pre_ffn) || !aligned16(gamma_post_ffn) ||
+      !aligned16(W_gating) || !aligned16(W_down) ||
+      (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return GEMMA3_ERR_MISALIGNED;
+  if (workspace_bytes < ffn_ws(M, D, D_ff).total) return GEMMA3_ERR_WORKSPACE;
+  rc = check_device();
+  if (rc != GEMMA3_OK) return rc;
+  return ffn_pipeline(M, D, D_ff, h, kF32, y, gamma_pre_ffn, gamma_post_ffn, W_gating, W_down,
+                      static_cast<uint8_t*>(workspace), as_stream(stream));
+}
+
+int gemma3_block_workspace_size(const gemma3_attn_dims* dims, int D_ff, size_t* bytes) {
+  if (bytes == nullptr) return GEMMA3_ERR_INVALID_ARG;
+  size_t a = 0, f = 0;
+  int rc = gemma3_block_attn_workspace_size(dims, &a);
+  if (rc != GEMMA3_OK) return rc;
+  rc = gemma3_block_ffn_workspace_size(dims->B * dims->T, dims->D, D_ff, &f);
+  if (rc != GEMMA3_OK) return rc;
+  *bytes = a > f ? a : f;
+  return GEMMA3_OK;
+}
+
+int gemma3_block_forward(const gemma3_attn_dims* dims, int D_ff, const void* x, int x_dtype,
+                         float* y, const int32_t* segment_pos, const int32_t* pad_lens,
+                         const void* Wq, const void* Wkv, const void* Wo, const void* gamma_q,
+                         const void* gamma_k, const void* gamma_pre_attn,
+                         const void* gamma_post_attn, const void* gamma_pre_ffn,
+                         const void* gamma_post_ffn, const void* W_gating, const void* W_down,
+                         int attn_type, int window, double rope_base, double rope_scale,
+                         float query_scale, void* workspace, size_t workspace_bytes,
+                         void* stream) {
+  size_t need = 0;
+  int rc = gemma3_block_workspace_size(dims, D_ff, &need);
+  if (rc != GEMMA3_OK) return rc;
+  if (!gamma_pre_ffn || !gamma_post_ffn || !W_gating || !W_down) return GEMMA3_ERR_INVALID_ARG;
+  if (!aligned16(gamma_pre_ffn) || !aligned16(gamma_post_ffn) || !aligned16(W_gating) ||
+      !aligned16(W_down))
+    return GEMMA3_ERR_MISALIGNED;
+  if (workspace_bytes < need) return GEMMA3_ERR_WORKSPACE;
+  // h = x + RMSNorm_post-attn(Attn(RMSNorm_pre-attn(x))) into y, then the
+  // feed-forward sandwich in place on y (the workspace is reused in turn).
+  rc = gemma3_block_attn_forward(dims, x, x_dtype, y, segment_pos, pad_lens, Wq, Wkv, Wo, gamma_q,
+                                 gamma_k, gamma_pre_attn, gamma_post_attn, attn_type, window,
+                                 rope_base, rope_scale, query_scale, workspace, workspace_bytes,
+                                 stream);
+  if (rc != GEMMA3_OK) return rc;
+  return ffn_pipeline(dims->B * dims->T, dims->D, D_ff, y, kF32, y, gamma_pre_ffn,
+                      gamma_post_ffn, W_gating, W_down, static_cast<uint8_t*>(workspace),
+                      as_stream(stream));
+}
+
+int gemma3_geglu(const void* A, long lda, const void* W_gating, long ldw, void* Z, long ldz,
+                 int M, int D_ff, int K, int in_dtype, void* stream) {
+  if (!A || !W_gating || !Z || M < 0 || D_ff < 1 || K < 1) return GEMMA3_ERR_INVALID_ARG;
+  if (in_dtype != GEMMA3_BF16 && in_dtype != GEMMA3_F16) return GEMMA3_ERR_INVALID_ARG;
+  if (lda < K || ldw < K || ldz < D_ff) return GEMMA3_ERR_INVALID_ARG;
+  if (!aligned16(A) || !aligned16(W_gating) || !aligned16(Z) || (lda * 2) % 16 ||
+      (ldw * 2) % 16 || (ldz * 2) % 16)
+    return GEMMA3_ERR_MISALIGNED;
+  int rc = check_device();
+  if (rc != GEMMA3_OK) return rc;
+  int* st = status_ptr();
+  if (st == nullptr) return GEMMA3_ERR_CUDA;
+  return to_status(launch_geglu(A, lda, W_gating, ldw, Z, ldz, M, D_ff, K,
+                                in_dtype == GEMMA3_F16 ? kF16 : kBF16, as_stream(stream), st));
+}
+
 int gemma3_linear(const void* A, long lda, const void* W, long ldw, void* C, long ldc, int M,
                   int N, int K, int in_dtype, int out_dtype, int max_ctas, void* stream) {
   if (!A || !W || !C || M < 0 || N < 0 || K < 1) return GEMMA3_ERR_INVALID_ARG;

@@ -75,10 +75,22 @@ __device__ __forceinline__ void store_chunk16(T* dst, const uint32_t (&r)[32], i
   }
 }
 
-template <int AB_BF16, typename OutT>
+// GeGLU epilogue of the feed-forward gating projection ("Full Gemma 3
+// Block", How it works: MLP): z = GELU(g) * u with the tanh-form GELU.
+__device__ __forceinline__ float gelu_tanh_mul(float g, float u) {
+  const float kC = 0.7978845608028654f;   // sqrt(2 / pi)
+  return 0.5f * g * (1.f + tanhf(kC * fmaf(0.044715f * g, g * g, g))) * u;
+}
+
+// GEGLU = false: C[M,N] = A W^T.  GEGLU = true: W is the [2*N, K] gating
+// weight (rows [0, N) gate, [N, 2N) up); each 256-wide accumulator tile holds
+// 128 gate and the matching 128 up columns, and the epilogue writes
+// C[M, N] = GELU(A Wg^T) * (A Wu^T).
+template <int AB_BF16, typename OutT, bool GEGLU>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_tn_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    OutT* __restrict__ C, long ldc, int M, int N, int K, int* status) {
+  constexpr int BN_OUT = GEGLU ? BN / 2 : BN;   // output columns per tile
   // A kernel launched after an earlier one gave up does no work.
   if (*reinterpret_cast<volatile int*>(status) != 0) return;
   extern __shared__ uint8_t smem_raw[];
@@ -90,7 +102,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   __shared__ int abort_flag;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int m_tiles = (M + BM - 1) / BM, n_tiles = (N + BN - 1) / BN;
+  const int m_tiles = (M + BM - 1) / BM, n_tiles = (N + BN_OUT - 1) / BN_OUT;
   const int num_tiles = m_tiles * n_tiles;
   const int num_kb = (K + BK - 1) / BK;
 
@@ -125,7 +137,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       int fills[STAGES] = {};
       bool ok = true;
       for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
-        const int m0 = (tile / n_tiles) * BM, n0 = (tile % n_tiles) * BN;
+        const int m0 = (tile / n_tiles) * BM, n0 = (tile % n_tiles) * BN_OUT;
         for (int kb = 0; kb < num_kb; ++kb) {
           if (!mbar_wait(smem_u32(&empty_bar[stage]), phase ^ 1, &abort_flag, status, kSiteEmpty)) {
             ok = false;
@@ -135,7 +147,13 @@ __global__ void __launch_bounds__(THREADS, 1)
           uint8_t* sa = smem + stage * STAGE_BYTES;
           mbar_arrive_expect_tx(fb, STAGE_BYTES);
           tma_load_2d(smem_u32(sa), &tmA, fb, kb * BK, m0);
-          tma_load_2d(smem_u32(sa + A_BYTES), &tmB, fb, kb * BK, n0);
+          if constexpr (GEGLU) {
+            // gate rows n0.. into the first 128 B-tile rows, up rows N + n0.. after them
+            tma_load_2d(smem_u32(sa + A_BYTES), &tmB, fb, kb * BK, n0);
+            tma_load_2d(smem_u32(sa + A_BYTES + B_BYTES / 2), &tmB, fb, kb * BK, N + n0);
+          } else {
+            tma_load_2d(smem_u32(sa + A_BYTES), &tmB, fb, kb * BK, n0);
+          }
           ++fills[stage];
           if (++stage == STAGES) { stage = 0; phase ^= 1; }
         }
@@ -190,18 +208,28 @@ __global__ void __launch_bounds__(THREADS, 1)
     int abuf = 0;
     uint32_t aphase = 0;
     for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
-      const int m0 = (tile / n_tiles) * BM, n0 = (tile % n_tiles) * BN;
+      const int m0 = (tile / n_tiles) * BM, n0 = (tile % n_tiles) * BN_OUT;
       bool ok = mbar_wait(smem_u32(&accf_bar[abuf]), aphase, &abort_flag, status, kSiteAccFull);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
       const int row = m0 + q * 32 + lane;
-      for (int c = 0; c < BN / 32; ++c) {
+      for (int c = 0; c < BN_OUT / 32; ++c) {
         const int col0 = n0 + c * 32;
         if (col0 >= N) break;
         uint32_t r[32];
         tmem_ld32(tbase + lane_off + abuf * BN + c * 32, r);
-        tmem_ld_wait(r);
+        if constexpr (GEGLU) {
+          uint32_t ru[32];
+          tmem_ld32(tbase + lane_off + abuf * BN + BN / 2 + c * 32, ru);
+          tmem_ld_wait(r);
+          tmem_ld_wait(ru);
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            r[e] = __float_as_uint(gelu_tanh_mul(__uint_as_float(r[e]), __uint_as_float(ru[e])));
+        } else {
+          tmem_ld_wait(r);
+        }
         if (row < M) {
           const int ncols = min(32, N - col0);
           OutT* dst = C + static_cast<long>(row) * ldc + col0;
@@ -223,10 +251,10 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
 }
 
-template <int AB_BF16, typename OutT>
+template <int AB_BF16, typename OutT, bool GEGLU = false>
 cudaError_t launch_typed(const CUtensorMap& ta, const CUtensorMap& tb, void* C, long ldc, int M,
                          int N, int K, cudaStream_t stream, int* status, int max_ctas) {
-  auto kern = gemm_tn_kernel<AB_BF16, OutT>;
+  auto kern = gemm_tn_kernel<AB_BF16, OutT, GEGLU>;
   static bool attr_set = false;  // benign race: setting the same attribute twice is harmless
   if (!attr_set) {
     cudaError_t e =
@@ -234,7 +262,8 @@ cudaError_t launch_typed(const CUtensorMap& ta, const CUtensorMap& tb, void* C, 
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  const int tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
+  const int bn_out = GEGLU ? BN / 2 : BN;
+  const int tiles = ((M + BM - 1) / BM) * ((N + bn_out - 1) / bn_out);
   int grid = num_sms();
   if (max_ctas > 0 && max_ctas < grid) grid = max_ctas;
   if (tiles < grid) grid = tiles;
@@ -274,6 +303,27 @@ cudaError_t launch_linear(const void* A, long lda, const void* W, long ldw, void
   }
   G3_GEMM_OUT(0)
 #undef G3_GEMM_OUT
+}
+
+cudaError_t launch_geglu(const void* A, long lda, const void* Wgu, long ldw, void* Z, long ldz,
+                         int M, int D_ff, int K, int in_dtype, cudaStream_t stream, int* status) {
+  if (M <= 0 || D_ff <= 0 || K <= 0) return cudaSuccess;
+  if (in_dtype != kBF16 && in_dtype != kF16) return cudaErrorInvalidValue;
+  const CUtensorMapDataType tdt =
+      in_dtype == kBF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  CUtensorMap ta, tb;
+  const uint64_t adims[2] = {static_cast<uint64_t>(K), static_cast<uint64_t>(M)};
+  const uint64_t astr[1] = {static_cast<uint64_t>(lda) * 2};
+  const uint32_t abox[2] = {BK, BM};
+  const uint64_t bdims[2] = {static_cast<uint64_t>(K), static_cast<uint64_t>(2) * D_ff};
+  const uint64_t bstr[1] = {static_cast<uint64_t>(ldw) * 2};
+  const uint32_t bbox[2] = {BK, BN / 2};
+  if (!encode_tiled(&ta, tdt, 2, A, adims, astr, abox) ||
+      !encode_tiled(&tb, tdt, 2, Wgu, bdims, bstr, bbox))
+    return cudaErrorInvalidValue;
+  if (in_dtype == kBF16)
+    return launch_typed<1, __half, true>(ta, tb, Z, ldz, M, D_ff, K, stream, status, 0);
+  return launch_typed<0, __half, true>(ta, tb, Z, ldz, M, D_ff, K, stream, status, 0);
 }
 
 }  // namespace g3

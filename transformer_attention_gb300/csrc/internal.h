@@ -23,6 +23,11 @@ cudaError_t launch_linear(const void* A, long lda, const void* W, long ldw, void
                           int M, int N, int K, int in_dtype, int out_dtype, cudaStream_t stream,
                           int* status, int max_ctas);
 
+// Z[M, D_ff] (fp16) = GELU_tanh(A Wg^T) * (A Wu^T), Wgu = [Wg; Wu] of shape
+// [2*D_ff, K] (the transposed gating weight (2, D_ff, D) viewed as rows).
+cudaError_t launch_geglu(const void* A, long lda, const void* Wgu, long ldw, void* Z, long ldz,
+                         int M, int D_ff, int K, int in_dtype, cudaStream_t stream, int* status);
+
 // In place on fp16 rows: Q[m, h*d_h:(h+1)*d_h] and K[m, j*d_h:(j+1)*d_h] get
 // last-axis RMSNorm, (1 + gamma), RoPE; Q also the query scale.
 cudaError_t launch_qk_norm_rope(void* Q, long ldq, void* K, long ldk, const void* gamma_q,

@@ -28,6 +28,7 @@ ROW_BLOCK = 1024          # rows of x per independently seeded block
 # Seeds of the individual input tensors (per layer: + 100 * layer).
 SEED_X, SEED_WQ, SEED_WKV, SEED_WO, SEED_GQ, SEED_GK, SEED_PAD = 1, 2, 3, 4, 5, 6, 7
 SEED_GPRE, SEED_GPOST = 8, 9
+SEED_WGATE, SEED_WDOWN, SEED_GPRE_FFN, SEED_GPOST_FFN = 10, 11, 12, 13
 
 
 @dataclass(frozen=True)
@@ -48,6 +49,7 @@ class Workload:
     model_size: str           # Gemma 3 size the shape follows
     pad: tuple = ("none",)    # ("none",) | ("pad_uniform", lo, hi) | ("valid_uniform", lo, hi)
     num_layers: int = 1
+    d_ff: int = 0             # > 0: the workload is the whole block (attention + feed-forward)
     description: str = field(default="", compare=False)
 
     @property
@@ -82,9 +84,16 @@ WORKLOADS = {
         window=1024, rope_base=0.0, rope_scale=0.0, query_scale=256 ** -0.5, model_size="12B",
         pad=("valid_uniform", 2048, 16384), num_layers=6,
         description="12B-shaped 6-layer routed attention stack: B8 T16384 D3840 H16/8 d256"),
+    # The full-block row (attention sandwich + GeGLU feed-forward sandwich) on
+    # the 4B-shaped local layer; the feed-forward width 4D follows the 4B size.
+    "4b_block": Workload(
+        "4b_block", B=2, T=32768, D=2560, H=8, H_kv=4, d_h=256, attn_type="local",
+        window=1024, rope_base=1e4, rope_scale=1.0, query_scale=256 ** -0.5, model_size="4B",
+        d_ff=10240,
+        description="4B-shaped full block: local attention layer + GeGLU FFN (D_ff 10240)"),
 }
 
-ORDER = ["tiny_local", "1b_global", "4b_local", "27b_global", "12b_stack"]
+ORDER = ["tiny_local", "1b_global", "4b_local", "27b_global", "12b_stack", "4b_block"]
 
 
 def small(w: Workload, **kw) -> Workload:
@@ -163,6 +172,19 @@ def block_norm_gammas(w: Workload, layer: int) -> dict:
     return {
         "gamma_pre": _normal_bf16((w.D,), math.sqrt(0.1), SEED_GPRE + off),
         "gamma_post": _normal_bf16((w.D,), math.sqrt(0.1), SEED_GPOST + off),
+    }
+
+
+def ffn_weights(w: Workload, layer: int = 0) -> dict:
+    """Feed-forward weights of one block (bf16, CPU): W_gating [2, D_ff, D]
+    ([0] gate, [1] up), W_down [D, D_ff] (the (D_ff, D) linear stored
+    transposed), and the pre/post feed-forward RMSNorm scales [D]."""
+    off = 100 * layer
+    return {
+        "W_gating": _normal_bf16((2, w.d_ff, w.D), 1.0 / math.sqrt(w.D), SEED_WGATE + off),
+        "W_down": _normal_bf16((w.D, w.d_ff), 1.0 / math.sqrt(w.d_ff), SEED_WDOWN + off),
+        "gamma_pre_ffn": _normal_bf16((w.D,), math.sqrt(0.1), SEED_GPRE_FFN + off),
+        "gamma_post_ffn": _normal_bf16((w.D,), math.sqrt(0.1), SEED_GPOST_FFN + off),
     }
 
 
