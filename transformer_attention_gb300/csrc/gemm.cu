@@ -13,7 +13,14 @@
 //               TMEM, double-buffered (2 x 256 columns) so the epilogue of one
 //               tile overlaps the main loop of the next.
 //   warps 4-7   epilogue: tcgen05.ld of the accumulator rows (one TMEM lane
-//               per thread), conversion to the output type, global stores.
+//               per thread), conversion to the output type, then each warp
+//               writes its 32 rows x 128 B chunk into a double-buffered,
+//               128-byte-swizzled shared-memory staging tile that one lane
+//               stores with a TMA bulk tensor store (full-line writes instead
+//               of 32 scattered 16-byte pieces per warp instruction).
+// Tiles are visited in groups of 8 M-tiles (N-tiles varying slowest within
+// a group), so the tiles in flight share A rows and W rows through L2 even
+// when W is larger than L2.
 // Every mbarrier wait is bounded (see ptx.cuh).
 #include <type_traits>
 
@@ -28,22 +35,23 @@ constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4, THREADS = 256;
 constexpr uint32_t A_BYTES = BM * BK * 2;   // 16 KB
 constexpr uint32_t B_BYTES = BN * BK * 2;   // 32 KB
 constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr uint32_t SMEM_BYTES = STAGES * STAGE_BYTES + 1024;
+constexpr uint32_t STAGING_BYTES = 32 * 128;           // one warp's 32 rows x 128 B
+constexpr uint32_t STAGING_TOTAL = 4 * 2 * STAGING_BYTES;   // 4 warps, double-buffered
+constexpr uint32_t SMEM_BYTES = STAGES * STAGE_BYTES + STAGING_TOTAL + 1024;
+constexpr int GROUP_M = 8;   // M-tiles per rasterisation group
+
+// Tile t of the grouped order -> (m tile, n tile).
+__device__ __forceinline__ void tile_coords(int t, int m_tiles, int n_tiles, int& mt, int& nt) {
+  const int per_group = GROUP_M * n_tiles;
+  const int first_m = (t / per_group) * GROUP_M;
+  const int gm = min(GROUP_M, m_tiles - first_m);
+  const int r = t % per_group;
+  mt = first_m + r % gm;
+  nt = r / gm;
+}
 constexpr uint32_t TMEM_COLS = 512;
 
 enum : int { kSiteEmpty = 1, kSiteFull = 2, kSiteAccEmpty = 3, kSiteAccFull = 4 };
-
-__device__ __forceinline__ void store_chunk(float* dst, const uint32_t (&r)[32], int ncols) {
-  if (ncols == 32) {
-#pragma unroll
-    for (int v = 0; v < 8; ++v)
-      reinterpret_cast<float4*>(dst)[v] =
-          make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
-                      __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
-  } else {
-    for (int c = 0; c < ncols; ++c) dst[c] = __uint_as_float(r[c]);
-  }
-}
 
 template <typename T>
 __device__ __forceinline__ uint32_t pack2(float a, float b);
@@ -52,27 +60,6 @@ template <> __device__ __forceinline__ uint32_t pack2<__half>(float a, float b) 
 }
 template <> __device__ __forceinline__ uint32_t pack2<__nv_bfloat16>(float a, float b) {
   return pack_bf162(a, b);
-}
-
-template <typename T>
-__device__ __forceinline__ void store_chunk16(T* dst, const uint32_t (&r)[32], int ncols) {
-  if (ncols == 32) {
-#pragma unroll
-    for (int v = 0; v < 4; ++v) {
-      uint4 w;
-      w.x = pack2<T>(__uint_as_float(r[8 * v + 0]), __uint_as_float(r[8 * v + 1]));
-      w.y = pack2<T>(__uint_as_float(r[8 * v + 2]), __uint_as_float(r[8 * v + 3]));
-      w.z = pack2<T>(__uint_as_float(r[8 * v + 4]), __uint_as_float(r[8 * v + 5]));
-      w.w = pack2<T>(__uint_as_float(r[8 * v + 6]), __uint_as_float(r[8 * v + 7]));
-      reinterpret_cast<uint4*>(dst)[v] = w;
-    }
-  } else {
-    for (int c = 0; c < ncols; ++c) {
-      float f = __uint_as_float(r[c]);
-      if constexpr (std::is_same<T, __half>::value) dst[c] = __float2half_rn(f);
-      else dst[c] = __float2bfloat16_rn(f);
-    }
-  }
 }
 
 // GeGLU epilogue of the feed-forward gating projection ("Full Gemma 3
@@ -89,8 +76,9 @@ __device__ __forceinline__ float gelu_tanh_mul(float g, float u) {
 template <int AB_BF16, typename OutT, bool GEGLU>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_tn_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   OutT* __restrict__ C, long ldc, int M, int N, int K, int* status) {
+                   const __grid_constant__ CUtensorMap tmC, int M, int N, int K, int* status) {
   constexpr int BN_OUT = GEGLU ? BN / 2 : BN;   // output columns per tile
+  constexpr int CW = 128 / static_cast<int>(sizeof(OutT));   // output columns per 128 B chunk
   // A kernel launched after an earlier one gave up does no work.
   if (*reinterpret_cast<volatile int*>(status) != 0) return;
   extern __shared__ uint8_t smem_raw[];
@@ -120,6 +108,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     fence_barrier_init();
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
+    tma_prefetch_desc(&tmC);
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(&tmem_base_sh), TMEM_COLS);
@@ -137,7 +126,9 @@ __global__ void __launch_bounds__(THREADS, 1)
       int fills[STAGES] = {};
       bool ok = true;
       for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
-        const int m0 = (tile / n_tiles) * BM, n0 = (tile % n_tiles) * BN_OUT;
+        int mt, nt;
+        tile_coords(tile, m_tiles, n_tiles, mt, nt);
+        const int m0 = mt * BM, n0 = nt * BN_OUT;
         for (int kb = 0; kb < num_kb; ++kb) {
           if (!mbar_wait(smem_u32(&empty_bar[stage]), phase ^ 1, &abort_flag, status, kSiteEmpty)) {
             ok = false;
@@ -202,47 +193,87 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_wait_drain(smem_u32(&drain_bar), 0);
     }
   } else if (warp >= 4) {
-    // ---------------- epilogue: TMEM -> registers -> global
+    // ---------------- epilogue: TMEM -> registers -> swizzled staging -> TMA store
     const int q = warp - 4;
     const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
-    int abuf = 0;
+    uint8_t* staging = smem + STAGES * STAGE_BYTES + q * 2 * STAGING_BYTES;
+    int abuf = 0, nchunk = 0;
     uint32_t aphase = 0;
     for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
-      const int m0 = (tile / n_tiles) * BM, n0 = (tile % n_tiles) * BN_OUT;
+      int mt, nt;
+      tile_coords(tile, m_tiles, n_tiles, mt, nt);
+      const int m0 = mt * BM, n0 = nt * BN_OUT;
       bool ok = mbar_wait(smem_u32(&accf_bar[abuf]), aphase, &abort_flag, status, kSiteAccFull);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
-      const int row = m0 + q * 32 + lane;
-      for (int c = 0; c < BN_OUT / 32; ++c) {
-        const int col0 = n0 + c * 32;
-        if (col0 >= N) break;
-        uint32_t r[32];
-        tmem_ld32(tbase + lane_off + abuf * BN + c * 32, r);
-        if constexpr (GEGLU) {
-          uint32_t ru[32];
-          tmem_ld32(tbase + lane_off + abuf * BN + BN / 2 + c * 32, ru);
-          tmem_ld_wait(r);
-          tmem_ld_wait(ru);
-#pragma unroll
-          for (int e = 0; e < 32; ++e)
-            r[e] = __float_as_uint(gelu_tanh_mul(__uint_as_float(r[e]), __uint_as_float(ru[e])));
+      const uint32_t acc = tbase + lane_off + abuf * BN;
+      for (int c = 0; c < BN_OUT / CW; ++c, ++nchunk) {
+        const int col0 = n0 + c * CW;
+        if (col0 >= N) break;   // warp-uniform
+        // 128 bytes of this thread's row: 8 x 16-byte units
+        uint32_t w[32];
+        if constexpr (sizeof(OutT) == 4) {
+          tmem_ld32(acc + c * 32, w);
+          tmem_ld_wait(w);
         } else {
-          tmem_ld_wait(r);
+          uint32_t r0[32], r1[32];
+          tmem_ld32(acc + c * 64, r0);
+          tmem_ld32(acc + c * 64 + 32, r1);
+          if constexpr (GEGLU) {
+            uint32_t u0[32], u1[32];
+            tmem_ld32(acc + BN / 2 + c * 64, u0);
+            tmem_ld32(acc + BN / 2 + c * 64 + 32, u1);
+            tmem_ld_wait(r0);
+            tmem_ld_wait(r1);
+            tmem_ld_wait(u0);
+            tmem_ld_wait(u1);
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              w[e] = pack2<OutT>(gelu_tanh_mul(__uint_as_float(r0[2 * e]), __uint_as_float(u0[2 * e])),
+                                 gelu_tanh_mul(__uint_as_float(r0[2 * e + 1]),
+                                               __uint_as_float(u0[2 * e + 1])));
+              w[16 + e] =
+                  pack2<OutT>(gelu_tanh_mul(__uint_as_float(r1[2 * e]), __uint_as_float(u1[2 * e])),
+                              gelu_tanh_mul(__uint_as_float(r1[2 * e + 1]),
+                                            __uint_as_float(u1[2 * e + 1])));
+            }
+          } else {
+            tmem_ld_wait(r0);
+            tmem_ld_wait(r1);
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              w[e] = pack2<OutT>(__uint_as_float(r0[2 * e]), __uint_as_float(r0[2 * e + 1]));
+              w[16 + e] = pack2<OutT>(__uint_as_float(r1[2 * e]), __uint_as_float(r1[2 * e + 1]));
+            }
+          }
         }
-        if (row < M) {
-          const int ncols = min(32, N - col0);
-          OutT* dst = C + static_cast<long>(row) * ldc + col0;
-          if constexpr (std::is_same<OutT, float>::value) store_chunk(dst, r, ncols);
-          else store_chunk16<OutT>(dst, r, ncols);
+        if (c == BN_OUT / CW - 1 || col0 + CW >= N) {
+          // last TMEM read of this tile: the accumulator may be reused
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&acce_bar[abuf]));
+        }
+        // The staging buffer used two chunks ago must have been read by its store.
+        uint8_t* buf = staging + (nchunk & 1) * STAGING_BYTES;
+        if (lane == 0 && nchunk >= 2) bulk_wait_group_read<1>();
+        __syncwarp();
+        // row `lane`, 16-byte unit u lands at unit u ^ (lane % 8) (128-byte swizzle)
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          *reinterpret_cast<uint4*>(buf + lane * 128 + ((u ^ (lane & 7)) << 4)) =
+              make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_2d(&tmC, smem_u32(buf), col0, m0 + q * 32);
+          bulk_commit_group();
         }
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&acce_bar[abuf]));
       abuf ^= 1;
       if (abuf == 0) aphase ^= 1;
     }
+    if (lane == 0) bulk_wait_group_all();
   }
   __syncthreads();
   if (warp == 1) {
@@ -255,6 +286,16 @@ template <int AB_BF16, typename OutT, bool GEGLU = false>
 cudaError_t launch_typed(const CUtensorMap& ta, const CUtensorMap& tb, void* C, long ldc, int M,
                          int N, int K, cudaStream_t stream, int* status, int max_ctas) {
   auto kern = gemm_tn_kernel<AB_BF16, OutT, GEGLU>;
+  // Output tile map: boxes of 32 rows x 128 bytes, 128-byte swizzle.
+  CUtensorMap tc;
+  const CUtensorMapDataType cdt = sizeof(OutT) == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                  : std::is_same<OutT, __half>::value
+                                      ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                      : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const uint64_t cdims[2] = {static_cast<uint64_t>(N), static_cast<uint64_t>(M)};
+  const uint64_t cstr[1] = {static_cast<uint64_t>(ldc) * sizeof(OutT)};
+  const uint32_t cbox[2] = {static_cast<uint32_t>(128 / sizeof(OutT)), 32};
+  if (!encode_tiled(&tc, cdt, 2, C, cdims, cstr, cbox)) return cudaErrorInvalidValue;
   static bool attr_set = false;  // benign race: setting the same attribute twice is harmless
   if (!attr_set) {
     cudaError_t e =
@@ -267,7 +308,7 @@ cudaError_t launch_typed(const CUtensorMap& ta, const CUtensorMap& tb, void* C, 
   int grid = num_sms();
   if (max_ctas > 0 && max_ctas < grid) grid = max_ctas;
   if (tiles < grid) grid = tiles;
-  kern<<<grid, THREADS, SMEM_BYTES, stream>>>(ta, tb, static_cast<OutT*>(C), ldc, M, N, K, status);
+  kern<<<grid, THREADS, SMEM_BYTES, stream>>>(ta, tb, tc, M, N, K, status);
   return cudaGetLastError();
 }
 
