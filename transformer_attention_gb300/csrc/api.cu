@@ -174,7 +174,8 @@ __global__ void wait_forever_kernel(long long timeout_ns, int* status) {
 }  // namespace
 
 bool encode_tiled(CUtensorMap* map, CUtensorMapDataType dt, int rank, const void* base,
-                  const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box) {
+                  const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box,
+                  CUtensorMapSwizzle swizzle) {
   std::call_once(g_encode_once, [] {
     cudaDriverEntryPointQueryResult q;
     void* fn = nullptr;
@@ -194,7 +195,7 @@ bool encode_tiled(CUtensorMap* map, CUtensorMapDataType dt, int rank, const void
     if (i + 1 < rank) gs[i] = strides_bytes[i];
   }
   const CUresult r = g_encode(map, dt, rank, const_cast<void*>(base), gd, gs, bx, es,
-                              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
                               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;

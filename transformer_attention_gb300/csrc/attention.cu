@@ -70,7 +70,7 @@ struct Cfg {
   static constexpr uint32_t Q_BYTES = BM * DH * 2;
   static constexpr uint32_t KV_BYTES = BN * DH * 2;
   static constexpr uint32_t SMEM = Q_BYTES + (KS + VS) * KV_BYTES + 1024;
-  static_assert(SMEM + 2304 <= 232448, "shared memory budget");
+  static_assert(SMEM + 2304 + SM_WARPS * 2048 <= 232448, "shared memory budget");
   // S buffers in TMEM: one at columns 0-127; with d_h = 128 the columns
   // 384-511 left over by O hold a second one.
   static constexpr int NS = (DH == 128) ? 2 : 1;
@@ -138,7 +138,8 @@ __device__ __forceinline__ int item_position(int r) {
 template <int DH, int G>
 __global__ void __launch_bounds__(THREADS, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                    const __grid_constant__ CUtensorMap tmV, uint16_t* __restrict__ O, int o_f16,
+                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+                    uint16_t* __restrict__ O, int o_f16,
                     const int32_t* __restrict__ pad_lens, int B, int T, int H, int H_kv,
                     int window, int num_q_tiles, int gsz, int num_items, int* status) {
   using C = Cfg<DH, G>;
@@ -156,6 +157,9 @@ __global__ void __launch_bounds__(THREADS, 1)
       v_full[C::VS], v_empty[C::VS], s_full[C::NS], s_free[C::NS], p_full[2], pv_done[2],
       o_final, o_free, drain, red_bar[4];
   __shared__ float red[2][2][BM];   // [handshake parity][warpgroup][row]
+  // Per softmax warp: 32 rows x 32 O columns (64 B per row, 64-byte swizzle)
+  // staged for a TMA store.
+  __shared__ __align__(1024) uint8_t ostage[SM_WARPS][32 * 64];
   __shared__ uint32_t tmem_sh;
   __shared__ int abort_flag;
 
@@ -187,6 +191,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     tma_prefetch_desc(&tmQ);
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
+    tma_prefetch_desc(&tmO);
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(&tmem_sh), 512);
@@ -489,38 +494,47 @@ __global__ void __launch_bounds__(THREADS, 1)
       tc_fence_after();
       const bool row_valid = t < it.valid;
       const float inv_l = row_valid ? 1.f / l_tot : 0.f;
-      uint16_t* dst =
-          O + ((static_cast<size_t>(it.b) * T + t) * H + h) * DH + wg * (DH / 2);
+      // This warp's 32 rows are tokens t0 + 32q/G .. of the G heads: one box
+      // {32 channels, G heads, 32/G tokens} of the [B, T, H, d_h] output
+      // (rows past T are clipped by the store).
+      uint8_t* stage = ostage[warp - 4];
 #pragma unroll 1
       for (int c = 0; c < DH / 64; ++c) {
         uint32_t rr[32];
         tmem_ld32(tbase + lane_off + O_COL + wg * (DH / 2) + c * 32, rr);
         tmem_ld_wait(rr);
-        if (t < T) {
+        if (c == DH / 64 - 1) {
+          // O has been read: the next item's first PV may overwrite it.
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&o_free));
+        }
+        uint32_t wv[16];
 #pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            uint4 w;
-            if (row_valid) {
-              uint32_t* wp = reinterpret_cast<uint32_t*>(&w);
+        for (int e = 0; e < 16; ++e) {
+          const float lo = __uint_as_float(rr[2 * e]) * inv_l;
+          const float hi = __uint_as_float(rr[2 * e + 1]) * inv_l;
+          wv[e] = row_valid ? (o_f16 ? pack_half2(lo, hi) : pack_bf162(lo, hi)) : 0u;
+        }
+        // The previous chunk's store must have read the staging tile.
+        if (lane == 0) bulk_wait_group_read<0>();
+        __syncwarp();
+        // row `lane` (64 B), 16-byte unit u at unit u ^ ((lane >> 1) & 3): 64-byte swizzle
 #pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const float lo = __uint_as_float(rr[8 * v + 2 * e]) * inv_l;
-                const float hi = __uint_as_float(rr[8 * v + 2 * e + 1]) * inv_l;
-                wp[e] = o_f16 ? pack_half2(lo, hi) : pack_bf162(lo, hi);
-              }
-            } else {
-              w = make_uint4(0, 0, 0, 0);
-            }
-            reinterpret_cast<uint4*>(dst + c * 32)[v] = w;
-          }
+        for (int u = 0; u < 4; ++u)
+          *reinterpret_cast<uint4*>(stage + lane * 64 + ((u ^ ((lane >> 1) & 3)) << 4)) =
+              make_uint4(wv[4 * u], wv[4 * u + 1], wv[4 * u + 2], wv[4 * u + 3]);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_4d(&tmO, smem_u32(stage), wg * (DH / 2) + c * 32, it.j * G,
+                       it.t0 + (q * 32) / G, it.b);
+          bulk_commit_group();
         }
       }
-      // O may now be overwritten by the next item's first PV.
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&o_free));
       ++nitem;
     }
+    if (lane == 0) bulk_wait_group_all();
   }
   __syncthreads();
   if (warp == 1) {
@@ -546,6 +560,13 @@ cudaError_t launch_cfg(const void* Q, const void* K, const void* V, long ldkv, v
                              static_cast<uint64_t>(B)};
   const uint64_t kstr[2] = {static_cast<uint64_t>(ldkv) * 2, static_cast<uint64_t>(T) * ldkv * 2};
   const uint32_t kbox[3] = {64, BN, 1};
+  // O [B, T, H, d_h] (16-bit, bf16 or fp16 bits alike): box {32 channels, G
+  // heads, 32/G tokens, 1}, 64-byte swizzle.
+  CUtensorMap to;
+  const uint32_t obox[4] = {32, static_cast<uint32_t>(G), static_cast<uint32_t>(32 / G), 1};
+  if (!encode_tiled(&to, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4, O, qdims, qstr, obox,
+                    CU_TENSOR_MAP_SWIZZLE_64B))
+    return cudaErrorInvalidValue;
   if (!encode_tiled(&tq, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4, Q, qdims, qstr, qbox) ||
       !encode_tiled(&tk, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, K, kdims, kstr, kbox) ||
       !encode_tiled(&tv, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, V, kdims, kstr, kbox))
@@ -567,7 +588,7 @@ cudaError_t launch_cfg(const void* Q, const void* K, const void* V, long ldkv, v
   const double kv_bytes = static_cast<double>(T) * DH * 2.0 * 2.0;
   int gsz = window > 0 ? B * H_kv : static_cast<int>(48.0 * 1024 * 1024 / kv_bytes);
   gsz = gsz < 1 ? 1 : (gsz > B * H_kv ? B * H_kv : gsz);
-  kern<<<grid, THREADS, C::SMEM, stream>>>(tq, tk, tv, static_cast<uint16_t*>(O),
+  kern<<<grid, THREADS, C::SMEM, stream>>>(tq, tk, tv, to, static_cast<uint16_t*>(O),
                                            o_dtype == kF16 ? 1 : 0, pad_lens, B, T, H, H_kv,
                                            window, num_q_tiles, gsz, static_cast<int>(items),
                                            status);

@@ -13,7 +13,8 @@ enum DType : int { kBF16 = 0, kF16 = 1, kF32 = 2 };
 // cuTensorMapEncodeTiled, fetched from the driver at first use (the library
 // does not link libcuda, so it loads on machines without a driver).
 bool encode_tiled(CUtensorMap* map, CUtensorMapDataType dt, int rank, const void* base,
-                  const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box);
+                  const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box,
+                  CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B);
 
 int num_sms();
 
