@@ -28,6 +28,11 @@ Readings where the pages are silent (each also listed in the design notes):
   R5  gamma_q / gamma_k have shape [d_h], shared across heads and positions.
   R6  GQA: query head h reads kv head h // G (reshape to [H_kv, G]).
   R7  The query scale multiplies Q after RoPE, before the logits.
+  R8  A cache slot that holds no token stores position -1 (EMPTY_SLOT); a
+      fresh cache is all empty, and pad tokens are written as empty.
+  R9  With a cache, the causal-and-padding mask is over slots (s <= the
+      query's own slot, slot not empty) and the sliding mask compares stored
+      positions with the query position.
 """
 from __future__ import annotations
 
@@ -152,16 +157,22 @@ def attend(Q, K, V, t_idx, s_idx, valid, attn_type, window):
     s_idx, query positions t_idx.  Q is reshaped to [Tq, H_kv, G, d_h] and
     contracted with K; blocked logits are K_MASK; softmax over s mixes V.
     Returns [Tq, H, d_h]."""
+    # Mask: causal + padding; local layers also multiply in the sliding mask
+    mask = causal_padding_mask(t_idx, s_idx, valid)
+    if attn_type == LOCAL_SLIDING:
+        mask = mask & create_sliding_mask(t_idx, s_idx, window)
+    return attend_masked(Q, K, V, mask)
+
+
+def attend_masked(Q, K, V, mask):
+    """[AB] How it works, Scores: GQA logits, K_MASK where ``mask`` [Tq, S] is
+    False, softmax over s, V mix.  Q [Tq, H, d_h], K, V [S, H_kv, d_h];
+    returns [Tq, H, d_h]."""
     Tq, H, d_h = Q.shape
     H_kv = K.shape[1]
     G = H // H_kv
     Qg = Q.reshape(Tq, H_kv, G, d_h)
     logits = torch.einsum("tkgc,skc->tkgs", Qg, K)        # [Tq, H_kv, G, S]
-
-    # Mask: causal + padding; local layers also multiply in the sliding mask
-    mask = causal_padding_mask(t_idx, s_idx, valid)
-    if attn_type == LOCAL_SLIDING:
-        mask = mask & create_sliding_mask(t_idx, s_idx, window)
     logits = torch.where(mask[:, None, None, :], logits, torch.tensor(K_MASK, dtype=F64))
 
     # Softmax over s, then mix V ([AB] Scores)
@@ -236,6 +247,98 @@ def attention_layer(x, segment_pos, pad_lens, Wq, Wkv, Wo, gamma_q, gamma_k, *,
     if rows is None:
         return torch.stack(outs, 0)
     return outs
+
+
+# ----------------------------------------------------------------------------
+# the KV-cache path
+# ----------------------------------------------------------------------------
+# Reading R8: stored position of a cache slot that holds no token (never
+# written, or written by a pad token).  Every real position is >= 0.
+EMPTY_SLOT = -1
+
+
+def init_cache(B: int, S: int, H_kv: int, d_h: int) -> dict:
+    """An empty left-aligned cache of S slots per batch row ([AB] How it works,
+    Cache): K and V [B, S, H_kv, d_h] and the stored positions [B, S]."""
+    return {"k": torch.zeros(B, S, H_kv, d_h, dtype=F64),
+            "v": torch.zeros(B, S, H_kv, d_h, dtype=F64),
+            "pos": torch.full((B, S), EMPTY_SLOT, dtype=torch.int64)}
+
+
+def dynamic_update_slice(buf: torch.Tensor, update: torch.Tensor, start: int) -> torch.Tensor:
+    """[AB] How it works, Cache: a copy of ``buf`` whose slots
+    [start, start + update.shape[1]) along axis 1 are replaced by ``update``;
+    every other slot keeps its value."""
+    out = buf.clone()
+    out[:, start:start + update.shape[1]] = update.to(out.dtype)
+    return out
+
+
+def cache_mask(q_slots, q_pos, slot_pos, attn_type, window):
+    """Mask of one batch row's queries over its cache slots.
+
+    q_slots [Tq] are the slots the queries were written to, q_pos [Tq] their
+    positions, slot_pos [S] the stored positions.  Reading R9: the incoming
+    causal-and-padding mask over the cache keeps s <= slot(t) and slots that
+    hold a token (stored position >= 0); a local layer multiplies in the
+    sliding mask of [AB] How it works evaluated on the stored positions, which
+    is what the stored positions are kept for ([AB] How it works, Cache)."""
+    s = torch.arange(slot_pos.shape[0])
+    mask = (s[None, :] <= q_slots[:, None]) & (slot_pos[None, :] >= 0)
+    if attn_type == LOCAL_SLIDING:
+        mask = mask & create_sliding_mask(q_pos, slot_pos, window)
+    return mask
+
+
+def attention_layer_cached(x, segment_pos, pad_lens, cache, end_index, Wq, Wkv, Wo,
+                           gamma_q, gamma_k, *, H, H_kv, d_h, attn_type, window,
+                           rope_base, rope_scale, query_scale):
+    """One attention layer over T new tokens per batch row with a KV cache.
+
+    [AB] How it works: the new tokens' K (after QK-norm and RoPE) and V, and
+    their positions, are written into the left-aligned cache at slot
+    ``end_index`` with dynamic_update_slice; the queries then attend over every
+    cache slot under ``cache_mask``.  Pad tokens (t >= T - pad_b, reading R3)
+    are stored with position EMPTY_SLOT and get output 0.
+
+    x [B,T,D], segment_pos [B,T], cache from ``init_cache`` (or a previous
+    call).  Returns (out [B,T,D], the updated cache); the input cache is not
+    modified.
+    """
+    B, T, D = x.shape
+    S = cache["pos"].shape[1]
+    if end_index < 0 or end_index + T > S:
+        raise ValueError("cache overflow: end_index + T > S")
+    if pad_lens is None:
+        pad_lens = torch.zeros(B, dtype=torch.int64)
+    t = torch.arange(T)
+    is_pad = t[None, :] >= (T - torch.as_tensor(pad_lens, dtype=torch.int64))[:, None]   # [B, T]
+
+    # Projections, QK-norm, RoPE, then the query scale ([AB] How it works)
+    Q = project(x, Wq).reshape(B, T, H, d_h)
+    K = project(x, Wkv[0]).reshape(B, T, H_kv, d_h)
+    V = project(x, Wkv[1]).reshape(B, T, H_kv, d_h)
+    Q = rms_norm(Q, gamma_q)
+    K = rms_norm(K, gamma_k)
+    Q = rope(Q, segment_pos, rope_base, rope_scale)
+    K = rope(K, segment_pos, rope_base, rope_scale)
+    Q = Q * query_scale
+
+    # Cache write ([AB] How it works, Cache)
+    stored_pos = torch.where(is_pad, torch.tensor(EMPTY_SLOT), segment_pos.to(torch.int64))
+    new = {"k": dynamic_update_slice(cache["k"], K, end_index),
+           "v": dynamic_update_slice(cache["v"], V, end_index),
+           "pos": dynamic_update_slice(cache["pos"], stored_pos, end_index)}
+
+    outs = []
+    for b in range(B):
+        mask = cache_mask(end_index + t, segment_pos[b].to(torch.int64), new["pos"][b],
+                          attn_type, window)
+        enc = attend_masked(Q[b], new["k"][b], new["v"][b], mask)
+        out = project(enc.reshape(T, H * d_h), Wo)
+        out[is_pad[b]] = 0.0
+        outs.append(out)
+    return torch.stack(outs, 0), new
 
 
 def block_attention(x, gamma_pre, gamma_post, **layer_kwargs):
