@@ -517,6 +517,227 @@ def run_e2e(args, w, layers, x_cpu, pads, torch, G3, dev, stack, world):
                     "gemma3_block_attn_forward" if stack else "gemma3_attn_forward")}
 
 
+# ---------------------------------------------------------------------------- decode arm
+DECODE_METRIC = "attention-layer decode tokens/s (new tokens per row per step over a KV cache)"
+
+
+def _timed_clock_region(torch, args, world, local, dev, stream, step):
+    """W warm-up steps, then K timed steps between barriers (each after an L2
+    flush outside its events); returns (per-kernel events, step ms, wall s,
+    clock summary)."""
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    gpu_index = None
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    if vis:
+        gpu_index = vis.split(",")[local]
+    events, step_ev = {}, []
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(gpu_index) as clocks:
+        wall0 = time.perf_counter()
+        for _ in range(args.steps):
+            flush.zero_()
+            s0 = torch.cuda.Event(enable_timing=True)
+            s1 = torch.cuda.Event(enable_timing=True)
+            s0.record(stream)
+            step(events)
+            s1.record(stream)
+            step_ev.append((s0, s1))
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - wall0
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    return events, [a.elapsed_time(b) for a, b in step_ev], wall, clocks.summary()
+
+
+def decode_work(w, sms: int) -> tuple:
+    """Algorithmic bytes per step of each kernel of a decode step, and the
+    launches per step.  Attention reads the visible slots' K' and V once (a
+    local layer's window, a global layer's whole prompt) plus Q' and O."""
+    M, D, H, H_kv, d_h = w.M, w.D, w.H, w.H_kv, w.d_h
+    HD, KVD = H * d_h, H_kv * d_h
+    end = w.cache_len - w.T
+    visible = end + w.T if w.window == 0 else min(w.window + w.T - 1, end + w.T)
+    attn = w.B * visible * KVD * 2 * 2 + 2 * M * HD * 2 + w.B * (end + w.T) * 4
+    lin = (HD * D + 2 * KVD * D + D * HD) * 2 + M * D * 2 * 2 + M * (HD + 2 * KVD) * 2
+    work = {"attention": float(attn), "linear": float(lin),
+            "qk_norm_rope": float(metrics.prologue_bytes(M, H, H_kv, d_h)),
+            "cache_write": float(M * KVD * 2 * 2 * 2 + M * 4)}
+    # splits of the cache attention (the library's plan: two CTAs per SM over
+    # B * H_kv * query groups, at least one 32-slot tile each)
+    G = H // H_kv
+    want = min(w.T * G, 8)
+    rb = max(G, 2 if want <= 2 else (4 if want <= 4 else 8))
+    units = w.B * H_kv * ((w.T + rb // G - 1) // (rb // G))
+    nsplit = max(1, min((2 * sms) // units, (end + w.T + 31) // 32, max(1, 2048 // units)))
+    launches = {"linear": 3, "qk_norm_rope": 1, "cache_write": 1,
+                "attention": 1 + (1 if w.window > 0 else 0) + (1 if nsplit > 1 else 0)}
+    return work, launches
+
+
+def run_gpu_decode(args, world, rank, local):
+    import torch
+
+    import __graft_entry__
+    __graft_entry__.build()
+    import transformer_attention_gb300 as G3
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    w = WL.WORKLOADS[args.workload]
+    M, D, H, H_kv, d_h, S = w.M, w.D, w.H, w.H_kv, w.d_h, w.cache_len
+    HD, KVD = H * d_h, H_kv * d_h
+    end = S - w.T
+    L = LayerBuffers(w, 0, None, torch, G3)
+    x_cpu = WL.x_full(w)
+    x = x_cpu.to(dev)
+    seg = WL.segment_pos(w).to(dev)
+    Kc, Vc, pc = (t.to(dev) for t in WL.kv_cache(w))
+    qbuf = torch.empty((M, HD), dtype=torch.float16, device=dev)
+    kvbuf = torch.empty((M, 2 * KVD), dtype=torch.float16, device=dev)
+    out = torch.empty((M, D), dtype=torch.bfloat16, device=dev)
+    aws_bytes = G3.gemma3_cached_attention_workspace_size(w.B, w.T, S, H, H_kv, d_h)
+    aws = torch.empty(max(aws_bytes, 256), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    win = L.window if L.attn_type == G3.GEMMA3_LOCAL_SLIDING else 0
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    work, launches = decode_work(w, sms)
+
+    def step(ev=None):
+        """One decode step as stage calls (the kernels and launch shapes of
+        gemma3_attn_forward_cached); re-writing the same slot every step."""
+        def mark():
+            if ev is None:
+                return None
+            e0 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            return e0
+
+        def done(name, e0):
+            if ev is not None:
+                e1 = torch.cuda.Event(enable_timing=True)
+                e1.record(stream)
+                ev.setdefault(name, []).append((e0, e1))
+
+        e = mark()
+        G3.gemma3_linear(x.reshape(M, D), D, L.p["Wq"], D, qbuf, HD, M, HD, D, G3.GEMMA3_BF16,
+                         G3.GEMMA3_F16)
+        done("proj_q", e)
+        e = mark()
+        G3.gemma3_linear(x.reshape(M, D), D, L.p["Wkv"], D, kvbuf, 2 * KVD, M, 2 * KVD, D,
+                         G3.GEMMA3_BF16, G3.GEMMA3_F16)
+        done("proj_kv", e)
+        e = mark()
+        G3.gemma3_qk_norm_rope(qbuf, HD, kvbuf, 2 * KVD, L.p["gamma_q"], L.p["gamma_k"], seg, M,
+                               H, H_kv, d_h, L.rope_base, L.rope_scale, w.query_scale)
+        done("qk_norm_rope", e)
+        e = mark()
+        G3.gemma3_kv_cache_write(kvbuf, kvbuf[:, KVD:], 2 * KVD, seg, None, w.B, w.T, S, end,
+                                 H_kv, d_h, Kc, Vc, pc)
+        done("cache_write", e)
+        e = mark()
+        G3.gemma3_cached_attention(qbuf, Kc, Vc, pc, seg, None, qbuf, G3.GEMMA3_BF16, w.B, w.T,
+                                   S, end, H, H_kv, d_h, win, aws, aws.numel())
+        done("attention", e)
+        e = mark()
+        G3.gemma3_linear(qbuf, HD, L.p["Wo"], HD, out, D, M, D, HD, G3.GEMMA3_BF16,
+                         G3.GEMMA3_BF16)
+        done("proj_o", e)
+
+    step()
+    assert G3.gemma3_attn_check_status() == 0
+    events, step_ms, wall, clk = _timed_clock_region(torch, args, world, local, dev, stream, step)
+    st = G3.gemma3_attn_check_status()
+    assert st == 0, st
+    tokens = float(w.B * w.T)
+    dev_seconds = sum(step_ms) / 1e3
+    value, max_seconds = whole_job_value(tokens * args.steps, dev_seconds, world, dev)
+    kern_ms = {k: sum(a.elapsed_time(b) for a, b in v) for k, v in events.items()}
+    proj = {k: kern_ms.pop(k) / args.steps for k in ("proj_q", "proj_kv", "proj_o")}
+    kern_ms["linear"] = sum(proj.values()) * args.steps
+
+    peaks, peak_src = load_peaks()
+    dom = max(("attention", "linear"), key=lambda k: kern_ms[k])
+    avg_s = kern_ms[dom] / 1e3 / (launches[dom] * args.steps)
+    achieved = work[dom] / launches[dom] / avg_s / 1e9
+    roof = {"bound": "hbm", "unit": "GB/s", "peak_kind": f"hbm copy ({peak_src})",
+            "kernel": dom, "achieved": achieved, "peak": peaks["hbm_gbs"],
+            "frac": achieved / peaks["hbm_gbs"], "traffic": traffic_for(dom, w.name)}
+    total_ms = sum(step_ms)
+    breakdown = {k: {"ms_per_step": ms / args.steps, "share": ms / total_ms,
+                     "gbs": work[k] * args.steps / (ms / 1e3) / 1e9}
+                 for k, ms in kern_ms.items()}
+    for k, ms in proj.items():
+        breakdown[k] = {"ms_per_step": ms}
+
+    # ---- end to end through gemma3_attn_forward_cached with host buffers
+    x_host = x_cpu.pin_memory()
+    seg_host = WL.segment_pos(w).pin_memory()
+    x_d = torch.empty_like(x_host, device=dev)
+    seg_d = torch.empty_like(seg_host, device=dev)
+    out_host = torch.empty((w.B, w.T, D), dtype=torch.bfloat16, pin_memory=True)
+    y = torch.empty((w.B, w.T, D), dtype=torch.bfloat16, device=dev)
+    dims = (w.B, w.T, D, H, H_kv, d_h)
+    ws_bytes = G3.gemma3_attn_cached_workspace_size(dims, S)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+
+    def one(ev=None):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        x_d.copy_(x_host, non_blocking=True)
+        seg_d.copy_(seg_host, non_blocking=True)
+        G3.gemma3_attn_forward_cached(dims, S, end, x_d, seg_d, None, L.p["Wq"], L.p["Wkv"],
+                                      L.p["Wo"], L.p["gamma_q"], L.p["gamma_k"], L.attn_type,
+                                      L.window, L.rope_base, L.rope_scale, w.query_scale, Kc,
+                                      Vc, pc, y, ws, ws_bytes)
+        out_host.copy_(y, non_blocking=True)
+        if ev is not None:
+            e1 = torch.cuda.Event(enable_timing=True)
+            e1.record(stream)
+            ev.setdefault("e2e", []).append((e0, e1))
+
+    e_events, _, _, _ = _timed_clock_region(torch, args, world, local, dev, stream, one)
+    e_secs = sum(a.elapsed_time(b) for a, b in e_events["e2e"]) / 1e3
+    e_value, _ = whole_job_value(tokens * args.steps, e_secs, world, dev)
+    assert G3.gemma3_attn_check_status() == 0
+    e2e = {"value": e_value, "unit": "tokens/s",
+           "h2d_bytes_per_step": x_host.numel() * 2 + seg_host.numel() * 4,
+           "d2h_bytes_per_step": out_host.numel() * 2, "api": "gemma3_attn_forward_cached"}
+
+    line = {
+        "metric": DECODE_METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": max_seconds * 1e3 / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) activations and cached K'/V, N(0,1/D) weights)",
+        "config": {"workload": w.name, "B": w.B, "T_new": w.T, "cache_slots": S,
+                   "D": D, "H": H, "H_kv": H_kv, "d_h": d_h, "attn": w.attn_type,
+                   "window": w.window,
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": "flushed before every timed step (256 MiB write, outside step events)",
+                   "operands": "bf16 projections, f16 cache and attention operands, f32 math"},
+        "roofline": roof, "kernels": breakdown,
+        "gpu_launches": int(sum(launches.values()) * args.steps),
+        "wall_s_timed_region": wall, "e2e": e2e, "clocks": clk,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, budget_s=args.cpu_budget)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
 # ---------------------------------------------------------------------------- oracle (CPU)
 _ORACLE_WEIGHTS = {}
 
@@ -566,6 +787,28 @@ def oracle_sample(w, n_tokens: int):
     return time.perf_counter() - t0
 
 
+def oracle_decode_sample(w):
+    """The fp64 oracle's cached layer for one decode step of batch row 0
+    (its whole cache).  Returns seconds; input generation is outside."""
+    import torch
+
+    from oracle import gemma3_oracle as O
+    ws = WL.small(w, B=1)
+    K, V, pos = WL.kv_cache(ws)
+    cache = {"k": K.to(torch.float64), "v": V.to(torch.float64), "pos": pos.to(torch.int64)}
+    del K, V
+    x = WL.x_full(ws)
+    seg = WL.segment_pos(ws)
+    p = _oracle_weights(w)
+    t0 = time.perf_counter()
+    O.attention_layer_cached(x, seg, None, cache, w.cache_len - w.T, p["Wq"], p["Wkv"], p["Wo"],
+                             p["gamma_q"], p["gamma_k"], H=w.H, H_kv=w.H_kv, d_h=w.d_h,
+                             attn_type=O.LOCAL_SLIDING if w.attn_type == "local" else O.GLOBAL,
+                             window=w.window, rope_base=w.rope_base, rope_scale=w.rope_scale,
+                             query_scale=w.query_scale)
+    return time.perf_counter() - t0
+
+
 def sample_tokens(w, budget_s: float) -> int:
     """Prefix length whose oracle run takes roughly budget_s (probed at 256)."""
     probe = min(256, w.T)
@@ -578,6 +821,12 @@ def sample_tokens(w, budget_s: float) -> int:
 
 def cpu_baseline(w, budget_s: float = 15.0):
     import torch
+    if w.cache_len > 0:
+        secs = oracle_decode_sample(w)
+        return {"value": w.T / secs, "unit": "tokens/s", "cores": torch.get_num_threads(),
+                "kind": "oracle",
+                "sample": f"fp64 oracle, one decode step of batch row 0 of {w.name} over its "
+                          f"{w.cache_len}-slot cache, {secs:.2f} s"}
     n = sample_tokens(w, budget_s)
     secs = oracle_sample(w, n)
     return {"value": n / secs, "unit": "tokens/s", "cores": torch.get_num_threads(),
@@ -591,13 +840,19 @@ def run_reference(args, world, rank):
         return
     import torch
     w = WL.WORKLOADS[args.workload]
-    n = sample_tokens(w, 4.0)
+    if w.cache_len > 0:
+        n = w.T
+        run = lambda: oracle_decode_sample(w)          # noqa: E731
+    else:
+        n = sample_tokens(w, 4.0)
+        run = lambda: oracle_sample(w, n)              # noqa: E731
     for _ in range(args.warmup):
-        oracle_sample(w, n)
-    times = [oracle_sample(w, n) for _ in range(args.steps)]
+        run()
+    times = [run() for _ in range(args.steps)]
     secs = sum(times)
     value = n * args.steps / secs
-    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+    line = {"metric": DECODE_METRIC if w.cache_len > 0 else METRIC, "value": value,
+            "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs * 1e3 / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "impl": "reference",
@@ -605,7 +860,9 @@ def run_reference(args, world, rank):
                        "H_kv": w.H_kv, "d_h": w.d_h, "attn": w.attn_type},
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": torch.get_num_threads(),
                              "kind": "oracle",
-                             "sample": f"first {n} tokens of batch row 0 per step"},
+                             "sample": (f"one decode step of batch row 0 per step"
+                                        if w.cache_len > 0 else
+                                        f"first {n} tokens of batch row 0 per step")},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -632,6 +889,9 @@ def main(argv=None):
         WL.WORKLOADS[args.workload] = WL.small(WL.WORKLOADS[args.workload], **over)
     if args.impl == "reference":
         run_reference(args, world, rank)
+        return
+    if WL.WORKLOADS[args.workload].cache_len > 0:
+        run_gpu_decode(args, world, rank, local)
         return
     run_gpu(args, world, rank, local)
 

@@ -217,6 +217,69 @@ int gemma3_block_forward(const gemma3_attn_dims* dims, int D_ff, const void* x, 
                          float query_scale, void* workspace, size_t workspace_bytes,
                          void* stream);
 
+/* ------------------------------------------------------------------ KV cache */
+
+/* A layer's KV cache ([AB] How it works, Cache): K' (after QK-norm and RoPE)
+ * and V of earlier tokens in a left-aligned buffer of S slots per batch row,
+ * with the position each slot was written at.
+ *   K_cache, V_cache  [B, S, H_kv, d_h] fp16, 16-byte aligned
+ *   pos_cache         [B, S] int32; a slot that holds no token stores a
+ *                     negative position.  A fresh cache must be all negative
+ *                     (cudaMemset to 0xFF gives -1 everywhere).
+ * Mask with a cache, for the new token t of row b written to slot end + t
+ * (the pages' causal-and-padding mask taken over slots, and the sliding mask
+ * evaluated on stored positions, which is why they are stored):
+ *   slot s is visible  <=>  s <= end + t  and  pos_cache[b, s] >= 0  and, on a
+ *   local layer, segment_pos[b, t] - W < pos_cache[b, s] < segment_pos[b, t] + W.
+ * The caller owns the cache and advances end_index itself; nothing wraps. */
+
+/* Workspace of gemma3_attn_forward_cached for T new tokens per row and a
+ * cache of S slots. */
+int gemma3_attn_cached_workspace_size(const gemma3_attn_dims* dims, int S, size_t* bytes);
+
+/* One attention layer over dims->T new tokens per row with a KV cache.
+ * Computes Q, K', V of the new tokens exactly as gemma3_attn_forward, writes
+ * K', V and their positions into slots [end_index, end_index + T) of the
+ * cache with a dynamic_update_slice (pad tokens, t >= T - pad_lens[b], are
+ * stored with position -1), then attends every new token over the cache
+ * under the mask above and applies the output projection.
+ *   0 <= end_index, end_index + T <= S; segment_pos [B, T] >= 0 for valid
+ *   tokens; out [B, T, D] bf16, pad rows 0.  Other arguments as in
+ *   gemma3_attn_forward.  T = 1 is one decode step.
+ * The attention of few new tokens is bound by reading the cache (HBM); a
+ * prompt of >= 128 tokens written at slot 0 of a global layer runs on the
+ * tensor-core flash kernel instead, whose mask is the same there. */
+int gemma3_attn_forward_cached(const gemma3_attn_dims* dims, int S, int end_index, const void* x,
+                               const int32_t* segment_pos, const int32_t* pad_lens,
+                               const void* Wq, const void* Wkv, const void* Wo,
+                               const void* gamma_q, const void* gamma_k, int attn_type,
+                               int window, double rope_base, double rope_scale, float query_scale,
+                               void* K_cache, void* V_cache, int32_t* pos_cache, void* out,
+                               void* workspace, size_t workspace_bytes, void* stream);
+
+/* The cache write alone: K_rows / V_rows are fp16 rows with stride ld_rows
+ * elements, row b*T + t holding token (b, t)'s H_kv*d_h values; they go to
+ * slot end_index + t, and pos_cache[b, end_index + t] = segment_pos[b, t]
+ * (-1 for pad tokens; pad_lens may be NULL). */
+int gemma3_kv_cache_write(const void* K_rows, const void* V_rows, long ld_rows,
+                          const int32_t* segment_pos, const int32_t* pad_lens, int B, int T,
+                          int S, int end_index, int H_kv, int d_h, void* K_cache, void* V_cache,
+                          int32_t* pos_cache, void* stream);
+
+/* Workspace of gemma3_cached_attention. */
+int gemma3_cached_attention_workspace_size(int B, int T, int S, int H, int H_kv, int d_h,
+                                           size_t* bytes);
+
+/* The attention over a cache alone: Q' [B, T, H, d_h] fp16 (query scale
+ * applied) of tokens already written to slots [end_index, end_index + T);
+ * O [B, T, H, d_h] in o_dtype (GEMMA3_BF16 | GEMMA3_F16; may alias Q'), pad
+ * rows 0; window <= 0 means global.  Mask as above. */
+int gemma3_cached_attention(const void* Q, const void* K_cache, const void* V_cache,
+                            const int32_t* pos_cache, const int32_t* segment_pos,
+                            const int32_t* pad_lens, void* O, int o_dtype, int B, int T, int S,
+                            int end_index, int H, int H_kv, int d_h, int window, void* workspace,
+                            size_t workspace_bytes, void* stream);
+
 /* ------------------------------------------------------------- stage entry points */
 
 /* C[M, N] = A[M, K] * W[N, K]^T (the projection einsums of [AB] How it

@@ -8,7 +8,9 @@ from __future__ import annotations
 
 from ._lib import (  # noqa: F401  (re-exported C-ABI names)
     GEMMA3_BF16, GEMMA3_F16, GEMMA3_F32, GEMMA3_GLOBAL, GEMMA3_LOCAL_SLIDING, Gemma3Error,
-    gemma3_attn_check_status, gemma3_attn_forward, gemma3_attn_workspace_size,
+    gemma3_attn_cached_workspace_size, gemma3_attn_check_status, gemma3_attn_forward,
+    gemma3_attn_forward_cached, gemma3_attn_workspace_size, gemma3_cached_attention,
+    gemma3_cached_attention_workspace_size, gemma3_kv_cache_write,
     gemma3_block_attn_forward, gemma3_block_attn_workspace_size, gemma3_block_ffn_forward,
     gemma3_block_ffn_workspace_size, gemma3_block_forward, gemma3_block_workspace_size,
     gemma3_cast_bf16_f16, gemma3_geglu,
@@ -17,7 +19,8 @@ from ._lib import (  # noqa: F401  (re-exported C-ABI names)
     gemma3_postnorm_residual, gemma3_qk_norm_rope, gemma3_query_scale, gemma3_rmsnorm,
     gemma3_selftest_wait_timeout, lib)
 
-__all__ = ["attention_forward", "block_attention_forward", "block_forward", "linear", "lib"]
+__all__ = ["attention_forward", "attention_forward_cached", "block_attention_forward",
+           "block_forward", "new_kv_cache", "linear", "lib"]
 
 
 def _empty_ws(nbytes: int, device):
@@ -44,6 +47,40 @@ def attention_forward(x, segment_pos, pad_lens, Wq, Wkv, Wo, gamma_q, gamma_k, *
     gemma3_attn_forward(dims, x, segment_pos, pad_lens, Wq, Wkv, Wo, gamma_q, gamma_k, attn_type,
                         window, rope_base, rope_scale, query_scale, out, workspace,
                         workspace.numel(), stream)
+    return out
+
+
+def new_kv_cache(B, S, H_kv, d_h, device):
+    """An empty KV cache of S slots per row: (K_cache, V_cache) [B, S, H_kv,
+    d_h] fp16 and pos_cache [B, S] int32, every stored position -1."""
+    import torch
+    K = torch.zeros((B, S, H_kv, d_h), dtype=torch.float16, device=device)
+    V = torch.zeros_like(K)
+    pos = torch.full((B, S), -1, dtype=torch.int32, device=device)
+    return K, V, pos
+
+
+def attention_forward_cached(x, segment_pos, pad_lens, cache, end_index, Wq, Wkv, Wo, gamma_q,
+                             gamma_k, *, H, H_kv, attn_type, window, rope_base, rope_scale,
+                             query_scale, out=None, workspace=None, stream=None):
+    """One attention layer over x [B,T,D] bf16, new tokens written to slots
+    [end_index, end_index + T) of ``cache`` = (K_cache, V_cache, pos_cache)
+    from new_kv_cache (updated in place).  Returns out [B,T,D] bf16."""
+    import torch
+    B, T, D = x.shape
+    d_h = gamma_q.shape[0]
+    K_cache, V_cache, pos_cache = cache
+    S = pos_cache.shape[1]
+    dims = (B, T, D, H, H_kv, d_h)
+    ws_bytes = gemma3_attn_cached_workspace_size(dims, S)
+    if workspace is None:
+        workspace = _empty_ws(ws_bytes, x.device)
+    if out is None:
+        out = torch.empty((B, T, D), dtype=torch.bfloat16, device=x.device)
+    gemma3_attn_forward_cached(dims, S, end_index, x, segment_pos, pad_lens, Wq, Wkv, Wo,
+                               gamma_q, gamma_k, attn_type, window, rope_base, rope_scale,
+                               query_scale, K_cache, V_cache, pos_cache, out, workspace,
+                               workspace.numel(), stream)
     return out
 
 

@@ -63,6 +63,22 @@ SIGNATURES = {
                                      c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                                      c_void_p, c_void_p, c_int, c_int, c_double, c_double,
                                      c_float, c_void_p, c_size_t, c_void_p]),
+    "gemma3_attn_cached_workspace_size": (c_int, [ctypes.POINTER(gemma3_attn_dims), c_int,
+                                                  ctypes.POINTER(c_size_t)]),
+    "gemma3_attn_forward_cached": (c_int, [ctypes.POINTER(gemma3_attn_dims), c_int, c_int,
+                                           c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
+                                           c_void_p, c_void_p, c_void_p, c_int, c_int, c_double,
+                                           c_double, c_float, c_void_p, c_void_p, c_void_p,
+                                           c_void_p, c_void_p, c_size_t, c_void_p]),
+    "gemma3_kv_cache_write": (c_int, [c_void_p, c_void_p, c_long, c_void_p, c_void_p, c_int,
+                                      c_int, c_int, c_int, c_int, c_int, c_void_p, c_void_p,
+                                      c_void_p, c_void_p]),
+    "gemma3_cached_attention_workspace_size": (c_int, [c_int, c_int, c_int, c_int, c_int, c_int,
+                                                       ctypes.POINTER(c_size_t)]),
+    "gemma3_cached_attention": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
+                                        c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_int,
+                                        c_int, c_int, c_int, c_int, c_void_p, c_size_t,
+                                        c_void_p]),
     "gemma3_geglu": (c_int, [c_void_p, c_long, c_void_p, c_long, c_void_p, c_long, c_int, c_int,
                              c_int, c_int, c_void_p]),
     "gemma3_linear": (c_int, [c_void_p, c_long, c_void_p, c_long, c_void_p, c_long, c_int, c_int,
@@ -247,6 +263,49 @@ def gemma3_block_forward(dims, D_ff, x, x_dtype, y, segment_pos, pad_lens, Wq, W
         _ptr(gamma_post_attn), _ptr(gamma_pre_ffn), _ptr(gamma_post_ffn), _ptr(W_gating),
         _ptr(W_down), attn_type, window, rope_base, rope_scale, query_scale, _ptr(workspace),
         workspace_bytes, _stream(stream)))
+
+
+def gemma3_attn_cached_workspace_size(dims, S) -> int:
+    n = c_size_t()
+    d = _dims(*dims)
+    _check("gemma3_attn_cached_workspace_size",
+           lib().gemma3_attn_cached_workspace_size(ctypes.byref(d), S, ctypes.byref(n)))
+    return n.value
+
+
+def gemma3_attn_forward_cached(dims, S, end_index, x, segment_pos, pad_lens, Wq, Wkv, Wo,
+                               gamma_q, gamma_k, attn_type, window, rope_base, rope_scale,
+                               query_scale, K_cache, V_cache, pos_cache, out, workspace,
+                               workspace_bytes, stream=None):
+    d = _dims(*dims)
+    return _check("gemma3_attn_forward_cached", lib().gemma3_attn_forward_cached(
+        ctypes.byref(d), S, end_index, _ptr(x), _ptr(segment_pos), _ptr(pad_lens), _ptr(Wq),
+        _ptr(Wkv), _ptr(Wo), _ptr(gamma_q), _ptr(gamma_k), attn_type, window, rope_base,
+        rope_scale, query_scale, _ptr(K_cache), _ptr(V_cache), _ptr(pos_cache), _ptr(out),
+        _ptr(workspace), workspace_bytes, _stream(stream)))
+
+
+def gemma3_kv_cache_write(K_rows, V_rows, ld_rows, segment_pos, pad_lens, B, T, S, end_index,
+                          H_kv, d_h, K_cache, V_cache, pos_cache, stream=None):
+    return _check("gemma3_kv_cache_write", lib().gemma3_kv_cache_write(
+        _ptr(K_rows), _ptr(V_rows), ld_rows, _ptr(segment_pos), _ptr(pad_lens), B, T, S,
+        end_index, H_kv, d_h, _ptr(K_cache), _ptr(V_cache), _ptr(pos_cache), _stream(stream)))
+
+
+def gemma3_cached_attention_workspace_size(B, T, S, H, H_kv, d_h) -> int:
+    n = c_size_t()
+    _check("gemma3_cached_attention_workspace_size", lib().gemma3_cached_attention_workspace_size(
+        B, T, S, H, H_kv, d_h, ctypes.byref(n)))
+    return n.value
+
+
+def gemma3_cached_attention(Q, K_cache, V_cache, pos_cache, segment_pos, pad_lens, O, o_dtype, B,
+                            T, S, end_index, H, H_kv, d_h, window, workspace, workspace_bytes,
+                            stream=None):
+    return _check("gemma3_cached_attention", lib().gemma3_cached_attention(
+        _ptr(Q), _ptr(K_cache), _ptr(V_cache), _ptr(pos_cache), _ptr(segment_pos),
+        _ptr(pad_lens), _ptr(O), o_dtype, B, T, S, end_index, H, H_kv, d_h, window,
+        _ptr(workspace), workspace_bytes, _stream(stream)))
 
 
 def gemma3_geglu(A, lda, W_gating, ldw, Z, ldz, M, D_ff, K, in_dtype, stream=None):

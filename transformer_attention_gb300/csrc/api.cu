@@ -430,6 +430,154 @@ int gemma3_block_forward(const gemma3_attn_dims* dims, int D_ff, const void* x, 
                       as_stream(stream));
 }
 
+// ------------------------------------------------------------ KV-cache path
+
+namespace {
+
+struct CachedWs {
+  size_t q, kv, attn, total;
+};
+
+CachedWs cached_ws(const gemma3_attn_dims* d, int S) {
+  const size_t M = static_cast<size_t>(d->B) * d->T;
+  CachedWs w;
+  w.q = round_up(M * d->H * d->d_h * 2, 256);
+  w.kv = round_up(M * 2 * d->H_kv * d->d_h * 2, 256);
+  w.attn = round_up(cached_attention_ws_bytes(d->B, d->T, S, d->H, d->H_kv, d->d_h), 256);
+  w.total = w.q + w.kv + w.attn;
+  return w;
+}
+
+int validate_cache(int B, int T, int S, int end_index, int H_kv, int d_h, const void* K_cache,
+                   const void* V_cache, const int32_t* pos_cache) {
+  if (!K_cache || !V_cache || !pos_cache) return GEMMA3_ERR_INVALID_ARG;
+  if (S < 1 || S > (1 << 30) || end_index < 0 || T < 1 ||
+      static_cast<long long>(end_index) + T > S)
+    return GEMMA3_ERR_INVALID_ARG;
+  if (static_cast<long long>(B) * S >= (1LL << 40) / (static_cast<long long>(H_kv) * d_h))
+    return GEMMA3_ERR_INVALID_ARG;
+  if (!aligned16(K_cache) || !aligned16(V_cache) || (reinterpret_cast<uintptr_t>(pos_cache) & 3u))
+    return GEMMA3_ERR_MISALIGNED;
+  return GEMMA3_OK;
+}
+
+// A prompt written at slot 0 of a global layer sees exactly the causal,
+// unpadded part of itself (every later slot is beyond its causal limit), which
+// is the mask of the tensor-core flash kernel; from this length on that kernel
+// is used for it.
+constexpr int kFlashPrefillMinT = 128;
+
+}  // namespace
+
+int gemma3_attn_cached_workspace_size(const gemma3_attn_dims* dims, int S, size_t* bytes) {
+  const int rc = validate_dims(dims);
+  if (rc != GEMMA3_OK) return rc;
+  if (bytes == nullptr || S < 1) return GEMMA3_ERR_INVALID_ARG;
+  *bytes = cached_ws(dims, S).total;
+  return GEMMA3_OK;
+}
+
+int gemma3_attn_forward_cached(const gemma3_attn_dims* dims, int S, int end_index, const void* x,
+                               const int32_t* segment_pos, const int32_t* pad_lens,
+                               const void* Wq, const void* Wkv, const void* Wo,
+                               const void* gamma_q, const void* gamma_k, int attn_type,
+                               int window, double rope_base, double rope_scale, float query_scale,
+                               void* K_cache, void* V_cache, int32_t* pos_cache, void* out,
+                               void* workspace, size_t workspace_bytes, void* stream) {
+  int rc = validate_layer_args(dims, x, segment_pos, Wq, Wkv, Wo, gamma_q, gamma_k, attn_type,
+                               window, rope_base, rope_scale, workspace);
+  if (rc != GEMMA3_OK) return rc;
+  rc = validate_cache(dims->B, dims->T, S, end_index, dims->H_kv, dims->d_h, K_cache, V_cache,
+                      pos_cache);
+  if (rc != GEMMA3_OK) return rc;
+  if (out == nullptr) return GEMMA3_ERR_INVALID_ARG;
+  if (!aligned16(out)) return GEMMA3_ERR_MISALIGNED;
+  const CachedWs w = cached_ws(dims, S);
+  if (workspace_bytes < w.total) return GEMMA3_ERR_WORKSPACE;
+  int* st = status_ptr();
+  if (st == nullptr) return GEMMA3_ERR_CUDA;
+  const gemma3_attn_dims* d = dims;
+  const int M = d->B * d->T;
+  const int HD = d->H * d->d_h, KVD = d->H_kv * d->d_h;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  uint8_t* qbuf = ws;                 // Q, then Q', then O  [M, H*d_h] fp16/bf16
+  uint8_t* kvbuf = ws + w.q;          // [K'|V] fp16  [M, 2*KVD]
+  uint8_t* aws = kvbuf + w.kv;        // attention partials
+  cudaStream_t s = as_stream(stream);
+  if (launch_linear(x, d->D, Wq, d->D, qbuf, HD, M, HD, d->D, kBF16, kF16, s, st, 0) !=
+          cudaSuccess ||
+      launch_linear(x, d->D, Wkv, d->D, kvbuf, 2 * KVD, M, 2 * KVD, d->D, kBF16, kF16, s, st, 0) !=
+          cudaSuccess ||
+      launch_qk_norm_rope(qbuf, HD, kvbuf, 2 * KVD, gamma_q, gamma_k, segment_pos, M, d->H,
+                          d->H_kv, d->d_h, rope_base, rope_scale, query_scale, s) != cudaSuccess ||
+      launch_kv_cache_append(kvbuf, kvbuf + KVD * 2, 2 * KVD, segment_pos, pad_lens, d->B, d->T, S,
+                             end_index, KVD, K_cache, V_cache, pos_cache, s) != cudaSuccess)
+    return GEMMA3_ERR_CUDA;
+  cudaError_t e;
+  if (end_index == 0 && attn_type == GEMMA3_GLOBAL && d->T >= kFlashPrefillMinT)
+    e = launch_flash_attention(qbuf, kvbuf, kvbuf + KVD * 2, 2 * KVD, qbuf, kBF16, pad_lens, d->B,
+                               d->T, d->H, d->H_kv, d->d_h, 0, s, st);
+  else
+    e = launch_cached_attention(qbuf, K_cache, V_cache, pos_cache, segment_pos, pad_lens, qbuf,
+                                kBF16, d->B, d->T, S, end_index, d->H, d->H_kv, d->d_h,
+                                attn_type == GEMMA3_LOCAL_SLIDING ? window : 0, aws, s, st);
+  if (e != cudaSuccess) return GEMMA3_ERR_CUDA;
+  return to_status(launch_linear(qbuf, HD, Wo, HD, out, d->D, M, d->D, HD, kBF16, kBF16, s, st, 0));
+}
+
+int gemma3_kv_cache_write(const void* K_rows, const void* V_rows, long ld_rows,
+                          const int32_t* segment_pos, const int32_t* pad_lens, int B, int T,
+                          int S, int end_index, int H_kv, int d_h, void* K_cache, void* V_cache,
+                          int32_t* pos_cache, void* stream) {
+  if (!K_rows || !V_rows || !segment_pos || B < 1 || H_kv < 1) return GEMMA3_ERR_INVALID_ARG;
+  if (d_h != 128 && d_h != 256) return GEMMA3_ERR_UNSUPPORTED;
+  int rc = validate_cache(B, T, S, end_index, H_kv, d_h, K_cache, V_cache, pos_cache);
+  if (rc != GEMMA3_OK) return rc;
+  if (ld_rows < static_cast<long>(H_kv) * d_h) return GEMMA3_ERR_INVALID_ARG;
+  if (!aligned16(K_rows) || !aligned16(V_rows) || (ld_rows * 2) % 16) return GEMMA3_ERR_MISALIGNED;
+  rc = check_device();
+  if (rc != GEMMA3_OK) return rc;
+  return to_status(launch_kv_cache_append(K_rows, V_rows, ld_rows, segment_pos, pad_lens, B, T, S,
+                                          end_index, H_kv * d_h, K_cache, V_cache, pos_cache,
+                                          as_stream(stream)));
+}
+
+int gemma3_cached_attention_workspace_size(int B, int T, int S, int H, int H_kv, int d_h,
+                                           size_t* bytes) {
+  if (bytes == nullptr || B < 1 || T < 1 || S < 1 || H < 1 || H_kv < 1 || H % H_kv)
+    return GEMMA3_ERR_INVALID_ARG;
+  const int G = H / H_kv;
+  if ((d_h != 128 && d_h != 256) || (G != 1 && G != 2 && G != 4)) return GEMMA3_ERR_UNSUPPORTED;
+  *bytes = round_up(cached_attention_ws_bytes(B, T, S, H, H_kv, d_h), 256);
+  return GEMMA3_OK;
+}
+
+int gemma3_cached_attention(const void* Q, const void* K_cache, const void* V_cache,
+                            const int32_t* pos_cache, const int32_t* segment_pos,
+                            const int32_t* pad_lens, void* O, int o_dtype, int B, int T, int S,
+                            int end_index, int H, int H_kv, int d_h, int window, void* workspace,
+                            size_t workspace_bytes, void* stream) {
+  size_t need = 0;
+  int rc = gemma3_cached_attention_workspace_size(B, T, S, H, H_kv, d_h, &need);
+  if (rc != GEMMA3_OK) return rc;
+  if (!Q || !O || !segment_pos || !workspace) return GEMMA3_ERR_INVALID_ARG;
+  if (o_dtype != GEMMA3_BF16 && o_dtype != GEMMA3_F16) return GEMMA3_ERR_INVALID_ARG;
+  if (static_cast<long long>(B) * T * H >= (1LL << 31)) return GEMMA3_ERR_INVALID_ARG;
+  rc = validate_cache(B, T, S, end_index, H_kv, d_h, K_cache, V_cache, pos_cache);
+  if (rc != GEMMA3_OK) return rc;
+  if (!aligned16(Q) || !aligned16(O) || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return GEMMA3_ERR_MISALIGNED;
+  if (workspace_bytes < need) return GEMMA3_ERR_WORKSPACE;
+  rc = check_device();
+  if (rc != GEMMA3_OK) return rc;
+  int* st = status_ptr();
+  if (st == nullptr) return GEMMA3_ERR_CUDA;
+  return to_status(launch_cached_attention(Q, K_cache, V_cache, pos_cache, segment_pos, pad_lens, O,
+                                           o_dtype == GEMMA3_F16 ? kF16 : kBF16, B, T, S,
+                                           end_index, H, H_kv, d_h, window > 0 ? window : 0,
+                                           workspace, as_stream(stream), st));
+}
+
 int gemma3_geglu(const void* A, long lda, const void* W_gating, long ldw, void* Z, long ldz,
                  int M, int D_ff, int K, int in_dtype, void* stream) {
   if (!A || !W_gating || !Z || M < 0 || D_ff < 1 || K < 1) return GEMMA3_ERR_INVALID_ARG;

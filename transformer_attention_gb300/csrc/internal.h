@@ -58,4 +58,24 @@ cudaError_t launch_postnorm_residual(const float* a, const void* x, int x_dtype,
                                      const void* gamma, float* y, int M, int D,
                                      cudaStream_t stream);
 
+// KV cache: copy the T new tokens' K' and V rows (KVD = H_kv*d_h fp16 each,
+// row (b, t) at K_rows/V_rows + (b*T + t)*ld) into slot end + t of the caches
+// [B, S, KVD] and store their positions (-1 for pad tokens) in pos_cache [B, S].
+cudaError_t launch_kv_cache_append(const void* K_rows, const void* V_rows, long ld,
+                                   const int32_t* segment_pos, const int32_t* pad_lens, int B,
+                                   int T, int S, int end, int KVD, void* K_cache, void* V_cache,
+                                   int32_t* pos_cache, cudaStream_t stream);
+
+// Workspace of launch_cached_attention (depends only on the shapes and S).
+size_t cached_attention_ws_bytes(int B, int T, int S, int H, int H_kv, int d_h);
+
+// Attention of T query tokens per row (written to slots end..end+T-1) over a
+// left-aligned K'/V cache [B, S, H_kv, d_h] fp16 with stored positions
+// pos_cache [B, S]; Q' and O [B, T, H, d_h] (O in o_dtype, may alias Q').
+cudaError_t launch_cached_attention(const void* Q, const void* K_cache, const void* V_cache,
+                                    const int32_t* pos_cache, const int32_t* qpos,
+                                    const int32_t* pad_lens, void* O, int o_dtype, int B, int T,
+                                    int S, int end, int H, int H_kv, int d_h, int window,
+                                    void* ws, cudaStream_t stream, int* status);
+
 }  // namespace g3

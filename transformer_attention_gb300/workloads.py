@@ -29,6 +29,7 @@ ROW_BLOCK = 1024          # rows of x per independently seeded block
 SEED_X, SEED_WQ, SEED_WKV, SEED_WO, SEED_GQ, SEED_GK, SEED_PAD = 1, 2, 3, 4, 5, 6, 7
 SEED_GPRE, SEED_GPOST = 8, 9
 SEED_WGATE, SEED_WDOWN, SEED_GPRE_FFN, SEED_GPOST_FFN = 10, 11, 12, 13
+SEED_KCACHE, SEED_VCACHE = 14, 15
 
 
 @dataclass(frozen=True)
@@ -50,6 +51,7 @@ class Workload:
     pad: tuple = ("none",)    # ("none",) | ("pad_uniform", lo, hi) | ("valid_uniform", lo, hi)
     num_layers: int = 1
     d_ff: int = 0             # > 0: the workload is the whole block (attention + feed-forward)
+    cache_len: int = 0        # > 0: T new tokens per row appended to a KV cache of this many slots
     description: str = field(default="", compare=False)
 
     @property
@@ -93,7 +95,20 @@ WORKLOADS = {
         description="4B-shaped full block: local attention layer + GeGLU FFN (D_ff 10240)"),
 }
 
-ORDER = ["tiny_local", "1b_global", "4b_local", "27b_global", "12b_stack", "4b_block"]
+# Decode steps with a KV cache (one new token per row) on the 4B-shaped local
+# and the 27B-shaped global layer: the cache holds a prompt that fills every
+# slot but the last, which the new token is written to.
+WORKLOADS["4b_local_decode"] = Workload(
+    "4b_local_decode", B=2, T=1, D=2560, H=8, H_kv=4, d_h=256, attn_type="local", window=1024,
+    rope_base=1e4, rope_scale=1.0, query_scale=256 ** -0.5, model_size="4B", cache_len=32768,
+    description="decode step, 4B-shaped local layer: B2, 1 new token after 32767 cached, W1024")
+WORKLOADS["27b_global_decode"] = Workload(
+    "27b_global_decode", B=1, T=1, D=5376, H=32, H_kv=16, d_h=128, attn_type="global", window=0,
+    rope_base=1e6, rope_scale=8.0, query_scale=168 ** -0.5, model_size="27B", cache_len=131072,
+    description="decode step, 27B-shaped global layer: B1, 1 new token after 131071 cached")
+
+ORDER = ["tiny_local", "1b_global", "4b_local", "27b_global", "12b_stack", "4b_block",
+         "4b_local_decode", "27b_global_decode"]
 
 
 def small(w: Workload, **kw) -> Workload:
@@ -204,8 +219,37 @@ def pad_lens(w: Workload) -> torch.Tensor:
 
 
 def segment_pos(w: Workload) -> torch.Tensor:
-    """RoPE positions: 0..T-1 in every batch row, int32 [B, T]."""
-    return torch.arange(w.T, dtype=torch.int32).repeat(w.B, 1)
+    """RoPE positions, int32 [B, T]: 0..T-1 in every batch row, or for a
+    decode workload the positions after the cached prompt (end .. end+T-1)."""
+    base = w.cache_len - w.T if w.cache_len > 0 else 0
+    return (base + torch.arange(w.T, dtype=torch.int32)).repeat(w.B, 1)
+
+
+def kv_cache(w: Workload, threads: int = 16):
+    """The prompt's cache of a decode workload (CPU): K' and V [B, S, H_kv, d_h]
+    fp16 drawn N(0, 1) (sampled in fp32, rounded to nearest even) in slots
+    [0, S - T), and the stored positions [B, S] int32: 0 .. S-T-1 there and -1
+    (empty) in the last T slots, which the new tokens are written to."""
+    S, end = w.cache_len, w.cache_len - w.T
+    K = torch.zeros((w.B, S, w.H_kv, w.d_h), dtype=torch.float16)
+    V = torch.zeros_like(K)
+    pos = torch.full((w.B, S), -1, dtype=torch.int32)
+    pos[:, :end] = torch.arange(end, dtype=torch.int32)
+    nblk = (end + ROW_BLOCK - 1) // ROW_BLOCK
+
+    def fill(job):
+        b, blk = job
+        s0, s1 = blk * ROW_BLOCK, min((blk + 1) * ROW_BLOCK, end)
+        key = b * nblk + blk
+        for buf, seed in ((K, SEED_KCACHE), (V, SEED_VCACHE)):
+            g = _gen(seed, key)
+            buf[b, s0:s1] = torch.randn((s1 - s0, w.H_kv, w.d_h), generator=g,
+                                        dtype=torch.float32).to(torch.float16)
+
+    jobs = [(b, k) for b in range(w.B) for k in range(nblk)]
+    with ThreadPoolExecutor(max_workers=threads) as ex:
+        list(ex.map(fill, jobs))
+    return K, V, pos
 
 
 def valid_tokens(w: Workload) -> int:
