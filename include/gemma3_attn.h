@@ -287,7 +287,9 @@ int gemma3_cached_attention(const void* Q, const void* K_cache, const void* V_ca
  * ldw (elements); C in out_dtype (GEMMA3_BF16 | GEMMA3_F16 | GEMMA3_F32) with
  * row stride ldc.  fp32 accumulation on the tcgen05 tensor cores.  K % 8 == 0;
  * strides in bytes must be multiples of 16.  max_ctas > 0 caps the
- * persistent grid. */
+ * persistent grid.  For M <= 16 (a decode step's projections) the product is
+ * bound by reading W, and a CUDA-core kernel that streams W once with fp32
+ * sums runs instead (max_ctas is ignored there). */
 int gemma3_linear(const void* A, long lda, const void* W, long ldw, void* C, long ldc, int M,
                   int N, int K, int in_dtype, int out_dtype, int max_ctas, void* stream);
 

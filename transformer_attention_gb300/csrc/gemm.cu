@@ -319,6 +319,8 @@ cudaError_t launch_linear(const void* A, long lda, const void* W, long ldw, void
                           int* status, int max_ctas) {
   if (M <= 0 || N <= 0 || K <= 0) return cudaSuccess;
   if (in_dtype != kBF16 && in_dtype != kF16) return cudaErrorInvalidValue;
+  if (M <= kSkinnyMaxRows)
+    return launch_linear_skinny(A, lda, W, ldw, C, ldc, M, N, K, in_dtype, out_dtype, stream);
   const CUtensorMapDataType tdt =
       in_dtype == kBF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   CUtensorMap ta, tb;

@@ -19,10 +19,18 @@ bool encode_tiled(CUtensorMap* map, CUtensorMapDataType dt, int rank, const void
 int num_sms();
 
 // C[M,N] = A[M,K] * W[N,K]^T, operands in in_dtype (bf16|f16), fp32
-// accumulation, C in out_dtype.
+// accumulation, C in out_dtype.  M <= kSkinnyMaxRows goes to
+// launch_linear_skinny, everything else to the tcgen05 GEMM.
 cudaError_t launch_linear(const void* A, long lda, const void* W, long ldw, void* C, long ldc,
                           int M, int N, int K, int in_dtype, int out_dtype, cudaStream_t stream,
                           int* status, int max_ctas);
+
+// The same product for M <= kSkinnyMaxRows on the CUDA cores (bound by
+// reading W from HBM); K % 8 == 0, 16-byte aligned rows.
+constexpr int kSkinnyMaxRows = 16;
+cudaError_t launch_linear_skinny(const void* A, long lda, const void* W, long ldw, void* C,
+                                 long ldc, int M, int N, int K, int in_dtype, int out_dtype,
+                                 cudaStream_t stream);
 
 // Z[M, D_ff] (fp16) = GELU_tanh(A Wg^T) * (A Wu^T), Wgu = [Wg; Wu] of shape
 // [2*D_ff, K] (the transposed gating weight (2, D_ff, D) viewed as rows).
