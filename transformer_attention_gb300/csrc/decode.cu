@@ -16,6 +16,7 @@
 // softmax per query row and writes an unnormalised partial (m, l, o) that a
 // second kernel merges.  On a local layer a small kernel first finds the
 // first slot any query of the row can see, so CTAs cover only the window.
+#include <algorithm>
 #include <climits>
 #include <cmath>
 
@@ -29,8 +30,10 @@ namespace {
 constexpr int kSlots = 32;         // slots per tile: one per lane in the logits phase
 constexpr int kCWarps = 4;         // consumer warps; warp 4 issues the TMA loads
 constexpr int kDecThreads = (kCWarps + 1) * 32;
-constexpr int kSpanChunk = 4096;   // slots scanned per CTA by the span kernel
+constexpr int kSpanChunk = 4096;   // slots scanned per CTA by the span kernel (256 x 16)
 constexpr int kMaxSplitCtas = 2048;
+constexpr int kMaxCombineSplits = 256;   // splits per row the combine kernel holds weights for
+constexpr int kMinSplitTiles = 4;        // fewest tiles worth a split of its own
 constexpr float kLog2e = 1.4426950408889634f;
 
 enum { kSiteDecFull = 40, kSiteDecEmpty = 41, kSiteDecIssued = 42 };
@@ -151,15 +154,31 @@ __global__ void __launch_bounds__(256) kv_span_kernel(
   for (int i = 0; i < 8; ++i) qmin = min(qmin, red[i]);
   __syncthreads();
   const long long thr = static_cast<long long>(qmin) - window;
+  // Each thread owns 16 consecutive slots of the chunk and loads them at once
+  // (four 16-byte loads when the row is 16-byte aligned), so the scan costs
+  // one memory round trip.
   const int s_end = min(end + T, (c + 1) * kSpanChunk);
-  int best = INT_MAX;
-  for (int s = c * kSpanChunk + threadIdx.x; s < s_end; s += blockDim.x) {
-    const int p = posc[static_cast<size_t>(b) * S + s];
-    if (p >= 0 && static_cast<long long>(p) > thr) {
-      best = s;
-      break;
+  const int s0 = c * kSpanChunk + threadIdx.x * 16;
+  const int32_t* row = posc + static_cast<size_t>(b) * S;
+  int v[16];
+  if ((reinterpret_cast<uintptr_t>(row + s0) & 15u) == 0 && s0 + 16 <= s_end) {
+    const int4* q = reinterpret_cast<const int4*>(row + s0);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int4 x = __ldg(q + i);
+      v[4 * i] = x.x;
+      v[4 * i + 1] = x.y;
+      v[4 * i + 2] = x.z;
+      v[4 * i + 3] = x.w;
     }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = s0 + i < s_end ? __ldg(row + s0 + i) : -1;
   }
+  int best = INT_MAX;
+#pragma unroll
+  for (int i = 15; i >= 0; --i)
+    if (v[i] >= 0 && static_cast<long long>(v[i]) > thr) best = s0 + i;
   best = warp_min_i(best);
   if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = best;
   __syncthreads();
@@ -287,14 +306,20 @@ __global__ void __launch_bounds__(kDecThreads, 2)
   }
   // Query rows in shared memory as fp32, pre-multiplied by log2(e) so the
   // softmax runs on exp2.
-  for (int i = tid; i < RB * DH; i += kDecThreads) {
-    const int r = i / DH, c = i % DH;
-    float v = 0.f;
+  for (int i = tid; i < RB * DH / 8; i += kDecThreads) {
+    const int r = (i * 8) / DH, c = (i * 8) % DH;
+    float f[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) f[e] = 0.f;
     if (r < R) {
       const int t = t0 + r / G, h = j * G + r % G;
-      v = __half2float(p.Q[((static_cast<size_t>(b) * p.T + t) * p.H + h) * DH + c]) * kLog2e;
+      unpack8(__ldg(reinterpret_cast<const uint4*>(
+                  p.Q + ((static_cast<size_t>(b) * p.T + t) * p.H + h) * DH + c)),
+              f);
     }
-    qs[i] = v;
+    float4* dst = reinterpret_cast<float4*>(qs + r * DH + c);
+    dst[0] = make_float4(f[0] * kLog2e, f[1] * kLog2e, f[2] * kLog2e, f[3] * kLog2e);
+    dst[1] = make_float4(f[4] * kLog2e, f[5] * kLog2e, f[6] * kLog2e, f[7] * kLog2e);
   }
   __syncthreads();
   const int s_lo = rng[0], s_hi = rng[1];
@@ -501,48 +526,38 @@ __global__ void __launch_bounds__(kDecThreads, 2)
 
 // ---------------------------------------------------------------- combine
 // One warp per (b, t, h) row: O = sum_i 2^(m_i - M) o_i / sum_i 2^(m_i - M) l_i.
+// One CTA of DH threads per (b, t, h) row; thread c owns channel c.
 template <int DH>
-__global__ void __launch_bounds__(256) decode_combine_kernel(const float* __restrict__ part,
-                                                             void* O, int o_f16, int rows,
-                                                             int nsplit) {
-  constexpr int REC = DH + 4, VPL = DH / 32;
-  const int row = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
-  if (row >= rows) return;
-  const float* base = part + static_cast<size_t>(row) * nsplit * REC;
+__global__ void __launch_bounds__(DH) decode_combine_kernel(const float* __restrict__ part,
+                                                            void* O, int o_f16, int nsplit) {
+  constexpr int REC = DH + 4, NW = DH / 32;
+  __shared__ float fw[NW][kMaxCombineSplits];
+  const int wid = threadIdx.x >> 5, lane = threadIdx.x & 31, c = threadIdx.x;
+  const size_t row = blockIdx.x;
+  const float* base = part + row * nsplit * REC;
+  // weights 2^(m_i - M) and their l-weighted total, lanes over splits (each
+  // warp computes its own copy; the records are L2-resident)
   float M = -INFINITY;
   for (int i = lane; i < nsplit; i += 32) M = fmaxf(M, base[static_cast<size_t>(i) * REC]);
   M = warp_max(M);
-  float acc[VPL];
-#pragma unroll
-  for (int k = 0; k < VPL; ++k) acc[k] = 0.f;
   float L = 0.f;
-  if (M != -INFINITY) {
-    for (int i = 0; i < nsplit; ++i) {
-      const float* rec = base + static_cast<size_t>(i) * REC;
-      const float f = ex2_approx(rec[0] - M);
-      L += f * rec[1];
-      const float4* src = reinterpret_cast<const float4*>(rec + 4 + lane * VPL);
-#pragma unroll
-      for (int k = 0; k < VPL / 4; ++k) {
-        const float4 v = src[k];
-        acc[4 * k] = fmaf(f, v.x, acc[4 * k]);
-        acc[4 * k + 1] = fmaf(f, v.y, acc[4 * k + 1]);
-        acc[4 * k + 2] = fmaf(f, v.z, acc[4 * k + 2]);
-        acc[4 * k + 3] = fmaf(f, v.w, acc[4 * k + 3]);
-      }
-    }
+  for (int i = lane; i < nsplit; i += 32) {
+    const float* rec = base + static_cast<size_t>(i) * REC;
+    const float f = M == -INFINITY ? 0.f : ex2_approx(rec[0] - M);
+    fw[wid][i] = f;
+    L += f * rec[1];
   }
-  const float inv = L > 0.f ? 1.f / L : 0.f;
-  uint32_t packed[VPL / 2];
-#pragma unroll
-  for (int k = 0; k < VPL / 2; ++k)
-    packed[k] = o_f16 ? pack_half2(acc[2 * k] * inv, acc[2 * k + 1] * inv)
-                      : pack_bf162(acc[2 * k] * inv, acc[2 * k + 1] * inv);
-  uint16_t* dst = static_cast<uint16_t*>(O) + static_cast<size_t>(row) * DH + lane * VPL;
-  if constexpr (VPL == 8)
-    *reinterpret_cast<uint4*>(dst) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+  L = warp_sum(L);
+  __syncwarp();
+  float acc = 0.f;
+#pragma unroll 8
+  for (int i = 0; i < nsplit; ++i)
+    acc = fmaf(fw[wid][i], __ldg(base + static_cast<size_t>(i) * REC + 4 + c), acc);
+  const float v = L > 0.f ? acc / L : 0.f;
+  if (o_f16)
+    static_cast<__half*>(O)[row * DH + c] = __float2half_rn(v);
   else
-    *reinterpret_cast<uint2*>(dst) = make_uint2(packed[0], packed[1]);
+    static_cast<__nv_bfloat16*>(O)[row * DH + c] = __float2bfloat16_rn(v);
 }
 
 // ---------------------------------------------------------------- planning
@@ -564,7 +579,8 @@ DecPlan plan_rows(int B, int T, int H, int H_kv) {
 }
 
 int max_splits(const DecPlan& d) {
-  const int m = kMaxSplitCtas / d.units;
+  int m = kMaxSplitCtas / d.units;
+  if (m > kMaxCombineSplits) m = kMaxCombineSplits;
   return m < 1 ? 1 : m;
 }
 
@@ -624,11 +640,15 @@ cudaError_t launch_cached_attention(const void* Q, const void* K_cache, const vo
       static_cast<uint8_t*>(ws) +
       (static_cast<size_t>(B) * nchunk_max * 4 + 255) / 256 * 256);
 
-  // Splits: enough CTAs for two per SM, at least one tile each, within the
-  // workspace bound.
+  // Splits: enough CTAs for two per SM, but at least kMinSplitTiles tiles
+  // each over the span the rows are expected to see (a local layer's window
+  // plus the new tokens; empty slots or position gaps only make the real span
+  // longer, which costs time, never correctness), within the workspace bound.
   int nsplit = (2 * num_sms()) / d.units;
-  const int tiles = (hi + kSlots - 1) / kSlots;
-  if (nsplit > tiles) nsplit = tiles;
+  const long long est = window > 0 ? std::min<long long>(hi, static_cast<long long>(window) + T)
+                                   : static_cast<long long>(hi);
+  const long long by_span = (est + kMinSplitTiles * kSlots - 1) / (kMinSplitTiles * kSlots);
+  if (nsplit > by_span) nsplit = static_cast<int>(by_span);
   if (nsplit > max_splits(d)) nsplit = max_splits(d);
   if (nsplit < 1) nsplit = 1;
 
@@ -685,9 +705,9 @@ cudaError_t launch_cached_attention(const void* Q, const void* K_cache, const vo
   if (e != cudaSuccess || nsplit == 1) return e;
   const int rows = B * T * H;
   if (d_h == 256)
-    decode_combine_kernel<256><<<(rows + 7) / 8, 256, 0, stream>>>(part, O, p.o_f16, rows, nsplit);
+    decode_combine_kernel<256><<<rows, 256, 0, stream>>>(part, O, p.o_f16, nsplit);
   else
-    decode_combine_kernel<128><<<(rows + 7) / 8, 256, 0, stream>>>(part, O, p.o_f16, rows, nsplit);
+    decode_combine_kernel<128><<<rows, 128, 0, stream>>>(part, O, p.o_f16, nsplit);
   return cudaGetLastError();
 }
 

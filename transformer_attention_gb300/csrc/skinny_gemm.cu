@@ -6,7 +6,7 @@
 // bound by reading W once from HBM, and a 128-row tensor-core tile would be
 // almost all padding.  The kernel runs on the CUDA cores: each warp owns two
 // output columns (two rows of W), its lanes stride K in 16-byte chunks with
-// four chunks of both rows in flight, A (a few KB) is read through L1, the
+// eight chunks of both rows in flight, A (a few KB) is read through L1, the
 // sums are fp32, and a warp reduction finishes each output.
 #include "internal.h"
 #include "ptx.cuh"
@@ -17,7 +17,7 @@ namespace {
 
 constexpr int kWarps = 4;     // warps per CTA
 constexpr int kRows = 2;      // rows of W per warp
-constexpr int kUnroll = 4;    // 256-element K chunks in flight per row
+constexpr int kUnroll = 8;    // 256-element K chunks in flight per row
 
 __device__ __forceinline__ uint4 ld_stream(const void* p) {
   uint4 v;
