@@ -300,6 +300,22 @@ int gemma3_linear(const void* A, long lda, const void* W, long ldw, void* C, lon
 int gemma3_geglu(const void* A, long lda, const void* W_gating, long ldw, void* Z, long ldz,
                  int M, int D_ff, int K, int in_dtype, void* stream);
 
+/* C[M, N] fp16 = A W^T with the attention prologue fused into the GEMM
+ * epilogue (what gemma3_linear followed by gemma3_qk_norm_rope computes, but
+ * from the fp32 accumulator, without the fp16 round trip): columns [0,
+ * n_norm) are head vectors of d_h that get RMSNorm with (1 + gamma) ([QK] How
+ * it works), RoPE at pos[row] with (rope_base, rope_scale) and the factor
+ * `scale` ([AB] QK-norm, then RoPE, then scale); columns from n_norm on are
+ * the plain product (the V half of the KV projection).  gamma bf16 [d_h];
+ * pos int32 [M].  Requires M > 16, d_h in {128, 256} and n_norm a multiple of
+ * 256 with n_norm <= N (else GEMMA3_ERR_UNSUPPORTED); other rules as
+ * gemma3_linear.  The layer entry points use it for Q (gamma_q, scale =
+ * query_scale, n_norm = N) and for KV (gamma_k, scale 1, n_norm = H_kv*d_h). */
+int gemma3_linear_qk_norm_rope(const void* A, long lda, const void* W, long ldw, void* C,
+                               long ldc, int M, int N, int K, int in_dtype, const void* gamma,
+                               const int32_t* pos, int d_h, int n_norm, double rope_base,
+                               double rope_scale, float scale, void* stream);
+
 /* dst[i] = src[i] for i < n, bf16 -> fp16 with round-to-nearest-even
  * (n % 8 == 0; both 16-byte aligned). */
 int gemma3_cast_bf16_f16(const void* src, void* dst, size_t n, void* stream);

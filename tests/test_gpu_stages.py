@@ -103,6 +103,59 @@ def test_qk_norm_rope_matches_oracle(d_h, H, H_kv, base, scale, alpha):
     assert torch.equal(KVo[:, H_kv * d_h:], KVr[:, H_kv * d_h:])
 
 
+# ---------------------------------------------------------------- fused projection + prologue
+@pytest.mark.parametrize("M,D,d_h,H,H_kv,base,scale,alpha,inp", [
+    (300, 1152, 256, 4, 1, 1e6, 1.0, 256 ** -0.5, "bf16"),
+    (1000, 512, 256, 8, 4, 1e4, 1.0, 256 ** -0.5, "f16"),
+    (257, 384, 128, 4, 2, 1e6, 8.0, 168 ** -0.5, "bf16"),
+    (129, 256, 128, 32, 16, 1e6, 8.0, 168 ** -0.5, "bf16"),
+    (17, 192, 128, 2, 2, 1e4, 1.0, 128 ** -0.5, "f16"),
+])
+def test_linear_qk_norm_rope_matches_oracle(M, D, d_h, H, H_kv, base, scale, alpha, inp):
+    """The Q and KV projections with QK-norm, RoPE and the query scale in the
+    GEMM epilogue against the oracle's normalised and rotated Q/K (before
+    the query scale) and its plain V projection."""
+    import transformer_attention_gb300 as G3
+    it = {"bf16": torch.bfloat16, "f16": torch.float16}[inp]
+    code = {"bf16": G3.GEMMA3_BF16, "f16": G3.GEMMA3_F16}[inp]
+    HD, KVD = H * d_h, H_kv * d_h
+    x = _randn((M, D), 20, 1.0, it)
+    Wq = _randn((HD, D), 21, D ** -0.5, it)
+    Wkv = _randn((2, KVD, D), 22, D ** -0.5, it)
+    gq = _randn((d_h,), 23, 0.1 ** 0.5)
+    gk = _randn((d_h,), 24, 0.1 ** 0.5)
+    g = torch.Generator().manual_seed(25)
+    pos = torch.randint(0, 131072, (M,), generator=g).to(torch.int32)
+    pos[:3] = torch.tensor([0, 1, 131071], dtype=torch.int32)
+    Qd = torch.empty((M, HD), dtype=torch.float16, device="cuda")
+    KVd = torch.empty((M, 2 * KVD), dtype=torch.float16, device="cuda")
+    xd, posd = x.cuda(), pos.cuda()
+    G3.gemma3_linear_qk_norm_rope(xd, D, Wq.cuda(), D, Qd, HD, M, HD, D, code, gq.cuda(), posd,
+                                  d_h, HD, base, scale, alpha)
+    G3.gemma3_linear_qk_norm_rope(xd, D, Wkv.reshape(2 * KVD, D).cuda(), D, KVd, 2 * KVD, M,
+                                  2 * KVD, D, code, gk.cuda(), posd, d_h, KVD, base, scale, 1.0)
+    assert G3.gemma3_attn_check_status() == 0
+    q_ref, k_ref = O.normalised_rotated_qk(x, pos, Wq, Wkv, gq, gk, H=H, H_kv=H_kv, d_h=d_h,
+                                           rope_base=base, rope_scale=scale)
+    q_got = Qd.cpu().reshape(M, H, d_h).to(F64) / alpha
+    kv = KVd.cpu()
+    assert max_abs(q_got, q_ref) <= QK_MAX_ABS
+    assert max_abs(kv[:, :KVD].reshape(M, H_kv, d_h), k_ref) <= QK_MAX_ABS
+    assert rel_frob(kv[:, KVD:], O.project(x, Wkv[1])) <= 1e-3
+
+
+def test_linear_qk_norm_rope_rejects_unaligned_heads():
+    import transformer_attention_gb300 as G3
+    x = torch.zeros((64, 64), dtype=torch.bfloat16, device="cuda")
+    W = torch.zeros((384, 64), dtype=torch.bfloat16, device="cuda")
+    C = torch.empty((64, 384), dtype=torch.float16, device="cuda")
+    g = torch.zeros(128, dtype=torch.bfloat16, device="cuda")
+    pos = torch.zeros(64, dtype=torch.int32, device="cuda")
+    with pytest.raises(G3.Gemma3Error):   # n_norm = 128 is not a whole 256-wide tile
+        G3.gemma3_linear_qk_norm_rope(x, 64, W, 64, C, 384, 64, 384, 64, G3.GEMMA3_BF16, g, pos,
+                                      128, 128, 1e4, 1.0, 1.0)
+
+
 # ---------------------------------------------------------------- flash attention
 ATTN_CASES = [
     # B, T, H, H_kv, d_h, window, pads

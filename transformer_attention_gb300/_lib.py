@@ -83,6 +83,9 @@ SIGNATURES = {
                              c_int, c_int, c_void_p]),
     "gemma3_linear": (c_int, [c_void_p, c_long, c_void_p, c_long, c_void_p, c_long, c_int, c_int,
                               c_int, c_int, c_int, c_int, c_void_p]),
+    "gemma3_linear_qk_norm_rope": (c_int, [c_void_p, c_long, c_void_p, c_long, c_void_p, c_long,
+                                           c_int, c_int, c_int, c_int, c_void_p, c_void_p, c_int,
+                                           c_int, c_double, c_double, c_float, c_void_p]),
     "gemma3_cast_bf16_f16": (c_int, [c_void_p, c_void_p, c_size_t, c_void_p]),
     "gemma3_qk_norm_rope": (c_int, [c_void_p, c_long, c_void_p, c_long, c_void_p, c_void_p,
                                     c_void_p, c_int, c_int, c_int, c_int, c_double, c_double,
@@ -318,6 +321,13 @@ def gemma3_linear(A, lda, W, ldw, C, ldc, M, N, K, in_dtype, out_dtype, max_ctas
     return _check("gemma3_linear", lib().gemma3_linear(
         _ptr(A), lda, _ptr(W), ldw, _ptr(C), ldc, M, N, K, in_dtype, out_dtype, max_ctas,
         _stream(stream)))
+
+
+def gemma3_linear_qk_norm_rope(A, lda, W, ldw, C, ldc, M, N, K, in_dtype, gamma, pos, d_h, n_norm,
+                               rope_base, rope_scale, scale, stream=None):
+    return _check("gemma3_linear_qk_norm_rope", lib().gemma3_linear_qk_norm_rope(
+        _ptr(A), lda, _ptr(W), ldw, _ptr(C), ldc, M, N, K, in_dtype, _ptr(gamma), _ptr(pos), d_h,
+        n_norm, rope_base, rope_scale, scale, _stream(stream)))
 
 
 def gemma3_cast_bf16_f16(src, dst, n, stream=None):

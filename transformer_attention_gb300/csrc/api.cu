@@ -83,6 +83,31 @@ AttnWs attn_ws(const gemma3_attn_dims* d, bool f16_weights = false) {
   return w;
 }
 
+// Q' and [K'|V] of M token rows: the Q / KV projections with QK-norm, RoPE
+// and the query scale fused into the GEMM epilogue when the head vectors
+// tile the 256-wide output tiles (every Gemma 3 shape with more than 16
+// rows), else the projections followed by the prologue kernel.
+cudaError_t project_qk(const void* x, long ldx, int act_dtype, const void* Wq, const void* Wkv,
+                       void* qbuf, void* kvbuf, const void* gamma_q, const void* gamma_k,
+                       const int32_t* pos, int M, int D, int H, int H_kv, int d_h,
+                       double rope_base, double rope_scale, float query_scale, cudaStream_t s,
+                       int* st) {
+  const int HD = H * d_h, KVD = H_kv * d_h;
+  if (linear_qknorm_fusable(M, HD, HD, d_h) && linear_qknorm_fusable(M, 2 * KVD, KVD, d_h)) {
+    cudaError_t e = launch_linear_qknorm(x, ldx, Wq, D, qbuf, HD, M, HD, D, act_dtype, gamma_q, pos,
+                                         d_h, HD, rope_base, rope_scale, query_scale, s, st);
+    if (e != cudaSuccess) return e;
+    return launch_linear_qknorm(x, ldx, Wkv, D, kvbuf, 2 * KVD, M, 2 * KVD, D, act_dtype, gamma_k,
+                                pos, d_h, KVD, rope_base, rope_scale, 1.f, s, st);
+  }
+  cudaError_t e = launch_linear(x, ldx, Wq, D, qbuf, HD, M, HD, D, act_dtype, kF16, s, st, 0);
+  if (e != cudaSuccess) return e;
+  e = launch_linear(x, ldx, Wkv, D, kvbuf, 2 * KVD, M, 2 * KVD, D, act_dtype, kF16, s, st, 0);
+  if (e != cudaSuccess) return e;
+  return launch_qk_norm_rope(qbuf, HD, kvbuf, 2 * KVD, gamma_q, gamma_k, pos, M, H, H_kv, d_h,
+                             rope_base, rope_scale, query_scale, s);
+}
+
 // The layer pipeline shared by the single-layer and block entry points.
 // act_dtype kBF16: x and the weights are used as given (bf16) and O is bf16.
 // act_dtype kF16: x is fp16, the weights are first cast to fp16 copies in the
@@ -115,13 +140,8 @@ int attn_pipeline(const gemma3_attn_dims* d, const void* x, int act_dtype,
     Wkv = wkv;
     Wo = wo;
   }
-  e = launch_linear(x, d->D, Wq, d->D, qbuf, HD, M, HD, d->D, act_dtype, kF16, s, st, 0);
-  if (e != cudaSuccess) return GEMMA3_ERR_CUDA;
-  e = launch_linear(x, d->D, Wkv, d->D, kvbuf, 2 * KVD, M, 2 * KVD, d->D, act_dtype, kF16, s, st,
-                    0);
-  if (e != cudaSuccess) return GEMMA3_ERR_CUDA;
-  e = launch_qk_norm_rope(qbuf, HD, kvbuf, 2 * KVD, gamma_q, gamma_k, segment_pos, M, d->H,
-                          d->H_kv, d->d_h, rope_base, rope_scale, query_scale, s);
+  e = project_qk(x, d->D, act_dtype, Wq, Wkv, qbuf, kvbuf, gamma_q, gamma_k, segment_pos, M,
+                 d->D, d->H, d->H_kv, d->d_h, rope_base, rope_scale, query_scale, s, st);
   if (e != cudaSuccess) return GEMMA3_ERR_CUDA;
   const int win = attn_type == GEMMA3_LOCAL_SLIDING ? window : 0;
   e = launch_flash_attention(qbuf, kvbuf, static_cast<uint8_t*>(kvbuf) + KVD * 2, 2 * KVD, qbuf,
@@ -504,12 +524,9 @@ int gemma3_attn_forward_cached(const gemma3_attn_dims* dims, int S, int end_inde
   uint8_t* kvbuf = ws + w.q;          // [K'|V] fp16  [M, 2*KVD]
   uint8_t* aws = kvbuf + w.kv;        // attention partials
   cudaStream_t s = as_stream(stream);
-  if (launch_linear(x, d->D, Wq, d->D, qbuf, HD, M, HD, d->D, kBF16, kF16, s, st, 0) !=
+  if (project_qk(x, d->D, kBF16, Wq, Wkv, qbuf, kvbuf, gamma_q, gamma_k, segment_pos, M, d->D,
+                 d->H, d->H_kv, d->d_h, rope_base, rope_scale, query_scale, s, st) !=
           cudaSuccess ||
-      launch_linear(x, d->D, Wkv, d->D, kvbuf, 2 * KVD, M, 2 * KVD, d->D, kBF16, kF16, s, st, 0) !=
-          cudaSuccess ||
-      launch_qk_norm_rope(qbuf, HD, kvbuf, 2 * KVD, gamma_q, gamma_k, segment_pos, M, d->H,
-                          d->H_kv, d->d_h, rope_base, rope_scale, query_scale, s) != cudaSuccess ||
       launch_kv_cache_append(kvbuf, kvbuf + KVD * 2, 2 * KVD, segment_pos, pad_lens, d->B, d->T, S,
                              end_index, KVD, K_cache, V_cache, pos_cache, s) != cudaSuccess)
     return GEMMA3_ERR_CUDA;
@@ -613,6 +630,28 @@ int gemma3_linear(const void* A, long lda, const void* W, long ldw, void* C, lon
   const int dt = out_dtype == GEMMA3_F32 ? kF32 : (out_dtype == GEMMA3_F16 ? kF16 : kBF16);
   return to_status(launch_linear(A, lda, W, ldw, C, ldc, M, N, K, it, dt, as_stream(stream), st,
                                  max_ctas));
+}
+
+int gemma3_linear_qk_norm_rope(const void* A, long lda, const void* W, long ldw, void* C,
+                               long ldc, int M, int N, int K, int in_dtype, const void* gamma,
+                               const int32_t* pos, int d_h, int n_norm, double rope_base,
+                               double rope_scale, float scale, void* stream) {
+  if (!A || !W || !C || !gamma || !pos || M < 0 || N < 1 || K < 1) return GEMMA3_ERR_INVALID_ARG;
+  if (in_dtype != GEMMA3_BF16 && in_dtype != GEMMA3_F16) return GEMMA3_ERR_INVALID_ARG;
+  if (lda < K || ldw < K || ldc < N) return GEMMA3_ERR_INVALID_ARG;
+  if (!(rope_base > 0.0) || !(rope_scale > 0.0)) return GEMMA3_ERR_INVALID_ARG;
+  if (!aligned16(A) || !aligned16(W) || !aligned16(C) || !aligned16(gamma) || (lda * 2) % 16 ||
+      (ldw * 2) % 16 || (ldc * 2) % 16)
+    return GEMMA3_ERR_MISALIGNED;
+  if (M > 0 && !linear_qknorm_fusable(M, N, n_norm, d_h)) return GEMMA3_ERR_UNSUPPORTED;
+  int rc = check_device();
+  if (rc != GEMMA3_OK) return rc;
+  int* st = status_ptr();
+  if (st == nullptr) return GEMMA3_ERR_CUDA;
+  return to_status(launch_linear_qknorm(A, lda, W, ldw, C, ldc, M, N, K,
+                                        in_dtype == GEMMA3_F16 ? kF16 : kBF16, gamma, pos, d_h,
+                                        n_norm, rope_base, rope_scale, scale, as_stream(stream),
+                                        st));
 }
 
 int gemma3_cast_bf16_f16(const void* src, void* dst, size_t n, void* stream) {

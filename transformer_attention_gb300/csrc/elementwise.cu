@@ -10,13 +10,10 @@
 //     Q only: x <- x * query_scale
 //   One warp per token, d_h/8 lanes per head vector, 8 fp16 elements (one
 //   16-byte load) per lane; the RMS is a shuffle reduction over those lanes
-//   and the RoPE partner element sits d_h/16 lanes away.  The rotation angle
-//   is formed as an fp32 double-float (exact two-product of pos and the split
-//   frequency, split hi + lo on the host in double precision) and reduced
-//   modulo 2*pi by Cody-Waite with a two-part 2*pi, so positions up to 2^24
-//   keep ~1e-6 rad of angle error without any fp64 work on the device; sin
-//   and cos of the reduced angle come from the hardware approximation.  Rows
-//   are updated in place.
+//   and the RoPE partner element sits d_h/16 lanes away.  Angles: rope.cuh.
+//   Rows are updated in place.  (The layer pipelines fuse this step into the
+//   projection GEMM's epilogue; this kernel serves the cases that fusion does
+//   not cover and the stage entry point.)
 //
 // rmsnorm_rows / postnorm_residual: the D-axis norms of the block sandwich
 //   ("Full Gemma 3 Block", How it works: a = Attn(RMSNorm_pre(x));
@@ -25,22 +22,13 @@
 
 #include "internal.h"
 #include "ptx.cuh"
+#include "rope.cuh"
 
 namespace g3 {
 
 namespace {
 
-constexpr double kTwoPi = 6.283185307179586476925286766559;
-constexpr float kTwoPiHi = static_cast<float>(kTwoPi);
-constexpr float kTwoPiMid = static_cast<float>(kTwoPi - static_cast<double>(kTwoPiHi));
-constexpr float kInvTwoPi = static_cast<float>(1.0 / kTwoPi);
 constexpr float kEps = 1e-6f;
-
-// RoPE frequencies inv_scale * base^(-2c/d_h), c < d_h/2, each split into an
-// fp32 (hi, lo) pair on the host in double precision.
-struct RopeFreqs {
-  float2 f[128];
-};
 
 constexpr int kVecUnroll = 8;  // head vectors in flight per lane
 
@@ -79,19 +67,7 @@ __global__ void __launch_bounds__(256, 2)
     const float p = static_cast<float>(pos[m]);
     float cs[8], sn[8];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      const float2 f = freqs.f[c0 + e];
-      const float a_hi = p * f.x;
-      const float a_err = fmaf(p, f.x, -a_hi);     // exact residual of the product
-      const float a_lo = fmaf(p, f.y, a_err);
-      const float k = rintf(a_hi * kInvTwoPi);
-      float r = fmaf(-k, kTwoPiHi, a_hi);
-      r = fmaf(-k, kTwoPiMid, r);
-      r += a_lo;
-      // r is already reduced to about [-pi, pi], where the hardware
-      // approximation's absolute error (~2^-21) is far below fp16 rounding.
-      __sincosf(r, &sn[e], &cs[e]);
-    }
+    for (int e = 0; e < 8; ++e) rope_sincos(p, freqs.f[c0 + e], sn[e], cs[e]);
     for (int base = 0; base < nvec; base += VPW * kVecUnroll) {
       if (base > 0) {
 #pragma unroll
@@ -265,12 +241,7 @@ cudaError_t launch_qk_norm_rope(void* Q, long ldq, void* K, long ldk, const void
   long blocks = (M + warps_per_block - 1) / warps_per_block;
   const long cap = static_cast<long>(num_sms()) * 4;
   if (blocks > cap) blocks = cap;
-  RopeFreqs freqs;
-  for (int c = 0; c < d_h / 2; ++c) {
-    const double f = std::pow(rope_base, -2.0 * c / d_h) / rope_scale;
-    freqs.f[c].x = static_cast<float>(f);
-    freqs.f[c].y = static_cast<float>(f - static_cast<double>(freqs.f[c].x));
-  }
+  const RopeFreqs freqs = make_rope_freqs(d_h, rope_base, rope_scale);
   auto q = static_cast<__half*>(Q);
   auto k = static_cast<__half*>(K);
   auto gq = static_cast<const __nv_bfloat16*>(gamma_q);

@@ -21,11 +21,19 @@
 // Tiles are visited in groups of 8 M-tiles (N-tiles varying slowest within
 // a group), so the tiles in flight share A rows and W rows through L2 even
 // when W is larger than L2.
+// Epilogue modes: plain conversion; GeGLU (the feed-forward gating
+// projection); and the attention prologue ("QK-Norm", How it works; "Gemma 3
+// Attention Block", How it works: QK-norm, then RoPE, then scale) applied to
+// the Q or K head vectors straight from the fp32 accumulator: a 256-wide tile
+// holds one d_h = 256 head or two d_h = 128 heads of a row, so each thread
+// (one row) sums the squares of its head, then rotates the pairs (c, c +
+// d_h/2) with (1 + gamma) and the query scale folded in.
 // Every mbarrier wait is bounded (see ptx.cuh).
 #include <type_traits>
 
 #include "internal.h"
 #include "ptx.cuh"
+#include "rope.cuh"
 
 namespace g3 {
 
@@ -53,6 +61,19 @@ constexpr uint32_t TMEM_COLS = 512;
 
 enum : int { kSiteEmpty = 1, kSiteFull = 2, kSiteAccEmpty = 3, kSiteAccFull = 4 };
 
+enum : int { kEpiPlain = 0, kEpiGeglu = 1, kEpiQkNorm = 2 };
+
+// Arguments of the QK-norm + RoPE epilogue: columns [0, n_norm) of C are head
+// vectors (d_h each) to normalise with (1 + gamma), rotate at pos[row] and
+// multiply by scale; columns from n_norm on are converted as they are.
+struct QkEpi {
+  RopeFreqs freqs;
+  const __nv_bfloat16* gamma;
+  const int32_t* pos;
+  int n_norm;
+  float scale;
+};
+
 template <typename T>
 __device__ __forceinline__ uint32_t pack2(float a, float b);
 template <> __device__ __forceinline__ uint32_t pack2<__half>(float a, float b) {
@@ -73,10 +94,15 @@ __device__ __forceinline__ float gelu_tanh_mul(float g, float u) {
 // weight (rows [0, N) gate, [N, 2N) up); each 256-wide accumulator tile holds
 // 128 gate and the matching 128 up columns, and the epilogue writes
 // C[M, N] = GELU(A Wg^T) * (A Wu^T).
-template <int AB_BF16, typename OutT, bool GEGLU>
+// EPI = kEpiQkNorm (OutT = __half, DH = d_h): the attention prologue above.
+template <int AB_BF16, typename OutT, int EPI, int DH>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_tn_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const __grid_constant__ CUtensorMap tmC, int M, int N, int K, int* status) {
+                   const __grid_constant__ CUtensorMap tmC, int M, int N, int K, int* status,
+                   const __grid_constant__ QkEpi epi) {
+  constexpr bool GEGLU = EPI == kEpiGeglu;
+  static_assert(EPI != kEpiQkNorm || (std::is_same<OutT, __half>::value && (DH == 128 || DH == 256)),
+                "the QK-norm epilogue writes fp16 head vectors of 128 or 256");
   constexpr int BN_OUT = GEGLU ? BN / 2 : BN;   // output columns per tile
   constexpr int CW = 128 / static_cast<int>(sizeof(OutT));   // output columns per 128 B chunk
   // A kernel launched after an earlier one gave up does no work.
@@ -208,7 +234,124 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (!ok) break;
       tc_fence_after();
       const uint32_t acc = tbase + lane_off + abuf * BN;
-      for (int c = 0; c < BN_OUT / CW; ++c, ++nchunk) {
+      // Stage one 32-row x 128-byte chunk of this warp and store it with TMA.
+      auto stage_store = [&](const uint32_t (&w)[32], int col0) {
+        // The staging buffer used two chunks ago must have been read by its store.
+        uint8_t* buf = staging + (nchunk & 1) * STAGING_BYTES;
+        if (lane == 0 && nchunk >= 2) bulk_wait_group_read<1>();
+        __syncwarp();
+        // row `lane`, 16-byte unit u lands at unit u ^ (lane % 8) (128-byte swizzle)
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          *reinterpret_cast<uint4*>(buf + lane * 128 + ((u ^ (lane & 7)) << 4)) =
+              make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_2d(&tmC, smem_u32(buf), col0, m0 + q * 32);
+          bulk_commit_group();
+        }
+        ++nchunk;
+      };
+      auto release_acc = [&]() {
+        // last TMEM read of this tile: the accumulator may be reused
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&acce_bar[abuf]));
+      };
+      bool fused = false;
+      if constexpr (EPI == kEpiQkNorm) fused = n0 < epi.n_norm;   // warp-uniform
+      if constexpr (EPI == kEpiQkNorm) {
+        if (fused) {
+          constexpr int HALF = DH / 2;
+          constexpr int HEADS = BN / DH;      // head vectors per tile row
+          constexpr int PAIRS = HALF / 64;    // 64-column chunk pairs per head
+          const int row = m0 + q * 32 + lane;
+          const float p = row < M ? static_cast<float>(__ldg(epi.pos + row)) : 0.f;
+          float rs[HEADS];
+#pragma unroll
+          for (int e = 0; e < HEADS; ++e) {
+            float ss = 0.f;
+#pragma unroll
+            for (int k = 0; k < DH / 64; ++k) {
+              uint32_t a0[32], a1[32];
+              tmem_ld32(acc + e * DH + k * 64, a0);
+              tmem_ld32(acc + e * DH + k * 64 + 32, a1);
+              tmem_ld_wait(a0);
+              tmem_ld_wait(a1);
+#pragma unroll
+              for (int t = 0; t < 32; ++t) {
+                ss = fmaf(__uint_as_float(a0[t]), __uint_as_float(a0[t]), ss);
+                ss = fmaf(__uint_as_float(a1[t]), __uint_as_float(a1[t]), ss);
+              }
+            }
+            rs[e] = rsqrtf(ss * (1.f / DH) + 1e-6f);
+          }
+          // Each pair of 64-column chunks (first half, partner half) goes to
+          // the two staging buffers: the first-half chunk to buffer 0, the
+          // partner chunk to buffer 1 (nchunk is even here).
+          uint8_t* buf_a = staging;
+          uint8_t* buf_b = staging + STAGING_BYTES;
+#pragma unroll
+          for (int e = 0; e < HEADS; ++e) {
+#pragma unroll
+            for (int i = 0; i < PAIRS; ++i) {
+              const int ca = e * (DH / 64) + i, cb = ca + PAIRS;   // first-half, partner chunk
+#pragma unroll
+              for (int h = 0; h < 2; ++h) {
+                uint32_t x1[32], x2[32];
+                tmem_ld32(acc + ca * 64 + h * 32, x1);
+                tmem_ld32(acc + cb * 64 + h * 32, x2);
+                tmem_ld_wait(x1);
+                tmem_ld_wait(x2);
+                if (e == HEADS - 1 && i == PAIRS - 1 && h == 1) release_acc();
+                uint32_t wa[16], wb[16];
+#pragma unroll
+                for (int t = 0; t < 32; t += 2) {
+                  float o1[2], o2[2];
+#pragma unroll
+                  for (int v = 0; v < 2; ++v) {
+                    const int j = i * 64 + h * 32 + t + v;   // pair index within the head
+                    float sn, cs;
+                    rope_sincos(p, epi.freqs.f[j], sn, cs);
+                    const float g1 = 1.f + __bfloat162float(epi.gamma[j]);
+                    const float g2 = 1.f + __bfloat162float(epi.gamma[j + HALF]);
+                    const float y1 = __uint_as_float(x1[t + v]) * rs[e] * g1;
+                    const float y2 = __uint_as_float(x2[t + v]) * rs[e] * g2;
+                    o1[v] = (y1 * cs - y2 * sn) * epi.scale;
+                    o2[v] = (y2 * cs + y1 * sn) * epi.scale;
+                  }
+                  wa[t / 2] = pack_half2(o1[0], o1[1]);
+                  wb[t / 2] = pack_half2(o2[0], o2[1]);
+                }
+                if (h == 0) {
+                  // both buffers must have been read by the earlier stores
+                  if (lane == 0 && nchunk > 0) bulk_wait_group_read<0>();
+                  __syncwarp();
+                }
+                // row `lane`, 16-byte unit u at unit u ^ (lane % 8) (128-byte swizzle)
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                  const int pu = ((4 * h + u) ^ (lane & 7)) << 4;
+                  *reinterpret_cast<uint4*>(buf_a + lane * 128 + pu) =
+                      make_uint4(wa[4 * u], wa[4 * u + 1], wa[4 * u + 2], wa[4 * u + 3]);
+                  *reinterpret_cast<uint4*>(buf_b + lane * 128 + pu) =
+                      make_uint4(wb[4 * u], wb[4 * u + 1], wb[4 * u + 2], wb[4 * u + 3]);
+                }
+              }
+              fence_proxy_async_smem();
+              __syncwarp();
+              if (lane == 0) {
+                tma_store_2d(&tmC, smem_u32(buf_a), n0 + ca * 64, m0 + q * 32);
+                tma_store_2d(&tmC, smem_u32(buf_b), n0 + cb * 64, m0 + q * 32);
+                bulk_commit_group();
+              }
+              nchunk += 2;
+            }
+          }
+        }
+      }
+      for (int c = 0; !fused && c < BN_OUT / CW; ++c) {
         const int col0 = n0 + c * CW;
         if (col0 >= N) break;   // warp-uniform
         // 128 bytes of this thread's row: 8 x 16-byte units
@@ -248,27 +391,8 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
           }
         }
-        if (c == BN_OUT / CW - 1 || col0 + CW >= N) {
-          // last TMEM read of this tile: the accumulator may be reused
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(smem_u32(&acce_bar[abuf]));
-        }
-        // The staging buffer used two chunks ago must have been read by its store.
-        uint8_t* buf = staging + (nchunk & 1) * STAGING_BYTES;
-        if (lane == 0 && nchunk >= 2) bulk_wait_group_read<1>();
-        __syncwarp();
-        // row `lane`, 16-byte unit u lands at unit u ^ (lane % 8) (128-byte swizzle)
-#pragma unroll
-        for (int u = 0; u < 8; ++u)
-          *reinterpret_cast<uint4*>(buf + lane * 128 + ((u ^ (lane & 7)) << 4)) =
-              make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          tma_store_2d(&tmC, smem_u32(buf), col0, m0 + q * 32);
-          bulk_commit_group();
-        }
+        if (c == BN_OUT / CW - 1 || col0 + CW >= N) release_acc();
+        stage_store(w, col0);
       }
       abuf ^= 1;
       if (abuf == 0) aphase ^= 1;
@@ -282,10 +406,12 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
 }
 
-template <int AB_BF16, typename OutT, bool GEGLU = false>
+template <int AB_BF16, typename OutT, int EPI = kEpiPlain, int DH = 0>
 cudaError_t launch_typed(const CUtensorMap& ta, const CUtensorMap& tb, void* C, long ldc, int M,
-                         int N, int K, cudaStream_t stream, int* status, int max_ctas) {
-  auto kern = gemm_tn_kernel<AB_BF16, OutT, GEGLU>;
+                         int N, int K, cudaStream_t stream, int* status, int max_ctas,
+                         const QkEpi& epi = QkEpi{}) {
+  constexpr bool GEGLU = EPI == kEpiGeglu;
+  auto kern = gemm_tn_kernel<AB_BF16, OutT, EPI, DH>;
   // Output tile map: boxes of 32 rows x 128 bytes, 128-byte swizzle.
   CUtensorMap tc;
   const CUtensorMapDataType cdt = sizeof(OutT) == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
@@ -308,8 +434,22 @@ cudaError_t launch_typed(const CUtensorMap& ta, const CUtensorMap& tb, void* C, 
   int grid = num_sms();
   if (max_ctas > 0 && max_ctas < grid) grid = max_ctas;
   if (tiles < grid) grid = tiles;
-  kern<<<grid, THREADS, SMEM_BYTES, stream>>>(ta, tb, tc, M, N, K, status);
+  kern<<<grid, THREADS, SMEM_BYTES, stream>>>(ta, tb, tc, M, N, K, status, epi);
   return cudaGetLastError();
+}
+
+bool encode_ab(CUtensorMap& ta, CUtensorMap& tb, const void* A, long lda, const void* W, long ldw,
+               int M, int N_rows, int K, int in_dtype, uint32_t b_box_rows) {
+  const CUtensorMapDataType tdt =
+      in_dtype == kBF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  const uint64_t adims[2] = {static_cast<uint64_t>(K), static_cast<uint64_t>(M)};
+  const uint64_t astr[1] = {static_cast<uint64_t>(lda) * 2};
+  const uint32_t abox[2] = {BK, BM};
+  const uint64_t bdims[2] = {static_cast<uint64_t>(K), static_cast<uint64_t>(N_rows)};
+  const uint64_t bstr[1] = {static_cast<uint64_t>(ldw) * 2};
+  const uint32_t bbox[2] = {BK, b_box_rows};
+  return encode_tiled(&ta, tdt, 2, A, adims, astr, abox) &&
+         encode_tiled(&tb, tdt, 2, W, bdims, bstr, bbox);
 }
 
 }  // namespace
@@ -321,18 +461,8 @@ cudaError_t launch_linear(const void* A, long lda, const void* W, long ldw, void
   if (in_dtype != kBF16 && in_dtype != kF16) return cudaErrorInvalidValue;
   if (M <= kSkinnyMaxRows)
     return launch_linear_skinny(A, lda, W, ldw, C, ldc, M, N, K, in_dtype, out_dtype, stream);
-  const CUtensorMapDataType tdt =
-      in_dtype == kBF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   CUtensorMap ta, tb;
-  const uint64_t adims[2] = {static_cast<uint64_t>(K), static_cast<uint64_t>(M)};
-  const uint64_t astr[1] = {static_cast<uint64_t>(lda) * 2};
-  const uint32_t abox[2] = {BK, BM};
-  const uint64_t bdims[2] = {static_cast<uint64_t>(K), static_cast<uint64_t>(N)};
-  const uint64_t bstr[1] = {static_cast<uint64_t>(ldw) * 2};
-  const uint32_t bbox[2] = {BK, BN};
-  if (!encode_tiled(&ta, tdt, 2, A, adims, astr, abox) ||
-      !encode_tiled(&tb, tdt, 2, W, bdims, bstr, bbox))
-    return cudaErrorInvalidValue;
+  if (!encode_ab(ta, tb, A, lda, W, ldw, M, N, K, in_dtype, BN)) return cudaErrorInvalidValue;
 #define G3_GEMM_OUT(AB)                                                                         \
   switch (out_dtype) {                                                                          \
     case kF32: return launch_typed<AB, float>(ta, tb, C, ldc, M, N, K, stream, status, max_ctas); \
@@ -352,21 +482,44 @@ cudaError_t launch_geglu(const void* A, long lda, const void* Wgu, long ldw, voi
                          int M, int D_ff, int K, int in_dtype, cudaStream_t stream, int* status) {
   if (M <= 0 || D_ff <= 0 || K <= 0) return cudaSuccess;
   if (in_dtype != kBF16 && in_dtype != kF16) return cudaErrorInvalidValue;
-  const CUtensorMapDataType tdt =
-      in_dtype == kBF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   CUtensorMap ta, tb;
-  const uint64_t adims[2] = {static_cast<uint64_t>(K), static_cast<uint64_t>(M)};
-  const uint64_t astr[1] = {static_cast<uint64_t>(lda) * 2};
-  const uint32_t abox[2] = {BK, BM};
-  const uint64_t bdims[2] = {static_cast<uint64_t>(K), static_cast<uint64_t>(2) * D_ff};
-  const uint64_t bstr[1] = {static_cast<uint64_t>(ldw) * 2};
-  const uint32_t bbox[2] = {BK, BN / 2};
-  if (!encode_tiled(&ta, tdt, 2, A, adims, astr, abox) ||
-      !encode_tiled(&tb, tdt, 2, Wgu, bdims, bstr, bbox))
+  if (!encode_ab(ta, tb, A, lda, Wgu, ldw, M, 2 * D_ff, K, in_dtype, BN / 2))
     return cudaErrorInvalidValue;
   if (in_dtype == kBF16)
-    return launch_typed<1, __half, true>(ta, tb, Z, ldz, M, D_ff, K, stream, status, 0);
-  return launch_typed<0, __half, true>(ta, tb, Z, ldz, M, D_ff, K, stream, status, 0);
+    return launch_typed<1, __half, kEpiGeglu>(ta, tb, Z, ldz, M, D_ff, K, stream, status, 0);
+  return launch_typed<0, __half, kEpiGeglu>(ta, tb, Z, ldz, M, D_ff, K, stream, status, 0);
+}
+
+bool linear_qknorm_fusable(int M, int N, int n_norm, int d_h) {
+  return M > kSkinnyMaxRows && (d_h == 128 || d_h == 256) && n_norm > 0 && n_norm <= N &&
+         n_norm % BN == 0;
+}
+
+cudaError_t launch_linear_qknorm(const void* A, long lda, const void* W, long ldw, void* C,
+                                 long ldc, int M, int N, int K, int in_dtype, const void* gamma,
+                                 const int32_t* pos, int d_h, int n_norm, double rope_base,
+                                 double rope_scale, float scale, cudaStream_t stream,
+                                 int* status) {
+  if (M <= 0 || N <= 0 || K <= 0) return cudaSuccess;
+  if (in_dtype != kBF16 && in_dtype != kF16) return cudaErrorInvalidValue;
+  if (!linear_qknorm_fusable(M, N, n_norm, d_h)) return cudaErrorInvalidValue;
+  CUtensorMap ta, tb;
+  if (!encode_ab(ta, tb, A, lda, W, ldw, M, N, K, in_dtype, BN)) return cudaErrorInvalidValue;
+  QkEpi epi{};
+  epi.freqs = make_rope_freqs(d_h, rope_base, rope_scale);
+  epi.gamma = static_cast<const __nv_bfloat16*>(gamma);
+  epi.pos = pos;
+  epi.n_norm = n_norm;
+  epi.scale = scale;
+#define G3_QKN(AB, DH_) \
+  return launch_typed<AB, __half, kEpiQkNorm, DH_>(ta, tb, C, ldc, M, N, K, stream, status, 0, epi);
+  if (in_dtype == kBF16) {
+    if (d_h == 256) G3_QKN(1, 256)
+    G3_QKN(1, 128)
+  }
+  if (d_h == 256) G3_QKN(0, 256)
+  G3_QKN(0, 128)
+#undef G3_QKN
 }
 
 }  // namespace g3

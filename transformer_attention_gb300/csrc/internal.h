@@ -37,6 +37,17 @@ cudaError_t launch_linear_skinny(const void* A, long lda, const void* W, long ld
 cudaError_t launch_geglu(const void* A, long lda, const void* Wgu, long ldw, void* Z, long ldz,
                          int M, int D_ff, int K, int in_dtype, cudaStream_t stream, int* status);
 
+// C[M, N] (fp16) = A W^T with the attention prologue in the epilogue: columns
+// [0, n_norm) are head vectors of d_h that get RMSNorm with (1 + gamma), RoPE
+// at pos[row] with (rope_base, rope_scale) and the factor `scale`; the other
+// columns are stored as they are.  Requires linear_qknorm_fusable().
+bool linear_qknorm_fusable(int M, int N, int n_norm, int d_h);
+cudaError_t launch_linear_qknorm(const void* A, long lda, const void* W, long ldw, void* C,
+                                 long ldc, int M, int N, int K, int in_dtype, const void* gamma,
+                                 const int32_t* pos, int d_h, int n_norm, double rope_base,
+                                 double rope_scale, float scale, cudaStream_t stream,
+                                 int* status);
+
 // In place on fp16 rows: Q[m, h*d_h:(h+1)*d_h] and K[m, j*d_h:(j+1)*d_h] get
 // last-axis RMSNorm, (1 + gamma), RoPE; Q also the query scale.
 cudaError_t launch_qk_norm_rope(void* Q, long ldq, void* K, long ldk, const void* gamma_q,
