@@ -13,6 +13,7 @@ name the page and the section on it:
   [FB] "Full Gemma 3 Block"               (How it works: Block.__call__ equations)
   [RT] "Global vs Local Layer Routing"    (How it works, Watch-outs)
   [QK] "QK-Norm"                          (How it works: RMSNorm equation, Watch-outs)
+  [FB] last paragraph of How it works: the model around the blocks
 
 Readings where the pages are silent (each also listed in the design notes):
   R1  RoPE: the pages name only a base frequency and a scale.  We use the
@@ -33,6 +34,10 @@ Readings where the pages are silent (each also listed in the design notes):
   R9  With a cache, the causal-and-padding mask is over slots (s <= the
       query's own slot, slot not empty) and the sliding mask compares stored
       positions with the query position.
+  R10 The model's read-out multiplies by the embedding table itself (the
+      page's "decode through the embedding table"); the depth N and the
+      vocabulary size V are parameters (the page's depth table is empty and
+      it names no vocabulary size).
 """
 from __future__ import annotations
 
@@ -417,3 +422,44 @@ def full_block(x, gamma_pre_attn, gamma_post_attn, gamma_pre_ffn, gamma_post_ffn
     feed-forward sandwich, on the residual stream (fp64)."""
     h = block_attention(x, gamma_pre_attn, gamma_post_attn, **layer_kwargs)
     return block_ffn(h, gamma_pre_ffn, gamma_post_ffn, W_gating, W_down)
+
+
+# ----------------------------------------------------------------------------
+# the model around the blocks
+# ----------------------------------------------------------------------------
+def embed(tokens: torch.Tensor, E: torch.Tensor) -> torch.Tensor:
+    """[FB] How it works, last paragraph: the token's row of the embedding
+    table times sqrt(D).  tokens [B, T] int, E [V, D] -> [B, T, D] fp64."""
+    D = E.shape[1]
+    return E.to(F64)[tokens.to(torch.int64)] * math.sqrt(D)
+
+
+def tied_logits(h: torch.Tensor, E: torch.Tensor) -> torch.Tensor:
+    """[FB] How it works, last paragraph: decode through the embedding table,
+    logits[..., v] = sum_d h[..., d] * E[v, d]; no final-logit soft-cap ([FB]
+    Overview: it is None on every size)."""
+    return torch.matmul(h.to(F64), E.to(F64).transpose(0, 1))
+
+
+def model_forward(tokens, E, layers, gamma_final, *, model_size, H, H_kv, d_h, segment_pos,
+                  pad_lens):
+    """[FB] How it works, last paragraph: embed (times sqrt(D)), N blocks,
+    final RMSNorm, read-out through the embedding table.  Block l has type
+    P[l mod 6] and that type's RoPE base/scale/window ([RT] How it works).
+
+    ``layers``: list of dicts with Wq, Wkv, Wo, gamma_q, gamma_k, gamma_pre,
+    gamma_post, gamma_pre_ffn, gamma_post_ffn, W_gating (2, D_ff, D) and
+    W_down (D_ff, D).  Returns logits [B, T, V] in fp64."""
+    x = embed(tokens, E)
+    D = E.shape[1]
+    types = make_attention_layers_types(len(layers))
+    alpha = query_pre_attn_scalar(model_size, D, H, d_h)
+    for l, p in enumerate(layers):
+        base, scale, window = layer_params(types[l], model_size)
+        x = full_block(x, p["gamma_pre"], p["gamma_post"], p["gamma_pre_ffn"],
+                       p["gamma_post_ffn"], p["W_gating"], p["W_down"], segment_pos=segment_pos,
+                       pad_lens=pad_lens, Wq=p["Wq"], Wkv=p["Wkv"], Wo=p["Wo"],
+                       gamma_q=p["gamma_q"], gamma_k=p["gamma_k"], H=H, H_kv=H_kv, d_h=d_h,
+                       attn_type=types[l], window=window, rope_base=base, rope_scale=scale,
+                       query_scale=alpha)
+    return tied_logits(rms_norm(x, gamma_final), E)
