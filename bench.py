@@ -22,6 +22,7 @@ from __future__ import annotations
 import argparse
 import hashlib
 import json
+import math
 import os
 import statistics
 import subprocess
@@ -203,6 +204,13 @@ def run_gpu(args, world, rank, local):
     x = x_cpu.to(dev)
     pos = WL.segment_pos(w).to(dev)
     pad = pads.to(dev)
+    # the model around the blocks: token ids, embedding table, final norm, logits
+    model = w.vocab > 0
+    if model:
+        tok = WL.tokens(w).to(dev)
+        tables = {k: v.to(dev) for k, v in WL.model_tables(w).items()}
+        hbuf = torch.empty((M, D), dtype=torch.bfloat16, device=dev)
+        logits = torch.empty((M, w.vocab), dtype=torch.float32, device=dev)
     layers = [LayerBuffers(w, l, x, torch, G3, stack) for l in range(w.num_layers)]
     alpha = w.query_scale
     qbuf = torch.empty((M, HD), dtype=torch.float16, device=dev)
@@ -242,12 +250,19 @@ def run_gpu(args, world, rank, local):
             work["rmsnorm"] += metrics.rmsnorm_bytes(M, D, 4)
             work["postnorm"] += metrics.postnorm_bytes(M, D, 4)
             work["cast"] += 3 * w.d_ff * D * 4.0
+    if model:
+        work["linear"] += 2.0 * M * w.vocab * D
+        work["rmsnorm"] += metrics.rmsnorm_bytes(M, D, 4)
+        work["embed"] = float(M * D * (2 + 4) + M * 4)
     nl = w.num_layers
-    launches = {"linear": (5 if ffn else 3) * nl, "attention": nl,
+    launches = {"linear": (5 if ffn else 3) * nl + (1 if model else 0), "attention": nl,
                 "qk_norm_rope": 0 if fused_qk else nl,
                 "rmsnorm": (2 if ffn else 1) * nl if stack else 0,
                 "postnorm": (2 if ffn else 1) * nl if stack else 0,
                 "cast": (5 if ffn else 3) * nl if stack else 0}
+    if model:
+        launches["rmsnorm"] += 1
+        launches["embed"] = 1
 
     def step(ev=None):
         """One pass of the hot path as stage calls (the same kernels, buffers
@@ -267,11 +282,16 @@ def run_gpu(args, world, rank, local):
             e1.record(stream)
             ev.setdefault(name, []).append((e0, e1))
 
+        if model:
+            e = mark("embed")
+            G3.gemma3_embed(tok, tables["E"], w.vocab, D, M, math.sqrt(D), resid)
+            done("embed", e)
         for li, L in enumerate(layers):
             a_in, act = x.reshape(M, D), G3.GEMMA3_BF16
             wq, wkv, wo = L.p["Wq"], L.p["Wkv"], L.p["Wo"]
             # the stack's residual stream: bf16 x into layer 0, fp32 afterwards
-            r_in, r_t = (x, G3.GEMMA3_BF16) if li == 0 else (resid, G3.GEMMA3_F32)
+            r_in, r_t = ((x, G3.GEMMA3_BF16) if li == 0 and not model
+                         else (resid, G3.GEMMA3_F32))
             if stack:
                 e = mark("rmsnorm")
                 G3.gemma3_rmsnorm(r_in, r_t, L.p["gamma_pre"], u, G3.GEMMA3_F16, M, D)
@@ -340,6 +360,15 @@ def run_gpu(args, world, rank, local):
                 G3.gemma3_postnorm_residual(out, resid, G3.GEMMA3_F32, L.p["gamma_post_ffn"],
                                             resid, M, D)
                 done("postnorm", e)
+        if model:
+            e = mark("rmsnorm")
+            G3.gemma3_rmsnorm(resid, G3.GEMMA3_F32, tables["gamma_final"], hbuf, G3.GEMMA3_BF16,
+                              M, D)
+            done("rmsnorm", e)
+            e = mark("linear")
+            G3.gemma3_linear(hbuf, D, tables["E"], D, logits, w.vocab, M, w.vocab, D,
+                             G3.GEMMA3_BF16, G3.GEMMA3_F32)
+            done("read_out", e)
 
     for _ in range(args.warmup):
         flush.zero_()
@@ -377,7 +406,8 @@ def run_gpu(args, world, rank, local):
     dev_seconds = sum(step_ms) / 1e3
     value, max_seconds = whole_job_value(tokens * args.steps, dev_seconds, world, dev)
     kern_ms = {k: sum(a.elapsed_time(b) for a, b in v) for k, v in events.items()}
-    gemm_names = ("proj_q", "proj_kv", "proj_o") + (("ffn_geglu", "ffn_down") if ffn else ())
+    gemm_names = (("proj_q", "proj_kv", "proj_o") + (("ffn_geglu", "ffn_down") if ffn else ())
+                  + (("read_out",) if model else ()))
     proj_ms = {k: sum(a.elapsed_time(b) for a, b in events[k]) / args.steps for k in gemm_names}
     kern_ms["linear"] = sum(kern_ms.pop(k, 0.0) for k in gemm_names)
 
@@ -424,6 +454,10 @@ def run_gpu(args, world, rank, local):
         if k in proj_ms:
             breakdown[k] = {"ms_per_step": proj_ms[k],
                             "tflops": gf[name] * w.num_layers / (proj_ms[k] / 1e3) / 1e12}
+    if model:
+        breakdown["read_out"] = {"ms_per_step": proj_ms["read_out"],
+                                 "tflops": 2.0 * M * w.vocab * D / (proj_ms["read_out"] / 1e3)
+                                 / 1e12}
 
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
@@ -433,7 +467,8 @@ def run_gpu(args, world, rank, local):
         "data": "synthetic (seeded N(0,1) activations, N(0,1/D) weights, gamma N(0,0.1))",
         "config": {"workload": w.name, "B": w.B, "T": w.T, "D": D, "H": H, "H_kv": H_kv,
                    "d_h": d_h, "attn": w.attn_type, "window": w.window,
-                   "layers": w.num_layers, "d_ff": w.d_ff or None, "valid_tokens": int(tokens),
+                   "layers": w.num_layers, "d_ff": w.d_ff or None, "vocab": w.vocab or None,
+                   "valid_tokens": int(tokens),
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "l2": "flushed before every timed step (256 MiB write, outside step events)",
                    "operands": "bf16 projections, f16 attention operands, f32 accumulation"},
@@ -458,16 +493,26 @@ def run_e2e(args, w, layers, x_cpu, pads, torch, G3, dev, stack, world):
     gemma3_block_attn_forward), timing host->device copies of the step's
     activations from pinned memory and the device->host read of its result."""
     M, D = w.M, w.D
-    x_host = x_cpu.pin_memory()
+    model = w.vocab > 0
+    x_host = (WL.tokens(w) if model else x_cpu).pin_memory()
     pos_host = WL.segment_pos(w).pin_memory()
     pad_host = pads.pin_memory()
     x_d = torch.empty_like(x_host, device=dev)
     pos_d = torch.empty_like(pos_host, device=dev)
     pad_d = torch.empty_like(pad_host, device=dev)
-    out_host = torch.empty((w.B, w.T, D), dtype=torch.float32 if stack else torch.bfloat16,
-                           pin_memory=True)
+    out_host = torch.empty((w.B, w.T, w.vocab if model else D),
+                           dtype=torch.float32 if stack else torch.bfloat16, pin_memory=True)
     dims = (w.B, w.T, D, w.H, w.H_kv, w.d_h)
-    if w.d_ff > 0:
+    if model:
+        ws_bytes = G3.gemma3_model_workspace_size(dims, w.d_ff, w.vocab)
+        y = torch.empty((w.B, w.T, w.vocab), dtype=torch.float32, device=dev)
+        tables = {k: v.to(dev) for k, v in WL.model_tables(w).items()}
+        mlayers = [{"Wq": L.p["Wq"], "Wkv": L.p["Wkv"], "Wo": L.p["Wo"],
+                    "gamma_q": L.p["gamma_q"], "gamma_k": L.p["gamma_k"],
+                    "gamma_pre_attn": L.p["gamma_pre"], "gamma_post_attn": L.p["gamma_post"],
+                    "gamma_pre_ffn": L.p["gamma_pre_ffn"], "gamma_post_ffn": L.p["gamma_post_ffn"],
+                    "W_gating": L.p["W_gating"], "W_down": L.p["W_down"]} for L in layers]
+    elif w.d_ff > 0:
         ws_bytes = G3.gemma3_block_workspace_size(dims, w.d_ff)
         y = torch.empty((w.B, w.T, D), dtype=torch.float32, device=dev)
     elif stack:
@@ -483,7 +528,11 @@ def run_e2e(args, w, layers, x_cpu, pads, torch, G3, dev, stack, world):
         x_d.copy_(x_host, non_blocking=True)
         pos_d.copy_(pos_host, non_blocking=True)
         pad_d.copy_(pad_host, non_blocking=True)
-        if w.d_ff > 0:
+        if model:
+            G3.gemma3_model_forward(dims, w.d_ff, w.vocab, w.num_layers, w.model_size, x_d, pos_d,
+                                    pad_d, tables["E"], mlayers, tables["gamma_final"], y, ws,
+                                    ws_bytes)
+        elif w.d_ff > 0:
             src, src_t = x_d, G3.GEMMA3_BF16
             for L in layers:
                 G3.gemma3_block_forward(
@@ -531,7 +580,8 @@ def run_e2e(args, w, layers, x_cpu, pads, torch, G3, dev, stack, world):
     d2h = out_host.numel() * out_host.element_size()
     return {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h,
-            "api": ("gemma3_block_forward" if w.d_ff > 0 else
+            "api": ("gemma3_model_forward" if model else
+                    "gemma3_block_forward" if w.d_ff > 0 else
                     "gemma3_block_attn_forward" if stack else "gemma3_attn_forward")}
 
 
@@ -787,7 +837,13 @@ _ORACLE_WEIGHTS = {}
 
 def _oracle_weights(w):
     if w.name not in _ORACLE_WEIGHTS:
-        if w.attn_type == "stack":
+        if w.vocab > 0:
+            _ORACLE_WEIGHTS[w.name] = [
+                dict(WL.weights(w, l), **WL.block_norm_gammas(w, l),
+                     **{k: (v.transpose(0, 1) if k == "W_down" else v)
+                        for k, v in WL.ffn_weights(w, l).items()})
+                for l in range(w.num_layers)]
+        elif w.attn_type == "stack":
             _ORACLE_WEIGHTS[w.name] = [dict(WL.weights(w, l), **WL.block_norm_gammas(w, l))
                                        for l in range(w.num_layers)]
         elif w.d_ff > 0:
@@ -809,6 +865,13 @@ def oracle_sample(w, n_tokens: int):
     x = WL.x_rows(w, 0, 0, n_tokens)[None]
     pos = WL.segment_pos(ws)
     p = _oracle_weights(w)
+    if w.vocab > 0:
+        tok = WL.tokens(w)[:1, :n_tokens]
+        tables = WL.model_tables(w)
+        t0 = time.perf_counter()
+        O.model_forward(tok, tables["E"], p, tables["gamma_final"], model_size=w.model_size,
+                        H=w.H, H_kv=w.H_kv, d_h=w.d_h, segment_pos=pos, pad_lens=None)
+        return time.perf_counter() - t0
     t0 = time.perf_counter()
     if w.attn_type == "stack":
         O.attention_stack(x, p, model_size=w.model_size, H=w.H, H_kv=w.H_kv, d_h=w.d_h,

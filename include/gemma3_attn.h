@@ -44,7 +44,8 @@ enum {
   GEMMA3_ERR_UNSUPPORTED = -3, /* d_h not in {128, 256}, G not in {1, 2, 4}, not sm_103 */
   GEMMA3_ERR_CUDA = -4,        /* a CUDA runtime call or kernel launch failed */
   GEMMA3_ERR_TIMEOUT = -5,     /* a kernel gave up on a bounded wait (device status word) */
-  GEMMA3_ERR_WORKSPACE = -6    /* workspace smaller than gemma3_*_workspace_size() */
+  GEMMA3_ERR_WORKSPACE = -6,   /* workspace smaller than gemma3_*_workspace_size() */
+  GEMMA3_ERR_BAD_INPUT = -7    /* a kernel found invalid data (a token id outside [0, V)) */
 };
 
 /* Attention types of [RT] How it works (AttentionType enum). */
@@ -217,6 +218,49 @@ int gemma3_block_forward(const gemma3_attn_dims* dims, int D_ff, const void* x, 
                          float query_scale, void* workspace, size_t workspace_bytes,
                          void* stream);
 
+/* ------------------------------------------------------------------ the model */
+
+/* Device pointers of one block's weights (as gemma3_block_forward takes them). */
+typedef struct {
+  const void* Wq;              /* [H*d_h, D] bf16 */
+  const void* Wkv;             /* [2, H_kv*d_h, D] bf16 */
+  const void* Wo;              /* [D, H*d_h] bf16 */
+  const void* gamma_q;         /* [d_h] bf16 */
+  const void* gamma_k;         /* [d_h] bf16 */
+  const void* gamma_pre_attn;  /* [D] bf16 */
+  const void* gamma_post_attn; /* [D] bf16 */
+  const void* gamma_pre_ffn;   /* [D] bf16 */
+  const void* gamma_post_ffn;  /* [D] bf16 */
+  const void* W_gating;        /* [2, D_ff, D] bf16 */
+  const void* W_down;          /* [D, D_ff] bf16 */
+} gemma3_block_weights;
+
+/* Workspace of gemma3_model_forward. */
+int gemma3_model_workspace_size(const gemma3_attn_dims* dims, int D_ff, int V, size_t* bytes);
+
+/* The model around the blocks ([FB] How it works, last paragraph):
+ *   x = E[tokens] * sqrt(D);  x <- Block_l(x) for l = 0..num_layers-1;
+ *   logits = RMSNorm_final(x) E^T  (read-out through the embedding table).
+ * Block l is gemma3_block_forward with the type, window and RoPE pair that
+ * gemma3_layer_config(l, num_layers, model_size) gives and the query scale of
+ * gemma3_query_scale(model_size, ...).  tokens [B, T] int32 in [0, V) (others
+ * give zero rows and GEMMA3_ERR_BAD_INPUT from gemma3_attn_check_status);
+ * E [V, D] bf16; layers: HOST array of num_layers structs of device
+ * pointers; gamma_final [D] bf16; logits [B, T, V] fp32 (V % 4 == 0).  The
+ * residual stream stays fp32 between blocks; the final norm is rounded to
+ * bf16 for the read-out GEMM.  Pad rows run through every block like the
+ * other rows (their attention output is 0). */
+int gemma3_model_forward(const gemma3_attn_dims* dims, int D_ff, int V, int num_layers,
+                         int model_size, const int32_t* tokens, const int32_t* segment_pos,
+                         const int32_t* pad_lens, const void* E,
+                         const gemma3_block_weights* layers, const void* gamma_final,
+                         float* logits, void* workspace, size_t workspace_bytes, void* stream);
+
+/* x[m, :] = E[tokens[m], :] * scale in fp32 ([FB] last paragraph, with
+ * scale = sqrt(D)); E [V, D] bf16, D % 8 == 0; x [M, D] fp32. */
+int gemma3_embed(const int32_t* tokens, const void* E, int V, int D, int M, float scale, float* x,
+                 void* stream);
+
 /* ------------------------------------------------------------------ KV cache */
 
 /* A layer's KV cache ([AB] How it works, Cache): K' (after QK-norm and RoPE)
@@ -354,10 +398,12 @@ int gemma3_postnorm_residual(const float* a, const void* x, int x_dtype, const v
 
 /* Synchronises `stream`, reads and clears the device status word of the
  * current device.  Returns GEMMA3_OK, GEMMA3_ERR_TIMEOUT (a bounded wait in a
- * kernel expired), or GEMMA3_ERR_CUDA (the stream reported an error). */
+ * kernel expired), GEMMA3_ERR_BAD_INPUT (a kernel found invalid data), or
+ * GEMMA3_ERR_CUDA (the stream reported an error). */
 int gemma3_attn_check_status(void* stream);
 
-/* Raw device status word of the last check (0 = none; 0x1000 + n = wait site n). */
+/* Raw device status word of the last check (0 = none; 0x1000 + n = wait site
+ * n; 0x2000 = a token id outside [0, V)). */
 int gemma3_last_device_status(void);
 
 /* Human-readable text of a status code. */

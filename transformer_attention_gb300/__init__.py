@@ -16,12 +16,13 @@ from ._lib import (  # noqa: F401  (re-exported C-ABI names)
     gemma3_cast_bf16_f16, gemma3_geglu,
     gemma3_flash_attention,
     gemma3_last_device_status, gemma3_layer_attn_type, gemma3_layer_config, gemma3_linear,
-    gemma3_linear_qk_norm_rope,
+    gemma3_linear_qk_norm_rope, gemma3_embed, gemma3_model_forward, gemma3_model_workspace_size,
+    GEMMA3_ERR_BAD_INPUT,
     gemma3_postnorm_residual, gemma3_qk_norm_rope, gemma3_query_scale, gemma3_rmsnorm,
     gemma3_selftest_wait_timeout, lib)
 
 __all__ = ["attention_forward", "attention_forward_cached", "block_attention_forward",
-           "block_forward", "new_kv_cache", "linear", "lib"]
+           "block_forward", "model_forward", "new_kv_cache", "linear", "lib"]
 
 
 def _empty_ws(nbytes: int, device):
@@ -127,6 +128,27 @@ def block_forward(x, segment_pos, pad_lens, Wq, Wkv, Wo, gamma_q, gamma_k, gamma
                          W_gating, W_down, attn_type, window, rope_base, rope_scale, query_scale,
                          workspace, workspace.numel(), stream)
     return y
+
+
+def model_forward(tokens, segment_pos, pad_lens, E, layers, gamma_final, *, H, H_kv, D_ff,
+                  model_size, logits=None, workspace=None, stream=None):
+    """The model: tokens [B,T] int32 -> logits [B,T,V] fp32 (read-out through
+    E [V,D] bf16).  ``layers``: list of dicts of device tensors (Wq, Wkv, Wo,
+    gamma_q, gamma_k, gamma_pre_attn, gamma_post_attn, gamma_pre_ffn,
+    gamma_post_ffn, W_gating [2,D_ff,D], W_down [D,D_ff])."""
+    import torch
+    B, T = tokens.shape
+    V, D = E.shape
+    d_h = layers[0]["gamma_q"].shape[0] if layers else 256
+    dims = (B, T, D, H, H_kv, d_h)
+    ws_bytes = gemma3_model_workspace_size(dims, D_ff, V)
+    if workspace is None:
+        workspace = _empty_ws(ws_bytes, tokens.device)
+    if logits is None:
+        logits = torch.empty((B, T, V), dtype=torch.float32, device=tokens.device)
+    gemma3_model_forward(dims, D_ff, V, len(layers), model_size, tokens, segment_pos, pad_lens,
+                         E, layers, gamma_final, logits, workspace, workspace.numel(), stream)
+    return logits
 
 
 def linear(A, W, out_dtype=None, max_ctas=0, stream=None):

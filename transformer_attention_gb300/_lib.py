@@ -17,6 +17,7 @@ c_int, c_long, c_double, c_float, c_size_t, c_void_p = (
 
 GEMMA3_OK = 0
 GEMMA3_ERR_TIMEOUT = -5
+GEMMA3_ERR_BAD_INPUT = -7
 GEMMA3_LOCAL_SLIDING, GEMMA3_GLOBAL = 0, 1
 GEMMA3_BF16, GEMMA3_F16, GEMMA3_F32 = 0, 1, 2
 MODEL_SIZES = {"270M": 0, "1B": 1, "4B": 2, "12B": 3, "27B": 4}
@@ -25,6 +26,12 @@ MODEL_SIZES = {"270M": 0, "1B": 1, "4B": 2, "12B": 3, "27B": 4}
 class gemma3_attn_dims(ctypes.Structure):
     _fields_ = [("B", c_int), ("T", c_int), ("D", c_int), ("H", c_int), ("H_kv", c_int),
                 ("d_h", c_int)]
+
+
+class gemma3_block_weights(ctypes.Structure):
+    _fields_ = [(n, c_void_p) for n in (
+        "Wq", "Wkv", "Wo", "gamma_q", "gamma_k", "gamma_pre_attn", "gamma_post_attn",
+        "gamma_pre_ffn", "gamma_post_ffn", "W_gating", "W_down")]
 
 
 # name -> (restype, argtypes); mirrors include/gemma3_attn.h
@@ -63,6 +70,14 @@ SIGNATURES = {
                                      c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                                      c_void_p, c_void_p, c_int, c_int, c_double, c_double,
                                      c_float, c_void_p, c_size_t, c_void_p]),
+    "gemma3_model_workspace_size": (c_int, [ctypes.POINTER(gemma3_attn_dims), c_int, c_int,
+                                            ctypes.POINTER(c_size_t)]),
+    "gemma3_model_forward": (c_int, [ctypes.POINTER(gemma3_attn_dims), c_int, c_int, c_int, c_int,
+                                     c_void_p, c_void_p, c_void_p, c_void_p,
+                                     ctypes.POINTER(gemma3_block_weights), c_void_p, c_void_p,
+                                     c_void_p, c_size_t, c_void_p]),
+    "gemma3_embed": (c_int, [c_void_p, c_void_p, c_int, c_int, c_int, c_float, c_void_p,
+                             c_void_p]),
     "gemma3_attn_cached_workspace_size": (c_int, [ctypes.POINTER(gemma3_attn_dims), c_int,
                                                   ctypes.POINTER(c_size_t)]),
     "gemma3_attn_forward_cached": (c_int, [ctypes.POINTER(gemma3_attn_dims), c_int, c_int,
@@ -266,6 +281,34 @@ def gemma3_block_forward(dims, D_ff, x, x_dtype, y, segment_pos, pad_lens, Wq, W
         _ptr(gamma_post_attn), _ptr(gamma_pre_ffn), _ptr(gamma_post_ffn), _ptr(W_gating),
         _ptr(W_down), attn_type, window, rope_base, rope_scale, query_scale, _ptr(workspace),
         workspace_bytes, _stream(stream)))
+
+
+def gemma3_model_workspace_size(dims, D_ff, V) -> int:
+    n = c_size_t()
+    d = _dims(*dims)
+    _check("gemma3_model_workspace_size",
+           lib().gemma3_model_workspace_size(ctypes.byref(d), D_ff, V, ctypes.byref(n)))
+    return n.value
+
+
+def gemma3_model_forward(dims, D_ff, V, num_layers, model_size, tokens, segment_pos, pad_lens, E,
+                         layers, gamma_final, logits, workspace, workspace_bytes, stream=None):
+    """``layers``: a sequence of dicts of device tensors keyed by the
+    gemma3_block_weights field names; ``model_size``: "270M" .. "27B"."""
+    d = _dims(*dims)
+    arr = (gemma3_block_weights * max(1, num_layers))()
+    for i, L in enumerate(layers):
+        for name, _ in gemma3_block_weights._fields_:
+            setattr(arr[i], name, _ptr(L[name]))
+    return _check("gemma3_model_forward", lib().gemma3_model_forward(
+        ctypes.byref(d), D_ff, V, num_layers, MODEL_SIZES[model_size], _ptr(tokens),
+        _ptr(segment_pos), _ptr(pad_lens), _ptr(E), arr, _ptr(gamma_final), _ptr(logits),
+        _ptr(workspace), workspace_bytes, _stream(stream)))
+
+
+def gemma3_embed(tokens, E, V, D, M, scale, x, stream=None):
+    return _check("gemma3_embed", lib().gemma3_embed(_ptr(tokens), _ptr(E), V, D, M, scale,
+                                                     _ptr(x), _stream(stream)))
 
 
 def gemma3_attn_cached_workspace_size(dims, S) -> int:

@@ -450,6 +450,99 @@ int gemma3_block_forward(const gemma3_attn_dims* dims, int D_ff, const void* x, 
                       as_stream(stream));
 }
 
+// ------------------------------------------------------------ the model
+
+namespace {
+
+struct ModelWs {
+  size_t x, h, block, total;
+};
+
+int model_ws(const gemma3_attn_dims* d, int D_ff, ModelWs* w) {
+  size_t blk = 0;
+  const int rc = gemma3_block_workspace_size(d, D_ff, &blk);
+  if (rc != GEMMA3_OK) return rc;
+  const size_t M = static_cast<size_t>(d->B) * d->T;
+  w->x = round_up(M * d->D * 4, 256);
+  w->h = round_up(M * d->D * 2, 256);
+  w->block = round_up(blk, 256);
+  w->total = w->x + w->h + w->block;
+  return GEMMA3_OK;
+}
+
+}  // namespace
+
+int gemma3_model_workspace_size(const gemma3_attn_dims* dims, int D_ff, int V, size_t* bytes) {
+  if (bytes == nullptr || V < 1) return GEMMA3_ERR_INVALID_ARG;
+  ModelWs w;
+  const int rc = model_ws(dims, D_ff, &w);
+  if (rc != GEMMA3_OK) return rc;
+  *bytes = w.total;
+  return GEMMA3_OK;
+}
+
+int gemma3_embed(const int32_t* tokens, const void* E, int V, int D, int M, float scale, float* x,
+                 void* stream) {
+  if (!tokens || !E || !x || V < 1 || D < 8 || D % 8 || M < 0) return GEMMA3_ERR_INVALID_ARG;
+  if (!aligned16(E) || !aligned16(x)) return GEMMA3_ERR_MISALIGNED;
+  int rc = check_device();
+  if (rc != GEMMA3_OK) return rc;
+  int* st = status_ptr();
+  if (st == nullptr) return GEMMA3_ERR_CUDA;
+  return to_status(launch_embed_rows(tokens, E, V, D, M, scale, x, as_stream(stream), st));
+}
+
+int gemma3_model_forward(const gemma3_attn_dims* dims, int D_ff, int V, int num_layers,
+                         int model_size, const int32_t* tokens, const int32_t* segment_pos,
+                         const int32_t* pad_lens, const void* E,
+                         const gemma3_block_weights* layers, const void* gamma_final,
+                         float* logits, void* workspace, size_t workspace_bytes, void* stream) {
+  ModelWs w;
+  int rc = validate_dims(dims);
+  if (rc != GEMMA3_OK) return rc;
+  rc = model_ws(dims, D_ff, &w);
+  if (rc != GEMMA3_OK) return rc;
+  if (V < 1 || num_layers < 0 || !tokens || !segment_pos || !E || !gamma_final || !logits ||
+      !workspace || (num_layers > 0 && !layers))
+    return GEMMA3_ERR_INVALID_ARG;
+  if (model_size < GEMMA3_270M || model_size > GEMMA3_27B) return GEMMA3_ERR_INVALID_ARG;
+  if (!aligned16(E) || !aligned16(gamma_final) || !aligned16(logits) || V % 4 ||
+      (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return GEMMA3_ERR_MISALIGNED;
+  if (workspace_bytes < w.total) return GEMMA3_ERR_WORKSPACE;
+  rc = check_device();
+  if (rc != GEMMA3_OK) return rc;
+  int* st = status_ptr();
+  if (st == nullptr) return GEMMA3_ERR_CUDA;
+  float alpha = 0.f;
+  rc = gemma3_query_scale(model_size, dims->D, dims->H, dims->d_h, &alpha);
+  if (rc != GEMMA3_OK) return rc;
+  const int M = dims->B * dims->T, D = dims->D;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  float* x = reinterpret_cast<float*>(ws);           // residual stream, fp32 [M, D]
+  void* h = ws + w.x;                                 // final norm, bf16 [M, D]
+  void* bws = ws + w.x + w.h;                         // the blocks' workspace
+  cudaStream_t s = as_stream(stream);
+  if (launch_embed_rows(tokens, E, V, D, M, static_cast<float>(std::sqrt(static_cast<double>(D))),
+                        x, s, st) != cudaSuccess)
+    return GEMMA3_ERR_CUDA;
+  for (int l = 0; l < num_layers; ++l) {
+    int type = 0, window = 0;
+    double base = 0.0, scale = 0.0;
+    rc = gemma3_layer_config(l, num_layers, model_size, &type, &window, &base, &scale);
+    if (rc < 0) return rc;
+    const gemma3_block_weights& L = layers[l];
+    rc = gemma3_block_forward(dims, D_ff, x, GEMMA3_F32, x, segment_pos, pad_lens, L.Wq, L.Wkv,
+                              L.Wo, L.gamma_q, L.gamma_k, L.gamma_pre_attn, L.gamma_post_attn,
+                              L.gamma_pre_ffn, L.gamma_post_ffn, L.W_gating, L.W_down, type,
+                              window, base, scale, alpha, bws, w.block, stream);
+    if (rc != GEMMA3_OK) return rc;
+  }
+  if (launch_rmsnorm_rows(x, kF32, gamma_final, h, kBF16, M, D, s) != cudaSuccess)
+    return GEMMA3_ERR_CUDA;
+  return to_status(launch_linear(h, D, E, D, logits, V, M, V, D, kBF16, kF32, s, st, 0));
+}
+
 // ------------------------------------------------------------ KV-cache path
 
 namespace {
@@ -739,7 +832,7 @@ int gemma3_attn_check_status(void* stream) {
     const int zero = 0;
     if (cudaMemcpyToSymbol(g3_device_status, &zero, sizeof(int)) != cudaSuccess)
       return GEMMA3_ERR_CUDA;
-    return GEMMA3_ERR_TIMEOUT;
+    return v >= kDevErrBadToken ? GEMMA3_ERR_BAD_INPUT : GEMMA3_ERR_TIMEOUT;
   }
   return GEMMA3_OK;
 }
@@ -755,6 +848,7 @@ const char* gemma3_strerror(int status) {
     case GEMMA3_ERR_CUDA: return "CUDA error";
     case GEMMA3_ERR_TIMEOUT: return "kernel gave up on a bounded wait";
     case GEMMA3_ERR_WORKSPACE: return "workspace too small";
+    case GEMMA3_ERR_BAD_INPUT: return "a kernel found invalid input data";
     default: return "unknown status";
   }
 }

@@ -15,6 +15,9 @@
 //   projection GEMM's epilogue; this kernel serves the cases that fusion does
 //   not cover and the stage entry point.)
 //
+// embed_rows: the model's input ("Full Gemma 3 Block", How it works, last
+//   paragraph: embed times sqrt(D)), x[m, :] = E[tokens[m], :] * scale in fp32.
+//
 // rmsnorm_rows / postnorm_residual: the D-axis norms of the block sandwich
 //   ("Full Gemma 3 Block", How it works: a = Attn(RMSNorm_pre(x));
 //   a <- RMSNorm_post(a); h = x + a), one warp per row.
@@ -288,6 +291,51 @@ cudaError_t launch_cast_bf16_f16(const void* src, void* dst, size_t n, cudaStrea
   if (blocks > cap) blocks = cap;
   cast_bf16_f16_kernel<<<blocks, 256, 0, stream>>>(static_cast<const uint4*>(src),
                                                    static_cast<uint4*>(dst), n8);
+  return cudaGetLastError();
+}
+
+namespace {
+
+// One warp per row, 8 columns (one 16-byte load) per lane per step.  A token
+// outside [0, V) gives a zero row and records kDevErrBadToken.
+__global__ void __launch_bounds__(256) embed_rows_kernel(const int32_t* __restrict__ tokens,
+                                                         const __nv_bfloat16* __restrict__ E,
+                                                         int V, int D, int M, float scale,
+                                                         float* __restrict__ x, int* status) {
+  const int m = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  if (m >= M) return;
+  const int t = tokens[m];
+  const bool ok = t >= 0 && t < V;
+  if (!ok && lane == 0) record_error(status, kDevErrBadToken);
+  const __nv_bfloat16* src = E + static_cast<size_t>(ok ? t : 0) * D;
+  float* dst = x + static_cast<size_t>(m) * D;
+  for (int c = lane * 8; c < D; c += 256) {
+    float f[8];
+    if (ok) {
+      const uint4 r = __ldg(reinterpret_cast<const uint4*>(src + c));
+      const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&r);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 v = __bfloat1622float2(h[i]);
+        f[2 * i] = v.x * scale;
+        f[2 * i + 1] = v.y * scale;
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) f[i] = 0.f;
+    }
+    reinterpret_cast<float4*>(dst + c)[0] = make_float4(f[0], f[1], f[2], f[3]);
+    reinterpret_cast<float4*>(dst + c)[1] = make_float4(f[4], f[5], f[6], f[7]);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_embed_rows(const int32_t* tokens, const void* E, int V, int D, int M,
+                              float scale, float* x, cudaStream_t stream, int* status) {
+  if (M <= 0) return cudaSuccess;
+  embed_rows_kernel<<<(M + 7) / 8, 256, 0, stream>>>(
+      tokens, static_cast<const __nv_bfloat16*>(E), V, D, M, scale, x, status);
   return cudaGetLastError();
 }
 

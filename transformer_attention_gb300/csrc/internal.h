@@ -72,6 +72,11 @@ cudaError_t launch_rmsnorm_rows(const void* x, int x_dtype, const void* gamma, v
 // dst[i] = src[i] converted bf16 -> f16 (round to nearest even), n elements.
 cudaError_t launch_cast_bf16_f16(const void* src, void* dst, size_t n, cudaStream_t stream);
 
+// x[m, :] = E[tokens[m], :] * scale (fp32), E [V, D] bf16; bad token ids give
+// a zero row and a device status error.
+cudaError_t launch_embed_rows(const int32_t* tokens, const void* E, int V, int D, int M,
+                              float scale, float* x, cudaStream_t stream, int* status);
+
 // y[m,:] = x[m,:] + RMSNorm(a[m,:]) * (1 + gamma); a f32, x bf16|f32, y f32.
 cudaError_t launch_postnorm_residual(const float* a, const void* x, int x_dtype,
                                      const void* gamma, float* y, int M, int D,

@@ -18,6 +18,7 @@ constexpr unsigned long long kWaitTimeoutNs = 1000000000ull;  // 1 s per wait
 // Error codes written into g_status by device code.
 enum : int {
   kDevErrTimeoutBase = 0x1000,   // + wait-site id
+  kDevErrBadToken = 0x2000,      // a token id outside [0, V)
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {

@@ -30,6 +30,7 @@ SEED_X, SEED_WQ, SEED_WKV, SEED_WO, SEED_GQ, SEED_GK, SEED_PAD = 1, 2, 3, 4, 5, 
 SEED_GPRE, SEED_GPOST = 8, 9
 SEED_WGATE, SEED_WDOWN, SEED_GPRE_FFN, SEED_GPOST_FFN = 10, 11, 12, 13
 SEED_KCACHE, SEED_VCACHE = 14, 15
+SEED_TOKENS, SEED_EMBED, SEED_GFINAL = 16, 17, 18
 
 
 @dataclass(frozen=True)
@@ -52,6 +53,7 @@ class Workload:
     num_layers: int = 1
     d_ff: int = 0             # > 0: the workload is the whole block (attention + feed-forward)
     cache_len: int = 0        # > 0: T new tokens per row appended to a KV cache of this many slots
+    vocab: int = 0            # > 0: the whole model (embedding, routed full blocks, read-out)
     description: str = field(default="", compare=False)
 
     @property
@@ -107,8 +109,17 @@ WORKLOADS["27b_global_decode"] = Workload(
     rope_base=1e6, rope_scale=8.0, query_scale=168 ** -0.5, model_size="27B", cache_len=131072,
     description="decode step, 27B-shaped global layer: B1, 1 new token after 131071 cached")
 
+# The model around the blocks on the 1B sizes: embedding, one routing tile of
+# six full blocks (the pages give no depth table) and the read-out through a
+# synthetic 32768-row embedding table (the pages give no vocabulary size).
+WORKLOADS["1b_model"] = Workload(
+    "1b_model", B=2, T=4096, D=1152, H=4, H_kv=1, d_h=256, attn_type="stack", window=512,
+    rope_base=0.0, rope_scale=0.0, query_scale=256 ** -0.5, model_size="1B", num_layers=6,
+    d_ff=6 * 1152, vocab=32768,
+    description="1B-shaped model: embed, 6 routed full blocks (D_ff 6912), tied read-out V32768")
+
 ORDER = ["tiny_local", "1b_global", "4b_local", "27b_global", "12b_stack", "4b_block",
-         "4b_local_decode", "27b_global_decode"]
+         "4b_local_decode", "27b_global_decode", "1b_model"]
 
 
 def small(w: Workload, **kw) -> Workload:
@@ -201,6 +212,19 @@ def ffn_weights(w: Workload, layer: int = 0) -> dict:
         "gamma_pre_ffn": _normal_bf16((w.D,), math.sqrt(0.1), SEED_GPRE_FFN + off),
         "gamma_post_ffn": _normal_bf16((w.D,), math.sqrt(0.1), SEED_GPOST_FFN + off),
     }
+
+
+def tokens(w: Workload) -> torch.Tensor:
+    """Token ids of a model workload, int32 [B, T], uniform over [0, vocab)."""
+    g = _gen(SEED_TOKENS)
+    return torch.randint(0, w.vocab, (w.B, w.T), generator=g, dtype=torch.int64).to(torch.int32)
+
+
+def model_tables(w: Workload) -> dict:
+    """The embedding table E [vocab, D] ~ N(0, 1/D) (so E * sqrt(D) has unit
+    variance) and the final RMSNorm scale [D] ~ N(0, 0.1), bf16."""
+    return {"E": _normal_bf16((w.vocab, w.D), 1.0 / math.sqrt(w.D), SEED_EMBED),
+            "gamma_final": _normal_bf16((w.D,), math.sqrt(0.1), SEED_GFINAL)}
 
 
 def pad_lens(w: Workload) -> torch.Tensor:
