@@ -35,9 +35,9 @@ Readings where the pages are silent (each also listed in the design notes):
       query's own slot, slot not empty) and the sliding mask compares stored
       positions with the query position.
   R10 The model's read-out multiplies by the embedding table itself (the
-      page's "decode through the embedding table"); the depth N and the
-      vocabulary size V are parameters (the page's depth table is empty and
-      it names no vocabulary size).
+      page's last step reads the logits out through that table, in garbled
+      words); the depth N and the vocabulary size V are parameters (the
+      page's depth table is empty and it names no vocabulary size).
 """
 from __future__ import annotations
 
@@ -435,9 +435,9 @@ def embed(tokens: torch.Tensor, E: torch.Tensor) -> torch.Tensor:
 
 
 def tied_logits(h: torch.Tensor, E: torch.Tensor) -> torch.Tensor:
-    """[FB] How it works, last paragraph: decode through the embedding table,
-    logits[..., v] = sum_d h[..., d] * E[v, d]; no final-logit soft-cap ([FB]
-    Overview: it is None on every size)."""
+    """[FB] How it works, last paragraph: the read-out uses the embedding
+    table, logits[..., v] = sum_d h[..., d] * E[v, d]; no final-logit
+    soft-cap ([FB] Overview: none on any size)."""
     return torch.matmul(h.to(F64), E.to(F64).transpose(0, 1))
 
 
