@@ -229,6 +229,7 @@ def run_gpu(args, world, rank, local):
         wd16 = torch.empty((D, w.d_ff), dtype=torch.float16, device=dev)
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
+    sched_buf = torch.zeros(256, dtype=torch.uint8, device=dev)   # attention work counter
 
     # the library's rule for fusing the prologue into the Q / KV projections
     fused_qk = M > 16 and HD % 256 == 0 and KVD % 256 == 0
@@ -329,7 +330,7 @@ def run_gpu(args, world, rank, local):
             e = mark("attention")
             win = L.window if L.attn_type == G3.GEMMA3_LOCAL_SLIDING else 0
             G3.gemma3_flash_attention(qbuf, kvbuf, kvbuf[:, KVD:], 2 * KVD, qbuf, act, pad, w.B,
-                                      w.T, H, H_kv, d_h, win)
+                                      w.T, H, H_kv, d_h, win, sched_buf)
             done("attention", e)
             e = mark("linear")
             G3.gemma3_linear(qbuf, HD, wo, HD, out, D, M, D, HD, act,

@@ -378,10 +378,13 @@ int gemma3_qk_norm_rope(void* Q, long ldq, void* K, long ldk, const void* gamma_
  * fp16 (query scale already applied); K', V rows of fp16 buffers with row
  * stride ldkv elements, head j at column j*d_h ([B*T, ldkv]); O [B, T, H, d_h]
  * in o_dtype (GEMMA3_BF16 | GEMMA3_F16; may alias Q').  Mask and padding as in
- * gemma3_attn_forward (window <= 0 means global / causal only). */
+ * gemma3_attn_forward (window <= 0 means global / causal only).  scratch: 256
+ * bytes of 16-byte-aligned device memory that hold the work counter through
+ * which free SMs take the next (heaviest remaining) query tile, or NULL for a
+ * fixed assignment; the call zeroes it on `stream` before the launch. */
 int gemma3_flash_attention(const void* Q, const void* K, const void* V, long ldkv, void* O,
                            int o_dtype, const int32_t* pad_lens, int B, int T, int H, int H_kv,
-                           int d_h, int window, void* stream);
+                           int d_h, int window, void* scratch, void* stream);
 
 /* u[m, :] = x[m, :] / sqrt(mean(x[m, :]^2) + 1e-6) * (1 + gamma)  ([FB] block
  * norms).  x [M, D] bf16 or fp32 (x_dtype), gamma [D] bf16, u [M, D] in

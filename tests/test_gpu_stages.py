@@ -172,8 +172,8 @@ ATTN_CASES = [
 
 
 @pytest.mark.parametrize("B,T,H,H_kv,d_h,window,pads", ATTN_CASES)
-@pytest.mark.parametrize("o_f16", [False, True])
-def test_flash_attention_matches_oracle(B, T, H, H_kv, d_h, window, pads, o_f16):
+@pytest.mark.parametrize("o_f16,sched", [(False, True), (True, True), (False, False)])
+def test_flash_attention_matches_oracle(B, T, H, H_kv, d_h, window, pads, o_f16, sched):
     import transformer_attention_gb300 as G3
     G = H // H_kv
     alpha = d_h ** -0.5
@@ -185,9 +185,11 @@ def test_flash_attention_matches_oracle(B, T, H, H_kv, d_h, window, pads, o_f16)
     Od = torch.empty((B, T, H, d_h), dtype=torch.float16 if o_f16 else torch.bfloat16,
                      device="cuda")
     Od.fill_(float("nan"))
+    # sched: the work counter (dynamic order) or none (fixed assignment)
+    scratch = torch.full((256,), 0x5A, dtype=torch.uint8, device="cuda") if sched else None
     G3.gemma3_flash_attention(Qd, KVd, KVd[..., H_kv * d_h:], 2 * H_kv * d_h, Od,
                               G3.GEMMA3_F16 if o_f16 else G3.GEMMA3_BF16, pad.cuda(), B, T,
-                              H, H_kv, d_h, window)
+                              H, H_kv, d_h, window, scratch)
     assert G3.gemma3_attn_check_status() == 0
     got = Od.cpu().to(F64)
     kind = O.LOCAL_SLIDING if window > 0 else O.GLOBAL

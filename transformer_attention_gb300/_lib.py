@@ -107,7 +107,7 @@ SIGNATURES = {
                                     c_float, c_void_p]),
     "gemma3_flash_attention": (c_int, [c_void_p, c_void_p, c_void_p, c_long, c_void_p, c_int,
                                        c_void_p, c_int, c_int, c_int, c_int, c_int, c_int,
-                                       c_void_p]),
+                                       c_void_p, c_void_p]),
     "gemma3_rmsnorm": (c_int, [c_void_p, c_int, c_void_p, c_void_p, c_int, c_int, c_int,
                                c_void_p]),
     "gemma3_postnorm_residual": (c_int, [c_void_p, c_void_p, c_int, c_void_p, c_void_p, c_int,
@@ -386,10 +386,12 @@ def gemma3_qk_norm_rope(Q, ldq, K, ldk, gamma_q, gamma_k, pos, M, H, H_kv, d_h, 
 
 
 def gemma3_flash_attention(Q, K, V, ldkv, O, o_dtype, pad_lens, B, T, H, H_kv, d_h, window,
-                           stream=None):
+                           scratch=None, stream=None):
+    """scratch: a 256-byte device tensor for the dynamic work order, or None
+    for the fixed assignment."""
     return _check("gemma3_flash_attention", lib().gemma3_flash_attention(
         _ptr(Q), _ptr(K), _ptr(V), ldkv, _ptr(O), o_dtype, _ptr(pad_lens), B, T, H, H_kv, d_h,
-        window, _stream(stream)))
+        window, _ptr(scratch), _stream(stream)))
 
 
 def gemma3_rmsnorm(x, x_dtype, gamma, u, u_dtype, M, D, stream=None):

@@ -65,7 +65,7 @@ int validate_dims(const gemma3_attn_dims* d) {
 size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 struct AttnWs {
-  size_t q_bytes, kv_bytes, w_bytes, total;
+  size_t q_bytes, kv_bytes, w_bytes, sched_bytes, total;
 };
 
 // Workspace of the layer pipeline: Q/O rows, K/V rows and, when the
@@ -79,7 +79,8 @@ AttnWs attn_ws(const gemma3_attn_dims* d, bool f16_weights = false) {
   w.w_bytes = f16_weights ? round_up(HD * d->D * 2, 256) + round_up(2 * KVD * d->D * 2, 256) +
                                 round_up(HD * d->D * 2, 256)
                           : 0;
-  w.total = w.q_bytes + w.kv_bytes + w.w_bytes;
+  w.sched_bytes = kAttnSchedBytes;
+  w.total = w.q_bytes + w.kv_bytes + w.w_bytes + w.sched_bytes;
   return w;
 }
 
@@ -144,8 +145,10 @@ int attn_pipeline(const gemma3_attn_dims* d, const void* x, int act_dtype,
                  d->D, d->H, d->H_kv, d->d_h, rope_base, rope_scale, query_scale, s, st);
   if (e != cudaSuccess) return GEMMA3_ERR_CUDA;
   const int win = attn_type == GEMMA3_LOCAL_SLIDING ? window : 0;
+  void* sched = ws + w.q_bytes + w.kv_bytes + w.w_bytes;
   e = launch_flash_attention(qbuf, kvbuf, static_cast<uint8_t*>(kvbuf) + KVD * 2, 2 * KVD, qbuf,
-                             act_dtype, pad_lens, d->B, d->T, d->H, d->H_kv, d->d_h, win, s, st);
+                             act_dtype, pad_lens, d->B, d->T, d->H, d->H_kv, d->d_h, win, sched, s,
+                             st);
   if (e != cudaSuccess) return GEMMA3_ERR_CUDA;
   e = launch_linear(qbuf, HD, Wo, HD, out, d->D, M, d->D, HD, act_dtype, out_dtype, s, st, 0);
   return to_status(e);
@@ -556,7 +559,8 @@ CachedWs cached_ws(const gemma3_attn_dims* d, int S) {
   CachedWs w;
   w.q = round_up(M * d->H * d->d_h * 2, 256);
   w.kv = round_up(M * 2 * d->H_kv * d->d_h * 2, 256);
-  w.attn = round_up(cached_attention_ws_bytes(d->B, d->T, S, d->H, d->H_kv, d->d_h), 256);
+  w.attn = round_up(cached_attention_ws_bytes(d->B, d->T, S, d->H, d->H_kv, d->d_h), 256) +
+           kAttnSchedBytes;
   w.total = w.q + w.kv + w.attn;
   return w;
 }
@@ -626,7 +630,8 @@ int gemma3_attn_forward_cached(const gemma3_attn_dims* dims, int S, int end_inde
   cudaError_t e;
   if (end_index == 0 && attn_type == GEMMA3_GLOBAL && d->T >= kFlashPrefillMinT)
     e = launch_flash_attention(qbuf, kvbuf, kvbuf + KVD * 2, 2 * KVD, qbuf, kBF16, pad_lens, d->B,
-                               d->T, d->H, d->H_kv, d->d_h, 0, s, st);
+                               d->T, d->H, d->H_kv, d->d_h, 0, aws + w.attn - kAttnSchedBytes, s,
+                               st);
   else
     e = launch_cached_attention(qbuf, K_cache, V_cache, pos_cache, segment_pos, pad_lens, qbuf,
                                 kBF16, d->B, d->T, S, end_index, d->H, d->H_kv, d->d_h,
@@ -777,7 +782,7 @@ int gemma3_qk_norm_rope(void* Q, long ldq, void* K, long ldk, const void* gamma_
 
 int gemma3_flash_attention(const void* Q, const void* K, const void* V, long ldkv, void* O,
                            int o_dtype, const int32_t* pad_lens, int B, int T, int H, int H_kv,
-                           int d_h, int window, void* stream) {
+                           int d_h, int window, void* scratch, void* stream) {
   if (!Q || !K || !V || !O || B < 1 || T < 1 || H < 1 || H_kv < 1 || H % H_kv)
     return GEMMA3_ERR_INVALID_ARG;
   if (o_dtype != GEMMA3_BF16 && o_dtype != GEMMA3_F16) return GEMMA3_ERR_INVALID_ARG;
@@ -785,7 +790,8 @@ int gemma3_flash_attention(const void* Q, const void* K, const void* V, long ldk
   if ((d_h != 128 && d_h != 256) || (G != 1 && G != 2 && G != 4)) return GEMMA3_ERR_UNSUPPORTED;
   if (ldkv < static_cast<long>(H_kv) * d_h) return GEMMA3_ERR_INVALID_ARG;
   if (static_cast<long long>(B) * T >= (1LL << 31)) return GEMMA3_ERR_INVALID_ARG;
-  if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O) || (ldkv * 2) % 16)
+  if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O) || (ldkv * 2) % 16 ||
+      !aligned16(scratch))
     return GEMMA3_ERR_MISALIGNED;
   int rc = check_device();
   if (rc != GEMMA3_OK) return rc;
@@ -793,7 +799,7 @@ int gemma3_flash_attention(const void* Q, const void* K, const void* V, long ldk
   if (st == nullptr) return GEMMA3_ERR_CUDA;
   return to_status(launch_flash_attention(Q, K, V, ldkv, O, o_dtype == GEMMA3_F16 ? kF16 : kBF16,
                                           pad_lens, B, T, H, H_kv, d_h, window > 0 ? window : 0,
-                                          as_stream(stream), st));
+                                          scratch, as_stream(stream), st));
 }
 
 int gemma3_rmsnorm(const void* x, int x_dtype, const void* gamma, void* u, int u_dtype, int M,

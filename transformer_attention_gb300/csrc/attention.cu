@@ -57,8 +57,15 @@ constexpr float RESCALE_THRESHOLD = 8.0f;  // log2 units
 
 enum : int {
   kSiteQ = 11, kSiteKEmpty, kSiteVEmpty, kSiteKFull, kSiteSFree, kSitePFull, kSiteVFull,
-  kSiteSFull, kSiteORescale, kSitePFree, kSiteOFinal, kSiteRed
+  kSiteSFull, kSiteORescale, kSitePFree, kSiteOFinal, kSiteRed, kSiteSchedFull,
+  kSiteSchedEmpty
 };
+
+// Dynamic order: with a scheduler counter the K producer takes positions of
+// the heavy-first order from it (a CTA that is free takes the heaviest item
+// left) and hands them to the other roles through a ring in shared memory.
+constexpr int SCHED_SLOTS = 4;
+constexpr int SCHED_CONSUMERS = 2 + SM_WARPS;   // V producer, MMA issuer, softmax warps
 
 template <int DH, int G>
 struct Cfg {
@@ -131,7 +138,8 @@ __device__ __forceinline__ int item_position(int r) {
                   : static_cast<int>(blockIdx.x));
 }
 
-// Persistent: one CTA per SM walks the positions item_position(0, 1, ...).
+// Persistent: one CTA per SM walks the positions item_position(0, 1, ...), or
+// with `sched` the positions it takes from that counter (zeroed per launch).
 // All pipeline phases count tiles (g) and items globally, so the K/V rings
 // run ahead into the next item and the next item's Q is fetched as soon as
 // the current item's last S MMA has consumed the Q buffer.
@@ -141,7 +149,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
                     uint16_t* __restrict__ O, int o_f16,
                     const int32_t* __restrict__ pad_lens, int B, int T, int H, int H_kv,
-                    int window, int num_q_tiles, int gsz, int num_items, int* status) {
+                    int window, int num_q_tiles, int gsz, int num_items, unsigned int* sched,
+                    int* status) {
   using C = Cfg<DH, G>;
   // After a CTA of this or an earlier launch gave up, the rest do no work.
   if (*reinterpret_cast<volatile int*>(status) != 0) return;
@@ -162,6 +171,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   __shared__ __align__(1024) uint8_t ostage[SM_WARPS][32 * 64];
   __shared__ uint32_t tmem_sh;
   __shared__ int abort_flag;
+  __shared__ int sched_pos[SCHED_SLOTS];
+  __shared__ __align__(8) uint64_t sched_full[SCHED_SLOTS], sched_empty[SCHED_SLOTS];
 
   if (threadIdx.x == 0) {
     mbar_init(smem_u32(&q_full), 1);
@@ -183,6 +194,10 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_init(smem_u32(&pv_done[s]), 1);
     }
     for (int s = 0; s < 4; ++s) mbar_init(smem_u32(&red_bar[s]), 2);
+    for (int s = 0; s < SCHED_SLOTS; ++s) {
+      mbar_init(smem_u32(&sched_full[s]), 1);
+      mbar_init(smem_u32(&sched_empty[s]), SCHED_CONSUMERS);
+    }
     mbar_init(smem_u32(&o_final), 1);
     mbar_init(smem_u32(&o_free), SM_WARPS);
     mbar_init(smem_u32(&drain), 1);
@@ -201,13 +216,41 @@ __global__ void __launch_bounds__(THREADS, 1)
   tc_fence_after();
   const uint32_t tbase = tmem_sh;
 
+  // Position of round rr for the K producer (which takes it from the
+  // scheduler and publishes it) ...
+  auto fetch_pos = [&](int rr) -> int {
+    if (sched == nullptr) return item_position(rr);
+    const int slot = rr % SCHED_SLOTS;
+    if (rr >= SCHED_SLOTS && !mbar_wait(smem_u32(&sched_empty[slot]), ((rr / SCHED_SLOTS) - 1) & 1,
+                                        &abort_flag, status, kSiteSchedEmpty))
+      return num_items;
+    const int p = static_cast<int>(min(atomicAdd(sched, 1u), static_cast<unsigned>(num_items)));
+    *reinterpret_cast<volatile int*>(&sched_pos[slot]) = p;
+    mbar_arrive(smem_u32(&sched_full[slot]));
+    return p;
+  };
+  // ... and for every other role (a whole warp; lane 0 releases the slot).
+  auto take_pos = [&](int rr) -> int {
+    if (sched == nullptr) return item_position(rr);
+    const int slot = rr % SCHED_SLOTS;
+    if (!mbar_wait(smem_u32(&sched_full[slot]), (rr / SCHED_SLOTS) & 1, &abort_flag, status,
+                   kSiteSchedFull))
+      return num_items;
+    const int p = *reinterpret_cast<volatile int*>(&sched_pos[slot]);
+    return p;
+  };
+  auto release_pos = [&](int rr) {
+    if (sched == nullptr) return;
+    mbar_arrive(smem_u32(&sched_empty[rr % SCHED_SLOTS]));
+  };
+
   if (warp == 0) {
     if (lane == 0) {
       // ---------------- producer: Q of each item, then its K tiles
       int fills[C::KS] = {};
       int f = 0, nq = 0;
       bool ok = true;
-      for (int rr = 0, pos; ok && (pos = item_position(rr)) < num_items; ++rr) {
+      for (int rr = 0, pos; ok && (pos = fetch_pos(rr)) < num_items; ++rr) {
         const Item it = decode_item<C::TQ>(pos, num_q_tiles, gsz, B, H_kv, T, window, pad_lens);
         if (it.pad) continue;
         // The Q buffer is free once the previous item's last S MMA is done.
@@ -242,7 +285,10 @@ __global__ void __launch_bounds__(THREADS, 1)
       int fills[C::VS] = {};
       int f = 0;
       bool ok = true;
-      for (int rr = 0, pos; ok && (pos = item_position(rr)) < num_items; ++rr) {
+      for (int rr = 0;; ++rr) {
+        const int pos = take_pos(rr);
+        release_pos(rr);
+        if (pos >= num_items) break;
         const Item it = decode_item<C::TQ>(pos, num_q_tiles, gsz, B, H_kv, T, window, pad_lens);
         for (int i = 0; i < it.n_tiles; ++i, ++f) {
           const int st = f % C::VS;
@@ -294,7 +340,10 @@ __global__ void __launch_bounds__(THREADS, 1)
       };
       bool ok = true;
       int g = 0;
-      for (int rr = 0, pos; ok && (pos = item_position(rr)) < num_items; ++rr) {
+      for (int rr = 0; ok; ++rr) {
+        const int pos = take_pos(rr);
+        release_pos(rr);
+        if (pos >= num_items) break;
         const Item it = decode_item<C::TQ>(pos, num_q_tiles, gsz, B, H_kv, T, window, pad_lens);
         if (it.pad) continue;
         if (!mbar_wait(smem_u32(&q_full), nitem & 1, &abort_flag, status, kSiteQ)) break;
@@ -347,7 +396,12 @@ __global__ void __launch_bounds__(THREADS, 1)
     const uint32_t rbar = smem_u32(&red_bar[q]);
     int g = 0, nitem = 0, hs = 0;   // global tile, items, handshakes
     bool ok = true;
-    for (int rr = 0, pos; ok && (pos = item_position(rr)) < num_items; ++rr) {
+    for (int rr = 0; ok; ++rr) {
+      int pos = take_pos(rr);
+      pos = __shfl_sync(0xffffffffu, pos, 0);
+      __syncwarp();
+      if (lane == 0) release_pos(rr);
+      if (pos >= num_items) break;
       const Item it = decode_item<C::TQ>(pos, num_q_tiles, gsz, B, H_kv, T, window, pad_lens);
       if (it.pad) {
         // The whole tile is padding: its output rows are zero (bits 0 in bf16 and f16).
@@ -546,7 +600,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 template <int DH, int G>
 cudaError_t launch_cfg(const void* Q, const void* K, const void* V, long ldkv, void* O,
                        int o_dtype, const int32_t* pad_lens, int B, int T, int H, int H_kv,
-                       int window, cudaStream_t stream, int* status) {
+                       int window, unsigned int* sched, cudaStream_t stream, int* status) {
   using C = Cfg<DH, G>;
   CUtensorMap tq, tk, tv;
   // Q' [B, T, H, d_h]: box {64 of d_h, the G heads of one group, TQ tokens, 1}.
@@ -588,10 +642,12 @@ cudaError_t launch_cfg(const void* Q, const void* K, const void* V, long ldkv, v
   const double kv_bytes = static_cast<double>(T) * DH * 2.0 * 2.0;
   int gsz = window > 0 ? B * H_kv : static_cast<int>(48.0 * 1024 * 1024 / kv_bytes);
   gsz = gsz < 1 ? 1 : (gsz > B * H_kv ? B * H_kv : gsz);
+  if (sched != nullptr && cudaMemsetAsync(sched, 0, sizeof(unsigned int), stream) != cudaSuccess)
+    return cudaErrorUnknown;
   kern<<<grid, THREADS, C::SMEM, stream>>>(tq, tk, tv, to, static_cast<uint16_t*>(O),
                                            o_dtype == kF16 ? 1 : 0, pad_lens, B, T, H, H_kv,
                                            window, num_q_tiles, gsz, static_cast<int>(items),
-                                           status);
+                                           sched, status);
   return cudaGetLastError();
 }
 
@@ -599,15 +655,15 @@ cudaError_t launch_cfg(const void* Q, const void* K, const void* V, long ldkv, v
 
 cudaError_t launch_flash_attention(const void* Q, const void* K, const void* V, long ldkv,
                                    void* O, int o_dtype, const int32_t* pad_lens, int B, int T,
-                                   int H, int H_kv, int d_h, int window, cudaStream_t stream,
-                                   int* status) {
+                                   int H, int H_kv, int d_h, int window, void* sched,
+                                   cudaStream_t stream, int* status) {
   if (B <= 0 || T <= 0) return cudaSuccess;
   if (o_dtype != kBF16 && o_dtype != kF16) return cudaErrorInvalidValue;
   const int G = H / H_kv;
 #define G3_ATTN_CASE(DH_, G_)                                                                   \
   if (d_h == DH_ && G == G_)                                                                    \
-    return launch_cfg<DH_, G_>(Q, K, V, ldkv, O, o_dtype, pad_lens, B, T, H, H_kv, window, stream, \
-                               status);
+    return launch_cfg<DH_, G_>(Q, K, V, ldkv, O, o_dtype, pad_lens, B, T, H, H_kv, window,        \
+                               static_cast<unsigned int*>(sched), stream, status);
   G3_ATTN_CASE(256, 1)
   G3_ATTN_CASE(256, 2)
   G3_ATTN_CASE(256, 4)

@@ -58,11 +58,14 @@ cudaError_t launch_qk_norm_rope(void* Q, long ldq, void* K, long ldk, const void
 // Flash attention forward over Q' [B,T,H,d_h] fp16 and K'/V rows of an fp16
 // buffer with row stride ldkv (K' at column j*d_h, V at column v_off + j*d_h).
 // Writes O [B,T,H,d_h] in o_dtype (bf16|f16; may alias Q'); rows past the
-// valid length are 0.
+// valid length are 0.  sched: kAttnSchedBytes of device scratch for the
+// dynamic work order (zeroed here before the launch), or null for the
+// static order.
+constexpr size_t kAttnSchedBytes = 256;
 cudaError_t launch_flash_attention(const void* Q, const void* K, const void* V, long ldkv,
                                    void* O, int o_dtype, const int32_t* pad_lens, int B, int T,
-                                   int H, int H_kv, int d_h, int window, cudaStream_t stream,
-                                   int* status);
+                                   int H, int H_kv, int d_h, int window, void* sched,
+                                   cudaStream_t stream, int* status);
 
 // u[m,:] = RMSNorm(x[m,:]) * (1 + gamma) over D, x in x_dtype (bf16|f32), u in
 // u_dtype (bf16|f16).
