@@ -256,7 +256,8 @@ def run_gpu(args, world, rank, local):
         work["rmsnorm"] += metrics.rmsnorm_bytes(M, D, 4)
         work["embed"] = float(M * D * (2 + 4) + M * 4)
     nl = w.num_layers
-    launches = {"linear": (5 if ffn else 3) * nl + (1 if model else 0), "attention": nl,
+    launches = {"linear": ((4 if ffn else 2) + (1 if not fused_qk else 0)) * nl
+                + (1 if model else 0), "attention": nl,
                 "qk_norm_rope": 0 if fused_qk else nl,
                 "rmsnorm": (2 if ffn else 1) * nl if stack else 0,
                 "postnorm": (2 if ffn else 1) * nl if stack else 0,
@@ -304,17 +305,13 @@ def run_gpu(args, world, rank, local):
                 done("cast", e)
                 a_in, act, wq, wkv, wo = u, G3.GEMMA3_F16, wq16, wkv16, wo16
             if fused_qk:
-                # QK-norm, RoPE and the query scale in the projection epilogue
+                # one launch for both projections, QK-norm, RoPE and the
+                # query scale in its epilogue
                 e = mark("linear")
-                G3.gemma3_linear_qk_norm_rope(a_in, D, wq, D, qbuf, HD, M, HD, D, act,
-                                              L.p["gamma_q"], pos, d_h, HD, L.rope_base,
-                                              L.rope_scale, alpha)
-                done("proj_q", e)
-                e = mark("linear")
-                G3.gemma3_linear_qk_norm_rope(a_in, D, wkv, D, kvbuf, 2 * KVD, M, 2 * KVD, D, act,
-                                              L.p["gamma_k"], pos, d_h, KVD, L.rope_base,
-                                              L.rope_scale, 1.0)
-                done("proj_kv", e)
+                G3.gemma3_qkv_proj_norm_rope(a_in, D, wq, wkv, qbuf, kvbuf, M, D, H, H_kv, d_h, act,
+                                             L.p["gamma_q"], L.p["gamma_k"], pos, L.rope_base,
+                                             L.rope_scale, alpha)
+                done("proj_qkv", e)
             else:
                 e = mark("linear")
                 G3.gemma3_linear(a_in, D, wq, D, qbuf, HD, M, HD, D, act, G3.GEMMA3_F16)
@@ -407,8 +404,8 @@ def run_gpu(args, world, rank, local):
     dev_seconds = sum(step_ms) / 1e3
     value, max_seconds = whole_job_value(tokens * args.steps, dev_seconds, world, dev)
     kern_ms = {k: sum(a.elapsed_time(b) for a, b in v) for k, v in events.items()}
-    gemm_names = (("proj_q", "proj_kv", "proj_o") + (("ffn_geglu", "ffn_down") if ffn else ())
-                  + (("read_out",) if model else ()))
+    gemm_names = ((("proj_qkv",) if fused_qk else ("proj_q", "proj_kv")) + ("proj_o",)
+                  + (("ffn_geglu", "ffn_down") if ffn else ()) + (("read_out",) if model else ()))
     proj_ms = {k: sum(a.elapsed_time(b) for a, b in events[k]) / args.steps for k in gemm_names}
     kern_ms["linear"] = sum(kern_ms.pop(k, 0.0) for k in gemm_names)
 
@@ -450,8 +447,9 @@ def run_gpu(args, world, rank, local):
     if ffn:
         gf["ffn_geglu"] = 2.0 * M * (2 * w.d_ff) * D
         gf["ffn_down"] = 2.0 * M * D * w.d_ff
-    for k, name in (("proj_q", "q_proj"), ("proj_kv", "kv_proj"), ("proj_o", "o_proj"),
-                    ("ffn_geglu", "ffn_geglu"), ("ffn_down", "ffn_down")):
+    gf["qkv_proj"] = gf["q_proj"] + gf["kv_proj"]
+    for k, name in (("proj_q", "q_proj"), ("proj_kv", "kv_proj"), ("proj_qkv", "qkv_proj"),
+                    ("proj_o", "o_proj"), ("ffn_geglu", "ffn_geglu"), ("ffn_down", "ffn_down")):
         if k in proj_ms:
             breakdown[k] = {"ms_per_step": proj_ms[k],
                             "tflops": gf[name] * w.num_layers / (proj_ms[k] / 1e3) / 1e12}

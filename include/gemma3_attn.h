@@ -344,6 +344,21 @@ int gemma3_linear(const void* A, long lda, const void* W, long ldw, void* C, lon
 int gemma3_geglu(const void* A, long lda, const void* W_gating, long ldw, void* Z, long ldz,
                  int M, int D_ff, int K, int in_dtype, void* stream);
 
+/* Q' [M, H*d_h] and [K'|V] [M, 2*H_kv*d_h] (fp16, row strides H*d_h and
+ * 2*H_kv*d_h) of M token rows x [M, D] (row stride ldx) in in_dtype: the Q and
+ * KV projections ([AB] Projections) with QK-norm, RoPE and the query scale
+ * ([QK] How it works; [AB] QK-norm, then RoPE, then scale), exactly the first
+ * stage of gemma3_attn_forward.  When H*d_h and H_kv*d_h are multiples of 256
+ * and M > 16 this is one GEMM launch whose epilogue normalises and rotates
+ * the head vectors from the fp32 accumulator (each tile of x feeds both
+ * projections); otherwise the two projections and gemma3_qk_norm_rope.
+ * Wq [H*d_h, D], Wkv [2, H_kv*d_h, D] and x in in_dtype; gamma bf16 [d_h]. */
+int gemma3_qkv_proj_norm_rope(const void* x, long ldx, const void* Wq, const void* Wkv, void* Q,
+                              void* KV, int M, int D, int H, int H_kv, int d_h, int in_dtype,
+                              const void* gamma_q, const void* gamma_k, const int32_t* pos,
+                              double rope_base, double rope_scale, float query_scale,
+                              void* stream);
+
 /* C[M, N] fp16 = A W^T with the attention prologue fused into the GEMM
  * epilogue (what gemma3_linear followed by gemma3_qk_norm_rope computes, but
  * from the fp32 accumulator, without the fp16 round trip): columns [0,

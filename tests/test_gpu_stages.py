@@ -144,6 +144,38 @@ def test_linear_qk_norm_rope_matches_oracle(M, D, d_h, H, H_kv, base, scale, alp
     assert rel_frob(kv[:, KVD:], O.project(x, Wkv[1])) <= 1e-3
 
 
+@pytest.mark.parametrize("M,D,d_h,H,H_kv,base,scale,alpha", [
+    (300, 1152, 256, 4, 1, 1e6, 1.0, 256 ** -0.5),     # one launch, Q 4 tiles + K|V 2 tiles
+    (777, 640, 128, 32, 16, 1e6, 8.0, 168 ** -0.5),    # one launch, two heads per tile
+    (9, 256, 256, 8, 4, 1e4, 1.0, 256 ** -0.5),        # <= 16 rows: projections + prologue
+    (40, 256, 128, 2, 1, 1e4, 1.0, 128 ** -0.5),       # K|V width 256 is one tile, K 128
+])
+def test_qkv_proj_norm_rope_matches_oracle(M, D, d_h, H, H_kv, base, scale, alpha):
+    """The whole first stage (both projections with the prologue) against the
+    oracle's normalised and rotated Q/K and its V projection."""
+    import transformer_attention_gb300 as G3
+    HD, KVD = H * d_h, H_kv * d_h
+    x = _randn((M, D), 40, 1.0)
+    Wq = _randn((HD, D), 41, D ** -0.5)
+    Wkv = _randn((2, KVD, D), 42, D ** -0.5)
+    gq = _randn((d_h,), 43, 0.1 ** 0.5)
+    gk = _randn((d_h,), 44, 0.1 ** 0.5)
+    g = torch.Generator().manual_seed(45)
+    pos = torch.randint(0, 131072, (M,), generator=g).to(torch.int32)
+    Qd = torch.empty((M, HD), dtype=torch.float16, device="cuda")
+    KVd = torch.empty((M, 2 * KVD), dtype=torch.float16, device="cuda")
+    G3.gemma3_qkv_proj_norm_rope(x.cuda(), D, Wq.cuda(), Wkv.cuda(), Qd, KVd, M, D, H, H_kv, d_h,
+                                 G3.GEMMA3_BF16, gq.cuda(), gk.cuda(), pos.cuda(), base, scale,
+                                 alpha)
+    assert G3.gemma3_attn_check_status() == 0
+    q_ref, k_ref = O.normalised_rotated_qk(x, pos, Wq, Wkv, gq, gk, H=H, H_kv=H_kv, d_h=d_h,
+                                           rope_base=base, rope_scale=scale)
+    kv = KVd.cpu()
+    assert max_abs(Qd.cpu().reshape(M, H, d_h).to(F64) / alpha, q_ref) <= QK_MAX_ABS
+    assert max_abs(kv[:, :KVD].reshape(M, H_kv, d_h), k_ref) <= QK_MAX_ABS
+    assert rel_frob(kv[:, KVD:], O.project(x, Wkv[1])) <= 1e-3
+
+
 def test_linear_qk_norm_rope_rejects_unaligned_heads():
     import transformer_attention_gb300 as G3
     x = torch.zeros((64, 64), dtype=torch.bfloat16, device="cuda")

@@ -16,7 +16,7 @@ from ._lib import (  # noqa: F401  (re-exported C-ABI names)
     gemma3_cast_bf16_f16, gemma3_geglu,
     gemma3_flash_attention,
     gemma3_last_device_status, gemma3_layer_attn_type, gemma3_layer_config, gemma3_linear,
-    gemma3_linear_qk_norm_rope, gemma3_embed, gemma3_model_forward, gemma3_model_workspace_size,
+    gemma3_linear_qk_norm_rope, gemma3_qkv_proj_norm_rope, gemma3_embed, gemma3_model_forward, gemma3_model_workspace_size,
     GEMMA3_ERR_BAD_INPUT,
     gemma3_postnorm_residual, gemma3_qk_norm_rope, gemma3_query_scale, gemma3_rmsnorm,
     gemma3_selftest_wait_timeout, lib)

@@ -98,6 +98,10 @@ SIGNATURES = {
                              c_int, c_int, c_void_p]),
     "gemma3_linear": (c_int, [c_void_p, c_long, c_void_p, c_long, c_void_p, c_long, c_int, c_int,
                               c_int, c_int, c_int, c_int, c_void_p]),
+    "gemma3_qkv_proj_norm_rope": (c_int, [c_void_p, c_long, c_void_p, c_void_p, c_void_p,
+                                          c_void_p, c_int, c_int, c_int, c_int, c_int, c_int,
+                                          c_void_p, c_void_p, c_void_p, c_double, c_double,
+                                          c_float, c_void_p]),
     "gemma3_linear_qk_norm_rope": (c_int, [c_void_p, c_long, c_void_p, c_long, c_void_p, c_long,
                                            c_int, c_int, c_int, c_int, c_void_p, c_void_p, c_int,
                                            c_int, c_double, c_double, c_float, c_void_p]),
@@ -363,6 +367,14 @@ def gemma3_linear(A, lda, W, ldw, C, ldc, M, N, K, in_dtype, out_dtype, max_ctas
                   stream=None):
     return _check("gemma3_linear", lib().gemma3_linear(
         _ptr(A), lda, _ptr(W), ldw, _ptr(C), ldc, M, N, K, in_dtype, out_dtype, max_ctas,
+        _stream(stream)))
+
+
+def gemma3_qkv_proj_norm_rope(x, ldx, Wq, Wkv, Q, KV, M, D, H, H_kv, d_h, in_dtype, gamma_q,
+                              gamma_k, pos, rope_base, rope_scale, query_scale, stream=None):
+    return _check("gemma3_qkv_proj_norm_rope", lib().gemma3_qkv_proj_norm_rope(
+        _ptr(x), ldx, _ptr(Wq), _ptr(Wkv), _ptr(Q), _ptr(KV), M, D, H, H_kv, d_h, in_dtype,
+        _ptr(gamma_q), _ptr(gamma_k), _ptr(pos), rope_base, rope_scale, query_scale,
         _stream(stream)))
 
 

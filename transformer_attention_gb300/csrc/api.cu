@@ -84,23 +84,20 @@ AttnWs attn_ws(const gemma3_attn_dims* d, bool f16_weights = false) {
   return w;
 }
 
-// Q' and [K'|V] of M token rows: the Q / KV projections with QK-norm, RoPE
-// and the query scale fused into the GEMM epilogue when the head vectors
-// tile the 256-wide output tiles (every Gemma 3 shape with more than 16
-// rows), else the projections followed by the prologue kernel.
+// Q' and [K'|V] of M token rows: the Q and KV projections in one GEMM launch
+// with QK-norm, RoPE and the query scale fused into its epilogue when the
+// head vectors tile the 256-wide output tiles (every Gemma 3 shape with more
+// than 16 rows), else the two projections followed by the prologue kernel.
 cudaError_t project_qk(const void* x, long ldx, int act_dtype, const void* Wq, const void* Wkv,
                        void* qbuf, void* kvbuf, const void* gamma_q, const void* gamma_k,
                        const int32_t* pos, int M, int D, int H, int H_kv, int d_h,
                        double rope_base, double rope_scale, float query_scale, cudaStream_t s,
                        int* st) {
   const int HD = H * d_h, KVD = H_kv * d_h;
-  if (linear_qknorm_fusable(M, HD, HD, d_h) && linear_qknorm_fusable(M, 2 * KVD, KVD, d_h)) {
-    cudaError_t e = launch_linear_qknorm(x, ldx, Wq, D, qbuf, HD, M, HD, D, act_dtype, gamma_q, pos,
-                                         d_h, HD, rope_base, rope_scale, query_scale, s, st);
-    if (e != cudaSuccess) return e;
-    return launch_linear_qknorm(x, ldx, Wkv, D, kvbuf, 2 * KVD, M, 2 * KVD, D, act_dtype, gamma_k,
-                                pos, d_h, KVD, rope_base, rope_scale, 1.f, s, st);
-  }
+  if (linear_qknorm_fusable(M, HD, HD, d_h) && linear_qknorm_fusable(M, 2 * KVD, KVD, d_h))
+    return launch_qkv_qknorm(x, ldx, Wq, Wkv, D, qbuf, HD, kvbuf, 2 * KVD, M, HD, KVD, D, act_dtype,
+                             gamma_q, gamma_k, pos, d_h, rope_base, rope_scale, query_scale, s,
+                             st);
   cudaError_t e = launch_linear(x, ldx, Wq, D, qbuf, HD, M, HD, D, act_dtype, kF16, s, st, 0);
   if (e != cudaSuccess) return e;
   e = launch_linear(x, ldx, Wkv, D, kvbuf, 2 * KVD, M, 2 * KVD, D, act_dtype, kF16, s, st, 0);
@@ -728,6 +725,30 @@ int gemma3_linear(const void* A, long lda, const void* W, long ldw, void* C, lon
   const int dt = out_dtype == GEMMA3_F32 ? kF32 : (out_dtype == GEMMA3_F16 ? kF16 : kBF16);
   return to_status(launch_linear(A, lda, W, ldw, C, ldc, M, N, K, it, dt, as_stream(stream), st,
                                  max_ctas));
+}
+
+int gemma3_qkv_proj_norm_rope(const void* x, long ldx, const void* Wq, const void* Wkv, void* Q,
+                              void* KV, int M, int D, int H, int H_kv, int d_h, int in_dtype,
+                              const void* gamma_q, const void* gamma_k, const int32_t* pos,
+                              double rope_base, double rope_scale, float query_scale,
+                              void* stream) {
+  if (!x || !Wq || !Wkv || !Q || !KV || !gamma_q || !gamma_k || !pos || M < 0 || D < 8 ||
+      D % 8 || H < 1 || H_kv < 1)
+    return GEMMA3_ERR_INVALID_ARG;
+  if (d_h != 128 && d_h != 256) return GEMMA3_ERR_UNSUPPORTED;
+  if (in_dtype != GEMMA3_BF16 && in_dtype != GEMMA3_F16) return GEMMA3_ERR_INVALID_ARG;
+  if (ldx < D) return GEMMA3_ERR_INVALID_ARG;
+  if (!(rope_base > 0.0) || !(rope_scale > 0.0)) return GEMMA3_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(Wq) || !aligned16(Wkv) || !aligned16(Q) || !aligned16(KV) ||
+      !aligned16(gamma_q) || !aligned16(gamma_k) || (ldx * 2) % 16)
+    return GEMMA3_ERR_MISALIGNED;
+  int rc = check_device();
+  if (rc != GEMMA3_OK) return rc;
+  int* st = status_ptr();
+  if (st == nullptr) return GEMMA3_ERR_CUDA;
+  return to_status(project_qk(x, ldx, in_dtype == GEMMA3_F16 ? kF16 : kBF16, Wq, Wkv, Q, KV,
+                              gamma_q, gamma_k, pos, M, D, H, H_kv, d_h, rope_base, rope_scale,
+                              query_scale, as_stream(stream), st));
 }
 
 int gemma3_linear_qk_norm_rope(const void* A, long lda, const void* W, long ldw, void* C,

@@ -66,12 +66,18 @@ enum : int { kEpiPlain = 0, kEpiGeglu = 1, kEpiQkNorm = 2 };
 // Arguments of the QK-norm + RoPE epilogue: columns [0, n_norm) of C are head
 // vectors (d_h each) to normalise with (1 + gamma), rotate at pos[row] and
 // multiply by scale; columns from n_norm on are converted as they are.
+// n1 > 0 splits the output columns in two segments with their own weight
+// and output maps (tmB2 / tmC2 for columns n1..): the Q projection (segment
+// 0, gamma / scale / n_norm) and the KV projection (segment 1, gamma2 /
+// scale2 / n_norm2, counted from the segment's first column) in one launch,
+// so each tile of x feeds both.
 struct QkEpi {
   RopeFreqs freqs;
   const __nv_bfloat16* gamma;
+  const __nv_bfloat16* gamma2;
   const int32_t* pos;
-  int n_norm;
-  float scale;
+  int n_norm, n_norm2, n1;
+  float scale, scale2;
 };
 
 template <typename T>
@@ -98,7 +104,8 @@ __device__ __forceinline__ float gelu_tanh_mul(float g, float u) {
 template <int AB_BF16, typename OutT, int EPI, int DH>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_tn_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const __grid_constant__ CUtensorMap tmC, int M, int N, int K, int* status,
+                   const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmB2,
+                   const __grid_constant__ CUtensorMap tmC2, int M, int N, int K, int* status,
                    const __grid_constant__ QkEpi epi) {
   constexpr bool GEGLU = EPI == kEpiGeglu;
   static_assert(EPI != kEpiQkNorm || (std::is_same<OutT, __half>::value && (DH == 128 || DH == 256)),
@@ -135,6 +142,10 @@ __global__ void __launch_bounds__(THREADS, 1)
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
     tma_prefetch_desc(&tmC);
+    if (epi.n1 > 0) {
+      tma_prefetch_desc(&tmB2);
+      tma_prefetch_desc(&tmC2);
+    }
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(&tmem_base_sh), TMEM_COLS);
@@ -168,6 +179,8 @@ __global__ void __launch_bounds__(THREADS, 1)
             // gate rows n0.. into the first 128 B-tile rows, up rows N + n0.. after them
             tma_load_2d(smem_u32(sa + A_BYTES), &tmB, fb, kb * BK, n0);
             tma_load_2d(smem_u32(sa + A_BYTES + B_BYTES / 2), &tmB, fb, kb * BK, N + n0);
+          } else if (epi.n1 > 0 && n0 >= epi.n1) {
+            tma_load_2d(smem_u32(sa + A_BYTES), &tmB2, fb, kb * BK, n0 - epi.n1);
           } else {
             tma_load_2d(smem_u32(sa + A_BYTES), &tmB, fb, kb * BK, n0);
           }
@@ -234,7 +247,11 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (!ok) break;
       tc_fence_after();
       const uint32_t acc = tbase + lane_off + abuf * BN;
-      // Stage one 32-row x 128-byte chunk of this warp and store it with TMA.
+      const bool seg1 = epi.n1 > 0 && n0 >= epi.n1;     // second output segment
+      const int col_off = seg1 ? epi.n1 : 0;              // its first global column
+      const CUtensorMap* tcp = seg1 ? &tmC2 : &tmC;
+      // Stage one 32-row x 128-byte chunk of this warp and store it with TMA
+      // (col0 is a global column of C).
       auto stage_store = [&](const uint32_t (&w)[32], int col0) {
         // The staging buffer used two chunks ago must have been read by its store.
         uint8_t* buf = staging + (nchunk & 1) * STAGING_BYTES;
@@ -248,7 +265,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-          tma_store_2d(&tmC, smem_u32(buf), col0, m0 + q * 32);
+          tma_store_2d(tcp, smem_u32(buf), col0 - col_off, m0 + q * 32);
           bulk_commit_group();
         }
         ++nchunk;
@@ -260,7 +277,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (lane == 0) mbar_arrive(smem_u32(&acce_bar[abuf]));
       };
       bool fused = false;
-      if constexpr (EPI == kEpiQkNorm) fused = n0 < epi.n_norm;   // warp-uniform
+      if constexpr (EPI == kEpiQkNorm)   // warp-uniform
+        fused = seg1 ? (n0 - col_off) < epi.n_norm2 : n0 < epi.n_norm;
       if constexpr (EPI == kEpiQkNorm) {
         if (fused) {
           constexpr int HALF = DH / 2;
@@ -268,6 +286,8 @@ __global__ void __launch_bounds__(THREADS, 1)
           constexpr int PAIRS = HALF / 64;    // 64-column chunk pairs per head
           const int row = m0 + q * 32 + lane;
           const float p = row < M ? static_cast<float>(__ldg(epi.pos + row)) : 0.f;
+          const __nv_bfloat16* gam = seg1 ? epi.gamma2 : epi.gamma;
+          const float sc_seg = seg1 ? epi.scale2 : epi.scale;
           float rs[HEADS];
 #pragma unroll
           for (int e = 0; e < HEADS; ++e) {
@@ -314,12 +334,12 @@ __global__ void __launch_bounds__(THREADS, 1)
                     const int j = i * 64 + h * 32 + t + v;   // pair index within the head
                     float sn, cs;
                     rope_sincos(p, epi.freqs.f[j], sn, cs);
-                    const float g1 = 1.f + __bfloat162float(epi.gamma[j]);
-                    const float g2 = 1.f + __bfloat162float(epi.gamma[j + HALF]);
+                    const float g1 = 1.f + __bfloat162float(gam[j]);
+                    const float g2 = 1.f + __bfloat162float(gam[j + HALF]);
                     const float y1 = __uint_as_float(x1[t + v]) * rs[e] * g1;
                     const float y2 = __uint_as_float(x2[t + v]) * rs[e] * g2;
-                    o1[v] = (y1 * cs - y2 * sn) * epi.scale;
-                    o2[v] = (y2 * cs + y1 * sn) * epi.scale;
+                    o1[v] = (y1 * cs - y2 * sn) * sc_seg;
+                    o2[v] = (y2 * cs + y1 * sn) * sc_seg;
                   }
                   wa[t / 2] = pack_half2(o1[0], o1[1]);
                   wb[t / 2] = pack_half2(o2[0], o2[1]);
@@ -342,8 +362,11 @@ __global__ void __launch_bounds__(THREADS, 1)
               fence_proxy_async_smem();
               __syncwarp();
               if (lane == 0) {
-                tma_store_2d(&tmC, smem_u32(buf_a), n0 + ca * 64, m0 + q * 32);
-                tma_store_2d(&tmC, smem_u32(buf_b), n0 + cb * 64, m0 + q * 32);
+                // one bulk group per buffer: a plain chunk that follows waits
+                // for all but the newest group, i.e. for buffer 0's store
+                tma_store_2d(tcp, smem_u32(buf_a), n0 - col_off + ca * 64, m0 + q * 32);
+                bulk_commit_group();
+                tma_store_2d(tcp, smem_u32(buf_b), n0 - col_off + cb * 64, m0 + q * 32);
                 bulk_commit_group();
               }
               nchunk += 2;
@@ -406,10 +429,13 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
 }
 
+// C (and, for a split launch, the second segment's C2 with ldc2 and the
+// second weight map tb2; epi.n1 > 0) as 32-row x 128-byte TMA tiles.
 template <int AB_BF16, typename OutT, int EPI = kEpiPlain, int DH = 0>
 cudaError_t launch_typed(const CUtensorMap& ta, const CUtensorMap& tb, void* C, long ldc, int M,
                          int N, int K, cudaStream_t stream, int* status, int max_ctas,
-                         const QkEpi& epi = QkEpi{}) {
+                         const QkEpi& epi = QkEpi{}, const CUtensorMap* tb2 = nullptr,
+                         void* C2 = nullptr, long ldc2 = 0) {
   constexpr bool GEGLU = EPI == kEpiGeglu;
   auto kern = gemm_tn_kernel<AB_BF16, OutT, EPI, DH>;
   // Output tile map: boxes of 32 rows x 128 bytes, 128-byte swizzle.
@@ -418,10 +444,18 @@ cudaError_t launch_typed(const CUtensorMap& ta, const CUtensorMap& tb, void* C, 
                                   : std::is_same<OutT, __half>::value
                                       ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
                                       : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-  const uint64_t cdims[2] = {static_cast<uint64_t>(N), static_cast<uint64_t>(M)};
+  const uint64_t n_seg0 = epi.n1 > 0 ? static_cast<uint64_t>(epi.n1) : static_cast<uint64_t>(N);
+  const uint64_t cdims[2] = {n_seg0, static_cast<uint64_t>(M)};
   const uint64_t cstr[1] = {static_cast<uint64_t>(ldc) * sizeof(OutT)};
   const uint32_t cbox[2] = {static_cast<uint32_t>(128 / sizeof(OutT)), 32};
   if (!encode_tiled(&tc, cdt, 2, C, cdims, cstr, cbox)) return cudaErrorInvalidValue;
+  CUtensorMap tc2 = tc;
+  if (epi.n1 > 0) {
+    const uint64_t cdims2[2] = {static_cast<uint64_t>(N - epi.n1), static_cast<uint64_t>(M)};
+    const uint64_t cstr2[1] = {static_cast<uint64_t>(ldc2) * sizeof(OutT)};
+    if (tb2 == nullptr || C2 == nullptr || !encode_tiled(&tc2, cdt, 2, C2, cdims2, cstr2, cbox))
+      return cudaErrorInvalidValue;
+  }
   static bool attr_set = false;  // benign race: setting the same attribute twice is harmless
   if (!attr_set) {
     cudaError_t e =
@@ -434,7 +468,8 @@ cudaError_t launch_typed(const CUtensorMap& ta, const CUtensorMap& tb, void* C, 
   int grid = num_sms();
   if (max_ctas > 0 && max_ctas < grid) grid = max_ctas;
   if (tiles < grid) grid = tiles;
-  kern<<<grid, THREADS, SMEM_BYTES, stream>>>(ta, tb, tc, M, N, K, status, epi);
+  kern<<<grid, THREADS, SMEM_BYTES, stream>>>(ta, tb, tc, tb2 != nullptr ? *tb2 : tb, tc2, M, N,
+                                               K, status, epi);
   return cudaGetLastError();
 }
 
@@ -493,6 +528,42 @@ cudaError_t launch_geglu(const void* A, long lda, const void* Wgu, long ldw, voi
 bool linear_qknorm_fusable(int M, int N, int n_norm, int d_h) {
   return M > kSkinnyMaxRows && (d_h == 128 || d_h == 256) && n_norm > 0 && n_norm <= N &&
          n_norm % BN == 0;
+}
+
+cudaError_t launch_qkv_qknorm(const void* A, long lda, const void* Wq, const void* Wkv, long ldw,
+                              void* Qout, long ldq, void* KVout, long ldkv, int M, int HD, int KVD,
+                              int K, int in_dtype, const void* gamma_q, const void* gamma_k,
+                              const int32_t* pos, int d_h, double rope_base, double rope_scale,
+                              float query_scale, cudaStream_t stream, int* status) {
+  if (M <= 0 || K <= 0) return cudaSuccess;
+  if (in_dtype != kBF16 && in_dtype != kF16) return cudaErrorInvalidValue;
+  if (!linear_qknorm_fusable(M, HD, HD, d_h) || !linear_qknorm_fusable(M, 2 * KVD, KVD, d_h))
+    return cudaErrorInvalidValue;
+  CUtensorMap ta, tb, ta2, tb2;
+  if (!encode_ab(ta, tb, A, lda, Wq, ldw, M, HD, K, in_dtype, BN) ||
+      !encode_ab(ta2, tb2, A, lda, Wkv, ldw, M, 2 * KVD, K, in_dtype, BN))
+    return cudaErrorInvalidValue;
+  QkEpi epi{};
+  epi.freqs = make_rope_freqs(d_h, rope_base, rope_scale);
+  epi.gamma = static_cast<const __nv_bfloat16*>(gamma_q);
+  epi.gamma2 = static_cast<const __nv_bfloat16*>(gamma_k);
+  epi.pos = pos;
+  epi.n_norm = HD;
+  epi.n_norm2 = KVD;
+  epi.n1 = HD;
+  epi.scale = query_scale;
+  epi.scale2 = 1.f;
+  const int N = HD + 2 * KVD;
+#define G3_QKV(AB, DH_)                                                                        \
+  return launch_typed<AB, __half, kEpiQkNorm, DH_>(ta, tb, Qout, ldq, M, N, K, stream, status, 0, \
+                                                   epi, &tb2, KVout, ldkv);
+  if (in_dtype == kBF16) {
+    if (d_h == 256) G3_QKV(1, 256)
+    G3_QKV(1, 128)
+  }
+  if (d_h == 256) G3_QKV(0, 256)
+  G3_QKV(0, 128)
+#undef G3_QKV
 }
 
 cudaError_t launch_linear_qknorm(const void* A, long lda, const void* W, long ldw, void* C,

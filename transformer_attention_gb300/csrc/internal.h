@@ -48,6 +48,16 @@ cudaError_t launch_linear_qknorm(const void* A, long lda, const void* W, long ld
                                  double rope_scale, float scale, cudaStream_t stream,
                                  int* status);
 
+// The Q and KV projections with that epilogue in one launch: Qout [M, HD]
+// (all head vectors, gamma_q, query_scale) and KVout [M, 2*KVD] (K' head
+// vectors with gamma_k, then V as it is), Wq [HD, K] and Wkv [2*KVD, K]
+// sharing the row stride ldw.
+cudaError_t launch_qkv_qknorm(const void* A, long lda, const void* Wq, const void* Wkv, long ldw,
+                              void* Qout, long ldq, void* KVout, long ldkv, int M, int HD, int KVD,
+                              int K, int in_dtype, const void* gamma_q, const void* gamma_k,
+                              const int32_t* pos, int d_h, double rope_base, double rope_scale,
+                              float query_scale, cudaStream_t stream, int* status);
+
 // In place on fp16 rows: Q[m, h*d_h:(h+1)*d_h] and K[m, j*d_h:(j+1)*d_h] get
 // last-axis RMSNorm, (1 + gamma), RoPE; Q also the query scale.
 cudaError_t launch_qk_norm_rope(void* Q, long ldq, void* K, long ldk, const void* gamma_q,
