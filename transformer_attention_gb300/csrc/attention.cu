@@ -30,13 +30,16 @@
 //               warpgroup wg in {0,1} handles columns [64 wg, 64 wg + 64) of
 //               every row, exchanging the row max with its partner thread
 //               through shared memory (a bounded mbarrier handshake).
-// TMEM columns: S 0-127 | P[0] 128-191 | P[1] 192-255 | O 256..256+d_h, and
-// for d_h = 128 a second S buffer at 384-511.  The softmax releases an S
-// buffer (s_free) as soon as it has loaded its rows into registers, so the
-// next S overlaps the exponentials of this tile; P is double-buffered so
-// PV_{i-1} and the softmax of tile i never touch the same columns.  On
-// tiles without masked elements the row max comes from the TMEM load's own
-// max reduction (tcgen05.ld.red).  O is rescaled in TMEM only when a row max grows by
+// TMEM columns: S buffers at 0-127 and 128-255 (and 384-511 for d_h = 128),
+// O at 256..256+d_h.  The softmax writes P (fp16 pairs) over the first 64
+// columns of the S buffer it has just read, and PV reads it from there; the
+// S of tile i + NS reuses the buffer, issued after PV_i by the same thread,
+// so the tensor pipe's in-order execution keeps the two apart and no
+// barrier is needed to release S: the next S starts as soon as the tensor
+// pipe is free.  (The warpgroups' row-max exchange comes after both have
+// loaded their S columns, so one warpgroup's P never overwrites columns the
+// other still has to read.)  On tiles without masked elements the row max
+// comes from the TMEM load's own max reduction (tcgen05.ld.red).  O is rescaled in TMEM only when a row max grows by
 // more than 2^8, each warpgroup rescaling its half of the columns.
 #include "internal.h"
 #include "ptx.cuh"
@@ -51,7 +54,7 @@ constexpr int BM = 128;   // query rows per CTA
 constexpr int BN = 128;   // keys per KV tile
 constexpr int SM_WARPS = 8;  // softmax warps
 constexpr uint32_t CHUNK = 128 * 128;  // one 128-row x 64-element (128 B) swizzled chunk
-constexpr uint32_t P_COL = 128, O_COL = 256;
+constexpr uint32_t O_COL = 256;
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr float RESCALE_THRESHOLD = 8.0f;  // log2 units
 
@@ -78,10 +81,12 @@ struct Cfg {
   static constexpr uint32_t KV_BYTES = BN * DH * 2;
   static constexpr uint32_t SMEM = Q_BYTES + (KS + VS) * KV_BYTES + 1024;
   static_assert(SMEM + 2304 + SM_WARPS * 2048 <= 232448, "shared memory budget");
-  // S buffers in TMEM: one at columns 0-127; with d_h = 128 the columns
-  // 384-511 left over by O hold a second one.
-  static constexpr int NS = (DH == 128) ? 2 : 1;
-  static __device__ __forceinline__ uint32_t s_col(int buf) { return buf == 0 ? 0u : 384u; }
+  // S buffers in TMEM (P lives in their first 64 columns): 0-127 and
+  // 128-255; with d_h = 128 the columns 384-511 left over by O hold a third.
+  static constexpr int NS = (DH == 128) ? 3 : 2;
+  static __device__ __forceinline__ uint32_t s_col(int buf) {
+    return buf == 2 ? 384u : static_cast<uint32_t>(buf) * 128u;
+  }
 };
 
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
@@ -163,7 +168,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint8_t* sK = smem + C::Q_BYTES;                    // KS stages
   uint8_t* sV = sK + C::KS * C::KV_BYTES;             // VS stages
   __shared__ __align__(8) uint64_t q_full, q_empty, k_full[C::KS], k_empty[C::KS],
-      v_full[C::VS], v_empty[C::VS], s_full[C::NS], s_free[C::NS], p_full[2], pv_done[2],
+      v_full[C::VS], v_empty[C::VS], s_full[C::NS], p_full[2], pv_done[2],
       o_final, o_free, drain, red_bar[4];
   __shared__ float red[2][2][BM];   // [handshake parity][warpgroup][row]
   // Per softmax warp: 32 rows x 32 O columns (64 B per row, 64-byte swizzle)
@@ -187,7 +192,6 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     for (int s = 0; s < C::NS; ++s) {
       mbar_init(smem_u32(&s_full[s]), 1);
-      mbar_init(smem_u32(&s_free[s]), SM_WARPS);
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(smem_u32(&p_full[s]), SM_WARPS);
@@ -328,7 +332,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (!mbar_wait(smem_u32(&v_full[st]), (gt / C::VS) & 1, &abort_flag, status, kSiteVFull))
           return false;
         tc_fence_after();
-        const uint32_t p_tmem = tbase + P_COL + (gt & 1) * 64;
+        const uint32_t p_tmem = tbase + C::s_col(gt % C::NS);   // P over S_gt
         const uint32_t v_addr = smem_u32(sV + st * C::KV_BYTES);
 #pragma unroll
         for (int k = 0; k < BN / 16; ++k)
@@ -354,13 +358,9 @@ __global__ void __launch_bounds__(THREADS, 1)
             ok = false;
             break;
           }
-          // S buffer g % NS: the softmax must have read the S it held before.
+          // S buffer g % NS last held P_{g-NS}, whose PV this thread issued
+          // before: the tensor pipe runs them in order.
           const int sb = g % C::NS;
-          if (g >= C::NS && !mbar_wait(smem_u32(&s_free[sb]), ((g / C::NS) - 1) & 1, &abort_flag,
-                                       status, kSiteSFree)) {
-            ok = false;
-            break;
-          }
           tc_fence_after();
           const uint32_t k_addr = smem_u32(sK + st * C::KV_BYTES);
 #pragma unroll
@@ -444,10 +444,6 @@ __global__ void __launch_bounds__(THREADS, 1)
             s[32 + e] = __uint_as_float(rb[e]);
           }
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&s_free[sb]));
-
         const int s_tile = (it.tile_lo + i) * BN;
         const bool need_mask = (s_tile + BN - 1 > it.t0) || (s_tile + BN > it.valid) ||
                                (window > 0 && s_tile <= it.t_last - window);
@@ -468,11 +464,14 @@ __global__ void __launch_bounds__(THREADS, 1)
           mx = fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
         }
         // Row max over both column halves: exchange with the partner thread.
+        // (Also orders both warpgroups' S loads before either writes P.)
         red[hs & 1][wg][r] = mx;
+        tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(rbar);
         ok = __all_sync(0xffffffffu, mbar_wait(rbar, hs & 1, &abort_flag, status, kSiteRed));
         if (!ok) break;
+        tc_fence_after();
         mx = fmaxf(mx, red[hs & 1][wg ^ 1][r]) * LOG2E;
         ++hs;
 
@@ -521,13 +520,9 @@ __global__ void __launch_bounds__(THREADS, 1)
         const float2 a01 = __fadd2_rn(acc[0], acc[1]), a23 = __fadd2_rn(acc[2], acc[3]);
         const float2 a = __fadd2_rn(a01, a23);
         l += a.x + a.y;
-        if (g >= 2) {
-          // P buffer g%2 is free once the PV two tiles back has read it.
-          ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&pv_done[g & 1]), ((g - 2) >> 1) & 1,
-                                                 &abort_flag, status, kSitePFree));
-          if (!ok) break;
-        }
-        tmem_st32(tbase + lane_off + P_COL + (g & 1) * 64 + wg * 32, p);
+        // P over the first 64 columns of this tile's S buffer (both
+        // warpgroups have read their S columns: the row-max exchange above)
+        tmem_st32(tbase + lane_off + C::s_col(sb) + wg * 32, p);
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
