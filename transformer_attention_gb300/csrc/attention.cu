@@ -84,6 +84,7 @@ struct Cfg {
   // S buffers in TMEM (P lives in their first 64 columns): 0-127 and
   // 128-255; with d_h = 128 the columns 384-511 left over by O hold a third.
   static constexpr int NS = (DH == 128) ? 3 : 2;
+  static constexpr int LA = NS - 1;   // S issued this many tiles ahead of PV
   static __device__ __forceinline__ uint32_t s_col(int buf) {
     return buf == 2 ? 384u : static_cast<uint32_t>(buf) * 128u;
   }
@@ -372,13 +373,18 @@ __global__ void __launch_bounds__(THREADS, 1)
           mma_commit(smem_u32(&k_empty[st]));
           mma_commit(smem_u32(&s_full[sb]));
           if (i == it.n_tiles - 1) mma_commit(smem_u32(&q_empty));
-          if (i >= 1 && !issue_pv(g - 1, i - 1)) {
+          // S runs LA tiles ahead of PV (S_g reuses the buffer of P_{g-NS},
+          // so LA <= NS - 1): the softmax finds the next S already computed.
+          if (i >= C::LA && !issue_pv(g - C::LA, i - C::LA)) {
             ok = false;
             break;
           }
         }
-        // o_final: this item's O accumulation is complete.
-        if (!ok || !issue_pv(g - 1, it.n_tiles - 1)) break;
+        // the PVs of the item's last LA tiles, then o_final: this item's O
+        // accumulation is complete.
+        for (int d = C::LA; ok && d >= 1; --d)
+          if (it.n_tiles - d >= 0 && !issue_pv(g - d, it.n_tiles - d)) ok = false;
+        if (!ok) break;
         mma_commit(smem_u32(&o_final));
         ++nitem;
       }
