@@ -200,6 +200,13 @@ ATTN_CASES = [
     (1, 1, 4, 1, 256, 0, [0]),
     (3, 190, 4, 1, 256, 64, [0, 189, 190]),
     (1, 1500, 4, 1, 256, 512, [0]),
+    # d_h = 128 runs two query tiles per CTA: a second tile past T, a second
+    # tile all padding, an item all padding, windows with one and four heads
+    (2, 333, 4, 2, 128, 0, [0, 150]),
+    (1, 100, 2, 2, 128, 0, [0]),
+    (1, 300, 4, 1, 128, 100, [0]),
+    (3, 260, 2, 1, 128, 64, [0, 259, 260]),
+    (1, 1100, 8, 4, 128, 300, [0]),
 ]
 
 

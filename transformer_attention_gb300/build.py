@@ -19,7 +19,7 @@ BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libgemma3attn.so")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 
-SOURCES = ["api.cu", "gemm.cu", "attention.cu", "elementwise.cu", "decode.cu", "skinny_gemm.cu"]
+SOURCES = ["api.cu", "gemm.cu", "attention.cu", "attention_pair.cu", "elementwise.cu", "decode.cu", "skinny_gemm.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
           "--expt-relaxed-constexpr", "-I", INCLUDE]

@@ -660,6 +660,9 @@ cudaError_t launch_flash_attention(const void* Q, const void* K, const void* V, 
                                    cudaStream_t stream, int* status) {
   if (B <= 0 || T <= 0) return cudaSuccess;
   if (o_dtype != kBF16 && o_dtype != kF16) return cudaErrorInvalidValue;
+  if (d_h == 128)
+    return launch_flash_attention_pair(Q, K, V, ldkv, O, o_dtype, pad_lens, B, T, H, H_kv, window,
+                                       sched, stream, status);
   const int G = H / H_kv;
 #define G3_ATTN_CASE(DH_, G_)                                                                   \
   if (d_h == DH_ && G == G_)                                                                    \

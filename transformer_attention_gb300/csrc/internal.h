@@ -76,6 +76,12 @@ cudaError_t launch_flash_attention(const void* Q, const void* K, const void* V, 
                                    void* O, int o_dtype, const int32_t* pad_lens, int B, int T,
                                    int H, int H_kv, int d_h, int window, void* sched,
                                    cudaStream_t stream, int* status);
+// The d_h = 128 kernel behind launch_flash_attention (two query tiles per
+// CTA); same arguments, G = H / H_kv in {1, 2, 4}.
+cudaError_t launch_flash_attention_pair(const void* Q, const void* K, const void* V, long ldkv,
+                                        void* O, int o_dtype, const int32_t* pad_lens, int B,
+                                        int T, int H, int H_kv, int window, void* sched,
+                                        cudaStream_t stream, int* status);
 
 // u[m,:] = RMSNorm(x[m,:]) * (1 + gamma) over D, x in x_dtype (bf16|f32), u in
 // u_dtype (bf16|f16).

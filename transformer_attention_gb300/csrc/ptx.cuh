@@ -182,6 +182,19 @@ __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
+// Register budget of a warpgroup (all 128 threads execute these).  An
+// increase waits until the CTA's launch allocation has room for it, so the
+// caller checks that the warpgroups' new shares add up to no more than the
+// launch's registers per thread x threads before it launches.
+template <uint32_t N>
+__device__ __forceinline__ void regs_increase() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void regs_decrease() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 // Shared-memory matrix descriptor, 128-byte swizzle (the layout a TMA load
 // with CU_TENSOR_MAP_SWIZZLE_128B writes): start address, leading and stride
 // byte offsets (>> 4), descriptor version 1, layout type 2 (SWIZZLE_128B).
