@@ -293,100 +293,96 @@ __global__ void __launch_bounds__(THREADS, 1)
           if (fills[s] > 0) mbar_wait_drain(smem_u32(&v_full[s]), (fills[s] - 1) & 1);
       }
     } else if (warp == 1) {
-      if (lane == 0) {
-        // ---------------- MMA issuer
-        constexpr uint32_t idesc_qk = idesc_f16(BM, BN, /*f16*/ 0, 0, 0);
-        constexpr uint32_t idesc_pv = idesc_f16(BM, DH, /*f16*/ 0, 0, /*B MN-major*/ 1);
-        int nitem = 0;
-        int g0 = 0;   // global index of the current item's first tile
-        // S_e of global tile g (item-local tile i) from K stage g % KS.
-        auto issue_s = [&](int e, int g) {
-          const uint32_t q_addr = smem_u32(sQ + e * QT_BYTES);
-          const uint32_t k_addr = smem_u32(sK + (g % KS) * KV_BYTES);
-  #pragma unroll
-          for (int k = 0; k < DH / 16; ++k) {
-            const uint32_t off = (k >> 2) * CHUNK + (k & 3) * 32;
-            mma_ss(tbase + s_col(e), sdesc_sw128(q_addr + off, 16, 1024),
-                   sdesc_sw128(k_addr + off, 16, 1024), idesc_qk, k > 0 ? 1u : 0u);
-          }
-          mma_commit(smem_u32(&s_full[e]));
-        };
-        // PV_e of global tile g, item-local tile i.
-        auto issue_pv = [&](int e, int g, int i) -> bool {
-          if (i == 0 && nitem >= 1 &&
-              !mbar_wait(smem_u32(&o_free[e]), (nitem - 1) & 1, &abort_flag, status, kSiteOFree))
-            return false;
-          if (!mbar_wait(smem_u32(&p_full[e][g & 1]), (g >> 1) & 1, &abort_flag, status,
-                         kSitePFull))
-            return false;
-          tc_fence_after();
-          const uint32_t v_addr = smem_u32(sV + (g % VS) * KV_BYTES);
-  #pragma unroll
-          for (int k = 0; k < BN / 16; ++k)
-            mma_ts(tbase + o_col(e), tbase + s_col(e) + k * 8,
-                   sdesc_sw128(v_addr + k * 2048, CHUNK, 1024), idesc_pv, (i > 0 || k > 0) ? 1u : 0u);
-          mma_commit(smem_u32(&pv_done[e][g & 1]));
-          return true;
-        };
-        auto wait_k = [&](int g) -> bool {
-          return mbar_wait(smem_u32(&k_full[g % KS]), (g / KS) & 1, &abort_flag, status, kSiteKFull);
-        };
-        auto wait_v = [&](int g) -> bool {
-          return mbar_wait(smem_u32(&v_full[g % VS]), (g / VS) & 1, &abort_flag, status, kSiteVFull);
-        };
-        bool ok = true;
-        for (int rr = 0; ok; ++rr) {
-          const int pos = take_pos(rr);
-          release_pos(rr);
-          if (pos >= num_items) break;
-          const PairItem it =
-              decode_pair<TQ>(pos, num_pairs, gsz, B, H_kv, T, window, pad_lens);
-          if (it.pad) continue;
-          const int n = it.n_tiles;
-          if (!mbar_wait(smem_u32(&q_full), nitem & 1, &abort_flag, status, kSiteQ) || !wait_k(g0)) {
+      // ---------------- MMA issuer: the whole warp runs the loop (its state
+      // warp-uniform); each tcgen05 instruction is issued by one elected lane.
+      constexpr uint32_t idesc_qk = idesc_f16(BM, BN, /*f16*/ 0, 0, 0);
+      constexpr uint32_t idesc_pv = idesc_f16(BM, DH, /*f16*/ 0, 0, /*B MN-major*/ 1);
+      int nitem = 0;
+      int g0 = 0;   // global index of the current item's first tile
+      auto wait_all = [&](uint64_t& bar, int parity, int site) -> bool {
+        return __all_sync(0xffffffffu,
+                          mbar_wait(smem_u32(&bar), parity, &abort_flag, status, site));
+      };
+      // S_e of global tile g from K stage g % KS.
+      auto issue_s = [&](int e, int g) {
+        const uint32_t q_addr = smem_u32(sQ + e * QT_BYTES);
+        const uint32_t k_addr = smem_u32(sK + (g % KS) * KV_BYTES);
+#pragma unroll
+        for (int k = 0; k < DH / 16; ++k) {
+          const uint32_t off = (k >> 2) * CHUNK + (k & 3) * 32;
+          mma_ss_warp(tbase + s_col(e), sdesc_sw128(q_addr + off, 16, 1024),
+                      sdesc_sw128(k_addr + off, 16, 1024), idesc_qk, k > 0 ? 1u : 0u);
+        }
+        mma_commit_warp(smem_u32(&s_full[e]));
+      };
+      // PV_e of global tile g, item-local tile i.
+      auto issue_pv = [&](int e, int g, int i) -> bool {
+        if (i == 0 && nitem >= 1 && !wait_all(o_free[e], (nitem - 1) & 1, kSiteOFree)) return false;
+        if (!wait_all(p_full[e][g & 1], (g >> 1) & 1, kSitePFull)) return false;
+        tc_fence_after();
+        const uint32_t v_addr = smem_u32(sV + (g % VS) * KV_BYTES);
+#pragma unroll
+        for (int k = 0; k < BN / 16; ++k)
+          mma_ts_warp(tbase + o_col(e), tbase + s_col(e) + k * 8,
+                      sdesc_sw128(v_addr + k * 2048, CHUNK, 1024), idesc_pv,
+                      (i > 0 || k > 0) ? 1u : 0u);
+        mma_commit_warp(smem_u32(&pv_done[e][g & 1]));
+        return true;
+      };
+      bool ok = true;
+      for (int rr = 0; ok; ++rr) {
+        int pos = take_pos(rr);
+        pos = __shfl_sync(0xffffffffu, pos, 0);
+        __syncwarp();
+        if (lane == 0) release_pos(rr);
+        if (pos >= num_items) break;
+        const PairItem it = decode_pair<TQ>(pos, num_pairs, gsz, B, H_kv, T, window, pad_lens);
+        if (it.pad) continue;
+        const int n = it.n_tiles;
+        if (!wait_all(q_full, nitem & 1, kSiteQ) ||
+            !wait_all(k_full[g0 % KS], (g0 / KS) & 1, kSiteKFull)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        issue_s(0, g0);
+        issue_s(1, g0);
+        mma_commit_warp(smem_u32(&k_empty[g0 % KS]));
+        if (n == 1) mma_commit_warp(smem_u32(&q_empty));
+        for (int i = 0; i < n; ++i) {
+          const int g = g0 + i;
+          if (!wait_all(v_full[g % VS], (g / VS) & 1, kSiteVFull) || !issue_pv(0, g, i)) {
             ok = false;
             break;
           }
-          tc_fence_after();
-          issue_s(0, g0);
-          issue_s(1, g0);
-          mma_commit(smem_u32(&k_empty[g0 % KS]));
-          if (n == 1) mma_commit(smem_u32(&q_empty));
-          for (int i = 0; i < n; ++i) {
-            const int g = g0 + i;
-            if (!wait_v(g) || !issue_pv(0, g, i)) {
+          if (i + 1 < n) {
+            if (!wait_all(k_full[(g + 1) % KS], ((g + 1) / KS) & 1, kSiteKFull)) {
               ok = false;
               break;
             }
-            if (i + 1 < n) {
-              if (!wait_k(g + 1)) {
-                ok = false;
-                break;
-              }
-              tc_fence_after();
-              issue_s(0, g + 1);
-            }
-            if (i + 1 == n) mma_commit(smem_u32(&o_final[0]));   // O0 of this item complete
-            if (!issue_pv(1, g, i)) {
-              ok = false;
-              break;
-            }
-            mma_commit(smem_u32(&v_empty[g % VS]));
-            if (i + 1 < n) {
-              issue_s(1, g + 1);
-              mma_commit(smem_u32(&k_empty[(g + 1) % KS]));
-              if (i + 1 == n - 1) mma_commit(smem_u32(&q_empty));
-            } else {
-              mma_commit(smem_u32(&o_final[1]));
-            }
+            tc_fence_after();
+            issue_s(0, g + 1);
           }
-          if (!ok) break;
-          g0 += n;
-          ++nitem;
+          if (i + 1 == n) mma_commit_warp(smem_u32(&o_final[0]));   // O0 of this item complete
+          if (!issue_pv(1, g, i)) {
+            ok = false;
+            break;
+          }
+          mma_commit_warp(smem_u32(&v_empty[g % VS]));
+          if (i + 1 < n) {
+            issue_s(1, g + 1);
+            mma_commit_warp(smem_u32(&k_empty[(g + 1) % KS]));
+            if (i + 1 == n - 1) mma_commit_warp(smem_u32(&q_empty));
+          } else {
+            mma_commit_warp(smem_u32(&o_final[1]));
+          }
         }
-        mma_commit(smem_u32(&drain));
-        mbar_wait_drain(smem_u32(&drain), 0);
+        if (!ok) break;
+        g0 += n;
+        ++nitem;
       }
+      mma_commit_warp(smem_u32(&drain));
+      mbar_wait_drain(smem_u32(&drain), 0);
     }
   } else {
     regs_increase<REGS_HIGH>();
