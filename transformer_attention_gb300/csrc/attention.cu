@@ -30,8 +30,8 @@
 //               warpgroup wg in {0,1} handles columns [64 wg, 64 wg + 64) of
 //               every row, exchanging the row max with its partner thread
 //               through shared memory (a bounded mbarrier handshake).
-// TMEM columns: S buffers at 0-127 and 128-255 (and 384-511 for d_h = 128),
-// O at 256..256+d_h.  The softmax writes P (fp16 pairs) over the first 64
+// TMEM columns: S buffers at 0-127 and 128-255, O at 256-511.  (d_h = 128
+// runs in attention_pair.cu, two query tiles per CTA.)  The softmax writes P (fp16 pairs) over the first 64
 // columns of the S buffer it has just read, and PV reads it from there; the
 // S of tile i + NS reuses the buffer, issued after PV_i by the same thread,
 // so the tensor pipe's in-order execution keeps the two apart and no
@@ -72,21 +72,21 @@ constexpr int SCHED_CONSUMERS = 2 + SM_WARPS;   // V producer, MMA issuer, softm
 
 template <int DH, int G>
 struct Cfg {
+  static_assert(DH == 256, "d_h = 128 has its own kernel");
   static constexpr int TQ = BM / G;
   static constexpr int NCH = DH / 64;
   // Ring depths within the 227 KB of shared memory (Q + K ring + V ring).
-  static constexpr int KS = (DH == 256) ? 1 : 3;   // K ring depth
-  static constexpr int VS = (DH == 256) ? 1 : 2;   // V ring depth
+  static constexpr int KS = 1;   // K ring depth
+  static constexpr int VS = 1;   // V ring depth
   static constexpr uint32_t Q_BYTES = BM * DH * 2;
   static constexpr uint32_t KV_BYTES = BN * DH * 2;
   static constexpr uint32_t SMEM = Q_BYTES + (KS + VS) * KV_BYTES + 1024;
   static_assert(SMEM + 2304 + SM_WARPS * 2048 <= 232448, "shared memory budget");
-  // S buffers in TMEM (P lives in their first 64 columns): 0-127 and
-  // 128-255; with d_h = 128 the columns 384-511 left over by O hold a third.
-  static constexpr int NS = (DH == 128) ? 3 : 2;
+  // S buffers in TMEM (P lives in their first 64 columns): 0-127 and 128-255.
+  static constexpr int NS = 2;
   static constexpr int LA = NS - 1;   // S issued this many tiles ahead of PV
   static __device__ __forceinline__ uint32_t s_col(int buf) {
-    return buf == 2 ? 384u : static_cast<uint32_t>(buf) * 128u;
+    return static_cast<uint32_t>(buf) * 128u;
   }
 };
 
@@ -314,83 +314,82 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (fills[s] > 0) mbar_wait_drain(smem_u32(&v_full[s]), (fills[s] - 1) & 1);
     }
   } else if (warp == 1) {
-    if (lane == 0) {
-      // ---------------- MMA issuer
-      constexpr uint32_t idesc_qk = idesc_f16(BM, BN, /*f16*/ 0, 0, 0);
-      constexpr uint32_t idesc_pv = idesc_f16(BM, DH, /*f16*/ 0, 0, /*B MN-major*/ 1);
-      const uint32_t q_addr = smem_u32(sQ);
-      int nitem = 0;   // items processed so far
-      // PV of global tile gt, local tile lt of the current item.
-      auto issue_pv = [&](int gt, int lt) -> bool {
-        // The first PV of an item overwrites O: the previous item's epilogue
-        // must have read it.
-        if (lt == 0 && nitem >= 1 &&
-            !mbar_wait(smem_u32(&o_free), (nitem - 1) & 1, &abort_flag, status, kSiteOFinal))
-          return false;
-        if (!mbar_wait(smem_u32(&p_full[gt & 1]), (gt >> 1) & 1, &abort_flag, status, kSitePFull))
-          return false;
-        const int st = gt % C::VS;
-        if (!mbar_wait(smem_u32(&v_full[st]), (gt / C::VS) & 1, &abort_flag, status, kSiteVFull))
-          return false;
-        tc_fence_after();
-        const uint32_t p_tmem = tbase + C::s_col(gt % C::NS);   // P over S_gt
-        const uint32_t v_addr = smem_u32(sV + st * C::KV_BYTES);
+    // ---------------- MMA issuer: the whole warp runs the loop (its state
+    // warp-uniform); each tcgen05 instruction is issued by one elected lane.
+    constexpr uint32_t idesc_qk = idesc_f16(BM, BN, /*f16*/ 0, 0, 0);
+    constexpr uint32_t idesc_pv = idesc_f16(BM, DH, /*f16*/ 0, 0, /*B MN-major*/ 1);
+    const uint32_t q_addr = smem_u32(sQ);
+    int nitem = 0;   // items processed so far
+    auto wait_all = [&](uint64_t& bar, int parity, int site) -> bool {
+      return __all_sync(0xffffffffu, mbar_wait(smem_u32(&bar), parity, &abort_flag, status, site));
+    };
+    // PV of global tile gt, local tile lt of the current item.
+    auto issue_pv = [&](int gt, int lt) -> bool {
+      // The first PV of an item overwrites O: the previous item's epilogue
+      // must have read it.
+      if (lt == 0 && nitem >= 1 && !wait_all(o_free, (nitem - 1) & 1, kSiteOFinal)) return false;
+      if (!wait_all(p_full[gt & 1], (gt >> 1) & 1, kSitePFull)) return false;
+      const int st = gt % C::VS;
+      if (!wait_all(v_full[st], (gt / C::VS) & 1, kSiteVFull)) return false;
+      tc_fence_after();
+      const uint32_t p_tmem = tbase + C::s_col(gt % C::NS);   // P over S_gt
+      const uint32_t v_addr = smem_u32(sV + st * C::KV_BYTES);
 #pragma unroll
-        for (int k = 0; k < BN / 16; ++k)
-          mma_ts(tbase + O_COL, p_tmem + k * 8, sdesc_sw128(v_addr + k * 2048, CHUNK, 1024),
-                 idesc_pv, (lt > 0 || k > 0) ? 1u : 0u);
-        mma_commit(smem_u32(&v_empty[st]));
-        mma_commit(smem_u32(&pv_done[gt & 1]));
-        return true;
-      };
-      bool ok = true;
-      int g = 0;
-      for (int rr = 0; ok; ++rr) {
-        const int pos = take_pos(rr);
-        release_pos(rr);
-        if (pos >= num_items) break;
-        const Item it = decode_item<C::TQ>(pos, num_q_tiles, gsz, B, H_kv, T, window, pad_lens);
-        if (it.pad) continue;
-        if (!mbar_wait(smem_u32(&q_full), nitem & 1, &abort_flag, status, kSiteQ)) break;
-        for (int i = 0; i < it.n_tiles; ++i, ++g) {
-          const int st = g % C::KS;
-          if (!mbar_wait(smem_u32(&k_full[st]), (g / C::KS) & 1, &abort_flag, status,
-                         kSiteKFull)) {
-            ok = false;
-            break;
-          }
-          // S buffer g % NS last held P_{g-NS}, whose PV this thread issued
-          // before: the tensor pipe runs them in order.
-          const int sb = g % C::NS;
-          tc_fence_after();
-          const uint32_t k_addr = smem_u32(sK + st * C::KV_BYTES);
-#pragma unroll
-          for (int k = 0; k < DH / 16; ++k) {
-            const uint32_t off = (k >> 2) * CHUNK + (k & 3) * 32;
-            mma_ss(tbase + C::s_col(sb), sdesc_sw128(q_addr + off, 16, 1024),
-                   sdesc_sw128(k_addr + off, 16, 1024), idesc_qk, k > 0 ? 1u : 0u);
-          }
-          mma_commit(smem_u32(&k_empty[st]));
-          mma_commit(smem_u32(&s_full[sb]));
-          if (i == it.n_tiles - 1) mma_commit(smem_u32(&q_empty));
-          // S runs LA tiles ahead of PV (S_g reuses the buffer of P_{g-NS},
-          // so LA <= NS - 1): the softmax finds the next S already computed.
-          if (i >= C::LA && !issue_pv(g - C::LA, i - C::LA)) {
-            ok = false;
-            break;
-          }
+      for (int k = 0; k < BN / 16; ++k)
+        mma_ts_warp(tbase + O_COL, p_tmem + k * 8, sdesc_sw128(v_addr + k * 2048, CHUNK, 1024),
+                    idesc_pv, (lt > 0 || k > 0) ? 1u : 0u);
+      mma_commit_warp(smem_u32(&v_empty[st]));
+      mma_commit_warp(smem_u32(&pv_done[gt & 1]));
+      return true;
+    };
+    bool ok = true;
+    int g = 0;
+    for (int rr = 0; ok; ++rr) {
+      int pos = take_pos(rr);
+      pos = __shfl_sync(0xffffffffu, pos, 0);
+      __syncwarp();
+      if (lane == 0) release_pos(rr);
+      if (pos >= num_items) break;
+      const Item it = decode_item<C::TQ>(pos, num_q_tiles, gsz, B, H_kv, T, window, pad_lens);
+      if (it.pad) continue;
+      if (!wait_all(q_full, nitem & 1, kSiteQ)) break;
+      for (int i = 0; i < it.n_tiles; ++i, ++g) {
+        const int st = g % C::KS;
+        if (!wait_all(k_full[st], (g / C::KS) & 1, kSiteKFull)) {
+          ok = false;
+          break;
         }
-        // the PVs of the item's last LA tiles, then o_final: this item's O
-        // accumulation is complete.
-        for (int d = C::LA; ok && d >= 1; --d)
-          if (it.n_tiles - d >= 0 && !issue_pv(g - d, it.n_tiles - d)) ok = false;
-        if (!ok) break;
-        mma_commit(smem_u32(&o_final));
-        ++nitem;
+        // S buffer g % NS last held P_{g-NS}, whose PV this warp issued
+        // before: the tensor pipe runs them in order.
+        const int sb = g % C::NS;
+        tc_fence_after();
+        const uint32_t k_addr = smem_u32(sK + st * C::KV_BYTES);
+#pragma unroll
+        for (int k = 0; k < DH / 16; ++k) {
+          const uint32_t off = (k >> 2) * CHUNK + (k & 3) * 32;
+          mma_ss_warp(tbase + C::s_col(sb), sdesc_sw128(q_addr + off, 16, 1024),
+                      sdesc_sw128(k_addr + off, 16, 1024), idesc_qk, k > 0 ? 1u : 0u);
+        }
+        mma_commit_warp(smem_u32(&k_empty[st]));
+        mma_commit_warp(smem_u32(&s_full[sb]));
+        if (i == it.n_tiles - 1) mma_commit_warp(smem_u32(&q_empty));
+        // S runs LA tiles ahead of PV (S_g reuses the buffer of P_{g-NS},
+        // so LA <= NS - 1): the softmax finds the next S already computed.
+        if (i >= C::LA && !issue_pv(g - C::LA, i - C::LA)) {
+          ok = false;
+          break;
+        }
       }
-      mma_commit(smem_u32(&drain));
-      mbar_wait_drain(smem_u32(&drain), 0);
+      // the PVs of the item's last LA tiles, then o_final: this item's O
+      // accumulation is complete.
+      for (int d = C::LA; ok && d >= 1; --d)
+        if (it.n_tiles - d >= 0 && !issue_pv(g - d, it.n_tiles - d)) ok = false;
+      if (!ok) break;
+      mma_commit_warp(smem_u32(&o_final));
+      ++nitem;
     }
+    mma_commit_warp(smem_u32(&drain));
+    mbar_wait_drain(smem_u32(&drain), 0);
   } else if (warp >= 4) {
     // ---------------- softmax + epilogue
     const int wg = (warp - 4) >> 2;        // column half of every row
@@ -671,9 +670,6 @@ cudaError_t launch_flash_attention(const void* Q, const void* K, const void* V, 
   G3_ATTN_CASE(256, 1)
   G3_ATTN_CASE(256, 2)
   G3_ATTN_CASE(256, 4)
-  G3_ATTN_CASE(128, 1)
-  G3_ATTN_CASE(128, 2)
-  G3_ATTN_CASE(128, 4)
 #undef G3_ATTN_CASE
   return cudaErrorInvalidValue;
 }

@@ -193,44 +193,45 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (fills[s] > 0) mbar_wait_drain(smem_u32(&full_bar[s]), (fills[s] - 1) & 1);
     }
   } else if (warp == 1) {
-    if (lane == 0) {
-      // ---------------- MMA issuer
-      const uint32_t idesc = idesc_f16(BM, BN, AB_BF16, 0, 0);
-      int stage = 0;
-      uint32_t phase = 0;
-      int abuf = 0;
-      uint32_t aphase = 0;
-      bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
-        if (!mbar_wait(smem_u32(&acce_bar[abuf]), aphase ^ 1, &abort_flag, status, kSiteAccEmpty))
+    // ---------------- MMA issuer: the whole warp runs the loop (its state
+    // warp-uniform); each tcgen05 instruction is issued by one elected lane.
+    const uint32_t idesc = idesc_f16(BM, BN, AB_BF16, 0, 0);
+    int stage = 0;
+    uint32_t phase = 0;
+    int abuf = 0;
+    uint32_t aphase = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+      if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&acce_bar[abuf]), aphase ^ 1, &abort_flag,
+                                             status, kSiteAccEmpty)))
+        break;
+      tc_fence_after();
+      const uint32_t d_tmem = tbase + abuf * BN;
+      for (int kb = 0; kb < num_kb; ++kb) {
+        if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&full_bar[stage]), phase, &abort_flag,
+                                               status, kSiteFull))) {
+          ok = false;
           break;
-        tc_fence_after();
-        const uint32_t d_tmem = tbase + abuf * BN;
-        for (int kb = 0; kb < num_kb; ++kb) {
-          if (!mbar_wait(smem_u32(&full_bar[stage]), phase, &abort_flag, status, kSiteFull)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t a_addr = smem_u32(smem + stage * STAGE_BYTES);
-          const uint32_t b_addr = a_addr + A_BYTES;
-#pragma unroll
-          for (int k = 0; k < BK / 16; ++k) {
-            mma_ss(d_tmem, sdesc_sw128(a_addr + k * 32, 16, 1024),
-                   sdesc_sw128(b_addr + k * 32, 16, 1024), idesc, (kb | k) != 0);
-          }
-          mma_commit(smem_u32(&empty_bar[stage]));
-          if (++stage == STAGES) { stage = 0; phase ^= 1; }
         }
-        if (!ok) break;
-        mma_commit(smem_u32(&accf_bar[abuf]));
-        abuf ^= 1;
-        if (abuf == 0) aphase ^= 1;
+        tc_fence_after();
+        const uint32_t a_addr = smem_u32(smem + stage * STAGE_BYTES);
+        const uint32_t b_addr = a_addr + A_BYTES;
+#pragma unroll
+        for (int k = 0; k < BK / 16; ++k) {
+          mma_ss_warp(d_tmem, sdesc_sw128(a_addr + k * 32, 16, 1024),
+                      sdesc_sw128(b_addr + k * 32, 16, 1024), idesc, (kb | k) != 0);
+        }
+        mma_commit_warp(smem_u32(&empty_bar[stage]));
+        if (++stage == STAGES) { stage = 0; phase ^= 1; }
       }
-      // Drain the tensor pipe before TMEM is released.
-      mma_commit(smem_u32(&drain_bar));
-      mbar_wait_drain(smem_u32(&drain_bar), 0);
+      if (!ok) break;
+      mma_commit_warp(smem_u32(&accf_bar[abuf]));
+      abuf ^= 1;
+      if (abuf == 0) aphase ^= 1;
     }
+    // Drain the tensor pipe before TMEM is released.
+    mma_commit_warp(smem_u32(&drain_bar));
+    mbar_wait_drain(smem_u32(&drain_bar), 0);
   } else if (warp >= 4) {
     // ---------------- epilogue: TMEM -> registers -> swizzled staging -> TMA store
     const int q = warp - 4;
