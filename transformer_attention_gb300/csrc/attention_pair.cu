@@ -45,7 +45,7 @@ constexpr float LOG2E = 1.4426950408889634f;
 constexpr float RESCALE_THRESHOLD = 8.0f;   // log2 units
 constexpr int SCHED_SLOTS = 4;
 constexpr int SCHED_CONSUMERS = 2 + SM_WARPS;
-static_assert(SMEM + SM_WARPS * 2048 + 1024 <= 232448, "shared memory budget");
+static_assert(SMEM + 1024 <= 232448, "shared memory budget");
 // Registers per thread: the launch gives every thread 65536 / 384 = 168;
 // the producer / MMA warpgroup then drops to REGS_LOW and the two softmax
 // warpgroups rise to REGS_HIGH (a whole 128-column row of S in registers).
@@ -135,7 +135,7 @@ __device__ __forceinline__ int static_position(int r) {
 template <int G>
 __global__ void __launch_bounds__(THREADS, 1)
     attn_pair_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+                     const __grid_constant__ CUtensorMap tmV,
                      uint16_t* __restrict__ O, int o_f16, const int32_t* __restrict__ pad_lens,
                      int B, int T, int H, int H_kv, int window, int num_pairs, int gsz,
                      int num_items, unsigned int* sched, int* status) {
@@ -151,7 +151,6 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint8_t* sV = sK + KS * KV_BYTES;          // VS stages
   __shared__ __align__(8) uint64_t q_full, q_empty, k_full[KS], k_empty[KS], v_full[VS],
       v_empty[VS], s_full[2], p_full[2][2], pv_done[2][2], o_final[2], o_free[2], drain;
-  __shared__ __align__(1024) uint8_t ostage[SM_WARPS][32 * 64];
   __shared__ uint32_t tmem_sh;
   __shared__ int abort_flag;
   __shared__ int sched_pos[SCHED_SLOTS];
@@ -187,7 +186,6 @@ __global__ void __launch_bounds__(THREADS, 1)
     tma_prefetch_desc(&tmQ);
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
-    tma_prefetch_desc(&tmO);
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(&tmem_sh), 512);
@@ -527,44 +525,35 @@ __global__ void __launch_bounds__(THREADS, 1)
       tc_fence_after();
       const bool row_valid = t < it.valid;
       const float inv_l = row_valid && l > 0.f ? 1.f / l : 0.f;
-      uint8_t* stage = ostage[warp - 4];
-#pragma unroll 1
-      for (int c = 0; c < DH / 32; ++c) {
-        uint32_t ro[32];
-        tmem_ld32(o_base + c * 32, ro);
-        tmem_ld_wait(ro);
-        if (c == DH / 32 - 1) {
-          // O_e has been read: the next item's first PV_e may overwrite it.
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(smem_u32(&o_free[e]));
-        }
-        uint32_t wv[16];
-#pragma unroll
-        for (int k = 0; k < 16; ++k) {
-          const float lo = __uint_as_float(ro[2 * k]) * inv_l;
-          const float hi = __uint_as_float(ro[2 * k + 1]) * inv_l;
-          wv[k] = row_valid ? (o_f16 ? pack_half2(lo, hi) : pack_bf162(lo, hi)) : 0u;
-        }
-        if (lane == 0) bulk_wait_group_read<0>();
+      // Each thread writes its own row of O_e straight from registers
+      // (16-byte stores); rows past T, in a second tile beyond the sequence,
+      // are not written.
+      {
+        uint32_t ra[32], rb[32], rc[32], rd[32];
+        tmem_ld32(o_base, ra);
+        tmem_ld32(o_base + 32, rb);
+        tmem_ld32(o_base + 64, rc);
+        tmem_ld32(o_base + 96, rd);
+        tmem_ld_wait(ra);
+        tmem_ld_wait(rb);
+        tmem_ld_wait(rc);
+        tmem_ld_wait(rd);
+        // O_e has been read: the next item's first PV_e may overwrite it.
+        tc_fence_before();
         __syncwarp();
-#pragma unroll
-        for (int u = 0; u < 4; ++u)
-          *reinterpret_cast<uint4*>(stage + lane * 64 + ((u ^ ((lane >> 1) & 3)) << 4)) =
-              make_uint4(wv[4 * u], wv[4 * u + 1], wv[4 * u + 2], wv[4 * u + 3]);
-        fence_proxy_async_smem();
-        __syncwarp();
-        // (a box that starts past T, in a second tile beyond the sequence, is skipped;
-        // one that straddles T is clipped by the store)
-        if (lane == 0 && te0 + (q * 32) / G < T) {
-          tma_store_4d(&tmO, smem_u32(stage), c * 32, it.j * G, te0 + (q * 32) / G, it.b);
-          bulk_commit_group();
+        if (lane == 0) mbar_arrive(smem_u32(&o_free[e]));
+        if (t < T) {
+          uint16_t* orow =
+              O + ((static_cast<size_t>(it.b) * T + t) * H + it.j * G + r % G) * DH;
+          store_row32(orow, ra, inv_l, row_valid, o_f16);
+          store_row32(orow + 32, rb, inv_l, row_valid, o_f16);
+          store_row32(orow + 64, rc, inv_l, row_valid, o_f16);
+          store_row32(orow + 96, rd, inv_l, row_valid, o_f16);
         }
       }
       g0 += it.n_tiles;
       ++nitem;
     }
-    if (lane == 0) bulk_wait_group_all();
   }
   __syncthreads();
   if (warp == 1) {
@@ -578,7 +567,7 @@ cudaError_t launch_pair_cfg(const void* Q, const void* K, const void* V, long ld
                             int o_dtype, const int32_t* pad_lens, int B, int T, int H, int H_kv,
                             int window, unsigned int* sched, cudaStream_t stream, int* status) {
   constexpr int TQ = BM / G;
-  CUtensorMap tq, tk, tv, to;
+  CUtensorMap tq, tk, tv;
   const uint64_t qdims[4] = {static_cast<uint64_t>(DH), static_cast<uint64_t>(H),
                              static_cast<uint64_t>(T), static_cast<uint64_t>(B)};
   const uint64_t qstr[3] = {static_cast<uint64_t>(DH) * 2, static_cast<uint64_t>(H) * DH * 2,
@@ -588,10 +577,9 @@ cudaError_t launch_pair_cfg(const void* Q, const void* K, const void* V, long ld
                              static_cast<uint64_t>(B)};
   const uint64_t kstr[2] = {static_cast<uint64_t>(ldkv) * 2, static_cast<uint64_t>(T) * ldkv * 2};
   const uint32_t kbox[3] = {64, BN, 1};
-  const uint32_t obox[4] = {32, static_cast<uint32_t>(G), static_cast<uint32_t>(32 / G), 1};
-  if (!encode_tiled(&to, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4, O, qdims, qstr, obox,
-                    CU_TENSOR_MAP_SWIZZLE_64B) ||
-      !encode_tiled(&tq, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4, Q, qdims, qstr, qbox) ||
+  // O [B, T, H, d_h] is written with 16-byte stores.
+  if (reinterpret_cast<uintptr_t>(O) % 16 != 0) return cudaErrorInvalidValue;
+  if (!encode_tiled(&tq, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4, Q, qdims, qstr, qbox) ||
       !encode_tiled(&tk, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, K, kdims, kstr, kbox) ||
       !encode_tiled(&tv, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, V, kdims, kstr, kbox))
     return cudaErrorInvalidValue;
@@ -620,7 +608,7 @@ cudaError_t launch_pair_cfg(const void* Q, const void* K, const void* V, long ld
   gsz = gsz < 1 ? 1 : (gsz > B * H_kv ? B * H_kv : gsz);
   if (sched != nullptr && cudaMemsetAsync(sched, 0, sizeof(unsigned int), stream) != cudaSuccess)
     return cudaErrorUnknown;
-  kern<<<grid, THREADS, SMEM, stream>>>(tq, tk, tv, to, static_cast<uint16_t*>(O),
+  kern<<<grid, THREADS, SMEM, stream>>>(tq, tk, tv, static_cast<uint16_t*>(O),
                                         o_dtype == kF16 ? 1 : 0, pad_lens, B, T, H, H_kv, window,
                                         num_pairs, gsz, static_cast<int>(items), sched, status);
   return cudaGetLastError();

@@ -359,4 +359,20 @@ __device__ __forceinline__ uint32_t pack_bf162(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
+// 32 fp32 values of an O row times inv_l, packed to bf16 or fp16 (zeros for
+// a row past the valid length), as four 16-byte stores to dst.
+__device__ __forceinline__ void store_row32(uint16_t* dst, const uint32_t (&v)[32], float inv_l,
+                                            bool row_valid, int o_f16) {
+  uint32_t w[16];
+#pragma unroll
+  for (int e = 0; e < 16; ++e) {
+    const float lo = __uint_as_float(v[2 * e]) * inv_l;
+    const float hi = __uint_as_float(v[2 * e + 1]) * inv_l;
+    w[e] = row_valid ? (o_f16 ? pack_half2(lo, hi) : pack_bf162(lo, hi)) : 0u;
+  }
+  uint4* d = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int u = 0; u < 4; ++u) d[u] = make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
+}
+
 }  // namespace g3
