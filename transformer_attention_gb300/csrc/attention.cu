@@ -75,12 +75,12 @@ struct Cfg {
   static_assert(DH == 256, "d_h = 128 has its own kernel");
   static constexpr int TQ = BM / G;
   static constexpr int NCH = DH / 64;
-  // Ring depths within the 227 KB of shared memory (Q + K ring + V ring).
-  static constexpr int KS = 1;   // K ring depth
-  static constexpr int VS = 1;   // V ring depth
+  // Q, one K tile and one V tile fill the 227 KB of shared memory; K is
+  // released and refilled per 64-channel chunk (the S MMAs of chunk c are
+  // its only readers), V per half of its 128 keys (the PV MMAs of that half).
   static constexpr uint32_t Q_BYTES = BM * DH * 2;
   static constexpr uint32_t KV_BYTES = BN * DH * 2;
-  static constexpr uint32_t SMEM = Q_BYTES + (KS + VS) * KV_BYTES + 1024;
+  static constexpr uint32_t SMEM = Q_BYTES + 2 * KV_BYTES + 1024;
   static_assert(SMEM + 2304 + SM_WARPS * 2048 <= 232448, "shared memory budget");
   // S buffers in TMEM (P lives in their first 64 columns): 0-127 and 128-255.
   static constexpr int NS = 2;
@@ -166,10 +166,10 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   uint8_t* sQ = smem;
-  uint8_t* sK = smem + C::Q_BYTES;                    // KS stages
-  uint8_t* sV = sK + C::KS * C::KV_BYTES;             // VS stages
-  __shared__ __align__(8) uint64_t q_full, q_empty, k_full[C::KS], k_empty[C::KS],
-      v_full[C::VS], v_empty[C::VS], s_full[C::NS], p_full[2], pv_done[2],
+  uint8_t* sK = smem + C::Q_BYTES;                    // chunk c at c * CHUNK
+  uint8_t* sV = sK + C::KV_BYTES;                     // key half h at c * CHUNK + h * CHUNK / 2
+  __shared__ __align__(8) uint64_t q_full, q_empty, k_full[C::NCH], k_empty[C::NCH],
+      v_full[2], v_empty[2], s_full[C::NS], p_full[2], pv_done[2],
       o_final, o_free, drain, red_bar[4];
   __shared__ float red[2][2][BM];   // [handshake parity][warpgroup][row]
   // Per softmax warp: 32 rows x 32 O columns (64 B per row, 64-byte swizzle)
@@ -183,11 +183,11 @@ __global__ void __launch_bounds__(THREADS, 1)
   if (threadIdx.x == 0) {
     mbar_init(smem_u32(&q_full), 1);
     mbar_init(smem_u32(&q_empty), 1);
-    for (int s = 0; s < C::KS; ++s) {
+    for (int s = 0; s < C::NCH; ++s) {
       mbar_init(smem_u32(&k_full[s]), 1);
       mbar_init(smem_u32(&k_empty[s]), 1);
     }
-    for (int s = 0; s < C::VS; ++s) {
+    for (int s = 0; s < 2; ++s) {
       mbar_init(smem_u32(&v_full[s]), 1);
       mbar_init(smem_u32(&v_empty[s]), 1);
     }
@@ -251,9 +251,9 @@ __global__ void __launch_bounds__(THREADS, 1)
 
   if (warp == 0) {
     if (lane == 0) {
-      // ---------------- producer: Q of each item, then its K tiles
-      int fills[C::KS] = {};
-      int f = 0, nq = 0;
+      // ---------------- producer: Q of each item, then its K tiles chunk by chunk
+      int f = 0, nq = 0;   // K tiles and Q tiles loaded
+      int kf[C::NCH] = {};  // loads issued per chunk buffer
       bool ok = true;
       for (int rr = 0, pos; ok && (pos = fetch_pos(rr)) < num_items; ++rr) {
         const Item it = decode_item<C::TQ>(pos, num_q_tiles, gsz, B, H_kv, T, window, pad_lens);
@@ -265,53 +265,55 @@ __global__ void __launch_bounds__(THREADS, 1)
         for (int ch = 0; ch < C::NCH; ++ch)
           tma_load_4d(smem_u32(sQ + ch * CHUNK), &tmQ, qb, ch * 64, it.j * G, it.t0, it.b);
         ++nq;
-        for (int i = 0; i < it.n_tiles; ++i, ++f) {
-          const int st = f % C::KS;
-          if (!mbar_wait(smem_u32(&k_empty[st]), ((f / C::KS) & 1) ^ 1, &abort_flag, status,
-                         kSiteKEmpty)) {
-            ok = false;
-            break;
+        for (int i = 0; ok && i < it.n_tiles; ++i, ++f) {
+          for (int ch = 0; ch < C::NCH; ++ch) {
+            if (!mbar_wait(smem_u32(&k_empty[ch]), (f & 1) ^ 1, &abort_flag, status,
+                           kSiteKEmpty)) {
+              ok = false;
+              break;
+            }
+            const uint32_t fb = smem_u32(&k_full[ch]);
+            mbar_arrive_expect_tx(fb, CHUNK);
+            tma_load_3d(smem_u32(sK + ch * CHUNK), &tmK, fb, it.j * DH + ch * 64,
+                        (it.tile_lo + i) * BN, it.b);
+            ++kf[ch];
           }
-          const uint32_t fb = smem_u32(&k_full[st]);
-          mbar_arrive_expect_tx(fb, C::KV_BYTES);
-          for (int ch = 0; ch < C::NCH; ++ch)
-            tma_load_3d(smem_u32(sK + st * C::KV_BYTES + ch * CHUNK), &tmK, fb,
-                        it.j * DH + ch * 64, (it.tile_lo + i) * BN, it.b);
-          ++fills[st];
         }
       }
       if (nq > 0) mbar_wait_drain(smem_u32(&q_full), (nq - 1) & 1);
-      for (int s = 0; s < C::KS; ++s)
-        if (fills[s] > 0) mbar_wait_drain(smem_u32(&k_full[s]), (fills[s] - 1) & 1);
+      for (int ch = 0; ch < C::NCH; ++ch)
+        if (kf[ch] > 0) mbar_wait_drain(smem_u32(&k_full[ch]), (kf[ch] - 1) & 1);
     }
   } else if (warp == 2) {
     if (lane == 0) {
-      // ---------------- producer: V tiles of each item
-      int fills[C::VS] = {};
-      int f = 0;
+      // ---------------- producer: V tiles of each item, half by half
+      int f = 0;            // V tiles loaded
+      int vf[2] = {0, 0};   // loads issued per half
       bool ok = true;
       for (int rr = 0;; ++rr) {
         const int pos = take_pos(rr);
         release_pos(rr);
         if (pos >= num_items) break;
         const Item it = decode_item<C::TQ>(pos, num_q_tiles, gsz, B, H_kv, T, window, pad_lens);
-        for (int i = 0; i < it.n_tiles; ++i, ++f) {
-          const int st = f % C::VS;
-          if (!mbar_wait(smem_u32(&v_empty[st]), ((f / C::VS) & 1) ^ 1, &abort_flag, status,
-                         kSiteVEmpty)) {
-            ok = false;
-            break;
+        for (int i = 0; ok && i < it.n_tiles; ++i, ++f) {
+          for (int h = 0; h < 2; ++h) {
+            if (!mbar_wait(smem_u32(&v_empty[h]), (f & 1) ^ 1, &abort_flag, status,
+                           kSiteVEmpty)) {
+              ok = false;
+              break;
+            }
+            const uint32_t fb = smem_u32(&v_full[h]);
+            mbar_arrive_expect_tx(fb, C::KV_BYTES / 2);
+            for (int ch = 0; ch < C::NCH; ++ch)
+              tma_load_3d(smem_u32(sV + ch * CHUNK + h * (CHUNK / 2)), &tmV, fb,
+                          it.j * DH + ch * 64, (it.tile_lo + i) * BN + h * (BN / 2), it.b);
+            ++vf[h];
           }
-          const uint32_t fb = smem_u32(&v_full[st]);
-          mbar_arrive_expect_tx(fb, C::KV_BYTES);
-          for (int ch = 0; ch < C::NCH; ++ch)
-            tma_load_3d(smem_u32(sV + st * C::KV_BYTES + ch * CHUNK), &tmV, fb,
-                        it.j * DH + ch * 64, (it.tile_lo + i) * BN, it.b);
-          ++fills[st];
         }
+        if (!ok) break;
       }
-      for (int s = 0; s < C::VS; ++s)
-        if (fills[s] > 0) mbar_wait_drain(smem_u32(&v_full[s]), (fills[s] - 1) & 1);
+      for (int h = 0; h < 2; ++h)
+        if (vf[h] > 0) mbar_wait_drain(smem_u32(&v_full[h]), (vf[h] - 1) & 1);
     }
   } else if (warp == 1) {
     // ---------------- MMA issuer: the whole warp runs the loop (its state
@@ -329,16 +331,18 @@ __global__ void __launch_bounds__(THREADS, 1)
       // must have read it.
       if (lt == 0 && nitem >= 1 && !wait_all(o_free, (nitem - 1) & 1, kSiteOFinal)) return false;
       if (!wait_all(p_full[gt & 1], (gt >> 1) & 1, kSitePFull)) return false;
-      const int st = gt % C::VS;
-      if (!wait_all(v_full[st], (gt / C::VS) & 1, kSiteVFull)) return false;
-      tc_fence_after();
       const uint32_t p_tmem = tbase + C::s_col(gt % C::NS);   // P over S_gt
-      const uint32_t v_addr = smem_u32(sV + st * C::KV_BYTES);
+      const uint32_t v_addr = smem_u32(sV);
+      // Keys 64h .. 64h + 63 of V: its half h, released as soon as they are used.
+      for (int h = 0; h < 2; ++h) {
+        if (!wait_all(v_full[h], gt & 1, kSiteVFull)) return false;
+        tc_fence_after();
 #pragma unroll
-      for (int k = 0; k < BN / 16; ++k)
-        mma_ts_warp(tbase + O_COL, p_tmem + k * 8, sdesc_sw128(v_addr + k * 2048, CHUNK, 1024),
-                    idesc_pv, (lt > 0 || k > 0) ? 1u : 0u);
-      mma_commit_warp(smem_u32(&v_empty[st]));
+        for (int k = 4 * h; k < 4 * h + 4; ++k)
+          mma_ts_warp(tbase + O_COL, p_tmem + k * 8, sdesc_sw128(v_addr + k * 2048, CHUNK, 1024),
+                      idesc_pv, (lt > 0 || k > 0) ? 1u : 0u);
+        mma_commit_warp(smem_u32(&v_empty[h]));
+      }
       mma_commit_warp(smem_u32(&pv_done[gt & 1]));
       return true;
     };
@@ -353,24 +357,27 @@ __global__ void __launch_bounds__(THREADS, 1)
       const Item it = decode_item<C::TQ>(pos, num_q_tiles, gsz, B, H_kv, T, window, pad_lens);
       if (it.pad) continue;
       if (!wait_all(q_full, nitem & 1, kSiteQ)) break;
-      for (int i = 0; i < it.n_tiles; ++i, ++g) {
-        const int st = g % C::KS;
-        if (!wait_all(k_full[st], (g / C::KS) & 1, kSiteKFull)) {
-          ok = false;
-          break;
-        }
+      for (int i = 0; ok && i < it.n_tiles; ++i, ++g) {
         // S buffer g % NS last held P_{g-NS}, whose PV this warp issued
         // before: the tensor pipe runs them in order.
         const int sb = g % C::NS;
-        tc_fence_after();
-        const uint32_t k_addr = smem_u32(sK + st * C::KV_BYTES);
+        const uint32_t k_addr = smem_u32(sK);
+        // Channels 64c .. 64c + 63 of K: its chunk c, released as soon as used.
+        for (int c = 0; c < C::NCH; ++c) {
+          if (!wait_all(k_full[c], g & 1, kSiteKFull)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
 #pragma unroll
-        for (int k = 0; k < DH / 16; ++k) {
-          const uint32_t off = (k >> 2) * CHUNK + (k & 3) * 32;
-          mma_ss_warp(tbase + C::s_col(sb), sdesc_sw128(q_addr + off, 16, 1024),
-                      sdesc_sw128(k_addr + off, 16, 1024), idesc_qk, k > 0 ? 1u : 0u);
+          for (int k = 4 * c; k < 4 * c + 4; ++k) {
+            const uint32_t off = c * CHUNK + (k & 3) * 32;
+            mma_ss_warp(tbase + C::s_col(sb), sdesc_sw128(q_addr + off, 16, 1024),
+                        sdesc_sw128(k_addr + off, 16, 1024), idesc_qk, k > 0 ? 1u : 0u);
+          }
+          mma_commit_warp(smem_u32(&k_empty[c]));
         }
-        mma_commit_warp(smem_u32(&k_empty[st]));
+        if (!ok) break;
         mma_commit_warp(smem_u32(&s_full[sb]));
         if (i == it.n_tiles - 1) mma_commit_warp(smem_u32(&q_empty));
         // S runs LA tiles ahead of PV (S_g reuses the buffer of P_{g-NS},
@@ -614,6 +621,7 @@ cudaError_t launch_cfg(const void* Q, const void* K, const void* V, long ldkv, v
                              static_cast<uint64_t>(B)};
   const uint64_t kstr[2] = {static_cast<uint64_t>(ldkv) * 2, static_cast<uint64_t>(T) * ldkv * 2};
   const uint32_t kbox[3] = {64, BN, 1};
+  const uint32_t vbox[3] = {64, BN / 2, 1};   // V arrives half a tile of keys at a time
   // O [B, T, H, d_h] (16-bit, bf16 or fp16 bits alike): box {32 channels, G
   // heads, 32/G tokens, 1}, 64-byte swizzle.
   CUtensorMap to;
@@ -623,7 +631,7 @@ cudaError_t launch_cfg(const void* Q, const void* K, const void* V, long ldkv, v
     return cudaErrorInvalidValue;
   if (!encode_tiled(&tq, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4, Q, qdims, qstr, qbox) ||
       !encode_tiled(&tk, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, K, kdims, kstr, kbox) ||
-      !encode_tiled(&tv, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, V, kdims, kstr, kbox))
+      !encode_tiled(&tv, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, V, kdims, kstr, vbox))
     return cudaErrorInvalidValue;
   auto kern = attn_fwd_kernel<DH, G>;
   static bool attr_set = false;
