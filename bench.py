@@ -878,19 +878,19 @@ def _oracle_weights(w):
     return _ORACLE_WEIGHTS[w.name]
 
 
-def oracle_sample(w, n_tokens: int):
-    """The fp64 oracle over the first n_tokens of batch row 0 (a causal prefix,
-    so these rows equal the full workload's first rows).  Returns seconds;
-    input generation is outside the timing."""
+def oracle_sample(w, n_tokens: int, row: int = 0):
+    """The fp64 oracle over the first n_tokens of batch row `row` (a causal
+    prefix, so these rows equal the full workload's first rows).  Returns
+    seconds; input generation is outside the timing."""
     import torch
 
     from oracle import gemma3_oracle as O
     ws = WL.small(w, B=1, T=n_tokens, pad=("none",))
-    x = WL.x_rows(w, 0, 0, n_tokens)[None]
+    x = WL.x_rows(w, row, 0, n_tokens)[None]
     pos = WL.segment_pos(ws)
     p = _oracle_weights(w)
     if w.vocab > 0:
-        tok = WL.tokens(w)[:1, :n_tokens]
+        tok = WL.tokens(w)[row:row + 1, :n_tokens]
         tables = WL.model_tables(w)
         t0 = time.perf_counter()
         O.model_forward(tok, tables["E"], p, tables["gamma_final"], model_size=w.model_size,
@@ -917,9 +917,10 @@ def oracle_sample(w, n_tokens: int):
     return time.perf_counter() - t0
 
 
-def oracle_decode_sample(w):
+def oracle_decode_sample(w, budget_s: float = 0.0):
     """The fp64 oracle's cached layer for one decode step of batch row 0
-    (its whole cache).  Returns seconds; input generation is outside."""
+    (its whole cache), repeated until budget_s seconds are measured (at
+    least once).  Returns (seconds, runs); input generation is outside."""
     import torch
 
     from oracle import gemma3_oracle as O
@@ -930,39 +931,61 @@ def oracle_decode_sample(w):
     x = WL.x_full(ws)
     seg = WL.segment_pos(ws)
     p = _oracle_weights(w)
-    t0 = time.perf_counter()
-    O.attention_layer_cached(x, seg, None, cache, w.cache_len - w.T, p["Wq"], p["Wkv"], p["Wo"],
-                             p["gamma_q"], p["gamma_k"], H=w.H, H_kv=w.H_kv, d_h=w.d_h,
-                             attn_type=O.LOCAL_SLIDING if w.attn_type == "local" else O.GLOBAL,
-                             window=w.window, rope_base=w.rope_base, rope_scale=w.rope_scale,
-                             query_scale=w.query_scale)
-    return time.perf_counter() - t0
+    secs, runs = 0.0, 0
+    while runs == 0 or secs < budget_s:
+        t0 = time.perf_counter()
+        O.attention_layer_cached(x, seg, None, cache, w.cache_len - w.T, p["Wq"], p["Wkv"],
+                                 p["Wo"], p["gamma_q"], p["gamma_k"], H=w.H, H_kv=w.H_kv,
+                                 d_h=w.d_h,
+                                 attn_type=O.LOCAL_SLIDING if w.attn_type == "local" else O.GLOBAL,
+                                 window=w.window, rope_base=w.rope_base, rope_scale=w.rope_scale,
+                                 query_scale=w.query_scale)
+        secs += time.perf_counter() - t0
+        runs += 1
+    return secs, runs
 
 
-def sample_tokens(w, budget_s: float) -> int:
-    """Prefix length whose oracle run takes roughly budget_s (probed at 256)."""
-    probe = min(256, w.T)
-    t = oracle_sample(w, probe)
-    n = probe
-    while n < w.T and t * (2 * n / probe) <= budget_s:
-        n *= 2
-    return min(n, w.T, 4096)
+def sample_tokens(w, budget_s: float):
+    """Prefix length of one batch row whose oracle run takes at most about
+    budget_s, found by doubling from 512 tokens with measured times (the
+    attention term grows quadratically, so one doubling at most quadruples
+    the time), up to the row length and to a memory cap: the oracle holds
+    about three fp64 logit tensors of H x n x n, kept under ~4 GB.
+    Returns (n, seconds of the run at n)."""
+    cap = max(1, min(w.T, int((4e9 / (24.0 * w.H)) ** 0.5)))
+    n = min(512, cap)
+    t = oracle_sample(w, n)
+    while n < cap and 4.0 * t <= budget_s:
+        n = min(2 * n, cap)
+        t = oracle_sample(w, n)
+    return n, t
 
 
 def cpu_baseline(w, budget_s: float = 15.0):
     import torch
     if w.cache_len > 0:
-        secs = oracle_decode_sample(w)
-        return {"value": w.T / secs, "unit": "tokens/s", "cores": torch.get_num_threads(),
+        secs, runs = oracle_decode_sample(w, budget_s)
+        return {"value": w.T * runs / secs, "unit": "tokens/s", "cores": torch.get_num_threads(),
                 "kind": "oracle",
-                "sample": f"fp64 oracle, one decode step of batch row 0 of {w.name} over its "
-                          f"{w.cache_len}-slot cache, {secs:.2f} s"}
-    n = sample_tokens(w, budget_s)
-    secs = oracle_sample(w, n)
-    return {"value": n / secs, "unit": "tokens/s", "cores": torch.get_num_threads(),
+                "sample": f"fp64 oracle, decode steps of batch row 0 of {w.name} over its "
+                          f"{w.cache_len}-slot cache: {runs} steps, {secs:.1f} s"}
+    # Rows' prefixes (each row clipped to its valid length), one row after
+    # another, until about budget_s seconds of oracle work are measured.
+    n, _ = sample_tokens(w, budget_s / 2)
+    pads = [int(v) for v in WL.pad_lens(w)]
+    total, tokens, runs = 0.0, 0, 0
+    while runs == 0 or total < budget_s:
+        b = runs % w.B
+        nb = max(1, min(n, w.T - pads[b]))
+        total += oracle_sample(w, nb, b)
+        tokens += nb
+        runs += 1
+    rows = sorted({r % w.B for r in range(runs)})
+    return {"value": tokens / total, "unit": "tokens/s", "cores": torch.get_num_threads(),
             "kind": "oracle",
-            "sample": f"fp64 oracle on the first {n} tokens of batch row 0 of {w.name} "
-                      f"(causal prefix; {w.num_layers} layer(s)), {secs:.2f} s"}
+            "sample": f"fp64 oracle on causal prefixes of up to {n} tokens of batch rows "
+                      f"{rows[0]}..{rows[-1]} of {w.name} ({w.num_layers} layer(s)); "
+                      f"{runs} row runs, {tokens} tokens, {total:.1f} s"}
 
 
 def run_reference(args, world, rank):
@@ -972,9 +995,9 @@ def run_reference(args, world, rank):
     w = WL.WORKLOADS[args.workload]
     if w.cache_len > 0:
         n = w.T
-        run = lambda: oracle_decode_sample(w)          # noqa: E731
+        run = lambda: oracle_decode_sample(w)[0]       # noqa: E731
     else:
-        n = sample_tokens(w, 4.0)
+        n, _ = sample_tokens(w, 4.0)
         run = lambda: oracle_sample(w, n)              # noqa: E731
     for _ in range(args.warmup):
         run()
