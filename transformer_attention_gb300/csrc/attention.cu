@@ -41,6 +41,7 @@
 // other still has to read.)  On tiles without masked elements the row max
 // comes from the TMEM load's own max reduction (tcgen05.ld.red).  O is rescaled in TMEM only when a row max grows by
 // more than 2^8, each warpgroup rescaling its half of the columns.
+#include "attention_common.cuh"
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -51,7 +52,7 @@ namespace {
 constexpr int NUM_WARPS = 12;
 constexpr int THREADS = NUM_WARPS * 32;
 constexpr int BM = 128;   // query rows per CTA
-constexpr int BN = 128;   // keys per KV tile
+constexpr int BN = attn::KV_TILE;   // keys per KV tile
 constexpr int SM_WARPS = 8;  // softmax warps
 constexpr uint32_t CHUNK = 128 * 128;  // one 128-row x 64-element (128 B) swizzled chunk
 constexpr uint32_t O_COL = 256;
@@ -90,62 +91,13 @@ struct Cfg {
   }
 };
 
-__device__ __forceinline__ float fmax3(float a, float b, float c) {
-  float r;
-  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
-  return r;
-}
+using attn::Item;
+using attn::decode_item;
+using attn::ex2;
+using attn::fmax3;
 
-__device__ __forceinline__ float ex2(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-
-// One work item: a query tile of TQ tokens x G heads of kv head j in batch row b.
-struct Item {
-  int b, j, t0, valid, t_last, tile_lo, n_tiles;
-  bool pad;   // every row past the valid length: the item only writes zeros
-};
-
-// Work items are ordered by groups of `gsz` (b, j) pairs whose K/V fit in L2
-// together; within a group the heaviest query tiles come first (longest
-// processing time first for causal layers), the group's (b, j) pairs
-// varying fastest.  Position p of that order -> item.
-template <int TQ>
-__device__ __forceinline__ Item decode_item(int p, int num_q_tiles, int gsz, int B, int H_kv,
-                                            int T, int window, const int32_t* pad_lens) {
-  Item it;
-  const int BH = B * H_kv;
-  const int group = p / (gsz * num_q_tiles);
-  const int base = group * gsz;
-  const int gs = min(gsz, BH - base);
-  const int within = p - group * gsz * num_q_tiles;
-  const int qi = within / gs;
-  const int bj = base + within % gs;
-  it.b = bj / H_kv;
-  it.j = bj % H_kv;
-  it.t0 = (num_q_tiles - 1 - qi) * TQ;
-  it.valid = T - (pad_lens != nullptr ? pad_lens[it.b] : 0);
-  it.pad = it.t0 >= it.valid;
-  it.t_last = min(it.t0 + TQ, it.valid) - 1;
-  const int s_lo = window > 0 ? max(0, it.t0 - window + 1) : 0;
-  it.tile_lo = s_lo / BN;
-  it.n_tiles = it.pad ? 0 : it.t_last / BN - it.tile_lo + 1;
-  return it;
-}
-
-// Static boustrophedon assignment: in round r the CTAs take the next
-// gridDim.x positions, in reverse order on odd rounds, so heavy-first
-// costs even out across CTAs.  Positions grow with r.
-__device__ __forceinline__ int item_position(int r) {
-  return r * static_cast<int>(gridDim.x) +
-         ((r & 1) ? static_cast<int>(gridDim.x) - 1 - static_cast<int>(blockIdx.x)
-                  : static_cast<int>(blockIdx.x));
-}
-
-// Persistent: one CTA per SM walks the positions item_position(0, 1, ...), or
-// with `sched` the positions it takes from that counter (zeroed per launch).
+// Persistent: one CTA per SM walks the static order, or with `sched` the
+// positions it takes from that counter (zeroed per launch).
 // All pipeline phases count tiles (g) and items globally, so the K/V rings
 // run ahead into the next item and the next item's Q is fetched as soon as
 // the current item's last S MMA has consumed the Q buffer.
@@ -177,8 +129,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   __shared__ __align__(1024) uint8_t ostage[SM_WARPS][32 * 64];
   __shared__ uint32_t tmem_sh;
   __shared__ int abort_flag;
-  __shared__ int sched_pos[SCHED_SLOTS];
-  __shared__ __align__(8) uint64_t sched_full[SCHED_SLOTS], sched_empty[SCHED_SLOTS];
+  __shared__ attn::SchedRing<SCHED_SLOTS, SCHED_CONSUMERS> ring;
 
   if (threadIdx.x == 0) {
     mbar_init(smem_u32(&q_full), 1);
@@ -199,10 +150,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_init(smem_u32(&pv_done[s]), 1);
     }
     for (int s = 0; s < 4; ++s) mbar_init(smem_u32(&red_bar[s]), 2);
-    for (int s = 0; s < SCHED_SLOTS; ++s) {
-      mbar_init(smem_u32(&sched_full[s]), 1);
-      mbar_init(smem_u32(&sched_empty[s]), SCHED_CONSUMERS);
-    }
+    ring.init();
     mbar_init(smem_u32(&o_final), 1);
     mbar_init(smem_u32(&o_free), SM_WARPS);
     mbar_init(smem_u32(&drain), 1);
@@ -221,33 +169,13 @@ __global__ void __launch_bounds__(THREADS, 1)
   tc_fence_after();
   const uint32_t tbase = tmem_sh;
 
-  // Position of round rr for the K producer (which takes it from the
-  // scheduler and publishes it) ...
-  auto fetch_pos = [&](int rr) -> int {
-    if (sched == nullptr) return item_position(rr);
-    const int slot = rr % SCHED_SLOTS;
-    if (rr >= SCHED_SLOTS && !mbar_wait(smem_u32(&sched_empty[slot]), ((rr / SCHED_SLOTS) - 1) & 1,
-                                        &abort_flag, status, kSiteSchedEmpty))
-      return num_items;
-    const int p = static_cast<int>(min(atomicAdd(sched, 1u), static_cast<unsigned>(num_items)));
-    *reinterpret_cast<volatile int*>(&sched_pos[slot]) = p;
-    mbar_arrive(smem_u32(&sched_full[slot]));
-    return p;
+  auto fetch_pos = [&](int rr) {
+    return ring.fetch(rr, sched, num_items, &abort_flag, status, kSiteSchedEmpty);
   };
-  // ... and for every other role (a whole warp; lane 0 releases the slot).
-  auto take_pos = [&](int rr) -> int {
-    if (sched == nullptr) return item_position(rr);
-    const int slot = rr % SCHED_SLOTS;
-    if (!mbar_wait(smem_u32(&sched_full[slot]), (rr / SCHED_SLOTS) & 1, &abort_flag, status,
-                   kSiteSchedFull))
-      return num_items;
-    const int p = *reinterpret_cast<volatile int*>(&sched_pos[slot]);
-    return p;
+  auto take_pos = [&](int rr) {
+    return ring.take(rr, sched, num_items, &abort_flag, status, kSiteSchedFull);
   };
-  auto release_pos = [&](int rr) {
-    if (sched == nullptr) return;
-    mbar_arrive(smem_u32(&sched_empty[rr % SCHED_SLOTS]));
-  };
+  auto release_pos = [&](int rr) { ring.release(rr, sched); };
 
   if (warp == 0) {
     if (lane == 0) {
@@ -256,7 +184,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       int kf[C::NCH] = {};  // loads issued per chunk buffer
       bool ok = true;
       for (int rr = 0, pos; ok && (pos = fetch_pos(rr)) < num_items; ++rr) {
-        const Item it = decode_item<C::TQ>(pos, num_q_tiles, gsz, B, H_kv, T, window, pad_lens);
+        const Item it = decode_item(pos, C::TQ, num_q_tiles, gsz, B, H_kv, T, window, pad_lens);
         if (it.pad) continue;
         // The Q buffer is free once the previous item's last S MMA is done.
         if (!mbar_wait(smem_u32(&q_empty), (nq & 1) ^ 1, &abort_flag, status, kSiteQ)) break;
@@ -294,7 +222,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int pos = take_pos(rr);
         release_pos(rr);
         if (pos >= num_items) break;
-        const Item it = decode_item<C::TQ>(pos, num_q_tiles, gsz, B, H_kv, T, window, pad_lens);
+        const Item it = decode_item(pos, C::TQ, num_q_tiles, gsz, B, H_kv, T, window, pad_lens);
         for (int i = 0; ok && i < it.n_tiles; ++i, ++f) {
           for (int h = 0; h < 2; ++h) {
             if (!mbar_wait(smem_u32(&v_empty[h]), (f & 1) ^ 1, &abort_flag, status,
@@ -354,7 +282,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       __syncwarp();
       if (lane == 0) release_pos(rr);
       if (pos >= num_items) break;
-      const Item it = decode_item<C::TQ>(pos, num_q_tiles, gsz, B, H_kv, T, window, pad_lens);
+      const Item it = decode_item(pos, C::TQ, num_q_tiles, gsz, B, H_kv, T, window, pad_lens);
       if (it.pad) continue;
       if (!wait_all(q_full, nitem & 1, kSiteQ)) break;
       for (int i = 0; ok && i < it.n_tiles; ++i, ++g) {
@@ -414,7 +342,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       __syncwarp();
       if (lane == 0) release_pos(rr);
       if (pos >= num_items) break;
-      const Item it = decode_item<C::TQ>(pos, num_q_tiles, gsz, B, H_kv, T, window, pad_lens);
+      const Item it = decode_item(pos, C::TQ, num_q_tiles, gsz, B, H_kv, T, window, pad_lens);
       if (it.pad) {
         // The whole tile is padding: its output rows are zero (bits 0 in bf16 and f16).
         const int rows = min(C::TQ, T - it.t0);
@@ -644,12 +572,7 @@ cudaError_t launch_cfg(const void* Q, const void* K, const void* V, long ldkv, v
   const long items = static_cast<long>(num_q_tiles) * B * H_kv;
   if (items > 0x7fffffffL) return cudaErrorInvalidValue;
   const int grid = static_cast<int>(items < num_sms() ? items : num_sms());
-  // (b, j) pairs per ordering group: as many as keep their K/V (T x d_h x 2
-  // tensors x 2 B) within ~48 MB of L2; local layers touch only a window of
-  // K/V per item, so they use a single group (pure heavy-first order).
-  const double kv_bytes = static_cast<double>(T) * DH * 2.0 * 2.0;
-  int gsz = window > 0 ? B * H_kv : static_cast<int>(48.0 * 1024 * 1024 / kv_bytes);
-  gsz = gsz < 1 ? 1 : (gsz > B * H_kv ? B * H_kv : gsz);
+  const int gsz = attn::l2_group_size(B, H_kv, T, DH, window);
   if (sched != nullptr && cudaMemsetAsync(sched, 0, sizeof(unsigned int), stream) != cudaSuccess)
     return cudaErrorUnknown;
   kern<<<grid, THREADS, C::SMEM, stream>>>(tq, tk, tv, to, static_cast<uint16_t*>(O),

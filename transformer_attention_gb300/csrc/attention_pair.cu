@@ -20,6 +20,7 @@
 // by the same thread (the tensor pipe runs them in order).
 // Every wait is bounded (ptx.cuh); a free CTA takes the next item of the
 // heavy-first order from the scheduler counter, as in attention.cu.
+#include "attention_common.cuh"
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -31,7 +32,7 @@ constexpr int DH = 128;
 constexpr int NUM_WARPS = 12;
 constexpr int THREADS = NUM_WARPS * 32;
 constexpr int BM = 128;                 // query rows per tile
-constexpr int BN = 128;                 // keys per KV tile
+constexpr int BN = attn::KV_TILE;        // keys per KV tile
 constexpr int SM_WARPS = 8;
 constexpr int KS = 2, VS = 2;           // K / V ring depths
 constexpr uint32_t CHUNK = 128 * 128;   // 128 rows x 64 elements (128 B), swizzled
@@ -59,11 +60,8 @@ enum : int {
   kSiteORescale, kSiteOFinal, kSiteOFree, kSiteSchedFull, kSiteSchedEmpty
 };
 
-__device__ __forceinline__ float ex2(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
+using attn::ex2;
+using attn::fmax3;
 
 // Columns outside [lo, hi] of a 32-column group (indices relative to the
 // group, shifted by its first column) become -inf.
@@ -88,50 +86,6 @@ __device__ __forceinline__ void exp_pack16(const uint32_t (&s)[32], uint32_t* p,
   }
 }
 
-__device__ __forceinline__ float fmax3(float a, float b, float c) {
-  float r;
-  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
-  return r;
-}
-
-// A pair of query tiles of TQ tokens each (2 TQ tokens) of kv head j in
-// batch row b.
-struct PairItem {
-  int b, j, t0, valid, tile_lo, n_tiles;
-  bool pad;   // both tiles past the valid length: the item only writes zeros
-};
-
-// Position p of the heavy-first order (groups of gsz (b, j) pairs whose K/V
-// share L2, heaviest pairs first within a group) -> item.
-template <int TQ>
-__device__ __forceinline__ PairItem decode_pair(int p, int num_pairs, int gsz, int B, int H_kv,
-                                                int T, int window, const int32_t* pad_lens) {
-  PairItem it;
-  const int BH = B * H_kv;
-  const int group = p / (gsz * num_pairs);
-  const int base = group * gsz;
-  const int gs = min(gsz, BH - base);
-  const int within = p - group * gsz * num_pairs;
-  const int qi = within / gs;
-  const int bj = base + within % gs;
-  it.b = bj / H_kv;
-  it.j = bj % H_kv;
-  it.t0 = (num_pairs - 1 - qi) * (2 * TQ);
-  it.valid = T - (pad_lens != nullptr ? pad_lens[it.b] : 0);
-  it.pad = it.t0 >= it.valid;
-  const int t_last = min(it.t0 + 2 * TQ, it.valid) - 1;
-  const int s_lo = window > 0 ? max(0, it.t0 - window + 1) : 0;
-  it.tile_lo = s_lo / BN;
-  it.n_tiles = it.pad ? 0 : t_last / BN - it.tile_lo + 1;
-  return it;
-}
-
-__device__ __forceinline__ int static_position(int r) {
-  return r * static_cast<int>(gridDim.x) +
-         ((r & 1) ? static_cast<int>(gridDim.x) - 1 - static_cast<int>(blockIdx.x)
-                  : static_cast<int>(blockIdx.x));
-}
-
 template <int G>
 __global__ void __launch_bounds__(THREADS, 1)
     attn_pair_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -153,8 +107,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       v_empty[VS], s_full[2], p_full[2][2], pv_done[2][2], o_final[2], o_free[2], drain;
   __shared__ uint32_t tmem_sh;
   __shared__ int abort_flag;
-  __shared__ int sched_pos[SCHED_SLOTS];
-  __shared__ __align__(8) uint64_t sched_full[SCHED_SLOTS], sched_empty[SCHED_SLOTS];
+  __shared__ attn::SchedRing<SCHED_SLOTS, SCHED_CONSUMERS> ring;
 
   if (threadIdx.x == 0) {
     mbar_init(smem_u32(&q_full), 1);
@@ -176,10 +129,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         mbar_init(smem_u32(&pv_done[e][s]), 1);
       }
     }
-    for (int s = 0; s < SCHED_SLOTS; ++s) {
-      mbar_init(smem_u32(&sched_full[s]), 1);
-      mbar_init(smem_u32(&sched_empty[s]), SCHED_CONSUMERS);
-    }
+    ring.init();
     mbar_init(smem_u32(&drain), 1);
     abort_flag = 0;
     fence_barrier_init();
@@ -195,28 +145,13 @@ __global__ void __launch_bounds__(THREADS, 1)
   tc_fence_after();
   const uint32_t tbase = tmem_sh;
 
-  auto fetch_pos = [&](int rr) -> int {
-    if (sched == nullptr) return static_position(rr);
-    const int slot = rr % SCHED_SLOTS;
-    if (rr >= SCHED_SLOTS && !mbar_wait(smem_u32(&sched_empty[slot]), ((rr / SCHED_SLOTS) - 1) & 1,
-                                        &abort_flag, status, kSiteSchedEmpty))
-      return num_items;
-    const int p = static_cast<int>(min(atomicAdd(sched, 1u), static_cast<unsigned>(num_items)));
-    *reinterpret_cast<volatile int*>(&sched_pos[slot]) = p;
-    mbar_arrive(smem_u32(&sched_full[slot]));
-    return p;
+  auto fetch_pos = [&](int rr) {
+    return ring.fetch(rr, sched, num_items, &abort_flag, status, kSiteSchedEmpty);
   };
-  auto take_pos = [&](int rr) -> int {
-    if (sched == nullptr) return static_position(rr);
-    const int slot = rr % SCHED_SLOTS;
-    if (!mbar_wait(smem_u32(&sched_full[slot]), (rr / SCHED_SLOTS) & 1, &abort_flag, status,
-                   kSiteSchedFull))
-      return num_items;
-    return *reinterpret_cast<volatile int*>(&sched_pos[slot]);
+  auto take_pos = [&](int rr) {
+    return ring.take(rr, sched, num_items, &abort_flag, status, kSiteSchedFull);
   };
-  auto release_pos = [&](int rr) {
-    if (sched != nullptr) mbar_arrive(smem_u32(&sched_empty[rr % SCHED_SLOTS]));
-  };
+  auto release_pos = [&](int rr) { ring.release(rr, sched); };
 
   // Registers move from the producer / MMA warpgroup to the softmax warpgroups
   // (each warpgroup executes its own setmaxnreg at the top of its branch).
@@ -229,8 +164,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         int f = 0, nq = 0;
         bool ok = true;
         for (int rr = 0, pos; ok && (pos = fetch_pos(rr)) < num_items; ++rr) {
-          const PairItem it =
-              decode_pair<TQ>(pos, num_pairs, gsz, B, H_kv, T, window, pad_lens);
+          const attn::Item it =
+            attn::decode_item(pos, 2 * TQ, num_pairs, gsz, B, H_kv, T, window, pad_lens);
           if (it.pad) continue;
           if (!mbar_wait(smem_u32(&q_empty), (nq & 1) ^ 1, &abort_flag, status, kSiteQ)) break;
           const uint32_t qb = smem_u32(&q_full);
@@ -269,8 +204,8 @@ __global__ void __launch_bounds__(THREADS, 1)
           const int pos = take_pos(rr);
           release_pos(rr);
           if (pos >= num_items) break;
-          const PairItem it =
-              decode_pair<TQ>(pos, num_pairs, gsz, B, H_kv, T, window, pad_lens);
+          const attn::Item it =
+            attn::decode_item(pos, 2 * TQ, num_pairs, gsz, B, H_kv, T, window, pad_lens);
           for (int i = 0; i < it.n_tiles; ++i, ++f) {
             const int st = f % VS;
             if (!mbar_wait(smem_u32(&v_empty[st]), ((f / VS) & 1) ^ 1, &abort_flag, status,
@@ -334,7 +269,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         __syncwarp();
         if (lane == 0) release_pos(rr);
         if (pos >= num_items) break;
-        const PairItem it = decode_pair<TQ>(pos, num_pairs, gsz, B, H_kv, T, window, pad_lens);
+        const attn::Item it =
+            attn::decode_item(pos, 2 * TQ, num_pairs, gsz, B, H_kv, T, window, pad_lens);
         if (it.pad) continue;
         const int n = it.n_tiles;
         if (!wait_all(q_full, nitem & 1, kSiteQ) ||
@@ -400,7 +336,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       __syncwarp();
       if (lane == 0) release_pos(rr);
       if (pos >= num_items) break;
-      const PairItem it = decode_pair<TQ>(pos, num_pairs, gsz, B, H_kv, T, window, pad_lens);
+      const attn::Item it =
+            attn::decode_item(pos, 2 * TQ, num_pairs, gsz, B, H_kv, T, window, pad_lens);
       const int te0 = it.t0 + e * TQ;       // first token of this tile
       if (it.pad) {
         // The whole pair is padding: rows < T of this tile are zero.
@@ -603,9 +540,7 @@ cudaError_t launch_pair_cfg(const void* Q, const void* K, const void* V, long ld
   const long items = static_cast<long>(num_pairs) * B * H_kv;
   if (items > 0x7fffffffL) return cudaErrorInvalidValue;
   const int grid = static_cast<int>(items < num_sms() ? items : num_sms());
-  const double kv_bytes = static_cast<double>(T) * DH * 2.0 * 2.0;
-  int gsz = window > 0 ? B * H_kv : static_cast<int>(48.0 * 1024 * 1024 / kv_bytes);
-  gsz = gsz < 1 ? 1 : (gsz > B * H_kv ? B * H_kv : gsz);
+  const int gsz = attn::l2_group_size(B, H_kv, T, DH, window);
   if (sched != nullptr && cudaMemsetAsync(sched, 0, sizeof(unsigned int), stream) != cudaSuccess)
     return cudaErrorUnknown;
   kern<<<grid, THREADS, SMEM, stream>>>(tq, tk, tv, static_cast<uint16_t*>(O),
