@@ -35,7 +35,9 @@ def _randn(shape, seed, std=1.0, dtype=torch.bfloat16):
 @pytest.mark.parametrize("M,N,K", [(256, 512, 1152), (300, 1152, 4096), (1024, 2048, 2560),
                                    (130, 200, 72), (128, 256, 64), (4096, 1536, 1024),
                                    (1, 2048, 2560), (2, 5376, 4096), (3, 88, 72), (5, 1000, 1160),
-                                   (8, 512, 1152), (16, 4096, 5376), (17, 296, 264)])
+                                   (8, 512, 1152), (16, 4096, 5376), (17, 296, 264),
+                                   # M <= 16 (CUDA-core path): many rows, and a wide K
+                                   (2, 20000, 1024), (4, 64, 16384)])
 @pytest.mark.parametrize("out", ["bf16", "f16", "f32"])
 @pytest.mark.parametrize("inp", ["bf16", "f16"])
 def test_linear_matches_fp64(M, N, K, out, inp):
