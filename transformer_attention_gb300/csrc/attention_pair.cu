@@ -104,7 +104,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint8_t* sK = smem + 2 * QT_BYTES;         // KS stages
   uint8_t* sV = sK + KS * KV_BYTES;          // VS stages
   __shared__ __align__(8) uint64_t q_full, q_empty, k_full[KS], k_empty[KS], v_full[VS],
-      v_empty[VS], s_full[2], p_full[2][2], pv_done[2][2], o_final[2], o_free[2], drain;
+      v_empty[VS], s_full[2], p_full[2][2], o_final[2], o_free[2], drain;
   __shared__ uint32_t tmem_sh;
   __shared__ int abort_flag;
   __shared__ attn::SchedRing<SCHED_SLOTS, SCHED_CONSUMERS> ring;
@@ -126,7 +126,6 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_init(smem_u32(&o_free[e]), 4);
       for (int s = 0; s < 2; ++s) {
         mbar_init(smem_u32(&p_full[e][s]), 4);
-        mbar_init(smem_u32(&pv_done[e][s]), 1);
       }
     }
     ring.init();
@@ -230,6 +229,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       // warp-uniform); each tcgen05 instruction is issued by one elected lane.
       constexpr uint32_t idesc_qk = idesc_f16(BM, BN, /*f16*/ 0, 0, 0);
       constexpr uint32_t idesc_pv = idesc_f16(BM, DH, /*f16*/ 0, 0, /*B MN-major*/ 1);
+      const uint32_t lead = elect_one();   // the lane that issues every tcgen05 instruction
       int nitem = 0;
       int g0 = 0;   // global index of the current item's first tile
       auto wait_all = [&](uint64_t& bar, int parity, int site) -> bool {
@@ -243,10 +243,10 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
         for (int k = 0; k < DH / 16; ++k) {
           const uint32_t off = (k >> 2) * CHUNK + (k & 3) * 32;
-          mma_ss_warp(tbase + s_col(e), sdesc_sw128(q_addr + off, 16, 1024),
+          mma_ss_lead(lead, tbase + s_col(e), sdesc_sw128(q_addr + off, 16, 1024),
                       sdesc_sw128(k_addr + off, 16, 1024), idesc_qk, k > 0 ? 1u : 0u);
         }
-        mma_commit_warp(smem_u32(&s_full[e]));
+        mma_commit_lead(lead, smem_u32(&s_full[e]));
       };
       // PV_e of global tile g, item-local tile i.
       auto issue_pv = [&](int e, int g, int i) -> bool {
@@ -256,10 +256,9 @@ __global__ void __launch_bounds__(THREADS, 1)
         const uint32_t v_addr = smem_u32(sV + (g % VS) * KV_BYTES);
 #pragma unroll
         for (int k = 0; k < BN / 16; ++k)
-          mma_ts_warp(tbase + o_col(e), tbase + s_col(e) + k * 8,
+          mma_ts_lead(lead, tbase + o_col(e), tbase + s_col(e) + k * 8,
                       sdesc_sw128(v_addr + k * 2048, CHUNK, 1024), idesc_pv,
                       (i > 0 || k > 0) ? 1u : 0u);
-        mma_commit_warp(smem_u32(&pv_done[e][g & 1]));
         return true;
       };
       bool ok = true;
@@ -281,8 +280,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         tc_fence_after();
         issue_s(0, g0);
         issue_s(1, g0);
-        mma_commit_warp(smem_u32(&k_empty[g0 % KS]));
-        if (n == 1) mma_commit_warp(smem_u32(&q_empty));
+        mma_commit_lead(lead, smem_u32(&k_empty[g0 % KS]));
+        if (n == 1) mma_commit_lead(lead, smem_u32(&q_empty));
         for (int i = 0; i < n; ++i) {
           const int g = g0 + i;
           if (!wait_all(v_full[g % VS], (g / VS) & 1, kSiteVFull) || !issue_pv(0, g, i)) {
@@ -297,25 +296,25 @@ __global__ void __launch_bounds__(THREADS, 1)
             tc_fence_after();
             issue_s(0, g + 1);
           }
-          if (i + 1 == n) mma_commit_warp(smem_u32(&o_final[0]));   // O0 of this item complete
+          if (i + 1 == n) mma_commit_lead(lead, smem_u32(&o_final[0]));   // O0 of this item complete
           if (!issue_pv(1, g, i)) {
             ok = false;
             break;
           }
-          mma_commit_warp(smem_u32(&v_empty[g % VS]));
+          mma_commit_lead(lead, smem_u32(&v_empty[g % VS]));
           if (i + 1 < n) {
             issue_s(1, g + 1);
-            mma_commit_warp(smem_u32(&k_empty[(g + 1) % KS]));
-            if (i + 1 == n - 1) mma_commit_warp(smem_u32(&q_empty));
+            mma_commit_lead(lead, smem_u32(&k_empty[(g + 1) % KS]));
+            if (i + 1 == n - 1) mma_commit_lead(lead, smem_u32(&q_empty));
           } else {
-            mma_commit_warp(smem_u32(&o_final[1]));
+            mma_commit_lead(lead, smem_u32(&o_final[1]));
           }
         }
         if (!ok) break;
         g0 += n;
         ++nitem;
       }
-      mma_commit_warp(smem_u32(&drain));
+      mma_commit_lead(lead, smem_u32(&drain));
       mbar_wait_drain(smem_u32(&drain), 0);
     }
   } else {
@@ -408,12 +407,9 @@ __global__ void __launch_bounds__(THREADS, 1)
           const float m_new = grow ? mx : m_used;
           const float factor = (m_new == m_used) ? 1.f : ex2(m_used - m_new);
           if (i > 0) {
-            // O_e holds this item's PV so far: rescale once the previous PV landed.
-            ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&pv_done[e][(g - 1) & 1]),
-                                                   ((g - 1) >> 1) & 1, &abort_flag, status,
-                                                   kSiteORescale));
-            if (!ok) break;
-            tc_fence_after();
+            // O_e holds this item's PV so far.  The previous PV_e has landed:
+            // S_e of this tile, whose completion the s_full wait above saw,
+            // was committed after that PV_e was issued.
 #pragma unroll 1
             for (int c = 0; c < DH / 32; ++c) {
               uint32_t ro[32];
