@@ -246,6 +246,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   } else if (warp == 1) {
     // ---------------- MMA issuer: the whole warp runs the loop (its state
     // warp-uniform); each tcgen05 instruction is issued by one elected lane.
+    const uint32_t lead = elect_one();
     constexpr uint32_t idesc_qk = idesc_f16(BM, BN, /*f16*/ 0, 0, 0);
     constexpr uint32_t idesc_pv = idesc_f16(BM, DH, /*f16*/ 0, 0, /*B MN-major*/ 1);
     const uint32_t q_addr = smem_u32(sQ);
@@ -267,11 +268,11 @@ __global__ void __launch_bounds__(THREADS, 1)
         tc_fence_after();
 #pragma unroll
         for (int k = 4 * h; k < 4 * h + 4; ++k)
-          mma_ts_warp(tbase + O_COL, p_tmem + k * 8, sdesc_sw128(v_addr + k * 2048, CHUNK, 1024),
+          mma_ts_lead(lead, tbase + O_COL, p_tmem + k * 8, sdesc_sw128(v_addr + k * 2048, CHUNK, 1024),
                       idesc_pv, (lt > 0 || k > 0) ? 1u : 0u);
-        mma_commit_warp(smem_u32(&v_empty[h]));
+        mma_commit_lead(lead, smem_u32(&v_empty[h]));
       }
-      mma_commit_warp(smem_u32(&pv_done[gt & 1]));
+      mma_commit_lead(lead, smem_u32(&pv_done[gt & 1]));
       return true;
     };
     bool ok = true;
@@ -300,14 +301,14 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
           for (int k = 4 * c; k < 4 * c + 4; ++k) {
             const uint32_t off = c * CHUNK + (k & 3) * 32;
-            mma_ss_warp(tbase + C::s_col(sb), sdesc_sw128(q_addr + off, 16, 1024),
+            mma_ss_lead(lead, tbase + C::s_col(sb), sdesc_sw128(q_addr + off, 16, 1024),
                         sdesc_sw128(k_addr + off, 16, 1024), idesc_qk, k > 0 ? 1u : 0u);
           }
-          mma_commit_warp(smem_u32(&k_empty[c]));
+          mma_commit_lead(lead, smem_u32(&k_empty[c]));
         }
         if (!ok) break;
-        mma_commit_warp(smem_u32(&s_full[sb]));
-        if (i == it.n_tiles - 1) mma_commit_warp(smem_u32(&q_empty));
+        mma_commit_lead(lead, smem_u32(&s_full[sb]));
+        if (i == it.n_tiles - 1) mma_commit_lead(lead, smem_u32(&q_empty));
         // S runs LA tiles ahead of PV (S_g reuses the buffer of P_{g-NS},
         // so LA <= NS - 1): the softmax finds the next S already computed.
         if (i >= C::LA && !issue_pv(g - C::LA, i - C::LA)) {
@@ -320,10 +321,10 @@ __global__ void __launch_bounds__(THREADS, 1)
       for (int d = C::LA; ok && d >= 1; --d)
         if (it.n_tiles - d >= 0 && !issue_pv(g - d, it.n_tiles - d)) ok = false;
       if (!ok) break;
-      mma_commit_warp(smem_u32(&o_final));
+      mma_commit_lead(lead, smem_u32(&o_final));
       ++nitem;
     }
-    mma_commit_warp(smem_u32(&drain));
+    mma_commit_lead(lead, smem_u32(&drain));
     mbar_wait_drain(smem_u32(&drain), 0);
   } else if (warp >= 4) {
     // ---------------- softmax + epilogue

@@ -195,6 +195,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   } else if (warp == 1) {
     // ---------------- MMA issuer: the whole warp runs the loop (its state
     // warp-uniform); each tcgen05 instruction is issued by one elected lane.
+    const uint32_t lead = elect_one();
     const uint32_t idesc = idesc_f16(BM, BN, AB_BF16, 0, 0);
     int stage = 0;
     uint32_t phase = 0;
@@ -218,19 +219,19 @@ __global__ void __launch_bounds__(THREADS, 1)
         const uint32_t b_addr = a_addr + A_BYTES;
 #pragma unroll
         for (int k = 0; k < BK / 16; ++k) {
-          mma_ss_warp(d_tmem, sdesc_sw128(a_addr + k * 32, 16, 1024),
+          mma_ss_lead(lead, d_tmem, sdesc_sw128(a_addr + k * 32, 16, 1024),
                       sdesc_sw128(b_addr + k * 32, 16, 1024), idesc, (kb | k) != 0);
         }
-        mma_commit_warp(smem_u32(&empty_bar[stage]));
+        mma_commit_lead(lead, smem_u32(&empty_bar[stage]));
         if (++stage == STAGES) { stage = 0; phase ^= 1; }
       }
       if (!ok) break;
-      mma_commit_warp(smem_u32(&accf_bar[abuf]));
+      mma_commit_lead(lead, smem_u32(&accf_bar[abuf]));
       abuf ^= 1;
       if (abuf == 0) aphase ^= 1;
     }
     // Drain the tensor pipe before TMEM is released.
-    mma_commit_warp(smem_u32(&drain_bar));
+    mma_commit_lead(lead, smem_u32(&drain_bar));
     mbar_wait_drain(smem_u32(&drain_bar), 0);
   } else if (warp >= 4) {
     // ---------------- epilogue: TMEM -> registers -> swizzled staging -> TMA store
