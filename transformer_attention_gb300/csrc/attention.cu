@@ -76,9 +76,12 @@ struct Cfg {
   static_assert(DH == 256, "d_h = 128 has its own kernel");
   static constexpr int TQ = BM / G;
   static constexpr int NCH = DH / 64;
+  static constexpr int KGRP = 2;            // 64-channel chunks of K per barrier
+  static constexpr int NKB = NCH / KGRP;    // K barriers
   // Q, one K tile and one V tile fill the 227 KB of shared memory; K is
-  // released and refilled per 64-channel chunk (the S MMAs of chunk c are
-  // its only readers), V per half of its 128 keys (the PV MMAs of that half).
+  // released and refilled per KGRP 64-channel chunks (the S MMAs over them
+  // are their only readers), V per half of its 128 keys (the PV MMAs of
+  // that half).
   static constexpr uint32_t Q_BYTES = BM * DH * 2;
   static constexpr uint32_t KV_BYTES = BN * DH * 2;
   static constexpr uint32_t SMEM = Q_BYTES + 2 * KV_BYTES + 1024;
@@ -118,9 +121,9 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   uint8_t* sQ = smem;
-  uint8_t* sK = smem + C::Q_BYTES;                    // chunk c at c * CHUNK
+  uint8_t* sK = smem + C::Q_BYTES;                    // 64-channel chunk c at c * CHUNK
   uint8_t* sV = sK + C::KV_BYTES;                     // key half h at c * CHUNK + h * CHUNK / 2
-  __shared__ __align__(8) uint64_t q_full, q_empty, k_full[C::NCH], k_empty[C::NCH],
+  __shared__ __align__(8) uint64_t q_full, q_empty, k_full[C::NKB], k_empty[C::NKB],
       v_full[2], v_empty[2], s_full[C::NS], p_full[2], pv_done[2],
       o_final, o_free, drain, red_bar[4];
   __shared__ float red[2][2][BM];   // [handshake parity][warpgroup][row]
@@ -134,7 +137,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   if (threadIdx.x == 0) {
     mbar_init(smem_u32(&q_full), 1);
     mbar_init(smem_u32(&q_empty), 1);
-    for (int s = 0; s < C::NCH; ++s) {
+    for (int s = 0; s < C::NKB; ++s) {
       mbar_init(smem_u32(&k_full[s]), 1);
       mbar_init(smem_u32(&k_empty[s]), 1);
     }
@@ -181,7 +184,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (lane == 0) {
       // ---------------- producer: Q of each item, then its K tiles chunk by chunk
       int f = 0, nq = 0;   // K tiles and Q tiles loaded
-      int kf[C::NCH] = {};  // loads issued per chunk buffer
+      int kf[C::NKB] = {};  // loads issued per K barrier
       bool ok = true;
       for (int rr = 0, pos; ok && (pos = fetch_pos(rr)) < num_items; ++rr) {
         const Item it = decode_item(pos, C::TQ, num_q_tiles, gsz, B, H_kv, T, window, pad_lens);
@@ -194,23 +197,24 @@ __global__ void __launch_bounds__(THREADS, 1)
           tma_load_4d(smem_u32(sQ + ch * CHUNK), &tmQ, qb, ch * 64, it.j * G, it.t0, it.b);
         ++nq;
         for (int i = 0; ok && i < it.n_tiles; ++i, ++f) {
-          for (int ch = 0; ch < C::NCH; ++ch) {
-            if (!mbar_wait(smem_u32(&k_empty[ch]), (f & 1) ^ 1, &abort_flag, status,
+          for (int kb = 0; kb < C::NKB; ++kb) {
+            if (!mbar_wait(smem_u32(&k_empty[kb]), (f & 1) ^ 1, &abort_flag, status,
                            kSiteKEmpty)) {
               ok = false;
               break;
             }
-            const uint32_t fb = smem_u32(&k_full[ch]);
-            mbar_arrive_expect_tx(fb, CHUNK);
-            tma_load_3d(smem_u32(sK + ch * CHUNK), &tmK, fb, it.j * DH + ch * 64,
-                        (it.tile_lo + i) * BN, it.b);
-            ++kf[ch];
+            const uint32_t fb = smem_u32(&k_full[kb]);
+            mbar_arrive_expect_tx(fb, C::KGRP * CHUNK);
+            for (int ch = kb * C::KGRP; ch < (kb + 1) * C::KGRP; ++ch)
+              tma_load_3d(smem_u32(sK + ch * CHUNK), &tmK, fb, it.j * DH + ch * 64,
+                          (it.tile_lo + i) * BN, it.b);
+            ++kf[kb];
           }
         }
       }
       if (nq > 0) mbar_wait_drain(smem_u32(&q_full), (nq - 1) & 1);
-      for (int ch = 0; ch < C::NCH; ++ch)
-        if (kf[ch] > 0) mbar_wait_drain(smem_u32(&k_full[ch]), (kf[ch] - 1) & 1);
+      for (int kb = 0; kb < C::NKB; ++kb)
+        if (kf[kb] > 0) mbar_wait_drain(smem_u32(&k_full[kb]), (kf[kb] - 1) & 1);
     }
   } else if (warp == 2) {
     if (lane == 0) {
@@ -291,20 +295,21 @@ __global__ void __launch_bounds__(THREADS, 1)
         // before: the tensor pipe runs them in order.
         const int sb = g % C::NS;
         const uint32_t k_addr = smem_u32(sK);
-        // Channels 64c .. 64c + 63 of K: its chunk c, released as soon as used.
-        for (int c = 0; c < C::NCH; ++c) {
-          if (!wait_all(k_full[c], g & 1, kSiteKFull)) {
+        // Channels of K barrier kb (KGRP 64-channel chunks), released as soon
+        // as their S MMAs have read them.
+        for (int kb = 0; kb < C::NKB; ++kb) {
+          if (!wait_all(k_full[kb], g & 1, kSiteKFull)) {
             ok = false;
             break;
           }
           tc_fence_after();
 #pragma unroll
-          for (int k = 4 * c; k < 4 * c + 4; ++k) {
-            const uint32_t off = c * CHUNK + (k & 3) * 32;
+          for (int k = 4 * C::KGRP * kb; k < 4 * C::KGRP * (kb + 1); ++k) {
+            const uint32_t off = (k >> 2) * CHUNK + (k & 3) * 32;
             mma_ss_lead(lead, tbase + C::s_col(sb), sdesc_sw128(q_addr + off, 16, 1024),
                         sdesc_sw128(k_addr + off, 16, 1024), idesc_qk, k > 0 ? 1u : 0u);
           }
-          mma_commit_lead(lead, smem_u32(&k_empty[c]));
+          mma_commit_lead(lead, smem_u32(&k_empty[kb]));
         }
         if (!ok) break;
         mma_commit_lead(lead, smem_u32(&s_full[sb]));
