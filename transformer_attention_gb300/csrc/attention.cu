@@ -17,13 +17,17 @@
 // band edge, the window edge or the valid length apply an element mask.
 // Work items are ordered in groups of (b, kv-head) pairs whose K/V fit in L2,
 // heaviest query tiles first within a group, and the persistent CTAs (one per
-// SM) take them in boustrophedon rounds, so the items in flight stream the
-// same K/V tiles through L2 together and causal costs even out.
+// SM) take the next position from a counter (or walk the order in
+// boustrophedon rounds without one), so the items in flight stream the same
+// K/V tiles through L2 together and causal costs even out
+// (attention_common.cuh).
 //
 // Warp roles (12 warps):
-//   warp 0      TMA producer of Q (once, 4-D box over [B,T,H,d_h]) and K_i
-//   warp 2      TMA producer of V_i
-//   warp 1      TMEM allocation + single-thread MMA issue:
+//   warp 0      TMA producer of Q (once per item, 4-D box over [B,T,H,d_h])
+//               and K_i, released per half of its channels
+//   warp 2      TMA producer of V_i, released per half of its keys
+//   warp 1      TMEM allocation + MMA issue (the whole warp runs the loop,
+//               one elected lane issues every tcgen05 instruction):
 //                 S  = Q K_i^T   (SS, M=128 N=128, K=d_h)      -> TMEM S
 //                 O += P_i V_i   (TS: P_i read from TMEM,      M=128 N=d_h K=128)
 //   warps 4-11  softmax, two warpgroups: row r of S lives in TMEM lane r; the
@@ -31,16 +35,18 @@
 //               every row, exchanging the row max with its partner thread
 //               through shared memory (a bounded mbarrier handshake).
 // TMEM columns: S buffers at 0-127 and 128-255, O at 256-511.  (d_h = 128
-// runs in attention_pair.cu, two query tiles per CTA.)  The softmax writes P (fp16 pairs) over the first 64
-// columns of the S buffer it has just read, and PV reads it from there; the
-// S of tile i + NS reuses the buffer, issued after PV_i by the same thread,
+// runs in attention_pair.cu, two query tiles per CTA.)  The softmax writes P
+// (fp16 pairs) over the first 64 columns of the S buffer it has just read,
+// and PV reads it from there; the S of tile i + NS reuses the buffer, issued
+// after PV_i by the same warp,
 // so the tensor pipe's in-order execution keeps the two apart and no
 // barrier is needed to release S: the next S starts as soon as the tensor
 // pipe is free.  (The warpgroups' row-max exchange comes after both have
 // loaded their S columns, so one warpgroup's P never overwrites columns the
 // other still has to read.)  On tiles without masked elements the row max
-// comes from the TMEM load's own max reduction (tcgen05.ld.red).  O is rescaled in TMEM only when a row max grows by
-// more than 2^8, each warpgroup rescaling its half of the columns.
+// comes from the TMEM load's own max reduction (tcgen05.ld.red).  O is
+// rescaled in TMEM only when a row max grows by more than 2^8, each
+// warpgroup rescaling its half of the columns.
 #include "attention_common.cuh"
 #include "internal.h"
 #include "ptx.cuh"

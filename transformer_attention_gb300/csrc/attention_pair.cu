@@ -8,16 +8,19 @@
 // tiles stream the same K/V tiles of 128 keys.  Warps:
 //   0      TMA: the pair's Q tiles, then the K ring
 //   2      TMA: the V ring
-//   1      TMEM allocation and single-thread MMA issue
+//   1      TMEM allocation and MMA issue (the whole warp runs the loop,
+//          one elected lane issues every tcgen05 instruction)
 //   4-7    softmax of tile 0, 8-11 softmax of tile 1: one thread per row
-//          over all 128 columns, so the two warpgroups never wait for each
-//          other (no row-max exchange), and each rescales / stores its own O.
+//          holds all 128 columns of S in registers (setmaxnreg moves
+//          registers to these warpgroups), so the two warpgroups never wait
+//          for each other (no row-max exchange), and each rescales and
+//          writes its own O.
 // TMEM: S0 0-127, S1 128-255, O0 256-383, O1 384-511; P_e (fp16 pairs) is
 // written over the first 64 columns of S_e.  The MMA issues S0_0, S1_0 and
 // then, per KV tile i: PV0_i, S0_{i+1}, PV1_i, S1_{i+1}.  While one
 // warpgroup computes its exponentials the tensor pipe runs the other tile's
 // products; S_e of tile i+1 reuses S_e after PV_e of tile i, issued before it
-// by the same thread (the tensor pipe runs them in order).
+// by the same warp (the tensor pipe runs them in order).
 // Every wait is bounded (ptx.cuh); a free CTA takes the next item of the
 // heavy-first order from the scheduler counter, as in attention.cu.
 #include "attention_common.cuh"

@@ -9,7 +9,8 @@
 //   warp 0      TMA producer: 128x64 A and 256x64 W tiles, 128-byte swizzle,
 //               into a 4-stage shared-memory ring (48 KB per stage).
 //   warp 1      allocates 512 TMEM columns and issues tcgen05.mma
-//               (M=128, N=256, K=16) from one thread; accumulators live in
+//               (M=128, N=256, K=16): the whole warp runs the loop, one
+//               elected lane issues each instruction; accumulators live in
 //               TMEM, double-buffered (2 x 256 columns) so the epilogue of one
 //               tile overlaps the main loop of the next.
 //   warps 4-7   epilogue: tcgen05.ld of the accumulator rows (one TMEM lane
