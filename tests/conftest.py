@@ -11,3 +11,18 @@ if ROOT not in sys.path:
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (sm_103a) and the built library")
     config.addinivalue_line("markers", "slow: long-running parity case")
+
+
+def pytest_terminal_summary(terminalreporter):
+    """The GPU parity errors next to the bf16 rounding floor of each case."""
+    try:
+        from tests import helpers
+    except Exception:   # pragma: no cover - helpers not imported in this run
+        return
+    if not helpers.RESULTS:
+        return
+    tr = terminalreporter
+    tr.section("parity against the fp64 oracle (GPU error | bf16 floor of the oracle)")
+    tr.write_line(f"{'case':60s} {'rel_frob':>10s} {'max_abs':>10s} | {'rel_frob':>10s} {'max_abs':>10s}")
+    for what, rf, ma, frf, fma in helpers.RESULTS:
+        tr.write_line(f"{what[:60]:60s} {rf:10.3e} {ma:10.3e} | {frf:10.3e} {fma:10.3e}")

@@ -22,9 +22,25 @@ def max_abs(got: torch.Tensor, ref: torch.Tensor) -> float:
     return float((got.to(torch.float64) - ref.to(torch.float64)).abs().max())
 
 
+# Every assert_close records (what, GPU rel_frob, GPU max_abs, floor rel_frob,
+# floor max_abs); the floor is the error of the oracle itself rounded to
+# bf16 (round to nearest even), the least a bf16 output can show.  The
+# conftest prints the table at the end of the run.
+RESULTS: list = []
+
+
+def bf16_floor(ref: torch.Tensor):
+    ref64 = ref.to(torch.float64)
+    r = ref64.to(torch.bfloat16)
+    return rel_frob(r, ref64), max_abs(r, ref64)
+
+
 def assert_close(got, ref, what=""):
     rf, ma = rel_frob(got, ref), max_abs(got, ref)
-    assert rf <= REL_FROB and ma <= MAX_ABS, f"{what}: rel_frob={rf:.3e} max_abs={ma:.3e}"
+    frf, fma = bf16_floor(ref)
+    RESULTS.append((what, rf, ma, frf, fma))
+    assert rf <= REL_FROB and ma <= MAX_ABS, (
+        f"{what}: rel_frob={rf:.3e} max_abs={ma:.3e} (bf16 floor {frf:.3e} / {fma:.3e})")
     return rf, ma
 
 
