@@ -118,6 +118,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                     const int32_t* __restrict__ pad_lens, int B, int T, int H, int H_kv,
                     int window, int num_q_tiles, int gsz, int num_items, unsigned int* sched,
                     int* status) {
+  pdl_enter();
   using C = Cfg<DH, G>;
   // After a CTA of this or an earlier launch gave up, the rest do no work.
   if (*reinterpret_cast<volatile int*>(status) != 0) return;
@@ -587,11 +588,9 @@ cudaError_t launch_cfg(const void* Q, const void* K, const void* V, long ldkv, v
   const int gsz = attn::l2_group_size(B, H_kv, T, DH, window);
   if (sched != nullptr && cudaMemsetAsync(sched, 0, sizeof(unsigned int), stream) != cudaSuccess)
     return cudaErrorUnknown;
-  kern<<<grid, THREADS, C::SMEM, stream>>>(tq, tk, tv, to, static_cast<uint16_t*>(O),
-                                           o_dtype == kF16 ? 1 : 0, pad_lens, B, T, H, H_kv,
-                                           window, num_q_tiles, gsz, static_cast<int>(items),
-                                           sched, status);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(grid), dim3(THREADS), C::SMEM, stream, tq, tk, tv, to,
+                    static_cast<uint16_t*>(O), o_dtype == kF16 ? 1 : 0, pad_lens, B, T, H, H_kv,
+                    window, num_q_tiles, gsz, static_cast<int>(items), sched, status);
 }
 
 }  // namespace

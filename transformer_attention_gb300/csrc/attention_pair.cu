@@ -96,6 +96,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                      uint16_t* __restrict__ O, int o_f16, const int32_t* __restrict__ pad_lens,
                      int B, int T, int H, int H_kv, int window, int num_pairs, int gsz,
                      int num_items, unsigned int* sched, int* status) {
+  pdl_enter();
   constexpr int TQ = BM / G;
   if (*reinterpret_cast<volatile int*>(status) != 0) return;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -542,10 +543,9 @@ cudaError_t launch_pair_cfg(const void* Q, const void* K, const void* V, long ld
   const int gsz = attn::l2_group_size(B, H_kv, T, DH, window);
   if (sched != nullptr && cudaMemsetAsync(sched, 0, sizeof(unsigned int), stream) != cudaSuccess)
     return cudaErrorUnknown;
-  kern<<<grid, THREADS, SMEM, stream>>>(tq, tk, tv, static_cast<uint16_t*>(O),
-                                        o_dtype == kF16 ? 1 : 0, pad_lens, B, T, H, H_kv, window,
-                                        num_pairs, gsz, static_cast<int>(items), sched, status);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(grid), dim3(THREADS), SMEM, stream, tq, tk, tv,
+                    static_cast<uint16_t*>(O), o_dtype == kF16 ? 1 : 0, pad_lens, B, T, H, H_kv,
+                    window, num_pairs, gsz, static_cast<int>(items), sched, status);
 }
 
 }  // namespace

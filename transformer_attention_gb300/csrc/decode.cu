@@ -116,6 +116,7 @@ __global__ void __launch_bounds__(128) kv_cache_append_kernel(
     const int32_t* __restrict__ segment_pos, const int32_t* __restrict__ pad_lens, int T, int S,
     int end, int KVD, __half* __restrict__ Kc, __half* __restrict__ Vc,
     int32_t* __restrict__ posc) {
+  pdl_enter();
   const int t = blockIdx.x, b = blockIdx.y;
   const size_t src = (static_cast<size_t>(b) * T + t) * ld;
   const size_t slot = static_cast<size_t>(b) * S + end + t;
@@ -141,6 +142,7 @@ __global__ void __launch_bounds__(256) kv_span_kernel(
     const int32_t* __restrict__ posc, const int32_t* __restrict__ qpos,
     const int32_t* __restrict__ pad_lens, int T, int S, int end, int window, int nchunk,
     int32_t* __restrict__ span_part) {
+  pdl_enter();
   __shared__ int red[8];
   const int c = blockIdx.x, b = blockIdx.y;
   const int valid = T - (pad_lens != nullptr ? pad_lens[b] : 0);
@@ -223,6 +225,7 @@ template <int DH, int RB>
 __global__ void __launch_bounds__(kDecThreads, 2)
     decode_attn_kernel(const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, const DecParams p) {
+  pdl_enter();
   using C = DecCfg<DH, RB>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -530,6 +533,7 @@ __global__ void __launch_bounds__(kDecThreads, 2)
 template <int DH>
 __global__ void __launch_bounds__(DH) decode_combine_kernel(const float* __restrict__ part,
                                                             void* O, int o_f16, int nsplit) {
+  pdl_enter();
   constexpr int REC = DH + 4, NW = DH / 32;
   __shared__ float fw[NW][kMaxCombineSplits];
   const int wid = threadIdx.x >> 5, lane = threadIdx.x & 31, c = threadIdx.x;
@@ -595,8 +599,7 @@ cudaError_t launch_decode_cfg(const CUtensorMap& tk, const CUtensorMap& tv, cons
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  kern<<<grid, kDecThreads, C::SMEM, stream>>>(tk, tv, p);
-  return cudaGetLastError();
+  return launch_pdl(kern, grid, dim3(kDecThreads), C::SMEM, stream, tk, tv, p);
 }
 
 }  // namespace
@@ -607,11 +610,10 @@ cudaError_t launch_kv_cache_append(const void* K_rows, const void* V_rows, long 
                                    int32_t* pos_cache, cudaStream_t stream) {
   if (B <= 0 || T <= 0) return cudaSuccess;
   if (B > 65535) return cudaErrorInvalidValue;
-  kv_cache_append_kernel<<<dim3(T, B), 128, 0, stream>>>(
-      static_cast<const __half*>(K_rows), static_cast<const __half*>(V_rows), ld, segment_pos,
-      pad_lens, T, S, end, KVD, static_cast<__half*>(K_cache), static_cast<__half*>(V_cache),
-      pos_cache);
-  return cudaGetLastError();
+  return launch_pdl(kv_cache_append_kernel, dim3(T, B), dim3(128), 0, stream,
+                    static_cast<const __half*>(K_rows), static_cast<const __half*>(V_rows), ld,
+                    segment_pos, pad_lens, T, S, end, KVD, static_cast<__half*>(K_cache),
+                    static_cast<__half*>(V_cache), pos_cache);
 }
 
 size_t cached_attention_ws_bytes(int B, int T, int S, int H, int H_kv, int d_h) {
@@ -653,9 +655,8 @@ cudaError_t launch_cached_attention(const void* Q, const void* K_cache, const vo
   if (nsplit < 1) nsplit = 1;
 
   if (window > 0) {
-    kv_span_kernel<<<dim3(nchunk, B), 256, 0, stream>>>(pos_cache, qpos, pad_lens, T, S, end,
-                                                         window, nchunk, span_part);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_pdl(kv_span_kernel, dim3(nchunk, B), dim3(256), 0, stream, pos_cache,
+                               qpos, pad_lens, T, S, end, window, nchunk, span_part);
     if (e != cudaSuccess) return e;
   }
 
@@ -705,10 +706,10 @@ cudaError_t launch_cached_attention(const void* Q, const void* K_cache, const vo
   if (e != cudaSuccess || nsplit == 1) return e;
   const int rows = B * T * H;
   if (d_h == 256)
-    decode_combine_kernel<256><<<rows, 256, 0, stream>>>(part, O, p.o_f16, nsplit);
-  else
-    decode_combine_kernel<128><<<rows, 128, 0, stream>>>(part, O, p.o_f16, nsplit);
-  return cudaGetLastError();
+    return launch_pdl(decode_combine_kernel<256>, dim3(rows), dim3(256), 0, stream,
+                      static_cast<const float*>(part), O, p.o_f16, nsplit);
+  return launch_pdl(decode_combine_kernel<128>, dim3(rows), dim3(128), 0, stream,
+                    static_cast<const float*>(part), O, p.o_f16, nsplit);
 }
 
 }  // namespace g3

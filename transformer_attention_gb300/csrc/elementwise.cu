@@ -42,6 +42,7 @@ __global__ void __launch_bounds__(256, 2)
                         const __nv_bfloat16* __restrict__ gamma_k, const int32_t* __restrict__ pos,
                         int M, int H, int H_kv, const __grid_constant__ RopeFreqs freqs,
                         float query_scale) {
+  pdl_enter();
   constexpr int LPV = DH / 8;      // lanes per head vector
   constexpr int VPW = 32 / LPV;    // head vectors per warp step
   constexpr int HALF = LPV / 2;    // lane distance of the RoPE partner
@@ -154,6 +155,7 @@ template <typename T, bool OUT_F16>
 __global__ void __launch_bounds__(256)
     rmsnorm_rows_kernel(const T* __restrict__ x, const __nv_bfloat16* __restrict__ gamma,
                         uint16_t* __restrict__ u, int M, int D) {
+  pdl_enter();
   const int lane = threadIdx.x & 31;
   const int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (row >= M) return;
@@ -187,6 +189,7 @@ __global__ void __launch_bounds__(256)
 // bf16 -> fp16, 8 elements per thread per step (n % 8 == 0, 16-byte aligned).
 __global__ void __launch_bounds__(256)
     cast_bf16_f16_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst, size_t n8) {
+  pdl_enter();
   for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n8;
        i += static_cast<size_t>(gridDim.x) * blockDim.x) {
     const uint4 v = src[i];
@@ -206,6 +209,7 @@ template <typename T>
 __global__ void __launch_bounds__(256)
     postnorm_residual_kernel(const float* __restrict__ a, const T* x,
                              const __nv_bfloat16* __restrict__ gamma, float* y, int M, int D) {
+  pdl_enter();
   const int lane = threadIdx.x & 31;
   const int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (row >= M) return;
@@ -250,14 +254,12 @@ cudaError_t launch_qk_norm_rope(void* Q, long ldq, void* K, long ldk, const void
   auto gq = static_cast<const __nv_bfloat16*>(gamma_q);
   auto gk = static_cast<const __nv_bfloat16*>(gamma_k);
   if (d_h == 256)
-    qk_norm_rope_kernel<256><<<blocks, 256, 0, stream>>>(q, ldq, k, ldk, gq, gk, pos, M, H, H_kv,
-                                                         freqs, query_scale);
-  else if (d_h == 128)
-    qk_norm_rope_kernel<128><<<blocks, 256, 0, stream>>>(q, ldq, k, ldk, gq, gk, pos, M, H, H_kv,
-                                                         freqs, query_scale);
-  else
-    return cudaErrorInvalidValue;
-  return cudaGetLastError();
+    return launch_pdl(qk_norm_rope_kernel<256>, dim3(blocks), dim3(256), 0, stream, q, ldq, k,
+                      ldk, gq, gk, pos, M, H, H_kv, freqs, query_scale);
+  if (d_h == 128)
+    return launch_pdl(qk_norm_rope_kernel<128>, dim3(blocks), dim3(256), 0, stream, q, ldq, k,
+                      ldk, gq, gk, pos, M, H, H_kv, freqs, query_scale);
+  return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_rmsnorm_rows(const void* x, int x_dtype, const void* gamma, void* u,
@@ -268,18 +270,21 @@ cudaError_t launch_rmsnorm_rows(const void* x, int x_dtype, const void* gamma, v
   auto uo = static_cast<uint16_t*>(u);
   if (u_dtype != kBF16 && u_dtype != kF16) return cudaErrorInvalidValue;
   const bool f16 = u_dtype == kF16;
+  const dim3 grid(blocks), block(256);
   if (x_dtype == kF32) {
     auto xp = static_cast<const float*>(x);
-    if (f16) rmsnorm_rows_kernel<float, true><<<blocks, 256, 0, stream>>>(xp, g, uo, M, D);
-    else rmsnorm_rows_kernel<float, false><<<blocks, 256, 0, stream>>>(xp, g, uo, M, D);
-  } else if (x_dtype == kBF16) {
-    auto xp = static_cast<const __nv_bfloat16*>(x);
-    if (f16) rmsnorm_rows_kernel<__nv_bfloat16, true><<<blocks, 256, 0, stream>>>(xp, g, uo, M, D);
-    else rmsnorm_rows_kernel<__nv_bfloat16, false><<<blocks, 256, 0, stream>>>(xp, g, uo, M, D);
-  } else {
-    return cudaErrorInvalidValue;
+    return f16 ? launch_pdl(rmsnorm_rows_kernel<float, true>, grid, block, 0, stream, xp, g, uo, M, D)
+               : launch_pdl(rmsnorm_rows_kernel<float, false>, grid, block, 0, stream, xp, g, uo,
+                            M, D);
   }
-  return cudaGetLastError();
+  if (x_dtype == kBF16) {
+    auto xp = static_cast<const __nv_bfloat16*>(x);
+    return f16 ? launch_pdl(rmsnorm_rows_kernel<__nv_bfloat16, true>, grid, block, 0, stream, xp,
+                            g, uo, M, D)
+               : launch_pdl(rmsnorm_rows_kernel<__nv_bfloat16, false>, grid, block, 0, stream, xp,
+                            g, uo, M, D);
+  }
+  return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_cast_bf16_f16(const void* src, void* dst, size_t n, cudaStream_t stream) {
@@ -289,9 +294,8 @@ cudaError_t launch_cast_bf16_f16(const void* src, void* dst, size_t n, cudaStrea
   long blocks = static_cast<long>((n8 + 255) / 256);
   const long cap = static_cast<long>(num_sms()) * 8;
   if (blocks > cap) blocks = cap;
-  cast_bf16_f16_kernel<<<blocks, 256, 0, stream>>>(static_cast<const uint4*>(src),
-                                                   static_cast<uint4*>(dst), n8);
-  return cudaGetLastError();
+  return launch_pdl(cast_bf16_f16_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream,
+                    static_cast<const uint4*>(src), static_cast<uint4*>(dst), n8);
 }
 
 namespace {
@@ -302,6 +306,7 @@ __global__ void __launch_bounds__(256) embed_rows_kernel(const int32_t* __restri
                                                          const __nv_bfloat16* __restrict__ E,
                                                          int V, int D, int M, float scale,
                                                          float* __restrict__ x, int* status) {
+  pdl_enter();
   const int m = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
   if (m >= M) return;
   const int t = tokens[m];
@@ -334,9 +339,8 @@ __global__ void __launch_bounds__(256) embed_rows_kernel(const int32_t* __restri
 cudaError_t launch_embed_rows(const int32_t* tokens, const void* E, int V, int D, int M,
                               float scale, float* x, cudaStream_t stream, int* status) {
   if (M <= 0) return cudaSuccess;
-  embed_rows_kernel<<<(M + 7) / 8, 256, 0, stream>>>(
-      tokens, static_cast<const __nv_bfloat16*>(E), V, D, M, scale, x, status);
-  return cudaGetLastError();
+  return launch_pdl(embed_rows_kernel, dim3((M + 7) / 8), dim3(256), 0, stream, tokens,
+                    static_cast<const __nv_bfloat16*>(E), V, D, M, scale, x, status);
 }
 
 cudaError_t launch_postnorm_residual(const float* a, const void* x, int x_dtype,
@@ -346,14 +350,12 @@ cudaError_t launch_postnorm_residual(const float* a, const void* x, int x_dtype,
   const int blocks = (M + 7) / 8;
   auto g = static_cast<const __nv_bfloat16*>(gamma);
   if (x_dtype == kF32)
-    postnorm_residual_kernel<float><<<blocks, 256, 0, stream>>>(a, static_cast<const float*>(x), g,
-                                                                y, M, D);
-  else if (x_dtype == kBF16)
-    postnorm_residual_kernel<__nv_bfloat16><<<blocks, 256, 0, stream>>>(
-        a, static_cast<const __nv_bfloat16*>(x), g, y, M, D);
-  else
-    return cudaErrorInvalidValue;
-  return cudaGetLastError();
+    return launch_pdl(postnorm_residual_kernel<float>, dim3(blocks), dim3(256), 0, stream, a,
+                      static_cast<const float*>(x), g, y, M, D);
+  if (x_dtype == kBF16)
+    return launch_pdl(postnorm_residual_kernel<__nv_bfloat16>, dim3(blocks), dim3(256), 0, stream,
+                      a, static_cast<const __nv_bfloat16*>(x), g, y, M, D);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace g3

@@ -108,6 +108,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                    const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmB2,
                    const __grid_constant__ CUtensorMap tmC2, int M, int N, int K, int* status,
                    const __grid_constant__ QkEpi epi) {
+  pdl_enter();
   constexpr bool GEGLU = EPI == kEpiGeglu;
   static_assert(EPI != kEpiQkNorm || (std::is_same<OutT, __half>::value && (DH == 128 || DH == 256)),
                 "the QK-norm epilogue writes fp16 head vectors of 128 or 256");
@@ -471,9 +472,8 @@ cudaError_t launch_typed(const CUtensorMap& ta, const CUtensorMap& tb, void* C, 
   int grid = num_sms();
   if (max_ctas > 0 && max_ctas < grid) grid = max_ctas;
   if (tiles < grid) grid = tiles;
-  kern<<<grid, THREADS, SMEM_BYTES, stream>>>(ta, tb, tc, tb2 != nullptr ? *tb2 : tb, tc2, M, N,
-                                               K, status, epi);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(grid), dim3(THREADS), SMEM_BYTES, stream, ta, tb, tc,
+                    tb2 != nullptr ? *tb2 : tb, tc2, M, N, K, status, epi);
 }
 
 bool encode_ab(CUtensorMap& ta, CUtensorMap& tb, const void* A, long lda, const void* W, long ldw,

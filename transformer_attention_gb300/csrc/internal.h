@@ -18,6 +18,26 @@ bool encode_tiled(CUtensorMap* map, CUtensorMapDataType dt, int rank, const void
 
 int num_sms();
 
+// Launch `kern` on `stream` with programmatic dependent launch allowed: the
+// grid may start while the previous kernel on the stream is finishing, and
+// its pdl_enter() (ptx.cuh) waits for that kernel before any global-memory
+// access.  Only kernels that begin with pdl_enter() are launched this way.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
+}
+
 // C[M,N] = A[M,K] * W[N,K]^T, operands in in_dtype (bf16|f16), fp32
 // accumulation, C in out_dtype.  M <= kSkinnyMaxRows goes to
 // launch_linear_skinny, everything else to the tcgen05 GEMM.

@@ -21,6 +21,16 @@ enum : int {
   kDevErrBadToken = 0x2000,      // a token id outside [0, V)
 };
 
+// Programmatic dependent launch.  Every kernel of the library is launched
+// so that it may start while the kernel before it on the stream finishes
+// (launch_pdl, internal.h); its first statement waits until that kernel
+// has completed and its writes are visible, then lets the next kernel
+// launch.  Nothing touches global memory before this point.
+__device__ __forceinline__ void pdl_enter() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }

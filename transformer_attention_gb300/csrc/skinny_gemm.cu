@@ -65,6 +65,7 @@ template <typename InT, typename OutT, int MB>
 __global__ void __launch_bounds__(kWarps * 32) skinny_gemm_kernel(
     const InT* __restrict__ A, long lda, const InT* __restrict__ W, long ldw,
     OutT* __restrict__ C, long ldc, int M, int N, int K) {
+  pdl_enter();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n0 = (blockIdx.x * kWarps + warp) * kRows;
   if (n0 >= N) return;
@@ -129,16 +130,15 @@ cudaError_t launch_skinny_typed(const void* A, long lda, const void* W, long ldw
   const InT* a = static_cast<const InT*>(A);
   const InT* w = static_cast<const InT*>(W);
   OutT* c = static_cast<OutT*>(C);
+  const dim3 block(kWarps * 32);
   if (M <= 4)
-    skinny_gemm_kernel<InT, OutT, 4><<<grid, kWarps * 32, 0, stream>>>(a, lda, w, ldw, c, ldc, M,
-                                                                       N, K);
-  else if (M <= 8)
-    skinny_gemm_kernel<InT, OutT, 8><<<grid, kWarps * 32, 0, stream>>>(a, lda, w, ldw, c, ldc, M,
-                                                                       N, K);
-  else
-    skinny_gemm_kernel<InT, OutT, 16><<<grid, kWarps * 32, 0, stream>>>(a, lda, w, ldw, c, ldc,
-                                                                        M, N, K);
-  return cudaGetLastError();
+    return launch_pdl(skinny_gemm_kernel<InT, OutT, 4>, grid, block, 0, stream, a, lda, w, ldw, c,
+                      ldc, M, N, K);
+  if (M <= 8)
+    return launch_pdl(skinny_gemm_kernel<InT, OutT, 8>, grid, block, 0, stream, a, lda, w, ldw, c,
+                      ldc, M, N, K);
+  return launch_pdl(skinny_gemm_kernel<InT, OutT, 16>, grid, block, 0, stream, a, lda, w, ldw, c,
+                    ldc, M, N, K);
 }
 
 }  // namespace
