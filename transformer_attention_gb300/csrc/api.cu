@@ -124,6 +124,10 @@ int attn_pipeline(const gemma3_attn_dims* d, const void* x, int act_dtype,
   const AttnWs w = attn_ws(d, f16);
   void* qbuf = ws;                // Q then Q' (fp16), then O, [M, H*d_h]
   void* kvbuf = ws + w.q_bytes;   // [K'|V] fp16, [M, 2*H_kv*d_h]
+  // The attention's work counter is zeroed first, so that the projection,
+  // attention and output-projection kernels follow each other directly.
+  void* sched = ws + w.q_bytes + w.kv_bytes + w.w_bytes;
+  if (cudaMemsetAsync(sched, 0, sizeof(unsigned int), s) != cudaSuccess) return GEMMA3_ERR_CUDA;
   cudaError_t e;
   if (f16) {
     uint8_t* wb = ws + w.q_bytes + w.kv_bytes;
@@ -142,10 +146,9 @@ int attn_pipeline(const gemma3_attn_dims* d, const void* x, int act_dtype,
                  d->D, d->H, d->H_kv, d->d_h, rope_base, rope_scale, query_scale, s, st);
   if (e != cudaSuccess) return GEMMA3_ERR_CUDA;
   const int win = attn_type == GEMMA3_LOCAL_SLIDING ? window : 0;
-  void* sched = ws + w.q_bytes + w.kv_bytes + w.w_bytes;
   e = launch_flash_attention(qbuf, kvbuf, static_cast<uint8_t*>(kvbuf) + KVD * 2, 2 * KVD, qbuf,
                              act_dtype, pad_lens, d->B, d->T, d->H, d->H_kv, d->d_h, win, sched, s,
-                             st);
+                             st, /*sched_zeroed=*/true);
   if (e != cudaSuccess) return GEMMA3_ERR_CUDA;
   e = launch_linear(qbuf, HD, Wo, HD, out, d->D, M, d->D, HD, act_dtype, out_dtype, s, st, 0);
   return to_status(e);

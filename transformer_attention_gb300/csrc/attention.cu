@@ -548,7 +548,8 @@ __global__ void __launch_bounds__(THREADS, 1)
 template <int DH, int G>
 cudaError_t launch_cfg(const void* Q, const void* K, const void* V, long ldkv, void* O,
                        int o_dtype, const int32_t* pad_lens, int B, int T, int H, int H_kv,
-                       int window, unsigned int* sched, cudaStream_t stream, int* status) {
+                       int window, unsigned int* sched, cudaStream_t stream, int* status,
+                       bool sched_zeroed) {
   using C = Cfg<DH, G>;
   CUtensorMap tq, tk, tv;
   // Q' [B, T, H, d_h]: box {64 of d_h, the G heads of one group, TQ tokens, 1}.
@@ -586,7 +587,8 @@ cudaError_t launch_cfg(const void* Q, const void* K, const void* V, long ldkv, v
   if (items > 0x7fffffffL) return cudaErrorInvalidValue;
   const int grid = static_cast<int>(items < num_sms() ? items : num_sms());
   const int gsz = attn::l2_group_size(B, H_kv, T, DH, window);
-  if (sched != nullptr && cudaMemsetAsync(sched, 0, sizeof(unsigned int), stream) != cudaSuccess)
+  if (sched != nullptr && !sched_zeroed &&
+      cudaMemsetAsync(sched, 0, sizeof(unsigned int), stream) != cudaSuccess)
     return cudaErrorUnknown;
   return launch_pdl(kern, dim3(grid), dim3(THREADS), C::SMEM, stream, tq, tk, tv, to,
                     static_cast<uint16_t*>(O), o_dtype == kF16 ? 1 : 0, pad_lens, B, T, H, H_kv,
@@ -598,17 +600,17 @@ cudaError_t launch_cfg(const void* Q, const void* K, const void* V, long ldkv, v
 cudaError_t launch_flash_attention(const void* Q, const void* K, const void* V, long ldkv,
                                    void* O, int o_dtype, const int32_t* pad_lens, int B, int T,
                                    int H, int H_kv, int d_h, int window, void* sched,
-                                   cudaStream_t stream, int* status) {
+                                   cudaStream_t stream, int* status, bool sched_zeroed) {
   if (B <= 0 || T <= 0) return cudaSuccess;
   if (o_dtype != kBF16 && o_dtype != kF16) return cudaErrorInvalidValue;
   if (d_h == 128)
     return launch_flash_attention_pair(Q, K, V, ldkv, O, o_dtype, pad_lens, B, T, H, H_kv, window,
-                                       sched, stream, status);
+                                       sched, stream, status, sched_zeroed);
   const int G = H / H_kv;
 #define G3_ATTN_CASE(DH_, G_)                                                                   \
   if (d_h == DH_ && G == G_)                                                                    \
     return launch_cfg<DH_, G_>(Q, K, V, ldkv, O, o_dtype, pad_lens, B, T, H, H_kv, window,        \
-                               static_cast<unsigned int*>(sched), stream, status);
+                               static_cast<unsigned int*>(sched), stream, status, sched_zeroed);
   G3_ATTN_CASE(256, 1)
   G3_ATTN_CASE(256, 2)
   G3_ATTN_CASE(256, 4)

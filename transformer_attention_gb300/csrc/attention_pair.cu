@@ -502,7 +502,8 @@ __global__ void __launch_bounds__(THREADS, 1)
 template <int G>
 cudaError_t launch_pair_cfg(const void* Q, const void* K, const void* V, long ldkv, void* O,
                             int o_dtype, const int32_t* pad_lens, int B, int T, int H, int H_kv,
-                            int window, unsigned int* sched, cudaStream_t stream, int* status) {
+                            int window, unsigned int* sched, cudaStream_t stream, int* status,
+                            bool sched_zeroed) {
   constexpr int TQ = BM / G;
   CUtensorMap tq, tk, tv;
   const uint64_t qdims[4] = {static_cast<uint64_t>(DH), static_cast<uint64_t>(H),
@@ -541,7 +542,8 @@ cudaError_t launch_pair_cfg(const void* Q, const void* K, const void* V, long ld
   if (items > 0x7fffffffL) return cudaErrorInvalidValue;
   const int grid = static_cast<int>(items < num_sms() ? items : num_sms());
   const int gsz = attn::l2_group_size(B, H_kv, T, DH, window);
-  if (sched != nullptr && cudaMemsetAsync(sched, 0, sizeof(unsigned int), stream) != cudaSuccess)
+  if (sched != nullptr && !sched_zeroed &&
+      cudaMemsetAsync(sched, 0, sizeof(unsigned int), stream) != cudaSuccess)
     return cudaErrorUnknown;
   return launch_pdl(kern, dim3(grid), dim3(THREADS), SMEM, stream, tq, tk, tv,
                     static_cast<uint16_t*>(O), o_dtype == kF16 ? 1 : 0, pad_lens, B, T, H, H_kv,
@@ -553,18 +555,18 @@ cudaError_t launch_pair_cfg(const void* Q, const void* K, const void* V, long ld
 cudaError_t launch_flash_attention_pair(const void* Q, const void* K, const void* V, long ldkv,
                                         void* O, int o_dtype, const int32_t* pad_lens, int B,
                                         int T, int H, int H_kv, int window, void* sched,
-                                        cudaStream_t stream, int* status) {
+                                        cudaStream_t stream, int* status, bool sched_zeroed) {
   const int G = H / H_kv;
   unsigned int* sc = static_cast<unsigned int*>(sched);
   if (G == 1)
     return launch_pair_cfg<1>(Q, K, V, ldkv, O, o_dtype, pad_lens, B, T, H, H_kv, window, sc,
-                              stream, status);
+                              stream, status, sched_zeroed);
   if (G == 2)
     return launch_pair_cfg<2>(Q, K, V, ldkv, O, o_dtype, pad_lens, B, T, H, H_kv, window, sc,
-                              stream, status);
+                              stream, status, sched_zeroed);
   if (G == 4)
     return launch_pair_cfg<4>(Q, K, V, ldkv, O, o_dtype, pad_lens, B, T, H, H_kv, window, sc,
-                              stream, status);
+                              stream, status, sched_zeroed);
   return cudaErrorInvalidValue;
 }
 

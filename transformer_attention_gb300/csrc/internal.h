@@ -89,19 +89,21 @@ cudaError_t launch_qk_norm_rope(void* Q, long ldq, void* K, long ldk, const void
 // buffer with row stride ldkv (K' at column j*d_h, V at column v_off + j*d_h).
 // Writes O [B,T,H,d_h] in o_dtype (bf16|f16; may alias Q'); rows past the
 // valid length are 0.  sched: kAttnSchedBytes of device scratch for the
-// dynamic work order (zeroed here before the launch), or null for the
-// static order.
+// dynamic work order, or null for the static order; its counter is zeroed
+// here before the launch unless sched_zeroed says the caller already zeroed
+// it on the stream (a pipeline does so at its start, so that no memset
+// separates the kernels before and after the attention).
 constexpr size_t kAttnSchedBytes = 256;
 cudaError_t launch_flash_attention(const void* Q, const void* K, const void* V, long ldkv,
                                    void* O, int o_dtype, const int32_t* pad_lens, int B, int T,
                                    int H, int H_kv, int d_h, int window, void* sched,
-                                   cudaStream_t stream, int* status);
+                                   cudaStream_t stream, int* status, bool sched_zeroed = false);
 // The d_h = 128 kernel behind launch_flash_attention (two query tiles per
 // CTA); same arguments, G = H / H_kv in {1, 2, 4}.
 cudaError_t launch_flash_attention_pair(const void* Q, const void* K, const void* V, long ldkv,
                                         void* O, int o_dtype, const int32_t* pad_lens, int B,
                                         int T, int H, int H_kv, int window, void* sched,
-                                        cudaStream_t stream, int* status);
+                                        cudaStream_t stream, int* status, bool sched_zeroed);
 
 // u[m,:] = RMSNorm(x[m,:]) * (1 + gamma) over D, x in x_dtype (bf16|f32), u in
 // u_dtype (bf16|f16).
