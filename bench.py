@@ -657,9 +657,11 @@ def decode_work(w, sms: int) -> tuple:
     end = w.cache_len - w.T
     visible = end + w.T if w.window == 0 else min(w.window + w.T - 1, end + w.T)
     attn = w.B * visible * KVD * 2 * 2 + 2 * M * HD * 2 + w.B * (end + w.T) * 4
+    # the projections: Wq, Wkv, Wo read once, x and O read, outputs written,
+    # and the QK prologue that runs in the same stage as the Q / KV projection
     lin = (HD * D + 2 * KVD * D + D * HD) * 2 + M * D * 2 * 2 + M * (HD + 2 * KVD) * 2
+    lin += metrics.prologue_bytes(M, H, H_kv, d_h)
     work = {"attention": float(attn), "linear": float(lin),
-            "qk_norm_rope": float(metrics.prologue_bytes(M, H, H_kv, d_h)),
             "cache_write": float(M * KVD * 2 * 2 * 2 + M * 4)}
     # splits of the cache attention (the library's plan: two CTAs per SM over
     # B * H_kv * query groups, at least one 32-slot tile each)
@@ -669,7 +671,7 @@ def decode_work(w, sms: int) -> tuple:
     units = w.B * H_kv * ((w.T + rb // G - 1) // (rb // G))
     est = end + w.T if w.window == 0 else min(end + w.T, w.window + w.T)
     nsplit = max(1, min((2 * sms) // units, (est + 127) // 128, max(1, 2048 // units), 256))
-    launches = {"linear": 3, "qk_norm_rope": 1, "cache_write": 1,
+    launches = {"linear": 3, "cache_write": 1,
                 "attention": 1 + (1 if w.window > 0 else 0) + (1 if nsplit > 1 else 0)}
     return work, launches
 
@@ -707,13 +709,10 @@ def run_gpu_decode(args, world, rank, local):
 
     x2 = x.reshape(M, D)
     stages = [
-        ("proj_q", lambda: G3.gemma3_linear(x2, D, L.p["Wq"], D, qbuf, HD, M, HD, D,
-                                            G3.GEMMA3_BF16, G3.GEMMA3_F16)),
-        ("proj_kv", lambda: G3.gemma3_linear(x2, D, L.p["Wkv"], D, kvbuf, 2 * KVD, M, 2 * KVD, D,
-                                             G3.GEMMA3_BF16, G3.GEMMA3_F16)),
-        ("qk_norm_rope", lambda: G3.gemma3_qk_norm_rope(
-            qbuf, HD, kvbuf, 2 * KVD, L.p["gamma_q"], L.p["gamma_k"], seg, M, H, H_kv, d_h,
-            L.rope_base, L.rope_scale, w.query_scale)),
+        # Q and KV projections in one launch, then the QK prologue
+        ("proj_qkv", lambda: G3.gemma3_qkv_proj_norm_rope(
+            x2, D, L.p["Wq"], L.p["Wkv"], qbuf, kvbuf, M, D, H, H_kv, d_h, G3.GEMMA3_BF16,
+            L.p["gamma_q"], L.p["gamma_k"], seg, L.rope_base, L.rope_scale, w.query_scale)),
         ("cache_write", lambda: G3.gemma3_kv_cache_write(
             kvbuf, kvbuf[:, KVD:], 2 * KVD, seg, None, w.B, w.T, S, end, H_kv, d_h, Kc, Vc, pc)),
         ("attention", lambda: G3.gemma3_cached_attention(
@@ -771,7 +770,7 @@ def run_gpu_decode(args, world, rank, local):
     dev_seconds = sum(step_ms) / 1e3
     value, max_seconds = whole_job_value(tokens * args.steps, dev_seconds, world, dev)
     kern_ms = {k: sum(a.elapsed_time(b) for a, b in v) for k, v in events.items()}
-    proj = {k: kern_ms.pop(k) / args.steps for k in ("proj_q", "proj_kv", "proj_o")}
+    proj = {k: kern_ms.pop(k) / args.steps for k in ("proj_qkv", "proj_o")}
     kern_ms["linear"] = sum(proj.values()) * args.steps
 
     peaks, peak_src = load_peaks()
@@ -781,7 +780,7 @@ def run_gpu_decode(args, world, rank, local):
         # (together a few percent of the stage) counted as one launch
         n_l, kname = 1, "decode_attn (+ span, combine)"
     else:
-        n_l, kname = launches[dom], "skinny_gemm (3 projections, averaged)"
+        n_l, kname = 1, "projections (Q|KV in one skinny_gemm launch + QK prologue, O)"
     avg_s = kern_ms[dom] / 1e3 / (n_l * args.steps)
     achieved = work[dom] / n_l / avg_s / 1e9
     roof = {"bound": "hbm", "unit": "GB/s", "peak_kind": f"hbm copy ({peak_src})",

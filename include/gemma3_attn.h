@@ -351,7 +351,9 @@ int gemma3_geglu(const void* A, long lda, const void* W_gating, long ldw, void* 
  * stage of gemma3_attn_forward.  When H*d_h and H_kv*d_h are multiples of 256
  * and M > 16 this is one GEMM launch whose epilogue normalises and rotates
  * the head vectors from the fp32 accumulator (each tile of x feeds both
- * projections); otherwise the two projections and gemma3_qk_norm_rope.
+ * projections); for M <= 16 (a decode step) the two projections run in one
+ * CUDA-core launch followed by gemma3_qk_norm_rope; otherwise the two
+ * projections and gemma3_qk_norm_rope.
  * Wq [H*d_h, D], Wkv [2, H_kv*d_h, D] and x in in_dtype; gamma bf16 [d_h]. */
 int gemma3_qkv_proj_norm_rope(const void* x, long ldx, const void* Wq, const void* Wkv, void* Q,
                               void* KV, int M, int D, int H, int H_kv, int d_h, int in_dtype,

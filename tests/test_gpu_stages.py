@@ -149,7 +149,9 @@ def test_linear_qk_norm_rope_matches_oracle(M, D, d_h, H, H_kv, base, scale, alp
 @pytest.mark.parametrize("M,D,d_h,H,H_kv,base,scale,alpha", [
     (300, 1152, 256, 4, 1, 1e6, 1.0, 256 ** -0.5),     # one launch, Q 4 tiles + K|V 2 tiles
     (777, 640, 128, 32, 16, 1e6, 8.0, 168 ** -0.5),    # one launch, two heads per tile
-    (9, 256, 256, 8, 4, 1e4, 1.0, 256 ** -0.5),        # <= 16 rows: projections + prologue
+    (9, 256, 256, 8, 4, 1e4, 1.0, 256 ** -0.5),        # <= 16 rows: one two-projection
+    (2, 512, 128, 4, 2, 1e6, 8.0, 168 ** -0.5),        # launch on the CUDA cores + prologue
+    (16, 384, 128, 2, 2, 1e4, 1.0, 128 ** -0.5),
     (40, 256, 128, 2, 1, 1e4, 1.0, 128 ** -0.5),       # K|V width 256 is one tile, K 128
 ])
 def test_qkv_proj_norm_rope_matches_oracle(M, D, d_h, H, H_kv, base, scale, alpha):

@@ -98,9 +98,16 @@ cudaError_t project_qk(const void* x, long ldx, int act_dtype, const void* Wq, c
     return launch_qkv_qknorm(x, ldx, Wq, Wkv, D, qbuf, HD, kvbuf, 2 * KVD, M, HD, KVD, D, act_dtype,
                              gamma_q, gamma_k, pos, d_h, rope_base, rope_scale, query_scale, s,
                              st);
-  cudaError_t e = launch_linear(x, ldx, Wq, D, qbuf, HD, M, HD, D, act_dtype, kF16, s, st, 0);
-  if (e != cudaSuccess) return e;
-  e = launch_linear(x, ldx, Wkv, D, kvbuf, 2 * KVD, M, 2 * KVD, D, act_dtype, kF16, s, st, 0);
+  cudaError_t e;
+  if (M <= kSkinnyMaxRows) {
+    // A decode step: both projections in one CUDA-core launch.
+    e = launch_linear_skinny2(x, ldx, Wq, D, qbuf, HD, HD, Wkv, D, kvbuf, 2 * KVD, 2 * KVD, M, D,
+                              act_dtype, kF16, s);
+  } else {
+    e = launch_linear(x, ldx, Wq, D, qbuf, HD, M, HD, D, act_dtype, kF16, s, st, 0);
+    if (e != cudaSuccess) return e;
+    e = launch_linear(x, ldx, Wkv, D, kvbuf, 2 * KVD, M, 2 * KVD, D, act_dtype, kF16, s, st, 0);
+  }
   if (e != cudaSuccess) return e;
   return launch_qk_norm_rope(qbuf, HD, kvbuf, 2 * KVD, gamma_q, gamma_k, pos, M, H, H_kv, d_h,
                              rope_base, rope_scale, query_scale, s);

@@ -61,15 +61,25 @@ __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float v) {
   return __float2bfloat16_rn(v);
 }
 
+// Output columns n < n1 come from rows of W into C, columns n >= n1 from
+// rows n - n1 of W2 into columns n - n1 of C2 (two projections of the same
+// A in one launch; n1 = N for one).
 template <typename InT, typename OutT, int MB>
 __global__ void __launch_bounds__(kWarps * 32) skinny_gemm_kernel(
     const InT* __restrict__ A, long lda, const InT* __restrict__ W, long ldw,
-    OutT* __restrict__ C, long ldc, int M, int N, int K) {
+    OutT* __restrict__ C, long ldc, const InT* __restrict__ W2, long ldw2,
+    OutT* __restrict__ C2, long ldc2, int n1, int M, int N, int K) {
   pdl_enter();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n0 = (blockIdx.x * kWarps + warp) * kRows;
   if (n0 >= N) return;
   const int nr = min(kRows, N - n0);
+  const InT* wrow[kRows];
+#pragma unroll
+  for (int r = 0; r < kRows; ++r) {
+    const int n = n0 + r;
+    wrow[r] = n < n1 ? W + static_cast<size_t>(n) * ldw : W2 + static_cast<size_t>(n - n1) * ldw2;
+  }
   float acc[MB][kRows];
 #pragma unroll
   for (int m = 0; m < MB; ++m)
@@ -83,8 +93,7 @@ __global__ void __launch_bounds__(kWarps * 32) skinny_gemm_kernel(
       const int k = k0 + u * 256;
 #pragma unroll
       for (int r = 0; r < kRows; ++r)
-        w[u][r] = (k < K && r < nr) ? ld_stream(W + static_cast<size_t>(n0 + r) * ldw + k)
-                                    : make_uint4(0u, 0u, 0u, 0u);
+        w[u][r] = (k < K && r < nr) ? ld_stream(wrow[r] + k) : make_uint4(0u, 0u, 0u, 0u);
     }
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
@@ -116,7 +125,13 @@ __global__ void __launch_bounds__(kWarps * 32) skinny_gemm_kernel(
         float v = acc[m][r];
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-        if (lane == 0 && r < nr) C[static_cast<size_t>(m) * ldc + n0 + r] = from_f<OutT>(v);
+        if (lane == 0 && r < nr) {
+          const int n = n0 + r;
+          if (n < n1)
+            C[static_cast<size_t>(m) * ldc + n] = from_f<OutT>(v);
+          else
+            C2[static_cast<size_t>(m) * ldc2 + (n - n1)] = from_f<OutT>(v);
+        }
       }
     }
   }
@@ -124,21 +139,58 @@ __global__ void __launch_bounds__(kWarps * 32) skinny_gemm_kernel(
 
 template <typename InT, typename OutT>
 cudaError_t launch_skinny_typed(const void* A, long lda, const void* W, long ldw, void* C,
-                                long ldc, int M, int N, int K, cudaStream_t stream) {
+                                long ldc, const void* W2, long ldw2, void* C2, long ldc2, int n1,
+                                int M, int N, int K, cudaStream_t stream) {
   const int per_cta = kWarps * kRows;
   const dim3 grid((N + per_cta - 1) / per_cta);
   const InT* a = static_cast<const InT*>(A);
   const InT* w = static_cast<const InT*>(W);
+  const InT* w2 = static_cast<const InT*>(W2);
   OutT* c = static_cast<OutT*>(C);
+  OutT* c2 = static_cast<OutT*>(C2);
   const dim3 block(kWarps * 32);
   if (M <= 4)
     return launch_pdl(skinny_gemm_kernel<InT, OutT, 4>, grid, block, 0, stream, a, lda, w, ldw, c,
-                      ldc, M, N, K);
+                      ldc, w2, ldw2, c2, ldc2, n1, M, N, K);
   if (M <= 8)
     return launch_pdl(skinny_gemm_kernel<InT, OutT, 8>, grid, block, 0, stream, a, lda, w, ldw, c,
-                      ldc, M, N, K);
+                      ldc, w2, ldw2, c2, ldc2, n1, M, N, K);
   return launch_pdl(skinny_gemm_kernel<InT, OutT, 16>, grid, block, 0, stream, a, lda, w, ldw, c,
-                    ldc, M, N, K);
+                    ldc, w2, ldw2, c2, ldc2, n1, M, N, K);
+}
+
+template <typename IT>
+cudaError_t launch_skinny_out(const void* A, long lda, const void* W, long ldw, void* C, long ldc,
+                              const void* W2, long ldw2, void* C2, long ldc2, int n1, int M, int N,
+                              int K, int out_dtype, cudaStream_t stream) {
+  switch (out_dtype) {
+    case kF32:
+      return launch_skinny_typed<IT, float>(A, lda, W, ldw, C, ldc, W2, ldw2, C2, ldc2, n1, M, N,
+                                            K, stream);
+    case kF16:
+      return launch_skinny_typed<IT, __half>(A, lda, W, ldw, C, ldc, W2, ldw2, C2, ldc2, n1, M, N,
+                                             K, stream);
+    case kBF16:
+      return launch_skinny_typed<IT, __nv_bfloat16>(A, lda, W, ldw, C, ldc, W2, ldw2, C2, ldc2,
+                                                    n1, M, N, K, stream);
+    default:
+      return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t launch_skinny_any(const void* A, long lda, const void* W, long ldw, void* C,
+                              long ldc, const void* W2, long ldw2, void* C2, long ldc2, int n1,
+                              int M, int N, int K, int in_dtype, int out_dtype,
+                              cudaStream_t stream) {
+  if (M <= 0 || N <= 0 || K <= 0) return cudaSuccess;
+  if (M > kSkinnyMaxRows || K % 8 != 0) return cudaErrorInvalidValue;
+  if (in_dtype == kBF16)
+    return launch_skinny_out<__nv_bfloat16>(A, lda, W, ldw, C, ldc, W2, ldw2, C2, ldc2, n1, M, N,
+                                            K, out_dtype, stream);
+  if (in_dtype == kF16)
+    return launch_skinny_out<__half>(A, lda, W, ldw, C, ldc, W2, ldw2, C2, ldc2, n1, M, N, K,
+                                     out_dtype, stream);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace
@@ -146,24 +198,16 @@ cudaError_t launch_skinny_typed(const void* A, long lda, const void* W, long ldw
 cudaError_t launch_linear_skinny(const void* A, long lda, const void* W, long ldw, void* C,
                                  long ldc, int M, int N, int K, int in_dtype, int out_dtype,
                                  cudaStream_t stream) {
-  if (M <= 0 || N <= 0 || K <= 0) return cudaSuccess;
-  if (M > kSkinnyMaxRows || K % 8 != 0) return cudaErrorInvalidValue;
-#define G3_SKINNY_OUT(IT)                                                                      \
-  switch (out_dtype) {                                                                         \
-    case kF32: return launch_skinny_typed<IT, float>(A, lda, W, ldw, C, ldc, M, N, K, stream); \
-    case kF16: return launch_skinny_typed<IT, __half>(A, lda, W, ldw, C, ldc, M, N, K, stream); \
-    case kBF16:                                                                                \
-      return launch_skinny_typed<IT, __nv_bfloat16>(A, lda, W, ldw, C, ldc, M, N, K, stream);  \
-    default: return cudaErrorInvalidValue;                                                     \
-  }
-  if (in_dtype == kBF16) {
-    G3_SKINNY_OUT(__nv_bfloat16)
-  }
-  if (in_dtype == kF16) {
-    G3_SKINNY_OUT(__half)
-  }
-#undef G3_SKINNY_OUT
-  return cudaErrorInvalidValue;
+  return launch_skinny_any(A, lda, W, ldw, C, ldc, W, ldw, C, ldc, N, M, N, K, in_dtype,
+                           out_dtype, stream);
+}
+
+cudaError_t launch_linear_skinny2(const void* A, long lda, const void* W1, long ldw1, void* C1,
+                                  long ldc1, int N1, const void* W2, long ldw2, void* C2,
+                                  long ldc2, int N2, int M, int K, int in_dtype, int out_dtype,
+                                  cudaStream_t stream) {
+  return launch_skinny_any(A, lda, W1, ldw1, C1, ldc1, W2, ldw2, C2, ldc2, N1, M, N1 + N2, K,
+                           in_dtype, out_dtype, stream);
 }
 
 }  // namespace g3
