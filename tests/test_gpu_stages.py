@@ -262,3 +262,43 @@ def test_flash_attention_local_window_ge_T_equals_global():
         outs.append(Od.cpu())
     assert G3.gemma3_attn_check_status() == 0
     assert torch.equal(outs[0], outs[1]) and torch.equal(outs[0], outs[2])
+
+
+# ---------------------------------------------------------------- block norms
+# Widths of every row-kernel variant: the register-resident ones (D <= 1024,
+# 2048, 4096, 6144) and the two-pass one above; row counts not a multiple of
+# the 4 or 8 rows per CTA.
+NORM_CASES = [(37, 256), (13, 1152), (9, 3840), (7, 5376), (5, 8192)]
+
+
+@pytest.mark.parametrize("M,D", NORM_CASES)
+@pytest.mark.parametrize("x_t,u_t", [("f32", "f16"), ("bf16", "bf16")])
+def test_rmsnorm_rows_matches_oracle(M, D, x_t, u_t):
+    import transformer_attention_gb300 as G3
+    xd = {"f32": torch.float32, "bf16": torch.bfloat16}[x_t]
+    ud = {"f16": torch.float16, "bf16": torch.bfloat16}[u_t]
+    x = _randn((M, D), 50, 3.0, xd)
+    gamma = _randn((D,), 51, 0.1 ** 0.5)
+    u = torch.empty((M, D), dtype=ud, device="cuda")
+    G3.gemma3_rmsnorm(x.cuda(), G3.GEMMA3_F32 if x_t == "f32" else G3.GEMMA3_BF16, gamma.cuda(),
+                      u, G3.GEMMA3_F16 if u_t == "f16" else G3.GEMMA3_BF16, M, D)
+    assert G3.gemma3_attn_check_status() == 0
+    ref = O.rms_norm(x, gamma)
+    tol = {"f16": 1e-3, "bf16": 4e-3}[u_t]
+    assert rel_frob(u.cpu(), ref) <= tol
+
+
+@pytest.mark.parametrize("M,D", NORM_CASES)
+@pytest.mark.parametrize("x_t", ["f32", "bf16"])
+def test_postnorm_residual_matches_oracle(M, D, x_t):
+    import transformer_attention_gb300 as G3
+    xd = {"f32": torch.float32, "bf16": torch.bfloat16}[x_t]
+    a = _randn((M, D), 52, 2.0, torch.float32)
+    x = _randn((M, D), 53, 1.0, xd)
+    gamma = _randn((D,), 54, 0.1 ** 0.5)
+    y = torch.empty((M, D), dtype=torch.float32, device="cuda")
+    G3.gemma3_postnorm_residual(a.cuda(), x.cuda(), G3.GEMMA3_F32 if x_t == "f32" else
+                                G3.GEMMA3_BF16, gamma.cuda(), y, M, D)
+    assert G3.gemma3_attn_check_status() == 0
+    ref = x.to(F64) + O.rms_norm(a, gamma)
+    assert rel_frob(y.cpu(), ref) <= 1e-6

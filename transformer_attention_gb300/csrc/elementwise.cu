@@ -186,6 +186,52 @@ __global__ void __launch_bounds__(256)
   }
 }
 
+// The same with the row held in registers (NV 4-element vectors per lane,
+// D <= 128 * NV): every load of the row is issued before the sum, and x is
+// read once.
+template <typename T, bool OUT_F16, int NV>
+__global__ void __launch_bounds__(128)
+    rmsnorm_rows_reg_kernel(const T* __restrict__ x, const __nv_bfloat16* __restrict__ gamma,
+                            uint16_t* __restrict__ u, int M, int D) {
+  pdl_enter();
+  const int lane = threadIdx.x & 31;
+  const int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (row >= M) return;
+  const T* xr = x + static_cast<long>(row) * D;
+  float4 v[NV];
+#pragma unroll
+  for (int i = 0; i < NV; ++i) {
+    const int c = lane * 4 + i * 128;
+    v[i] = c < D ? load4<T>(xr + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  float ss = 0.f;
+#pragma unroll
+  for (int i = 0; i < NV; ++i)
+    ss += v[i].x * v[i].x + v[i].y * v[i].y + v[i].z * v[i].z + v[i].w * v[i].w;
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+  const float rs = rsqrtf(ss / D + kEps);
+  uint16_t* ur = u + static_cast<long>(row) * D;
+#pragma unroll
+  for (int i = 0; i < NV; ++i) {
+    const int c = lane * 4 + i * 128;
+    if (c < D) {
+      const float4 g = load4<__nv_bfloat16>(gamma + c);
+      const float a0 = v[i].x * rs * (1.f + g.x), a1 = v[i].y * rs * (1.f + g.y);
+      const float a2 = v[i].z * rs * (1.f + g.z), a3 = v[i].w * rs * (1.f + g.w);
+      uint2 w;
+      if (OUT_F16) {
+        w.x = pack_half2(a0, a1);
+        w.y = pack_half2(a2, a3);
+      } else {
+        w.x = pack_bf162(a0, a1);
+        w.y = pack_bf162(a2, a3);
+      }
+      *reinterpret_cast<uint2*>(ur + c) = w;
+    }
+  }
+}
+
 // bf16 -> fp16, 8 elements per thread per step (n % 8 == 0, 16-byte aligned).
 __global__ void __launch_bounds__(256)
     cast_bf16_f16_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst, size_t n8) {
@@ -237,6 +283,92 @@ __global__ void __launch_bounds__(256)
   }
 }
 
+// The same with a's row held in registers (D <= 128 * NV): a is read once.
+template <typename T, int NV>
+__global__ void __launch_bounds__(128)
+    postnorm_residual_reg_kernel(const float* __restrict__ a, const T* x,
+                                 const __nv_bfloat16* __restrict__ gamma, float* y, int M, int D) {
+  pdl_enter();
+  const int lane = threadIdx.x & 31;
+  const int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (row >= M) return;
+  const float* ar = a + static_cast<long>(row) * D;
+  float4 v[NV];
+#pragma unroll
+  for (int i = 0; i < NV; ++i) {
+    const int c = lane * 4 + i * 128;
+    v[i] = c < D ? *reinterpret_cast<const float4*>(ar + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  float ss = 0.f;
+#pragma unroll
+  for (int i = 0; i < NV; ++i)
+    ss += v[i].x * v[i].x + v[i].y * v[i].y + v[i].z * v[i].z + v[i].w * v[i].w;
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+  const float rs = rsqrtf(ss / D + kEps);
+  const T* xr = x + static_cast<long>(row) * D;
+  float* yr = y + static_cast<long>(row) * D;
+  // y may alias x, so x is loaded eight vectors at a time before their stores
+  // (a batch of loads in flight instead of one load per store).
+#pragma unroll
+  for (int i0 = 0; i0 < NV; i0 += 8) {
+    float4 xv[8], g[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int c = lane * 4 + (i0 + j) * 128;
+      if (c < D) {
+        xv[j] = load4<T>(xr + c);
+        g[j] = load4<__nv_bfloat16>(gamma + c);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int c = lane * 4 + (i0 + j) * 128;
+      if (c < D) {
+        const float4& a4 = v[i0 + j];
+        float4 o;
+        o.x = xv[j].x + a4.x * rs * (1.f + g[j].x);
+        o.y = xv[j].y + a4.y * rs * (1.f + g[j].y);
+        o.z = xv[j].z + a4.z * rs * (1.f + g[j].z);
+        o.w = xv[j].w + a4.w * rs * (1.f + g[j].w);
+        *reinterpret_cast<float4*>(yr + c) = o;
+      }
+    }
+  }
+}
+
+// Row widths 2049..4096 (and up to 6144 for the pre-norm) are read once,
+// from registers, one warp per row and 4 rows per CTA (their 150-250
+// registers per thread would otherwise leave one CTA per SM).  Narrower
+// rows use the two-pass kernels (8 rows per CTA): their second pass finds
+// the row still in cache, and their low register use keeps more rows in
+// flight.  At 48 vectors per lane the post-norm's row and batch of x would
+// not fit in registers, so those widths use its two-pass kernel too.
+inline dim3 row_grid(int M, int rows) { return dim3((M + rows - 1) / rows); }
+
+template <typename T, bool OUT_F16>
+cudaError_t launch_rms_typed(cudaStream_t s, const T* x, const __nv_bfloat16* g, uint16_t* u,
+                             int M, int D) {
+  if (D > 2048 && D <= 4096)
+    return launch_pdl(rmsnorm_rows_reg_kernel<T, OUT_F16, 32>, row_grid(M, 4), dim3(128), 0, s,
+                      x, g, u, M, D);
+  if (D > 4096 && D <= 6144)
+    return launch_pdl(rmsnorm_rows_reg_kernel<T, OUT_F16, 48>, row_grid(M, 4), dim3(128), 0, s,
+                      x, g, u, M, D);
+  return launch_pdl(rmsnorm_rows_kernel<T, OUT_F16>, row_grid(M, 8), dim3(256), 0, s, x, g, u, M,
+                    D);
+}
+
+template <typename T>
+cudaError_t launch_post_typed(cudaStream_t s, const float* a, const T* x, const __nv_bfloat16* g,
+                              float* y, int M, int D) {
+  if (D > 2048 && D <= 4096)
+    return launch_pdl(postnorm_residual_reg_kernel<T, 32>, row_grid(M, 4), dim3(128), 0, s, a, x,
+                      g, y, M, D);
+  return launch_pdl(postnorm_residual_kernel<T>, row_grid(M, 8), dim3(256), 0, s, a, x, g, y, M,
+                    D);
+}
+
 }  // namespace
 
 cudaError_t launch_qk_norm_rope(void* Q, long ldq, void* K, long ldk, const void* gamma_q,
@@ -265,24 +397,19 @@ cudaError_t launch_qk_norm_rope(void* Q, long ldq, void* K, long ldk, const void
 cudaError_t launch_rmsnorm_rows(const void* x, int x_dtype, const void* gamma, void* u,
                                 int u_dtype, int M, int D, cudaStream_t stream) {
   if (M <= 0) return cudaSuccess;
-  const int blocks = (M + 7) / 8;
   auto g = static_cast<const __nv_bfloat16*>(gamma);
   auto uo = static_cast<uint16_t*>(u);
   if (u_dtype != kBF16 && u_dtype != kF16) return cudaErrorInvalidValue;
   const bool f16 = u_dtype == kF16;
-  const dim3 grid(blocks), block(256);
   if (x_dtype == kF32) {
     auto xp = static_cast<const float*>(x);
-    return f16 ? launch_pdl(rmsnorm_rows_kernel<float, true>, grid, block, 0, stream, xp, g, uo, M, D)
-               : launch_pdl(rmsnorm_rows_kernel<float, false>, grid, block, 0, stream, xp, g, uo,
-                            M, D);
+    return f16 ? launch_rms_typed<float, true>(stream, xp, g, uo, M, D)
+               : launch_rms_typed<float, false>(stream, xp, g, uo, M, D);
   }
   if (x_dtype == kBF16) {
     auto xp = static_cast<const __nv_bfloat16*>(x);
-    return f16 ? launch_pdl(rmsnorm_rows_kernel<__nv_bfloat16, true>, grid, block, 0, stream, xp,
-                            g, uo, M, D)
-               : launch_pdl(rmsnorm_rows_kernel<__nv_bfloat16, false>, grid, block, 0, stream, xp,
-                            g, uo, M, D);
+    return f16 ? launch_rms_typed<__nv_bfloat16, true>(stream, xp, g, uo, M, D)
+               : launch_rms_typed<__nv_bfloat16, false>(stream, xp, g, uo, M, D);
   }
   return cudaErrorInvalidValue;
 }
@@ -347,14 +474,12 @@ cudaError_t launch_postnorm_residual(const float* a, const void* x, int x_dtype,
                                      const void* gamma, float* y, int M, int D,
                                      cudaStream_t stream) {
   if (M <= 0) return cudaSuccess;
-  const int blocks = (M + 7) / 8;
   auto g = static_cast<const __nv_bfloat16*>(gamma);
   if (x_dtype == kF32)
-    return launch_pdl(postnorm_residual_kernel<float>, dim3(blocks), dim3(256), 0, stream, a,
-                      static_cast<const float*>(x), g, y, M, D);
+    return launch_post_typed<float>(stream, a, static_cast<const float*>(x), g, y, M, D);
   if (x_dtype == kBF16)
-    return launch_pdl(postnorm_residual_kernel<__nv_bfloat16>, dim3(blocks), dim3(256), 0, stream,
-                      a, static_cast<const __nv_bfloat16*>(x), g, y, M, D);
+    return launch_post_typed<__nv_bfloat16>(stream, a, static_cast<const __nv_bfloat16*>(x), g, y,
+                                            M, D);
   return cudaErrorInvalidValue;
 }
 
