@@ -32,7 +32,9 @@ def _randn(shape, seed, std=1.0, dtype=torch.bfloat16):
     return (torch.randn(shape, generator=g) * std).to(dtype)
 
 
-@pytest.mark.parametrize("M,D,D_ff", [(256, 512, 2048), (300, 640, 1000), (1024, 2560, 10240)])
+@pytest.mark.parametrize("M,D,D_ff", [(256, 512, 2048), (300, 640, 1000), (1024, 2560, 10240),
+                                      # a wave of tiles, odd m-tile count, ragged D_ff
+                                      (1100, 640, 2600)])
 def test_geglu_gemm_matches_oracle(M, D, D_ff):
     import transformer_attention_gb300 as G3
     u = _randn((M, D), 1, 1.0, torch.float16)

@@ -37,7 +37,12 @@ def _randn(shape, seed, std=1.0, dtype=torch.bfloat16):
                                    (1, 2048, 2560), (2, 5376, 4096), (3, 88, 72), (5, 1000, 1160),
                                    (8, 512, 1152), (16, 4096, 5376), (17, 296, 264),
                                    # M <= 16 (CUDA-core path): many rows, and a wide K
-                                   (2, 20000, 1024), (4, 64, 16384)])
+                                   (2, 20000, 1024), (4, 64, 16384),
+                                   # a wave or more of tiles, 8+ wide (CTA pairs sharing each
+                                   # weight tile): odd m-tile count, ragged M / N / K
+                                   (5170, 2200, 1024), (2000, 3000, 200),
+                                   # a wave of tiles 5 wide (one CTA per tile)
+                                   (5170, 1152, 1024)])
 @pytest.mark.parametrize("out", ["bf16", "f16", "f32"])
 @pytest.mark.parametrize("inp", ["bf16", "f16"])
 def test_linear_matches_fp64(M, N, K, out, inp):
@@ -70,6 +75,40 @@ def test_linear_small_grid_many_tiles():
     C = G3.linear(A.cuda(), W.cuda(), out_dtype=torch.float32, max_ctas=3)
     assert G3.gemma3_attn_check_status() == 0
     assert rel_frob(C.cpu(), O.project(A, W)) <= 1e-5
+
+
+def _pairs_in_use():
+    import transformer_attention_gb300 as G3
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    return 20 * G3.gemma3_gemm_pair_clusters() >= 9 * sms
+
+
+def test_linear_pairs_small_grid_many_units():
+    # two CTA pairs walking 80 units (160 tiles): the shared stage ring and
+    # both CTAs' accumulator rings turn over many times
+    import transformer_attention_gb300 as G3
+    if not _pairs_in_use():
+        pytest.skip("the device holds GEMM CTA pairs on fewer than 90% of its SMs")
+    A = _randn((2048, 640), 6)
+    W = _randn((2560, 640), 7, 640 ** -0.5)
+    C = G3.linear(A.cuda(), W.cuda(), out_dtype=torch.float32, max_ctas=4)
+    assert G3.gemma3_attn_check_status() == 0
+    assert rel_frob(C.cpu(), O.project(A, W)) <= 1e-5
+
+
+def test_linear_pairs_match_single_ctas_bitwise():
+    # the same tile sums in the same order either way: a launch with pairs
+    # (160 tiles) and the same rows computed in a launch too small for pairs
+    # (the first 128 rows: 10 tiles) agree bit for bit on those rows
+    import transformer_attention_gb300 as G3
+    if not _pairs_in_use():
+        pytest.skip("the device holds GEMM CTA pairs on fewer than 90% of its SMs")
+    A = _randn((2048, 640), 8).cuda()
+    W = _randn((2560, 640), 9, 640 ** -0.5).cuda()
+    C_pairs = G3.linear(A, W, out_dtype=torch.float32)
+    C_one = G3.linear(A[:128].contiguous(), W, out_dtype=torch.float32)
+    assert G3.gemma3_attn_check_status() == 0
+    assert torch.equal(C_pairs[:128].cpu(), C_one.cpu())
 
 
 # ---------------------------------------------------------------- QK-norm + RoPE prologue

@@ -876,6 +876,11 @@ int gemma3_attn_check_status(void* stream) {
 
 int gemma3_last_device_status(void) { return t_last_device_status; }
 
+int gemma3_gemm_pair_clusters(void) {
+  if (check_device() != GEMMA3_OK) return 0;
+  return g3::gemm_pair_clusters();
+}
+
 const char* gemma3_strerror(int status) {
   switch (status) {
     case GEMMA3_OK: return "ok";

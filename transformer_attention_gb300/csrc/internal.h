@@ -18,6 +18,9 @@ bool encode_tiled(CUtensorMap* map, CUtensorMapDataType dt, int rank, const void
 
 int num_sms();
 
+// Clusters of two projection-GEMM CTAs the current device holds at once.
+int gemm_pair_clusters();
+
 // Launch `kern` on `stream` with programmatic dependent launch allowed: the
 // grid may start while the previous kernel on the stream is finishing, and
 // its pdl_enter() (ptx.cuh) waits for that kernel before any global-memory
@@ -35,6 +38,28 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
+}
+
+// The same launch in thread-block clusters of cluster_x CTAs along x
+// (grid.x a multiple of cluster_x).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl_cluster(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                               int cluster_x, cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = static_cast<unsigned>(cluster_x);
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
 }
 
