@@ -322,7 +322,22 @@ __global__ void __launch_bounds__(THREADS, 1)
           const float p = row < M ? static_cast<float>(__ldg(epi.pos + row)) : 0.f;
           const __nv_bfloat16* gam = seg1 ? epi.gamma2 : epi.gamma;
           const float sc_seg = seg1 ? epi.scale2 : epi.scale;
-          float rs[HEADS];
+          // d_h = 256 (one head per tile, the short-K 1B shapes where this
+          // epilogue is as long as the main loop): the segment's gamma spread
+          // over the warp, word k of lane l holding the bf16 pair (gamma_j,
+          // gamma_{j + d_h/2}) of j = 32 k + l, fetched with one shuffle per
+          // rotated pair (shuffles and loads share the shared-memory data
+          // path that feeds the tensor core).  d_h = 128 reads gamma from
+          // global memory per use (the shuffles' registers would spill there).
+          constexpr bool G_SHFL = DH == 256;
+          uint32_t gl[G_SHFL ? HALF / 32 : 1];
+#pragma unroll
+          for (int k = 0; G_SHFL && k < HALF / 32; ++k) {
+            const uint16_t* gb = reinterpret_cast<const uint16_t*>(gam);
+            gl[k] = static_cast<uint32_t>(__ldg(gb + k * 32 + lane)) |
+                    (static_cast<uint32_t>(__ldg(gb + HALF + k * 32 + lane)) << 16);
+          }
+          float rs[HEADS];   // 1 / rms of each head, times the segment's scale
 #pragma unroll
           for (int e = 0; e < HEADS; ++e) {
             float ss = 0.f;
@@ -339,60 +354,82 @@ __global__ void __launch_bounds__(THREADS, 1)
                 ss = fmaf(__uint_as_float(a1[t]), __uint_as_float(a1[t]), ss);
               }
             }
-            rs[e] = rsqrtf(ss * (1.f / DH) + 1e-6f);
+            rs[e] = rsqrtf(ss * (1.f / DH) + 1e-6f) * sc_seg;
           }
           // Each pair of 64-column chunks (first half, partner half) goes to
           // the two staging buffers: the first-half chunk to buffer 0, the
           // partner chunk to buffer 1 (nchunk is even here).
           uint8_t* buf_a = staging;
           uint8_t* buf_b = staging + STAGING_BYTES;
+          // Blocks of 32 rotated pairs (head e, chunk pair i, 32-column half
+          // h): a runtime loop over the blocks, each block unrolled.  Fully
+          // unrolled, this epilogue is tens of KB of instructions, and
+          // streaming through them every tile evicts the MMA issuer's and the
+          // TMA producer's loops from the instruction caches they share.
+          constexpr int N_BLK = HEADS * PAIRS * 2;
+#pragma unroll 1
+          for (int blk = 0; blk < N_BLK; ++blk) {
+            const int e = blk / (2 * PAIRS), i = (blk >> 1) % PAIRS, h = blk & 1;
+            const int ca = e * (DH / 64) + i, cb = ca + PAIRS;   // first-half, partner chunk
+            const int jb = i * 64 + h * 32;                     // first pair index of the block
+            float rse = rs[0];
 #pragma unroll
-          for (int e = 0; e < HEADS; ++e) {
+            for (int k = 1; k < HEADS; ++k)
+              if (e == k) rse = rs[k];
+            uint32_t gw = 0;   // this block's gamma word of each lane
+            if constexpr (G_SHFL) {
 #pragma unroll
-            for (int i = 0; i < PAIRS; ++i) {
-              const int ca = e * (DH / 64) + i, cb = ca + PAIRS;   // first-half, partner chunk
+              for (int k = 0; k < HALF / 32; ++k)
+                if ((jb >> 5) == k) gw = gl[k];
+            }
+            const float2* fr = epi.freqs.f + jb;
+            uint32_t x1[32], x2[32];
+            tmem_ld32(acc + ca * 64 + h * 32, x1);
+            tmem_ld32(acc + cb * 64 + h * 32, x2);
+            tmem_ld_wait(x1);
+            tmem_ld_wait(x2);
+            if (blk == N_BLK - 1) release_acc();
+            uint32_t wa[16], wb[16];
 #pragma unroll
-              for (int h = 0; h < 2; ++h) {
-                uint32_t x1[32], x2[32];
-                tmem_ld32(acc + ca * 64 + h * 32, x1);
-                tmem_ld32(acc + cb * 64 + h * 32, x2);
-                tmem_ld_wait(x1);
-                tmem_ld_wait(x2);
-                if (e == HEADS - 1 && i == PAIRS - 1 && h == 1) release_acc();
-                uint32_t wa[16], wb[16];
+            for (int t = 0; t < 32; t += 2) {
+              float o1[2], o2[2];
 #pragma unroll
-                for (int t = 0; t < 32; t += 2) {
-                  float o1[2], o2[2];
-#pragma unroll
-                  for (int v = 0; v < 2; ++v) {
-                    const int j = i * 64 + h * 32 + t + v;   // pair index within the head
-                    float sn, cs;
-                    rope_sincos(p, epi.freqs.f[j], sn, cs);
-                    const float g1 = 1.f + __bfloat162float(gam[j]);
-                    const float g2 = 1.f + __bfloat162float(gam[j + HALF]);
-                    const float y1 = __uint_as_float(x1[t + v]) * rs[e] * g1;
-                    const float y2 = __uint_as_float(x2[t + v]) * rs[e] * g2;
-                    o1[v] = (y1 * cs - y2 * sn) * sc_seg;
-                    o2[v] = (y2 * cs + y1 * sn) * sc_seg;
-                  }
-                  wa[t / 2] = pack_half2(o1[0], o1[1]);
-                  wb[t / 2] = pack_half2(o2[0], o2[1]);
+              for (int v = 0; v < 2; ++v) {
+                float sn, cs;
+                rope_sincos(p, fr[t + v], sn, cs);
+                float gm1, gm2;   // gamma_j, gamma_{j + d_h/2} of pair j = jb + t + v
+                if constexpr (G_SHFL) {
+                  const uint32_t gp = __shfl_sync(0xffffffffu, gw, t + v);
+                  gm1 = __uint_as_float(gp << 16);
+                  gm2 = __uint_as_float(gp & 0xffff0000u);
+                } else {
+                  gm1 = __bfloat162float(gam[jb + t + v]);
+                  gm2 = __bfloat162float(gam[jb + t + v + HALF]);
                 }
-                if (h == 0) {
-                  // both buffers must have been read by the earlier stores
-                  if (lane == 0 && nchunk > 0) bulk_wait_group_read<0>();
-                  __syncwarp();
-                }
-                // row `lane`, 16-byte unit u at unit u ^ (lane % 8) (128-byte swizzle)
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                  const int pu = ((4 * h + u) ^ (lane & 7)) << 4;
-                  *reinterpret_cast<uint4*>(buf_a + lane * 128 + pu) =
-                      make_uint4(wa[4 * u], wa[4 * u + 1], wa[4 * u + 2], wa[4 * u + 3]);
-                  *reinterpret_cast<uint4*>(buf_b + lane * 128 + pu) =
-                      make_uint4(wb[4 * u], wb[4 * u + 1], wb[4 * u + 2], wb[4 * u + 3]);
-                }
+                // x (1 + gamma) as one fused multiply-add
+                const float y1 = fmaf(__uint_as_float(x1[t + v]), gm1, __uint_as_float(x1[t + v]));
+                const float y2 = fmaf(__uint_as_float(x2[t + v]), gm2, __uint_as_float(x2[t + v]));
+                o1[v] = (y1 * cs - y2 * sn) * rse;
+                o2[v] = (y2 * cs + y1 * sn) * rse;
               }
+              wa[t / 2] = pack_half2(o1[0], o1[1]);
+              wb[t / 2] = pack_half2(o2[0], o2[1]);
+            }
+            if (h == 0) {
+              // both buffers must have been read by the earlier stores
+              if (lane == 0 && nchunk > 0) bulk_wait_group_read<0>();
+              __syncwarp();
+            }
+            // row `lane`, 16-byte unit u at unit u ^ (lane % 8) (128-byte swizzle)
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const int pu = ((4 * h + u) ^ (lane & 7)) << 4;
+              *reinterpret_cast<uint4*>(buf_a + lane * 128 + pu) =
+                  make_uint4(wa[4 * u], wa[4 * u + 1], wa[4 * u + 2], wa[4 * u + 3]);
+              *reinterpret_cast<uint4*>(buf_b + lane * 128 + pu) =
+                  make_uint4(wb[4 * u], wb[4 * u + 1], wb[4 * u + 2], wb[4 * u + 3]);
+            }
+            if (h == 1) {
               fence_proxy_async_smem();
               __syncwarp();
               if (lane == 0) {
