@@ -36,8 +36,9 @@ def _randn(shape, seed, std=1.0, dtype=torch.bfloat16):
                                    (130, 200, 72), (128, 256, 64), (4096, 1536, 1024),
                                    (1, 2048, 2560), (2, 5376, 4096), (3, 88, 72), (5, 1000, 1160),
                                    (8, 512, 1152), (16, 4096, 5376), (17, 296, 264),
-                                   # M <= 16 (CUDA-core path): many rows, and a wide K
-                                   (2, 20000, 1024), (4, 64, 16384),
+                                   # M <= 16 (CUDA-core path): many rows (the weight ring
+                                   # wraps), a wide K, and rows too long for the ring
+                                   (2, 20000, 1024), (4, 64, 16384), (2, 64, 40000),
                                    # a wave or more of tiles, 8+ wide (CTA pairs sharing each
                                    # weight tile): odd m-tile count, ragged M / N / K
                                    (5170, 2200, 1024), (2000, 3000, 200),

@@ -102,7 +102,7 @@ cudaError_t project_qk(const void* x, long ldx, int act_dtype, const void* Wq, c
   if (M <= kSkinnyMaxRows) {
     // A decode step: both projections in one CUDA-core launch.
     e = launch_linear_skinny2(x, ldx, Wq, D, qbuf, HD, HD, Wkv, D, kvbuf, 2 * KVD, 2 * KVD, M, D,
-                              act_dtype, kF16, s);
+                              act_dtype, kF16, s, st);
   } else {
     e = launch_linear(x, ldx, Wq, D, qbuf, HD, M, HD, D, act_dtype, kF16, s, st, 0);
     if (e != cudaSuccess) return e;

@@ -624,7 +624,8 @@ cudaError_t launch_linear(const void* A, long lda, const void* W, long ldw, void
   if (M <= 0 || N <= 0 || K <= 0) return cudaSuccess;
   if (in_dtype != kBF16 && in_dtype != kF16) return cudaErrorInvalidValue;
   if (M <= kSkinnyMaxRows)
-    return launch_linear_skinny(A, lda, W, ldw, C, ldc, M, N, K, in_dtype, out_dtype, stream);
+    return launch_linear_skinny(A, lda, W, ldw, C, ldc, M, N, K, in_dtype, out_dtype, stream,
+                                status);
   const bool pairs = gemm_use_pairs(M, N);
   CUtensorMap ta, tb;
   if (!encode_ab(ta, tb, A, lda, W, ldw, M, N, K, in_dtype, pairs ? BN / 2 : BN))

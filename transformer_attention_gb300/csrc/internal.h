@@ -71,17 +71,18 @@ cudaError_t launch_linear(const void* A, long lda, const void* W, long ldw, void
                           int* status, int max_ctas);
 
 // The same product for M <= kSkinnyMaxRows on the CUDA cores (bound by
-// reading W from HBM); K % 8 == 0, 16-byte aligned rows.
+// reading W from HBM); K % 8 == 0, 16-byte aligned rows.  Its bounded waits
+// record into `status`.
 constexpr int kSkinnyMaxRows = 16;
 cudaError_t launch_linear_skinny(const void* A, long lda, const void* W, long ldw, void* C,
                                  long ldc, int M, int N, int K, int in_dtype, int out_dtype,
-                                 cudaStream_t stream);
+                                 cudaStream_t stream, int* status);
 // Two such products of the same A in one launch: C1 = A W1^T (N1 columns)
 // and C2 = A W2^T (N2 columns).
 cudaError_t launch_linear_skinny2(const void* A, long lda, const void* W1, long ldw1, void* C1,
                                   long ldc1, int N1, const void* W2, long ldw2, void* C2,
                                   long ldc2, int N2, int M, int K, int in_dtype, int out_dtype,
-                                  cudaStream_t stream);
+                                  cudaStream_t stream, int* status);
 
 // Z[M, D_ff] (fp16) = GELU_tanh(A Wg^T) * (A Wu^T), Wgu = [Wg; Wu] of shape
 // [2*D_ff, K] (the transposed gating weight (2, D_ff, D) viewed as rows).

@@ -25,7 +25,10 @@ enum : int {
 // so that it may start while the kernel before it on the stream finishes
 // (launch_pdl, internal.h); its first statement waits until that kernel
 // has completed and its writes are visible, then lets the next kernel
-// launch.  Nothing touches global memory before this point.
+// launch.  Nothing touches global memory before this point, except the
+// few-row projection's first weight copies (skinny_gemm.cu): weights are
+// written by no kernel of the library, and only the library's kernels let
+// the next kernel start early.
 __device__ __forceinline__ void pdl_enter() {
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -146,6 +149,24 @@ __device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const void* tmap, u
       ".multicast::cluster [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar), "r"(c0), "r"(c1), "h"(cta_mask)
       : "memory");
+}
+
+// `bytes` (a multiple of 16) from global `src` to shared `dst` (both 16-byte
+// aligned), completing on the mbarrier at `bar`.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
+                                          uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          dst),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+// The two halves of pdl_enter(), for a kernel that starts reading inputs no
+// earlier kernel writes before it waits for those kernels.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* tmap, uint32_t bar,
