@@ -780,7 +780,7 @@ def run_gpu_decode(args, world, rank, local):
         # (together a few percent of the stage) counted as one launch
         n_l, kname = 1, "decode_attn (+ span, combine)"
     else:
-        n_l, kname = 1, "projections (Q|KV in one skinny_gemm launch + QK prologue, O)"
+        n_l, kname = 1, "projections (Q|KV in one skinny_tc launch + QK prologue, O)"
     avg_s = kern_ms[dom] / 1e3 / (n_l * args.steps)
     achieved = work[dom] / n_l / avg_s / 1e9
     roof = {"bound": "hbm", "unit": "GB/s", "peak_kind": f"hbm copy ({peak_src})",

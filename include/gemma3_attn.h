@@ -332,8 +332,11 @@ int gemma3_cached_attention(const void* Q, const void* K_cache, const void* V_ca
  * row stride ldc.  fp32 accumulation on the tcgen05 tensor cores.  K % 8 == 0;
  * strides in bytes must be multiples of 16.  max_ctas > 0 caps the
  * persistent grid.  For M <= 16 (a decode step's projections) the product is
- * bound by reading W, and a CUDA-core kernel that streams W once with fp32
- * sums runs instead (max_ctas is ignored there). */
+ * bound by reading W, and a kernel that streams W once by TMA runs instead:
+ * W fills the 128-row side of the tcgen05 MMA, the rows of A its 16-wide
+ * side, and the K range of each 128-row tile of W is split over a cluster of
+ * up to 8 CTAs whose fp32 partials are summed through distributed shared
+ * memory (max_ctas is ignored there). */
 int gemma3_linear(const void* A, long lda, const void* W, long ldw, void* C, long ldc, int M,
                   int N, int K, int in_dtype, int out_dtype, int max_ctas, void* stream);
 
@@ -352,8 +355,9 @@ int gemma3_geglu(const void* A, long lda, const void* W_gating, long ldw, void* 
  * and M > 16 this is one GEMM launch whose epilogue normalises and rotates
  * the head vectors from the fp32 accumulator (each tile of x feeds both
  * projections); for M <= 16 (a decode step) the two projections run in one
- * CUDA-core launch followed by gemma3_qk_norm_rope; otherwise the two
- * projections and gemma3_qk_norm_rope.
+ * launch of the few-row kernel of gemma3_linear (H*d_h a multiple of 128)
+ * followed by gemma3_qk_norm_rope; otherwise the two projections and
+ * gemma3_qk_norm_rope.
  * Wq [H*d_h, D], Wkv [2, H_kv*d_h, D] and x in in_dtype; gamma bf16 [d_h]. */
 int gemma3_qkv_proj_norm_rope(const void* x, long ldx, const void* Wq, const void* Wkv, void* Q,
                               void* KV, int M, int D, int H, int H_kv, int d_h, int in_dtype,

@@ -36,8 +36,8 @@ def _randn(shape, seed, std=1.0, dtype=torch.bfloat16):
                                    (130, 200, 72), (128, 256, 64), (4096, 1536, 1024),
                                    (1, 2048, 2560), (2, 5376, 4096), (3, 88, 72), (5, 1000, 1160),
                                    (8, 512, 1152), (16, 4096, 5376), (17, 296, 264),
-                                   # M <= 16 (CUDA-core path): many rows (the weight ring
-                                   # wraps), a wide K, and rows too long for the ring
+                                   # M <= 16 (the few-row kernel: W on the MMA's 128-row
+                                   # side, K split over a cluster): many rows, wide K
                                    (2, 20000, 1024), (4, 64, 16384), (2, 64, 40000),
                                    # a wave or more of tiles, 8+ wide (CTA pairs sharing each
                                    # weight tile): odd m-tile count, ragged M / N / K
@@ -190,7 +190,7 @@ def test_linear_qk_norm_rope_matches_oracle(M, D, d_h, H, H_kv, base, scale, alp
     (300, 1152, 256, 4, 1, 1e6, 1.0, 256 ** -0.5),     # one launch, Q 4 tiles + K|V 2 tiles
     (777, 640, 128, 32, 16, 1e6, 8.0, 168 ** -0.5),    # one launch, two heads per tile
     (9, 256, 256, 8, 4, 1e4, 1.0, 256 ** -0.5),        # <= 16 rows: one two-projection
-    (2, 512, 128, 4, 2, 1e6, 8.0, 168 ** -0.5),        # launch on the CUDA cores + prologue
+    (2, 512, 128, 4, 2, 1e6, 8.0, 168 ** -0.5),        # launch of the few-row kernel + prologue
     (16, 384, 128, 2, 2, 1e4, 1.0, 128 ** -0.5),
     (40, 256, 128, 2, 1, 1e4, 1.0, 128 ** -0.5),       # K|V width 256 is one tile, K 128
 ])

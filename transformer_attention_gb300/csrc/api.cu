@@ -100,7 +100,7 @@ cudaError_t project_qk(const void* x, long ldx, int act_dtype, const void* Wq, c
                              st);
   cudaError_t e;
   if (M <= kSkinnyMaxRows) {
-    // A decode step: both projections in one CUDA-core launch.
+    // A decode step: both projections in one launch of the few-row kernel.
     e = launch_linear_skinny2(x, ldx, Wq, D, qbuf, HD, HD, Wkv, D, kvbuf, 2 * KVD, 2 * KVD, M, D,
                               act_dtype, kF16, s, st);
   } else {

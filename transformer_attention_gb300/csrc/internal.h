@@ -70,15 +70,16 @@ cudaError_t launch_linear(const void* A, long lda, const void* W, long ldw, void
                           int M, int N, int K, int in_dtype, int out_dtype, cudaStream_t stream,
                           int* status, int max_ctas);
 
-// The same product for M <= kSkinnyMaxRows on the CUDA cores (bound by
-// reading W from HBM); K % 8 == 0, 16-byte aligned rows.  Its bounded waits
-// record into `status`.
+// The same product for M <= kSkinnyMaxRows (bound by reading W from HBM):
+// W streamed by TMA into the 128-row side of the tcgen05 MMA, K split over
+// a cluster; K % 8 == 0, 16-byte aligned rows.  Its bounded waits record
+// into `status`.
 constexpr int kSkinnyMaxRows = 16;
 cudaError_t launch_linear_skinny(const void* A, long lda, const void* W, long ldw, void* C,
                                  long ldc, int M, int N, int K, int in_dtype, int out_dtype,
                                  cudaStream_t stream, int* status);
-// Two such products of the same A in one launch: C1 = A W1^T (N1 columns)
-// and C2 = A W2^T (N2 columns).
+// Two such products of the same A in one launch: C1 = A W1^T (N1 columns,
+// a multiple of 128) and C2 = A W2^T (N2 columns).
 cudaError_t launch_linear_skinny2(const void* A, long lda, const void* W1, long ldw1, void* C1,
                                   long ldc1, int N1, const void* W2, long ldw2, void* C2,
                                   long ldc2, int N2, int M, int K, int in_dtype, int out_dtype,

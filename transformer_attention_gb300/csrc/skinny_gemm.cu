@@ -3,18 +3,24 @@
 // new token per batch row).
 //
 // With M this small the product does 2*M flops per 2-byte weight, so it is
-// bound by reading W once from HBM, and a 128-row tensor-core tile would be
-// almost all padding.  Both kernels run on the CUDA cores with fp32 sums.
+// bound by reading W once from HBM.  The tensor cores still do the
+// arithmetic, with the operands' roles swapped so that the weights fill the
+// 128-row side of the MMA: D[128 rows of W, 16] = W_tile A^T (tcgen05,
+// M = 128, N = 16; the rows of A past M are read as zeros by TMA).  The CUDA
+// cores then execute no per-element instructions and the kernel is a TMA
+// stream of W.  A tile of 128 rows of W has K/64 k-blocks; to put enough
+// CTAs on the GPU the k-blocks of a tile are split over a cluster of up to 8
+// CTAs, and the cluster's rank-0 CTA sums their fp32 partials through
+// distributed shared memory before it writes C.
 //
-// skinny_bulk_kernel (rows of up to 10240 bf16): one persistent CTA per SM
-// owns an even share of the output columns.  One elected thread streams
-// its rows of W into a ring of shared-memory stages with bulk asynchronous
-// copies (four rows per stage, up to 160 KB in flight per SM), issuing the
-// first stages before it waits for the previous kernel; four groups of four
-// consumer warps each reduce the rows of a stage (one row per warp) against
-// the M rows of A (read through L1) and release the stage.  skinny_gemm_kernel (longer rows): each warp owns
-// two rows of W and streams them with 16-byte loads, eight chunks of both
-// rows in flight.
+// One CTA (4 warps, two CTAs per SM): warp 0's elected lane streams W boxes
+// {64 k, 128 rows} and A boxes {64 k, 16 rows} (128-byte swizzle) into a
+// 4-stage ring, issuing the W copies of the first stages before it waits for
+// the previous kernel (no kernel of the library writes weights, and only the
+// library's kernels let the next kernel start early); warp 1 allocates 32
+// TMEM columns and issues the MMAs; then all four warps read the
+// accumulator (warp w: rows 32w .. 32w + 31 of the tile).  Every mbarrier
+// wait is bounded (ptx.cuh).
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -22,40 +28,20 @@ namespace g3 {
 
 namespace {
 
-constexpr int kWarps = 4;     // warps per CTA
-constexpr int kRows = 2;      // rows of W per warp
-constexpr int kUnroll = 8;    // 256-element K chunks in flight per row
+constexpr int TN = 128;   // rows of W per tile (the MMA's M)
+constexpr int MA = 16;    // rows of A per MMA (the MMA's N); M <= 16
+constexpr int KB = 64;    // k per block
+constexpr int STAGES = 4;
+constexpr int THREADS = 128;
+constexpr int MAX_SPLITS = 8;   // portable cluster size
+constexpr uint32_t W_BYTES = TN * KB * 2;                 // 16 KB
+constexpr uint32_t A_BYTES = MA * KB * 2;                 // 2 KB
+constexpr uint32_t STAGE_BYTES = W_BYTES + A_BYTES;       // 18 KB, a multiple of 1 KB
+constexpr uint32_t RED_BYTES = TN * MA * 4;               // fp32 partials of the tile
+constexpr uint32_t SMEM_BYTES = STAGES * STAGE_BYTES + RED_BYTES + 1024;
+constexpr uint32_t TMEM_COLS = 32;                        // the smallest allocation
 
-__device__ __forceinline__ uint4 ld_stream(const void* p) {
-  uint4 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p));
-  return v;
-}
-
-template <typename T>
-__device__ __forceinline__ void to_f8(const uint4& v, float (&f)[8]);
-template <>
-__device__ __forceinline__ void to_f8<__nv_bfloat16>(const uint4& v, float (&f)[8]) {
-  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const float2 x = __bfloat1622float2(h[i]);
-    f[2 * i] = x.x;
-    f[2 * i + 1] = x.y;
-  }
-}
-template <>
-__device__ __forceinline__ void to_f8<__half>(const uint4& v, float (&f)[8]) {
-  const __half2* h = reinterpret_cast<const __half2*>(&v);
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const float2 x = __half22float2(h[i]);
-    f[2 * i] = x.x;
-    f[2 * i + 1] = x.y;
-  }
-}
+enum : int { kSiteSkFull = 41, kSiteSkEmpty = 42, kSiteSkDone = 43 };
 
 template <typename OutT>
 __device__ __forceinline__ OutT from_f(float v);
@@ -68,309 +54,220 @@ __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float v) {
   return __float2bfloat16_rn(v);
 }
 
-// Output columns n < n1 come from rows of W into C, columns n >= n1 from
-// rows n - n1 of W2 into columns n - n1 of C2 (two projections of the same
-// A in one launch; n1 = N for one).
-template <typename InT, typename OutT, int MB>
-__global__ void __launch_bounds__(kWarps * 32) skinny_gemm_kernel(
-    const InT* __restrict__ A, long lda, const InT* __restrict__ W, long ldw,
-    OutT* __restrict__ C, long ldc, const InT* __restrict__ W2, long ldw2,
-    OutT* __restrict__ C2, long ldc2, int n1, int M, int N, int K) {
-  pdl_enter();
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n0 = (blockIdx.x * kWarps + warp) * kRows;
-  if (n0 >= N) return;
-  const int nr = min(kRows, N - n0);
-  const InT* wrow[kRows];
-#pragma unroll
-  for (int r = 0; r < kRows; ++r) {
-    const int n = n0 + r;
-    wrow[r] = n < n1 ? W + static_cast<size_t>(n) * ldw : W2 + static_cast<size_t>(n - n1) * ldw2;
-  }
-  float acc[MB][kRows];
-#pragma unroll
-  for (int m = 0; m < MB; ++m)
-#pragma unroll
-    for (int r = 0; r < kRows; ++r) acc[m][r] = 0.f;
-
-  for (int k0 = lane * 8; k0 < K; k0 += 256 * kUnroll) {
-    uint4 w[kUnroll][kRows];
-#pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      const int k = k0 + u * 256;
-#pragma unroll
-      for (int r = 0; r < kRows; ++r)
-        w[u][r] = (k < K && r < nr) ? ld_stream(wrow[r] + k) : make_uint4(0u, 0u, 0u, 0u);
-    }
-#pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      const int k = k0 + u * 256;
-      if (k < K) {
-        float wf[kRows][8];
-#pragma unroll
-        for (int r = 0; r < kRows; ++r) to_f8<InT>(w[u][r], wf[r]);
-#pragma unroll
-        for (int m = 0; m < MB; ++m) {
-          if (m < M) {
-            float af[8];
-            to_f8<InT>(__ldg(reinterpret_cast<const uint4*>(A + static_cast<size_t>(m) * lda + k)),
-                       af);
-#pragma unroll
-            for (int r = 0; r < kRows; ++r)
-#pragma unroll
-              for (int e = 0; e < 8; ++e) acc[m][r] = fmaf(af[e], wf[r][e], acc[m][r]);
-          }
-        }
-      }
-    }
-  }
-#pragma unroll
-  for (int m = 0; m < MB; ++m) {
-    if (m < M) {
-#pragma unroll
-      for (int r = 0; r < kRows; ++r) {
-        float v = acc[m][r];
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-        if (lane == 0 && r < nr) {
-          const int n = n0 + r;
-          if (n < n1)
-            C[static_cast<size_t>(m) * ldc + n] = from_f<OutT>(v);
-          else
-            C2[static_cast<size_t>(m) * ldc2 + (n - n1)] = from_f<OutT>(v);
-        }
-      }
-    }
-  }
-}
-
-constexpr int kBulkConsumers = 4;                     // rows per stage = warps per group
-constexpr int kBulkGroups = 4;                        // consumer groups (stages in work at once)
-constexpr int kBulkThreads = 32 * (1 + kBulkConsumers * kBulkGroups);
-constexpr int kBulkMaxStages = 8;
-constexpr uint32_t kBulkRingBytes = 160 * 1024;       // shared memory for the ring
-
-enum : int { kSiteBulkFull = 41, kSiteBulkEmpty = 42 };
-
-// Output column n of this CTA's share [r0, r1) comes from row n of W (n < n1)
-// or row n - n1 of W2.  `stages` ring stages of kBulkConsumers rows (K
-// elements each) sit in dynamic shared memory; consumer group g < groups
-// (warps 1 + 4g .. 4 + 4g) takes stages g, g + groups, ..., its warp c row c
-// of each, so several stages are reduced at once (one warp per sub-partition
-// could not hide the loads' latency).  `stages` is a multiple of `groups`:
-// then every ring slot belongs to one group, which has consumed a slot's
-// previous fill before it waits on the next one (an mbarrier parity wait
-// cannot tell a phase from the one two fills earlier).
-template <typename InT, typename OutT, int MB>
-__global__ void __launch_bounds__(kBulkThreads, 1) skinny_bulk_kernel(
-    const InT* __restrict__ A, long lda, const InT* __restrict__ W, long ldw,
-    OutT* __restrict__ C, long ldc, const InT* __restrict__ W2, long ldw2,
-    OutT* __restrict__ C2, long ldc2, int n1, int M, int N, int K, int stages, int groups,
-    int* status) {
-  extern __shared__ __align__(128) uint8_t ring[];
-  __shared__ __align__(8) uint64_t full[kBulkMaxStages], empty[kBulkMaxStages];
+// Output column n comes from row n of W (tmW, n < n1) or row n - n1 of W2
+// (tmW2) and goes to C or to column n - n1 of C2; n1 is a multiple of TN.
+// CTA b works on tile b / splits, k-block share b % splits (its rank in a
+// cluster of `splits` CTAs).
+template <int AB_BF16, typename OutT>
+__global__ void __launch_bounds__(THREADS, 2)
+    skinny_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmW2,
+                     const __grid_constant__ CUtensorMap tmA, OutT* __restrict__ C, long ldc,
+                     OutT* __restrict__ C2, long ldc2, int n1, int M, int N, int K, int splits,
+                     int* status) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  float* red = reinterpret_cast<float*>(smem + STAGES * STAGE_BYTES);
+  __shared__ __align__(8) uint64_t full[STAGES], empty[STAGES], done;
+  __shared__ uint32_t tmem_sh;
   __shared__ int abort_flag;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const uint32_t row_bytes = static_cast<uint32_t>(K) * sizeof(InT);
-  const uint32_t stage_bytes = row_bytes * kBulkConsumers;
-  const int r0 = static_cast<int>(static_cast<long>(N) * blockIdx.x / gridDim.x);
-  const int r1 = static_cast<int>(static_cast<long>(N) * (blockIdx.x + 1) / gridDim.x);
-  const int nrows = r1 - r0;
-  const int nst = (nrows + kBulkConsumers - 1) / kBulkConsumers;   // stages streamed
+  const int tile = blockIdx.x / splits, split = blockIdx.x % splits;
+  const int row0 = tile * TN;
+  const bool seg2 = row0 >= n1;
+  const CUtensorMap* wmap = seg2 ? &tmW2 : &tmW;
+  const int wrow = seg2 ? row0 - n1 : row0;
+  const int nkb = (K + KB - 1) / KB;
+  const int kb0 = nkb * split / splits;
+  const int nk = nkb * (split + 1) / splits - kb0;   // >= 1: splits <= nkb
+
   if (threadIdx.x == 0) {
-    for (int i = 0; i < stages; ++i) {
-      mbar_init(smem_u32(&full[i]), 1);
-      mbar_init(smem_u32(&empty[i]), kBulkConsumers);
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(smem_u32(&full[s]), 1);
+      mbar_init(smem_u32(&empty[s]), 1);
     }
+    mbar_init(smem_u32(&done), 1);
     abort_flag = 0;
     fence_barrier_init();
+    tma_prefetch_desc(wmap);
+    tma_prefetch_desc(&tmA);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&tmem_sh), TMEM_COLS);
+    tmem_relinquish();
   }
   __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = tmem_sh;
 
   if (warp == 0) {
     if (lane == 0) {
-      // ---------------- producer: this CTA's rows, kBulkConsumers per stage
-      int fills[kBulkMaxStages] = {};
-      bool waited = false;
-      for (int s = 0; s < nst; ++s) {
-        const int st = s % stages;
-        if (s >= stages) {
-          // The ring is full: from here on wait for the previous kernel too.
-          if (!waited) {
-            pdl_wait();
-            pdl_trigger();
-            waited = true;
-          }
-          if (!mbar_wait(smem_u32(&empty[st]), ((s / stages) - 1) & 1, &abort_flag, status,
-                         kSiteBulkEmpty))
-            break;
-        }
-        const int rows = min(kBulkConsumers, nrows - s * kBulkConsumers);
+      // ---------------- producer
+      const int pre = nk < STAGES ? nk : STAGES;
+      int fills[STAGES] = {};
+      for (int j = 0; j < pre; ++j) {   // weights only: no earlier kernel writes them
+        const uint32_t fb = smem_u32(&full[j]);
+        mbar_arrive_expect_tx(fb, STAGE_BYTES);
+        tma_load_2d(smem_u32(smem + j * STAGE_BYTES), wmap, fb, (kb0 + j) * KB, wrow);
+        fills[j] = 1;
+      }
+      pdl_wait();
+      pdl_trigger();
+      for (int j = 0; j < pre; ++j)
+        tma_load_2d(smem_u32(smem + j * STAGE_BYTES + W_BYTES), &tmA, smem_u32(&full[j]),
+                    (kb0 + j) * KB, 0);
+      for (int j = pre; j < nk; ++j) {
+        const int st = j % STAGES;
+        if (!mbar_wait(smem_u32(&empty[st]), ((j / STAGES) - 1) & 1, &abort_flag, status,
+                       kSiteSkEmpty))
+          break;
         const uint32_t fb = smem_u32(&full[st]);
-        mbar_arrive_expect_tx(fb, rows * row_bytes);
-        for (int i = 0; i < rows; ++i) {
-          const int n = r0 + s * kBulkConsumers + i;
-          const InT* src = n < n1 ? W + static_cast<size_t>(n) * ldw
-                                  : W2 + static_cast<size_t>(n - n1) * ldw2;
-          bulk_load(smem_u32(ring + st * stage_bytes + i * row_bytes), src, row_bytes, fb);
-        }
+        mbar_arrive_expect_tx(fb, STAGE_BYTES);
+        tma_load_2d(smem_u32(smem + st * STAGE_BYTES), wmap, fb, (kb0 + j) * KB, wrow);
+        tma_load_2d(smem_u32(smem + st * STAGE_BYTES + W_BYTES), &tmA, fb, (kb0 + j) * KB, 0);
         ++fills[st];
       }
-      if (!waited) {
-        pdl_wait();
-        pdl_trigger();
-      }
       // Every copy lands before shared memory is released.
-      for (int i = 0; i < stages; ++i)
-        if (fills[i] > 0) mbar_wait_drain(smem_u32(&full[i]), (fills[i] - 1) & 1);
+      for (int s = 0; s < STAGES; ++s)
+        if (fills[s] > 0) mbar_wait_drain(smem_u32(&full[s]), (fills[s] - 1) & 1);
     }
-  } else {
-    // ---------------- consumers: warp c of group g reduces row c of its stages
-    pdl_enter();   // A is read and C written only after the previous kernel
-    const int c = (warp - 1) % kBulkConsumers, g = (warp - 1) / kBulkConsumers;
-    for (int s = g; g < groups && s < nst; s += groups) {
-      const int st = s % stages;
-      if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&full[st]), (s / stages) & 1, &abort_flag,
-                                             status, kSiteBulkFull)))
+    __syncwarp();
+  } else if (warp == 1) {
+    // ---------------- MMA issuer: the whole warp runs the loop, one elected
+    // lane issues each tcgen05 instruction
+    const uint32_t lead = elect_one();
+    constexpr uint32_t idesc = idesc_f16(TN, MA, AB_BF16, 0, 0);
+    for (int j = 0; j < nk; ++j) {
+      const int st = j % STAGES;
+      if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&full[st]), (j / STAGES) & 1, &abort_flag,
+                                             status, kSiteSkFull)))
         break;
-      const int r = s * kBulkConsumers + c;
-      if (r < nrows) {
-        const InT* wr = reinterpret_cast<const InT*>(ring + st * stage_bytes + c * row_bytes);
-        float acc[MB];
+      tc_fence_after();
+      const uint32_t w_addr = smem_u32(smem + st * STAGE_BYTES);
+      const uint32_t a_addr = w_addr + W_BYTES;
 #pragma unroll
-        for (int m = 0; m < MB; ++m) acc[m] = 0.f;
-#pragma unroll 2
-        for (int k = lane * 8; k < K; k += 256) {
-          float wf[8];
-          to_f8<InT>(*reinterpret_cast<const uint4*>(wr + k), wf);
-#pragma unroll
-          for (int m = 0; m < MB; ++m) {
-            if (m < M) {
-              float af[8];
-              to_f8<InT>(
-                  __ldg(reinterpret_cast<const uint4*>(A + static_cast<size_t>(m) * lda + k)), af);
-#pragma unroll
-              for (int e = 0; e < 8; ++e) acc[m] = fmaf(af[e], wf[e], acc[m]);
-            }
-          }
-        }
-        const int n = r0 + r;
-#pragma unroll
-        for (int m = 0; m < MB; ++m) {
-          if (m < M) {
-            float v = acc[m];
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-            if (lane == 0) {
-              if (n < n1)
-                C[static_cast<size_t>(m) * ldc + n] = from_f<OutT>(v);
-              else
-                C2[static_cast<size_t>(m) * ldc2 + (n - n1)] = from_f<OutT>(v);
-            }
-          }
-        }
-      }
-      // This warp's reads of the stage are done: the producer may refill it.
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&empty[st]));
+      for (int k = 0; k < KB / 16; ++k)
+        mma_ss_lead(lead, tbase, sdesc_sw128(w_addr + k * 32, 16, 1024),
+                    sdesc_sw128(a_addr + k * 32, 16, 1024), idesc, (j | k) != 0 ? 1u : 0u);
+      mma_commit_lead(lead, smem_u32(&empty[st]));
     }
+    // After the MMAs issued so far (all of them unless a wait gave up).
+    mma_commit_lead(lead, smem_u32(&done));
+  }
+
+  // ---------------- epilogue: all four warps, row r of the tile per thread
+  pdl_wait();   // C is written only after the previous kernel
+  pdl_trigger();
+  const bool got = __all_sync(0xffffffffu, mbar_wait(smem_u32(&done), 0, &abort_flag, status,
+                                                     kSiteSkDone));
+  tc_fence_after();
+  uint32_t v[32];   // columns 0 .. MA - 1 hold this row's products with the rows of A
+  tmem_ld32(tbase + (static_cast<uint32_t>(warp * 32) << 16), v);
+  tmem_ld_wait(v);
+  const int r = warp * 32 + lane;
+  if (splits > 1) {
+#pragma unroll
+    for (int m = 0; m < MA; ++m)
+      if (m < M) red[r * MA + m] = __uint_as_float(v[m]);
+    cluster_sync();   // every CTA's partials are in its shared memory
+    if (split == 0) {
+      for (int q = 1; q < splits; ++q) {
+        const uint32_t peer = mapa_shared(smem_u32(red + r * MA), static_cast<uint32_t>(q));
+#pragma unroll
+        for (int m = 0; m < MA; ++m)
+          if (m < M)
+            v[m] = __float_as_uint(__uint_as_float(v[m]) + ld_shared_cluster_f32(peer + m * 4));
+      }
+    }
+  }
+  const int n = row0 + r;
+  if (split == 0 && got && n < N) {
+#pragma unroll
+    for (int m = 0; m < MA; ++m) {
+      if (m < M) {
+        if (n < n1)
+          C[static_cast<size_t>(m) * ldc + n] = from_f<OutT>(__uint_as_float(v[m]));
+        else
+          C2[static_cast<size_t>(m) * ldc2 + (n - n1)] = from_f<OutT>(__uint_as_float(v[m]));
+      }
+    }
+  }
+  if (splits > 1) cluster_sync();   // rank 0 has read the peers' partials
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tbase, TMEM_COLS);
   }
 }
 
-// Ring stages for rows of K elements: the largest of 2, 4, 8 that fits in
-// kBulkRingBytes, or 0 when two do not fit or the rows cannot be
-// bulk-copied (16-byte alignment of the weights and their row strides).
-template <typename InT>
-int bulk_stages(const void* W, long ldw, const void* W2, long ldw2, int K) {
-  const uint64_t row_bytes = static_cast<uint64_t>(K) * sizeof(InT);
-  const auto al = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
-  if (row_bytes % 16 != 0 || !al(W) || !al(W2) || (ldw * sizeof(InT)) % 16 != 0 ||
-      (ldw2 * sizeof(InT)) % 16 != 0)
-    return 0;
-  const uint64_t st = kBulkRingBytes / (row_bytes * kBulkConsumers);
-  return st >= 8 ? 8 : st >= 4 ? 4 : st >= 2 ? 2 : 0;
+// Tensor maps over W (rows of K elements, row stride ldw) and A, boxes of 64
+// k by `rows` rows, 128-byte swizzle.
+bool encode_rows(CUtensorMap& map, const void* base, long ld, int K, int rows_total,
+                 uint32_t box_rows, int in_dtype) {
+  const CUtensorMapDataType dt =
+      in_dtype == kBF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  const uint64_t dims[2] = {static_cast<uint64_t>(K), static_cast<uint64_t>(rows_total)};
+  const uint64_t str[1] = {static_cast<uint64_t>(ld) * 2};
+  const uint32_t box[2] = {static_cast<uint32_t>(KB), box_rows};
+  return encode_tiled(&map, dt, 2, base, dims, str, box);
 }
 
-template <typename InT, typename OutT, int MB>
-cudaError_t launch_bulk(const InT* a, long lda, const InT* w, long ldw, OutT* c, long ldc,
-                        const InT* w2, long ldw2, OutT* c2, long ldc2, int n1, int M, int N,
-                        int K, int stages, cudaStream_t stream, int* status) {
-  auto kern = skinny_bulk_kernel<InT, OutT, MB>;
+template <int AB, typename OutT>
+cudaError_t launch_tc(const CUtensorMap& tw, const CUtensorMap& tw2, const CUtensorMap& ta,
+                      void* C, long ldc, void* C2, long ldc2, int n1, int M, int N, int K,
+                      cudaStream_t stream, int* status) {
+  auto kern = skinny_tc_kernel<AB, OutT>;
   static bool attr_set = false;  // benign race: setting the same attribute twice is harmless
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(kBulkRingBytes));
+    cudaError_t e =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  const size_t smem = static_cast<size_t>(stages) * K * sizeof(InT) * kBulkConsumers;
-  const int grid = N < num_sms() ? N : num_sms();
-  const int groups = stages < kBulkGroups ? stages : kBulkGroups;   // divides stages
-  return launch_pdl(kern, dim3(grid), dim3(kBulkThreads), smem, stream, a, lda, w, ldw, c, ldc,
-                    w2, ldw2, c2, ldc2, n1, M, N, K, stages, groups, status);
-}
-
-template <typename InT, typename OutT>
-cudaError_t launch_skinny_typed(const void* A, long lda, const void* W, long ldw, void* C,
-                                long ldc, const void* W2, long ldw2, void* C2, long ldc2, int n1,
-                                int M, int N, int K, cudaStream_t stream, int* status) {
-  const int stages = bulk_stages<InT>(W, ldw, W2, ldw2, K);
-  if (stages > 0) {
-    const InT* a = static_cast<const InT*>(A);
-    const InT* w = static_cast<const InT*>(W);
-    const InT* w2 = static_cast<const InT*>(W2);
-    OutT* c = static_cast<OutT*>(C);
-    OutT* c2 = static_cast<OutT*>(C2);
-    if (M <= 1)
-      return launch_bulk<InT, OutT, 1>(a, lda, w, ldw, c, ldc, w2, ldw2, c2, ldc2, n1, M, N, K,
-                                       stages, stream, status);
-    if (M <= 2)
-      return launch_bulk<InT, OutT, 2>(a, lda, w, ldw, c, ldc, w2, ldw2, c2, ldc2, n1, M, N, K,
-                                       stages, stream, status);
-    if (M <= 4)
-      return launch_bulk<InT, OutT, 4>(a, lda, w, ldw, c, ldc, w2, ldw2, c2, ldc2, n1, M, N, K,
-                                       stages, stream, status);
-    if (M <= 8)
-      return launch_bulk<InT, OutT, 8>(a, lda, w, ldw, c, ldc, w2, ldw2, c2, ldc2, n1, M, N, K,
-                                       stages, stream, status);
-    return launch_bulk<InT, OutT, 16>(a, lda, w, ldw, c, ldc, w2, ldw2, c2, ldc2, n1, M, N, K,
-                                      stages, stream, status);
-  }
-  const int per_cta = kWarps * kRows;
-  const dim3 grid((N + per_cta - 1) / per_cta);
-  const InT* a = static_cast<const InT*>(A);
-  const InT* w = static_cast<const InT*>(W);
-  const InT* w2 = static_cast<const InT*>(W2);
+  // Split each tile's k-blocks over enough CTAs to fill two per SM.
+  const int tiles = (N + TN - 1) / TN;
+  const int nkb = (K + KB - 1) / KB;
+  int splits = 2 * num_sms() / tiles;
+  if (splits > MAX_SPLITS) splits = MAX_SPLITS;
+  if (splits > nkb) splits = nkb;
+  if (splits < 1) splits = 1;
   OutT* c = static_cast<OutT*>(C);
   OutT* c2 = static_cast<OutT*>(C2);
-  const dim3 block(kWarps * 32);
-  if (M <= 4)
-    return launch_pdl(skinny_gemm_kernel<InT, OutT, 4>, grid, block, 0, stream, a, lda, w, ldw, c,
-                      ldc, w2, ldw2, c2, ldc2, n1, M, N, K);
-  if (M <= 8)
-    return launch_pdl(skinny_gemm_kernel<InT, OutT, 8>, grid, block, 0, stream, a, lda, w, ldw, c,
-                      ldc, w2, ldw2, c2, ldc2, n1, M, N, K);
-  return launch_pdl(skinny_gemm_kernel<InT, OutT, 16>, grid, block, 0, stream, a, lda, w, ldw, c,
-                    ldc, w2, ldw2, c2, ldc2, n1, M, N, K);
+  const dim3 grid(tiles * splits);
+  if (splits == 1)
+    return launch_pdl(kern, grid, dim3(THREADS), SMEM_BYTES, stream, tw, tw2, ta, c, ldc, c2,
+                      ldc2, n1, M, N, K, splits, status);
+  return launch_pdl_cluster(kern, grid, dim3(THREADS), SMEM_BYTES, splits, stream, tw, tw2, ta, c,
+                            ldc, c2, ldc2, n1, M, N, K, splits, status);
 }
 
-template <typename IT>
-cudaError_t launch_skinny_out(const void* A, long lda, const void* W, long ldw, void* C, long ldc,
-                              const void* W2, long ldw2, void* C2, long ldc2, int n1, int M, int N,
-                              int K, int out_dtype, cudaStream_t stream, int* status) {
-  switch (out_dtype) {
-    case kF32:
-      return launch_skinny_typed<IT, float>(A, lda, W, ldw, C, ldc, W2, ldw2, C2, ldc2, n1, M, N,
-                                            K, stream, status);
-    case kF16:
-      return launch_skinny_typed<IT, __half>(A, lda, W, ldw, C, ldc, W2, ldw2, C2, ldc2, n1, M, N,
-                                             K, stream, status);
-    case kBF16:
-      return launch_skinny_typed<IT, __nv_bfloat16>(A, lda, W, ldw, C, ldc, W2, ldw2, C2, ldc2,
-                                                    n1, M, N, K, stream, status);
-    default:
-      return cudaErrorInvalidValue;
+// One launch over the columns [0, N) (two weight segments split at n1, a
+// multiple of TN, or n1 = N).
+cudaError_t launch_segments(const void* A, long lda, const void* W, long ldw, void* C, long ldc,
+                            const void* W2, long ldw2, void* C2, long ldc2, int n1, int M, int N,
+                            int K, int in_dtype, int out_dtype, cudaStream_t stream, int* status) {
+  CUtensorMap tw, tw2, ta;
+  if (!encode_rows(tw, W, ldw, K, n1, TN, in_dtype) ||
+      !encode_rows(ta, A, lda, K, M, MA, in_dtype))
+    return cudaErrorInvalidValue;
+  tw2 = tw;
+  if (n1 < N && !encode_rows(tw2, W2, ldw2, K, N - n1, TN, in_dtype)) return cudaErrorInvalidValue;
+#define G3_SK_OUT(AB)                                                                            \
+  switch (out_dtype) {                                                                           \
+    case kF32:                                                                                   \
+      return launch_tc<AB, float>(tw, tw2, ta, C, ldc, C2, ldc2, n1, M, N, K, stream, status);   \
+    case kF16:                                                                                   \
+      return launch_tc<AB, __half>(tw, tw2, ta, C, ldc, C2, ldc2, n1, M, N, K, stream, status);  \
+    case kBF16:                                                                                  \
+      return launch_tc<AB, __nv_bfloat16>(tw, tw2, ta, C, ldc, C2, ldc2, n1, M, N, K, stream,    \
+                                          status);                                               \
+    default: return cudaErrorInvalidValue;                                                       \
   }
+  if (in_dtype == kBF16) {
+    G3_SK_OUT(1)
+  }
+  G3_SK_OUT(0)
+#undef G3_SK_OUT
 }
 
 cudaError_t launch_skinny_any(const void* A, long lda, const void* W, long ldw, void* C,
@@ -379,13 +276,11 @@ cudaError_t launch_skinny_any(const void* A, long lda, const void* W, long ldw, 
                               cudaStream_t stream, int* status) {
   if (M <= 0 || N <= 0 || K <= 0) return cudaSuccess;
   if (M > kSkinnyMaxRows || K % 8 != 0) return cudaErrorInvalidValue;
-  if (in_dtype == kBF16)
-    return launch_skinny_out<__nv_bfloat16>(A, lda, W, ldw, C, ldc, W2, ldw2, C2, ldc2, n1, M, N,
-                                            K, out_dtype, stream, status);
-  if (in_dtype == kF16)
-    return launch_skinny_out<__half>(A, lda, W, ldw, C, ldc, W2, ldw2, C2, ldc2, n1, M, N, K,
-                                     out_dtype, stream, status);
-  return cudaErrorInvalidValue;
+  if (in_dtype != kBF16 && in_dtype != kF16) return cudaErrorInvalidValue;
+  // (the two-segment callers split at H * d_h, a multiple of TN)
+  if (n1 < N && n1 % TN != 0) return cudaErrorInvalidValue;
+  return launch_segments(A, lda, W, ldw, C, ldc, W2, ldw2, C2, ldc2, n1 < N ? n1 : N, M, N, K,
+                         in_dtype, out_dtype, stream, status);
 }
 
 }  // namespace
