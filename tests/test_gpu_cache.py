@@ -155,7 +155,9 @@ LAYERS = [
                          f"{k['attn_type']}-T0{k['T0']}")
 def test_forward_cached_prompt_decode_chunk(kw):
     """A padded prompt at slot 0, then 1-token decode steps, then a 3-token
-    chunk; every call's output against the oracle's cached layer."""
+    chunk and a padded 4-token chunk (these few-row calls write the cache
+    from the QK-norm/RoPE kernel); every call's output against the oracle's
+    cached layer."""
     import transformer_attention_gb300 as G3
     kw = dict(kw)
     T0, pads, S = kw.pop("T0"), kw.pop("pads"), kw.pop("S")
@@ -182,6 +184,11 @@ def test_forward_cached_prompt_decode_chunk(kw):
     calls.append((x_all[:, used:used + n],
                   torch.stack([torch.arange(v + 4, v + 4 + n, dtype=torch.int32) for v in valid]),
                   None, end))
+    end, used = end + n, used + n
+    n = 4
+    calls.append((x_all[:, used:used + n],
+                  torch.stack([torch.arange(v + 7, v + 7 + n, dtype=torch.int32) for v in valid]),
+                  torch.tensor([1] + [0] * (B - 1), dtype=torch.int32), end))
 
     for xc, seg, pad, e in calls:
         got = G3.attention_forward_cached(

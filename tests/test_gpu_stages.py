@@ -119,16 +119,16 @@ def test_linear_pairs_match_single_ctas_bitwise():
     (128, 32, 16, 1e6, 8.0, 168 ** -0.5),
     (128, 4, 2, 1e4, 1.0, 128 ** -0.5),
 ])
-def test_qk_norm_rope_matches_oracle(d_h, H, H_kv, base, scale, alpha):
+@pytest.mark.parametrize("M", [777, 3])   # head vectors 8 steps per warp / 1 step per warp
+def test_qk_norm_rope_matches_oracle(d_h, H, H_kv, base, scale, alpha, M):
     import transformer_attention_gb300 as G3
-    M = 777
     Qr = _randn((M, H * d_h), 10, 1.0, torch.float16)
     KVr = _randn((M, 2 * H_kv * d_h), 11, 1.0, torch.float16)
     gq = _randn((d_h,), 12, 0.1 ** 0.5)
     gk = _randn((d_h,), 13, 0.1 ** 0.5)
     g = torch.Generator().manual_seed(14)
-    pos = torch.cat([torch.arange(0, 300), torch.randint(0, 131072, (M - 302,), generator=g),
-                     torch.tensor([131071, 2 ** 20])]).to(torch.int32)
+    pos = torch.cat([torch.arange(0, 300), torch.randint(0, 131072, (475,), generator=g),
+                     torch.tensor([131071, 2 ** 20])]).to(torch.int32)[-M:].contiguous()
     Qd, KVd = Qr.cuda(), KVr.cuda()
     G3.gemma3_qk_norm_rope(Qd, H * d_h, KVd, 2 * H_kv * d_h, gq.cuda(), gk.cuda(), pos.cuda(),
                            M, H, H_kv, d_h, base, scale, alpha)

@@ -88,11 +88,15 @@ AttnWs attn_ws(const gemma3_attn_dims* d, bool f16_weights = false) {
 // with QK-norm, RoPE and the query scale fused into its epilogue when the
 // head vectors tile the 256-wide output tiles (every Gemma 3 shape with more
 // than 16 rows), else the two projections followed by the prologue kernel.
+// With `cache` (a CacheRows with Kc set) the prologue kernel also writes the
+// rows to their cache slots, and *cache_done tells whether it ran (the fused
+// GEMM does not write the cache).
 cudaError_t project_qk(const void* x, long ldx, int act_dtype, const void* Wq, const void* Wkv,
                        void* qbuf, void* kvbuf, const void* gamma_q, const void* gamma_k,
                        const int32_t* pos, int M, int D, int H, int H_kv, int d_h,
                        double rope_base, double rope_scale, float query_scale, cudaStream_t s,
-                       int* st) {
+                       int* st, const CacheRows* cache = nullptr, bool* cache_done = nullptr) {
+  if (cache_done != nullptr) *cache_done = false;
   const int HD = H * d_h, KVD = H_kv * d_h;
   if (linear_qknorm_fusable(M, HD, HD, d_h) && linear_qknorm_fusable(M, 2 * KVD, KVD, d_h))
     return launch_qkv_qknorm(x, ldx, Wq, Wkv, D, qbuf, HD, kvbuf, 2 * KVD, M, HD, KVD, D, act_dtype,
@@ -109,8 +113,11 @@ cudaError_t project_qk(const void* x, long ldx, int act_dtype, const void* Wq, c
     e = launch_linear(x, ldx, Wkv, D, kvbuf, 2 * KVD, M, 2 * KVD, D, act_dtype, kF16, s, st, 0);
   }
   if (e != cudaSuccess) return e;
-  return launch_qk_norm_rope(qbuf, HD, kvbuf, 2 * KVD, gamma_q, gamma_k, pos, M, H, H_kv, d_h,
-                             rope_base, rope_scale, query_scale, s);
+  e = launch_qk_norm_rope(qbuf, HD, kvbuf, 2 * KVD, gamma_q, gamma_k, pos, M, H, H_kv, d_h,
+                          rope_base, rope_scale, query_scale, s,
+                          cache != nullptr ? *cache : CacheRows{});
+  if (e == cudaSuccess && cache != nullptr && cache_done != nullptr) *cache_done = true;
+  return e;
 }
 
 // The layer pipeline shared by the single-layer and block entry points.
@@ -628,11 +635,25 @@ int gemma3_attn_forward_cached(const gemma3_attn_dims* dims, int S, int end_inde
   uint8_t* kvbuf = ws + w.q;          // [K'|V] fp16  [M, 2*KVD]
   uint8_t* aws = kvbuf + w.kv;        // attention partials
   cudaStream_t s = as_stream(stream);
+  // The new K'/V rows go to the cache from the prologue kernel when it runs
+  // on its own (a decode step), else by the append kernel.
+  CacheRows cr;
+  cr.Kc = K_cache;
+  cr.Vc = V_cache;
+  cr.posc = pos_cache;
+  cr.V = kvbuf + KVD * 2;
+  cr.ldv = 2 * KVD;
+  cr.pad_lens = pad_lens;
+  cr.T = d->T;
+  cr.S = S;
+  cr.end = end_index;
+  bool cached = false;
   if (project_qk(x, d->D, kBF16, Wq, Wkv, qbuf, kvbuf, gamma_q, gamma_k, segment_pos, M, d->D,
-                 d->H, d->H_kv, d->d_h, rope_base, rope_scale, query_scale, s, st) !=
-          cudaSuccess ||
-      launch_kv_cache_append(kvbuf, kvbuf + KVD * 2, 2 * KVD, segment_pos, pad_lens, d->B, d->T, S,
-                             end_index, KVD, K_cache, V_cache, pos_cache, s) != cudaSuccess)
+                 d->H, d->H_kv, d->d_h, rope_base, rope_scale, query_scale, s, st, &cr,
+                 &cached) != cudaSuccess ||
+      (!cached &&
+       launch_kv_cache_append(kvbuf, kvbuf + KVD * 2, 2 * KVD, segment_pos, pad_lens, d->B, d->T, S,
+                              end_index, KVD, K_cache, V_cache, pos_cache, s) != cudaSuccess))
     return GEMMA3_ERR_CUDA;
   cudaError_t e;
   if (end_index == 0 && attn_type == GEMMA3_GLOBAL && d->T >= kFlashPrefillMinT)

@@ -35,13 +35,17 @@ constexpr float kEps = 1e-6f;
 
 constexpr int kVecUnroll = 8;  // head vectors in flight per lane
 
+// Work items are (row m, chunk of up to chunk_u * VPW head vectors): a warp
+// per item, so that a decode step's few rows spread over many warps
+// (chunk_u = 1) while long inputs amortise the angle math over a row's
+// vectors (chunk_u = kVecUnroll).
 template <int DH>
 __global__ void __launch_bounds__(256, 2)
     qk_norm_rope_kernel(__half* __restrict__ Q, long ldq, __half* __restrict__ K, long ldk,
                         const __nv_bfloat16* __restrict__ gamma_q,
                         const __nv_bfloat16* __restrict__ gamma_k, const int32_t* __restrict__ pos,
                         int M, int H, int H_kv, const __grid_constant__ RopeFreqs freqs,
-                        float query_scale) {
+                        float query_scale, const __grid_constant__ CacheRows cache, int chunk_u) {
   pdl_enter();
   constexpr int LPV = DH / 8;      // lanes per head vector
   constexpr int VPW = 32 / LPV;    // head vectors per warp step
@@ -57,36 +61,38 @@ __global__ void __launch_bounds__(256, 2)
 
   const int warps_total = gridDim.x * (blockDim.x >> 5);
   const int nvec = H + H_kv;
-  for (int m = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); m < M; m += warps_total) {
-    // Issue this token's head-vector loads first, then the angle math.
+  const int vpc = VPW * chunk_u;                   // head vectors per item
+  const int nch = (nvec + vpc - 1) / vpc;          // items per row
+  const long items = static_cast<long>(M) * nch;
+  const int KVD = H_kv * DH;
+  __half* const Kc = static_cast<__half*>(cache.Kc);
+  for (long item = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); item < items;
+       item += warps_total) {
+    const int m = static_cast<int>(item / nch);
+    const int base = static_cast<int>(item % nch) * vpc;   // first head vector of the item
+    // this row's cache slot (with cache.Kc)
+    const size_t slot =
+        static_cast<size_t>(m / cache.T) * cache.S + cache.end + m % cache.T;
+    // Issue the item's head-vector loads first, then the angle math.
     uint4 raw[kVecUnroll];
-    const int first = sub;
+    const int first = base + sub;
 #pragma unroll
     for (int u = 0; u < kVecUnroll; ++u) {
       const int hv = first + u * VPW;
       const __half* src = hv < H ? Q + static_cast<long>(m) * ldq + hv * DH
                                  : K + static_cast<long>(m) * ldk + (hv - H) * DH;
-      raw[u] = hv < nvec ? *reinterpret_cast<const uint4*>(src + ll * 8) : make_uint4(0, 0, 0, 0);
+      raw[u] = (u < chunk_u && hv < nvec) ? *reinterpret_cast<const uint4*>(src + ll * 8)
+                                          : make_uint4(0, 0, 0, 0);
     }
     const float p = static_cast<float>(pos[m]);
     float cs[8], sn[8];
 #pragma unroll
     for (int e = 0; e < 8; ++e) rope_sincos(p, freqs.f[c0 + e], sn[e], cs[e]);
-    for (int base = 0; base < nvec; base += VPW * kVecUnroll) {
-      if (base > 0) {
-#pragma unroll
-        for (int u = 0; u < kVecUnroll; ++u) {
-          const int hv = base + first + u * VPW;
-          const __half* src = hv < H ? Q + static_cast<long>(m) * ldq + hv * DH
-                                     : K + static_cast<long>(m) * ldk + (hv - H) * DH;
-          raw[u] =
-              hv < nvec ? *reinterpret_cast<const uint4*>(src + ll * 8) : make_uint4(0, 0, 0, 0);
-        }
-      }
+    {
 #pragma unroll
       for (int u = 0; u < kVecUnroll; ++u) {
-        if (base + u * VPW >= nvec) break;   // warp-uniform
-        const int hv = base + first + u * VPW;
+        if (u >= chunk_u || base + u * VPW >= nvec) break;   // warp-uniform
+        const int hv = first + u * VPW;
         const bool is_q = hv < H;
         float x[8];
         const __half2* h2 = reinterpret_cast<const __half2*>(&raw[u]);
@@ -132,8 +138,21 @@ __global__ void __launch_bounds__(256, 2)
           __half* dst = is_q ? Q + static_cast<long>(m) * ldq + hv * DH
                              : K + static_cast<long>(m) * ldk + (hv - H) * DH;
           *reinterpret_cast<uint4*>(dst + ll * 8) = w;
+          if (!is_q && Kc != nullptr) {
+            // K' head j and V head j of the row go to its cache slot
+            const int off = (hv - H) * DH + ll * 8;
+            *reinterpret_cast<uint4*>(Kc + slot * KVD + off) = w;
+            *reinterpret_cast<uint4*>(static_cast<__half*>(cache.Vc) + slot * KVD + off) =
+                *reinterpret_cast<const uint4*>(static_cast<const __half*>(cache.V) +
+                                                static_cast<long>(m) * cache.ldv + off);
+          }
         }
       }
+    }
+    if (Kc != nullptr && base == 0 && lane == 0) {   // the slot's position
+      const int b = m / cache.T, t = m % cache.T;
+      const int valid = cache.T - (cache.pad_lens != nullptr ? cache.pad_lens[b] : 0);
+      cache.posc[slot] = t < valid ? pos[m] : -1;
     }
   }
 }
@@ -374,10 +393,18 @@ cudaError_t launch_post_typed(cudaStream_t s, const float* a, const T* x, const 
 cudaError_t launch_qk_norm_rope(void* Q, long ldq, void* K, long ldk, const void* gamma_q,
                                 const void* gamma_k, const int32_t* pos, int M, int H, int H_kv,
                                 int d_h, double rope_base, double rope_scale, float query_scale,
-                                cudaStream_t stream) {
+                                cudaStream_t stream, const CacheRows& cache) {
   if (M <= 0) return cudaSuccess;
+  if (cache.Kc != nullptr && (cache.T < 1 || M % cache.T != 0)) return cudaErrorInvalidValue;
+  if (d_h != 128 && d_h != 256) return cudaErrorInvalidValue;
+  // Few rows (a decode step): one warp per head-vector step of a row, so the
+  // rows' vectors run on many warps at once; else up to kVecUnroll steps per
+  // warp.
+  const int chunk_u = M <= 64 ? 1 : kVecUnroll;
+  const int vpc = (32 / (d_h / 8)) * chunk_u;
+  const long items = static_cast<long>(M) * ((H + H_kv + vpc - 1) / vpc);
   const int warps_per_block = 8;
-  long blocks = (M + warps_per_block - 1) / warps_per_block;
+  long blocks = (items + warps_per_block - 1) / warps_per_block;
   const long cap = static_cast<long>(num_sms()) * 4;
   if (blocks > cap) blocks = cap;
   const RopeFreqs freqs = make_rope_freqs(d_h, rope_base, rope_scale);
@@ -387,10 +414,10 @@ cudaError_t launch_qk_norm_rope(void* Q, long ldq, void* K, long ldk, const void
   auto gk = static_cast<const __nv_bfloat16*>(gamma_k);
   if (d_h == 256)
     return launch_pdl(qk_norm_rope_kernel<256>, dim3(blocks), dim3(256), 0, stream, q, ldq, k,
-                      ldk, gq, gk, pos, M, H, H_kv, freqs, query_scale);
+                      ldk, gq, gk, pos, M, H, H_kv, freqs, query_scale, cache, chunk_u);
   if (d_h == 128)
     return launch_pdl(qk_norm_rope_kernel<128>, dim3(blocks), dim3(256), 0, stream, q, ldq, k,
-                      ldk, gq, gk, pos, M, H, H_kv, freqs, query_scale);
+                      ldk, gq, gk, pos, M, H, H_kv, freqs, query_scale, cache, chunk_u);
   return cudaErrorInvalidValue;
 }
 

@@ -111,12 +111,28 @@ cudaError_t launch_qkv_qknorm(const void* A, long lda, const void* Wq, const voi
                               const int32_t* pos, int d_h, double rope_base, double rope_scale,
                               float query_scale, cudaStream_t stream, int* status);
 
+// Where a decode step's new K'/V rows also go: row m = b*T + t to slot
+// b*S + end + t of the fp16 caches Kc / Vc ([B, S, H_kv*d_h]), its position
+// pos[m] (or -1 for t past the valid length T - pad_lens[b]) to posc
+// ([B, S]); V is read from rows of V with stride ldv.  Kc == nullptr: none.
+struct CacheRows {
+  void* Kc = nullptr;
+  void* Vc = nullptr;
+  int32_t* posc = nullptr;
+  const void* V = nullptr;
+  long ldv = 0;
+  const int32_t* pad_lens = nullptr;
+  int T = 1, S = 0, end = 0;
+};
+
 // In place on fp16 rows: Q[m, h*d_h:(h+1)*d_h] and K[m, j*d_h:(j+1)*d_h] get
-// last-axis RMSNorm, (1 + gamma), RoPE; Q also the query scale.
+// last-axis RMSNorm, (1 + gamma), RoPE; Q also the query scale.  With
+// cache.Kc the normalised K' rows, the V rows and the positions are also
+// written to their cache slots (the cache write of a decode step).
 cudaError_t launch_qk_norm_rope(void* Q, long ldq, void* K, long ldk, const void* gamma_q,
                                 const void* gamma_k, const int32_t* pos, int M, int H, int H_kv,
                                 int d_h, double rope_base, double rope_scale, float query_scale,
-                                cudaStream_t stream);
+                                cudaStream_t stream, const CacheRows& cache = CacheRows{});
 
 // Flash attention forward over Q' [B,T,H,d_h] fp16 and K'/V rows of an fp16
 // buffer with row stride ldkv (K' at column j*d_h, V at column v_off + j*d_h).
