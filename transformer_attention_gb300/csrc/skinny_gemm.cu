@@ -32,6 +32,7 @@ constexpr int TN = 128;   // rows of W per tile (the MMA's M)
 constexpr int MA = 16;    // rows of A per MMA (the MMA's N); M <= 16
 constexpr int KB = 64;    // k per block
 constexpr int STAGES = 4;
+constexpr int CTAS_PER_SM = 2;
 constexpr int THREADS = 128;
 constexpr int MAX_SPLITS = 8;   // portable cluster size
 constexpr uint32_t W_BYTES = TN * KB * 2;                 // 16 KB
@@ -59,7 +60,7 @@ __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float v) {
 // CTA b works on tile b / splits, k-block share b % splits (its rank in a
 // cluster of `splits` CTAs).
 template <int AB_BF16, typename OutT>
-__global__ void __launch_bounds__(THREADS, 2)
+__global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
     skinny_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmW2,
                      const __grid_constant__ CUtensorMap tmA, OutT* __restrict__ C, long ldc,
                      OutT* __restrict__ C2, long ldc2, int n1, int M, int N, int K, int splits,
@@ -224,10 +225,10 @@ cudaError_t launch_tc(const CUtensorMap& tw, const CUtensorMap& tw2, const CUten
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  // Split each tile's k-blocks over enough CTAs to fill two per SM.
+  // Split each tile's k-blocks over enough CTAs to fill every SM.
   const int tiles = (N + TN - 1) / TN;
   const int nkb = (K + KB - 1) / KB;
-  int splits = 2 * num_sms() / tiles;
+  int splits = CTAS_PER_SM * num_sms() / tiles;
   if (splits > MAX_SPLITS) splits = MAX_SPLITS;
   if (splits > nkb) splits = nkb;
   if (splits < 1) splits = 1;
