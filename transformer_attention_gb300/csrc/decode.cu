@@ -33,7 +33,7 @@ constexpr int kDecThreads = (kCWarps + 1) * 32;
 constexpr int kSpanChunk = 4096;   // slots scanned per CTA by the span kernel (256 x 16)
 constexpr int kMaxSplitCtas = 2048;
 constexpr int kMaxCombineSplits = 256;   // splits per row the combine kernel holds weights for
-constexpr int kMinSplitTiles = 4;        // fewest tiles worth a split of its own
+constexpr int kMinSplitTiles = 2;        // fewest tiles worth a split of its own
 constexpr float kLog2e = 1.4426950408889634f;
 
 enum { kSiteDecFull = 40, kSiteDecEmpty = 41, kSiteDecIssued = 42 };
