@@ -663,13 +663,13 @@ def decode_work(w, sms: int) -> tuple:
     lin += metrics.prologue_bytes(M, H, H_kv, d_h)
     work = {"attention": float(attn), "linear": float(lin)}
     # splits of the cache attention (the library's plan: two CTAs per SM over
-    # B * H_kv * query groups, at least one 32-slot tile each)
+    # B * H_kv * query groups, at least two 32-slot tiles each)
     G = H // H_kv
     want = min(w.T * G, 8)
     rb = max(G, 2 if want <= 2 else (4 if want <= 4 else 8))
     units = w.B * H_kv * ((w.T + rb // G - 1) // (rb // G))
     est = end + w.T if w.window == 0 else min(end + w.T, w.window + w.T)
-    nsplit = max(1, min((2 * sms) // units, (est + 127) // 128, max(1, 2048 // units), 256))
+    nsplit = max(1, min((2 * sms) // units, (est + 63) // 64, max(1, 2048 // units), 256))
     # (the QK prologue also writes the new K'/V rows and positions to the cache)
     launches = {"linear": 3,
                 "attention": 1 + (1 if w.window > 0 else 0) + (1 if nsplit > 1 else 0)}
