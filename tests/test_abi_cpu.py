@@ -41,6 +41,26 @@ def test_library_exports_every_declared_function(lib):
     assert set(names) == set(L.SIGNATURES), "binding and header disagree"
 
 
+def _declared_arities():
+    """Parameter count of every function the header declares."""
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    out = {}
+    for m in re.finditer(r"\b(gemma3_[a-z0-9_]+)\s*\(([^;{]*?)\)\s*;", src):
+        params = " ".join(m.group(2).split())
+        out[m.group(1)] = 0 if params in ("", "void") else params.count(",") + 1
+    return out
+
+
+def test_binding_argument_counts_match_header():
+    # a ctypes table entry with the wrong number of arguments would pass
+    # every call's arguments shifted; compare it with the header's prototypes
+    arity = _declared_arities()
+    assert set(arity) == set(L.SIGNATURES)
+    for name, (_, argtypes) in L.SIGNATURES.items():
+        assert len(argtypes) == arity[name], (name, len(argtypes), arity[name])
+
+
 def test_routing_matches_golden_table(lib):
     with open(os.path.join(ROOT, "tests", "golden", "routing_types.json")) as f:
         table = json.load(f)["types"]
