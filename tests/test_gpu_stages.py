@@ -84,15 +84,17 @@ def _pairs_in_use():
     return 20 * G3.gemma3_gemm_pair_clusters() >= 9 * sms
 
 
-def test_linear_pairs_small_grid_many_units():
+@pytest.mark.parametrize("max_ctas", [4, 1])
+def test_linear_pairs_small_grid_many_units(max_ctas):
     # two CTA pairs walking 80 units (160 tiles): the shared stage ring and
-    # both CTAs' accumulator rings turn over many times
+    # both CTAs' accumulator rings turn over many times; a cap of one CTA
+    # runs the same 160 tiles on a single CTA instead
     import transformer_attention_gb300 as G3
     if not _pairs_in_use():
         pytest.skip("the device holds GEMM CTA pairs on fewer than 90% of its SMs")
     A = _randn((2048, 640), 6)
     W = _randn((2560, 640), 7, 640 ** -0.5)
-    C = G3.linear(A.cuda(), W.cuda(), out_dtype=torch.float32, max_ctas=4)
+    C = G3.linear(A.cuda(), W.cuda(), out_dtype=torch.float32, max_ctas=max_ctas)
     assert G3.gemma3_attn_check_status() == 0
     assert rel_frob(C.cpu(), O.project(A, W)) <= 1e-5
 

@@ -587,7 +587,7 @@ cudaError_t launch_typed(const CUtensorMap& ta, const CUtensorMap& tb, void* C, 
   if (pairs && EPI == kEpiPlain) {
     const int units = (((M + BM - 1) / BM + 1) / 2) * ((N + bn_out - 1) / bn_out);
     int ncl = gemm_max_pairs();
-    if (max_ctas > 0 && max_ctas / 2 < ncl) ncl = max_ctas / 2 > 0 ? max_ctas / 2 : 1;
+    if (max_ctas > 0 && max_ctas / 2 < ncl) ncl = max_ctas / 2;   // max_ctas >= 2 here
     if (units < ncl) ncl = units;
     return launch_pdl_cluster(kern, dim3(2 * ncl), dim3(THREADS), SMEM_BYTES, 2, stream, ta, tb,
                               tc, tb2 != nullptr ? *tb2 : tb, tc2, M, N, K, status, epi);
@@ -626,7 +626,8 @@ cudaError_t launch_linear(const void* A, long lda, const void* W, long ldw, void
   if (M <= kSkinnyMaxRows)
     return launch_linear_skinny(A, lda, W, ldw, C, ldc, M, N, K, in_dtype, out_dtype, stream,
                                 status);
-  const bool pairs = gemm_use_pairs(M, N);
+  // (a cap of one CTA rules out a pair)
+  const bool pairs = gemm_use_pairs(M, N) && max_ctas != 1;
   CUtensorMap ta, tb;
   if (!encode_ab(ta, tb, A, lda, W, ldw, M, N, K, in_dtype, pairs ? BN / 2 : BN))
     return cudaErrorInvalidValue;
