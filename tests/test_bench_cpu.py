@@ -1,0 +1,55 @@
+"""CPU checks of the measurement code in bench.py: the DRAM-traffic lookup
+honours the captured source's hash, and the decode step's algorithmic bytes
+and launch counts follow the workloads' shapes."""
+import json
+import os
+
+import pytest
+
+import bench
+from transformer_attention_gb300 import workloads as WL
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def test_traffic_for_returns_the_committed_bytes_while_the_source_matches():
+    with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+        table = json.load(f)
+    checked = 0
+    for kernel, rows in table.items():
+        for workload, e in rows.items():
+            src = os.path.join(ROOT, "transformer_attention_gb300", "csrc", e["source"])
+            if bench.source_hash(src) == e["source_sha256_16"]:
+                assert bench.traffic_for(kernel, workload) == e["dram_bytes_per_launch"]
+                checked += 1
+            else:
+                assert bench.traffic_for(kernel, workload) is None
+    assert checked > 0
+    assert bench.traffic_for("attention", "no_such_workload") is None
+    assert bench.traffic_for("no_such_kernel", "1b_global") is None
+
+
+def test_traffic_for_is_null_once_the_source_changed(monkeypatch):
+    monkeypatch.setattr(bench, "source_hash", lambda path: "0" * 16)
+    assert bench.traffic_for("attention", "1b_global") is None
+
+
+@pytest.mark.parametrize("name", ["27b_global_decode", "4b_local_decode"])
+def test_decode_work_bytes(name):
+    w = WL.WORKLOADS[name]
+    work, launches = bench.decode_work(w, 152)
+    KVD, HD = w.H_kv * w.d_h, w.H * w.d_h
+    end = w.cache_len - w.T
+    # every visible slot's K' and V once: a global layer sees the whole
+    # cache, a local one its window plus the new tokens
+    visible = end + w.T if w.window == 0 else min(w.window + w.T - 1, end + w.T)
+    kv = w.B * visible * KVD * 2 * 2
+    assert work["attention"] == kv + 2 * w.M * HD * 2 + w.B * (end + w.T) * 4
+    # the projections read Wq, Wkv and Wo once
+    weights = (HD * w.D + 2 * KVD * w.D + w.D * HD) * 2
+    assert weights < work["linear"] < 1.01 * weights
+    # Q|KV projection, QK prologue (which also writes the cache), O projection;
+    # attention: the split kernel and its merge, plus the span scan on local
+    # layers
+    assert launches["linear"] == 3
+    assert launches["attention"] == (3 if w.window > 0 else 2)
