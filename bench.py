@@ -6,9 +6,12 @@ One step is one pass of the whole hot path over one batch of synthetic input:
 the Q and KV projections with the QK-norm + RoPE + query-scale prologue in
 their epilogue, flash attention and the output projection (for the 6-layer stack, all six routed
 block-attention layers including their pre/post norms; for the full-block
-workload, the attention sandwich and the GeGLU feed-forward sandwich).  Inputs are resident
-in HBM when the timed region starts; L2 is flushed (a 256 MiB write) before
-every timed step, outside the step's CUDA events.  Prints one JSON line.
+workload, the attention sandwich and the GeGLU feed-forward sandwich).  The
+timed step is one call of the library's public entry point for the workload
+(gemma3_attn_forward for one layer) on inputs resident in HBM; L2 is flushed
+(a 256 MiB write) before every timed step, outside the step's CUDA events.
+A second timed pass runs the same kernels as separate stage calls, for the
+per-kernel times and the roofline.  Prints one JSON line.
 
 Under torchrun (N > 1) every rank runs its own replica of the workload on its
 own GPU (data-parallel replicas, no collective on the data path); rank 0
@@ -38,7 +41,7 @@ from transformer_attention_gb300 import metrics  # noqa: E402
 from transformer_attention_gb300 import workloads as WL  # noqa: E402
 
 METRIC = "attention-layer tokens/s; attn TFLOP/s as % of GB300 dense BF16 peak"
-DEFAULT_WORKLOAD = "1b_global"
+DEFAULT_WORKLOAD = "27b_global"
 MODEL_CODE = {"270M": 0, "1B": 1, "4B": 2, "12B": 3, "27B": 4}
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
@@ -368,41 +371,24 @@ def run_gpu(args, world, rank, local):
                              G3.GEMMA3_BF16, G3.GEMMA3_F32)
             done("read_out", e)
 
-    for _ in range(args.warmup):
-        flush.zero_()
-        step()
-    assert G3.gemma3_attn_check_status() == 0
+    # ---- the timed value: whole calls of the public entry point
+    api = ApiForward(w, layers, torch, G3, dev, stack)
+    y_dev = torch.empty(api.out_shape, dtype=api.out_dtype, device=dev)
+    x_in = tok if model else x
 
-    gpu_index = None
-    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
-    if vis:
-        gpu_index = vis.split(",")[local]
-    events = {}
-    step_ev = []
-    if world > 1:
-        import torch.distributed as dist
-        dist.barrier()
-    torch.cuda.synchronize()
-    with ClockSampler(gpu_index) as clocks:
-        wall0 = time.perf_counter()
-        for _ in range(args.steps):
-            flush.zero_()
-            s0 = torch.cuda.Event(enable_timing=True)
-            s1 = torch.cuda.Event(enable_timing=True)
-            s0.record(stream)
-            step(events)
-            s1.record(stream)
-            step_ev.append((s0, s1))
-        torch.cuda.synchronize()
-        wall = time.perf_counter() - wall0
-    if world > 1:
-        import torch.distributed as dist
-        dist.barrier()
+    def api_step(ev=None):
+        api(x_in, pos, pad, y_dev)
+
+    _, step_ms, wall, clk = _timed_clock_region(torch, args, world, local, dev, stream, api_step)
     st = G3.gemma3_attn_check_status()
     assert st == 0, st
-    step_ms = [a.elapsed_time(b) for a, b in step_ev]
     dev_seconds = sum(step_ms) / 1e3
     value, max_seconds = whole_job_value(tokens * args.steps, dev_seconds, world, dev)
+
+    # ---- the same kernels as stage calls, each bracketed by its own events
+    events, stage_ms, _, _ = _timed_clock_region(torch, args, world, local, dev, stream, step)
+    st = G3.gemma3_attn_check_status()
+    assert st == 0, st
     kern_ms = {k: sum(a.elapsed_time(b) for a, b in v) for k, v in events.items()}
     gemm_names = ((("proj_qkv",) if fused_qk else ("proj_q", "proj_kv")) + ("proj_o",)
                   + (("ffn_geglu", "ffn_down") if ffn else ()) + (("read_out",) if model else ()))
@@ -410,7 +396,7 @@ def run_gpu(args, world, rank, local):
     kern_ms["linear"] = sum(kern_ms.pop(k, 0.0) for k in gemm_names)
 
     # ---- end to end through the public C ABI with host buffers
-    e2e = run_e2e(args, w, layers, x_cpu, pads, torch, G3, dev, stack, world)
+    e2e = run_e2e(args, w, api, x_cpu, pads, torch, G3, dev, world)
 
     # ---- roofline of the dominant kernel (largest share of device time)
     peaks, peak_src = load_peaks()
@@ -433,8 +419,8 @@ def run_gpu(args, world, rank, local):
     roof.update({"kernel": dom, "achieved": achieved, "peak": peak, "frac": achieved / peak,
                  "traffic": traffic_for(dom, w.name)})
 
-    # ---- per-kernel breakdown (device time over the timed region)
-    total_ms = sum(step_ms)
+    # ---- per-kernel breakdown (device time over the stage pass)
+    total_ms = sum(stage_ms)
     breakdown = {}
     for k, ms in kern_ms.items():
         b = {"ms_per_step": ms / args.steps, "share": ms / total_ms}
@@ -476,7 +462,11 @@ def run_gpu(args, world, rank, local):
                                    / 1e12) / peaks["bf16_tflops"],
         "roofline": roof, "kernels": breakdown,
         "gpu_launches": int(sum(launches.values()) * args.steps),
-        "wall_s_timed_region": wall, "e2e": e2e, "clocks": clocks.summary(),
+        "timing": (f"value: each step one call of {api.api} on device-resident inputs; "
+                   "kernels and roofline: a second pass of the same kernels as stage calls, "
+                   "each bracketed by its own events"),
+        "stage_pass_ms_per_step": sum(stage_ms) / args.steps,
+        "wall_s_timed_region": wall, "e2e": e2e, "clocks": clk,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, budget_s=args.cpu_budget)
@@ -487,15 +477,80 @@ def run_gpu(args, world, rank, local):
         dist.destroy_process_group()
 
 
-def run_e2e(args, w, layers, x_cpu, pads, torch, G3, dev, stack, world):
-    """Same metric through the public C ABI (gemma3_attn_forward,
-    gemma3_block_attn_forward, gemma3_block_forward or gemma3_model_forward),
+class ApiForward:
+    """One whole-step call of the library's public entry point for workload w
+    (gemma3_attn_forward, gemma3_block_attn_forward per layer,
+    gemma3_block_forward per layer, or gemma3_model_forward), with its own
+    workspace.  Calling it with device tensors (x or token ids, positions,
+    pads, out) launches the step on the current stream."""
+
+    def __init__(self, w, layers, torch, G3, dev, stack):
+        self.w, self.layers, self.G3 = w, layers, G3
+        self.model = w.vocab > 0
+        self.stack = stack
+        D = w.D
+        self.dims = dims = (w.B, w.T, D, w.H, w.H_kv, w.d_h)
+        self.out_shape = (w.B, w.T, w.vocab if self.model else D)
+        self.out_dtype = torch.float32 if stack else torch.bfloat16
+        if self.model:
+            self.ws_bytes = G3.gemma3_model_workspace_size(dims, w.d_ff, w.vocab)
+            self.tables = {k: v.to(dev) for k, v in WL.model_tables(w).items()}
+            self.mlayers = [
+                {"Wq": L.p["Wq"], "Wkv": L.p["Wkv"], "Wo": L.p["Wo"],
+                 "gamma_q": L.p["gamma_q"], "gamma_k": L.p["gamma_k"],
+                 "gamma_pre_attn": L.p["gamma_pre"], "gamma_post_attn": L.p["gamma_post"],
+                 "gamma_pre_ffn": L.p["gamma_pre_ffn"], "gamma_post_ffn": L.p["gamma_post_ffn"],
+                 "W_gating": L.p["W_gating"], "W_down": L.p["W_down"]} for L in layers]
+        elif w.d_ff > 0:
+            self.ws_bytes = G3.gemma3_block_workspace_size(dims, w.d_ff)
+        elif stack:
+            self.ws_bytes = G3.gemma3_block_attn_workspace_size(*dims)
+        else:
+            self.ws_bytes = G3.gemma3_attn_workspace_size(*dims)
+        self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device=dev)
+        self.api = ("gemma3_model_forward" if self.model else
+                    "gemma3_block_forward" if w.d_ff > 0 else
+                    "gemma3_block_attn_forward" if stack else "gemma3_attn_forward")
+
+    def __call__(self, xk, pk, dk, yk):
+        w, G3, dims, ws, ws_bytes = self.w, self.G3, self.dims, self.ws, self.ws_bytes
+        if self.model:
+            t = self.tables
+            G3.gemma3_model_forward(dims, w.d_ff, w.vocab, w.num_layers, w.model_size, xk, pk, dk,
+                                    t["E"], self.mlayers, t["gamma_final"], yk, ws, ws_bytes)
+        elif w.d_ff > 0:
+            src, src_t = xk, G3.GEMMA3_BF16
+            for L in self.layers:
+                G3.gemma3_block_forward(
+                    dims, w.d_ff, src, src_t, yk, pk, dk, L.p["Wq"], L.p["Wkv"], L.p["Wo"],
+                    L.p["gamma_q"], L.p["gamma_k"], L.p["gamma_pre"], L.p["gamma_post"],
+                    L.p["gamma_pre_ffn"], L.p["gamma_post_ffn"], L.p["W_gating"],
+                    L.p["W_down"], L.attn_type, L.window, L.rope_base, L.rope_scale,
+                    w.query_scale, ws, ws_bytes)
+                src, src_t = yk, G3.GEMMA3_F32
+        elif self.stack:
+            src, src_t = xk, G3.GEMMA3_BF16
+            for L in self.layers:
+                G3.gemma3_block_attn_forward(
+                    dims, src, src_t, yk, pk, dk, L.p["Wq"], L.p["Wkv"], L.p["Wo"],
+                    L.p["gamma_q"], L.p["gamma_k"], L.p["gamma_pre"], L.p["gamma_post"],
+                    L.attn_type, L.window, L.rope_base, L.rope_scale, w.query_scale, ws,
+                    ws_bytes)
+                src, src_t = yk, G3.GEMMA3_F32
+        else:
+            L = self.layers[0]
+            G3.gemma3_attn_forward(dims, xk, pk, dk, L.p["Wq"], L.p["Wkv"], L.p["Wo"],
+                                   L.p["gamma_q"], L.p["gamma_k"], L.attn_type, L.window,
+                                   L.rope_base, L.rope_scale, w.query_scale, yk, ws, ws_bytes)
+
+
+def run_e2e(args, w, api, x_cpu, pads, torch, G3, dev, world):
+    """Same metric through the public C ABI (the ApiForward entry point),
     every step copying its inputs host -> device from pinned memory and its
     result device -> host, as a serving loop runs it: the copies go on their
     own streams into double-buffered device tensors, so step i+1's input and
     step i-1's output move while step i computes (event-ordered; the L2 flush
     stays on the compute stream, inside the timed region)."""
-    M, D = w.M, w.D
     model = w.vocab > 0
     NB = 2
     x_host = (WL.tokens(w) if model else x_cpu).pin_memory()
@@ -504,57 +559,13 @@ def run_e2e(args, w, layers, x_cpu, pads, torch, G3, dev, stack, world):
     x_d = [torch.empty_like(x_host, device=dev) for _ in range(NB)]
     pos_d = [torch.empty_like(pos_host, device=dev) for _ in range(NB)]
     pad_d = [torch.empty_like(pad_host, device=dev) for _ in range(NB)]
-    out_shape = (w.B, w.T, w.vocab if model else D)
-    out_dtype = torch.float32 if stack else torch.bfloat16
-    out_host = [torch.empty(out_shape, dtype=out_dtype, pin_memory=True) for _ in range(NB)]
-    y = [torch.empty(out_shape, dtype=out_dtype, device=dev) for _ in range(NB)]
-    dims = (w.B, w.T, D, w.H, w.H_kv, w.d_h)
-    if model:
-        ws_bytes = G3.gemma3_model_workspace_size(dims, w.d_ff, w.vocab)
-        tables = {k: v.to(dev) for k, v in WL.model_tables(w).items()}
-        mlayers = [{"Wq": L.p["Wq"], "Wkv": L.p["Wkv"], "Wo": L.p["Wo"],
-                    "gamma_q": L.p["gamma_q"], "gamma_k": L.p["gamma_k"],
-                    "gamma_pre_attn": L.p["gamma_pre"], "gamma_post_attn": L.p["gamma_post"],
-                    "gamma_pre_ffn": L.p["gamma_pre_ffn"], "gamma_post_ffn": L.p["gamma_post_ffn"],
-                    "W_gating": L.p["W_gating"], "W_down": L.p["W_down"]} for L in layers]
-    elif w.d_ff > 0:
-        ws_bytes = G3.gemma3_block_workspace_size(dims, w.d_ff)
-    elif stack:
-        ws_bytes = G3.gemma3_block_attn_workspace_size(*dims)
-    else:
-        ws_bytes = G3.gemma3_attn_workspace_size(*dims)
-    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    out_host = [torch.empty(api.out_shape, dtype=api.out_dtype, pin_memory=True)
+                for _ in range(NB)]
+    y = [torch.empty(api.out_shape, dtype=api.out_dtype, device=dev) for _ in range(NB)]
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
 
     def forward(k):
-        xk, pk, dk, yk = x_d[k], pos_d[k], pad_d[k], y[k]
-        if model:
-            G3.gemma3_model_forward(dims, w.d_ff, w.vocab, w.num_layers, w.model_size, xk, pk, dk,
-                                    tables["E"], mlayers, tables["gamma_final"], yk, ws, ws_bytes)
-        elif w.d_ff > 0:
-            src, src_t = xk, G3.GEMMA3_BF16
-            for L in layers:
-                G3.gemma3_block_forward(
-                    dims, w.d_ff, src, src_t, yk, pk, dk, L.p["Wq"], L.p["Wkv"], L.p["Wo"],
-                    L.p["gamma_q"], L.p["gamma_k"], L.p["gamma_pre"], L.p["gamma_post"],
-                    L.p["gamma_pre_ffn"], L.p["gamma_post_ffn"], L.p["W_gating"],
-                    L.p["W_down"], L.attn_type, L.window, L.rope_base, L.rope_scale,
-                    w.query_scale, ws, ws_bytes)
-                src, src_t = yk, G3.GEMMA3_F32
-        elif stack:
-            src, src_t = xk, G3.GEMMA3_BF16
-            for L in layers:
-                G3.gemma3_block_attn_forward(
-                    dims, src, src_t, yk, pk, dk, L.p["Wq"], L.p["Wkv"], L.p["Wo"],
-                    L.p["gamma_q"], L.p["gamma_k"], L.p["gamma_pre"], L.p["gamma_post"],
-                    L.attn_type, L.window, L.rope_base, L.rope_scale, w.query_scale, ws,
-                    ws_bytes)
-                src, src_t = yk, G3.GEMMA3_F32
-        else:
-            L = layers[0]
-            G3.gemma3_attn_forward(dims, xk, pk, dk, L.p["Wq"], L.p["Wkv"], L.p["Wo"],
-                                   L.p["gamma_q"], L.p["gamma_k"], L.attn_type, L.window,
-                                   L.rope_base, L.rope_scale, w.query_scale, yk, ws, ws_bytes)
+        api(x_d[k], pos_d[k], pad_d[k], y[k])
 
     s_c = torch.cuda.current_stream(dev)
     s_in = torch.cuda.Stream(dev)
@@ -604,9 +615,7 @@ def run_e2e(args, w, layers, x_cpu, pads, torch, G3, dev, stack, world):
     return {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h,
             "overlap": "copies on their own streams, double-buffered, event-ordered",
-            "api": ("gemma3_model_forward" if model else
-                    "gemma3_block_forward" if w.d_ff > 0 else
-                    "gemma3_block_attn_forward" if stack else "gemma3_attn_forward")}
+            "api": api.api}
 
 
 # ---------------------------------------------------------------------------- decode arm
@@ -983,12 +992,37 @@ def sample_tokens(w, budget_s: float):
     return n, t
 
 
+def host_cpu() -> dict:
+    """The host the CPU baseline ran on: logical CPUs and the CPU model."""
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().startswith("Model name:"):
+                model = line.split(":", 1)[1].strip()
+                break
+    except Exception:
+        pass
+    if not model:
+        try:
+            with open("/proc/cpuinfo") as f:
+                for line in f:
+                    if line.startswith("model name"):
+                        model = line.split(":", 1)[1].strip()
+                        break
+        except OSError:
+            pass
+    import platform
+    return {"nproc": os.cpu_count(), "cpu_model": model or platform.processor() or "unknown",
+            "machine": platform.machine()}
+
+
 def cpu_baseline(w, budget_s: float = 15.0):
     import torch
     if w.cache_len > 0:
         secs, runs = oracle_decode_sample(w, budget_s)
         return {"value": w.T * runs / secs, "unit": "tokens/s", "cores": torch.get_num_threads(),
-                "kind": "oracle",
+                "kind": "oracle", **host_cpu(),
                 "sample": f"fp64 oracle, decode steps of batch row 0 of {w.name} over its "
                           f"{w.cache_len}-slot cache: {runs} steps, {secs:.1f} s"}
     # Rows' prefixes (each row clipped to its valid length), one row after
@@ -1004,7 +1038,7 @@ def cpu_baseline(w, budget_s: float = 15.0):
         runs += 1
     rows = sorted({r % w.B for r in range(runs)})
     return {"value": tokens / total, "unit": "tokens/s", "cores": torch.get_num_threads(),
-            "kind": "oracle",
+            "kind": "oracle", **host_cpu(),
             "sample": f"fp64 oracle on causal prefixes of up to {n} tokens of batch rows "
                       f"{rows[0]}..{rows[-1]} of {w.name} ({w.num_layers} layer(s)); "
                       f"{runs} row runs, {tokens} tokens, {total:.1f} s"}
@@ -1034,7 +1068,7 @@ def run_reference(args, world, rank):
             "config": {"workload": w.name, "B": w.B, "T": w.T, "D": w.D, "H": w.H,
                        "H_kv": w.H_kv, "d_h": w.d_h, "attn": w.attn_type},
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": torch.get_num_threads(),
-                             "kind": "oracle",
+                             "kind": "oracle", **host_cpu(),
                              "sample": (f"one decode step of batch row 0 per step"
                                         if w.cache_len > 0 else
                                         f"first {n} tokens of batch row 0 per step")},

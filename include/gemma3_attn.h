@@ -433,15 +433,6 @@ int gemma3_last_device_status(void);
 /* Human-readable text of a status code. */
 const char* gemma3_strerror(int status);
 
-/* Clusters of two projection-GEMM CTAs that the current device holds at
- * once (0 when it holds none, or on a CUDA error).  gemma3_linear (and the
- * output projection inside the attention and block entry points) runs as
- * such pairs, which share each weight tile (one TMA multicast per half),
- * when a launch has at least one 128x256 tile per SM, an output at least 8
- * tiles wide (N >= 1793) and the pairs cover at least 90% of the SMs;
- * otherwise one CTA per SM.  Either way the results are the same bits. */
-int gemma3_gemm_pair_clusters(void);
-
 /* Runs one kernel whose single wait nothing ever completes, with the given
  * time limit in nanoseconds (1e6 .. 5e9), and returns what
  * gemma3_attn_check_status() reports (GEMMA3_ERR_TIMEOUT when the bounded wait

@@ -87,9 +87,10 @@ def oracle_forward(w: WL.Workload, inp: dict, rows=None):
 
 def sample_rows(w: WL.Workload, valid: int, n_random: int, seed: int, limit: int | None = None):
     """Query rows to check: boundary rows (first, window edges, tile edges,
-    last valid, first pad) and seeded random rows, all < limit (if given)."""
+    the middle, the last two valid, first pad) and seeded random rows, all
+    < limit (if given)."""
     hi = valid if limit is None else min(valid, limit)
-    rows = {0, 1, 63, 64, 127, 128, 129, hi - 1}
+    rows = {0, 1, 63, 64, 127, 128, 129, hi // 2 - 1, hi // 2, hi - 2, hi - 1}
     if w.window:
         rows |= {w.window - 1, w.window, w.window + 1, w.window + 127}
     if valid < w.T and (limit is None or valid < limit):

@@ -12,21 +12,29 @@ from transformer_attention_gb300 import workloads as WL
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
-def test_traffic_for_returns_the_committed_bytes_while_the_source_matches():
+def _traffic_table():
     with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
-        table = json.load(f)
-    checked = 0
+        return json.load(f)
+
+
+def test_traffic_for_returns_the_committed_bytes_while_the_source_matches(monkeypatch):
+    table = _traffic_table()
+    assert table
     for kernel, rows in table.items():
         for workload, e in rows.items():
-            src = os.path.join(ROOT, "transformer_attention_gb300", "csrc", e["source"])
-            if bench.source_hash(src) == e["source_sha256_16"]:
-                assert bench.traffic_for(kernel, workload) == e["dram_bytes_per_launch"]
-                checked += 1
-            else:
-                assert bench.traffic_for(kernel, workload) is None
-    assert checked > 0
+            monkeypatch.setattr(bench, "source_hash", lambda path, h=e["source_sha256_16"]: h)
+            assert bench.traffic_for(kernel, workload) == e["dram_bytes_per_launch"]
     assert bench.traffic_for("attention", "no_such_workload") is None
     assert bench.traffic_for("no_such_kernel", "1b_global") is None
+
+
+def test_traffic_for_follows_the_current_sources():
+    for kernel, rows in _traffic_table().items():
+        for workload, e in rows.items():
+            src = os.path.join(ROOT, "transformer_attention_gb300", "csrc", e["source"])
+            live = bench.source_hash(src) == e["source_sha256_16"]
+            assert bench.traffic_for(kernel, workload) == (e["dram_bytes_per_launch"] if live
+                                                           else None)
 
 
 def test_traffic_for_is_null_once_the_source_changed(monkeypatch):
@@ -53,3 +61,16 @@ def test_decode_work_bytes(name):
     # layers
     assert launches["linear"] == 3
     assert launches["attention"] == (3 if w.window > 0 else 2)
+
+
+def test_host_cpu_names_the_cores_and_the_model():
+    h = bench.host_cpu()
+    assert h["nproc"] == os.cpu_count() and h["nproc"] >= 1
+    assert isinstance(h["cpu_model"], str) and h["cpu_model"]
+
+
+def test_default_workload_is_the_largest_single_gpu_layer():
+    # the 27B-shaped global layer: the most attention work of the layer workloads
+    w = WL.WORKLOADS[bench.DEFAULT_WORKLOAD]
+    assert (w.B, w.T, w.D, w.H, w.H_kv, w.d_h) == (1, 131072, 5376, 32, 16, 128)
+    assert w.attn_type == "global" and w.rope_scale == 8.0

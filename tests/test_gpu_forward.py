@@ -5,8 +5,9 @@
   d_h in {128, 256}, checked in full;
 - the normalised and rotated Q/K of the forward's own stages (max abs 1e-2);
 - the three single-layer workloads at full size, in the launch configuration
-  the benchmark times, on sampled query rows the oracle computes one by one
-  (rows past the valid length must be exactly zero).
+  the benchmark times, on sampled query rows across the whole sequence that
+  the oracle computes one by one (rows past the valid length must be exactly
+  zero).
 """
 import pytest
 import torch
@@ -101,12 +102,14 @@ def test_normalised_rotated_qk_of_the_forward_stages():
 @pytest.mark.parametrize("name,limit,n_random", [
     ("1b_global", None, 24),
     ("4b_local", None, 24),
-    ("27b_global", 3072, 12),
+    pytest.param("27b_global", None, 12, marks=pytest.mark.slow),
 ])
 def test_full_size_sampled_rows(name, limit, n_random):
-    """Full-size workload on the GPU; sampled rows against the oracle.  For the
-    131072-token global layer the sampled rows lie in the first ``limit``
-    tokens (the oracle then needs only that key prefix)."""
+    """Full-size workload on the GPU; sampled rows against the oracle, spread
+    over the whole sequence (for the 131072-token global layer the oracle
+    projects every key once: rows up to t = 131071 see the full causal
+    prefix, so the long online-softmax reduction over ~1024 key tiles and the
+    longest work items are checked)."""
     w = WL.WORKLOADS[name]
     inp = Hh.make_inputs(w)
     dev = Hh.to_dev(inp)

@@ -61,6 +61,26 @@ def test_small_stack_full():
         assert torch.equal(got[b, valid:], x[b, valid:].float())
 
 
+@pytest.mark.slow
+def test_full_size_stack_shortest_row_in_full():
+    """Full 12B-shaped stack (B8 T16384, 6 layers) on the GPU; the oracle runs
+    the batch row with the fewest valid tokens through all six layers over its
+    whole valid length (the global layer l = 5 over every valid key), and the
+    row's pad tail must pass the residual through unchanged."""
+    w = WL.WORKLOADS["12b_stack"]
+    x = WL.x_full(w)
+    pads = WL.pad_lens(w)
+    got = _gpu_stack(w, x, pads)
+    valids = w.T - pads
+    b = int(torch.argmin(valids))
+    valid = int(valids[b])
+    # pad keys are blocked for every valid query, so the valid rows of the
+    # padded row equal the unpadded stack over its first `valid` tokens
+    ref = _oracle_stack(w, x[b:b + 1, :valid], torch.zeros(1, dtype=torch.int64), valid)[0]
+    Hh.assert_close(got[b, :valid].cpu(), ref, f"12b stack row b={b} (valid {valid}) in full")
+    assert torch.equal(got[b, valid:].cpu(), x[b, valid:].float())
+
+
 def test_full_size_stack_prefix():
     """Full 12B-shaped stack (B8 T16384, 6 layers) on the GPU; the oracle runs
     the first L tokens of two batch rows through all six layers (the stack is

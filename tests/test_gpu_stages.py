@@ -39,8 +39,8 @@ def _randn(shape, seed, std=1.0, dtype=torch.bfloat16):
                                    # M <= 16 (the few-row kernel: W on the MMA's 128-row
                                    # side, K split over a cluster): many rows, wide K
                                    (2, 20000, 1024), (4, 64, 16384), (2, 64, 40000),
-                                   # a wave or more of tiles, 8+ wide (CTA pairs sharing each
-                                   # weight tile): odd m-tile count, ragged M / N / K
+                                   # a wave or more of tiles, 8+ wide: odd m-tile count,
+                                   # ragged M / N / K
                                    (5170, 2200, 1024), (2000, 3000, 200),
                                    # a wave of tiles 5 wide (one CTA per tile)
                                    (5170, 1152, 1024)])
@@ -78,20 +78,12 @@ def test_linear_small_grid_many_tiles():
     assert rel_frob(C.cpu(), O.project(A, W)) <= 1e-5
 
 
-def _pairs_in_use():
-    import transformer_attention_gb300 as G3
-    sms = torch.cuda.get_device_properties(0).multi_processor_count
-    return 20 * G3.gemma3_gemm_pair_clusters() >= 9 * sms
-
-
 @pytest.mark.parametrize("max_ctas", [4, 1])
-def test_linear_pairs_small_grid_many_units(max_ctas):
-    # two CTA pairs walking 80 units (160 tiles): the shared stage ring and
-    # both CTAs' accumulator rings turn over many times; a cap of one CTA
-    # runs the same 160 tiles on a single CTA instead
+def test_linear_wide_output_small_grid(max_ctas):
+    # 160 tiles of a 10-tile-wide output walked by a persistent grid of 4
+    # CTAs, or by one: the stage ring and the accumulator ring turn over
+    # many times within each CTA
     import transformer_attention_gb300 as G3
-    if not _pairs_in_use():
-        pytest.skip("the device holds GEMM CTA pairs on fewer than 90% of its SMs")
     A = _randn((2048, 640), 6)
     W = _randn((2560, 640), 7, 640 ** -0.5)
     C = G3.linear(A.cuda(), W.cuda(), out_dtype=torch.float32, max_ctas=max_ctas)
@@ -99,19 +91,17 @@ def test_linear_pairs_small_grid_many_units(max_ctas):
     assert rel_frob(C.cpu(), O.project(A, W)) <= 1e-5
 
 
-def test_linear_pairs_match_single_ctas_bitwise():
-    # the same tile sums in the same order either way: a launch with pairs
-    # (160 tiles) and the same rows computed in a launch too small for pairs
-    # (the first 128 rows: 10 tiles) agree bit for bit on those rows
+def test_linear_tile_sums_independent_of_launch_size():
+    # every tile sums its k-steps in the same order whatever the grid: the
+    # first 128 rows of a 160-tile launch equal a 10-tile launch of those rows
+    # bit for bit
     import transformer_attention_gb300 as G3
-    if not _pairs_in_use():
-        pytest.skip("the device holds GEMM CTA pairs on fewer than 90% of its SMs")
     A = _randn((2048, 640), 8).cuda()
     W = _randn((2560, 640), 9, 640 ** -0.5).cuda()
-    C_pairs = G3.linear(A, W, out_dtype=torch.float32)
+    C_all = G3.linear(A, W, out_dtype=torch.float32)
     C_one = G3.linear(A[:128].contiguous(), W, out_dtype=torch.float32)
     assert G3.gemma3_attn_check_status() == 0
-    assert torch.equal(C_pairs[:128].cpu(), C_one.cpu())
+    assert torch.equal(C_all[:128].cpu(), C_one.cpu())
 
 
 # ---------------------------------------------------------------- QK-norm + RoPE prologue

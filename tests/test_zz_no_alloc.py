@@ -4,9 +4,10 @@ gemma3_attn_forward_noalloc serves callers that cannot give the library a
 workspace (code that may not call cudaMalloc, or whose device memory belongs
 to another framework's pool): it keeps the layer's intermediate rows in a
 fixed scratch array inside the library instead.  Its output must match the
-workspace entry point's on the same inputs, on two calls in a row (the second
-call finds the first call's leftovers in the shared scratch), and problems
-larger than the scratch must be refused before anything runs.
+fp64 oracle within the layer tolerances and the workspace entry point's
+output, on two calls in a row (the second call finds the first call's
+leftovers in the shared scratch), and problems larger than the scratch must
+be refused before anything runs.
 
 This file is collected last so that a run stopping at its first failure has
 already run every other test.
@@ -48,7 +49,9 @@ def test_noalloc_matches_workspace_entry_point_twice(lib):
     assert c.gemma3_attn_workspace_size(ctypes.byref(dims), ctypes.byref(need)) == 0
     assert need.value <= c.gemma3_attn_noalloc_max_scratch()
 
-    dev = Hh.to_dev(Hh.make_inputs(w))
+    inp = Hh.make_inputs(w)
+    dev = Hh.to_dev(inp)
+    oracle = Hh.oracle_forward(w, inp)
     stream = torch.cuda.current_stream().cuda_stream
     ref = torch.empty((w.B, w.T, w.D), dtype=torch.bfloat16, device="cuda")
     ws = torch.empty(need.value, dtype=torch.uint8, device="cuda")
@@ -66,6 +69,8 @@ def test_noalloc_matches_workspace_entry_point_twice(lib):
         got, exp = out.cpu(), ref.cpu()
         for b in range(w.B):
             valid = w.T - int(dev["pad_lens"][b])
+            Hh.assert_close(got[b, :valid], oracle[b, :valid],
+                            f"no-alloc call {call} b={b} vs oracle")
             Hh.assert_close(got[b, :valid], exp[b, :valid], f"no-alloc call {call} b={b}")
             assert bool((got[b, valid:] == 0).all())
 

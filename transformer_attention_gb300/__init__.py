@@ -13,7 +13,7 @@ from ._lib import (  # noqa: F401  (re-exported C-ABI names)
     gemma3_cached_attention_workspace_size, gemma3_kv_cache_write,
     gemma3_block_attn_forward, gemma3_block_attn_workspace_size, gemma3_block_ffn_forward,
     gemma3_block_ffn_workspace_size, gemma3_block_forward, gemma3_block_workspace_size,
-    gemma3_cast_bf16_f16, gemma3_geglu, gemma3_gemm_pair_clusters,
+    gemma3_cast_bf16_f16, gemma3_geglu,
     gemma3_flash_attention,
     gemma3_last_device_status, gemma3_layer_attn_type, gemma3_layer_config, gemma3_linear,
     gemma3_linear_qk_norm_rope, gemma3_qkv_proj_norm_rope, gemma3_embed, gemma3_model_forward, gemma3_model_workspace_size,

@@ -117,7 +117,6 @@ SIGNATURES = {
     "gemma3_postnorm_residual": (c_int, [c_void_p, c_void_p, c_int, c_void_p, c_void_p, c_int,
                                          c_int, c_void_p]),
     "gemma3_attn_check_status": (c_int, [c_void_p]),
-    "gemma3_gemm_pair_clusters": (c_int, []),
     "gemma3_last_device_status": (c_int, []),
     "gemma3_strerror": (ctypes.c_char_p, [c_int]),
     "gemma3_selftest_wait_timeout": (c_int, [ctypes.c_longlong, c_void_p]),
@@ -424,11 +423,6 @@ def gemma3_attn_check_status(stream=None) -> int:
 
 def gemma3_last_device_status() -> int:
     return lib().gemma3_last_device_status()
-
-
-def gemma3_gemm_pair_clusters() -> int:
-    """Two-CTA projection-GEMM clusters the device holds at once."""
-    return lib().gemma3_gemm_pair_clusters()
 
 
 def gemma3_selftest_wait_timeout(timeout_ns: int, stream=None) -> int:

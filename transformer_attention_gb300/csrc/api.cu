@@ -4,6 +4,7 @@
 #include <cmath>
 #include <cstdio>
 #include <cstring>
+#include <map>
 #include <mutex>
 
 #include <cudaTypedefs.h>
@@ -243,6 +244,29 @@ int num_sms() {
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
   return n > 0 ? n : 1;
+}
+
+namespace {
+std::mutex g_prepare_mu;
+std::map<std::pair<const void*, int>, int> g_prepared;   // (kernel, device) -> registers
+}  // namespace
+
+cudaError_t prepare_kernel(const void* kern, int smem_bytes, int* regs) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(g_prepare_mu);
+  auto it = g_prepared.find({kern, dev});
+  if (it == g_prepared.end()) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+    if (e != cudaSuccess) return e;
+    cudaFuncAttributes fa;
+    e = cudaFuncGetAttributes(&fa, kern);
+    if (e != cudaSuccess) return e;
+    it = g_prepared.emplace(std::make_pair(kern, dev), fa.numRegs).first;
+  }
+  if (regs != nullptr) *regs = it->second;
+  return cudaSuccess;
 }
 
 }  // namespace g3
@@ -896,11 +920,6 @@ int gemma3_attn_check_status(void* stream) {
 }
 
 int gemma3_last_device_status(void) { return t_last_device_status; }
-
-int gemma3_gemm_pair_clusters(void) {
-  if (check_device() != GEMMA3_OK) return 0;
-  return g3::gemm_pair_clusters();
-}
 
 const char* gemma3_strerror(int status) {
   switch (status) {

@@ -576,12 +576,7 @@ cudaError_t launch_cfg(const void* Q, const void* K, const void* V, long ldkv, v
       !encode_tiled(&tv, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, V, kdims, kstr, vbox))
     return cudaErrorInvalidValue;
   auto kern = attn_fwd_kernel<DH, G>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  if (cudaError_t e = prepare_kernel(reinterpret_cast<const void*>(kern), C::SMEM)) return e;
   const int num_q_tiles = (T + C::TQ - 1) / C::TQ;
   const long items = static_cast<long>(num_q_tiles) * B * H_kv;
   if (items > 0x7fffffffL) return cudaErrorInvalidValue;

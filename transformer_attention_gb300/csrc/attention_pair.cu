@@ -522,17 +522,9 @@ cudaError_t launch_pair_cfg(const void* Q, const void* K, const void* V, long ld
       !encode_tiled(&tv, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, V, kdims, kstr, kbox))
     return cudaErrorInvalidValue;
   auto kern = attn_pair_kernel<G>;
-  static bool attr_set = false;
-  static int launch_regs = 0;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
-    if (e != cudaSuccess) return e;
-    cudaFuncAttributes fa;
-    e = cudaFuncGetAttributes(&fa, kern);
-    if (e != cudaSuccess) return e;
-    launch_regs = fa.numRegs;
-    attr_set = true;
-  }
+  int launch_regs = 0;
+  if (cudaError_t e = prepare_kernel(reinterpret_cast<const void*>(kern), SMEM, &launch_regs))
+    return e;
   // The softmax warpgroups' register increase waits for the registers the
   // other warpgroup gives up: launch only when the split fits the CTA's
   // allocation.

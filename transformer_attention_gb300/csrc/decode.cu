@@ -593,12 +593,7 @@ cudaError_t launch_decode_cfg(const CUtensorMap& tk, const CUtensorMap& tv, cons
                               dim3 grid, cudaStream_t stream) {
   using C = DecCfg<DH, RB>;
   auto kern = decode_attn_kernel<DH, RB>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  if (cudaError_t e = prepare_kernel(reinterpret_cast<const void*>(kern), C::SMEM)) return e;
   return launch_pdl(kern, grid, dim3(kDecThreads), C::SMEM, stream, tk, tv, p);
 }
 

@@ -22,10 +22,6 @@
 // Tiles are visited in groups of 8 M-tiles (N-tiles varying slowest within
 // a group), so the tiles in flight share A rows and W rows through L2 even
 // when W is larger than L2.
-// Wide plain outputs run in clusters of two CTAs on neighbouring M tiles: each
-// CTA loads its A tile and one 128-row half of the shared W tile with a TMA
-// multicast to both, so each SM pulls 32 KB instead of 48 KB per k-step from
-// L2; each MMA commit releases the stage in both CTAs.
 // Epilogue modes: plain conversion; GeGLU (the feed-forward gating
 // projection); and the attention prologue ("QK-Norm", How it works; "Gemma 3
 // Attention Block", How it works: QK-norm, then RoPE, then scale) applied to
@@ -120,15 +116,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                 "the QK-norm epilogue writes fp16 head vectors of 128 or 256");
   constexpr int BN_OUT = GEGLU ? BN / 2 : BN;   // output columns per tile
   constexpr int CW = 128 / static_cast<int>(sizeof(OutT));   // output columns per 128 B chunk
-  // Launched in clusters of two, the CTAs of a pair share every B tile: each
-  // loads its own 128-row A tile and one half of the B tile, delivered to
-  // both (multicast), and a stage is refilled only once both CTAs' MMAs have
-  // read it.  The pair takes m tiles 2u and 2u + 1 of unit u.
-  const uint32_t ncta = cluster_nctarank();
-  const uint32_t crank = ncta > 1 ? cluster_ctarank() : 0;
-  // A kernel launched after an earlier one gave up does no work (a pair runs
-  // to its end together, so clusters take no early exit).
-  if (ncta == 1 && *reinterpret_cast<volatile int*>(status) != 0) return;
+  // A kernel launched after an earlier one gave up does no work.
+  if (*reinterpret_cast<volatile int*>(status) != 0) return;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -139,20 +128,15 @@ __global__ void __launch_bounds__(THREADS, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int m_tiles = (M + BM - 1) / BM, n_tiles = (N + BN_OUT - 1) / BN_OUT;
-  const int m_units = (m_tiles + static_cast<int>(ncta) - 1) / static_cast<int>(ncta);
-  const int num_units = m_units * n_tiles;
-  const int unit0 = blockIdx.x / ncta, unit_step = gridDim.x / ncta;
+  const int num_units = m_tiles * n_tiles;
+  const int unit0 = blockIdx.x, unit_step = gridDim.x;
   const int num_kb = (K + BK - 1) / BK;
-  auto unit_coords = [&](int u, int& mt, int& nt) {
-    int mu;
-    tile_coords(u, m_units, n_tiles, GROUP_M / static_cast<int>(ncta), mu, nt);
-    mt = mu * static_cast<int>(ncta) + static_cast<int>(crank);
-  };
+  auto unit_coords = [&](int u, int& mt, int& nt) { tile_coords(u, m_tiles, n_tiles, GROUP_M, mt, nt); };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(smem_u32(&full_bar[s]), 1);
-      mbar_init(smem_u32(&empty_bar[s]), ncta);   // one commit from each CTA's MMA
+      mbar_init(smem_u32(&empty_bar[s]), 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(&accf_bar[b]), 1);
@@ -174,8 +158,6 @@ __global__ void __launch_bounds__(THREADS, 1)
     tmem_relinquish();
   }
   __syncthreads();
-  // The pair's barriers are initialised before either CTA writes to the other.
-  if (ncta > 1) cluster_sync();
   tc_fence_after();
   const uint32_t tbase = tmem_base_sh;
 
@@ -197,13 +179,9 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
           const uint32_t fb = smem_u32(&full_bar[stage]);
           uint8_t* sa = smem + stage * STAGE_BYTES;
-          mbar_arrive_expect_tx(fb, STAGE_BYTES);   // in a pair: the partner's half of B too
+          mbar_arrive_expect_tx(fb, STAGE_BYTES);
           tma_load_2d(smem_u32(sa), &tmA, fb, kb * BK, m0);
-          if (EPI == kEpiPlain && ncta > 1) {
-            // this CTA's 128 rows of the B tile, to the same offset in both CTAs
-            tma_load_2d_mc(smem_u32(sa + A_BYTES + crank * (B_BYTES / 2)), &tmB, fb, kb * BK,
-                           n0 + static_cast<int>(crank) * (BN / 2), static_cast<uint16_t>(0x3));
-          } else if constexpr (GEGLU) {
+          if constexpr (GEGLU) {
             // gate rows n0.. into the first 128 B-tile rows, up rows N + n0.. after them
             tma_load_2d(smem_u32(sa + A_BYTES), &tmB, fb, kb * BK, n0);
             tma_load_2d(smem_u32(sa + A_BYTES + B_BYTES / 2), &tmB, fb, kb * BK, N + n0);
@@ -250,10 +228,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           mma_ss_lead(lead, d_tmem, sdesc_sw128(a_addr + k * 32, 16, 1024),
                       sdesc_sw128(b_addr + k * 32, 16, 1024), idesc, (kb | k) != 0);
         }
-        if (ncta > 1)   // the stage is free once both CTAs' MMAs have read it
-          mma_commit_mc_lead(lead, smem_u32(&empty_bar[stage]), static_cast<uint16_t>(0x3));
-        else
-          mma_commit_lead(lead, smem_u32(&empty_bar[stage]));
+        mma_commit_lead(lead, smem_u32(&empty_bar[stage]));
         if (++stage == STAGES) { stage = 0; phase ^= 1; }
       }
       if (!ok) break;
@@ -494,66 +469,21 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (lane == 0) bulk_wait_group_all();
   }
   __syncthreads();
-  // Neither CTA of a pair leaves while the other may still write to it.
-  if (ncta > 1) cluster_sync();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tbase, TMEM_COLS);
   }
 }
 
-// Clusters of two GEMM CTAs that the GPU holds at once (every instantiation
-// has the same block size and shared memory, so one query serves all).
-int gemm_max_pairs() {
-  static int pairs = -1;
-  if (pairs < 0) {
-    auto kern = gemm_tn_kernel<1, float, kEpiPlain, 0>;
-    int c = 0;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) ==
-        cudaSuccess) {
-      cudaLaunchConfig_t cfg = {};
-      cfg.gridDim = dim3(2);
-      cfg.blockDim = dim3(THREADS);
-      cfg.dynamicSmemBytes = SMEM_BYTES;
-      cudaLaunchAttribute attr[1];
-      attr[0].id = cudaLaunchAttributeClusterDimension;
-      attr[0].val.clusterDim.x = 2;
-      attr[0].val.clusterDim.y = 1;
-      attr[0].val.clusterDim.z = 1;
-      cfg.attrs = attr;
-      cfg.numAttrs = 1;
-      if (cudaOccupancyMaxActiveClusters(&c, kern, &cfg) != cudaSuccess) c = 0;
-    }
-    (void)cudaGetLastError();
-    pairs = c;
-  }
-  return pairs;
-}
-
 inline int gemm_tiles(int M, int N, int bn_out) {
   return ((M + BM - 1) / BM) * ((N + bn_out - 1) / bn_out);
 }
 
-// Pairs halve the B-tile traffic from L2 into each SM but make the two CTAs
-// advance together.  Measured on GB300 they pay for plain-epilogue outputs
-// of 8 or more 256-column tiles (N >= 2048: the O and down projections of
-// the 4B-27B shapes, 2-3% faster), not for narrower ones (N = 1152, 1536:
-// 1-7% slower), the GeGLU GEMM (flat) or the fused Q/KV projection (+3% to
-// -4% by shape), so they are used for plain launches with at least one tile
-// per SM and 8 or more n tiles, when the GPU holds a pair on at least 90%
-// of its SMs.
-bool gemm_use_pairs(int M, int N) {
-  const int sms = num_sms();
-  return (N + BN - 1) / BN >= 8 && gemm_tiles(M, N, BN) >= sms && 20 * gemm_max_pairs() >= 9 * sms;
-}
-
 // C (and, for a split launch, the second segment's C2 with ldc2 and the
-// second weight map tb2; epi.n1 > 0) as 32-row x 128-byte TMA tiles.  With
-// `pairs` (taken for the plain epilogue only) the weight map holds boxes of
-// BN / 2 rows and the grid runs in clusters of two.
+// second weight map tb2; epi.n1 > 0) as 32-row x 128-byte TMA tiles.
 template <int AB_BF16, typename OutT, int EPI = kEpiPlain, int DH = 0>
 cudaError_t launch_typed(const CUtensorMap& ta, const CUtensorMap& tb, void* C, long ldc, int M,
-                         int N, int K, cudaStream_t stream, int* status, int max_ctas, bool pairs,
+                         int N, int K, cudaStream_t stream, int* status, int max_ctas,
                          const QkEpi& epi = QkEpi{}, const CUtensorMap* tb2 = nullptr,
                          void* C2 = nullptr, long ldc2 = 0) {
   constexpr bool GEGLU = EPI == kEpiGeglu;
@@ -576,22 +506,9 @@ cudaError_t launch_typed(const CUtensorMap& ta, const CUtensorMap& tb, void* C, 
     if (tb2 == nullptr || C2 == nullptr || !encode_tiled(&tc2, cdt, 2, C2, cdims2, cstr2, cbox))
       return cudaErrorInvalidValue;
   }
-  static bool attr_set = false;  // benign race: setting the same attribute twice is harmless
-  if (!attr_set) {
-    cudaError_t e =
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  if (cudaError_t e = prepare_kernel(reinterpret_cast<const void*>(kern), SMEM_BYTES))
+    return e;
   const int bn_out = GEGLU ? BN / 2 : BN;
-  if (pairs && EPI == kEpiPlain) {
-    const int units = (((M + BM - 1) / BM + 1) / 2) * ((N + bn_out - 1) / bn_out);
-    int ncl = gemm_max_pairs();
-    if (max_ctas > 0 && max_ctas / 2 < ncl) ncl = max_ctas / 2;   // max_ctas >= 2 here
-    if (units < ncl) ncl = units;
-    return launch_pdl_cluster(kern, dim3(2 * ncl), dim3(THREADS), SMEM_BYTES, 2, stream, ta, tb,
-                              tc, tb2 != nullptr ? *tb2 : tb, tc2, M, N, K, status, epi);
-  }
   const int tiles = gemm_tiles(M, N, bn_out);
   int grid = num_sms();
   if (max_ctas > 0 && max_ctas < grid) grid = max_ctas;
@@ -616,8 +533,6 @@ bool encode_ab(CUtensorMap& ta, CUtensorMap& tb, const void* A, long lda, const 
 
 }  // namespace
 
-int gemm_pair_clusters() { return gemm_max_pairs(); }
-
 cudaError_t launch_linear(const void* A, long lda, const void* W, long ldw, void* C, long ldc,
                           int M, int N, int K, int in_dtype, int out_dtype, cudaStream_t stream,
                           int* status, int max_ctas) {
@@ -626,20 +541,17 @@ cudaError_t launch_linear(const void* A, long lda, const void* W, long ldw, void
   if (M <= kSkinnyMaxRows)
     return launch_linear_skinny(A, lda, W, ldw, C, ldc, M, N, K, in_dtype, out_dtype, stream,
                                 status);
-  // (a cap of one CTA rules out a pair)
-  const bool pairs = gemm_use_pairs(M, N) && max_ctas != 1;
   CUtensorMap ta, tb;
-  if (!encode_ab(ta, tb, A, lda, W, ldw, M, N, K, in_dtype, pairs ? BN / 2 : BN))
-    return cudaErrorInvalidValue;
+  if (!encode_ab(ta, tb, A, lda, W, ldw, M, N, K, in_dtype, BN)) return cudaErrorInvalidValue;
 #define G3_GEMM_OUT(AB)                                                                        \
   switch (out_dtype) {                                                                         \
     case kF32:                                                                                 \
-      return launch_typed<AB, float>(ta, tb, C, ldc, M, N, K, stream, status, max_ctas, pairs); \
+      return launch_typed<AB, float>(ta, tb, C, ldc, M, N, K, stream, status, max_ctas);      \
     case kF16:                                                                                 \
-      return launch_typed<AB, __half>(ta, tb, C, ldc, M, N, K, stream, status, max_ctas, pairs); \
+      return launch_typed<AB, __half>(ta, tb, C, ldc, M, N, K, stream, status, max_ctas);     \
     case kBF16:                                                                                \
-      return launch_typed<AB, __nv_bfloat16>(ta, tb, C, ldc, M, N, K, stream, status, max_ctas, \
-                                             pairs);                                           \
+      return launch_typed<AB, __nv_bfloat16>(ta, tb, C, ldc, M, N, K, stream, status,       \
+                                             max_ctas);                                        \
     default: return cudaErrorInvalidValue;                                                     \
   }
   if (in_dtype == kBF16) {
@@ -657,8 +569,8 @@ cudaError_t launch_geglu(const void* A, long lda, const void* Wgu, long ldw, voi
   if (!encode_ab(ta, tb, A, lda, Wgu, ldw, M, 2 * D_ff, K, in_dtype, BN / 2))
     return cudaErrorInvalidValue;
   if (in_dtype == kBF16)
-    return launch_typed<1, __half, kEpiGeglu>(ta, tb, Z, ldz, M, D_ff, K, stream, status, 0, false);
-  return launch_typed<0, __half, kEpiGeglu>(ta, tb, Z, ldz, M, D_ff, K, stream, status, 0, false);
+    return launch_typed<1, __half, kEpiGeglu>(ta, tb, Z, ldz, M, D_ff, K, stream, status, 0);
+  return launch_typed<0, __half, kEpiGeglu>(ta, tb, Z, ldz, M, D_ff, K, stream, status, 0);
 }
 
 bool linear_qknorm_fusable(int M, int N, int n_norm, int d_h) {
@@ -692,7 +604,7 @@ cudaError_t launch_qkv_qknorm(const void* A, long lda, const void* Wq, const voi
   const int N = HD + 2 * KVD;
 #define G3_QKV(AB, DH_)                                                                        \
   return launch_typed<AB, __half, kEpiQkNorm, DH_>(ta, tb, Qout, ldq, M, N, K, stream, status, 0, \
-                                                   false, epi, &tb2, KVout, ldkv);
+                                                   epi, &tb2, KVout, ldkv);
   if (in_dtype == kBF16) {
     if (d_h == 256) G3_QKV(1, 256)
     G3_QKV(1, 128)
@@ -720,7 +632,7 @@ cudaError_t launch_linear_qknorm(const void* A, long lda, const void* W, long ld
   epi.scale = scale;
 #define G3_QKN(AB, DH_)                                                                      \
   return launch_typed<AB, __half, kEpiQkNorm, DH_>(ta, tb, C, ldc, M, N, K, stream, status, 0, \
-                                                   false, epi);
+                                                   epi);
   if (in_dtype == kBF16) {
     if (d_h == 256) G3_QKN(1, 256)
     G3_QKN(1, 128)

@@ -18,8 +18,10 @@ bool encode_tiled(CUtensorMap* map, CUtensorMapDataType dt, int rank, const void
 
 int num_sms();
 
-// Clusters of two projection-GEMM CTAs the current device holds at once.
-int gemm_pair_clusters();
+// Raises `kern`'s dynamic shared-memory limit to `smem_bytes` on the current
+// device, once per (kernel, device) and safe to call from several host
+// threads; `regs`, if given, receives the kernel's registers per thread.
+cudaError_t prepare_kernel(const void* kern, int smem_bytes, int* regs = nullptr);
 
 // Launch `kern` on `stream` with programmatic dependent launch allowed: the
 // grid may start while the previous kernel on the stream is finishing, and

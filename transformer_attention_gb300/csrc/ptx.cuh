@@ -68,6 +68,11 @@ __device__ __forceinline__ float ld_shared_cluster_f32(uint32_t addr) {
   asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
   return v;
 }
+__device__ __forceinline__ uint32_t ld_shared_cluster_u32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
 
 __device__ __forceinline__ uint64_t globaltimer() {
   uint64_t t;
@@ -149,18 +154,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, uint
       "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar), "r"(c0), "r"(c1)
-      : "memory");
-}
-
-// The same box delivered to every CTA of `cta_mask` in this cluster, at the
-// same shared-memory offset, each completing bytes on the mbarrier at the
-// same offset in its own shared memory.
-__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const void* tmap, uint32_t bar,
-                                               int c0, int c1, uint16_t cta_mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
-      ".multicast::cluster [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar), "r"(c0), "r"(c1), "h"(cta_mask)
       : "memory");
 }
 
@@ -387,18 +380,6 @@ __device__ __forceinline__ void mma_commit_lead(uint32_t lead, uint32_t bar) {
       "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(
           bar),
       "r"(lead)
-      : "memory");
-}
-
-// The same arrival on the mbarrier at offset `bar` of every CTA in
-// `cta_mask` of this cluster.
-__device__ __forceinline__ void mma_commit_mc_lead(uint32_t lead, uint32_t bar, uint16_t cta_mask) {
-  asm volatile(
-      "{\n\t.reg .pred e;\n\t"
-      "setp.ne.b32 e, %1, 0;\n\t"
-      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%0], %2;\n\t}" ::"r"(bar),
-      "r"(lead), "h"(cta_mask)
       : "memory");
 }
 

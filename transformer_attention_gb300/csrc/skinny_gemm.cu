@@ -72,6 +72,7 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
   __shared__ __align__(8) uint64_t full[STAGES], empty[STAGES], done;
   __shared__ uint32_t tmem_sh;
   __shared__ int abort_flag;
+  __shared__ int partial_ok;   // 0 once a warp of this CTA found its MMAs unfinished
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int tile = blockIdx.x / splits, split = blockIdx.x % splits;
   const int row0 = tile * TN;
@@ -89,6 +90,7 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
     }
     mbar_init(smem_u32(&done), 1);
     abort_flag = 0;
+    partial_ok = 1;
     fence_barrier_init();
     tma_prefetch_desc(wmap);
     tma_prefetch_desc(&tmA);
@@ -159,8 +161,8 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
   // ---------------- epilogue: all four warps, row r of the tile per thread
   pdl_wait();   // C is written only after the previous kernel
   pdl_trigger();
-  const bool got = __all_sync(0xffffffffu, mbar_wait(smem_u32(&done), 0, &abort_flag, status,
-                                                     kSiteSkDone));
+  bool got = __all_sync(0xffffffffu, mbar_wait(smem_u32(&done), 0, &abort_flag, status,
+                                               kSiteSkDone));
   tc_fence_after();
   uint32_t v[32];   // columns 0 .. MA - 1 hold this row's products with the rows of A
   tmem_ld32(tbase + (static_cast<uint32_t>(warp * 32) << 16), v);
@@ -170,8 +172,14 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
 #pragma unroll
     for (int m = 0; m < MA; ++m)
       if (m < M) red[r * MA + m] = __uint_as_float(v[m]);
-    cluster_sync();   // every CTA's partials are in its shared memory
+    if (!got && lane == 0) partial_ok = 0;
+    cluster_sync();   // every CTA's partials and flag are in its shared memory
     if (split == 0) {
+      // a peer whose MMAs did not all complete holds a stale partial: no store
+      got = partial_ok != 0;
+      for (int q = 1; q < splits; ++q)
+        got = got && ld_shared_cluster_u32(mapa_shared(smem_u32(&partial_ok),
+                                                       static_cast<uint32_t>(q))) != 0;
       for (int q = 1; q < splits; ++q) {
         const uint32_t peer = mapa_shared(smem_u32(red + r * MA), static_cast<uint32_t>(q));
 #pragma unroll
@@ -218,13 +226,8 @@ cudaError_t launch_tc(const CUtensorMap& tw, const CUtensorMap& tw2, const CUten
                       void* C, long ldc, void* C2, long ldc2, int n1, int M, int N, int K,
                       cudaStream_t stream, int* status) {
   auto kern = skinny_tc_kernel<AB, OutT>;
-  static bool attr_set = false;  // benign race: setting the same attribute twice is harmless
-  if (!attr_set) {
-    cudaError_t e =
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  if (cudaError_t e = prepare_kernel(reinterpret_cast<const void*>(kern), SMEM_BYTES))
+    return e;
   // Split each tile's k-blocks over enough CTAs to fill every SM.
   const int tiles = (N + TN - 1) / TN;
   const int nkb = (K + KB - 1) / KB;
