@@ -112,12 +112,18 @@ struct SchedRing {
   }
 };
 
-// (b, kv head) pairs per ordering group: as many as keep their K/V (T x d_h
-// x 2 tensors x 2 B) within ~48 MB of L2; local layers touch only a window
-// of K/V per item and use a single group (pure heavy-first order).
-inline int l2_group_size(int B, int H_kv, int T, int d_h, int window) {
+// (b, kv head) pairs per ordering group.  Global layers: as many as keep
+// their K/V (T x d_h x 2 tensors x 2 B) within ~48 MB of L2.  Local layers
+// read only a window of K/V per item, shared by the ~W / span consecutive
+// query items of the same pair: the group is small enough that the `ctas`
+// items in flight hold that many consecutive items of each of its pairs, so
+// each K/V tile is read from DRAM about once.  (One group over all 64 pairs
+// of the 12B shape spread the items in flight over every pair, and each K/V
+// tile was evicted between its reuses: 3.4x the algorithmic DRAM reads.)
+inline int l2_group_size(int B, int H_kv, int T, int d_h, int window, int span, int ctas) {
   const double kv_bytes = static_cast<double>(T) * d_h * 2.0 * 2.0;
-  int gsz = window > 0 ? B * H_kv : static_cast<int>(48.0 * 1024 * 1024 / kv_bytes);
+  int gsz = window > 0 ? ctas / ((window + span - 1) / span + 1)
+                       : static_cast<int>(48.0 * 1024 * 1024 / kv_bytes);
   return gsz < 1 ? 1 : (gsz > B * H_kv ? B * H_kv : gsz);
 }
 

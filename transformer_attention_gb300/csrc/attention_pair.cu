@@ -533,7 +533,7 @@ cudaError_t launch_pair_cfg(const void* Q, const void* K, const void* V, long ld
   const long items = static_cast<long>(num_pairs) * B * H_kv;
   if (items > 0x7fffffffL) return cudaErrorInvalidValue;
   const int grid = static_cast<int>(items < num_sms() ? items : num_sms());
-  const int gsz = attn::l2_group_size(B, H_kv, T, DH, window);
+  const int gsz = attn::l2_group_size(B, H_kv, T, DH, window, 2 * TQ, grid);
   if (sched != nullptr && !sched_zeroed &&
       cudaMemsetAsync(sched, 0, sizeof(unsigned int), stream) != cudaSuccess)
     return cudaErrorUnknown;
