@@ -679,9 +679,9 @@ def decode_work(w, sms: int) -> tuple:
     units = w.B * H_kv * ((w.T + rb // G - 1) // (rb // G))
     est = end + w.T if w.window == 0 else min(end + w.T, w.window + w.T)
     nsplit = max(1, min((2 * sms) // units, (est + 63) // 64, max(1, 2048 // units), 256))
-    # (the QK prologue also writes the new K'/V rows and positions to the cache)
-    launches = {"linear": 3,
-                "attention": 1 + (1 if w.window > 0 else 0) + (1 if nsplit > 1 else 0)}
+    # (the QK prologue also writes the new K'/V rows and positions to the
+    # cache and, in the same launch, scans a local layer's cache span)
+    launches = {"linear": 3, "attention": 1 + (1 if nsplit > 1 else 0)}
     return work, launches
 
 

@@ -56,11 +56,11 @@ def test_decode_work_bytes(name):
     # the projections read Wq, Wkv and Wo once
     weights = (HD * w.D + 2 * KVD * w.D + w.D * HD) * 2
     assert weights < work["linear"] < 1.01 * weights
-    # Q|KV projection, QK prologue (which also writes the cache), O projection;
-    # attention: the split kernel and its merge, plus the span scan on local
-    # layers
+    # Q|KV projection, QK prologue (which also writes the cache and scans a
+    # local layer's cache span), O projection; attention: the split kernel
+    # and its merge
     assert launches["linear"] == 3
-    assert launches["attention"] == (3 if w.window > 0 else 2)
+    assert launches["attention"] == 2
 
 
 def test_host_cpu_names_the_cores_and_the_model():

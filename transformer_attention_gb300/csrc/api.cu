@@ -671,6 +671,14 @@ int gemma3_attn_forward_cached(const gemma3_attn_dims* dims, int S, int end_inde
   cr.T = d->T;
   cr.S = S;
   cr.end = end_index;
+  const bool flash = end_index == 0 && attn_type == GEMMA3_GLOBAL && d->T >= kFlashPrefillMinT;
+  if (!flash && attn_type == GEMMA3_LOCAL_SLIDING) {
+    // A prologue kernel that writes the cache also scans the local layer's
+    // cache span for the cache attention, in the same launch.
+    cr.span_part = cached_attention_layout(aws, d->B, d->T, S, d->H, d->H_kv, d->d_h).span_part;
+    cr.window = window;
+    cr.nchunk = cached_span_chunks(d->T, end_index);
+  }
   bool cached = false;
   if (project_qk(x, d->D, kBF16, Wq, Wkv, qbuf, kvbuf, gamma_q, gamma_k, segment_pos, M, d->D,
                  d->H, d->H_kv, d->d_h, rope_base, rope_scale, query_scale, s, st, &cr,
@@ -680,14 +688,15 @@ int gemma3_attn_forward_cached(const gemma3_attn_dims* dims, int S, int end_inde
                               end_index, KVD, K_cache, V_cache, pos_cache, s) != cudaSuccess))
     return GEMMA3_ERR_CUDA;
   cudaError_t e;
-  if (end_index == 0 && attn_type == GEMMA3_GLOBAL && d->T >= kFlashPrefillMinT)
+  if (flash)
     e = launch_flash_attention(qbuf, kvbuf, kvbuf + KVD * 2, 2 * KVD, qbuf, kBF16, pad_lens, d->B,
                                d->T, d->H, d->H_kv, d->d_h, 0, aws + w.attn - kAttnSchedBytes, s,
                                st);
   else
     e = launch_cached_attention(qbuf, K_cache, V_cache, pos_cache, segment_pos, pad_lens, qbuf,
                                 kBF16, d->B, d->T, S, end_index, d->H, d->H_kv, d->d_h,
-                                attn_type == GEMMA3_LOCAL_SLIDING ? window : 0, aws, s, st);
+                                attn_type == GEMMA3_LOCAL_SLIDING ? window : 0, aws, s, st,
+                                /*prepared=*/cached);
   if (e != cudaSuccess) return GEMMA3_ERR_CUDA;
   return to_status(launch_linear(qbuf, HD, Wo, HD, out, d->D, M, d->D, HD, kBF16, kBF16, s, st, 0));
 }

@@ -14,12 +14,14 @@
 // contractions on the CUDA cores in fp32.  The visible slot range of a batch
 // row is split across CTAs (two resident per SM); each CTA keeps an online
 // softmax per query row and writes an unnormalised partial (m, l, o) that a
-// second kernel merges.  On a local layer a small kernel first finds the
-// first slot any query of the row can see, so CTAs cover only the window.
+// second kernel merges.  On a local layer the first slot any query of the row
+// can see is found first (by the decode-step prologue kernel in its own
+// launch, or else by a small kernel here), so CTAs cover only the window.
 #include <algorithm>
 #include <climits>
 #include <cmath>
 
+#include "decode_span.cuh"
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -30,7 +32,6 @@ namespace {
 constexpr int kSlots = 32;         // slots per tile: one per lane in the logits phase
 constexpr int kCWarps = 4;         // consumer warps; warp 4 issues the TMA loads
 constexpr int kDecThreads = (kCWarps + 1) * 32;
-constexpr int kSpanChunk = 4096;   // slots scanned per CTA by the span kernel (256 x 16)
 constexpr int kMaxSplitCtas = 2048;
 constexpr int kMaxCombineSplits = 256;   // splits per row the combine kernel holds weights for
 constexpr int kMinSplitTiles = 2;        // fewest tiles worth a split of its own
@@ -135,60 +136,15 @@ __global__ void __launch_bounds__(128) kv_cache_append_kernel(
 }
 
 // ---------------------------------------------------------------- span
-// Local layers: slot s can be visible to a valid query of row b only if
-// p_s >= 0 and p_s > min_t(pos_t) - W.  CTA (c, b) writes the first such slot
-// among [c*kSpanChunk, (c+1)*kSpanChunk) ∩ [0, end + T), or INT_MAX.
+// Local layers: CTA (c, b) writes the first slot of chunk c that a valid
+// query of row b can see, or INT_MAX (decode_span.cuh).
 __global__ void __launch_bounds__(256) kv_span_kernel(
     const int32_t* __restrict__ posc, const int32_t* __restrict__ qpos,
     const int32_t* __restrict__ pad_lens, int T, int S, int end, int window, int nchunk,
     int32_t* __restrict__ span_part) {
   pdl_enter();
-  __shared__ int red[8];
-  const int c = blockIdx.x, b = blockIdx.y;
-  const int valid = T - (pad_lens != nullptr ? pad_lens[b] : 0);
-  int qmin = INT_MAX;
-  for (int t = threadIdx.x; t < valid; t += blockDim.x)
-    qmin = min(qmin, qpos[static_cast<size_t>(b) * T + t]);
-  qmin = warp_min_i(qmin);
-  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = qmin;
-  __syncthreads();
-  qmin = INT_MAX;
-  for (int i = 0; i < 8; ++i) qmin = min(qmin, red[i]);
-  __syncthreads();
-  const long long thr = static_cast<long long>(qmin) - window;
-  // Each thread owns 16 consecutive slots of the chunk and loads them at once
-  // (four 16-byte loads when the row is 16-byte aligned), so the scan costs
-  // one memory round trip.
-  const int s_end = min(end + T, (c + 1) * kSpanChunk);
-  const int s0 = c * kSpanChunk + threadIdx.x * 16;
-  const int32_t* row = posc + static_cast<size_t>(b) * S;
-  int v[16];
-  if ((reinterpret_cast<uintptr_t>(row + s0) & 15u) == 0 && s0 + 16 <= s_end) {
-    const int4* q = reinterpret_cast<const int4*>(row + s0);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int4 x = __ldg(q + i);
-      v[4 * i] = x.x;
-      v[4 * i + 1] = x.y;
-      v[4 * i + 2] = x.z;
-      v[4 * i + 3] = x.w;
-    }
-  } else {
-#pragma unroll
-    for (int i = 0; i < 16; ++i) v[i] = s0 + i < s_end ? __ldg(row + s0 + i) : -1;
-  }
-  int best = INT_MAX;
-#pragma unroll
-  for (int i = 15; i >= 0; --i)
-    if (v[i] >= 0 && static_cast<long long>(v[i]) > thr) best = s0 + i;
-  best = warp_min_i(best);
-  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = best;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    int m = INT_MAX;
-    for (int i = 0; i < 8; ++i) m = min(m, red[i]);
-    span_part[static_cast<size_t>(b) * nchunk + c] = m;
-  }
+  kv_span_chunk(posc, qpos, pad_lens, T, S, end, window, nchunk, span_part, blockIdx.x,
+                blockIdx.y);
 }
 
 // ---------------------------------------------------------------- attention
@@ -611,31 +567,41 @@ cudaError_t launch_kv_cache_append(const void* K_rows, const void* V_rows, long 
                     static_cast<__half*>(V_cache), pos_cache);
 }
 
-size_t cached_attention_ws_bytes(int B, int T, int S, int H, int H_kv, int d_h) {
+CachedAttnLayout cached_attention_layout(void* ws, int B, int T, int S, int H, int H_kv, int d_h) {
   const DecPlan d = plan_rows(B, T, H, H_kv);
-  const size_t nchunk = (static_cast<size_t>(S) + kSpanChunk - 1) / kSpanChunk;
-  const size_t span = (static_cast<size_t>(B) * nchunk * 4 + 255) / 256 * 256;
-  const size_t part = static_cast<size_t>(B) * T * H * max_splits(d) * (d_h + 4) * 4;
-  return span + (part + 255) / 256 * 256;
+  auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+  CachedAttnLayout L;
+  L.nchunk = (S + kSpanChunk - 1) / kSpanChunk;
+  const size_t span = up(static_cast<size_t>(B) * L.nchunk * 4);
+  const size_t part = up(static_cast<size_t>(B) * T * H * max_splits(d) * (d_h + 4) * 4);
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  L.span_part = reinterpret_cast<int32_t*>(w);
+  L.part = reinterpret_cast<float*>(w + span);
+  L.bytes = span + part;
+  return L;
 }
+
+size_t cached_attention_ws_bytes(int B, int T, int S, int H, int H_kv, int d_h) {
+  return cached_attention_layout(nullptr, B, T, S, H, H_kv, d_h).bytes;
+}
+
+int cached_span_chunks(int T, int end) { return (end + T + kSpanChunk - 1) / kSpanChunk; }
 
 cudaError_t launch_cached_attention(const void* Q, const void* K_cache, const void* V_cache,
                                     const int32_t* pos_cache, const int32_t* qpos,
                                     const int32_t* pad_lens, void* O, int o_dtype, int B, int T,
                                     int S, int end, int H, int H_kv, int d_h, int window,
-                                    void* ws, cudaStream_t stream, int* status) {
+                                    void* ws, cudaStream_t stream, int* status, bool prepared) {
   if (B <= 0 || T <= 0) return cudaSuccess;
   if (o_dtype != kBF16 && o_dtype != kF16) return cudaErrorInvalidValue;
   const DecPlan d = plan_rows(B, T, H, H_kv);
   if (static_cast<long long>(B) * d.ntg > 65535 || B > 65535 || H_kv > 65535)
     return cudaErrorInvalidValue;
-  const int nchunk_max = (S + kSpanChunk - 1) / kSpanChunk;
   const int hi = end + T;
-  const int nchunk = (hi + kSpanChunk - 1) / kSpanChunk;
-  int32_t* span_part = static_cast<int32_t*>(ws);
-  float* part = reinterpret_cast<float*>(
-      static_cast<uint8_t*>(ws) +
-      (static_cast<size_t>(B) * nchunk_max * 4 + 255) / 256 * 256);
+  const int nchunk = cached_span_chunks(T, end);
+  const CachedAttnLayout lay = cached_attention_layout(ws, B, T, S, H, H_kv, d_h);
+  int32_t* span_part = lay.span_part;
+  float* part = lay.part;
 
   // Splits: enough CTAs for two per SM, but at least kMinSplitTiles tiles
   // each over the span the rows are expected to see (a local layer's window
@@ -649,7 +615,9 @@ cudaError_t launch_cached_attention(const void* Q, const void* K_cache, const vo
   if (nsplit > max_splits(d)) nsplit = max_splits(d);
   if (nsplit < 1) nsplit = 1;
 
-  if (window > 0) {
+  // The span scan of a local layer, unless the decode-step prologue already
+  // wrote it (`prepared`).
+  if (window > 0 && !prepared) {
     cudaError_t e = launch_pdl(kv_span_kernel, dim3(nchunk, B), dim3(256), 0, stream, pos_cache,
                                qpos, pad_lens, T, S, end, window, nchunk, span_part);
     if (e != cudaSuccess) return e;

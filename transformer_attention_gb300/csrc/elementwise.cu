@@ -23,6 +23,7 @@
 //   a <- RMSNorm_post(a); h = x + a), one warp per row.
 #include <cmath>
 
+#include "decode_span.cuh"
 #include "internal.h"
 #include "ptx.cuh"
 #include "rope.cuh"
@@ -45,8 +46,18 @@ __global__ void __launch_bounds__(256, 2)
                         const __nv_bfloat16* __restrict__ gamma_q,
                         const __nv_bfloat16* __restrict__ gamma_k, const int32_t* __restrict__ pos,
                         int M, int H, int H_kv, const __grid_constant__ RopeFreqs freqs,
-                        float query_scale, const __grid_constant__ CacheRows cache, int chunk_u) {
+                        float query_scale, const __grid_constant__ CacheRows cache, int chunk_u,
+                        int qk_blocks) {
   pdl_enter();
+  if (static_cast<int>(blockIdx.x) >= qk_blocks) {
+    // CTAs past qk_blocks scan the local layer's cache span for the cache
+    // attention of a decode step: CTA qk_blocks + b * nchunk + c takes chunk c
+    // of row b.
+    const int idx = static_cast<int>(blockIdx.x) - qk_blocks;
+    kv_span_chunk(cache.posc, pos, cache.pad_lens, cache.T, cache.S, cache.end, cache.window,
+                  cache.nchunk, cache.span_part, idx % cache.nchunk, idx / cache.nchunk);
+    return;
+  }
   constexpr int LPV = DH / 8;      // lanes per head vector
   constexpr int VPW = 32 / LPV;    // head vectors per warp step
   constexpr int HALF = LPV / 2;    // lane distance of the RoPE partner
@@ -59,7 +70,7 @@ __global__ void __launch_bounds__(256, 2)
   const uint4 gq_raw = *reinterpret_cast<const uint4*>(gamma_q + ll * 8);
   const uint4 gk_raw = *reinterpret_cast<const uint4*>(gamma_k + ll * 8);
 
-  const int warps_total = gridDim.x * (blockDim.x >> 5);
+  const int warps_total = qk_blocks * (blockDim.x >> 5);
   const int nvec = H + H_kv;
   const int vpc = VPW * chunk_u;                   // head vectors per item
   const int nch = (nvec + vpc - 1) / vpc;          // items per row
@@ -408,16 +419,25 @@ cudaError_t launch_qk_norm_rope(void* Q, long ldq, void* K, long ldk, const void
   const long cap = static_cast<long>(num_sms()) * 4;
   if (blocks > cap) blocks = cap;
   const RopeFreqs freqs = make_rope_freqs(d_h, rope_base, rope_scale);
+  // the span-scan CTAs of a local layer's cache (see the kernel)
+  int prep = 0;
+  if (cache.span_part != nullptr && cache.window > 0) {
+    if (cache.Kc == nullptr || cache.T < 1 || cache.nchunk < 1) return cudaErrorInvalidValue;
+    prep = cache.nchunk * (M / cache.T);
+  }
   auto q = static_cast<__half*>(Q);
   auto k = static_cast<__half*>(K);
   auto gq = static_cast<const __nv_bfloat16*>(gamma_q);
   auto gk = static_cast<const __nv_bfloat16*>(gamma_k);
+  const int qk_blocks = static_cast<int>(blocks);
   if (d_h == 256)
-    return launch_pdl(qk_norm_rope_kernel<256>, dim3(blocks), dim3(256), 0, stream, q, ldq, k,
-                      ldk, gq, gk, pos, M, H, H_kv, freqs, query_scale, cache, chunk_u);
+    return launch_pdl(qk_norm_rope_kernel<256>, dim3(qk_blocks + prep), dim3(256), 0, stream, q,
+                      ldq, k, ldk, gq, gk, pos, M, H, H_kv, freqs, query_scale, cache, chunk_u,
+                      qk_blocks);
   if (d_h == 128)
-    return launch_pdl(qk_norm_rope_kernel<128>, dim3(blocks), dim3(256), 0, stream, q, ldq, k,
-                      ldk, gq, gk, pos, M, H, H_kv, freqs, query_scale, cache, chunk_u);
+    return launch_pdl(qk_norm_rope_kernel<128>, dim3(qk_blocks + prep), dim3(256), 0, stream, q,
+                      ldq, k, ldk, gq, gk, pos, M, H, H_kv, freqs, query_scale, cache, chunk_u,
+                      qk_blocks);
   return cudaErrorInvalidValue;
 }
 

@@ -125,6 +125,11 @@ struct CacheRows {
   long ldv = 0;
   const int32_t* pad_lens = nullptr;
   int T = 1, S = 0, end = 0;
+  // With span_part on a local layer (window > 0): the launch also writes the
+  // visible span of each row ([B, nchunk], nchunk = cached_span_chunks) for
+  // the cache attention that follows (launch_cached_attention with prepared).
+  int32_t* span_part = nullptr;
+  int window = 0, nchunk = 0;
 };
 
 // In place on fp16 rows: Q[m, h*d_h:(h+1)*d_h] and K[m, j*d_h:(j+1)*d_h] get
@@ -188,10 +193,24 @@ size_t cached_attention_ws_bytes(int B, int T, int S, int H, int H_kv, int d_h);
 // Attention of T query tokens per row (written to slots end..end+T-1) over a
 // left-aligned K'/V cache [B, S, H_kv, d_h] fp16 with stored positions
 // pos_cache [B, S]; Q' and O [B, T, H, d_h] (O in o_dtype, may alias Q').
+// prepared: the kernel before it on the stream already wrote the local
+// layer's span (CacheRows with span_part); otherwise this call scans it first.
 cudaError_t launch_cached_attention(const void* Q, const void* K_cache, const void* V_cache,
                                     const int32_t* pos_cache, const int32_t* qpos,
                                     const int32_t* pad_lens, void* O, int o_dtype, int B, int T,
                                     int S, int end, int H, int H_kv, int d_h, int window,
-                                    void* ws, cudaStream_t stream, int* status);
+                                    void* ws, cudaStream_t stream, int* status,
+                                    bool prepared = false);
+
+// Where launch_cached_attention keeps its span and split partials in a
+// workspace `ws` (bytes: the total), and the span chunks of a call.
+struct CachedAttnLayout {
+  int32_t* span_part;
+  float* part;
+  int nchunk;
+  size_t bytes;
+};
+CachedAttnLayout cached_attention_layout(void* ws, int B, int T, int S, int H, int H_kv, int d_h);
+int cached_span_chunks(int T, int end);
 
 }  // namespace g3
