@@ -44,6 +44,9 @@ METRIC = "attention-layer tokens/s; attn TFLOP/s as % of GB300 dense BF16 peak"
 DEFAULT_WORKLOAD = "27b_global"
 MODEL_CODE = {"270M": 0, "1B": 1, "4B": 2, "12B": 3, "27B": 4}
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# Dominant-kernel launches at least this long are compared with the sustained
+# tensor peak rather than the burst one.
+SUSTAINED_LAUNCH_S = 0.005
 
 
 # ---------------------------------------------------------------------------- helpers
@@ -406,11 +409,17 @@ def run_gpu(args, world, rank, local):
     avg_s = kern_ms[dom] / 1e3 / n_launch
     per_launch_work = work[dom] / launches[dom]
     if dom in ("attention", "linear"):
-        # each launch is sub-millisecond and bracketed by its own events, so
-        # the burst figure is the denominator; the sustained one is context
-        peak = peaks["bf16_tflops"]
+        # The denominator: the burst figure for launches short enough to run
+        # before the power cap engages, the sustained (seconds-long loop)
+        # figure for launches of several milliseconds, which run under it
+        # (the 27B-shaped attention: ~86 ms per launch); both fractions are
+        # reported.
         achieved = per_launch_work / avg_s / 1e12
-        roof = {"bound": "tensor", "unit": "TFLOP/s", "peak_kind": f"bf16 burst ({peak_src})",
+        sustained = avg_s >= SUSTAINED_LAUNCH_S
+        peak = peaks["bf16_tflops_sustained" if sustained else "bf16_tflops"]
+        roof = {"bound": "tensor", "unit": "TFLOP/s",
+                "peak_kind": f"bf16 {'sustained' if sustained else 'burst'} ({peak_src})",
+                "frac_of_burst": achieved / peaks["bf16_tflops"],
                 "frac_of_sustained": achieved / peaks["bf16_tflops_sustained"]}
     else:
         peak = peaks["hbm_gbs"]

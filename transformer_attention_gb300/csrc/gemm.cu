@@ -19,9 +19,9 @@
 //               128-byte-swizzled shared-memory staging tile that one lane
 //               stores with a TMA bulk tensor store (full-line writes instead
 //               of 32 scattered 16-byte pieces per warp instruction).
-// Tiles are visited in groups of 8 M-tiles (N-tiles varying slowest within
-// a group), so the tiles in flight share A rows and W rows through L2 even
-// when W is larger than L2.
+// Tiles are visited in groups of consecutive M tiles (N-tiles varying slowest
+// within a group), so the tiles in flight share A rows and W rows through
+// L2; weights larger than L2 get groups of ~20 MB of A.
 // Epilogue modes: plain conversion; GeGLU (the feed-forward gating
 // projection); and the attention prologue ("QK-Norm", How it works; "Gemma 3
 // Attention Block", How it works: QK-norm, then RoPE, then scale) applied to
@@ -47,7 +47,18 @@ constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr uint32_t STAGING_BYTES = 32 * 128;           // one warp's 32 rows x 128 B
 constexpr uint32_t STAGING_TOTAL = 4 * 2 * STAGING_BYTES;   // 4 warps, double-buffered
 constexpr uint32_t SMEM_BYTES = STAGES * STAGE_BYTES + STAGING_TOTAL + 1024;
-constexpr int GROUP_M = 8;   // M-tiles per rasterisation group
+// Rasterisation: tiles are visited in groups of consecutive M tiles, the N
+// tile varying slowest within a group, so a group's A rows stay in L2 while
+// W streams past them.  A weight that fits in L2 (up to kSmallWeightBytes)
+// is read from DRAM once whatever the grouping, and groups of 8 M tiles keep
+// each A tile shared by many CTAs at once.  A larger weight is read once per
+// group, so its groups hold about kGroupBytes of A.  Measured on GB300 (27B
+// projections, W 44-88 MB): 8-tile groups 1570, ~20 MB groups 1644, ~40 MB
+// 1624, ~80 MB 1494 TF/s; on the 1B shapes (W 3.5 MB) 8-tile groups were
+// the fastest (1250 against 1173 TF/s with ~20 MB groups).
+constexpr int kSmallGroupM = 8;
+constexpr size_t kSmallWeightBytes = size_t(32) << 20;
+constexpr size_t kGroupBytes = size_t(20) << 20;
 
 // Unit t of the grouped order -> (m unit, n tile); a group spans `group`
 // m units.
@@ -108,8 +119,8 @@ template <int AB_BF16, typename OutT, int EPI, int DH>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_tn_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmB2,
-                   const __grid_constant__ CUtensorMap tmC2, int M, int N, int K, int* status,
-                   const __grid_constant__ QkEpi epi) {
+                   const __grid_constant__ CUtensorMap tmC2, int M, int N, int K, int group_m,
+                   int* status, const __grid_constant__ QkEpi epi) {
   pdl_enter();
   constexpr bool GEGLU = EPI == kEpiGeglu;
   static_assert(EPI != kEpiQkNorm || (std::is_same<OutT, __half>::value && (DH == 128 || DH == 256)),
@@ -131,7 +142,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int num_units = m_tiles * n_tiles;
   const int unit0 = blockIdx.x, unit_step = gridDim.x;
   const int num_kb = (K + BK - 1) / BK;
-  auto unit_coords = [&](int u, int& mt, int& nt) { tile_coords(u, m_tiles, n_tiles, GROUP_M, mt, nt); };
+  auto unit_coords = [&](int u, int& mt, int& nt) { tile_coords(u, m_tiles, n_tiles, group_m, mt, nt); };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -513,8 +524,17 @@ cudaError_t launch_typed(const CUtensorMap& ta, const CUtensorMap& tb, void* C, 
   int grid = num_sms();
   if (max_ctas > 0 && max_ctas < grid) grid = max_ctas;
   if (tiles < grid) grid = tiles;
+  const size_t a_tile_bytes = static_cast<size_t>(BM) * K * 2;
+  const size_t w_bytes = static_cast<size_t>(GEGLU ? 2 * N : N) * K * 2;
+  const int m_tiles = (M + BM - 1) / BM;
+  int group_m = kSmallGroupM;
+  if (w_bytes > kSmallWeightBytes) {
+    const size_t g = kGroupBytes / a_tile_bytes;
+    if (g > static_cast<size_t>(group_m)) group_m = static_cast<int>(g);
+  }
+  if (group_m > m_tiles) group_m = m_tiles;
   return launch_pdl(kern, dim3(grid), dim3(THREADS), SMEM_BYTES, stream, ta, tb, tc,
-                    tb2 != nullptr ? *tb2 : tb, tc2, M, N, K, status, epi);
+                    tb2 != nullptr ? *tb2 : tb, tc2, M, N, K, group_m, status, epi);
 }
 
 bool encode_ab(CUtensorMap& ta, CUtensorMap& tb, const void* A, long lda, const void* W, long ldw,
