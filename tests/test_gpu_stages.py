@@ -243,6 +243,11 @@ ATTN_CASES = [
     (1, 300, 4, 1, 128, 100, [0]),
     (3, 260, 2, 1, 128, 64, [0, 259, 260]),
     (1, 1100, 8, 4, 128, 300, [0]),
+    # local layers with more (b, kv head) pairs than one L2 ordering group
+    # holds: groups of 8 pairs (d_h = 256) and of 50 + a partial 14 (d_h =
+    # 128), with a one-token row and an all-padding row
+    (4, 1024, 32, 16, 256, 1000, [0, 100, 1023, 1024]),
+    (2, 512, 64, 32, 128, 200, [0, 77]),
 ]
 
 
