@@ -113,13 +113,17 @@ def test_small_full_block(kw):
         Hh.assert_close(got[b, :valid], ref[b, :valid], f"full block b={b}")
 
 
+@pytest.mark.slow
 def test_full_size_4b_block_prefix():
+    """The 4B-shaped block (B2 T32768) on the GPU; the oracle runs the first
+    4096 tokens of each batch row (four 1024-token windows) through the
+    whole block."""
     w = WL.WORKLOADS["4b_block"]
     inp = Hh.make_inputs(w)
     inp.update(WL.block_norm_gammas(w, 0))
     ffn = WL.ffn_weights(w)
     got = _gpu_block(w, inp, ffn)
-    L = 1200
+    L = 4096
     for b in range(w.B):
         ref = _oracle_block(w, inp, ffn, x=inp["x"][b:b + 1, :L],
                             pad_lens=torch.zeros(1, dtype=torch.int64),
