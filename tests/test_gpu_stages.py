@@ -43,7 +43,10 @@ def _randn(shape, seed, std=1.0, dtype=torch.bfloat16):
                                    # ragged M / N / K
                                    (5170, 2200, 1024), (2000, 3000, 200),
                                    # a wave of tiles 5 wide (one CTA per tile)
-                                   (5170, 1152, 1024)])
+                                   (5170, 1152, 1024),
+                                   # a last tile column at most half full
+                                   # (half-width MMAs): 1096 = 4 x 256 + 72
+                                   (640, 1096, 512), (384, 96, 256)])
 @pytest.mark.parametrize("out", ["bf16", "f16", "f32"])
 @pytest.mark.parametrize("inp", ["bf16", "f16"])
 def test_linear_matches_fp64(M, N, K, out, inp):

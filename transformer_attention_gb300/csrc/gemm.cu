@@ -213,7 +213,10 @@ __global__ void __launch_bounds__(THREADS, 1)
     // ---------------- MMA issuer: the whole warp runs the loop (its state
     // warp-uniform); each tcgen05 instruction is issued by one elected lane.
     const uint32_t lead = elect_one();
-    const uint32_t idesc = idesc_f16(BM, BN, AB_BF16, 0, 0);
+    const uint32_t idesc_full = idesc_f16(BM, BN, AB_BF16, 0, 0);
+    // A plain output's last tile column holding at most half a tile runs
+    // MMAs half as wide (the rows of W past N are zeros either way).
+    const uint32_t idesc_half = idesc_f16(BM, BN / 2, AB_BF16, 0, 0);
     int stage = 0;
     uint32_t phase = 0;
     int abuf = 0;
@@ -225,6 +228,10 @@ __global__ void __launch_bounds__(THREADS, 1)
         break;
       tc_fence_after();
       const uint32_t d_tmem = tbase + abuf * BN;
+      int mt_u, nt_u;
+      unit_coords(u, mt_u, nt_u);
+      const uint32_t idesc =
+          (EPI == kEpiPlain && N - nt_u * BN_OUT <= BN / 2) ? idesc_half : idesc_full;
       for (int kb = 0; kb < num_kb; ++kb) {
         if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&full_bar[stage]), phase, &abort_flag,
                                                status, kSiteFull))) {
