@@ -251,6 +251,12 @@ ATTN_CASES = [
     # 128), with a one-token row and an all-padding row
     (4, 1024, 32, 16, 256, 1000, [0, 100, 1023, 1024]),
     (2, 512, 64, 32, 128, 200, [0, 77]),
+    # d_h = 256 local layers run KV tiles from each item's first visible key:
+    # last tiles of 128 (one head per kv head), 16 (two, a padded row) and
+    # 112 keys (four), tiles that run past T
+    (1, 2000, 2, 2, 256, 1024, [0]),
+    (2, 900, 8, 4, 256, 200, [0, 333]),
+    (1, 700, 8, 2, 256, 80, [3]),
 ]
 
 

@@ -148,6 +148,7 @@ using attn::fmax3;
 template <int DH, int G>
 __global__ void __launch_bounds__(THREADS, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                    const __grid_constant__ CUtensorMap tmK64,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
                     uint16_t* __restrict__ O, int o_f16,
                     const int32_t* __restrict__ pad_lens, int B, int T, int H, int H_kv,
@@ -204,6 +205,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     fence_barrier_init();
     tma_prefetch_desc(&tmQ);
     tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmK64);
     tma_prefetch_desc(&tmV);
     tma_prefetch_desc(&tmO);
   }
@@ -235,7 +237,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         int kf[C::NKB] = {};  // loads issued per K barrier
         bool ok = true;
         for (int rr = 0, pos; ok && (pos = fetch_pos(rr)) < num_items; ++rr) {
-          const Item it = decode_item(pos, C::TQ, num_q_tiles, gsz, B, H_kv, T, window, pad_lens);
+          const Item it = decode_item(pos, C::TQ, num_q_tiles, gsz, B, H_kv, T, window, pad_lens, true);
           if (it.pad) continue;
           // The Q buffer is free once the previous item's last S MMA is done.
           if (!mbar_wait(smem_u32(&q_empty), (nq & 1) ^ 1, &abort_flag, status, kSiteQ)) break;
@@ -252,10 +254,13 @@ __global__ void __launch_bounds__(THREADS, 1)
                 break;
               }
               const uint32_t fb = smem_u32(&k_full[kb]);
-              mbar_arrive_expect_tx(fb, C::KGRP * CHUNK);
+              // The last tile's S reads only its first last_n keys: when they
+              // fit in half a tile, only that half of each chunk is loaded.
+              const bool half = i == it.n_tiles - 1 && it.last_n <= BN / 2;
+              mbar_arrive_expect_tx(fb, half ? C::KGRP * CHUNK / 2 : C::KGRP * CHUNK);
               for (int ch = kb * C::KGRP; ch < (kb + 1) * C::KGRP; ++ch)
-                tma_load_3d(smem_u32(sK + ch * CHUNK), &tmK, fb, it.j * DH + ch * 64,
-                            (it.tile_lo + i) * BN, it.b);
+                tma_load_3d(smem_u32(sK + ch * CHUNK), half ? &tmK64 : &tmK, fb,
+                            it.j * DH + ch * 64, it.s_base + i * BN, it.b);
               ++kf[kb];
             }
           }
@@ -274,7 +279,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           const int pos = take_pos(rr);
           release_pos(rr);
           if (pos >= num_items) break;
-          const Item it = decode_item(pos, C::TQ, num_q_tiles, gsz, B, H_kv, T, window, pad_lens);
+          const Item it = decode_item(pos, C::TQ, num_q_tiles, gsz, B, H_kv, T, window, pad_lens, true);
           for (int i = 0; ok && i < it.n_tiles; ++i, ++f) {
             for (int h = 0; h < 2; ++h) {
               if (!mbar_wait(smem_u32(&v_empty[h]), (f & 1) ^ 1, &abort_flag, status,
@@ -283,10 +288,15 @@ __global__ void __launch_bounds__(THREADS, 1)
                 break;
               }
               const uint32_t fb = smem_u32(&v_full[h]);
-              mbar_arrive_expect_tx(fb, C::KV_BYTES / 2);
-              for (int ch = 0; ch < C::NCH; ++ch)
-                tma_load_3d(smem_u32(sV + ch * CHUNK + h * (CHUNK / 2)), &tmV, fb,
-                            it.j * DH + ch * 64, (it.tile_lo + i) * BN + h * (BN / 2), it.b);
+              if (h == 1 && i == it.n_tiles - 1 && it.last_n <= BN / 2) {
+                // No row sees the second half of the last tile: nothing to load.
+                mbar_arrive(fb);
+              } else {
+                mbar_arrive_expect_tx(fb, C::KV_BYTES / 2);
+                for (int ch = 0; ch < C::NCH; ++ch)
+                  tma_load_3d(smem_u32(sV + ch * CHUNK + h * (CHUNK / 2)), &tmV, fb,
+                              it.j * DH + ch * 64, it.s_base + i * BN + h * (BN / 2), it.b);
+              }
               ++vf[h];
             }
           }
@@ -306,8 +316,9 @@ __global__ void __launch_bounds__(THREADS, 1)
       auto wait_all = [&](uint64_t& bar, int parity, int site) -> bool {
         return __all_sync(0xffffffffu, mbar_wait(smem_u32(&bar), parity, &abort_flag, status, site));
       };
-      // PV of global tile gt, local tile lt of the current item.
-      auto issue_pv = [&](int gt, int lt) -> bool {
+      // PV of global tile gt, local tile lt of the current item, over its
+      // first nk / 16 key steps (all 128 keys but on the item's last tile).
+      auto issue_pv = [&](int gt, int lt, int nk) -> bool {
         // The first PV of an item overwrites O: the previous item's epilogue
         // must have read it.
         if (lt == 0 && nitem >= 1 && !wait_all(o_free, (nitem - 1) & 1, kSiteOFinal)) return false;
@@ -320,8 +331,10 @@ __global__ void __launch_bounds__(THREADS, 1)
           tc_fence_after();
 #pragma unroll
           for (int k = 4 * h; k < 4 * h + 4; ++k)
-            mma_ts_lead(lead, tbase + O_COL, p_tmem + k * 8, sdesc_sw128(v_addr + k * 2048, CHUNK, 1024),
-                        idesc_pv, (lt > 0 || k > 0) ? 1u : 0u);
+            if (k * 16 < nk)
+              mma_ts_lead(lead, tbase + O_COL, p_tmem + k * 8,
+                          sdesc_sw128(v_addr + k * 2048, CHUNK, 1024), idesc_pv,
+                          (lt > 0 || k > 0) ? 1u : 0u);
           mma_commit_lead(lead, smem_u32(&v_empty[h]));
         }
         mma_commit_lead(lead, smem_u32(&pv_done[gt & 1]));
@@ -335,9 +348,12 @@ __global__ void __launch_bounds__(THREADS, 1)
         __syncwarp();
         if (lane == 0) release_pos(rr);
         if (pos >= num_items) break;
-        const Item it = decode_item(pos, C::TQ, num_q_tiles, gsz, B, H_kv, T, window, pad_lens);
+        const Item it = decode_item(pos, C::TQ, num_q_tiles, gsz, B, H_kv, T, window, pad_lens, true);
         if (it.pad) continue;
         if (!wait_all(q_full, nitem & 1, kSiteQ)) break;
+        // The last tile's S covers only the keys some row can see.
+        const uint32_t idesc_last = idesc_f16(BM, it.last_n, /*f16*/ 0, 0, 0);
+        auto tile_keys = [&](int lt) { return lt == it.n_tiles - 1 ? it.last_n : BN; };
         for (int i = 0; ok && i < it.n_tiles; ++i, ++g) {
           // S buffer g % NS last held P_{g-NS}, whose PV this warp issued
           // before: the tensor pipe runs them in order.
@@ -355,7 +371,8 @@ __global__ void __launch_bounds__(THREADS, 1)
             for (int k = 4 * C::KGRP * kb; k < 4 * C::KGRP * (kb + 1); ++k) {
               const uint32_t off = (k >> 2) * CHUNK + (k & 3) * 32;
               mma_ss_lead(lead, tbase + C::s_col(sb), sdesc_sw128(q_addr + off, 16, 1024),
-                          sdesc_sw128(k_addr + off, 16, 1024), idesc_qk, k > 0 ? 1u : 0u);
+                          sdesc_sw128(k_addr + off, 16, 1024),
+                          i == it.n_tiles - 1 ? idesc_last : idesc_qk, k > 0 ? 1u : 0u);
             }
             mma_commit_lead(lead, smem_u32(&k_empty[kb]));
           }
@@ -364,7 +381,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           if (i == it.n_tiles - 1) mma_commit_lead(lead, smem_u32(&q_empty));
           // S runs LA tiles ahead of PV (S_g reuses the buffer of P_{g-NS},
           // so LA <= NS - 1): the softmax finds the next S already computed.
-          if (i >= C::LA && !issue_pv(g - C::LA, i - C::LA)) {
+          if (i >= C::LA && !issue_pv(g - C::LA, i - C::LA, tile_keys(i - C::LA))) {
             ok = false;
             break;
           }
@@ -372,7 +389,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         // the PVs of the item's last LA tiles, then o_final: this item's O
         // accumulation is complete.
         for (int d = C::LA; ok && d >= 1; --d)
-          if (it.n_tiles - d >= 0 && !issue_pv(g - d, it.n_tiles - d)) ok = false;
+          if (it.n_tiles - d >= 0 && !issue_pv(g - d, it.n_tiles - d, tile_keys(it.n_tiles - d)))
+            ok = false;
         if (!ok) break;
         mma_commit_lead(lead, smem_u32(&o_final));
         ++nitem;
@@ -395,7 +413,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       __syncwarp();
       if (lane == 0) release_pos(rr);
       if (pos >= num_items) break;
-      const Item it = decode_item(pos, C::TQ, num_q_tiles, gsz, B, H_kv, T, window, pad_lens);
+      const Item it = decode_item(pos, C::TQ, num_q_tiles, gsz, B, H_kv, T, window, pad_lens, true);
       if (it.pad) continue;   // the epilogue writes its zero rows
       const int t = it.t0 + i_tok;
       const int kv_lo = window > 0 ? t - window + 1 : 0;   // keys kv_lo..kv_hi are kept
@@ -408,7 +426,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                                                &abort_flag, status, kSiteSFull));
         if (!ok) break;
         tc_fence_after();
-        const int s_tile = (it.tile_lo + i) * BN;
+        const int s_tile = it.s_base + i * BN;
         const bool need_mask = (s_tile + BN - 1 > it.t0) || (s_tile + BN > it.valid) ||
                                (window > 0 && s_tile <= it.t_last - window);
         const int c_lo = kv_lo - s_tile, c_hi = kv_hi - s_tile;
@@ -487,7 +505,9 @@ __global__ void __launch_bounds__(THREADS, 1)
           exp_pack16(rb, p + 16, acc, l2e, negm);
           tmem_st32(s_base, p);
         }
-        {
+        // Columns 64-127 of a last tile of at most 64 visible keys are all
+        // masked (P = 0 there) and its PV stops at key 64: no exponentials.
+        if (!(i == it.n_tiles - 1 && it.last_n <= BN / 2)) {
           uint32_t p[32];
           exp_pack16(rc, p, acc, l2e, negm);
           exp_pack16(rd, p + 16, acc, l2e, negm);
@@ -525,7 +545,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       __syncwarp();
       if (lane == 0) release_pos(rr);
       if (pos >= num_items) break;
-      const Item it = decode_item(pos, C::TQ, num_q_tiles, gsz, B, H_kv, T, window, pad_lens);
+      const Item it = decode_item(pos, C::TQ, num_q_tiles, gsz, B, H_kv, T, window, pad_lens, true);
       if (it.pad) {
         // The whole tile is padding: its output rows are zero (bits 0 in bf16 and f16).
         const int rows = min(C::TQ, T - it.t0);
@@ -612,7 +632,7 @@ cudaError_t launch_cfg(const void* Q, const void* K, const void* V, long ldkv, v
                        int window, unsigned int* sched, cudaStream_t stream, int* status,
                        bool sched_zeroed) {
   using C = Cfg<DH, G>;
-  CUtensorMap tq, tk, tv;
+  CUtensorMap tq, tk, tk64, tv;
   // Q' [B, T, H, d_h]: box {64 of d_h, the G heads of one group, TQ tokens, 1}.
   const uint64_t qdims[4] = {static_cast<uint64_t>(DH), static_cast<uint64_t>(H),
                              static_cast<uint64_t>(T), static_cast<uint64_t>(B)};
@@ -624,7 +644,9 @@ cudaError_t launch_cfg(const void* Q, const void* K, const void* V, long ldkv, v
                              static_cast<uint64_t>(B)};
   const uint64_t kstr[2] = {static_cast<uint64_t>(ldkv) * 2, static_cast<uint64_t>(T) * ldkv * 2};
   const uint32_t kbox[3] = {64, BN, 1};
-  const uint32_t vbox[3] = {64, BN / 2, 1};   // V arrives half a tile of keys at a time
+  // V arrives half a tile of keys at a time; K in half tiles on an item's
+  // last tile when no row sees past its first half.
+  const uint32_t vbox[3] = {64, BN / 2, 1};
   // O [B, T, H, d_h] (16-bit, bf16 or fp16 bits alike): box {32 channels, G
   // heads, 32/G tokens, 1}, 64-byte swizzle.
   CUtensorMap to;
@@ -634,6 +656,7 @@ cudaError_t launch_cfg(const void* Q, const void* K, const void* V, long ldkv, v
     return cudaErrorInvalidValue;
   if (!encode_tiled(&tq, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4, Q, qdims, qstr, qbox) ||
       !encode_tiled(&tk, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, K, kdims, kstr, kbox) ||
+      !encode_tiled(&tk64, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, K, kdims, kstr, vbox) ||
       !encode_tiled(&tv, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, V, kdims, kstr, vbox))
     return cudaErrorInvalidValue;
   auto kern = attn_fwd_kernel<DH, G>;
@@ -652,7 +675,7 @@ cudaError_t launch_cfg(const void* Q, const void* K, const void* V, long ldkv, v
   if (sched != nullptr && !sched_zeroed &&
       cudaMemsetAsync(sched, 0, sizeof(unsigned int), stream) != cudaSuccess)
     return cudaErrorUnknown;
-  return launch_pdl(kern, dim3(grid), dim3(THREADS), C::SMEM, stream, tq, tk, tv, to,
+  return launch_pdl(kern, dim3(grid), dim3(THREADS), C::SMEM, stream, tq, tk, tk64, tv, to,
                     static_cast<uint16_t*>(O), o_dtype == kF16 ? 1 : 0, pad_lens, B, T, H, H_kv,
                     window, num_q_tiles, gsz, static_cast<int>(items), sched, status);
 }

@@ -32,14 +32,22 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
 // the G heads of kv head j) of batch row b, and the KV tiles it visits.
 struct Item {
   int b, j, t0, valid, t_last, tile_lo, n_tiles;
-  bool pad;   // every token past the valid length: the item only writes zeros
+  int s_base;   // first key of the first KV tile; tile i starts at s_base + i * KV_TILE
+  int last_n;   // keys of the last tile that any row can see, rounded up to 16
+  bool pad;     // every token past the valid length: the item only writes zeros
 };
 
 // Position p of the heavy-first order -> item.  n_q items of `span` tokens
 // cover each (b, j) pair; KV tiles outside the causal band and the window
-// (keep t - W < s <= t) are not visited.
+// (keep t - W < s <= t) are not visited.  By default the KV tiles sit on
+// multiples of KV_TILE.  With `from_window` they start at the item's first
+// visible key instead, t0 - W + 1 (0 on a global layer), so the item's keys
+// t0 - W + 1 .. t_last span ceil((W + span - 1) / KV_TILE) tiles whatever t0
+// is, and only the last tile's first last_n keys are visible to any row
+// (its S and PV products can stop there).
 __device__ __forceinline__ Item decode_item(int p, int span, int n_q, int gsz, int B, int H_kv,
-                                            int T, int window, const int32_t* pad_lens) {
+                                            int T, int window, const int32_t* pad_lens,
+                                            bool from_window = false) {
   Item it;
   const int BH = B * H_kv;
   const int group = p / (gsz * n_q);
@@ -56,7 +64,16 @@ __device__ __forceinline__ Item decode_item(int p, int span, int n_q, int gsz, i
   it.t_last = min(it.t0 + span, it.valid) - 1;
   const int s_lo = window > 0 ? max(0, it.t0 - window + 1) : 0;
   it.tile_lo = s_lo / KV_TILE;
-  it.n_tiles = it.pad ? 0 : it.t_last / KV_TILE - it.tile_lo + 1;
+  if (from_window) {
+    const int n_keys = it.t_last - s_lo + 1;
+    it.s_base = s_lo;
+    it.n_tiles = it.pad ? 0 : (n_keys + KV_TILE - 1) / KV_TILE;
+    it.last_n = it.pad ? 0 : (n_keys - (it.n_tiles - 1) * KV_TILE + 15) & ~15;
+  } else {
+    it.s_base = it.tile_lo * KV_TILE;
+    it.n_tiles = it.pad ? 0 : it.t_last / KV_TILE - it.tile_lo + 1;
+    it.last_n = KV_TILE;
+  }
   return it;
 }
 
