@@ -61,15 +61,18 @@ constexpr size_t kSmallWeightBytes = size_t(32) << 20;
 constexpr size_t kGroupBytes = size_t(20) << 20;
 
 // Unit t of the grouped order -> (m unit, n tile); a group spans `group`
-// m units.
+// m units.  Odd groups walk the N tiles in reverse, so each group starts on
+// the W tiles the previous one used last, which are still in L2 (a weight
+// larger than L2 is otherwise read from DRAM once per group in full).
 __device__ __forceinline__ void tile_coords(int t, int m_units, int n_tiles, int group, int& mu,
                                             int& nt) {
   const int per_group = group * n_tiles;
-  const int first_m = (t / per_group) * group;
+  const int g = t / per_group;
+  const int first_m = g * group;
   const int gm = min(group, m_units - first_m);
   const int r = t % per_group;
   mu = first_m + r % gm;
-  nt = r / gm;
+  nt = (g & 1) ? n_tiles - 1 - r / gm : r / gm;
 }
 constexpr uint32_t TMEM_COLS = 512;
 
