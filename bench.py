@@ -1059,12 +1059,44 @@ def host_cpu() -> dict:
             "machine": platform.machine()}
 
 
+def algorithmic_flops(w, valids, M: int) -> float:
+    """GEMM and attention FLOPs of a workload whose batch rows have the given
+    valid lengths (M rows through the GEMMs): every layer's projections,
+    attention over unmasked pairs, the feed-forward GEMMs of a block and the
+    model's read-out.  Stack layers are local but every sixth."""
+    f = 0.0
+    for layer in range(w.num_layers):
+        local = (layer % 6 != 5) if w.attn_type == "stack" else w.attn_type == "local"
+        f += sum(metrics.layer_gemm_flops(M, w.D, w.H, w.H_kv, w.d_h).values())
+        f += metrics.attention_flops(valids, w.H, w.d_h, w.window if local else 0)
+        if w.d_ff > 0:
+            f += 2.0 * M * (2 * w.d_ff) * w.D + 2.0 * M * w.D * w.d_ff
+    if w.vocab > 0:
+        f += 2.0 * M * w.vocab * w.D
+    return f
+
+
+def single_core_tiny(reps: int = 3) -> dict:
+    """The oracle on the whole tiny_local workload (1024 tokens) with one
+    thread: median of `reps` runs."""
+    import torch
+    w = WL.WORKLOADS["tiny_local"]
+    threads = torch.get_num_threads()
+    torch.set_num_threads(1)
+    try:
+        secs = sorted(oracle_sample(w, w.T) for _ in range(reps))[reps // 2]
+    finally:
+        torch.set_num_threads(threads)
+    return {"workload": w.name, "value": w.T / secs, "unit": "tokens/s", "cores": 1,
+            "seconds": secs, "tflops": algorithmic_flops(w, [w.T], w.T) / secs / 1e12}
+
+
 def cpu_baseline(w, budget_s: float = 15.0):
     import torch
     if w.cache_len > 0:
         secs, runs = oracle_decode_sample(w, budget_s)
         return {"value": w.T * runs / secs, "unit": "tokens/s", "cores": torch.get_num_threads(),
-                "kind": "oracle", **host_cpu(),
+                "kind": "oracle", **host_cpu(), "single_core": single_core_tiny(),
                 "sample": f"fp64 oracle, decode steps of batch row 0 of {w.name} over its "
                           f"{w.cache_len}-slot cache: {runs} steps, {secs:.1f} s"}
     # Rows' prefixes (each row clipped to its valid length), one row after
@@ -1079,8 +1111,18 @@ def cpu_baseline(w, budget_s: float = 15.0):
         tokens += nb
         runs += 1
     rows = sorted({r % w.B for r in range(runs)})
+    # FLOPs of the runs (each a one-row prefix) and of the whole workload:
+    # the full-size time is extrapolated at the sample's FLOP rate (cost
+    # proportional to unmasked pairs and tokens).
+    sample_flops = sum(algorithmic_flops(w, [max(1, min(n, w.T - pads[r % w.B]))],
+                                         max(1, min(n, w.T - pads[r % w.B])))
+                       for r in range(runs))
+    full_flops = algorithmic_flops(w, [w.T - p for p in pads], w.B * w.T)
+    rate = sample_flops / total
     return {"value": tokens / total, "unit": "tokens/s", "cores": torch.get_num_threads(),
             "kind": "oracle", **host_cpu(),
+            "oracle_tflops": rate / 1e12, "extrapolated_full_s": full_flops / rate,
+            "single_core": single_core_tiny(),
             "sample": f"fp64 oracle on causal prefixes of up to {n} tokens of batch rows "
                       f"{rows[0]}..{rows[-1]} of {w.name} ({w.num_layers} layer(s)); "
                       f"{runs} row runs, {tokens} tokens, {total:.1f} s"}

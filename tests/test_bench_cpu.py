@@ -74,3 +74,19 @@ def test_default_workload_is_the_largest_single_gpu_layer():
     w = WL.WORKLOADS[bench.DEFAULT_WORKLOAD]
     assert (w.B, w.T, w.D, w.H, w.H_kv, w.d_h) == (1, 131072, 5376, 32, 16, 128)
     assert w.attn_type == "global" and w.rope_scale == 8.0
+
+
+def test_algorithmic_flops_of_the_survey_configs():
+    """Attention over unmasked pairs plus the projections, as tabulated for
+    the 4B-local (0.541 + 2.062 TF) and 27B-global (140.7 + 17.3 TF) layers."""
+    w = WL.WORKLOADS["4b_local"]
+    f = bench.algorithmic_flops(w, [w.T] * w.B, w.B * w.T)
+    assert abs(f - (0.541e12 + 2.062e12)) / f < 2e-3
+    w = WL.WORKLOADS["27b_global"]
+    f = bench.algorithmic_flops(w, [w.T], w.T)
+    assert abs(f - (140.7e12 + 17.3e12)) / f < 2e-3
+    # a block adds its feed-forward GEMMs, a model its read-out
+    b = WL.small(WL.WORKLOADS["4b_block"], B=1, T=100)
+    base = WL.small(WL.WORKLOADS["4b_local"], B=1, T=100)
+    extra = bench.algorithmic_flops(b, [100], 100) - bench.algorithmic_flops(base, [100], 100)
+    assert extra == 2.0 * 100 * 2 * b.d_ff * b.D + 2.0 * 100 * b.D * b.d_ff
