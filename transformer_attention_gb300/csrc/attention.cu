@@ -14,7 +14,10 @@
 // heads that share kv head j, so every K/V tile loaded from memory feeds all G
 // heads of its group.  KV tiles of 128 keys outside the causal band / window
 // are never visited (local layers cost O(T*W)); only tiles that straddle the
-// band edge, the window edge or the valid length apply an element mask.
+// band edge, the window edge or the valid length apply an element mask.  The
+// tiles start at the item's first visible key (t0 - W + 1, or 0), so an item
+// spans ceil((W + TQ - 1) / 128) tiles, and the last tile's S and PV products
+// stop at the keys some row of the item can see.
 // Work items are ordered in groups of (b, kv-head) pairs whose K/V fit in L2,
 // heaviest query tiles first within a group, and the persistent CTAs (one per
 // SM) take the next position from a counter (or walk the order in
