@@ -209,6 +209,74 @@ def test_forward_cached_prompt_decode_chunk(kw):
     assert torch.equal(cache[2].cpu().to(torch.int64), ocache["pos"])
 
 
+# ---------------------------------------------------------------- one decode step
+# Decode steps (one new token per row) at the edges of the cache path: more
+# rows than the query-row blocks hold, pad rows, an empty cache, a long cache
+# split over many CTAs.
+STEP = [
+    # most rows, a pad row, four query heads per kv head, window inside the cache
+    dict(B=4, D=256, H=4, H_kv=1, d_h=256, attn_type="local", window=50, S=300, end=250,
+         pads=[0, 1, 0, 0]),
+    # the first token of an empty cache, one query head per kv head
+    dict(B=3, D=384, H=4, H_kv=4, d_h=128, attn_type="global", window=0, S=130, end=0,
+         pads=None, rope_base=1e6, rope_scale=8.0),
+    # five rows, one of them padding
+    dict(B=5, D=256, H=4, H_kv=2, d_h=256, attn_type="local", window=64, S=200, end=150,
+         pads=[0, 0, 1, 0, 0]),
+    # a long global cache over many splits, the last slot
+    dict(B=1, D=512, H=4, H_kv=2, d_h=128, attn_type="global", window=0, S=3000, end=2999,
+         pads=None, query_scale=168 ** -0.5),
+]
+
+
+@pytest.mark.parametrize("kw", STEP, ids=lambda k: f"B{k['B']}-d{k['d_h']}-H{k['H']}/{k['H_kv']}-"
+                         f"{k['attn_type']}-end{k['end']}")
+def test_decode_step_against_oracle(kw):
+    """One decode step over a cache holding a prompt in slots [0, end): the
+    output rows, the new slot's K', V and position, and that no other slot
+    changed, against the oracle's cached layer."""
+    import transformer_attention_gb300 as G3
+    kw = dict(kw)
+    S, end, pads = kw.pop("S"), kw.pop("end"), kw.pop("pads")
+    w = _layer_case(T=1, **kw)
+    B, d_h = w.B, w.d_h
+    p = WL.weights(w)
+    dev = {k: v.cuda() for k, v in p.items()}
+    x = WL.x_full(w)
+    K0 = _f16((B, S, w.H_kv, d_h), 71 + S)
+    V0 = _f16((B, S, w.H_kv, d_h), 72 + S)
+    pos0 = torch.full((B, S), -1, dtype=torch.int32)
+    pos0[:, :end] = torch.arange(end, dtype=torch.int32)
+    seg = torch.full((B, 1), end, dtype=torch.int32)
+    pad = None if pads is None else torch.tensor(pads, dtype=torch.int32)
+    cache = (K0.cuda(), V0.cuda(), pos0.cuda())
+    kind_g = G3.GEMMA3_LOCAL_SLIDING if w.attn_type == "local" else G3.GEMMA3_GLOBAL
+    got = G3.attention_forward_cached(
+        x.cuda(), seg.cuda(), None if pad is None else pad.cuda(), cache, end, dev["Wq"],
+        dev["Wkv"], dev["Wo"], dev["gamma_q"], dev["gamma_k"], H=w.H, H_kv=w.H_kv,
+        attn_type=kind_g, window=w.window, rope_base=w.rope_base, rope_scale=w.rope_scale,
+        query_scale=w.query_scale).cpu()
+    assert G3.gemma3_attn_check_status() == 0
+    ocache = {"k": K0.to(F64), "v": V0.to(F64), "pos": pos0.to(torch.int64)}
+    ref, ocache = O.attention_layer_cached(
+        x, seg, pad, ocache, end, p["Wq"], p["Wkv"], p["Wo"], p["gamma_q"], p["gamma_k"],
+        H=w.H, H_kv=w.H_kv, d_h=d_h, attn_type=Hh.oracle_type(w), window=w.window,
+        rope_base=w.rope_base, rope_scale=w.rope_scale, query_scale=w.query_scale)
+    Kc, Vc, pc = (t.cpu() for t in cache)
+    assert torch.equal(pc.to(torch.int64), ocache["pos"])
+    others = torch.ones(S, dtype=torch.bool)
+    others[end] = False
+    assert torch.equal(Kc[:, others], K0[:, others]) and torch.equal(Vc[:, others], V0[:, others])
+    for b in range(B):
+        if pad is not None and int(pad[b]) > 0:
+            assert torch.equal(got[b], torch.zeros_like(got[b]))
+            continue
+        Hh.assert_close(got[b], ref[b], f"decode step b={b}")
+        # the new slot: K' normalised and rotated, V as projected (fp16 storage)
+        assert (Kc[b, end].to(F64) - ocache["k"][b, end]).abs().max() <= Hh.QK_MAX_ABS
+        assert (Vc[b, end].to(F64) - ocache["v"][b, end]).abs().max() <= Hh.QK_MAX_ABS
+
+
 # ---------------------------------------------------------------- full size
 @pytest.mark.parametrize("name", ["4b_local_decode", "27b_global_decode"])
 def test_decode_workload_full_size(name):
