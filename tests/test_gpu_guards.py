@@ -62,10 +62,13 @@ LAYERS = [
          pad=("pad_uniform", 0, 120)),
     dict(B=2, T=260, D=384, H=4, H_kv=2, d_h=128, attn_type="global", window=0,
          rope_base=1e6, rope_scale=8.0, query_scale=168 ** -0.5, pad=("pad_uniform", 0, 100)),
+    # padding that fills whole 128-row tiles (the projections write them as zeros)
+    dict(B=3, T=512, D=256, H=4, H_kv=2, d_h=256, attn_type="local", window=100,
+         pad=("pad_uniform", 200, 512)),
 ]
 
 
-@pytest.mark.parametrize("kw", LAYERS, ids=["local-d256", "global-d128"])
+@pytest.mark.parametrize("kw", LAYERS, ids=["local-d256", "global-d128", "pad-tiles-d256"])
 def test_layer_writes_only_out_and_its_workspace(kw):
     import transformer_attention_gb300 as G3
     w = WL.small(WL.WORKLOADS["tiny_local"], name="guard", **kw)

@@ -96,22 +96,25 @@ cudaError_t project_qk(const void* x, long ldx, int act_dtype, const void* Wq, c
                        void* qbuf, void* kvbuf, const void* gamma_q, const void* gamma_k,
                        const int32_t* pos, int M, int D, int H, int H_kv, int d_h,
                        double rope_base, double rope_scale, float query_scale, cudaStream_t s,
-                       int* st, const CacheRows* cache = nullptr, bool* cache_done = nullptr) {
+                       int* st, const CacheRows* cache = nullptr, bool* cache_done = nullptr,
+                       const int32_t* pad_lens = nullptr, int seg_T = 0) {
   if (cache_done != nullptr) *cache_done = false;
   const int HD = H * d_h, KVD = H_kv * d_h;
   if (linear_qknorm_fusable(M, HD, HD, d_h) && linear_qknorm_fusable(M, 2 * KVD, KVD, d_h))
     return launch_qkv_qknorm(x, ldx, Wq, Wkv, D, qbuf, HD, kvbuf, 2 * KVD, M, HD, KVD, D, act_dtype,
                              gamma_q, gamma_k, pos, d_h, rope_base, rope_scale, query_scale, s,
-                             st);
+                             st, pad_lens, seg_T);
   cudaError_t e;
   if (M <= kSkinnyMaxRows) {
     // A decode step: both projections in one launch of the few-row kernel.
     e = launch_linear_skinny2(x, ldx, Wq, D, qbuf, HD, HD, Wkv, D, kvbuf, 2 * KVD, 2 * KVD, M, D,
                               act_dtype, kF16, s, st);
   } else {
-    e = launch_linear(x, ldx, Wq, D, qbuf, HD, M, HD, D, act_dtype, kF16, s, st, 0);
+    e = launch_linear(x, ldx, Wq, D, qbuf, HD, M, HD, D, act_dtype, kF16, s, st, 0, pad_lens,
+                      seg_T);
     if (e != cudaSuccess) return e;
-    e = launch_linear(x, ldx, Wkv, D, kvbuf, 2 * KVD, M, 2 * KVD, D, act_dtype, kF16, s, st, 0);
+    e = launch_linear(x, ldx, Wkv, D, kvbuf, 2 * KVD, M, 2 * KVD, D, act_dtype, kF16, s, st, 0,
+                      pad_lens, seg_T);
   }
   if (e != cudaSuccess) return e;
   e = launch_qk_norm_rope(qbuf, HD, kvbuf, 2 * KVD, gamma_q, gamma_k, pos, M, H, H_kv, d_h,
@@ -157,15 +160,19 @@ int attn_pipeline(const gemma3_attn_dims* d, const void* x, int act_dtype,
     Wkv = wkv;
     Wo = wo;
   }
+  // Tiles of pad rows only are skipped by both projections (their Q', K', V
+  // and output rows are zeros: no valid query or key reads them).
   e = project_qk(x, d->D, act_dtype, Wq, Wkv, qbuf, kvbuf, gamma_q, gamma_k, segment_pos, M,
-                 d->D, d->H, d->H_kv, d->d_h, rope_base, rope_scale, query_scale, s, st);
+                 d->D, d->H, d->H_kv, d->d_h, rope_base, rope_scale, query_scale, s, st, nullptr,
+                 nullptr, pad_lens, d->T);
   if (e != cudaSuccess) return GEMMA3_ERR_CUDA;
   const int win = attn_type == GEMMA3_LOCAL_SLIDING ? window : 0;
   e = launch_flash_attention(qbuf, kvbuf, static_cast<uint8_t*>(kvbuf) + KVD * 2, 2 * KVD, qbuf,
                              act_dtype, pad_lens, d->B, d->T, d->H, d->H_kv, d->d_h, win, sched, s,
                              st, /*sched_zeroed=*/true);
   if (e != cudaSuccess) return GEMMA3_ERR_CUDA;
-  e = launch_linear(qbuf, HD, Wo, HD, out, d->D, M, d->D, HD, act_dtype, out_dtype, s, st, 0);
+  e = launch_linear(qbuf, HD, Wo, HD, out, d->D, M, d->D, HD, act_dtype, out_dtype, s, st, 0,
+                    pad_lens, d->T);
   return to_status(e);
 }
 

@@ -75,6 +75,7 @@ __device__ __forceinline__ void tile_coords(int t, int m_units, int n_tiles, int
   nt = (g & 1) ? n_tiles - 1 - r / gm : r / gm;
 }
 constexpr uint32_t TMEM_COLS = 512;
+constexpr int kMaxPadSegs = 64;   // batch segments whose pad-only M tiles are skipped
 
 enum : int { kSiteEmpty = 1, kSiteFull = 2, kSiteAccEmpty = 3, kSiteAccFull = 4 };
 
@@ -123,7 +124,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     gemm_tn_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmB2,
                    const __grid_constant__ CUtensorMap tmC2, int M, int N, int K, int group_m,
-                   int* status, const __grid_constant__ QkEpi epi) {
+                   const int32_t* __restrict__ pad_lens, int seg_T, int* status,
+                   const __grid_constant__ QkEpi epi) {
   pdl_enter();
   constexpr bool GEGLU = EPI == kEpiGeglu;
   static_assert(EPI != kEpiQkNorm || (std::is_same<OutT, __half>::value && (DH == 128 || DH == 256)),
@@ -142,10 +144,49 @@ __global__ void __launch_bounds__(THREADS, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int m_tiles = (M + BM - 1) / BM, n_tiles = (N + BN_OUT - 1) / BN_OUT;
-  const int num_units = m_tiles * n_tiles;
   const int unit0 = blockIdx.x, unit_step = gridDim.x;
   const int num_kb = (K + BK - 1) / BK;
-  auto unit_coords = [&](int u, int& mt, int& nt) { tile_coords(u, m_tiles, n_tiles, group_m, mt, nt); };
+  // Rows of batch segments of seg_T rows with trailing padding (pad_lens):
+  // M tiles holding only pad rows are not computed; the epilogue writes them
+  // as zeros after the computed tiles.  pre_ne[b] / pre_z[b]: computed /
+  // zero M tiles of the segments before b.
+  __shared__ int pre_ne[kMaxPadSegs + 1], pre_z[kMaxPadSegs + 1];
+  const int n_seg = seg_T > 0 ? M / seg_T : 0;
+  const bool skip = pad_lens != nullptr && seg_T > 0 && seg_T % BM == 0 && M % seg_T == 0 &&
+                    n_seg <= kMaxPadSegs;
+  const int seg_tiles = skip ? seg_T / BM : 0;
+  if (skip && threadIdx.x == 0) {
+    pre_ne[0] = pre_z[0] = 0;
+    for (int b = 0; b < n_seg; ++b) {
+      const int valid = min(max(seg_T - pad_lens[b], 0), seg_T);
+      const int ne = (valid + BM - 1) / BM;
+      pre_ne[b + 1] = pre_ne[b] + ne;
+      pre_z[b + 1] = pre_z[b] + seg_tiles - ne;
+    }
+  }
+  __syncthreads();
+  const int m_units = skip ? pre_ne[n_seg] : m_tiles;   // computed M tiles
+  const int z_tiles = skip ? pre_z[n_seg] : 0;           // pad-only M tiles
+  const int num_units = m_units * n_tiles;
+  const int zero_units = z_tiles * n_tiles;
+  auto unit_coords = [&](int u, int& mt, int& nt) {
+    int cm;
+    tile_coords(u, m_units, n_tiles, group_m, cm, nt);
+    if (skip) {
+      int b = 0;
+      while (pre_ne[b + 1] <= cm) ++b;
+      cm = b * seg_tiles + (cm - pre_ne[b]);
+    }
+    mt = cm;
+  };
+  // zero unit z -> (pad-only M tile, N tile)
+  auto zero_coords = [&](int z, int& mt, int& nt) {
+    const int zm = z % z_tiles;
+    nt = z / z_tiles;
+    int b = 0;
+    while (pre_z[b + 1] <= zm) ++b;
+    mt = b * seg_tiles + (pre_ne[b + 1] - pre_ne[b]) + (zm - pre_z[b]);
+  };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -267,15 +308,21 @@ __global__ void __launch_bounds__(THREADS, 1)
     uint8_t* staging = smem + STAGES * STAGE_BYTES + q * 2 * STAGING_BYTES;
     int abuf = 0, nchunk = 0;
     uint32_t aphase = 0;
-    for (int u = unit0; u < num_units; u += unit_step) {
+    for (int u = unit0; u < num_units + zero_units; u += unit_step) {
+      const bool zero = u >= num_units;   // a pad-only tile: zeros, no accumulator
       int mt, nt;
-      unit_coords(u, mt, nt);
+      if (zero)
+        zero_coords(u - num_units, mt, nt);
+      else
+        unit_coords(u, mt, nt);
       const int m0 = mt * BM, n0 = nt * BN_OUT;
       const bool rows_in = m0 + q * 32 < M;   // this warp's 32 rows hold some of C
-      bool ok = mbar_wait(smem_u32(&accf_bar[abuf]), aphase, &abort_flag, status, kSiteAccFull);
-      ok = __all_sync(0xffffffffu, ok);
-      if (!ok) break;
-      tc_fence_after();
+      if (!zero) {
+        bool ok = mbar_wait(smem_u32(&accf_bar[abuf]), aphase, &abort_flag, status, kSiteAccFull);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        tc_fence_after();
+      }
       const uint32_t acc = tbase + lane_off + abuf * BN;
       const bool seg1 = epi.n1 > 0 && n0 >= epi.n1;     // second output segment
       const int col_off = seg1 ? epi.n1 : 0;              // its first global column
@@ -306,6 +353,26 @@ __global__ void __launch_bounds__(THREADS, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&acce_bar[abuf]));
       };
+      if (zero) {
+        for (int c = 0; c < BN_OUT / CW; ++c) {
+          const int col0 = n0 + c * CW;
+          if (col0 >= N) break;   // warp-uniform
+          uint8_t* buf = staging + (nchunk & 1) * STAGING_BYTES;
+          if (lane == 0 && nchunk >= 2) bulk_wait_group_read<1>();
+          __syncwarp();
+#pragma unroll
+          for (int v = 0; v < 8; ++v)
+            *reinterpret_cast<uint4*>(buf + lane * 128 + v * 16) = make_uint4(0u, 0u, 0u, 0u);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            if (rows_in) tma_store_2d(tcp, smem_u32(buf), col0 - col_off, m0 + q * 32);
+            bulk_commit_group();
+          }
+          ++nchunk;
+        }
+        continue;
+      }
       bool fused = false;
       if constexpr (EPI == kEpiQkNorm)   // warp-uniform
         fused = seg1 ? (n0 - col_off) < epi.n_norm2 : n0 < epi.n_norm;
@@ -506,7 +573,8 @@ template <int AB_BF16, typename OutT, int EPI = kEpiPlain, int DH = 0>
 cudaError_t launch_typed(const CUtensorMap& ta, const CUtensorMap& tb, void* C, long ldc, int M,
                          int N, int K, cudaStream_t stream, int* status, int max_ctas,
                          const QkEpi& epi = QkEpi{}, const CUtensorMap* tb2 = nullptr,
-                         void* C2 = nullptr, long ldc2 = 0) {
+                         void* C2 = nullptr, long ldc2 = 0, const int32_t* pad_lens = nullptr,
+                         int seg_T = 0) {
   constexpr bool GEGLU = EPI == kEpiGeglu;
   auto kern = gemm_tn_kernel<AB_BF16, OutT, EPI, DH>;
   // Output tile map: boxes of 32 rows x 128 bytes, 128-byte swizzle.
@@ -544,7 +612,8 @@ cudaError_t launch_typed(const CUtensorMap& ta, const CUtensorMap& tb, void* C, 
   }
   if (group_m > m_tiles) group_m = m_tiles;
   return launch_pdl(kern, dim3(grid), dim3(THREADS), SMEM_BYTES, stream, ta, tb, tc,
-                    tb2 != nullptr ? *tb2 : tb, tc2, M, N, K, group_m, status, epi);
+                    tb2 != nullptr ? *tb2 : tb, tc2, M, N, K, group_m, pad_lens, seg_T, status,
+                    epi);
 }
 
 bool encode_ab(CUtensorMap& ta, CUtensorMap& tb, const void* A, long lda, const void* W, long ldw,
@@ -565,7 +634,7 @@ bool encode_ab(CUtensorMap& ta, CUtensorMap& tb, const void* A, long lda, const 
 
 cudaError_t launch_linear(const void* A, long lda, const void* W, long ldw, void* C, long ldc,
                           int M, int N, int K, int in_dtype, int out_dtype, cudaStream_t stream,
-                          int* status, int max_ctas) {
+                          int* status, int max_ctas, const int32_t* pad_lens, int seg_T) {
   if (M <= 0 || N <= 0 || K <= 0) return cudaSuccess;
   if (in_dtype != kBF16 && in_dtype != kF16) return cudaErrorInvalidValue;
   if (M <= kSkinnyMaxRows)
@@ -576,12 +645,15 @@ cudaError_t launch_linear(const void* A, long lda, const void* W, long ldw, void
 #define G3_GEMM_OUT(AB)                                                                        \
   switch (out_dtype) {                                                                         \
     case kF32:                                                                                 \
-      return launch_typed<AB, float>(ta, tb, C, ldc, M, N, K, stream, status, max_ctas);      \
+      return launch_typed<AB, float>(ta, tb, C, ldc, M, N, K, stream, status, max_ctas, {},    \
+                                     nullptr, nullptr, 0, pad_lens, seg_T);                    \
     case kF16:                                                                                 \
-      return launch_typed<AB, __half>(ta, tb, C, ldc, M, N, K, stream, status, max_ctas);     \
+      return launch_typed<AB, __half>(ta, tb, C, ldc, M, N, K, stream, status, max_ctas, {},   \
+                                      nullptr, nullptr, 0, pad_lens, seg_T);                   \
     case kBF16:                                                                                \
       return launch_typed<AB, __nv_bfloat16>(ta, tb, C, ldc, M, N, K, stream, status,       \
-                                             max_ctas);                                        \
+                                             max_ctas, {}, nullptr, nullptr, 0, pad_lens,      \
+                                             seg_T);                                           \
     default: return cudaErrorInvalidValue;                                                     \
   }
   if (in_dtype == kBF16) {
@@ -612,7 +684,8 @@ cudaError_t launch_qkv_qknorm(const void* A, long lda, const void* Wq, const voi
                               void* Qout, long ldq, void* KVout, long ldkv, int M, int HD, int KVD,
                               int K, int in_dtype, const void* gamma_q, const void* gamma_k,
                               const int32_t* pos, int d_h, double rope_base, double rope_scale,
-                              float query_scale, cudaStream_t stream, int* status) {
+                              float query_scale, cudaStream_t stream, int* status,
+                              const int32_t* pad_lens, int seg_T) {
   if (M <= 0 || K <= 0) return cudaSuccess;
   if (in_dtype != kBF16 && in_dtype != kF16) return cudaErrorInvalidValue;
   if (!linear_qknorm_fusable(M, HD, HD, d_h) || !linear_qknorm_fusable(M, 2 * KVD, KVD, d_h))
@@ -634,7 +707,7 @@ cudaError_t launch_qkv_qknorm(const void* A, long lda, const void* Wq, const voi
   const int N = HD + 2 * KVD;
 #define G3_QKV(AB, DH_)                                                                        \
   return launch_typed<AB, __half, kEpiQkNorm, DH_>(ta, tb, Qout, ldq, M, N, K, stream, status, 0, \
-                                                   epi, &tb2, KVout, ldkv);
+                                                   epi, &tb2, KVout, ldkv, pad_lens, seg_T);
   if (in_dtype == kBF16) {
     if (d_h == 256) G3_QKV(1, 256)
     G3_QKV(1, 128)

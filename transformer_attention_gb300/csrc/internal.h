@@ -68,9 +68,13 @@ cudaError_t launch_pdl_cluster(void (*kern)(KArgs...), dim3 grid, dim3 block, si
 // C[M,N] = A[M,K] * W[N,K]^T, operands in in_dtype (bf16|f16), fp32
 // accumulation, C in out_dtype.  M <= kSkinnyMaxRows goes to
 // launch_linear_skinny, everything else to the tcgen05 GEMM.
+// With pad_lens, M = B * seg_T rows of B segments with trailing padding
+// (seg_T a multiple of 128): the 128-row tiles holding only pad rows are not
+// computed and their rows of C are written as zeros.
 cudaError_t launch_linear(const void* A, long lda, const void* W, long ldw, void* C, long ldc,
                           int M, int N, int K, int in_dtype, int out_dtype, cudaStream_t stream,
-                          int* status, int max_ctas);
+                          int* status, int max_ctas, const int32_t* pad_lens = nullptr,
+                          int seg_T = 0);
 
 // The same product for M <= kSkinnyMaxRows (bound by reading W from HBM):
 // W streamed by TMA into the 128-row side of the tcgen05 MMA, K split over
@@ -111,7 +115,8 @@ cudaError_t launch_qkv_qknorm(const void* A, long lda, const void* Wq, const voi
                               void* Qout, long ldq, void* KVout, long ldkv, int M, int HD, int KVD,
                               int K, int in_dtype, const void* gamma_q, const void* gamma_k,
                               const int32_t* pos, int d_h, double rope_base, double rope_scale,
-                              float query_scale, cudaStream_t stream, int* status);
+                              float query_scale, cudaStream_t stream, int* status,
+                              const int32_t* pad_lens = nullptr, int seg_T = 0);
 
 // Where a decode step's new K'/V rows also go: row m = b*T + t to slot
 // b*S + end + t of the fp16 caches Kc / Vc ([B, S, H_kv*d_h]), its position
