@@ -248,8 +248,12 @@ def run_gpu(args, world, rank, local, workload=None, quick=False):
     # per-kernel work of one step
     work = {"linear": 0.0, "attention": 0.0, "qk_norm_rope": 0.0, "rmsnorm": 0.0,
             "postnorm": 0.0}
+    # The attention projections count valid rows only (their 128-row tiles of
+    # padding alone are not computed); the feed-forward and read-out GEMMs
+    # run over every row.
+    Mv = int(sum(valids))
     for L in layers:
-        work["linear"] += sum(metrics.layer_gemm_flops(M, D, H, H_kv, d_h).values())
+        work["linear"] += sum(metrics.layer_gemm_flops(Mv, D, H, H_kv, d_h).values())
         work["attention"] += metrics.attention_flops(valids, H, d_h, L.window if
                                                      L.attn_type == G3.GEMMA3_LOCAL_SLIDING else 0)
         if not fused_qk:
@@ -322,15 +326,16 @@ def run_gpu(args, world, rank, local, workload=None, quick=False):
                 e = mark("linear")
                 G3.gemma3_qkv_proj_norm_rope(a_in, D, wq, wkv, qbuf, kvbuf, M, D, H, H_kv, d_h, act,
                                              L.p["gamma_q"], L.p["gamma_k"], pos, L.rope_base,
-                                             L.rope_scale, alpha)
+                                             L.rope_scale, alpha, pad_lens=pad, seg_T=w.T)
                 done("proj_qkv", e)
             else:
                 e = mark("linear")
-                G3.gemma3_linear(a_in, D, wq, D, qbuf, HD, M, HD, D, act, G3.GEMMA3_F16)
+                G3.gemma3_linear(a_in, D, wq, D, qbuf, HD, M, HD, D, act, G3.GEMMA3_F16,
+                                 pad_lens=pad, seg_T=w.T)
                 done("proj_q", e)
                 e = mark("linear")
                 G3.gemma3_linear(a_in, D, wkv, D, kvbuf, 2 * KVD, M, 2 * KVD, D, act,
-                                 G3.GEMMA3_F16)
+                                 G3.GEMMA3_F16, pad_lens=pad, seg_T=w.T)
                 done("proj_kv", e)
                 e = mark("qk_norm_rope")
                 G3.gemma3_qk_norm_rope(qbuf, HD, kvbuf, 2 * KVD, L.p["gamma_q"], L.p["gamma_k"],
@@ -343,7 +348,7 @@ def run_gpu(args, world, rank, local, workload=None, quick=False):
             done("attention", e)
             e = mark("linear")
             G3.gemma3_linear(qbuf, HD, wo, HD, out, D, M, D, HD, act,
-                             G3.GEMMA3_F32 if stack else G3.GEMMA3_BF16)
+                             G3.GEMMA3_F32 if stack else G3.GEMMA3_BF16, pad_lens=pad, seg_T=w.T)
             done("proj_o", e)
             if stack:
                 e = mark("postnorm")
@@ -458,7 +463,7 @@ def run_gpu(args, world, rank, local, workload=None, quick=False):
         elif k in work and work[k]:
             b["gbs"] = work[k] * args.steps / (ms / 1e3) / 1e9
         breakdown[k] = b
-    gf = metrics.layer_gemm_flops(M, D, H, H_kv, d_h)
+    gf = metrics.layer_gemm_flops(Mv, D, H, H_kv, d_h)
     if ffn:
         gf["ffn_geglu"] = 2.0 * M * (2 * w.d_ff) * D
         gf["ffn_down"] = 2.0 * M * D * w.d_ff
@@ -485,7 +490,10 @@ def run_gpu(args, world, rank, local, workload=None, quick=False):
                    "valid_tokens": int(tokens),
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "l2": "flushed before every timed step (256 MiB write, outside step events)",
-                   "operands": "bf16 projections, f16 attention operands, f32 accumulation"},
+                   "operands": "bf16 projections, f16 attention operands, f32 accumulation",
+                   "flops": ("attention over unmasked valid (t, s) pairs; attention "
+                             "projections over valid rows (pad-only 128-row tiles are not "
+                             "computed); feed-forward and read-out over all rows")},
         "attn_tflops": work["attention"] * args.steps / (kern_ms["attention"] / 1e3) / 1e12,
         "attn_frac_of_bf16_peak": (work["attention"] * args.steps / (kern_ms["attention"] / 1e3)
                                    / 1e12) / peaks["bf16_tflops"],
@@ -1061,13 +1069,13 @@ def host_cpu() -> dict:
 
 def algorithmic_flops(w, valids, M: int) -> float:
     """GEMM and attention FLOPs of a workload whose batch rows have the given
-    valid lengths (M rows through the GEMMs): every layer's projections,
-    attention over unmasked pairs, the feed-forward GEMMs of a block and the
-    model's read-out.  Stack layers are local but every sixth."""
+    valid lengths: every layer's projections over the valid rows, attention
+    over unmasked pairs, and over all M rows the feed-forward GEMMs of a block
+    and the model's read-out.  Stack layers are local but every sixth."""
     f = 0.0
     for layer in range(w.num_layers):
         local = (layer % 6 != 5) if w.attn_type == "stack" else w.attn_type == "local"
-        f += sum(metrics.layer_gemm_flops(M, w.D, w.H, w.H_kv, w.d_h).values())
+        f += sum(metrics.layer_gemm_flops(sum(valids), w.D, w.H, w.H_kv, w.d_h).values())
         f += metrics.attention_flops(valids, w.H, w.d_h, w.window if local else 0)
         if w.d_ff > 0:
             f += 2.0 * M * (2 * w.d_ff) * w.D + 2.0 * M * w.D * w.d_ff

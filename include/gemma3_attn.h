@@ -336,9 +336,16 @@ int gemma3_cached_attention(const void* Q, const void* K_cache, const void* V_ca
  * W fills the 128-row side of the tcgen05 MMA, the rows of A its 16-wide
  * side, and the K range of each 128-row tile of W is split over a cluster of
  * up to 8 CTAs whose fp32 partials are summed through distributed shared
- * memory (max_ctas is ignored there). */
+ * memory (max_ctas is ignored there).
+ * pad_lens NULL: every row is computed.  Else the M rows are M / seg_T
+ * segments of seg_T rows (M a multiple of seg_T) of which segment b's last
+ * pad_lens[b] are padding: when seg_T is a multiple of 128 (and M > 16),
+ * 128-row tiles that hold only pad rows are not computed and their rows of
+ * C are written as zeros (the rows an attention layer never reads); every
+ * other row is computed as without pad_lens. */
 int gemma3_linear(const void* A, long lda, const void* W, long ldw, void* C, long ldc, int M,
-                  int N, int K, int in_dtype, int out_dtype, int max_ctas, void* stream);
+                  int N, int K, int in_dtype, int out_dtype, int max_ctas,
+                  const int32_t* pad_lens, int seg_T, void* stream);
 
 /* Z[M, D_ff] fp16 = GELU_tanh(A Wg^T) * (A Wu^T), the gating projection of
  * the feed-forward with the GeGLU applied in the GEMM epilogue ([FB] How it
@@ -358,12 +365,14 @@ int gemma3_geglu(const void* A, long lda, const void* W_gating, long ldw, void* 
  * launch of the few-row kernel of gemma3_linear (H*d_h a multiple of 128)
  * followed by gemma3_qk_norm_rope; otherwise the two projections and
  * gemma3_qk_norm_rope.
- * Wq [H*d_h, D], Wkv [2, H_kv*d_h, D] and x in in_dtype; gamma bf16 [d_h]. */
+ * Wq [H*d_h, D], Wkv [2, H_kv*d_h, D] and x in in_dtype; gamma bf16 [d_h].
+ * pad_lens / seg_T as in gemma3_linear: pad-only 128-row tiles of the fused
+ * launch are written as zeros (Q', K' and V rows no valid query reads). */
 int gemma3_qkv_proj_norm_rope(const void* x, long ldx, const void* Wq, const void* Wkv, void* Q,
                               void* KV, int M, int D, int H, int H_kv, int d_h, int in_dtype,
                               const void* gamma_q, const void* gamma_k, const int32_t* pos,
                               double rope_base, double rope_scale, float query_scale,
-                              void* stream);
+                              const int32_t* pad_lens, int seg_T, void* stream);
 
 /* C[M, N] fp16 = A W^T with the attention prologue fused into the GEMM
  * epilogue (what gemma3_linear followed by gemma3_qk_norm_rope computes, but

@@ -135,6 +135,13 @@ def test_forward_rejects_bad_type_and_window(lib):
 
 
 def test_linear_rejects_misaligned(lib):
-    assert lib.gemma3_linear(4096 + 2, 64, 4096, 64, 4096, 64, 16, 16, 64, 0, 0, 0, None) == -2
-    assert lib.gemma3_linear(4096, 60, 4096, 64, 4096, 64, 16, 16, 64, 0, 0, 0, None) == -1
-    assert lib.gemma3_linear(4096, 64, 4096, 64, 4096, 64, 16, 16, 64, 2, 0, 0, None) == -1
+    assert lib.gemma3_linear(4096 + 2, 64, 4096, 64, 4096, 64, 16, 16, 64, 0, 0, 0, None, 0, None) == -2
+    assert lib.gemma3_linear(4096, 60, 4096, 64, 4096, 64, 16, 16, 64, 0, 0, 0, None, 0, None) == -1
+    assert lib.gemma3_linear(4096, 64, 4096, 64, 4096, 64, 16, 16, 64, 2, 0, 0, None, 0, None) == -1
+
+
+def test_linear_rejects_bad_pad_segments(lib):
+    # pad_lens given: the segment length must be >= 1 and divide M
+    args = (4096, 64, 4096, 64, 4096, 64, 16, 16, 64, 0, 0, 0, 4096)
+    assert lib.gemma3_linear(*args, 0, None) == -1
+    assert lib.gemma3_linear(*args, 5, None) == -1

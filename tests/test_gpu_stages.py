@@ -215,6 +215,62 @@ def test_qkv_proj_norm_rope_matches_oracle(M, D, d_h, H, H_kv, base, scale, alph
     assert rel_frob(kv[:, KVD:], O.project(x, Wkv[1])) <= 1e-3
 
 
+@pytest.mark.parametrize("out_dtype", ["bf16", "f32"])
+def test_linear_pad_only_tiles(out_dtype):
+    """Three segments of 384 rows with 0, 200 and 384 trailing pad rows: the
+    rows of pad-only 128-row tiles are zeros, every other row equals the
+    product without pad_lens bit for bit (the same tiles, the same k order)."""
+    import transformer_attention_gb300 as G3
+    T, pads = 384, [0, 200, 384]
+    M, N, K = T * len(pads), 640, 512
+    A = _randn((M, K), 60, 1.0).cuda()
+    W = _randn((N, K), 61, K ** -0.5).cuda()
+    dt, code = ((torch.bfloat16, G3.GEMMA3_BF16) if out_dtype == "bf16"
+                else (torch.float32, G3.GEMMA3_F32))
+    full = torch.empty((M, N), dtype=dt, device="cuda")
+    part = torch.full((M, N), float("nan"), dtype=dt, device="cuda")
+    G3.gemma3_linear(A, K, W, K, full, N, M, N, K, G3.GEMMA3_BF16, code)
+    G3.gemma3_linear(A, K, W, K, part, N, M, N, K, G3.GEMMA3_BF16, code,
+                     pad_lens=torch.tensor(pads, dtype=torch.int32, device="cuda"), seg_T=T)
+    assert G3.gemma3_attn_check_status() == 0
+    full, part = full.cpu(), part.cpu()
+    for b, pad in enumerate(pads):
+        kept = -(-(T - pad) // 128) * 128          # rows of the tiles holding a valid row
+        rows = slice(b * T, b * T + kept)
+        assert torch.equal(part[rows], full[rows])
+        assert torch.equal(part[b * T + kept:(b + 1) * T],
+                           torch.zeros_like(part[b * T + kept:(b + 1) * T]))
+
+
+def test_qkv_proj_pad_only_tiles():
+    """The fused Q|KV stage with pad_lens: Q', K', V rows of pad-only tiles are
+    zeros, the rest equal the call without pad_lens bit for bit."""
+    import transformer_attention_gb300 as G3
+    T, pads, D, d_h, H, H_kv = 256, [100, 256, 0], 256, 256, 2, 1
+    M, HD, KVD = T * len(pads), H * d_h, H_kv * d_h
+    x = _randn((M, D), 62, 1.0).cuda()
+    Wq = _randn((HD, D), 63, D ** -0.5).cuda()
+    Wkv = _randn((2, KVD, D), 64, D ** -0.5).cuda()
+    gq = _randn((d_h,), 65, 0.1 ** 0.5).cuda()
+    gk = _randn((d_h,), 66, 0.1 ** 0.5).cuda()
+    pos = torch.arange(M, dtype=torch.int32, device="cuda") % T
+    outs = []
+    for pl in (None, torch.tensor(pads, dtype=torch.int32, device="cuda")):
+        Qd = torch.full((M, HD), float("nan"), dtype=torch.float16, device="cuda")
+        KVd = torch.full((M, 2 * KVD), float("nan"), dtype=torch.float16, device="cuda")
+        G3.gemma3_qkv_proj_norm_rope(x, D, Wq, Wkv, Qd, KVd, M, D, H, H_kv, d_h, G3.GEMMA3_BF16,
+                                     gq, gk, pos, 1e4, 1.0, d_h ** -0.5, pad_lens=pl,
+                                     seg_T=T if pl is not None else 0)
+        assert G3.gemma3_attn_check_status() == 0
+        outs.append((Qd.cpu(), KVd.cpu()))
+    for full, part in zip(outs[0], outs[1]):
+        for b, pad in enumerate(pads):
+            kept = -(-(T - pad) // 128) * 128
+            assert torch.equal(part[b * T:b * T + kept], full[b * T:b * T + kept])
+            tail = part[b * T + kept:(b + 1) * T]
+            assert torch.equal(tail, torch.zeros_like(tail))
+
+
 def test_linear_qk_norm_rope_rejects_unaligned_heads():
     import transformer_attention_gb300 as G3
     x = torch.zeros((64, 64), dtype=torch.bfloat16, device="cuda")

@@ -97,11 +97,11 @@ SIGNATURES = {
     "gemma3_geglu": (c_int, [c_void_p, c_long, c_void_p, c_long, c_void_p, c_long, c_int, c_int,
                              c_int, c_int, c_void_p]),
     "gemma3_linear": (c_int, [c_void_p, c_long, c_void_p, c_long, c_void_p, c_long, c_int, c_int,
-                              c_int, c_int, c_int, c_int, c_void_p]),
+                              c_int, c_int, c_int, c_int, c_void_p, c_int, c_void_p]),
     "gemma3_qkv_proj_norm_rope": (c_int, [c_void_p, c_long, c_void_p, c_void_p, c_void_p,
                                           c_void_p, c_int, c_int, c_int, c_int, c_int, c_int,
                                           c_void_p, c_void_p, c_void_p, c_double, c_double,
-                                          c_float, c_void_p]),
+                                          c_float, c_void_p, c_int, c_void_p]),
     "gemma3_linear_qk_norm_rope": (c_int, [c_void_p, c_long, c_void_p, c_long, c_void_p, c_long,
                                            c_int, c_int, c_int, c_int, c_void_p, c_void_p, c_int,
                                            c_int, c_double, c_double, c_float, c_void_p]),
@@ -364,18 +364,19 @@ def gemma3_geglu(A, lda, W_gating, ldw, Z, ldz, M, D_ff, K, in_dtype, stream=Non
 
 
 def gemma3_linear(A, lda, W, ldw, C, ldc, M, N, K, in_dtype, out_dtype, max_ctas=0,
-                  stream=None):
+                  stream=None, pad_lens=None, seg_T=0):
     return _check("gemma3_linear", lib().gemma3_linear(
         _ptr(A), lda, _ptr(W), ldw, _ptr(C), ldc, M, N, K, in_dtype, out_dtype, max_ctas,
-        _stream(stream)))
+        _ptr(pad_lens), seg_T, _stream(stream)))
 
 
 def gemma3_qkv_proj_norm_rope(x, ldx, Wq, Wkv, Q, KV, M, D, H, H_kv, d_h, in_dtype, gamma_q,
-                              gamma_k, pos, rope_base, rope_scale, query_scale, stream=None):
+                              gamma_k, pos, rope_base, rope_scale, query_scale, stream=None,
+                              pad_lens=None, seg_T=0):
     return _check("gemma3_qkv_proj_norm_rope", lib().gemma3_qkv_proj_norm_rope(
         _ptr(x), ldx, _ptr(Wq), _ptr(Wkv), _ptr(Q), _ptr(KV), M, D, H, H_kv, d_h, in_dtype,
         _ptr(gamma_q), _ptr(gamma_k), _ptr(pos), rope_base, rope_scale, query_scale,
-        _stream(stream)))
+        _ptr(pad_lens), seg_T, _stream(stream)))
 
 
 def gemma3_linear_qk_norm_rope(A, lda, W, ldw, C, ldc, M, N, K, in_dtype, gamma, pos, d_h, n_norm,

@@ -778,8 +778,10 @@ int gemma3_geglu(const void* A, long lda, const void* W_gating, long ldw, void* 
 }
 
 int gemma3_linear(const void* A, long lda, const void* W, long ldw, void* C, long ldc, int M,
-                  int N, int K, int in_dtype, int out_dtype, int max_ctas, void* stream) {
+                  int N, int K, int in_dtype, int out_dtype, int max_ctas,
+                  const int32_t* pad_lens, int seg_T, void* stream) {
   if (!A || !W || !C || M < 0 || N < 0 || K < 1) return GEMMA3_ERR_INVALID_ARG;
+  if (pad_lens != nullptr && (seg_T < 1 || M % seg_T != 0)) return GEMMA3_ERR_INVALID_ARG;
   if (in_dtype != GEMMA3_BF16 && in_dtype != GEMMA3_F16) return GEMMA3_ERR_INVALID_ARG;
   if (out_dtype != GEMMA3_BF16 && out_dtype != GEMMA3_F16 && out_dtype != GEMMA3_F32)
     return GEMMA3_ERR_INVALID_ARG;
@@ -795,17 +797,18 @@ int gemma3_linear(const void* A, long lda, const void* W, long ldw, void* C, lon
   const int it = in_dtype == GEMMA3_F16 ? kF16 : kBF16;
   const int dt = out_dtype == GEMMA3_F32 ? kF32 : (out_dtype == GEMMA3_F16 ? kF16 : kBF16);
   return to_status(launch_linear(A, lda, W, ldw, C, ldc, M, N, K, it, dt, as_stream(stream), st,
-                                 max_ctas));
+                                 max_ctas, pad_lens, pad_lens != nullptr ? seg_T : 0));
 }
 
 int gemma3_qkv_proj_norm_rope(const void* x, long ldx, const void* Wq, const void* Wkv, void* Q,
                               void* KV, int M, int D, int H, int H_kv, int d_h, int in_dtype,
                               const void* gamma_q, const void* gamma_k, const int32_t* pos,
                               double rope_base, double rope_scale, float query_scale,
-                              void* stream) {
+                              const int32_t* pad_lens, int seg_T, void* stream) {
   if (!x || !Wq || !Wkv || !Q || !KV || !gamma_q || !gamma_k || !pos || M < 0 || D < 8 ||
       D % 8 || H < 1 || H_kv < 1)
     return GEMMA3_ERR_INVALID_ARG;
+  if (pad_lens != nullptr && (seg_T < 1 || M % seg_T != 0)) return GEMMA3_ERR_INVALID_ARG;
   if (d_h != 128 && d_h != 256) return GEMMA3_ERR_UNSUPPORTED;
   if (in_dtype != GEMMA3_BF16 && in_dtype != GEMMA3_F16) return GEMMA3_ERR_INVALID_ARG;
   if (ldx < D) return GEMMA3_ERR_INVALID_ARG;
@@ -819,7 +822,8 @@ int gemma3_qkv_proj_norm_rope(const void* x, long ldx, const void* Wq, const voi
   if (st == nullptr) return GEMMA3_ERR_CUDA;
   return to_status(project_qk(x, ldx, in_dtype == GEMMA3_F16 ? kF16 : kBF16, Wq, Wkv, Q, KV,
                               gamma_q, gamma_k, pos, M, D, H, H_kv, d_h, rope_base, rope_scale,
-                              query_scale, as_stream(stream), st));
+                              query_scale, as_stream(stream), st, nullptr, nullptr, pad_lens,
+                              pad_lens != nullptr ? seg_T : 0));
 }
 
 int gemma3_linear_qk_norm_rope(const void* A, long lda, const void* W, long ldw, void* C,
