@@ -259,8 +259,9 @@ def run_gpu(args, world, rank, local, workload=None, quick=False):
         if not fused_qk:
             work["qk_norm_rope"] += metrics.prologue_bytes(M, H, H_kv, d_h)
         if stack:
-            work["rmsnorm"] += metrics.rmsnorm_bytes(M, D, 4)
-            work["postnorm"] += metrics.postnorm_bytes(M, D, 4)
+            # the attention half's norms skip pad rows as its projections do
+            work["rmsnorm"] += metrics.rmsnorm_bytes(Mv, D, 4)
+            work["postnorm"] += metrics.postnorm_bytes(Mv, D, 4)
             work["cast"] = work.get("cast", 0.0) + (2 * HD * D + 2 * KVD * D) * 4.0
         if ffn:
             work["linear"] += 2.0 * M * (2 * w.d_ff) * D + 2.0 * M * D * w.d_ff
@@ -312,7 +313,8 @@ def run_gpu(args, world, rank, local, workload=None, quick=False):
                          else (resid, G3.GEMMA3_F32))
             if stack:
                 e = mark("rmsnorm")
-                G3.gemma3_rmsnorm(r_in, r_t, L.p["gamma_pre"], u, G3.GEMMA3_F16, M, D)
+                G3.gemma3_rmsnorm(r_in, r_t, L.p["gamma_pre"], u, G3.GEMMA3_F16, M, D,
+                                  pad_lens=pad, seg_T=w.T)
                 done("rmsnorm", e)
                 e = mark("cast")
                 G3.gemma3_cast_bf16_f16(wq, wq16, HD * D)
@@ -352,7 +354,8 @@ def run_gpu(args, world, rank, local, workload=None, quick=False):
             done("proj_o", e)
             if stack:
                 e = mark("postnorm")
-                G3.gemma3_postnorm_residual(out, r_in, r_t, L.p["gamma_post"], resid, M, D)
+                G3.gemma3_postnorm_residual(out, r_in, r_t, L.p["gamma_post"], resid, M, D,
+                                            pad_lens=pad, seg_T=w.T)
                 done("postnorm", e)
             if ffn:
                 # the feed-forward sandwich, in place on the fp32 residual stream
@@ -492,8 +495,9 @@ def run_gpu(args, world, rank, local, workload=None, quick=False):
                    "l2": "flushed before every timed step (256 MiB write, outside step events)",
                    "operands": "bf16 projections, f16 attention operands, f32 accumulation",
                    "flops": ("attention over unmasked valid (t, s) pairs; attention "
-                             "projections over valid rows (pad-only 128-row tiles are not "
-                             "computed); feed-forward and read-out over all rows")},
+                             "projections and the attention half's norms over valid rows "
+                             "(pad-only 128-row tiles are not computed); feed-forward and "
+                             "read-out over all rows")},
         "attn_tflops": work["attention"] * args.steps / (kern_ms["attention"] / 1e3) / 1e12,
         "attn_frac_of_bf16_peak": (work["attention"] * args.steps / (kern_ms["attention"] / 1e3)
                                    / 1e12) / peaks["bf16_tflops"],

@@ -418,14 +418,20 @@ int gemma3_flash_attention(const void* Q, const void* K, const void* V, long ldk
 
 /* u[m, :] = x[m, :] / sqrt(mean(x[m, :]^2) + 1e-6) * (1 + gamma)  ([FB] block
  * norms).  x [M, D] bf16 or fp32 (x_dtype), gamma [D] bf16, u [M, D] in
- * u_dtype (GEMMA3_BF16 | GEMMA3_F16). */
+ * u_dtype (GEMMA3_BF16 | GEMMA3_F16).  pad_lens / seg_T as in gemma3_linear
+ * (NULL: every row): rows of 128-row tiles that hold pad rows only (the
+ * tiles the projections skip; seg_T a multiple of 128) are not written. */
 int gemma3_rmsnorm(const void* x, int x_dtype, const void* gamma, void* u, int u_dtype, int M,
-                   int D, void* stream);
+                   int D, const int32_t* pad_lens, int seg_T, void* stream);
 
 /* y = x + RMSNorm(a) * (1 + gamma)  ([FB] post-attention norm + residual).
- * a [M, D] fp32, x [M, D] bf16|fp32, y [M, D] fp32 (may alias an fp32 x). */
+ * a [M, D] fp32, x [M, D] bf16|fp32, y [M, D] fp32 (may alias an fp32 x).
+ * pad_lens / seg_T as in gemma3_linear (NULL: every row): pad rows, where an
+ * attention layer's output a is zero, get y = x exactly without a being read
+ * (and are not written at all when y is x). */
 int gemma3_postnorm_residual(const float* a, const void* x, int x_dtype, const void* gamma,
-                             float* y, int M, int D, void* stream);
+                             float* y, int M, int D, const int32_t* pad_lens, int seg_T,
+                             void* stream);
 
 /* ------------------------------------------------------------------ status */
 

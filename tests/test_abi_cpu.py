@@ -140,6 +140,14 @@ def test_linear_rejects_misaligned(lib):
     assert lib.gemma3_linear(4096, 64, 4096, 64, 4096, 64, 16, 16, 64, 2, 0, 0, None, 0, None) == -1
 
 
+def test_norms_reject_bad_pad_segments(lib):
+    p = 4096
+    assert lib.gemma3_rmsnorm(p, 0, p, p, 1, 16, 64, p, 0, None) == -1
+    assert lib.gemma3_rmsnorm(p, 0, p, p, 1, 16, 64, p, 5, None) == -1
+    assert lib.gemma3_postnorm_residual(p, p, 0, p, p, 16, 64, p, 0, None) == -1
+    assert lib.gemma3_postnorm_residual(p, p, 0, p, p, 16, 64, p, 5, None) == -1
+
+
 def test_linear_rejects_bad_pad_segments(lib):
     # pad_lens given: the segment length must be >= 1 and divide M
     args = (4096, 64, 4096, 64, 4096, 64, 16, 16, 64, 0, 0, 0, 4096)

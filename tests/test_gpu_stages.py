@@ -404,3 +404,66 @@ def test_postnorm_residual_matches_oracle(M, D, x_t):
     assert G3.gemma3_attn_check_status() == 0
     ref = x.to(F64) + O.rms_norm(a, gamma)
     assert rel_frob(y.cpu(), ref) <= 1e-6
+
+
+PAD_NORM = [1152, 3840, 5376]   # the two-pass and both register-resident pre-norms
+
+
+@pytest.mark.parametrize("D", PAD_NORM)
+def test_rmsnorm_pad_tiles_untouched(D):
+    """With pad_lens the pre-norm leaves the rows of pad-only 128-row tiles
+    untouched and writes every other row as without pad_lens."""
+    import transformer_attention_gb300 as G3
+    T, pads = 384, [0, 200, 384]
+    M = T * len(pads)
+    x = _randn((M, D), 55, 3.0, torch.float32).cuda()
+    gamma = _randn((D,), 56, 0.1 ** 0.5).cuda()
+    full = torch.empty((M, D), dtype=torch.float16, device="cuda")
+    part = torch.full((M, D), float("nan"), dtype=torch.float16, device="cuda")
+    G3.gemma3_rmsnorm(x, G3.GEMMA3_F32, gamma, full, G3.GEMMA3_F16, M, D)
+    G3.gemma3_rmsnorm(x, G3.GEMMA3_F32, gamma, part, G3.GEMMA3_F16, M, D,
+                      pad_lens=torch.tensor(pads, dtype=torch.int32, device="cuda"), seg_T=T)
+    assert G3.gemma3_attn_check_status() == 0
+    full, part = full.cpu(), part.cpu()
+    for b, pad in enumerate(pads):
+        kept = -(-(T - pad) // 128) * 128
+        assert torch.equal(part[b * T:b * T + kept], full[b * T:b * T + kept])
+        assert bool(torch.isnan(part[b * T + kept:(b + 1) * T]).all())
+
+
+@pytest.mark.parametrize("D", [1152, 3840])
+@pytest.mark.parametrize("inplace", [True, False])
+def test_postnorm_pad_rows_pass_through(D, inplace):
+    """With pad_lens the pad rows get y = x exactly without a being read (a
+    holds NaN there), in place and not; valid rows as without pad_lens."""
+    import transformer_attention_gb300 as G3
+    T, pads = 256, [0, 100, 256]
+    M = T * len(pads)
+    valid = torch.ones(M, dtype=torch.bool)
+    for b, pad in enumerate(pads):
+        valid[b * T + T - pad:(b + 1) * T] = False
+    a = _randn((M, D), 57, 2.0, torch.float32)
+    a_nan = a.clone()
+    a_nan[~valid] = float("nan")
+    gamma = _randn((D,), 58, 0.1 ** 0.5).cuda()
+    pl = torch.tensor(pads, dtype=torch.int32, device="cuda")
+    if inplace:
+        x = _randn((M, D), 59, 1.0, torch.float32)
+        y_ref = x.clone().cuda()
+        y = x.clone().cuda()
+        G3.gemma3_postnorm_residual(a.cuda(), y_ref, G3.GEMMA3_F32, gamma, y_ref, M, D)
+        G3.gemma3_postnorm_residual(a_nan.cuda(), y, G3.GEMMA3_F32, gamma, y, M, D,
+                                    pad_lens=pl, seg_T=T)
+        x_f = x
+    else:
+        x = _randn((M, D), 59, 1.0, torch.bfloat16).cuda()
+        y_ref = torch.empty((M, D), dtype=torch.float32, device="cuda")
+        y = torch.full((M, D), float("nan"), dtype=torch.float32, device="cuda")
+        G3.gemma3_postnorm_residual(a.cuda(), x, G3.GEMMA3_BF16, gamma, y_ref, M, D)
+        G3.gemma3_postnorm_residual(a_nan.cuda(), x, G3.GEMMA3_BF16, gamma, y, M, D,
+                                    pad_lens=pl, seg_T=T)
+        x_f = x.cpu().float()
+    assert G3.gemma3_attn_check_status() == 0
+    y, y_ref = y.cpu(), y_ref.cpu()
+    assert torch.equal(y[valid], y_ref[valid])
+    assert torch.equal(y[~valid], x_f[~valid])

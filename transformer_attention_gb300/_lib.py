@@ -113,9 +113,9 @@ SIGNATURES = {
                                        c_void_p, c_int, c_int, c_int, c_int, c_int, c_int,
                                        c_void_p, c_void_p]),
     "gemma3_rmsnorm": (c_int, [c_void_p, c_int, c_void_p, c_void_p, c_int, c_int, c_int,
-                               c_void_p]),
+                               c_void_p, c_int, c_void_p]),
     "gemma3_postnorm_residual": (c_int, [c_void_p, c_void_p, c_int, c_void_p, c_void_p, c_int,
-                                         c_int, c_void_p]),
+                                         c_int, c_void_p, c_int, c_void_p]),
     "gemma3_attn_check_status": (c_int, [c_void_p]),
     "gemma3_last_device_status": (c_int, []),
     "gemma3_strerror": (ctypes.c_char_p, [c_int]),
@@ -407,14 +407,16 @@ def gemma3_flash_attention(Q, K, V, ldkv, O, o_dtype, pad_lens, B, T, H, H_kv, d
         window, _ptr(scratch), _stream(stream)))
 
 
-def gemma3_rmsnorm(x, x_dtype, gamma, u, u_dtype, M, D, stream=None):
+def gemma3_rmsnorm(x, x_dtype, gamma, u, u_dtype, M, D, stream=None, pad_lens=None, seg_T=0):
     return _check("gemma3_rmsnorm", lib().gemma3_rmsnorm(_ptr(x), x_dtype, _ptr(gamma), _ptr(u),
-                                                         u_dtype, M, D, _stream(stream)))
+                                                         u_dtype, M, D, _ptr(pad_lens), seg_T,
+                                                         _stream(stream)))
 
 
-def gemma3_postnorm_residual(a, x, x_dtype, gamma, y, M, D, stream=None):
+def gemma3_postnorm_residual(a, x, x_dtype, gamma, y, M, D, stream=None, pad_lens=None, seg_T=0):
     return _check("gemma3_postnorm_residual", lib().gemma3_postnorm_residual(
-        _ptr(a), _ptr(x), x_dtype, _ptr(gamma), _ptr(y), M, D, _stream(stream)))
+        _ptr(a), _ptr(x), x_dtype, _ptr(gamma), _ptr(y), M, D, _ptr(pad_lens), seg_T,
+        _stream(stream)))
 
 
 def gemma3_attn_check_status(stream=None) -> int:

@@ -374,12 +374,17 @@ int gemma3_block_attn_forward(const gemma3_attn_dims* dims, const void* x, int x
   float* a = reinterpret_cast<float*>(ws + a_ws + round_up(static_cast<size_t>(M) * dims->D * 2, 256));
   cudaStream_t s = as_stream(stream);
   const int xt = x_dtype == GEMMA3_F32 ? kF32 : kBF16;
-  if (launch_rmsnorm_rows(x, xt, gamma_pre, u, kF16, M, dims->D, s) != cudaSuccess)
+  // Pad rows: the pre-norm skips the tiles the projections skip, and the
+  // post-norm passes them through (their attention output is zero).
+  PadRows pad;
+  pad.pad_lens = pad_lens;
+  pad.seg_T = dims->T;
+  if (launch_rmsnorm_rows(x, xt, gamma_pre, u, kF16, M, dims->D, s, pad) != cudaSuccess)
     return GEMMA3_ERR_CUDA;
   rc = attn_pipeline(dims, u, kF16, segment_pos, pad_lens, Wq, Wkv, Wo, gamma_q, gamma_k,
                      attn_type, window, rope_base, rope_scale, query_scale, a, kF32, ws, s);
   if (rc != GEMMA3_OK) return rc;
-  return to_status(launch_postnorm_residual(a, x, xt, gamma_post, y, M, dims->D, s));
+  return to_status(launch_postnorm_residual(a, x, xt, gamma_post, y, M, dims->D, s, pad));
 }
 
 // ------------------------------------------------------------ feed-forward half
@@ -899,28 +904,37 @@ int gemma3_flash_attention(const void* Q, const void* K, const void* V, long ldk
 }
 
 int gemma3_rmsnorm(const void* x, int x_dtype, const void* gamma, void* u, int u_dtype, int M,
-                   int D, void* stream) {
+                   int D, const int32_t* pad_lens, int seg_T, void* stream) {
   if (!x || !gamma || !u || M < 0 || D < 4 || D % 4) return GEMMA3_ERR_INVALID_ARG;
+  if (pad_lens != nullptr && (seg_T < 1 || M % seg_T != 0)) return GEMMA3_ERR_INVALID_ARG;
   if (x_dtype != GEMMA3_BF16 && x_dtype != GEMMA3_F32) return GEMMA3_ERR_INVALID_ARG;
   if (u_dtype != GEMMA3_BF16 && u_dtype != GEMMA3_F16) return GEMMA3_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(gamma) || !aligned16(u)) return GEMMA3_ERR_MISALIGNED;
   int rc = check_device();
   if (rc != GEMMA3_OK) return rc;
+  PadRows pad;
+  pad.pad_lens = pad_lens;
+  pad.seg_T = seg_T;
   return to_status(launch_rmsnorm_rows(x, x_dtype == GEMMA3_F32 ? kF32 : kBF16, gamma, u,
                                        u_dtype == GEMMA3_F16 ? kF16 : kBF16, M, D,
-                                       as_stream(stream)));
+                                       as_stream(stream), pad));
 }
 
 int gemma3_postnorm_residual(const float* a, const void* x, int x_dtype, const void* gamma,
-                             float* y, int M, int D, void* stream) {
+                             float* y, int M, int D, const int32_t* pad_lens, int seg_T,
+                             void* stream) {
   if (!a || !x || !gamma || !y || M < 0 || D < 4 || D % 4) return GEMMA3_ERR_INVALID_ARG;
+  if (pad_lens != nullptr && (seg_T < 1 || M % seg_T != 0)) return GEMMA3_ERR_INVALID_ARG;
   if (x_dtype != GEMMA3_BF16 && x_dtype != GEMMA3_F32) return GEMMA3_ERR_INVALID_ARG;
   if (!aligned16(a) || !aligned16(x) || !aligned16(gamma) || !aligned16(y))
     return GEMMA3_ERR_MISALIGNED;
   int rc = check_device();
   if (rc != GEMMA3_OK) return rc;
+  PadRows pad;
+  pad.pad_lens = pad_lens;
+  pad.seg_T = seg_T;
   return to_status(launch_postnorm_residual(a, x, x_dtype == GEMMA3_F32 ? kF32 : kBF16, gamma, y,
-                                            M, D, as_stream(stream)));
+                                            M, D, as_stream(stream), pad));
 }
 
 int gemma3_attn_check_status(void* stream) {

@@ -180,15 +180,30 @@ template <> __device__ __forceinline__ float4 load4<__nv_bfloat16>(const __nv_bf
   return make_float4(a.x, a.y, b.x, b.y);
 }
 
+// Row m lies past its segment's valid length.
+__device__ __forceinline__ bool pad_row(const PadRows& p, int m) {
+  if (p.pad_lens == nullptr) return false;
+  const int b = m / p.seg_T, t = m - b * p.seg_T;
+  return t >= p.seg_T - p.pad_lens[b];
+}
+
+// Row m lies in a 128-row tile of its segment holding pad rows only (a tile
+// the projection GEMMs neither read nor compute).
+__device__ __forceinline__ bool pad_tile_row(const PadRows& p, int m) {
+  if (p.pad_lens == nullptr || p.seg_T % 128 != 0) return false;
+  const int b = m / p.seg_T, t = m - b * p.seg_T;
+  return (t & ~127) >= p.seg_T - p.pad_lens[b];
+}
+
 // u = RMSNorm(x) * (1 + gamma) -> bf16 or fp16, one warp per row, D % 4 == 0.
 template <typename T, bool OUT_F16>
 __global__ void __launch_bounds__(256)
     rmsnorm_rows_kernel(const T* __restrict__ x, const __nv_bfloat16* __restrict__ gamma,
-                        uint16_t* __restrict__ u, int M, int D) {
+                        uint16_t* __restrict__ u, int M, int D, PadRows pad) {
   pdl_enter();
   const int lane = threadIdx.x & 31;
   const int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  if (row >= M) return;
+  if (row >= M || pad_tile_row(pad, row)) return;
   const T* xr = x + static_cast<long>(row) * D;
   float ss = 0.f;
   for (int c = lane * 4; c < D; c += 128) {
@@ -222,11 +237,11 @@ __global__ void __launch_bounds__(256)
 template <typename T, bool OUT_F16, int NV>
 __global__ void __launch_bounds__(128)
     rmsnorm_rows_reg_kernel(const T* __restrict__ x, const __nv_bfloat16* __restrict__ gamma,
-                            uint16_t* __restrict__ u, int M, int D) {
+                            uint16_t* __restrict__ u, int M, int D, PadRows pad) {
   pdl_enter();
   const int lane = threadIdx.x & 31;
   const int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  if (row >= M) return;
+  if (row >= M || pad_tile_row(pad, row)) return;
   const T* xr = x + static_cast<long>(row) * D;
   float4 v[NV];
 #pragma unroll
@@ -280,15 +295,30 @@ __global__ void __launch_bounds__(256)
   }
 }
 
+// A pad row's y = x + RMSNorm(0) = x: copied (as fp32) unless y is x.
+template <typename T>
+__device__ __forceinline__ void pad_row_residual(const T* x, float* y, int row, int D, int lane,
+                                                 int inplace) {
+  if (inplace) return;
+  const T* xr = x + static_cast<long>(row) * D;
+  float* yr = y + static_cast<long>(row) * D;
+  for (int c = lane * 4; c < D; c += 128) *reinterpret_cast<float4*>(yr + c) = load4<T>(xr + c);
+}
+
 // y = x + RMSNorm(a) * (1 + gamma), one warp per row; y may alias x (f32).
 template <typename T>
 __global__ void __launch_bounds__(256)
     postnorm_residual_kernel(const float* __restrict__ a, const T* x,
-                             const __nv_bfloat16* __restrict__ gamma, float* y, int M, int D) {
+                             const __nv_bfloat16* __restrict__ gamma, float* y, int M, int D,
+                             PadRows pad, int inplace) {
   pdl_enter();
   const int lane = threadIdx.x & 31;
   const int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (row >= M) return;
+  if (pad_row(pad, row)) {
+    pad_row_residual(x, y, row, D, lane, inplace);
+    return;
+  }
   const float* ar = a + static_cast<long>(row) * D;
   float ss = 0.f;
   for (int c = lane * 4; c < D; c += 128) {
@@ -317,11 +347,16 @@ __global__ void __launch_bounds__(256)
 template <typename T, int NV>
 __global__ void __launch_bounds__(128)
     postnorm_residual_reg_kernel(const float* __restrict__ a, const T* x,
-                                 const __nv_bfloat16* __restrict__ gamma, float* y, int M, int D) {
+                                 const __nv_bfloat16* __restrict__ gamma, float* y, int M, int D,
+                                 PadRows pad, int inplace) {
   pdl_enter();
   const int lane = threadIdx.x & 31;
   const int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (row >= M) return;
+  if (pad_row(pad, row)) {
+    pad_row_residual(x, y, row, D, lane, inplace);
+    return;
+  }
   const float* ar = a + static_cast<long>(row) * D;
   float4 v[NV];
 #pragma unroll
@@ -378,25 +413,32 @@ inline dim3 row_grid(int M, int rows) { return dim3((M + rows - 1) / rows); }
 
 template <typename T, bool OUT_F16>
 cudaError_t launch_rms_typed(cudaStream_t s, const T* x, const __nv_bfloat16* g, uint16_t* u,
-                             int M, int D) {
+                             int M, int D, const PadRows& pad) {
   if (D > 2048 && D <= 4096)
     return launch_pdl(rmsnorm_rows_reg_kernel<T, OUT_F16, 32>, row_grid(M, 4), dim3(128), 0, s,
-                      x, g, u, M, D);
+                      x, g, u, M, D, pad);
   if (D > 4096 && D <= 6144)
     return launch_pdl(rmsnorm_rows_reg_kernel<T, OUT_F16, 48>, row_grid(M, 4), dim3(128), 0, s,
-                      x, g, u, M, D);
+                      x, g, u, M, D, pad);
   return launch_pdl(rmsnorm_rows_kernel<T, OUT_F16>, row_grid(M, 8), dim3(256), 0, s, x, g, u, M,
-                    D);
+                    D, pad);
 }
 
 template <typename T>
 cudaError_t launch_post_typed(cudaStream_t s, const float* a, const T* x, const __nv_bfloat16* g,
-                              float* y, int M, int D) {
+                              float* y, int M, int D, const PadRows& pad) {
+  const int inplace = static_cast<const void*>(x) == static_cast<const void*>(y) ? 1 : 0;
   if (D > 2048 && D <= 4096)
     return launch_pdl(postnorm_residual_reg_kernel<T, 32>, row_grid(M, 4), dim3(128), 0, s, a, x,
-                      g, y, M, D);
+                      g, y, M, D, pad, inplace);
   return launch_pdl(postnorm_residual_kernel<T>, row_grid(M, 8), dim3(256), 0, s, a, x, g, y, M,
-                    D);
+                    D, pad, inplace);
+}
+
+// Padding information is used only when the rows form whole segments.
+PadRows checked_pad(const PadRows& pad, int M) {
+  if (pad.pad_lens == nullptr || pad.seg_T < 1 || M % pad.seg_T != 0) return PadRows{};
+  return pad;
 }
 
 }  // namespace
@@ -442,21 +484,23 @@ cudaError_t launch_qk_norm_rope(void* Q, long ldq, void* K, long ldk, const void
 }
 
 cudaError_t launch_rmsnorm_rows(const void* x, int x_dtype, const void* gamma, void* u,
-                                int u_dtype, int M, int D, cudaStream_t stream) {
+                                int u_dtype, int M, int D, cudaStream_t stream,
+                                const PadRows& pad_in) {
   if (M <= 0) return cudaSuccess;
+  const PadRows pad = checked_pad(pad_in, M);
   auto g = static_cast<const __nv_bfloat16*>(gamma);
   auto uo = static_cast<uint16_t*>(u);
   if (u_dtype != kBF16 && u_dtype != kF16) return cudaErrorInvalidValue;
   const bool f16 = u_dtype == kF16;
   if (x_dtype == kF32) {
     auto xp = static_cast<const float*>(x);
-    return f16 ? launch_rms_typed<float, true>(stream, xp, g, uo, M, D)
-               : launch_rms_typed<float, false>(stream, xp, g, uo, M, D);
+    return f16 ? launch_rms_typed<float, true>(stream, xp, g, uo, M, D, pad)
+               : launch_rms_typed<float, false>(stream, xp, g, uo, M, D, pad);
   }
   if (x_dtype == kBF16) {
     auto xp = static_cast<const __nv_bfloat16*>(x);
-    return f16 ? launch_rms_typed<__nv_bfloat16, true>(stream, xp, g, uo, M, D)
-               : launch_rms_typed<__nv_bfloat16, false>(stream, xp, g, uo, M, D);
+    return f16 ? launch_rms_typed<__nv_bfloat16, true>(stream, xp, g, uo, M, D, pad)
+               : launch_rms_typed<__nv_bfloat16, false>(stream, xp, g, uo, M, D, pad);
   }
   return cudaErrorInvalidValue;
 }
@@ -519,14 +563,15 @@ cudaError_t launch_embed_rows(const int32_t* tokens, const void* E, int V, int D
 
 cudaError_t launch_postnorm_residual(const float* a, const void* x, int x_dtype,
                                      const void* gamma, float* y, int M, int D,
-                                     cudaStream_t stream) {
+                                     cudaStream_t stream, const PadRows& pad_in) {
   if (M <= 0) return cudaSuccess;
+  const PadRows pad = checked_pad(pad_in, M);
   auto g = static_cast<const __nv_bfloat16*>(gamma);
   if (x_dtype == kF32)
-    return launch_post_typed<float>(stream, a, static_cast<const float*>(x), g, y, M, D);
+    return launch_post_typed<float>(stream, a, static_cast<const float*>(x), g, y, M, D, pad);
   if (x_dtype == kBF16)
     return launch_post_typed<__nv_bfloat16>(stream, a, static_cast<const __nv_bfloat16*>(x), g, y,
-                                            M, D);
+                                            M, D, pad);
   return cudaErrorInvalidValue;
 }
 

@@ -166,10 +166,19 @@ cudaError_t launch_flash_attention_pair(const void* Q, const void* K, const void
                                         int T, int H, int H_kv, int window, void* sched,
                                         cudaStream_t stream, int* status, bool sched_zeroed);
 
+// Rows of M = B * seg_T in B segments of seg_T rows, segment b's last
+// pad_lens[b] rows padding (pad_lens null: no padding information).
+struct PadRows {
+  const int32_t* pad_lens = nullptr;
+  int seg_T = 0;
+};
+
 // u[m,:] = RMSNorm(x[m,:]) * (1 + gamma) over D, x in x_dtype (bf16|f32), u in
-// u_dtype (bf16|f16).
+// u_dtype (bf16|f16).  With `pad`, rows in 128-row tiles of pad rows alone
+// (seg_T a multiple of 128: the tiles the projections skip) are not written.
 cudaError_t launch_rmsnorm_rows(const void* x, int x_dtype, const void* gamma, void* u,
-                                int u_dtype, int M, int D, cudaStream_t stream);
+                                int u_dtype, int M, int D, cudaStream_t stream,
+                                const PadRows& pad = {});
 
 // dst[i] = src[i] converted bf16 -> f16 (round to nearest even), n elements.
 cudaError_t launch_cast_bf16_f16(const void* src, void* dst, size_t n, cudaStream_t stream);
@@ -180,9 +189,11 @@ cudaError_t launch_embed_rows(const int32_t* tokens, const void* E, int V, int D
                               float scale, float* x, cudaStream_t stream, int* status);
 
 // y[m,:] = x[m,:] + RMSNorm(a[m,:]) * (1 + gamma); a f32, x bf16|f32, y f32.
+// With `pad`, pad rows (whose a is zero, an attention layer's output there)
+// get y = x without reading a, and are left alone when y is x.
 cudaError_t launch_postnorm_residual(const float* a, const void* x, int x_dtype,
                                      const void* gamma, float* y, int M, int D,
-                                     cudaStream_t stream);
+                                     cudaStream_t stream, const PadRows& pad = {});
 
 // KV cache: copy the T new tokens' K' and V rows (KVD = H_kv*d_h fp16 each,
 // row (b, t) at K_rows/V_rows + (b*T + t)*ld) into slot end + t of the caches
