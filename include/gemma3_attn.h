@@ -340,9 +340,9 @@ int gemma3_cached_attention(const void* Q, const void* K_cache, const void* V_ca
  * pad_lens NULL: every row is computed.  Else the M rows are M / seg_T
  * segments of seg_T rows (M a multiple of seg_T) of which segment b's last
  * pad_lens[b] are padding: when seg_T is a multiple of 128 (and M > 16),
- * 128-row tiles that hold only pad rows are not computed and their rows of
- * C are written as zeros (the rows an attention layer never reads); every
- * other row is computed as without pad_lens. */
+ * 128-row tiles that hold only pad rows are neither computed nor written
+ * (rows an attention layer never reads); every other row is computed as
+ * without pad_lens. */
 int gemma3_linear(const void* A, long lda, const void* W, long ldw, void* C, long ldc, int M,
                   int N, int K, int in_dtype, int out_dtype, int max_ctas,
                   const int32_t* pad_lens, int seg_T, void* stream);
@@ -366,8 +366,11 @@ int gemma3_geglu(const void* A, long lda, const void* W_gating, long ldw, void* 
  * followed by gemma3_qk_norm_rope; otherwise the two projections and
  * gemma3_qk_norm_rope.
  * Wq [H*d_h, D], Wkv [2, H_kv*d_h, D] and x in in_dtype; gamma bf16 [d_h].
- * pad_lens / seg_T as in gemma3_linear: pad-only 128-row tiles of the fused
- * launch are written as zeros (Q', K' and V rows no valid query reads). */
+ * pad_lens / seg_T as in gemma3_linear: in pad-only 128-row tiles of the
+ * fused launch the V rows are written as zeros (the attention kernels may
+ * read a few of them at a tile edge, weighted by zero) and the Q' and K'
+ * rows are left unwritten (no valid query reads them; masked keys' scores
+ * are replaced, not weighted). */
 int gemma3_qkv_proj_norm_rope(const void* x, long ldx, const void* Wq, const void* Wkv, void* Q,
                               void* KV, int M, int D, int H, int H_kv, int d_h, int in_dtype,
                               const void* gamma_q, const void* gamma_k, const int32_t* pos,

@@ -110,11 +110,12 @@ cudaError_t project_qk(const void* x, long ldx, int act_dtype, const void* Wq, c
     e = launch_linear_skinny2(x, ldx, Wq, D, qbuf, HD, HD, Wkv, D, kvbuf, 2 * KVD, 2 * KVD, M, D,
                               act_dtype, kF16, s, st);
   } else {
+    // (pad-only tiles: V zeroed for the attention kernels' tile edges)
     e = launch_linear(x, ldx, Wq, D, qbuf, HD, M, HD, D, act_dtype, kF16, s, st, 0, pad_lens,
                       seg_T);
     if (e != cudaSuccess) return e;
     e = launch_linear(x, ldx, Wkv, D, kvbuf, 2 * KVD, M, 2 * KVD, D, act_dtype, kF16, s, st, 0,
-                      pad_lens, seg_T);
+                      pad_lens, seg_T, /*zero_pad_tiles=*/true);
   }
   if (e != cudaSuccess) return e;
   e = launch_qk_norm_rope(qbuf, HD, kvbuf, 2 * KVD, gamma_q, gamma_k, pos, M, H, H_kv, d_h,
@@ -133,7 +134,8 @@ int attn_pipeline(const gemma3_attn_dims* d, const void* x, int act_dtype,
                   const int32_t* segment_pos, const int32_t* pad_lens, const void* Wq,
                   const void* Wkv, const void* Wo, const void* gamma_q, const void* gamma_k,
                   int attn_type, int window, double rope_base, double rope_scale,
-                  float query_scale, void* out, int out_dtype, uint8_t* ws, cudaStream_t s) {
+                  float query_scale, void* out, int out_dtype, uint8_t* ws, cudaStream_t s,
+                  bool zero_pad_out) {
   int* st = status_ptr();
   if (st == nullptr) return GEMMA3_ERR_CUDA;
   const int M = d->B * d->T;
@@ -171,8 +173,10 @@ int attn_pipeline(const gemma3_attn_dims* d, const void* x, int act_dtype,
                              act_dtype, pad_lens, d->B, d->T, d->H, d->H_kv, d->d_h, win, sched, s,
                              st, /*sched_zeroed=*/true);
   if (e != cudaSuccess) return GEMMA3_ERR_CUDA;
+  // The layer's output has zero pad rows; a block's attention output is
+  // read only on valid rows (its post-norm passes pad rows through).
   e = launch_linear(qbuf, HD, Wo, HD, out, d->D, M, d->D, HD, act_dtype, out_dtype, s, st, 0,
-                    pad_lens, d->T);
+                    pad_lens, d->T, zero_pad_out);
   return to_status(e);
 }
 
@@ -338,7 +342,8 @@ int gemma3_attn_forward(const gemma3_attn_dims* dims, const void* x, const int32
   if (workspace_bytes < attn_ws(dims).total) return GEMMA3_ERR_WORKSPACE;
   return attn_pipeline(dims, x, kBF16, segment_pos, pad_lens, Wq, Wkv, Wo, gamma_q, gamma_k,
                        attn_type, window, rope_base, rope_scale, query_scale, out, kBF16,
-                       static_cast<uint8_t*>(workspace), as_stream(stream));
+                       static_cast<uint8_t*>(workspace), as_stream(stream),
+                       /*zero_pad_out=*/true);
 }
 
 int gemma3_block_attn_workspace_size(const gemma3_attn_dims* dims, size_t* bytes) {
@@ -382,7 +387,8 @@ int gemma3_block_attn_forward(const gemma3_attn_dims* dims, const void* x, int x
   if (launch_rmsnorm_rows(x, xt, gamma_pre, u, kF16, M, dims->D, s, pad) != cudaSuccess)
     return GEMMA3_ERR_CUDA;
   rc = attn_pipeline(dims, u, kF16, segment_pos, pad_lens, Wq, Wkv, Wo, gamma_q, gamma_k,
-                     attn_type, window, rope_base, rope_scale, query_scale, a, kF32, ws, s);
+                     attn_type, window, rope_base, rope_scale, query_scale, a, kF32, ws, s,
+                     /*zero_pad_out=*/false);
   if (rc != GEMMA3_OK) return rc;
   return to_status(launch_postnorm_residual(a, x, xt, gamma_post, y, M, dims->D, s, pad));
 }
@@ -1050,5 +1056,6 @@ extern "C" int gemma3_attn_forward_noalloc(const gemma3_attn_dims* dims, const v
   if (scratch == nullptr) return GEMMA3_ERR_CUDA;
   return attn_pipeline(dims, x, kBF16, segment_pos, pad_lens, Wq, Wkv, Wo, gamma_q, gamma_k,
                        attn_type, window, rope_base, rope_scale, query_scale, out, kBF16,
-                       static_cast<uint8_t*>(scratch), as_stream(stream));
+                       static_cast<uint8_t*>(scratch), as_stream(stream),
+                       /*zero_pad_out=*/true);
 }

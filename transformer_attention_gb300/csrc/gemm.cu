@@ -124,7 +124,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     gemm_tn_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmB2,
                    const __grid_constant__ CUtensorMap tmC2, int M, int N, int K, int group_m,
-                   const int32_t* __restrict__ pad_lens, int seg_T, int* status,
+                   const int32_t* __restrict__ pad_lens, int seg_T, int zero_from, int* status,
                    const __grid_constant__ QkEpi epi) {
   pdl_enter();
   constexpr bool GEGLU = EPI == kEpiGeglu;
@@ -147,9 +147,10 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int unit0 = blockIdx.x, unit_step = gridDim.x;
   const int num_kb = (K + BK - 1) / BK;
   // Rows of batch segments of seg_T rows with trailing padding (pad_lens):
-  // M tiles holding only pad rows are not computed; the epilogue writes them
-  // as zeros after the computed tiles.  pre_ne[b] / pre_z[b]: computed /
-  // zero M tiles of the segments before b.
+  // M tiles holding only pad rows are not computed; after the computed tiles
+  // the epilogue writes zeros in their N tiles from column zero_from on (a
+  // multiple of the tile width; N or more: none).  pre_ne[b] / pre_z[b]:
+  // computed / pad-only M tiles of the segments before b.
   __shared__ int pre_ne[kMaxPadSegs + 1], pre_z[kMaxPadSegs + 1];
   const int n_seg = seg_T > 0 ? M / seg_T : 0;
   const bool skip = pad_lens != nullptr && seg_T > 0 && seg_T % BM == 0 && M % seg_T == 0 &&
@@ -168,7 +169,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int m_units = skip ? pre_ne[n_seg] : m_tiles;   // computed M tiles
   const int z_tiles = skip ? pre_z[n_seg] : 0;           // pad-only M tiles
   const int num_units = m_units * n_tiles;
-  const int zero_units = z_tiles * n_tiles;
+  const int zn0 = zero_from < N ? zero_from / BN_OUT : n_tiles;   // first zeroed N tile
+  const int zero_units = z_tiles * (n_tiles - zn0);
   auto unit_coords = [&](int u, int& mt, int& nt) {
     int cm;
     tile_coords(u, m_units, n_tiles, group_m, cm, nt);
@@ -182,7 +184,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   // zero unit z -> (pad-only M tile, N tile)
   auto zero_coords = [&](int z, int& mt, int& nt) {
     const int zm = z % z_tiles;
-    nt = z / z_tiles;
+    nt = zn0 + z / z_tiles;
     int b = 0;
     while (pre_z[b + 1] <= zm) ++b;
     mt = b * seg_tiles + (pre_ne[b + 1] - pre_ne[b]) + (zm - pre_z[b]);
@@ -574,7 +576,7 @@ cudaError_t launch_typed(const CUtensorMap& ta, const CUtensorMap& tb, void* C, 
                          int N, int K, cudaStream_t stream, int* status, int max_ctas,
                          const QkEpi& epi = QkEpi{}, const CUtensorMap* tb2 = nullptr,
                          void* C2 = nullptr, long ldc2 = 0, const int32_t* pad_lens = nullptr,
-                         int seg_T = 0) {
+                         int seg_T = 0, int zero_from = 0) {
   constexpr bool GEGLU = EPI == kEpiGeglu;
   auto kern = gemm_tn_kernel<AB_BF16, OutT, EPI, DH>;
   // Output tile map: boxes of 32 rows x 128 bytes, 128-byte swizzle.
@@ -612,8 +614,8 @@ cudaError_t launch_typed(const CUtensorMap& ta, const CUtensorMap& tb, void* C, 
   }
   if (group_m > m_tiles) group_m = m_tiles;
   return launch_pdl(kern, dim3(grid), dim3(THREADS), SMEM_BYTES, stream, ta, tb, tc,
-                    tb2 != nullptr ? *tb2 : tb, tc2, M, N, K, group_m, pad_lens, seg_T, status,
-                    epi);
+                    tb2 != nullptr ? *tb2 : tb, tc2, M, N, K, group_m, pad_lens, seg_T, zero_from,
+                    status, epi);
 }
 
 bool encode_ab(CUtensorMap& ta, CUtensorMap& tb, const void* A, long lda, const void* W, long ldw,
@@ -634,7 +636,8 @@ bool encode_ab(CUtensorMap& ta, CUtensorMap& tb, const void* A, long lda, const 
 
 cudaError_t launch_linear(const void* A, long lda, const void* W, long ldw, void* C, long ldc,
                           int M, int N, int K, int in_dtype, int out_dtype, cudaStream_t stream,
-                          int* status, int max_ctas, const int32_t* pad_lens, int seg_T) {
+                          int* status, int max_ctas, const int32_t* pad_lens, int seg_T,
+                          bool zero_pad_tiles) {
   if (M <= 0 || N <= 0 || K <= 0) return cudaSuccess;
   if (in_dtype != kBF16 && in_dtype != kF16) return cudaErrorInvalidValue;
   if (M <= kSkinnyMaxRows)
@@ -642,18 +645,19 @@ cudaError_t launch_linear(const void* A, long lda, const void* W, long ldw, void
                                 status);
   CUtensorMap ta, tb;
   if (!encode_ab(ta, tb, A, lda, W, ldw, M, N, K, in_dtype, BN)) return cudaErrorInvalidValue;
+  const int zf = zero_pad_tiles ? 0 : N;   // zeros in every column of pad-only tiles, or none
 #define G3_GEMM_OUT(AB)                                                                        \
   switch (out_dtype) {                                                                         \
     case kF32:                                                                                 \
       return launch_typed<AB, float>(ta, tb, C, ldc, M, N, K, stream, status, max_ctas, {},    \
-                                     nullptr, nullptr, 0, pad_lens, seg_T);                    \
+                                     nullptr, nullptr, 0, pad_lens, seg_T, zf);                \
     case kF16:                                                                                 \
       return launch_typed<AB, __half>(ta, tb, C, ldc, M, N, K, stream, status, max_ctas, {},   \
-                                      nullptr, nullptr, 0, pad_lens, seg_T);                   \
+                                      nullptr, nullptr, 0, pad_lens, seg_T, zf);               \
     case kBF16:                                                                                \
       return launch_typed<AB, __nv_bfloat16>(ta, tb, C, ldc, M, N, K, stream, status,       \
                                              max_ctas, {}, nullptr, nullptr, 0, pad_lens,      \
-                                             seg_T);                                           \
+                                             seg_T, zf);                                       \
     default: return cudaErrorInvalidValue;                                                     \
   }
   if (in_dtype == kBF16) {
@@ -707,7 +711,8 @@ cudaError_t launch_qkv_qknorm(const void* A, long lda, const void* Wq, const voi
   const int N = HD + 2 * KVD;
 #define G3_QKV(AB, DH_)                                                                        \
   return launch_typed<AB, __half, kEpiQkNorm, DH_>(ta, tb, Qout, ldq, M, N, K, stream, status, 0, \
-                                                   epi, &tb2, KVout, ldkv, pad_lens, seg_T);
+                                                   epi, &tb2, KVout, ldkv, pad_lens, seg_T,    \
+                                                   HD + KVD);
   if (in_dtype == kBF16) {
     if (d_h == 256) G3_QKV(1, 256)
     G3_QKV(1, 128)

@@ -70,11 +70,12 @@ cudaError_t launch_pdl_cluster(void (*kern)(KArgs...), dim3 grid, dim3 block, si
 // launch_linear_skinny, everything else to the tcgen05 GEMM.
 // With pad_lens, M = B * seg_T rows of B segments with trailing padding
 // (seg_T a multiple of 128): the 128-row tiles holding only pad rows are not
-// computed and their rows of C are written as zeros.
+// computed, and their rows of C are written as zeros when zero_pad_tiles,
+// else left unwritten.
 cudaError_t launch_linear(const void* A, long lda, const void* W, long ldw, void* C, long ldc,
                           int M, int N, int K, int in_dtype, int out_dtype, cudaStream_t stream,
                           int* status, int max_ctas, const int32_t* pad_lens = nullptr,
-                          int seg_T = 0);
+                          int seg_T = 0, bool zero_pad_tiles = false);
 
 // The same product for M <= kSkinnyMaxRows (bound by reading W from HBM):
 // W streamed by TMA into the 128-row side of the tcgen05 MMA, K split over
