@@ -215,7 +215,8 @@ def run_gpu(args, world, rank, local, workload=None, quick=False):
     x_cpu = WL.x_full(w)
     x = x_cpu.to(dev)
     pos = WL.segment_pos(w).to(dev)
-    pad = pads.to(dev)
+    # pad_lens is passed only when the workload has padding (NULL: none)
+    pad = pads.to(dev) if w.pad[0] != "none" else None
     # the model around the blocks: token ids, embedding table, final norm, logits
     model = w.vocab > 0
     if model:
@@ -609,10 +610,11 @@ def run_e2e(args, w, api, x_cpu, pads, torch, G3, dev, world):
     NB = 2
     x_host = (WL.tokens(w) if model else x_cpu).pin_memory()
     pos_host = WL.segment_pos(w).pin_memory()
-    pad_host = pads.pin_memory()
+    pad_host = pads.pin_memory() if w.pad[0] != "none" else None
     x_d = [torch.empty_like(x_host, device=dev) for _ in range(NB)]
     pos_d = [torch.empty_like(pos_host, device=dev) for _ in range(NB)]
-    pad_d = [torch.empty_like(pad_host, device=dev) for _ in range(NB)]
+    pad_d = [torch.empty_like(pad_host, device=dev) if pad_host is not None else None
+             for _ in range(NB)]
     out_host = [torch.empty(api.out_shape, dtype=api.out_dtype, pin_memory=True)
                 for _ in range(NB)]
     y = [torch.empty(api.out_shape, dtype=api.out_dtype, device=dev) for _ in range(NB)]
@@ -637,7 +639,8 @@ def run_e2e(args, w, api, x_cpu, pads, torch, G3, dev, world):
                     s_in.wait_event(comp_done[k])          # slot k's inputs consumed
                 x_d[k].copy_(x_host, non_blocking=True)
                 pos_d[k].copy_(pos_host, non_blocking=True)
-                pad_d[k].copy_(pad_host, non_blocking=True)
+                if pad_host is not None:
+                    pad_d[k].copy_(pad_host, non_blocking=True)
                 h2d_done[k].record(s_in)
             s_c.wait_event(h2d_done[k])
             if i >= NB:
@@ -664,7 +667,8 @@ def run_e2e(args, w, api, x_cpu, pads, torch, G3, dev, world):
     assert G3.gemma3_attn_check_status() == 0
     valid = float(sum(w.T - int(p) for p in pads))
     value, _ = whole_job_value(valid * args.steps, total, world, dev)
-    h2d = x_host.numel() * x_host.element_size() + pos_host.numel() * 4 + pad_host.numel() * 4
+    h2d = (x_host.numel() * x_host.element_size() + pos_host.numel() * 4
+           + (pad_host.numel() * 4 if pad_host is not None else 0))
     d2h = out_host[0].numel() * out_host[0].element_size()
     return {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h,

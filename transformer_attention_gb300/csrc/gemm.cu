@@ -119,7 +119,7 @@ __device__ __forceinline__ float gelu_tanh_mul(float g, float u) {
 // 128 gate and the matching 128 up columns, and the epilogue writes
 // C[M, N] = GELU(A Wg^T) * (A Wu^T).
 // EPI = kEpiQkNorm (OutT = __half, DH = d_h): the attention prologue above.
-template <int AB_BF16, typename OutT, int EPI, int DH>
+template <int AB_BF16, typename OutT, int EPI, int DH, bool PAD>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_tn_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmB2,
@@ -153,43 +153,41 @@ __global__ void __launch_bounds__(THREADS, 1)
   // computed / pad-only M tiles of the segments before b.
   __shared__ int pre_ne[kMaxPadSegs + 1], pre_z[kMaxPadSegs + 1];
   const int n_seg = seg_T > 0 ? M / seg_T : 0;
-  const bool skip = pad_lens != nullptr && seg_T > 0 && seg_T % BM == 0 && M % seg_T == 0 &&
-                    n_seg <= kMaxPadSegs;
+  // (PAD false: an instantiation for calls without padding information, in
+  // which all of this folds away)
+  const bool skip = PAD && pad_lens != nullptr && seg_T > 0 && seg_T % BM == 0 &&
+                    M % seg_T == 0 && n_seg <= kMaxPadSegs;
   const int seg_tiles = skip ? seg_T / BM : 0;
-  if (skip && threadIdx.x == 0) {
-    pre_ne[0] = pre_z[0] = 0;
-    for (int b = 0; b < n_seg; ++b) {
-      const int valid = min(max(seg_T - pad_lens[b], 0), seg_T);
-      const int ne = (valid + BM - 1) / BM;
-      pre_ne[b + 1] = pre_ne[b] + ne;
-      pre_z[b + 1] = pre_z[b] + seg_tiles - ne;
+  if (skip && warp == 2) {
+    // Warp 2 (idle in this kernel) while warp 1 allocates TMEM: its lanes
+    // load 32 segments' pad counts at once and a warp scan forms the prefixes.
+    if (lane == 0) pre_ne[0] = pre_z[0] = 0;
+    int carry_ne = 0, carry_z = 0;
+    for (int b0 = 0; b0 < n_seg; b0 += 32) {
+      const int b = b0 + lane;
+      int ne = 0, z = 0;
+      if (b < n_seg) {
+        const int valid = min(max(seg_T - pad_lens[b], 0), seg_T);
+        ne = (valid + BM - 1) / BM;
+        z = seg_tiles - ne;
+      }
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int a = __shfl_up_sync(0xffffffffu, ne, o);
+        const int c = __shfl_up_sync(0xffffffffu, z, o);
+        if (lane >= o) {
+          ne += a;
+          z += c;
+        }
+      }
+      if (b < n_seg) {
+        pre_ne[b + 1] = carry_ne + ne;
+        pre_z[b + 1] = carry_z + z;
+      }
+      carry_ne += __shfl_sync(0xffffffffu, ne, 31);
+      carry_z += __shfl_sync(0xffffffffu, z, 31);
     }
   }
-  __syncthreads();
-  const int m_units = skip ? pre_ne[n_seg] : m_tiles;   // computed M tiles
-  const int z_tiles = skip ? pre_z[n_seg] : 0;           // pad-only M tiles
-  const int num_units = m_units * n_tiles;
-  const int zn0 = zero_from < N ? zero_from / BN_OUT : n_tiles;   // first zeroed N tile
-  const int zero_units = z_tiles * (n_tiles - zn0);
-  auto unit_coords = [&](int u, int& mt, int& nt) {
-    int cm;
-    tile_coords(u, m_units, n_tiles, group_m, cm, nt);
-    if (skip) {
-      int b = 0;
-      while (pre_ne[b + 1] <= cm) ++b;
-      cm = b * seg_tiles + (cm - pre_ne[b]);
-    }
-    mt = cm;
-  };
-  // zero unit z -> (pad-only M tile, N tile)
-  auto zero_coords = [&](int z, int& mt, int& nt) {
-    const int zm = z % z_tiles;
-    nt = zn0 + z / z_tiles;
-    int b = 0;
-    while (pre_z[b + 1] <= zm) ++b;
-    mt = b * seg_tiles + (pre_ne[b + 1] - pre_ne[b]) + (zm - pre_z[b]);
-  };
-
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(smem_u32(&full_bar[s]), 1);
@@ -217,6 +215,29 @@ __global__ void __launch_bounds__(THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = tmem_base_sh;
+  const int m_units = skip ? pre_ne[n_seg] : m_tiles;   // computed M tiles
+  const int z_tiles = skip ? pre_z[n_seg] : 0;           // pad-only M tiles
+  const int num_units = m_units * n_tiles;
+  const int zn0 = zero_from < N ? zero_from / BN_OUT : n_tiles;   // first zeroed N tile
+  const int zero_units = z_tiles * (n_tiles - zn0);
+  auto unit_coords = [&](int u, int& mt, int& nt) {
+    int cm;
+    tile_coords(u, m_units, n_tiles, group_m, cm, nt);
+    if (skip) {
+      int b = 0;
+      while (pre_ne[b + 1] <= cm) ++b;
+      cm = b * seg_tiles + (cm - pre_ne[b]);
+    }
+    mt = cm;
+  };
+  // zero unit z -> (pad-only M tile, N tile)
+  auto zero_coords = [&](int z, int& mt, int& nt) {
+    const int zm = z % z_tiles;
+    nt = zn0 + z / z_tiles;
+    int b = 0;
+    while (pre_z[b + 1] <= zm) ++b;
+    mt = b * seg_tiles + (pre_ne[b + 1] - pre_ne[b]) + (zm - pre_z[b]);
+  };
 
   if (warp == 0) {
     if (lane == 0) {
@@ -578,7 +599,8 @@ cudaError_t launch_typed(const CUtensorMap& ta, const CUtensorMap& tb, void* C, 
                          void* C2 = nullptr, long ldc2 = 0, const int32_t* pad_lens = nullptr,
                          int seg_T = 0, int zero_from = 0) {
   constexpr bool GEGLU = EPI == kEpiGeglu;
-  auto kern = gemm_tn_kernel<AB_BF16, OutT, EPI, DH>;
+  auto kern = pad_lens != nullptr ? gemm_tn_kernel<AB_BF16, OutT, EPI, DH, true>
+                                  : gemm_tn_kernel<AB_BF16, OutT, EPI, DH, false>;
   // Output tile map: boxes of 32 rows x 128 bytes, 128-byte swizzle.
   CUtensorMap tc;
   const CUtensorMapDataType cdt = sizeof(OutT) == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
