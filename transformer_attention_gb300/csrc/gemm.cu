@@ -20,8 +20,12 @@
 //               stores with a TMA bulk tensor store (full-line writes instead
 //               of 32 scattered 16-byte pieces per warp instruction).
 // Tiles are visited in groups of consecutive M tiles (N-tiles varying slowest
-// within a group), so the tiles in flight share A rows and W rows through
-// L2; weights larger than L2 get groups of ~20 MB of A.
+// within a group, in reverse on odd groups), so the tiles in flight share A
+// rows and W rows through L2; weights larger than L2 get groups of ~20 MB of
+// A.  Given the batch rows' trailing padding, M tiles of pad rows alone are
+// left out of that order (their rows are never read by the attention; the
+// epilogue writes zeros from a given column on where a later kernel reads
+// them).
 // Epilogue modes: plain conversion; GeGLU (the feed-forward gating
 // projection); and the attention prologue ("QK-Norm", How it works; "Gemma 3
 // Attention Block", How it works: QK-norm, then RoPE, then scale) applied to
