@@ -76,7 +76,7 @@ def test_default_workload_is_the_largest_single_gpu_layer():
     assert w.attn_type == "global" and w.rope_scale == 8.0
 
 
-def test_algorithmic_flops_of_the_survey_configs():
+def test_algorithmic_flops_of_the_4b_local_and_27b_global_layers():
     """Attention over unmasked pairs plus the projections, as tabulated for
     the 4B-local (0.541 + 2.062 TF) and 27B-global (140.7 + 17.3 TF) layers."""
     w = WL.WORKLOADS["4b_local"]
