@@ -454,18 +454,30 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (!need_mask) {
           mx = fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
         } else {
-          mask32(ra, 0 - c_lo, c_hi - c_lo);
-          mask32(rb, 32 - c_lo, c_hi - c_lo);
-          mask32(rc, 64 - c_lo, c_hi - c_lo);
-          mask32(rd, 96 - c_lo, c_hi - c_lo);
-          float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-          for (int c = 0; c < 32; ++c)
-            m4[c & 3] = fmax3(m4[c & 3],
-                              fmax3(__uint_as_float(ra[c]), __uint_as_float(rb[c]),
-                                    __uint_as_float(rc[c])),
-                              __uint_as_float(rd[c]));
-          mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+          // A 32-column chunk that every row of the warp sees whole keeps its
+          // values and the TMEM load's max; the others are masked column by
+          // column (a row's visible keys move by one every G rows, so most
+          // chunks of a warp are whole).
+#define G3_MASK_CHUNK(R, K, MK, OUT)                                              \
+  {                                                                               \
+    OUT = MK;                                                                     \
+    if (!__all_sync(0xffffffffu, c_lo <= 32 * (K) && c_hi >= 32 * (K) + 31)) {   \
+      mask32(R, 32 * (K) - c_lo, c_hi - c_lo);                                    \
+      float a_ = -INFINITY, b_ = -INFINITY;                                       \
+      _Pragma("unroll") for (int c = 0; c < 32; c += 2) {                         \
+        a_ = fmaxf(a_, __uint_as_float(R[c]));                                    \
+        b_ = fmaxf(b_, __uint_as_float(R[c + 1]));                                \
+      }                                                                           \
+      OUT = fmaxf(a_, b_);                                                        \
+    }                                                                             \
+  }
+          float x0, x1, x2, x3;
+          G3_MASK_CHUNK(ra, 0, m0, x0)
+          G3_MASK_CHUNK(rb, 1, m1, x1)
+          G3_MASK_CHUNK(rc, 2, m2, x2)
+          G3_MASK_CHUNK(rd, 3, m3, x3)
+#undef G3_MASK_CHUNK
+          mx = fmaxf(fmaxf(x0, x1), fmaxf(x2, x3));
         }
         mx *= LOG2E;
         const bool grow = mx > m_used + RESCALE_THRESHOLD;
