@@ -347,6 +347,16 @@ int gemma3_linear(const void* A, long lda, const void* W, long ldw, void* C, lon
                   int N, int K, int in_dtype, int out_dtype, int max_ctas,
                   const int32_t* pad_lens, int seg_T, void* stream);
 
+/* Rows per tile of the tcgen05 projection GEMM for later calls of this
+ * process (every entry point whose projections it runs): 0 = chosen per call
+ * (the default), 128, or 256.  A 256-row tile is two 128-row halves sharing
+ * each staged W tile, applied to plain and GeGLU outputs (outputs with the
+ * fused QK-norm/RoPE keep 128 rows); the results are bitwise the same either
+ * way, only the speed differs.  Returns the previous setting, or
+ * GEMMA3_ERR_INVALID_ARG for any other value.  A process-wide setting: not
+ * for threads that want different ones at once. */
+int gemma3_set_gemm_tile_rows(int rows);
+
 /* Z[M, D_ff] fp16 = GELU_tanh(A Wg^T) * (A Wu^T), the gating projection of
  * the feed-forward with the GeGLU applied in the GEMM epilogue ([FB] How it
  * works, MLP).  A [M, K] and W_gating [2*D_ff, K] (the (2, D_ff, K) weight

@@ -153,3 +153,12 @@ def test_linear_rejects_bad_pad_segments(lib):
     args = (4096, 64, 4096, 64, 4096, 64, 16, 16, 64, 0, 0, 0, 4096)
     assert lib.gemma3_linear(*args, 0, None) == -1
     assert lib.gemma3_linear(*args, 5, None) == -1
+
+
+def test_gemm_tile_rows_setting(lib):
+    # a host-side setting: each call returns the previous value, others are refused
+    assert lib.gemma3_set_gemm_tile_rows(256) == 0
+    assert lib.gemma3_set_gemm_tile_rows(128) == 256
+    assert lib.gemma3_set_gemm_tile_rows(0) == 128
+    assert lib.gemma3_set_gemm_tile_rows(192) == -1
+    assert lib.gemma3_set_gemm_tile_rows(0) == 0

@@ -6,7 +6,7 @@ larger allocation whose bytes before and after it hold a pattern, the call
 runs, and the pattern must be unchanged.  The workspace may be written only
 in the bytes the size query asked for; a cache only in the new tokens'
 slots; a strided output only in its rows' first N columns.  Inputs are checked to
-be left as they were.  Covered: the linear (few-row and tiled), one layer
+be left as they were.  Covered: the linear (few-row and tiled, 128- and 256-row tiles), one layer
 (local d_h = 256 and global d_h = 128, padded rows), the whole block, and a
 decode step and a prompt chunk over a cache (local and global).
 """
@@ -116,11 +116,13 @@ def test_block_writes_only_y_and_its_workspace():
     assert bool(torch.isfinite(y.view(torch.float32, (w.B, w.T, w.D))).all())
 
 
-@pytest.mark.parametrize("M", [2, 333])
+@pytest.mark.parametrize("M", [2, 333, 1400])
 @pytest.mark.parametrize("out_dtype", ["bf16", "f32"])
-def test_linear_writes_only_its_columns(M, out_dtype):
+@pytest.mark.parametrize("rows", [0, 256])
+def test_linear_writes_only_its_columns(M, out_dtype, rows):
     """C = A W^T into rows of stride ldc > N: the gap after each row's N
-    columns and the bytes around C keep their pattern (few-row and tiled)."""
+    columns and the bytes around C keep their pattern (few-row and tiled, on
+    the chosen tile height and on 256-row tiles)."""
     import transformer_attention_gb300 as G3
     N, K, ldc = 1096, 512, 1104
     g = torch.Generator().manual_seed(11)
@@ -130,8 +132,12 @@ def test_linear_writes_only_its_columns(M, out_dtype):
                 else (torch.float32, G3.GEMMA3_F32))
     esz = torch.tensor([], dtype=dt).element_size()
     C = Guarded(M * ldc * esz)
-    G3.gemma3_linear(A, K, W, K, C.inner, ldc, M, N, K, G3.GEMMA3_BF16, code)
-    assert G3.gemma3_attn_check_status() == 0
+    prev = G3.gemma3_set_gemm_tile_rows(rows)
+    try:
+        G3.gemma3_linear(A, K, W, K, C.inner, ldc, M, N, K, G3.GEMMA3_BF16, code)
+        assert G3.gemma3_attn_check_status() == 0
+    finally:
+        G3.gemma3_set_gemm_tile_rows(prev)
     assert C.guards_intact()
     rows = C.inner.view(torch.uint8).view(M, ldc * esz).cpu()
     assert bool((rows[:, N * esz:] == PATTERN).all())

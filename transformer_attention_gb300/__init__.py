@@ -19,7 +19,7 @@ from ._lib import (  # noqa: F401  (re-exported C-ABI names)
     gemma3_linear_qk_norm_rope, gemma3_qkv_proj_norm_rope, gemma3_embed, gemma3_model_forward, gemma3_model_workspace_size,
     GEMMA3_ERR_BAD_INPUT,
     gemma3_postnorm_residual, gemma3_qk_norm_rope, gemma3_query_scale, gemma3_rmsnorm,
-    gemma3_selftest_wait_timeout, lib)
+    gemma3_selftest_wait_timeout, gemma3_set_gemm_tile_rows, lib)
 
 __all__ = ["attention_forward", "attention_forward_cached", "block_attention_forward",
            "block_forward", "model_forward", "new_kv_cache", "linear", "lib"]

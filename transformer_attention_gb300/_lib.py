@@ -118,6 +118,7 @@ SIGNATURES = {
                                          c_int, c_void_p, c_int, c_void_p]),
     "gemma3_attn_check_status": (c_int, [c_void_p]),
     "gemma3_last_device_status": (c_int, []),
+    "gemma3_set_gemm_tile_rows": (c_int, [c_int]),
     "gemma3_strerror": (ctypes.c_char_p, [c_int]),
     "gemma3_selftest_wait_timeout": (c_int, [ctypes.c_longlong, c_void_p]),
 }
@@ -426,6 +427,12 @@ def gemma3_attn_check_status(stream=None) -> int:
 
 def gemma3_last_device_status() -> int:
     return lib().gemma3_last_device_status()
+
+
+def gemma3_set_gemm_tile_rows(rows: int) -> int:
+    """Rows per projection-GEMM tile for later calls (0 chosen per call, 128
+    or 256); returns the previous setting."""
+    return _check("gemma3_set_gemm_tile_rows", lib().gemma3_set_gemm_tile_rows(rows))
 
 
 def gemma3_selftest_wait_timeout(timeout_ns: int, stream=None) -> int:

@@ -788,6 +788,11 @@ int gemma3_geglu(const void* A, long lda, const void* W_gating, long ldw, void* 
                                 in_dtype == GEMMA3_F16 ? kF16 : kBF16, as_stream(stream), st));
 }
 
+int gemma3_set_gemm_tile_rows(int rows) {
+  const int prev = set_gemm_tile_rows(rows);
+  return prev < 0 ? GEMMA3_ERR_INVALID_ARG : prev;
+}
+
 int gemma3_linear(const void* A, long lda, const void* W, long ldw, void* C, long ldc, int M,
                   int N, int K, int in_dtype, int out_dtype, int max_ctas,
                   const int32_t* pad_lens, int seg_T, void* stream) {

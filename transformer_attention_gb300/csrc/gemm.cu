@@ -5,7 +5,7 @@
 // projection (O against Wo) of the attention layer ("Gemma 3 Attention
 // Block", How it works: Projections and the attn_vec_einsum).
 //
-// Design (one CTA per SM, persistent):
+// Design (one CTA per SM, persistent), for tiles of 128 x 256 ("one half"):
 //   warp 0      TMA producer: 128x64 A and 256x64 W tiles, 128-byte swizzle,
 //               into a 4-stage shared-memory ring (48 KB per stage).
 //   warp 1      allocates 512 TMEM columns and issues tcgen05.mma
@@ -19,6 +19,14 @@
 //               128-byte-swizzled shared-memory staging tile that one lane
 //               stores with a TMA bulk tensor store (full-line writes instead
 //               of 32 scattered 16-byte pieces per warp instruction).
+// Tiles of 256 x 256 ("two halves", plain outputs of large launches): each
+// stage holds two 128-row A tiles and one W tile (64 KB, 3 stages), both
+// halves' MMAs read the same W tile, and the halves' accumulators fill TMEM
+// (half h at column 256 h).  The epilogue drains half 0, then half 1; the
+// next tile's half-0 MMAs start as soon as half 0 is drained and its half-1
+// MMAs catch up on the held stages once half 1 is (the MMA issuer polls).
+// Both halves sum their k-steps in the same order as a one-half tile, so
+// the output is the same bit for bit.
 // Tiles are visited in groups of consecutive M tiles (N-tiles varying slowest
 // within a group, in reverse on odd groups), so the tiles in flight share A
 // rows and W rows through L2; weights larger than L2 get groups of ~20 MB of
@@ -34,6 +42,7 @@
 // (one row) sums the squares of its head, then rotates the pairs (c, c +
 // d_h/2) with (1 + gamma) and the query scale folded in.
 // Every mbarrier wait is bounded (see ptx.cuh).
+#include <atomic>
 #include <type_traits>
 
 #include "internal.h"
@@ -44,13 +53,27 @@ namespace g3 {
 
 namespace {
 
-constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4, THREADS = 256;
+constexpr int BM = 128, BN = 256, BK = 64, THREADS = 256;
 constexpr uint32_t A_BYTES = BM * BK * 2;   // 16 KB
 constexpr uint32_t B_BYTES = BN * BK * 2;   // 32 KB
-constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr uint32_t STAGING_BYTES = 32 * 128;           // one warp's 32 rows x 128 B
 constexpr uint32_t STAGING_TOTAL = 4 * 2 * STAGING_BYTES;   // 4 warps, double-buffered
-constexpr uint32_t SMEM_BYTES = STAGES * STAGE_BYTES + STAGING_TOTAL + 1024;
+// A tile is HALVES x 128 rows by 256 columns.  HALVES = 1: a stage holds one
+// A tile and one W tile (48 KB, four stages) and the accumulator is
+// double-buffered in TMEM.  HALVES = 2: a stage holds two A tiles and one W
+// tile (64 KB, three stages) and the two 128-row halves' accumulators fill
+// TMEM; each W byte brought into shared memory then feeds twice the MMA
+// work.  Measured on GB300 with the whole main loop issued twice per stage
+// (half the shared-memory fill per FLOP): the 4B and 27B projections ran at
+// an effective 2130-2140 TF/s against 1670-1690, so the one-tile main loop
+// waits on its operand copies rather than on the tensor core.
+template <int HALVES>
+struct Ring {
+  static constexpr int STAGES = HALVES == 2 ? 3 : 4;
+  static constexpr uint32_t STAGE_BYTES = HALVES * A_BYTES + B_BYTES;
+  static constexpr uint32_t SMEM_BYTES = STAGES * STAGE_BYTES + STAGING_TOTAL + 1024;
+};
+static_assert(Ring<2>::SMEM_BYTES + 1024 <= 232448, "two-half ring exceeds shared memory");
 // Rasterisation: tiles are visited in groups of consecutive M tiles, the N
 // tile varying slowest within a group, so a group's A rows stay in L2 while
 // W streams past them.  A weight that fits in L2 (up to kSmallWeightBytes)
@@ -123,7 +146,8 @@ __device__ __forceinline__ float gelu_tanh_mul(float g, float u) {
 // 128 gate and the matching 128 up columns, and the epilogue writes
 // C[M, N] = GELU(A Wg^T) * (A Wu^T).
 // EPI = kEpiQkNorm (OutT = __half, DH = d_h): the attention prologue above.
-template <int AB_BF16, typename OutT, int EPI, int DH, bool PAD>
+// HALVES: 128-row halves per tile (Ring).
+template <int AB_BF16, typename OutT, int EPI, int DH, bool PAD, int HALVES>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_tn_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmB2,
@@ -134,6 +158,11 @@ __global__ void __launch_bounds__(THREADS, 1)
   constexpr bool GEGLU = EPI == kEpiGeglu;
   static_assert(EPI != kEpiQkNorm || (std::is_same<OutT, __half>::value && (DH == 128 || DH == 256)),
                 "the QK-norm epilogue writes fp16 head vectors of 128 or 256");
+  // The fused prologue's epilogue is as long as a short main loop, which two
+  // halves sharing TMEM could not hide: it keeps one-half tiles.
+  static_assert(HALVES == 1 || (HALVES == 2 && EPI != kEpiQkNorm), "two halves: plain or GeGLU");
+  constexpr int STAGES = Ring<HALVES>::STAGES;
+  constexpr uint32_t STAGE_BYTES = Ring<HALVES>::STAGE_BYTES;
   constexpr int BN_OUT = GEGLU ? BN / 2 : BN;   // output columns per tile
   constexpr int CW = 128 / static_cast<int>(sizeof(OutT));   // output columns per 128 B chunk
   // A kernel launched after an earlier one gave up does no work.
@@ -219,25 +248,37 @@ __global__ void __launch_bounds__(THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = tmem_base_sh;
-  const int m_units = skip ? pre_ne[n_seg] : m_tiles;   // computed M tiles
+  const int m_units = skip ? pre_ne[n_seg] : m_tiles;   // computed 128-row M tiles
   const int z_tiles = skip ? pre_z[n_seg] : 0;           // pad-only M tiles
-  const int num_units = m_units * n_tiles;
+  const int mu_units = (m_units + HALVES - 1) / HALVES;  // tile rows of HALVES of them
+  const int num_units = mu_units * n_tiles;
   const int zn0 = zero_from < N ? zero_from / BN_OUT : n_tiles;   // first zeroed N tile
   const int zero_units = z_tiles * (n_tiles - zn0);
-  auto unit_coords = [&](int u, int& mt, int& nt) {
-    int cm;
-    tile_coords(u, m_units, n_tiles, group_m, cm, nt);
-    if (skip) {
-      int b = 0;
-      while (pre_ne[b + 1] <= cm) ++b;
-      cm = b * seg_tiles + (cm - pre_ne[b]);
+  // unit u -> the M tile of each half (-1: past the last computed tile) and
+  // the N tile
+  auto unit_coords = [&](int u, int (&mt)[HALVES], int& nt) {
+    int cu;
+    tile_coords(u, mu_units, n_tiles, group_m, cu, nt);
+#pragma unroll
+    for (int h = 0; h < HALVES; ++h) {
+      int cm = cu * HALVES + h;
+      if (cm >= m_units) {
+        mt[h] = -1;
+        continue;
+      }
+      if (skip) {
+        int b = 0;
+        while (pre_ne[b + 1] <= cm) ++b;
+        cm = b * seg_tiles + (cm - pre_ne[b]);
+      }
+      mt[h] = cm;
     }
-    mt = cm;
   };
   // zero unit z -> (pad-only M tile, N tile)
   auto zero_coords = [&](int z, int& mt, int& nt) {
-    const int zm = z % z_tiles;
-    nt = zn0 + z / z_tiles;
+    const int zt = z_tiles > 0 ? z_tiles : 1;   // (no zero units without pad-only tiles)
+    const int zm = z % zt;
+    nt = zn0 + z / zt;
     int b = 0;
     while (pre_z[b + 1] <= zm) ++b;
     mt = b * seg_tiles + (pre_ne[b + 1] - pre_ne[b]) + (zm - pre_z[b]);
@@ -251,9 +292,13 @@ __global__ void __launch_bounds__(THREADS, 1)
       int fills[STAGES] = {};
       bool ok = true;
       for (int u = unit0; ok && u < num_units; u += unit_step) {
-        int mt, nt;
+        int mt[HALVES], nt;
         unit_coords(u, mt, nt);
-        const int m0 = mt * BM, n0 = nt * BN_OUT;
+        const int n0 = nt * BN_OUT;
+        uint32_t bytes = B_BYTES;
+#pragma unroll
+        for (int h = 0; h < HALVES; ++h)
+          if (mt[h] >= 0) bytes += A_BYTES;
         for (int kb = 0; kb < num_kb; ++kb) {
           if (!mbar_wait(smem_u32(&empty_bar[stage]), phase ^ 1, &abort_flag, status, kSiteEmpty)) {
             ok = false;
@@ -261,16 +306,19 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
           const uint32_t fb = smem_u32(&full_bar[stage]);
           uint8_t* sa = smem + stage * STAGE_BYTES;
-          mbar_arrive_expect_tx(fb, STAGE_BYTES);
-          tma_load_2d(smem_u32(sa), &tmA, fb, kb * BK, m0);
+          uint8_t* sb = sa + HALVES * A_BYTES;   // the W tile follows the A tiles
+          mbar_arrive_expect_tx(fb, bytes);
+#pragma unroll
+          for (int h = 0; h < HALVES; ++h)
+            if (mt[h] >= 0) tma_load_2d(smem_u32(sa + h * A_BYTES), &tmA, fb, kb * BK, mt[h] * BM);
           if constexpr (GEGLU) {
             // gate rows n0.. into the first 128 B-tile rows, up rows N + n0.. after them
-            tma_load_2d(smem_u32(sa + A_BYTES), &tmB, fb, kb * BK, n0);
-            tma_load_2d(smem_u32(sa + A_BYTES + B_BYTES / 2), &tmB, fb, kb * BK, N + n0);
+            tma_load_2d(smem_u32(sb), &tmB, fb, kb * BK, n0);
+            tma_load_2d(smem_u32(sb + B_BYTES / 2), &tmB, fb, kb * BK, N + n0);
           } else if (epi.n1 > 0 && n0 >= epi.n1) {
-            tma_load_2d(smem_u32(sa + A_BYTES), &tmB2, fb, kb * BK, n0 - epi.n1);
+            tma_load_2d(smem_u32(sb), &tmB2, fb, kb * BK, n0 - epi.n1);
           } else {
-            tma_load_2d(smem_u32(sa + A_BYTES), &tmB, fb, kb * BK, n0);
+            tma_load_2d(smem_u32(sb), &tmB, fb, kb * BK, n0);
           }
           ++fills[stage];
           if (++stage == STAGES) { stage = 0; phase ^= 1; }
@@ -290,40 +338,127 @@ __global__ void __launch_bounds__(THREADS, 1)
     const uint32_t idesc_half = idesc_f16(BM, BN / 2, AB_BF16, 0, 0);
     int stage = 0;
     uint32_t phase = 0;
-    int abuf = 0;
-    uint32_t aphase = 0;
     bool ok = true;
-    for (int u = unit0; ok && u < num_units; u += unit_step) {
-      if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&acce_bar[abuf]), aphase ^ 1, &abort_flag,
-                                             status, kSiteAccEmpty)))
-        break;
-      tc_fence_after();
-      const uint32_t d_tmem = tbase + abuf * BN;
-      int mt_u, nt_u;
-      unit_coords(u, mt_u, nt_u);
-      const uint32_t idesc =
-          (EPI == kEpiPlain && N - nt_u * BN_OUT <= BN / 2) ? idesc_half : idesc_full;
-      for (int kb = 0; kb < num_kb; ++kb) {
-        if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&full_bar[stage]), phase, &abort_flag,
-                                               status, kSiteFull))) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t a_addr = smem_u32(smem + stage * STAGE_BYTES);
-        const uint32_t b_addr = a_addr + A_BYTES;
+    // the four K=16 MMAs of one 64-deep stage into accumulator d
+    auto mma_stage = [&](uint32_t d, uint32_t a_addr, uint32_t b_addr, uint32_t idesc, int kb) {
 #pragma unroll
-        for (int k = 0; k < BK / 16; ++k) {
-          mma_ss_lead(lead, d_tmem, sdesc_sw128(a_addr + k * 32, 16, 1024),
-                      sdesc_sw128(b_addr + k * 32, 16, 1024), idesc, (kb | k) != 0);
+      for (int k = 0; k < BK / 16; ++k)
+        mma_ss_lead(lead, d, sdesc_sw128(a_addr + k * 32, 16, 1024),
+                    sdesc_sw128(b_addr + k * 32, 16, 1024), idesc, (kb | k) != 0);
+    };
+    if constexpr (HALVES == 1) {
+      int abuf = 0;
+      uint32_t aphase = 0;
+      for (int u = unit0; ok && u < num_units; u += unit_step) {
+        if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&acce_bar[abuf]), aphase ^ 1, &abort_flag,
+                                               status, kSiteAccEmpty)))
+          break;
+        tc_fence_after();
+        const uint32_t d_tmem = tbase + abuf * BN;
+        int mt_u[1], nt_u;
+        unit_coords(u, mt_u, nt_u);
+        const uint32_t idesc =
+            (EPI == kEpiPlain && N - nt_u * BN_OUT <= BN / 2) ? idesc_half : idesc_full;
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&full_bar[stage]), phase, &abort_flag,
+                                                 status, kSiteFull))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_addr = smem_u32(smem + stage * STAGE_BYTES);
+          mma_stage(d_tmem, a_addr, a_addr + A_BYTES, idesc, kb);
+          mma_commit_lead(lead, smem_u32(&empty_bar[stage]));
+          if (++stage == STAGES) { stage = 0; phase ^= 1; }
         }
-        mma_commit_lead(lead, smem_u32(&empty_bar[stage]));
-        if (++stage == STAGES) { stage = 0; phase ^= 1; }
+        if (!ok) break;
+        mma_commit_lead(lead, smem_u32(&accf_bar[abuf]));
+        abuf ^= 1;
+        if (abuf == 0) aphase ^= 1;
       }
-      if (!ok) break;
-      mma_commit_lead(lead, smem_u32(&accf_bar[abuf]));
-      abuf ^= 1;
-      if (abuf == 0) aphase ^= 1;
+    } else {
+      // Two halves: half h accumulates at TMEM column h * BN.  A tile's
+      // half-0 MMAs start once the epilogue has drained half 0 of the tile
+      // before; its half-1 MMAs start once half 1 is drained too.  Until
+      // then each stage stays held after its half-0 MMAs (at most all but
+      // one, so the producer can still fill the next), and the held stages
+      // get their half-1 MMAs, oldest first, as soon as half 1 is free.
+      uint32_t tpar = 0;   // parity of this tile's accumulator phases
+      for (int u = unit0; ok && u < num_units; u += unit_step) {
+        int mt_u[HALVES], nt_u;
+        unit_coords(u, mt_u, nt_u);
+        const bool two = mt_u[1] >= 0;   // the unit's second half holds rows
+        const uint32_t idesc =
+            (EPI == kEpiPlain && N - nt_u * BN_OUT <= BN / 2) ? idesc_half : idesc_full;
+        if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&acce_bar[0]), tpar ^ 1, &abort_flag,
+                                               status, kSiteAccEmpty)))
+          break;
+        tc_fence_after();
+        bool have1 = false;        // half 1's accumulator is free for this tile
+        int held = 0, hs0 = 0, hkb0 = 0;   // held stages: count, first slot, its k block
+        auto catch_up = [&]() {
+          for (int i = 0; i < held; ++i) {
+            int s = hs0 + i;
+            if (s >= STAGES) s -= STAGES;
+            const uint32_t a_addr = smem_u32(smem + s * STAGE_BYTES);
+            mma_stage(tbase + BN, a_addr + A_BYTES, a_addr + 2 * A_BYTES, idesc, hkb0 + i);
+            mma_commit_lead(lead, smem_u32(&empty_bar[s]));
+          }
+          held = 0;
+        };
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&full_bar[stage]), phase, &abort_flag,
+                                                 status, kSiteFull))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_addr = smem_u32(smem + stage * STAGE_BYTES);
+          const uint32_t b_addr = a_addr + 2 * A_BYTES;
+          mma_stage(tbase, a_addr, b_addr, idesc, kb);
+          if (two && !have1) {
+            if (held + 1 >= STAGES) {
+              // every stage would be held: wait for half 1
+              if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&acce_bar[1]), tpar ^ 1,
+                                                     &abort_flag, status, kSiteAccEmpty))) {
+                ok = false;
+                break;
+              }
+              have1 = true;
+            } else {
+              have1 = __shfl_sync(0xffffffffu,
+                                  mbar_test(smem_u32(&acce_bar[1]), tpar ^ 1) ? 1 : 0, 0) != 0;
+            }
+            if (have1) {
+              tc_fence_after();
+              catch_up();
+            }
+          }
+          if (!two || have1) {
+            if (two) mma_stage(tbase + BN, a_addr + A_BYTES, b_addr, idesc, kb);
+            mma_commit_lead(lead, smem_u32(&empty_bar[stage]));
+          } else {
+            if (held == 0) {
+              hs0 = stage;
+              hkb0 = kb;
+            }
+            ++held;
+          }
+          if (++stage == STAGES) { stage = 0; phase ^= 1; }
+        }
+        if (!ok) break;
+        if (!have1) {
+          // half 1 unused by this unit, or not yet free: its phase is
+          // waited for every tile, so the two halves' phases stay paired
+          if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&acce_bar[1]), tpar ^ 1, &abort_flag,
+                                                 status, kSiteAccEmpty)))
+            break;
+          tc_fence_after();
+          catch_up();
+        }
+        mma_commit_lead(lead, smem_u32(&accf_bar[0]));
+        tpar ^= 1;
+      }
     }
     // Drain the tensor pipe before TMEM is released.
     mma_commit_lead(lead, smem_u32(&drain_bar));
@@ -337,59 +472,54 @@ __global__ void __launch_bounds__(THREADS, 1)
     uint32_t aphase = 0;
     for (int u = unit0; u < num_units + zero_units; u += unit_step) {
       const bool zero = u >= num_units;   // a pad-only tile: zeros, no accumulator
-      int mt, nt;
-      if (zero)
-        zero_coords(u - num_units, mt, nt);
-      else
-        unit_coords(u, mt, nt);
-      const int m0 = mt * BM, n0 = nt * BN_OUT;
-      const bool rows_in = m0 + q * 32 < M;   // this warp's 32 rows hold some of C
+      int mts[HALVES], nt;
+      if (zero) {
+        zero_coords(u - num_units, mts[0], nt);
+#pragma unroll
+        for (int hf = 1; hf < HALVES; ++hf) mts[hf] = -1;
+      } else {
+        unit_coords(u, mts, nt);
+      }
       if (!zero) {
         bool ok = mbar_wait(smem_u32(&accf_bar[abuf]), aphase, &abort_flag, status, kSiteAccFull);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         tc_fence_after();
       }
-      const uint32_t acc = tbase + lane_off + abuf * BN;
+      const int n0 = nt * BN_OUT;
       const bool seg1 = epi.n1 > 0 && n0 >= epi.n1;     // second output segment
       const int col_off = seg1 ? epi.n1 : 0;              // its first global column
       const CUtensorMap* tcp = seg1 ? &tmC2 : &tmC;
-      // Stage one 32-row x 128-byte chunk of this warp and store it with TMA
-      // (col0 is a global column of C).
-      auto stage_store = [&](const uint32_t (&w)[32], int col0) {
-        // The staging buffer used two chunks ago must have been read by its store.
-        uint8_t* buf = staging + (nchunk & 1) * STAGING_BYTES;
-        if (lane == 0 && nchunk >= 2) bulk_wait_group_read<1>();
-        __syncwarp();
-        // row `lane`, 16-byte unit u lands at unit u ^ (lane % 8) (128-byte swizzle)
-#pragma unroll
-        for (int u = 0; u < 8; ++u)
-          *reinterpret_cast<uint4*>(buf + lane * 128 + ((u ^ (lane & 7)) << 4)) =
-              make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          if (rows_in) tma_store_2d(tcp, smem_u32(buf), col0 - col_off, m0 + q * 32);
-          bulk_commit_group();
+#pragma unroll 1
+      for (int half = 0; half < HALVES; ++half) {
+        // this half's accumulator: buffer abuf of a one-half tile, or the
+        // TMEM columns of half `half` of a two-half tile
+        const int ab = HALVES == 2 ? half : abuf;
+        if (mts[half] < 0) {
+          // a second half past the last M tile: nothing to drain, but its
+          // barrier phase stays paired with the first half's
+          if (!zero) {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&acce_bar[ab]));
+          }
+          continue;
         }
-        ++nchunk;
-      };
-      auto release_acc = [&]() {
-        // last TMEM read of this tile: the accumulator may be reused
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&acce_bar[abuf]));
-      };
-      if (zero) {
-        for (int c = 0; c < BN_OUT / CW; ++c) {
-          const int col0 = n0 + c * CW;
-          if (col0 >= N) break;   // warp-uniform
+        const int mt = mts[half];
+        const int m0 = mt * BM;
+        const bool rows_in = m0 + q * 32 < M;   // this warp's 32 rows hold some of C
+        const uint32_t acc = tbase + lane_off + ab * BN;
+        // Stage one 32-row x 128-byte chunk of this warp and store it with TMA
+        // (col0 is a global column of C).
+        auto stage_store = [&](const uint32_t (&w)[32], int col0) {
+          // The staging buffer used two chunks ago must have been read by its store.
           uint8_t* buf = staging + (nchunk & 1) * STAGING_BYTES;
           if (lane == 0 && nchunk >= 2) bulk_wait_group_read<1>();
           __syncwarp();
+          // row `lane`, 16-byte unit u lands at unit u ^ (lane % 8) (128-byte swizzle)
 #pragma unroll
-          for (int v = 0; v < 8; ++v)
-            *reinterpret_cast<uint4*>(buf + lane * 128 + v * 16) = make_uint4(0u, 0u, 0u, 0u);
+          for (int u = 0; u < 8; ++u)
+            *reinterpret_cast<uint4*>(buf + lane * 128 + ((u ^ (lane & 7)) << 4)) =
+                make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
@@ -397,189 +527,220 @@ __global__ void __launch_bounds__(THREADS, 1)
             bulk_commit_group();
           }
           ++nchunk;
+        };
+        auto release_acc = [&]() {
+          // last TMEM read of this tile: the accumulator may be reused
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&acce_bar[ab]));
+        };
+        if (zero) {
+          for (int c = 0; c < BN_OUT / CW; ++c) {
+            const int col0 = n0 + c * CW;
+            if (col0 >= N) break;   // warp-uniform
+            uint8_t* buf = staging + (nchunk & 1) * STAGING_BYTES;
+            if (lane == 0 && nchunk >= 2) bulk_wait_group_read<1>();
+            __syncwarp();
+#pragma unroll
+            for (int v = 0; v < 8; ++v)
+              *reinterpret_cast<uint4*>(buf + lane * 128 + v * 16) = make_uint4(0u, 0u, 0u, 0u);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              if (rows_in) tma_store_2d(tcp, smem_u32(buf), col0 - col_off, m0 + q * 32);
+              bulk_commit_group();
+            }
+            ++nchunk;
+          }
+          continue;
         }
-        continue;
-      }
-      bool fused = false;
-      if constexpr (EPI == kEpiQkNorm)   // warp-uniform
-        fused = seg1 ? (n0 - col_off) < epi.n_norm2 : n0 < epi.n_norm;
-      if constexpr (EPI == kEpiQkNorm) {
-        if (fused) {
-          constexpr int HALF = DH / 2;
-          constexpr int HEADS = BN / DH;      // head vectors per tile row
-          constexpr int PAIRS = HALF / 64;    // 64-column chunk pairs per head
-          const int row = m0 + q * 32 + lane;
-          const float p = row < M ? static_cast<float>(__ldg(epi.pos + row)) : 0.f;
-          const __nv_bfloat16* gam = seg1 ? epi.gamma2 : epi.gamma;
-          const float sc_seg = seg1 ? epi.scale2 : epi.scale;
-          // d_h = 256 (one head per tile, the short-K 1B shapes where this
-          // epilogue is as long as the main loop): the segment's gamma spread
-          // over the warp, word k of lane l holding the bf16 pair (gamma_j,
-          // gamma_{j + d_h/2}) of j = 32 k + l, fetched with one shuffle per
-          // rotated pair (shuffles and loads share the shared-memory data
-          // path that feeds the tensor core).  d_h = 128 reads gamma from
-          // global memory per use (the shuffles' registers would spill there).
-          constexpr bool G_SHFL = DH == 256;
-          uint32_t gl[G_SHFL ? HALF / 32 : 1];
+        bool fused = false;
+        if constexpr (EPI == kEpiQkNorm)   // warp-uniform
+          fused = seg1 ? (n0 - col_off) < epi.n_norm2 : n0 < epi.n_norm;
+        if constexpr (EPI == kEpiQkNorm) {
+          if (fused) {
+            constexpr int HALF = DH / 2;
+            constexpr int HEADS = BN / DH;      // head vectors per tile row
+            constexpr int PAIRS = HALF / 64;    // 64-column chunk pairs per head
+            const int row = m0 + q * 32 + lane;
+            const float p = row < M ? static_cast<float>(__ldg(epi.pos + row)) : 0.f;
+            const __nv_bfloat16* gam = seg1 ? epi.gamma2 : epi.gamma;
+            const float sc_seg = seg1 ? epi.scale2 : epi.scale;
+            // d_h = 256 (one head per tile, the short-K 1B shapes where this
+            // epilogue is as long as the main loop): the segment's gamma spread
+            // over the warp, word k of lane l holding the bf16 pair (gamma_j,
+            // gamma_{j + d_h/2}) of j = 32 k + l, fetched with one shuffle per
+            // rotated pair (shuffles and loads share the shared-memory data
+            // path that feeds the tensor core).  d_h = 128 reads gamma from
+            // global memory per use (the shuffles' registers would spill there).
+            constexpr bool G_SHFL = DH == 256;
+            uint32_t gl[G_SHFL ? HALF / 32 : 1];
 #pragma unroll
-          for (int k = 0; G_SHFL && k < HALF / 32; ++k) {
-            const uint16_t* gb = reinterpret_cast<const uint16_t*>(gam);
-            gl[k] = static_cast<uint32_t>(__ldg(gb + k * 32 + lane)) |
-                    (static_cast<uint32_t>(__ldg(gb + HALF + k * 32 + lane)) << 16);
-          }
-          float rs[HEADS];   // 1 / rms of each head, times the segment's scale
-#pragma unroll
-          for (int e = 0; e < HEADS; ++e) {
-            float ss = 0.f;
-#pragma unroll
-            for (int k = 0; k < DH / 64; ++k) {
-              uint32_t a0[32], a1[32];
-              tmem_ld32(acc + e * DH + k * 64, a0);
-              tmem_ld32(acc + e * DH + k * 64 + 32, a1);
-              tmem_ld_wait(a0);
-              tmem_ld_wait(a1);
-#pragma unroll
-              for (int t = 0; t < 32; ++t) {
-                ss = fmaf(__uint_as_float(a0[t]), __uint_as_float(a0[t]), ss);
-                ss = fmaf(__uint_as_float(a1[t]), __uint_as_float(a1[t]), ss);
-              }
+            for (int k = 0; G_SHFL && k < HALF / 32; ++k) {
+              const uint16_t* gb = reinterpret_cast<const uint16_t*>(gam);
+              gl[k] = static_cast<uint32_t>(__ldg(gb + k * 32 + lane)) |
+                      (static_cast<uint32_t>(__ldg(gb + HALF + k * 32 + lane)) << 16);
             }
-            rs[e] = rsqrtf(ss * (1.f / DH) + 1e-6f) * sc_seg;
-          }
-          // Each pair of 64-column chunks (first half, partner half) goes to
-          // the two staging buffers: the first-half chunk to buffer 0, the
-          // partner chunk to buffer 1 (nchunk is even here).
-          uint8_t* buf_a = staging;
-          uint8_t* buf_b = staging + STAGING_BYTES;
-          // Blocks of 32 rotated pairs (head e, chunk pair i, 32-column half
-          // h): a runtime loop over the blocks, each block unrolled.  Fully
-          // unrolled, this epilogue is tens of KB of instructions, and
-          // streaming through them every tile evicts the MMA issuer's and the
-          // TMA producer's loops from the instruction caches they share.
-          constexpr int N_BLK = HEADS * PAIRS * 2;
-#pragma unroll 1
-          for (int blk = 0; blk < N_BLK; ++blk) {
-            const int e = blk / (2 * PAIRS), i = (blk >> 1) % PAIRS, h = blk & 1;
-            const int ca = e * (DH / 64) + i, cb = ca + PAIRS;   // first-half, partner chunk
-            const int jb = i * 64 + h * 32;                     // first pair index of the block
-            float rse = rs[0];
+            float rs[HEADS];   // 1 / rms of each head, times the segment's scale
 #pragma unroll
-            for (int k = 1; k < HEADS; ++k)
-              if (e == k) rse = rs[k];
-            uint32_t gw = 0;   // this block's gamma word of each lane
-            if constexpr (G_SHFL) {
+            for (int e = 0; e < HEADS; ++e) {
+              float ss = 0.f;
 #pragma unroll
-              for (int k = 0; k < HALF / 32; ++k)
-                if ((jb >> 5) == k) gw = gl[k];
-            }
-            const float2* fr = epi.freqs.f + jb;
-            uint32_t x1[32], x2[32];
-            tmem_ld32(acc + ca * 64 + h * 32, x1);
-            tmem_ld32(acc + cb * 64 + h * 32, x2);
-            tmem_ld_wait(x1);
-            tmem_ld_wait(x2);
-            if (blk == N_BLK - 1) release_acc();
-            uint32_t wa[16], wb[16];
+              for (int k = 0; k < DH / 64; ++k) {
+                uint32_t a0[32], a1[32];
+                tmem_ld32(acc + e * DH + k * 64, a0);
+                tmem_ld32(acc + e * DH + k * 64 + 32, a1);
+                tmem_ld_wait(a0);
+                tmem_ld_wait(a1);
 #pragma unroll
-            for (int t = 0; t < 32; t += 2) {
-              float o1[2], o2[2];
-#pragma unroll
-              for (int v = 0; v < 2; ++v) {
-                float sn, cs;
-                rope_sincos(p, fr[t + v], sn, cs);
-                float gm1, gm2;   // gamma_j, gamma_{j + d_h/2} of pair j = jb + t + v
-                if constexpr (G_SHFL) {
-                  const uint32_t gp = __shfl_sync(0xffffffffu, gw, t + v);
-                  gm1 = __uint_as_float(gp << 16);
-                  gm2 = __uint_as_float(gp & 0xffff0000u);
-                } else {
-                  gm1 = __bfloat162float(gam[jb + t + v]);
-                  gm2 = __bfloat162float(gam[jb + t + v + HALF]);
+                for (int t = 0; t < 32; ++t) {
+                  ss = fmaf(__uint_as_float(a0[t]), __uint_as_float(a0[t]), ss);
+                  ss = fmaf(__uint_as_float(a1[t]), __uint_as_float(a1[t]), ss);
                 }
-                // x (1 + gamma) as one fused multiply-add
-                const float y1 = fmaf(__uint_as_float(x1[t + v]), gm1, __uint_as_float(x1[t + v]));
-                const float y2 = fmaf(__uint_as_float(x2[t + v]), gm2, __uint_as_float(x2[t + v]));
-                o1[v] = (y1 * cs - y2 * sn) * rse;
-                o2[v] = (y2 * cs + y1 * sn) * rse;
               }
-              wa[t / 2] = pack_half2(o1[0], o1[1]);
-              wb[t / 2] = pack_half2(o2[0], o2[1]);
+              rs[e] = rsqrtf(ss * (1.f / DH) + 1e-6f) * sc_seg;
             }
-            if (h == 0) {
-              // both buffers must have been read by the earlier stores
-              if (lane == 0 && nchunk > 0) bulk_wait_group_read<0>();
-              __syncwarp();
-            }
-            // row `lane`, 16-byte unit u at unit u ^ (lane % 8) (128-byte swizzle)
+            // Each pair of 64-column chunks (first half, partner half) goes to
+            // the two staging buffers: the first-half chunk to buffer 0, the
+            // partner chunk to buffer 1 (nchunk is even here).
+            uint8_t* buf_a = staging;
+            uint8_t* buf_b = staging + STAGING_BYTES;
+            // Blocks of 32 rotated pairs (head e, chunk pair i, 32-column half
+            // h): a runtime loop over the blocks, each block unrolled.  Fully
+            // unrolled, this epilogue is tens of KB of instructions, and
+            // streaming through them every tile evicts the MMA issuer's and the
+            // TMA producer's loops from the instruction caches they share.
+            constexpr int N_BLK = HEADS * PAIRS * 2;
+#pragma unroll 1
+            for (int blk = 0; blk < N_BLK; ++blk) {
+              const int e = blk / (2 * PAIRS), i = (blk >> 1) % PAIRS, h = blk & 1;
+              const int ca = e * (DH / 64) + i, cb = ca + PAIRS;   // first-half, partner chunk
+              const int jb = i * 64 + h * 32;                     // first pair index of the block
+              float rse = rs[0];
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              const int pu = ((4 * h + u) ^ (lane & 7)) << 4;
-              *reinterpret_cast<uint4*>(buf_a + lane * 128 + pu) =
-                  make_uint4(wa[4 * u], wa[4 * u + 1], wa[4 * u + 2], wa[4 * u + 3]);
-              *reinterpret_cast<uint4*>(buf_b + lane * 128 + pu) =
-                  make_uint4(wb[4 * u], wb[4 * u + 1], wb[4 * u + 2], wb[4 * u + 3]);
-            }
-            if (h == 1) {
-              fence_proxy_async_smem();
-              __syncwarp();
-              if (lane == 0) {
-                // one bulk group per buffer: a plain chunk that follows waits
-                // for all but the newest group, i.e. for buffer 0's store
-                if (rows_in) tma_store_2d(tcp, smem_u32(buf_a), n0 - col_off + ca * 64, m0 + q * 32);
-                bulk_commit_group();
-                if (rows_in) tma_store_2d(tcp, smem_u32(buf_b), n0 - col_off + cb * 64, m0 + q * 32);
-                bulk_commit_group();
+              for (int k = 1; k < HEADS; ++k)
+                if (e == k) rse = rs[k];
+              uint32_t gw = 0;   // this block's gamma word of each lane
+              if constexpr (G_SHFL) {
+#pragma unroll
+                for (int k = 0; k < HALF / 32; ++k)
+                  if ((jb >> 5) == k) gw = gl[k];
               }
-              nchunk += 2;
+              const float2* fr = epi.freqs.f + jb;
+              uint32_t x1[32], x2[32];
+              tmem_ld32(acc + ca * 64 + h * 32, x1);
+              tmem_ld32(acc + cb * 64 + h * 32, x2);
+              tmem_ld_wait(x1);
+              tmem_ld_wait(x2);
+              if (blk == N_BLK - 1) release_acc();
+              uint32_t wa[16], wb[16];
+#pragma unroll
+              for (int t = 0; t < 32; t += 2) {
+                float o1[2], o2[2];
+#pragma unroll
+                for (int v = 0; v < 2; ++v) {
+                  float sn, cs;
+                  rope_sincos(p, fr[t + v], sn, cs);
+                  float gm1, gm2;   // gamma_j, gamma_{j + d_h/2} of pair j = jb + t + v
+                  if constexpr (G_SHFL) {
+                    const uint32_t gp = __shfl_sync(0xffffffffu, gw, t + v);
+                    gm1 = __uint_as_float(gp << 16);
+                    gm2 = __uint_as_float(gp & 0xffff0000u);
+                  } else {
+                    gm1 = __bfloat162float(gam[jb + t + v]);
+                    gm2 = __bfloat162float(gam[jb + t + v + HALF]);
+                  }
+                  // x (1 + gamma) as one fused multiply-add
+                  const float y1 = fmaf(__uint_as_float(x1[t + v]), gm1, __uint_as_float(x1[t + v]));
+                  const float y2 = fmaf(__uint_as_float(x2[t + v]), gm2, __uint_as_float(x2[t + v]));
+                  o1[v] = (y1 * cs - y2 * sn) * rse;
+                  o2[v] = (y2 * cs + y1 * sn) * rse;
+                }
+                wa[t / 2] = pack_half2(o1[0], o1[1]);
+                wb[t / 2] = pack_half2(o2[0], o2[1]);
+              }
+              if (h == 0) {
+                // both buffers must have been read by the earlier stores
+                if (lane == 0 && nchunk > 0) bulk_wait_group_read<0>();
+                __syncwarp();
+              }
+              // row `lane`, 16-byte unit u at unit u ^ (lane % 8) (128-byte swizzle)
+#pragma unroll
+              for (int u = 0; u < 4; ++u) {
+                const int pu = ((4 * h + u) ^ (lane & 7)) << 4;
+                *reinterpret_cast<uint4*>(buf_a + lane * 128 + pu) =
+                    make_uint4(wa[4 * u], wa[4 * u + 1], wa[4 * u + 2], wa[4 * u + 3]);
+                *reinterpret_cast<uint4*>(buf_b + lane * 128 + pu) =
+                    make_uint4(wb[4 * u], wb[4 * u + 1], wb[4 * u + 2], wb[4 * u + 3]);
+              }
+              if (h == 1) {
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                  // one bulk group per buffer: a plain chunk that follows waits
+                  // for all but the newest group, i.e. for buffer 0's store
+                  if (rows_in) tma_store_2d(tcp, smem_u32(buf_a), n0 - col_off + ca * 64, m0 + q * 32);
+                  bulk_commit_group();
+                  if (rows_in) tma_store_2d(tcp, smem_u32(buf_b), n0 - col_off + cb * 64, m0 + q * 32);
+                  bulk_commit_group();
+                }
+                nchunk += 2;
+              }
             }
           }
         }
-      }
-      for (int c = 0; !fused && c < BN_OUT / CW; ++c) {
-        const int col0 = n0 + c * CW;
-        if (col0 >= N) break;   // warp-uniform
-        // 128 bytes of this thread's row: 8 x 16-byte units
-        uint32_t w[32];
-        if constexpr (sizeof(OutT) == 4) {
-          tmem_ld32(acc + c * 32, w);
-          tmem_ld_wait(w);
-        } else {
-          uint32_t r0[32], r1[32];
-          tmem_ld32(acc + c * 64, r0);
-          tmem_ld32(acc + c * 64 + 32, r1);
-          if constexpr (GEGLU) {
-            uint32_t u0[32], u1[32];
-            tmem_ld32(acc + BN / 2 + c * 64, u0);
-            tmem_ld32(acc + BN / 2 + c * 64 + 32, u1);
-            tmem_ld_wait(r0);
-            tmem_ld_wait(r1);
-            tmem_ld_wait(u0);
-            tmem_ld_wait(u1);
-#pragma unroll
-            for (int e = 0; e < 16; ++e) {
-              w[e] = pack2<OutT>(gelu_tanh_mul(__uint_as_float(r0[2 * e]), __uint_as_float(u0[2 * e])),
-                                 gelu_tanh_mul(__uint_as_float(r0[2 * e + 1]),
-                                               __uint_as_float(u0[2 * e + 1])));
-              w[16 + e] =
-                  pack2<OutT>(gelu_tanh_mul(__uint_as_float(r1[2 * e]), __uint_as_float(u1[2 * e])),
-                              gelu_tanh_mul(__uint_as_float(r1[2 * e + 1]),
-                                            __uint_as_float(u1[2 * e + 1])));
-            }
+        for (int c = 0; !fused && c < BN_OUT / CW; ++c) {
+          const int col0 = n0 + c * CW;
+          if (col0 >= N) break;   // warp-uniform
+          // 128 bytes of this thread's row: 8 x 16-byte units
+          uint32_t w[32];
+          if constexpr (sizeof(OutT) == 4) {
+            tmem_ld32(acc + c * 32, w);
+            tmem_ld_wait(w);
           } else {
-            tmem_ld_wait(r0);
-            tmem_ld_wait(r1);
+            uint32_t r0[32], r1[32];
+            tmem_ld32(acc + c * 64, r0);
+            tmem_ld32(acc + c * 64 + 32, r1);
+            if constexpr (GEGLU) {
+              uint32_t u0[32], u1[32];
+              tmem_ld32(acc + BN / 2 + c * 64, u0);
+              tmem_ld32(acc + BN / 2 + c * 64 + 32, u1);
+              tmem_ld_wait(r0);
+              tmem_ld_wait(r1);
+              tmem_ld_wait(u0);
+              tmem_ld_wait(u1);
 #pragma unroll
-            for (int e = 0; e < 16; ++e) {
-              w[e] = pack2<OutT>(__uint_as_float(r0[2 * e]), __uint_as_float(r0[2 * e + 1]));
-              w[16 + e] = pack2<OutT>(__uint_as_float(r1[2 * e]), __uint_as_float(r1[2 * e + 1]));
+              for (int e = 0; e < 16; ++e) {
+                w[e] = pack2<OutT>(gelu_tanh_mul(__uint_as_float(r0[2 * e]), __uint_as_float(u0[2 * e])),
+                                   gelu_tanh_mul(__uint_as_float(r0[2 * e + 1]),
+                                                 __uint_as_float(u0[2 * e + 1])));
+                w[16 + e] =
+                    pack2<OutT>(gelu_tanh_mul(__uint_as_float(r1[2 * e]), __uint_as_float(u1[2 * e])),
+                                gelu_tanh_mul(__uint_as_float(r1[2 * e + 1]),
+                                              __uint_as_float(u1[2 * e + 1])));
+              }
+            } else {
+              tmem_ld_wait(r0);
+              tmem_ld_wait(r1);
+#pragma unroll
+              for (int e = 0; e < 16; ++e) {
+                w[e] = pack2<OutT>(__uint_as_float(r0[2 * e]), __uint_as_float(r0[2 * e + 1]));
+                w[16 + e] = pack2<OutT>(__uint_as_float(r1[2 * e]), __uint_as_float(r1[2 * e + 1]));
+              }
             }
           }
+          if (c == BN_OUT / CW - 1 || col0 + CW >= N) release_acc();
+          stage_store(w, col0);
         }
-        if (c == BN_OUT / CW - 1 || col0 + CW >= N) release_acc();
-        stage_store(w, col0);
       }
-      abuf ^= 1;
-      if (abuf == 0) aphase ^= 1;
+      if (!zero) {
+        if (HALVES == 1) {
+          abuf ^= 1;
+          if (abuf == 0) aphase ^= 1;
+        } else {
+          aphase ^= 1;
+        }
+      }
     }
     if (lane == 0) bulk_wait_group_all();
   }
@@ -590,21 +751,55 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
 }
 
-inline int gemm_tiles(int M, int N, int bn_out) {
-  return ((M + BM - 1) / BM) * ((N + bn_out - 1) / bn_out);
+// Rows per tile: 0 chooses (see launch_typed), 128 or 256 forces one.
+std::atomic<int> g_tile_rows{0};
+
+// The launch of one instantiation: grid (one CTA per SM, at most one per
+// unit) and the L2 grouping of M tiles (in units of HALVES 128-row tiles).
+template <int AB_BF16, typename OutT, int EPI, int DH, int HALVES>
+cudaError_t launch_kernel(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
+                          const CUtensorMap& tb2, const CUtensorMap& tc2, int M, int N, int K,
+                          cudaStream_t stream, int* status, int max_ctas, const QkEpi& epi,
+                          const int32_t* pad_lens, int seg_T, int zero_from) {
+  constexpr bool GEGLU = EPI == kEpiGeglu;
+  constexpr uint32_t smem_bytes = Ring<HALVES>::SMEM_BYTES;
+  auto kern = pad_lens != nullptr ? gemm_tn_kernel<AB_BF16, OutT, EPI, DH, true, HALVES>
+                                  : gemm_tn_kernel<AB_BF16, OutT, EPI, DH, false, HALVES>;
+  if (cudaError_t e = prepare_kernel(reinterpret_cast<const void*>(kern), smem_bytes)) return e;
+  const int bn_out = GEGLU ? BN / 2 : BN;
+  const int m_tiles = (M + BM - 1) / BM;
+  const int mu_units = (m_tiles + HALVES - 1) / HALVES;
+  const int units = mu_units * ((N + bn_out - 1) / bn_out);
+  int grid = num_sms();
+  if (max_ctas > 0 && max_ctas < grid) grid = max_ctas;
+  if (units < grid) grid = units;
+  const size_t a_tile_bytes = static_cast<size_t>(BM) * K * 2;
+  const size_t w_bytes = static_cast<size_t>(GEGLU ? 2 * N : N) * K * 2;
+  int group_m = kSmallGroupM;
+  if (w_bytes > kSmallWeightBytes) {
+    const size_t g = kGroupBytes / a_tile_bytes;
+    if (g > static_cast<size_t>(group_m)) group_m = static_cast<int>(g);
+  }
+  group_m = group_m / HALVES > 1 ? group_m / HALVES : 1;
+  if (group_m > mu_units) group_m = mu_units;
+  return launch_pdl(kern, dim3(grid), dim3(THREADS), smem_bytes, stream, ta, tb, tc, tb2, tc2, M,
+                    N, K, group_m, pad_lens, seg_T, zero_from, status, epi);
 }
 
 // C (and, for a split launch, the second segment's C2 with ldc2 and the
 // second weight map tb2; epi.n1 > 0) as 32-row x 128-byte TMA tiles.
+// Plain outputs with K of 512 or more take two-half (256-row) tiles unless
+// the last wave of their units would run too empty (the epilogue of a
+// two-half tile is not hidden behind a main loop, so a short K pays it more
+// often).  GeGLU outputs keep one-half tiles unless forced (their longer
+// epilogue, exposed, cost 4-18% on the 4B and 1B feed-forwards), and the
+// fused prologue always does.
 template <int AB_BF16, typename OutT, int EPI = kEpiPlain, int DH = 0>
 cudaError_t launch_typed(const CUtensorMap& ta, const CUtensorMap& tb, void* C, long ldc, int M,
                          int N, int K, cudaStream_t stream, int* status, int max_ctas,
                          const QkEpi& epi = QkEpi{}, const CUtensorMap* tb2 = nullptr,
                          void* C2 = nullptr, long ldc2 = 0, const int32_t* pad_lens = nullptr,
                          int seg_T = 0, int zero_from = 0) {
-  constexpr bool GEGLU = EPI == kEpiGeglu;
-  auto kern = pad_lens != nullptr ? gemm_tn_kernel<AB_BF16, OutT, EPI, DH, true>
-                                  : gemm_tn_kernel<AB_BF16, OutT, EPI, DH, false>;
   // Output tile map: boxes of 32 rows x 128 bytes, 128-byte swizzle.
   CUtensorMap tc;
   const CUtensorMapDataType cdt = sizeof(OutT) == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
@@ -623,25 +818,28 @@ cudaError_t launch_typed(const CUtensorMap& ta, const CUtensorMap& tb, void* C, 
     if (tb2 == nullptr || C2 == nullptr || !encode_tiled(&tc2, cdt, 2, C2, cdims2, cstr2, cbox))
       return cudaErrorInvalidValue;
   }
-  if (cudaError_t e = prepare_kernel(reinterpret_cast<const void*>(kern), SMEM_BYTES))
-    return e;
-  const int bn_out = GEGLU ? BN / 2 : BN;
-  const int tiles = gemm_tiles(M, N, bn_out);
-  int grid = num_sms();
-  if (max_ctas > 0 && max_ctas < grid) grid = max_ctas;
-  if (tiles < grid) grid = tiles;
-  const size_t a_tile_bytes = static_cast<size_t>(BM) * K * 2;
-  const size_t w_bytes = static_cast<size_t>(GEGLU ? 2 * N : N) * K * 2;
-  const int m_tiles = (M + BM - 1) / BM;
-  int group_m = kSmallGroupM;
-  if (w_bytes > kSmallWeightBytes) {
-    const size_t g = kGroupBytes / a_tile_bytes;
-    if (g > static_cast<size_t>(group_m)) group_m = static_cast<int>(g);
+  const CUtensorMap& tbb = tb2 != nullptr ? *tb2 : tb;
+  if constexpr (EPI != kEpiQkNorm) {
+    const int rows = g_tile_rows.load(std::memory_order_relaxed);
+    bool two = rows == 256;
+    if (rows == 0 && EPI == kEpiPlain && K >= 512) {
+      // A two-half tile does the work of two one-half tiles in ~1/1.12 of
+      // their time (measured, K = 1024-10240); it pays where its waves of
+      // units over the grid do not outnumber that.
+      const int n_tiles = (N + BN - 1) / BN, m_tiles = (M + BM - 1) / BM;
+      int grid = num_sms();
+      if (max_ctas > 0 && max_ctas < grid) grid = max_ctas;
+      const long waves1 = (static_cast<long>(m_tiles) * n_tiles + grid - 1) / grid;
+      const long waves2 = (static_cast<long>((m_tiles + 1) / 2) * n_tiles + grid - 1) / grid;
+      two = waves2 * 200 <= waves1 * 112;
+    }
+    if (two)
+      return launch_kernel<AB_BF16, OutT, EPI, DH, 2>(ta, tb, tc, tbb, tc2, M, N, K, stream,
+                                                      status, max_ctas, epi, pad_lens, seg_T,
+                                                      zero_from);
   }
-  if (group_m > m_tiles) group_m = m_tiles;
-  return launch_pdl(kern, dim3(grid), dim3(THREADS), SMEM_BYTES, stream, ta, tb, tc,
-                    tb2 != nullptr ? *tb2 : tb, tc2, M, N, K, group_m, pad_lens, seg_T, zero_from,
-                    status, epi);
+  return launch_kernel<AB_BF16, OutT, EPI, DH, 1>(ta, tb, tc, tbb, tc2, M, N, K, stream, status,
+                                                  max_ctas, epi, pad_lens, seg_T, zero_from);
 }
 
 bool encode_ab(CUtensorMap& ta, CUtensorMap& tb, const void* A, long lda, const void* W, long ldw,
@@ -659,6 +857,11 @@ bool encode_ab(CUtensorMap& ta, CUtensorMap& tb, const void* A, long lda, const 
 }
 
 }  // namespace
+
+int set_gemm_tile_rows(int rows) {
+  if (rows != 0 && rows != 128 && rows != 256) return -1;
+  return g_tile_rows.exchange(rows);
+}
 
 cudaError_t launch_linear(const void* A, long lda, const void* W, long ldw, void* C, long ldc,
                           int M, int N, int K, int in_dtype, int out_dtype, cudaStream_t stream,

@@ -65,6 +65,10 @@ cudaError_t launch_pdl_cluster(void (*kern)(KArgs...), dim3 grid, dim3 block, si
   return cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
 }
 
+// Rows per tile of the tcgen05 GEMM for later launches: 0 (chosen per
+// launch), 128 or 256; returns the previous value, or -1 for another value.
+int set_gemm_tile_rows(int rows);
+
 // C[M,N] = A[M,K] * W[N,K]^T, operands in in_dtype (bf16|f16), fp32
 // accumulation, C in out_dtype.  M <= kSkinnyMaxRows goes to
 // launch_linear_skinny, everything else to the tcgen05 GEMM.
