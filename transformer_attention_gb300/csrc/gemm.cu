@@ -135,10 +135,17 @@ template <> __device__ __forceinline__ uint32_t pack2<__nv_bfloat16>(float a, fl
 }
 
 // GeGLU epilogue of the feed-forward gating projection ("Full Gemma 3
-// Block", How it works: MLP): z = GELU(g) * u with the tanh-form GELU.
+// Block", How it works: MLP): z = GELU(g) * u with the tanh-form GELU
+// 0.5 g (1 + tanh t), t = sqrt(2/pi) (g + 0.044715 g^3).  Since
+// 0.5 (1 + tanh t) = 1 / (1 + exp(-2 t)), it is evaluated as
+// g u / (1 + exp(-2 t)) with the hardware exponential and division (one
+// approximate exp2 and one reciprocal; relative error ~1e-6, against fp16's
+// 5e-4 of the stored z).  Large negative t gives exp = inf and z = 0, the
+// function's limit.
 __device__ __forceinline__ float gelu_tanh_mul(float g, float u) {
-  const float kC = 0.7978845608028654f;   // sqrt(2 / pi)
-  return 0.5f * g * (1.f + tanhf(kC * fmaf(0.044715f * g, g * g, g))) * u;
+  const float kM2C = -1.5957691216057308f;   // -2 sqrt(2 / pi)
+  const float e = __expf(kM2C * fmaf(0.044715f * g, g * g, g));
+  return __fdividef(g * u, 1.f + e);
 }
 
 // GEGLU = false: C[M,N] = A W^T.  GEGLU = true: W is the [2*N, K] gating
@@ -788,12 +795,13 @@ cudaError_t launch_kernel(const CUtensorMap& ta, const CUtensorMap& tb, const CU
 
 // C (and, for a split launch, the second segment's C2 with ldc2 and the
 // second weight map tb2; epi.n1 > 0) as 32-row x 128-byte TMA tiles.
-// Plain outputs with K of 512 or more take two-half (256-row) tiles unless
-// the last wave of their units would run too empty (the epilogue of a
-// two-half tile is not hidden behind a main loop, so a short K pays it more
-// often).  GeGLU outputs keep one-half tiles unless forced (their longer
-// epilogue, exposed, cost 4-18% on the 4B and 1B feed-forwards), and the
-// fused prologue always does.
+// Plain outputs with K of 512 or more, and GeGLU outputs with K of 2048 or
+// more, take two-half (256-row) tiles unless the last wave of their units
+// would run too empty.  The epilogue of a two-half tile is not hidden behind
+// a main loop, so a short K pays it more often, and GeGLU's is the longer
+// (measured: 256-row GeGLU +2.5% at K = 2560, -3.5% at K = 1152).  The fused
+// prologue, whose epilogue is as long as a short main loop, keeps one-half
+// tiles.
 template <int AB_BF16, typename OutT, int EPI = kEpiPlain, int DH = 0>
 cudaError_t launch_typed(const CUtensorMap& ta, const CUtensorMap& tb, void* C, long ldc, int M,
                          int N, int K, cudaStream_t stream, int* status, int max_ctas,
@@ -822,11 +830,12 @@ cudaError_t launch_typed(const CUtensorMap& ta, const CUtensorMap& tb, void* C, 
   if constexpr (EPI != kEpiQkNorm) {
     const int rows = g_tile_rows.load(std::memory_order_relaxed);
     bool two = rows == 256;
-    if (rows == 0 && EPI == kEpiPlain && K >= 512) {
+    if (rows == 0 && K >= (EPI == kEpiGeglu ? 2048 : 512)) {
       // A two-half tile does the work of two one-half tiles in ~1/1.12 of
       // their time (measured, K = 1024-10240); it pays where its waves of
       // units over the grid do not outnumber that.
-      const int n_tiles = (N + BN - 1) / BN, m_tiles = (M + BM - 1) / BM;
+      const int bn_out = EPI == kEpiGeglu ? BN / 2 : BN;
+      const int n_tiles = (N + bn_out - 1) / bn_out, m_tiles = (M + BM - 1) / BM;
       int grid = num_sms();
       if (max_ctas > 0 && max_ctas < grid) grid = max_ctas;
       const long waves1 = (static_cast<long>(m_tiles) * n_tiles + grid - 1) / grid;
