@@ -591,7 +591,8 @@ __global__ void __launch_bounds__(THREADS, 1)
             float rs[HEADS];   // 1 / rms of each head, times the segment's scale
 #pragma unroll
             for (int e = 0; e < HEADS; ++e) {
-              float ss = 0.f;
+              // sum of squares in packed fp32x2 (four partial sums)
+              float2 sa = make_float2(0.f, 0.f), sb = make_float2(0.f, 0.f);
 #pragma unroll
               for (int k = 0; k < DH / 64; ++k) {
                 uint32_t a0[32], a1[32];
@@ -600,11 +601,14 @@ __global__ void __launch_bounds__(THREADS, 1)
                 tmem_ld_wait(a0);
                 tmem_ld_wait(a1);
 #pragma unroll
-                for (int t = 0; t < 32; ++t) {
-                  ss = fmaf(__uint_as_float(a0[t]), __uint_as_float(a0[t]), ss);
-                  ss = fmaf(__uint_as_float(a1[t]), __uint_as_float(a1[t]), ss);
+                for (int t = 0; t < 32; t += 2) {
+                  const float2 u = make_float2(__uint_as_float(a0[t]), __uint_as_float(a0[t + 1]));
+                  const float2 w = make_float2(__uint_as_float(a1[t]), __uint_as_float(a1[t + 1]));
+                  sa = __ffma2_rn(u, u, sa);
+                  sb = __ffma2_rn(w, w, sb);
                 }
               }
+              const float ss = (sa.x + sa.y) + (sb.x + sb.y);
               rs[e] = rsqrtf(ss * (1.f / DH) + 1e-6f) * sc_seg;
             }
             // Each pair of 64-column chunks (first half, partner half) goes to
@@ -641,30 +645,38 @@ __global__ void __launch_bounds__(THREADS, 1)
               tmem_ld_wait(x2);
               if (blk == N_BLK - 1) release_acc();
               uint32_t wa[16], wb[16];
+              const float2 rs2 = make_float2(rse, rse), nrs2 = make_float2(-rse, -rse);
+              // Two rotated pairs (j, j + 1), j = jb + t, per step in packed
+              // fp32x2 arithmetic.
 #pragma unroll
               for (int t = 0; t < 32; t += 2) {
-                float o1[2], o2[2];
-#pragma unroll
-                for (int v = 0; v < 2; ++v) {
-                  float sn, cs;
-                  rope_sincos(p, fr[t + v], sn, cs);
-                  float gm1, gm2;   // gamma_j, gamma_{j + d_h/2} of pair j = jb + t + v
-                  if constexpr (G_SHFL) {
-                    const uint32_t gp = __shfl_sync(0xffffffffu, gw, t + v);
-                    gm1 = __uint_as_float(gp << 16);
-                    gm2 = __uint_as_float(gp & 0xffff0000u);
-                  } else {
-                    gm1 = __bfloat162float(gam[jb + t + v]);
-                    gm2 = __bfloat162float(gam[jb + t + v + HALF]);
-                  }
-                  // x (1 + gamma) as one fused multiply-add
-                  const float y1 = fmaf(__uint_as_float(x1[t + v]), gm1, __uint_as_float(x1[t + v]));
-                  const float y2 = fmaf(__uint_as_float(x2[t + v]), gm2, __uint_as_float(x2[t + v]));
-                  o1[v] = (y1 * cs - y2 * sn) * rse;
-                  o2[v] = (y2 * cs + y1 * sn) * rse;
+                float2 g1, g2;   // (gamma_j, gamma_{j+1}), their partners at j + d_h/2
+                if constexpr (G_SHFL) {
+                  const uint32_t ga = __shfl_sync(0xffffffffu, gw, t);
+                  const uint32_t gb = __shfl_sync(0xffffffffu, gw, t + 1);
+                  g1 = make_float2(__uint_as_float(ga << 16), __uint_as_float(gb << 16));
+                  g2 = make_float2(__uint_as_float(ga & 0xffff0000u),
+                                   __uint_as_float(gb & 0xffff0000u));
+                } else {
+                  g1 = make_float2(__bfloat162float(gam[jb + t]), __bfloat162float(gam[jb + t + 1]));
+                  g2 = make_float2(__bfloat162float(gam[jb + t + HALF]),
+                                   __bfloat162float(gam[jb + t + 1 + HALF]));
                 }
-                wa[t / 2] = pack_half2(o1[0], o1[1]);
-                wb[t / 2] = pack_half2(o2[0], o2[1]);
+                const float2 xa = make_float2(__uint_as_float(x1[t]), __uint_as_float(x1[t + 1]));
+                const float2 xb = make_float2(__uint_as_float(x2[t]), __uint_as_float(x2[t + 1]));
+                // x (1 + gamma) as one fused multiply-add per lane
+                const float2 y1 = __ffma2_rn(xa, g1, xa);
+                const float2 y2 = __ffma2_rn(xb, g2, xb);
+                float2 sn, cs;
+                rope_sincos2(p, fr[t], fr[t + 1], sn, cs);
+                // (y1 cos - y2 sin) / rms and (y2 cos + y1 sin) / rms, the
+                // scale taken into cos and sin
+                const float2 c = __fmul2_rn(cs, rs2), s = __fmul2_rn(sn, rs2);
+                const float2 ns = __fmul2_rn(sn, nrs2);
+                const float2 o1 = __ffma2_rn(y1, c, __fmul2_rn(y2, ns));
+                const float2 o2 = __ffma2_rn(y2, c, __fmul2_rn(y1, s));
+                wa[t / 2] = pack_half2(o1.x, o1.y);
+                wb[t / 2] = pack_half2(o2.x, o2.y);
               }
               if (h == 0) {
                 // both buffers must have been read by the earlier stores
