@@ -89,11 +89,13 @@ def test_two_half_tiles_small_grid(max_ctas):
 
 
 @pytest.mark.parametrize("pads", [[0, 200, 384, 100], [384, 0, 250], [300, 300, 300]])
-def test_two_half_tiles_pad_only_tiles(pads):
+@pytest.mark.parametrize("max_ctas", [0, 1])
+def test_two_half_tiles_pad_only_tiles(pads, max_ctas):
     """Segments of 384 rows with trailing padding: the computed 128-row tiles
     pair up across segments (a unit's halves may come from different
     segments); pad-only tiles stay unwritten; every computed row equals the
-    128-row tiles' result."""
+    128-row tiles' result.  With one CTA, every unit goes through the same
+    rings in turn."""
     import transformer_attention_gb300 as G3
     T = 384
     M, N, K = T * len(pads), 640, 512
@@ -103,7 +105,7 @@ def test_two_half_tiles_pad_only_tiles(pads):
 
     def run():
         C = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
-        G3.gemma3_linear(A, K, W, K, C, N, M, N, K, G3.GEMMA3_BF16, G3.GEMMA3_F32,
+        G3.gemma3_linear(A, K, W, K, C, N, M, N, K, G3.GEMMA3_BF16, G3.GEMMA3_F32, max_ctas,
                          pad_lens=pl, seg_T=T)
         return C.cpu()
 

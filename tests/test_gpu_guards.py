@@ -69,7 +69,10 @@ LAYERS = [
 
 
 @pytest.mark.parametrize("kw", LAYERS, ids=["local-d256", "global-d128", "pad-tiles-d256"])
-def test_layer_writes_only_out_and_its_workspace(kw):
+@pytest.mark.parametrize("rows", [0, 256])
+def test_layer_writes_only_out_and_its_workspace(kw, rows):
+    """(rows: the projection GEMM's tile height, chosen per call or forced
+    to 256-row tiles for the output projection.)"""
     import transformer_attention_gb300 as G3
     w = WL.small(WL.WORKLOADS["tiny_local"], name="guard", **kw)
     inp = Hh.make_inputs(w)
@@ -77,11 +80,16 @@ def test_layer_writes_only_out_and_its_workspace(kw):
     need = G3.gemma3_attn_workspace_size(w.B, w.T, w.D, w.H, w.H_kv, w.d_h)
     ws = Guarded(need)
     out = Guarded(w.B * w.T * w.D * 2)
-    G3.gemma3_attn_forward((w.B, w.T, w.D, w.H, w.H_kv, w.d_h), dev["x"], dev["segment_pos"],
-                           dev["pad_lens"], dev["Wq"], dev["Wkv"], dev["Wo"], dev["gamma_q"],
-                           dev["gamma_k"], Hh.abi_type(w), w.window, w.rope_base, w.rope_scale,
-                           w.query_scale, out.inner, ws.inner, need)
-    assert G3.gemma3_attn_check_status() == 0
+    prev = G3.gemma3_set_gemm_tile_rows(rows)
+    try:
+        G3.gemma3_attn_forward((w.B, w.T, w.D, w.H, w.H_kv, w.d_h), dev["x"],
+                               dev["segment_pos"], dev["pad_lens"], dev["Wq"], dev["Wkv"],
+                               dev["Wo"], dev["gamma_q"], dev["gamma_k"], Hh.abi_type(w),
+                               w.window, w.rope_base, w.rope_scale, w.query_scale, out.inner,
+                               ws.inner, need)
+        assert G3.gemma3_attn_check_status() == 0
+    finally:
+        G3.gemma3_set_gemm_tile_rows(prev)
     assert ws.guards_intact() and out.guards_intact()
     assert _inputs_unchanged(dev, before)
     # and the result is the layer's
